@@ -1,0 +1,319 @@
+/*
+ * CPU oracle for the batched codec-LM decode step.  TEST INFRASTRUCTURE ONLY:
+ * it is called by the tests, by the smoke check and by the benchmark's CPU
+ * baseline, never by the product path, and it shares no code with the CUDA
+ * library.
+ *
+ * Plain loops, one stream at a time, sums in double.  Values the method keeps
+ * as fp32 (logits, probabilities, Gumbel keys) are rounded to float before a
+ * decision is taken on them, so that an argmax or an accept test is decided in
+ * the precision the kernels use.  Inputs are read as stored (fp32, or bf16 bit
+ * patterns upcast exactly).
+ *
+ * Sources (web pages on streaming codec-LM text-to-speech):
+ *  [OPT]  "Optimizing Streaming Text-to-Speech Models for Sub-50 Millisecond
+ *         Latency": section "Speculative Decoding for Acoustic Tokens"
+ *         (verify_draft_tokens) and section "Dynamic Token-Level Batching"
+ *         (static pool of 16-token KV blocks).
+ *  [TTS]  "TTS (Text-to-Speech) Serving, in depth", section "Token generation
+ *         under a frame budget" (one decode step per frame reads the KV cache).
+ *  [TON]  "TontaubeV1: Streaming Text-to-Speech with Hierarchical Codec
+ *         Modeling and Bounded Context", section 3 (codebooks of 16,384 and
+ *         4,096 entries, boundary token, later stages at temperature zero).
+ *  [SAL]  Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
+ *         1, 2, 3", SC'11: the Philox4x64-10 bijection.
+ *
+ * Readings where the pages are silent (each is also listed in the design
+ * notes): softmax scale 1/sqrt(D); query head h uses KV head h/(Hq/Hkv); the
+ * appended token attends to itself; in a q_len-row verify block row j sees the
+ * prefix and new tokens 0..j; the boundary token is vocab index V-1; equal
+ * keys resolve to the lowest index; the rejection draw samples the clamped
+ * residual by Gumbel-max; with every draft accepted no bonus token is drawn
+ * unless asked for.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_BLOCK 16
+
+/* ------------------------------------------------------------------ inputs */
+
+static double load_elem(const void *base, size_t i, int is_bf16) {
+    if (is_bf16) {
+        uint32_t bits = (uint32_t)((const uint16_t *)base)[i] << 16;
+        float f;
+        memcpy(&f, &bits, sizeof f);
+        return (double)f;
+    }
+    return (double)((const float *)base)[i];
+}
+
+/* ------------------------------------------------------------------ Philox */
+
+/* Philox4x64 with 10 rounds [SAL, section 5]: each round multiplies words 0
+ * and 2 by fixed 64-bit multipliers, keeps the low halves as the new words 3
+ * and 1, and xors the high halves with the other two words and the round key.
+ * The key is bumped by the Weyl constants between rounds. */
+void orc_philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]) {
+    const uint64_t M0 = 0xD2E7470EE14C6C93ULL, M1 = 0xCA5A826395121157ULL;
+    const uint64_t W0 = 0x9E3779B97F4A7C15ULL, W1 = 0xBB67AE8584CAA73BULL;
+    uint64_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+    uint64_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        unsigned __int128 p0 = (unsigned __int128)M0 * x0;
+        unsigned __int128 p1 = (unsigned __int128)M1 * x2;
+        uint64_t hi0 = (uint64_t)(p0 >> 64), lo0 = (uint64_t)p0;
+        uint64_t hi1 = (uint64_t)(p1 >> 64), lo1 = (uint64_t)p1;
+        uint64_t y0 = hi1 ^ x1 ^ k0;
+        uint64_t y1 = lo1;
+        uint64_t y2 = hi0 ^ x3 ^ k1;
+        uint64_t y3 = lo0;
+        x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+        k0 += W0;
+        k1 += W1;
+    }
+    out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+/* Uniform number idx of the stream named by (seed, step, tag, pos).
+ * Key = (seed, step); counter = (idx / 8, tag, pos, 0).  One Philox call gives
+ * four 64-bit words = eight 32-bit halves; half (idx % 8) is used, word
+ * (idx % 8) / 2, low half first.  Its top 23 bits k map to (2k + 1) / 2^24,
+ * which is exact in fp32 and lies strictly inside (0, 1).
+ * Tags: 0 head Gumbel noise, 1 verify accept uniforms, 2 verify residual /
+ * bonus Gumbel noise. */
+float orc_uniform(uint64_t seed, uint64_t step, uint32_t tag, uint32_t pos, uint32_t idx) {
+    const uint64_t ctr[4] = {idx / 8u, tag, pos, 0};
+    const uint64_t key[2] = {seed, step};
+    uint64_t w[4];
+    orc_philox4x64_10(ctr, key, w);
+    const uint32_t lane = idx % 8u;
+    const uint64_t word = w[lane / 2u];
+    const uint32_t half = (lane & 1u) ? (uint32_t)(word >> 32) : (uint32_t)word;
+    const uint32_t k = half >> 9;
+    return (float)(2u * k + 1u) * 0x1.0p-24f;
+}
+
+/* Standard Gumbel noise G = -log(-log u), in fp32. */
+float orc_gumbel(uint64_t seed, uint64_t step, uint32_t tag, uint32_t pos, uint32_t idx) {
+    const float u = orc_uniform(seed, step, tag, pos, idx);
+    return -logf(-logf(u));
+}
+
+/* ------------------------------------------------------------------ append */
+
+/* [OPT, "Dynamic Token-Level Batching"]: the KV cache is a static pool of
+ * 16-token blocks; a stream's logical token s lives in physical block
+ * table[b][s / 16], slot s % 16.  Pool layout [num_blocks][Hkv][16][D].
+ * New token j of stream b goes to logical slot ctx_before[b] + j.
+ * Returns 0, or -1 if a slot falls outside the table or the pool. */
+int orc_kv_append(int num_blocks, int Hkv, int D, int elem_bytes, void *k_pool, void *v_pool,
+                  const int32_t *block_table, int max_blocks, const int32_t *ctx_before,
+                  int B, int q_len, const void *k_new, const void *v_new) {
+    const size_t row = (size_t)D * (size_t)elem_bytes;
+    for (int b = 0; b < B; ++b) {
+        for (int j = 0; j < q_len; ++j) {
+            const int s = ctx_before[b] + j;
+            if (s < 0 || s / ORC_BLOCK >= max_blocks) return -1;
+            const int blk = block_table[(size_t)b * max_blocks + s / ORC_BLOCK];
+            if (blk < 0 || blk >= num_blocks) return -1;
+            for (int g = 0; g < Hkv; ++g) {
+                const size_t dst = (((size_t)blk * Hkv + g) * ORC_BLOCK + s % ORC_BLOCK) * row;
+                const size_t src = (((size_t)b * q_len + j) * Hkv + g) * row;
+                memcpy((char *)k_pool + dst, (const char *)k_new + src, row);
+                memcpy((char *)v_pool + dst, (const char *)v_new + src, row);
+            }
+        }
+    }
+    return 0;
+}
+
+/* --------------------------------------------------------------- attention */
+
+/* One decode step's attention [TTS, "Token generation under a frame budget"]:
+ * every query row of stream b attends over that stream's cached keys/values
+ * (gathered through the block table), softmax(scale * q.k) weighted sum of v.
+ * ctx_lens[b] counts tokens after the append.  Query row j of a q_len-row
+ * block sees tokens t < ctx_lens[b] - q_len + j + 1 when causal, all
+ * ctx_lens[b] tokens otherwise.  GQA: query head h reads KV head
+ * h / (Hq / Hkv).  Output out[B][q_len][Hq][D] in double.
+ * Returns 0, or -1 on an invalid block id or context length. */
+int orc_decode_attn(int num_blocks, int Hkv, int D, int is_bf16,
+                    const void *k_pool, const void *v_pool,
+                    const int32_t *block_table, int max_blocks, const int32_t *ctx_lens,
+                    int B, int q_len, int Hq, double scale, int causal,
+                    const void *q, double *out) {
+    const int group = Hq / Hkv;
+    double *s = (double *)malloc(sizeof(double) * (size_t)max_blocks * ORC_BLOCK);
+    if (!s) return -1;
+    for (int b = 0; b < B; ++b) {
+        const int L = ctx_lens[b];
+        if (L < q_len || L > max_blocks * ORC_BLOCK) { free(s); return -1; }
+        for (int j = 0; j < q_len; ++j) {
+            const int limit = causal ? L - q_len + j + 1 : L;
+            for (int h = 0; h < Hq; ++h) {
+                const int g = h / group;
+                const size_t qoff = (((size_t)b * q_len + j) * Hq + h) * D;
+                double m = -INFINITY;
+                for (int t = 0; t < limit; ++t) {
+                    const int blk = block_table[(size_t)b * max_blocks + t / ORC_BLOCK];
+                    if (blk < 0 || blk >= num_blocks) { free(s); return -1; }
+                    const size_t koff = (((size_t)blk * Hkv + g) * ORC_BLOCK + t % ORC_BLOCK) * D;
+                    double dot = 0.0;
+                    for (int d = 0; d < D; ++d)
+                        dot += load_elem(q, qoff + d, is_bf16) * load_elem(k_pool, koff + d, is_bf16);
+                    s[t] = scale * dot;
+                    if (s[t] > m) m = s[t];
+                }
+                double denom = 0.0;
+                for (int t = 0; t < limit; ++t) {
+                    s[t] = exp(s[t] - m);
+                    denom += s[t];
+                }
+                double *o = out + qoff;
+                for (int d = 0; d < D; ++d) o[d] = 0.0;
+                for (int t = 0; t < limit; ++t) {
+                    const int blk = block_table[(size_t)b * max_blocks + t / ORC_BLOCK];
+                    const size_t voff = (((size_t)blk * Hkv + g) * ORC_BLOCK + t % ORC_BLOCK) * D;
+                    const double p = s[t] / denom;
+                    for (int d = 0; d < D; ++d) o[d] += p * load_elem(v_pool, voff + d, is_bf16);
+                }
+            }
+        }
+    }
+    free(s);
+    return 0;
+}
+
+/* -------------------------------------------------------------------- head */
+
+/* Codebook head and token choice [TON, section 3]: logits[r][v] = h[r] . W[v]
+ * over the stage vocabulary (V entries, the last one the boundary token).
+ * mode 0 (temperature zero): id = argmax_v logits.  mode 1: id =
+ * argmax_v (logits / T + G_v) with G_v Gumbel noise (tag 0, pos 0, idx v), a
+ * draw from softmax(logits / T).  eos_allowed[r] == 0 removes v = V-1.
+ * Equal keys resolve to the lowest index.  best / second receive the top two
+ * keys (second = -inf when V == 1); logits_out (nullable) receives the fp32
+ * logits [R][V].  Returns 0, or -1 on bad arguments. */
+int orc_head_select(const void *h, const void *W, int is_bf16, int R, int H, int V, int mode,
+                    float T, const uint64_t *seed, const uint64_t *step,
+                    const uint8_t *eos_allowed, int32_t *ids, float *best, float *second,
+                    float *logits_out) {
+    if (R < 0 || H <= 0 || V <= 0 || (mode != 0 && mode != 1)) return -1;
+    if (mode == 1 && !(T > 0.0f)) return -1;
+    for (int r = 0; r < R; ++r) {
+        const int vmax = (eos_allowed && !eos_allowed[r]) ? V - 1 : V;
+        int arg = -1;
+        float top = -INFINITY, next = -INFINITY;
+        for (int v = 0; v < V; ++v) {
+            double acc = 0.0;
+            for (int k = 0; k < H; ++k)
+                acc += load_elem(h, (size_t)r * H + k, is_bf16) * load_elem(W, (size_t)v * H + k, is_bf16);
+            const float logit = (float)acc;
+            if (logits_out) logits_out[(size_t)r * V + v] = logit;
+            if (v >= vmax) continue;
+            float key = logit;
+            if (mode == 1) key = logit / T + orc_gumbel(seed[r], step[r], 0u, 0u, (uint32_t)v);
+            if (arg < 0 || key > top) {
+                next = top;
+                top = key;
+                arg = v;
+            } else if (key > next) {
+                next = key;
+            }
+        }
+        ids[r] = arg;
+        if (best) best[r] = top;
+        if (second) second[r] = next;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ verify */
+
+/* softmax(x / T)[v] for one row, in double, rounded to float. */
+static void row_probs(const float *x, int V, float T, float *p) {
+    double m = -INFINITY;
+    for (int v = 0; v < V; ++v)
+        if ((double)x[v] > m) m = (double)x[v];
+    double z = 0.0;
+    for (int v = 0; v < V; ++v) z += exp(((double)x[v] - m) / (double)T);
+    for (int v = 0; v < V; ++v) p[v] = (float)(exp(((double)x[v] - m) / (double)T) / z);
+}
+
+/* Speculative verification [OPT, "Speculative Decoding for Acoustic Tokens"],
+ * for every stream b (the page's function handles batch row 0 only):
+ * target probabilities p_t = softmax(target_logits[b][i] / T); for draft i in
+ * order with token d and draft probability p_d = draft_probs[b][i][d]:
+ * p_d == 0 rejects; otherwise the draft is accepted when u_i < p_t[d] / p_d
+ * (u_i the Philox uniform tag 1, pos 0, idx i).  At the first rejection the
+ * replacement token is drawn from the clamped residual max(p_t - p_d, 0),
+ * normalised (Gumbel-max over log of the residual, tag 2, pos i, idx v; if the
+ * residual is zero everywhere, from p_t itself) and verification stops.  If
+ * every draft is accepted next_token = -1, or with flags & 1 a bonus token is
+ * drawn from softmax(target_logits[b][K] / T) (tag 2, pos K).
+ * gap_accept[b]: min |p_t/p_d - u| over the tests made (inf if none);
+ * gap_resid[b]: gap between the two largest keys of the final draw (inf if
+ * none).  Returns 0, or -1 on a draft token outside [0, V). */
+int orc_spec_verify(const float *target_logits, const float *draft_probs,
+                    const int32_t *draft_tokens, int B, int K, int V, float T,
+                    const uint64_t *seed, const uint64_t *step, int flags,
+                    int32_t *n_accepted, int32_t *next_token,
+                    float *gap_accept, float *gap_resid) {
+    float *pt = (float *)malloc(sizeof(float) * (size_t)V);
+    if (!pt) return -1;
+    for (int b = 0; b < B; ++b) {
+        int acc = 0, next = -1;
+        float gacc = INFINITY, gres = INFINITY;
+        int rejected = 0;
+        for (int i = 0; i < K; ++i) {
+            const int d = draft_tokens[(size_t)b * K + i];
+            if (d < 0 || d >= V) { free(pt); return -1; }
+            const float *tl = target_logits + ((size_t)b * (K + 1) + i) * V;
+            const float *dp = draft_probs + ((size_t)b * K + i) * V;
+            row_probs(tl, V, T, pt);
+            int accepted = 0;
+            if (dp[d] > 0.0f) {
+                const float ratio = pt[d] / dp[d];
+                const float u = orc_uniform(seed[b], step[b], 1u, 0u, (uint32_t)i);
+                const float gap = fabsf(ratio - u);
+                if (gap < gacc) gacc = gap;
+                accepted = u < ratio;
+            }
+            if (accepted) { ++acc; continue; }
+            /* rejection: draw from the clamped residual */
+            int any = 0;
+            for (int v = 0; v < V; ++v)
+                if (pt[v] - dp[v] > 0.0f) { any = 1; break; }
+            float top = -INFINITY, sec = -INFINITY;
+            for (int v = 0; v < V; ++v) {
+                const float r = any ? fmaxf(pt[v] - dp[v], 0.0f) : pt[v];
+                if (!(r > 0.0f)) continue;
+                const float key = logf(r) + orc_gumbel(seed[b], step[b], 2u, (uint32_t)i, (uint32_t)v);
+                if (next < 0 || key > top) { sec = top; top = key; next = v; }
+                else if (key > sec) sec = key;
+            }
+            gres = top - sec;
+            rejected = 1;
+            break;
+        }
+        if (!rejected && (flags & 1)) {
+            const float *tl = target_logits + ((size_t)b * (K + 1) + K) * V;
+            float top = -INFINITY, sec = -INFINITY;
+            for (int v = 0; v < V; ++v) {
+                const float key = tl[v] / T + orc_gumbel(seed[b], step[b], 2u, (uint32_t)K, (uint32_t)v);
+                if (next < 0 || key > top) { sec = top; top = key; next = v; }
+                else if (key > sec) sec = key;
+            }
+            gres = top - sec;
+        }
+        n_accepted[b] = acc;
+        next_token[b] = next;
+        if (gap_accept) gap_accept[b] = gacc;
+        if (gap_resid) gap_resid[b] = gres;
+    }
+    free(pt);
+    return 0;
+}

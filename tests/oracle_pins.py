@@ -1,0 +1,418 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each `check_*` takes an `oracle.Oracle` and raises AssertionError when the
+oracle disagrees with a closed form, a library routine (numpy's Philox4x64-10,
+numpy matmul, torch's scaled_dot_product_attention, scipy's distributions), an
+invariance of the method, or a distributional theorem.  The pages print no
+numeric worked example for this path, so these are the pins.
+
+`tests/test_oracle_pins.py` runs every check on the real oracle;
+`tests/test_oracle_mutants.py` plants plausible mistakes in copies of the
+oracle source and requires each mistake to fail at least one check.
+"""
+from __future__ import annotations
+
+import math
+import sys
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parents[1]
+if str(ROOT) not in sys.path:
+    sys.path.insert(0, str(ROOT))
+
+import workloads as wl  # noqa: E402
+
+EULER_GAMMA = 0.5772156649015329
+U64 = 1 << 64
+
+
+# ------------------------------------------------------------------ helpers
+
+def _numpy_philox_block(ctr, key):
+    """The four 64-bit words numpy's Philox4x64-10 produces for counter `ctr`.
+
+    numpy advances its 256-bit counter before each block, so its state is set
+    to ctr - 1 (with borrow)."""
+    c = [int(x) for x in ctr]
+    value = sum(x << (64 * i) for i, x in enumerate(c)) - 1
+    value %= 1 << 256
+    state = [(value >> (64 * i)) & (U64 - 1) for i in range(4)]
+    bg = np.random.Philox(key=np.array(key, dtype=np.uint64), counter=np.array(state, dtype=np.uint64))
+    return [int(x) for x in bg.random_raw(4)]
+
+
+def _chi2_p(observed, probs):
+    from scipy.stats import chisquare
+    observed = np.asarray(observed, dtype=np.float64)
+    expected = np.asarray(probs, dtype=np.float64) * observed.sum()
+    keep = expected > 0
+    assert observed[~keep].sum() == 0, "mass on a zero-probability outcome"
+    return chisquare(observed[keep], expected[keep]).pvalue
+
+
+def _softmax64(x, T=1.0):
+    x = np.asarray(x, dtype=np.float64) / T
+    e = np.exp(x - x.max(axis=-1, keepdims=True))
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def attn_case(seed, B, Hq, Hkv, D, q_len, ctx_lens, dtype="f32", permute=False):
+    """Pools holding every context token (including this step's), q, table."""
+    rng = np.random.default_rng(seed)
+    L = np.asarray(ctx_lens, dtype=np.int32)
+    max_blocks = int(-(-L.max() // wl.BLOCK))
+    num_blocks, table = wl.layout_blocks(L, max_blocks, spare=2, permute=permute, rng=rng)
+    kp = wl.fill_pool(num_blocks, Hkv, D, dtype, table, L, rng)
+    vp = wl.fill_pool(num_blocks, Hkv, D, dtype, table, L, rng)
+    q = wl._store(rng.standard_normal((B, q_len, Hq, D), dtype=np.float32), dtype)
+    return dict(k_pool=kp, v_pool=vp, block_table=table, ctx_lens=L, q=q)
+
+
+def gather(pool, table, b, L, dtype):
+    """Logical [L][Hkv][D] float64 view of stream b's cache."""
+    t = np.arange(L)
+    blocks = table[b, t // wl.BLOCK]
+    return wl.to_f32(pool[blocks, :, t % wl.BLOCK, :], dtype).astype(np.float64)
+
+
+# ------------------------------------------------------------------- Philox
+
+def check_philox_matches_numpy(o):
+    keys = [(1, 2), (0, 0), (U64 - 1, 12345), (7919 * 4 + 17, 3)]
+    ctrs = [(1, 0, 0, 0), (0, 0, 0, 0), (5, 1, 0, 0), (U64 - 1, 2, 3, 0), (123456, 0, 4, 0),
+            (9, 1, 2, 3)]
+    for key in keys:
+        for ctr in ctrs:
+            got = [int(x) for x in o.philox(ctr, key)]
+            want = _numpy_philox_block(ctr, key)
+            assert got == want, f"Philox4x64-10 mismatch at ctr={ctr} key={key}"
+
+
+def check_uniform_words(o):
+    """Uniform idx takes half (idx % 8) of the block at counter (idx // 8, tag, pos, 0),
+    low half first, and maps its top 23 bits k to (2k + 1) / 2^24."""
+    for (seed, step, tag, pos) in [(3, 0, 0, 0), (99, 7, 1, 0), (5, 5, 2, 3)]:
+        for idx in [0, 1, 2, 5, 7, 8, 13, 4096, 16384]:
+            words = _numpy_philox_block((idx // 8, tag, pos, 0), (seed, step))
+            w = words[(idx % 8) // 2]
+            half = (w >> 32) if idx % 2 else (w & 0xFFFFFFFF)
+            want = (2 * (half >> 9) + 1) / 2.0 ** 24
+            got = o.uniform(seed, step, tag, pos, idx)
+            assert got == want, f"uniform({seed},{step},{tag},{pos},{idx}) = {got}, want {want}"
+            assert 0.0 < got < 1.0
+
+
+def check_gumbel_distribution(o):
+    from scipy.stats import kstest
+    g = np.array([o.gumbel(11, 3, 0, 0, i) for i in range(20000)])
+    assert abs(g.mean() - EULER_GAMMA) < 0.03, g.mean()
+    assert abs(g.var() - math.pi ** 2 / 6) < 0.08, g.var()
+    assert kstest(g, "gumbel_r").pvalue > 1e-4
+
+
+# --------------------------------------------------------------- attention
+
+def check_attn_matches_sdpa(o):
+    """torch's scaled_dot_product_attention on the gathered cache (float64)."""
+    import torch
+    import torch.nn.functional as F
+    for (Hq, Hkv, D, q_len, causal, L, dtype, seed) in [
+            (4, 2, 64, 1, False, [17, 1, 40], "f32", 1),
+            (8, 2, 32, 3, True, [3, 33, 20], "bf16", 2),
+            (6, 6, 16, 5, True, [5, 16, 48], "f32", 3),
+            (4, 1, 16, 2, False, [9, 31], "bf16", 4)]:
+        c = attn_case(seed, len(L), Hq, Hkv, D, q_len, L, dtype, permute=True)
+        scale = 0.7 / math.sqrt(D)
+        out = o.decode_attn(c["k_pool"], c["v_pool"], c["block_table"], c["ctx_lens"], c["q"],
+                            scale, causal)
+        g = Hq // Hkv
+        for b, Lb in enumerate(L):
+            k = torch.from_numpy(gather(c["k_pool"], c["block_table"], b, Lb, dtype))
+            v = torch.from_numpy(gather(c["v_pool"], c["block_table"], b, Lb, dtype))
+            k = k.permute(1, 0, 2).repeat_interleave(g, dim=0)
+            v = v.permute(1, 0, 2).repeat_interleave(g, dim=0)
+            q = torch.from_numpy(wl.to_f32(c["q"][b], dtype).astype(np.float64)).permute(1, 0, 2)
+            mask = None
+            if causal:
+                t = torch.arange(Lb)[None, :]
+                j = torch.arange(q_len)[:, None]
+                mask = t < (Lb - q_len + j + 1)
+            ref = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=scale)
+            got = torch.from_numpy(out[b]).permute(1, 0, 2)
+            err = (got - ref).abs().max().item()
+            assert err < 1e-10, f"attention vs SDPA: {err}"
+
+
+def check_attn_constant_keys(o):
+    """Equal scores give the mean of the visible values."""
+    for (q_len, causal, L) in [(1, False, [1, 16, 37]), (5, True, [5, 21, 64])]:
+        c = attn_case(7, len(L), 4, 2, 64, q_len, L)
+        kp = c["k_pool"]
+        kp[:] = np.float32(0.25)
+        out = o.decode_attn(kp, c["v_pool"], c["block_table"], c["ctx_lens"], c["q"], 0.125, causal)
+        for b, Lb in enumerate(L):
+            v = gather(c["v_pool"], c["block_table"], b, Lb, "f32")
+            for j in range(q_len):
+                lim = Lb - q_len + j + 1 if causal else Lb
+                for h in range(4):
+                    want = v[:lim, h // 2, :].mean(axis=0)
+                    assert np.allclose(out[b, j, h], want, atol=1e-12), "constant keys"
+
+
+def check_attn_dominant_score(o):
+    """One key aligned with the query and scaled up takes all the weight."""
+    L = [30, 45]
+    c = attn_case(8, 2, 2, 1, 16, 1, L)
+    kp, table, q = c["k_pool"], c["block_table"], c["q"]
+    picks = [3, 44]
+    for b, t in enumerate(picks):
+        kp[table[b, t // 16], 0, t % 16, :] = 400.0 * q[b, 0, 0, :]
+        q[b, 0, 1, :] = q[b, 0, 0, :]
+    out = o.decode_attn(kp, c["v_pool"], table, c["ctx_lens"], q, 1.0, False)
+    for b, t in enumerate(picks):
+        v = gather(c["v_pool"], table, b, L[b], "f32")[t, 0]
+        for h in range(2):
+            assert np.allclose(out[b, 0, h], v, atol=1e-9), "dominant score"
+
+
+def check_attn_single_token(o):
+    c = attn_case(9, 3, 4, 4, 32, 1, [1, 1, 1])
+    out = o.decode_attn(c["k_pool"], c["v_pool"], c["block_table"], c["ctx_lens"], c["q"], 0.3)
+    for b in range(3):
+        v = gather(c["v_pool"], c["block_table"], b, 1, "f32")[0]
+        assert np.array_equal(out[b, 0], v), "context of one token returns its value"
+
+
+def check_attn_block_permutation(o):
+    """Where blocks sit in the pool does not change the result."""
+    L = [40, 7, 64]
+    c = attn_case(10, 3, 4, 2, 64, 1, L, "bf16")
+    nb = c["k_pool"].shape[0]
+    perm = np.random.default_rng(1).permutation(nb)   # new position of each block
+    kp2 = np.empty_like(c["k_pool"])
+    vp2 = np.empty_like(c["v_pool"])
+    kp2[perm] = c["k_pool"]
+    vp2[perm] = c["v_pool"]
+    t2 = np.where(c["block_table"] >= 0, perm[c["block_table"]], -1).astype(np.int32)
+    a = o.decode_attn(c["k_pool"], c["v_pool"], c["block_table"], c["ctx_lens"], c["q"], 0.125)
+    b = o.decode_attn(kp2, vp2, t2, c["ctx_lens"], c["q"], 0.125)
+    assert np.array_equal(a, b), "block permutation changed the output"
+
+
+def check_attn_verify_rows(o):
+    """Row j of a causal q_len-row block equals a single-row step on the first
+    ctx - q_len + j + 1 tokens."""
+    L = [9, 33]
+    q_len = 5
+    c = attn_case(11, 2, 4, 2, 64, q_len, L, "bf16")
+    full = o.decode_attn(c["k_pool"], c["v_pool"], c["block_table"], c["ctx_lens"], c["q"],
+                         0.125, True)
+    for j in range(q_len):
+        Lj = np.array([x - q_len + j + 1 for x in L], dtype=np.int32)
+        one = o.decode_attn(c["k_pool"], c["v_pool"], c["block_table"], Lj,
+                            np.ascontiguousarray(c["q"][:, j:j + 1]), 0.125, False)
+        assert np.allclose(full[:, j], one[:, 0], atol=1e-13), f"verify row {j}"
+
+
+def check_kv_append_roundtrip(o):
+    """Appended rows read back at their logical slots; every other slot is untouched."""
+    w = wl.custom(1, B=3, q_len=5, ctx_lo=5, ctx_hi=40, permute_table=True, dtype="bf16")
+    inp = wl.make_inputs(w, seed=5, with_head=False, with_verify=False)
+    kp, vp = o.kv_append(inp["k_pool"], inp["v_pool"], inp["block_table"], inp["ctx_before"],
+                         inp["k_new"], inp["v_new"])
+    table = inp["block_table"]
+    touched = np.zeros(kp.shape[0] * 16, dtype=bool)
+    for b in range(w.B):
+        for j in range(w.q_len):
+            s = int(inp["ctx_before"][b]) + j
+            blk = table[b, s // 16]
+            assert np.array_equal(kp[blk, :, s % 16], inp["k_new"][b, j])
+            assert np.array_equal(vp[blk, :, s % 16], inp["v_new"][b, j])
+            touched[blk * 16 + s % 16] = True
+    flat = lambda p: p.transpose(0, 2, 1, 3).reshape(kp.shape[0] * 16, -1)  # noqa: E731
+    assert np.array_equal(flat(kp)[~touched], flat(inp["k_pool"])[~touched])
+    assert np.array_equal(flat(vp)[~touched], flat(inp["v_pool"])[~touched])
+
+
+# -------------------------------------------------------------------- head
+
+def check_head_logits_match_matmul(o):
+    rng = np.random.default_rng(12)
+    for dtype in ("f32", "bf16"):
+        h = wl._store(rng.standard_normal((5, 96), dtype=np.float32), dtype)
+        W = wl._store(0.05 * rng.standard_normal((37, 96), dtype=np.float32), dtype)
+        r = o.head_select(h, W, want_logits=True)
+        ref = (wl.to_f32(h, dtype).astype(np.float64) @ wl.to_f32(W, dtype).astype(np.float64).T)
+        assert np.allclose(r["logits"], ref.astype(np.float32), rtol=1e-6, atol=1e-7), "h W^T"
+        assert np.array_equal(r["ids"], ref.argmax(axis=1)), "argmax of the logits"
+
+
+def check_head_one_hot(o):
+    """A one-hot hidden state picks one column of W, exactly."""
+    rng = np.random.default_rng(13)
+    W = rng.standard_normal((50, 8), dtype=np.float32)
+    h = np.zeros((8, 8), dtype=np.float32)
+    h[np.arange(8), np.arange(8)] = 1.0
+    r = o.head_select(h, W, want_logits=True)
+    assert np.array_equal(r["logits"], W.T), "one-hot rows select columns of W"
+
+
+def check_head_constructed_winner(o):
+    rng = np.random.default_rng(14)
+    h = rng.standard_normal((6, 64), dtype=np.float32)
+    W = 0.01 * rng.standard_normal((300, 64), dtype=np.float32)
+    winners = [0, 17, 299, 150, 42, 298]
+    for r, v in enumerate(winners):
+        W[v] = 0.5 * h[r]
+    got = o.head_select(h, W)["ids"]
+    assert list(got) == winners, "constructed winner"
+
+
+def check_head_ties_and_eos(o):
+    V = 9
+    W = np.ones((V, 4), dtype=np.float32)
+    h = np.ones((3, 4), dtype=np.float32)
+    r = o.head_select(h, W, eos_allowed=np.array([1, 0, 1], dtype=np.uint8))
+    assert list(r["ids"]) == [0, 0, 0], "equal logits resolve to the lowest index"
+    assert list(r["second"] - r["best"]) == [0, 0, 0]
+    W2 = np.zeros((V, 4), dtype=np.float32)
+    W2[V - 1] = 1.0
+    W2[3] = 0.5
+    r = o.head_select(h, W2, eos_allowed=np.array([1, 0, 1], dtype=np.uint8))
+    assert list(r["ids"]) == [V - 1, 3, V - 1], "eos mask removes only the boundary token"
+
+
+def _gumbel_freq(o, logits, T, rows, seed0=1000, step=0):
+    logits = np.asarray(logits, dtype=np.float32)
+    h = np.ones((rows, 1), dtype=np.float32)
+    W = logits[:, None].copy()
+    seed = np.arange(seed0, seed0 + rows, dtype=np.uint64)
+    stp = np.full(rows, step, dtype=np.uint64)
+    ids = o.head_select(h, W, mode="gumbel", T=T, seed=seed, step=stp)["ids"]
+    return np.bincount(ids, minlength=len(logits))
+
+
+def check_head_gumbel_is_softmax_draw(o):
+    logits = [0.0, 0.9, 1.4, -0.6, 0.3]
+    for T, step in [(0.7, 0), (1.6, 5)]:
+        counts = _gumbel_freq(o, logits, T, 20000, step=step)
+        p = _chi2_p(counts, _softmax64(logits, T))
+        assert p > 1e-4, f"Gumbel draws do not follow softmax(logits/T) at T={T}: p={p}"
+
+
+def check_head_gumbel_low_temperature(o):
+    counts = _gumbel_freq(o, [0.1, 0.5, 0.45, -1.0], 1e-4, 500)
+    assert counts[1] == 500, "T -> 0 reduces to argmax"
+
+
+# ------------------------------------------------------------------ verify
+
+def _verify_one(o, tl_rows, dp_rows, tokens, seeds, T=0.7, bonus=False):
+    """Run the oracle over many independent streams that share logits."""
+    B = len(seeds)
+    K = len(dp_rows)
+    tl = np.broadcast_to(np.asarray(tl_rows, dtype=np.float32), (B, K + 1, len(tl_rows[0])))
+    dp = np.broadcast_to(np.asarray(dp_rows, dtype=np.float32), (B, K, len(tl_rows[0])))
+    seed = np.asarray(seeds, dtype=np.uint64)
+    return o.spec_verify(np.ascontiguousarray(tl), np.ascontiguousarray(dp),
+                         np.ascontiguousarray(tokens, dtype=np.int32), T, seed,
+                         np.zeros(B, dtype=np.uint64), bonus=bonus)
+
+
+def check_verify_matching_draft_accepts_all(o):
+    tl = np.random.default_rng(15).standard_normal((5, 33)).astype(np.float32)
+    T = 0.7
+    dp = _softmax64(tl[:4], T).astype(np.float32)
+    tokens = np.tile(np.array([3, 0, 32, 7], dtype=np.int32), (50, 1))
+    r = _verify_one(o, tl, dp, tokens, range(50), T)
+    assert (r["n_accepted"] == 4).all() and (r["next_token"] == -1).all(), "p_d == p_t accepts all"
+
+
+def check_verify_zero_target_rejects(o):
+    rng = np.random.default_rng(16)
+    tl = rng.standard_normal((5, 12)).astype(np.float32)
+    tl[2, 6] = -1e30                      # p_t = 0 at draft 2's token
+    dp = _softmax64(tl[:4], 0.7).astype(np.float32)
+    dp[2] = _softmax64(rng.standard_normal(12))
+    tokens = np.tile(np.array([1, 4, 6, 2], dtype=np.int32), (40, 1))
+    r = _verify_one(o, tl, dp, tokens, range(40))
+    assert (r["n_accepted"] == 2).all(), "a token the target gives zero mass is rejected"
+    assert (r["next_token"] != 6).all() and (r["next_token"] >= 0).all()
+
+
+def check_verify_zero_draft_rejects(o):
+    tl = np.zeros((2, 6), dtype=np.float32)
+    dp = np.array([[0.0, 0.2, 0.2, 0.2, 0.2, 0.2]], dtype=np.float32)
+    tokens = np.zeros((30, 1), dtype=np.int32)
+    r = _verify_one(o, tl, dp, tokens, range(30))
+    assert (r["n_accepted"] == 0).all(), "p_d == 0 rejects"
+    assert (r["next_token"] == 0).all(), "the residual then sits on the rejected token"
+
+
+def check_verify_accept_rate(o):
+    """P(accept) = min(1, p_t/p_d) at the drafted token."""
+    tl = np.log(np.array([[0.2, 0.3, 0.5], [1, 1, 1]], dtype=np.float64)).astype(np.float32)
+    dp = np.array([[0.5, 0.3, 0.2]], dtype=np.float32)
+    n = 20000
+    r = _verify_one(o, tl, dp, np.zeros((n, 1), dtype=np.int32), range(n), T=1.0)
+    rate = r["n_accepted"].mean()
+    ratio = 0.2 / 0.5
+    assert abs(rate - ratio) < 5 * math.sqrt(ratio * (1 - ratio) / n), f"accept rate {rate}"
+
+
+def check_verify_output_is_target_distribution(o):
+    """Speculative sampling theorem: the first emitted token follows p_t."""
+    rng = np.random.default_rng(17)
+    T = 0.7
+    tl = np.array([[1.0, 0.0, -1.0, 0.5], [0, 0, 0, 0]], dtype=np.float32)
+    pd = np.array([[0.1, 0.6, 0.2, 0.1]], dtype=np.float32)
+    n = 30000
+    pd64 = pd[0].astype(np.float64)
+    tokens = rng.choice(4, size=(n, 1), p=pd64 / pd64.sum()).astype(np.int32)
+    r = _verify_one(o, tl, pd, tokens, range(5000, 5000 + n), T)
+    emitted = np.where(r["n_accepted"] == 1, tokens[:, 0], r["next_token"])
+    p = _chi2_p(np.bincount(emitted, minlength=4), _softmax64(tl[0], T))
+    assert p > 1e-4, f"emitted tokens do not follow p_t: p={p}"
+
+
+def check_verify_residual_distribution(o):
+    T = 0.7
+    tl = np.array([[1.0, 0.0, -1e30, 0.5, -0.5], [0] * 5], dtype=np.float32)
+    pd = np.array([[0.1, 0.05, 0.1, 0.1, 0.65]], dtype=np.float32)
+    n = 20000
+    r = _verify_one(o, tl, pd, np.full((n, 1), 2, dtype=np.int32), range(n), T)
+    assert (r["n_accepted"] == 0).all()
+    pt = _softmax64(tl[0], T)
+    res = np.maximum(pt - pd[0], 0.0)
+    p = _chi2_p(np.bincount(r["next_token"], minlength=5), res / res.sum())
+    assert p > 1e-4, f"replacement tokens do not follow the clamped residual: p={p}"
+
+
+def check_verify_stops_at_first_rejection(o):
+    rng = np.random.default_rng(18)
+    T = 0.7
+    tl = rng.standard_normal((5, 10)).astype(np.float32)
+    tl[1, 3] = -1e30
+    dp = _softmax64(tl[:4], T).astype(np.float32)
+    tokens = np.tile(np.array([5, 3, 5, 5], dtype=np.int32), (20, 1))
+    r = _verify_one(o, tl, dp, tokens, range(20), T)
+    assert (r["n_accepted"] == 1).all(), "verification stops at the first rejection"
+
+
+def check_verify_bonus_token(o):
+    T = 0.7
+    tl = np.array([[0.0, 0.0, 0.0], [0.2, -0.4, 1.1]], dtype=np.float32)
+    dp = _softmax64(tl[:1], T).astype(np.float32)
+    n = 20000
+    tokens = np.zeros((n, 1), dtype=np.int32)
+    r = _verify_one(o, tl, dp, tokens, range(n), T, bonus=True)
+    assert (r["n_accepted"] == 1).all()
+    p = _chi2_p(np.bincount(r["next_token"], minlength=3), _softmax64(tl[1], T))
+    assert p > 1e-4, f"bonus token does not follow softmax(target[K]/T): p={p}"
+    r = _verify_one(o, tl, dp, tokens[:10], range(10), T, bonus=False)
+    assert (r["next_token"] == -1).all(), "no bonus token unless asked for"
+
+
+ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

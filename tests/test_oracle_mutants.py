@@ -1,0 +1,104 @@
+"""Plant plausible mistakes in copies of the oracle source; each must fail a pin.
+
+Every mutant is one textual edit of `oracle/tts_oracle.c` (a dropped term, a
+wrong sign, index or operand, an off-by-one).  The copy is compiled into a
+temporary library and all pins of `oracle_pins` run against it in a child
+process; the test passes when at least one pin fails.  The real oracle is
+never modified.
+"""
+import json
+import os
+import subprocess
+import sys
+import tempfile
+from concurrent.futures import ThreadPoolExecutor
+from pathlib import Path
+
+import pytest
+
+import oracle
+
+ROOT = Path(__file__).resolve().parents[1]
+
+MUTANTS = [
+    ("philox: low product word in place of the high one", "uint64_t y1 = lo1;", "uint64_t y1 = hi1;"),
+    ("philox: second key word not bumped", "        k1 += W1;\n", ""),
+    ("philox: nine rounds", "round < 10", "round < 9"),
+    ("philox: words 1 and 3 swapped in the xor", "uint64_t y0 = hi1 ^ x1 ^ k0;", "uint64_t y0 = hi1 ^ x3 ^ k0;"),
+    ("uniform: wrong bit window", "const uint32_t k = half >> 9;", "const uint32_t k = half >> 10;"),
+    ("uniform: high half first",
+     "(lane & 1u) ? (uint32_t)(word >> 32) : (uint32_t)word", "(lane & 1u) ? (uint32_t)word : (uint32_t)(word >> 32)"),
+    ("uniform: counter block index", "const uint64_t ctr[4] = {idx / 8u, tag, pos, 0};",
+     "const uint64_t ctr[4] = {idx / 4u, tag, pos, 0};"),
+    ("gumbel: sign", "return -logf(-logf(u));", "return logf(-logf(u));"),
+    ("append: slot offset", "+ s % ORC_BLOCK) * row;", "+ (s + 1) % ORC_BLOCK) * row;"),
+    ("append: logical block", "block_table[(size_t)b * max_blocks + s / ORC_BLOCK];",
+     "block_table[(size_t)b * max_blocks + (s + 1) / ORC_BLOCK];"),
+    ("attn: scale dropped", "s[t] = scale * dot;", "s[t] = dot;"),
+    ("attn: GQA head mapping", "const int g = h / group;", "const int g = h % Hkv;"),
+    ("attn: causal limit off by one", "causal ? L - q_len + j + 1 : L", "causal ? L - q_len + j + 2 : L"),
+    ("attn: causal limit short", "causal ? L - q_len + j + 1 : L", "causal ? L - q_len + j : L + 0"),
+    ("attn: key slot", "+ t % ORC_BLOCK) * D;\n                    double dot",
+     "+ (t + 1) % ORC_BLOCK) * D;\n                    double dot"),
+    ("attn: values from the key pool", "o[d] += p * load_elem(v_pool,", "o[d] += p * load_elem(k_pool,"),
+    ("attn: unnormalised weights", "const double p = s[t] / denom;", "const double p = s[t];"),
+    ("head: W transposed", "load_elem(W, (size_t)v * H + k, is_bf16)", "load_elem(W, (size_t)k * V + v, is_bf16)"),
+    ("head: highest index wins ties", "if (arg < 0 || key > top) {", "if (arg < 0 || key >= top) {"),
+    ("head: eos mask ignored", "? V - 1 : V;", "? V : V;"),
+    ("head: temperature multiplies", "key = logit / T + orc_gumbel", "key = logit * T + orc_gumbel"),
+    ("head: noise indexed by row", "orc_gumbel(seed[r], step[r], 0u, 0u, (uint32_t)v)",
+     "orc_gumbel(seed[r], step[r], 0u, 0u, (uint32_t)r)"),
+    ("verify: accept test reversed", "accepted = u < ratio;", "accepted = u > ratio;"),
+    ("verify: zero draft probability accepted", "if (dp[d] > 0.0f) {", "if (dp[d] >= 0.0f) {"),
+    ("verify: residual not clamped", "fmaxf(pt[v] - dp[v], 0.0f)", "fabsf(pt[v] - dp[v])"),
+    ("verify: residual ignores the draft", "fmaxf(pt[v] - dp[v], 0.0f)", "pt[v]"),
+    ("verify: does not stop at the first rejection", "rejected = 1;\n            break;", "rejected = 1;"),
+    ("verify: temperature dropped", "row_probs(tl, V, T, pt);", "row_probs(tl, V, 1.0f, pt);"),
+    ("verify: bonus always drawn", "if (!rejected && (flags & 1)) {", "if (!rejected) {"),
+    ("verify: bonus from the last draft row",
+     "target_logits + ((size_t)b * (K + 1) + K) * V;", "target_logits + ((size_t)b * (K + 1) + K - 1) * V;"),
+]
+
+_CHILD = r"""
+import json, sys
+sys.path[:0] = [{root!r}, {tests!r}]
+import oracle, oracle_pins
+o = oracle.Oracle({lib!r})
+failed = []
+for check in oracle_pins.ALL_CHECKS:
+    try:
+        check(o)
+    except Exception as e:  # a failed pin
+        failed.append(check.__name__)
+print(json.dumps(failed))
+"""
+
+
+def _run_mutant(tmp: Path, i: int, old: str, new: str):
+    src = oracle.SRC.read_text()
+    assert src.count(old) == 1, f"mutant {i}: snippet must occur exactly once: {old!r}"
+    msrc = tmp / f"mutant_{i}.c"
+    msrc.write_text(src.replace(old, new))
+    lib = oracle.build(msrc, tmp / f"libmutant_{i}.so", force=True)
+    code = _CHILD.format(root=str(ROOT), tests=str(ROOT / "tests"), lib=str(lib))
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    p = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                       timeout=600, env=env)
+    if p.returncode != 0:
+        return ["<child crashed: " + p.stderr.strip().splitlines()[-1][:200] + ">"]
+    return json.loads(p.stdout.strip().splitlines()[-1])
+
+
+def test_every_mutant_fails_a_pin():
+    with tempfile.TemporaryDirectory() as d:
+        tmp = Path(d)
+        with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 2)) as ex:
+            futs = [ex.submit(_run_mutant, tmp, i, old, new) for i, (_, old, new) in enumerate(MUTANTS)]
+            results = [f.result() for f in futs]
+    survivors = [MUTANTS[i][0] for i, failed in enumerate(results) if not failed]
+    assert not survivors, f"mistakes no pin catches: {survivors}"
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_snippet_present(name, old, new):
+    assert oracle.SRC.read_text().count(old) == 1
