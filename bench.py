@@ -1,0 +1,441 @@
+#!/usr/bin/env python
+"""Benchmark of one batched decode step (append -> attention -> head) on GB300.
+
+Workload (default): 64 streams, GQA 16 query / 8 KV heads, head_dim 128, bf16,
+context lengths uniform in [50, 1500] behind a randomly permuted block table,
+acoustic head 2048 -> 4097 at temperature zero.  A step processes one query
+token per stream; value = codec tokens per second = streams / step time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+Prints one JSON line.  Under torchrun (N > 1) every rank runs its own replica
+of the workload on its own GPU (streams are independent; no collective on the
+data path); timing is the max over ranks.  --impl reference times the CPU
+oracle on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+if str(ROOT) not in sys.path:
+    sys.path.insert(0, str(ROOT))
+
+import numpy as np  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "codec tokens/s per decode batch; decode-attn HBM GB/s and % of GB300 peak"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+ATTN_SOURCES = ["decode_step_gb300/csrc/decode_attn.cu", "decode_step_gb300/csrc/tts_common.cuh"]
+
+
+# ------------------------------------------------------------------ helpers
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", type=int, default=3, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU work budget of the oracle baseline in the native line")
+    ap.add_argument("--e2e-steps", type=int, default=1000)
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def combine_rank_times(per_rank_ms: list[float], streams_per_rank: int) -> tuple[float, float]:
+    """(ms per step = max over ranks, whole-job tokens/s = all ranks' streams / that time)."""
+    ms = max(per_rank_ms)
+    return ms, streams_per_rank * len(per_rank_ms) / (ms / 1e3)
+
+
+def max_over_ranks(x: float, world: int, device=None) -> list[float]:
+    """All ranks' values of x (gathered; works for nccl and gloo groups)."""
+    if world == 1:
+        return [x]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    out = [torch.zeros_like(t) for _ in range(world)]
+    dist.all_gather(out, t)
+    return [float(o.item()) for o in out]
+
+
+def load_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        h.update((ROOT / p).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    source is unchanged since the capture (else None)."""
+    p = ROOT / "profiles" / "traffic.json"
+    if not p.exists():
+        return None
+    try:
+        rec = json.loads(p.read_text()).get(kernel)
+    except (ValueError, AttributeError):
+        return None
+    if not rec or rec.get("workload") != workload or rec.get("source_sha") != source_sha(ATTN_SOURCES):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def attn_bytes(inp) -> int:
+    """Algorithmic bytes of one attention launch: every cached K/V row once,
+    q and out once, the used block-table entries and the context lengths."""
+    w = inp["workload"]
+    L = inp["ctx_lens"].astype(np.int64)
+    kv = int(L.sum()) * w.Hkv * w.D * w.elem_bytes * 2
+    qo = 2 * w.B * w.q_len * w.Hq * w.D * w.elem_bytes
+    table = int((-(-L // wl.BLOCK)).sum()) * 4
+    return kv + qo + table + 4 * w.B
+
+
+def head_bytes(w) -> int:
+    return w.V * w.H * w.elem_bytes + w.R * w.H * w.elem_bytes + 4 * w.R
+
+
+def append_bytes(w) -> int:
+    return 2 * 2 * w.B * w.q_len * w.Hkv * w.D * w.elem_bytes
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "100"]
+            if self.gpu_id:
+                cmd += ["-i", self.gpu_id]
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.25)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in Path(self.path).read_text().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def oracle_stream_steps(orc, inp, streams, kp, vp):
+    """The oracle's decode step for a list of streams (append, attention, head row)."""
+    w = inp["workload"]
+    for b in streams:
+        sl = slice(b, b + 1)
+        orc.kv_append(kp, vp, inp["block_table"][sl], inp["ctx_before"][sl], inp["k_new"][sl],
+                      inp["v_new"][sl], inplace=True)
+        att = orc.decode_attn(kp, vp, inp["block_table"][sl], inp["ctx_lens"][sl], inp["q"][sl],
+                              inp["scale"], w.causal)
+        h = wl.f32_to_bf16(att.reshape(w.q_len, -1).astype(np.float32)) if w.dtype == "bf16" \
+            else att.reshape(w.q_len, -1).astype(np.float32)
+        orc.head_select(h, inp["W"], w.mode, w.T, inp["seed"][b * w.q_len:(b + 1) * w.q_len],
+                        inp["step"][b * w.q_len:(b + 1) * w.q_len])
+
+
+def cpu_baseline(inp, seconds: float) -> dict:
+    """The oracle, single-threaded, over as many whole streams as fit in `seconds`."""
+    import oracle
+    orc = oracle.default()
+    w = inp["workload"]
+    kp, vp = inp["k_pool"].copy(), inp["v_pool"].copy()
+    done, t0 = 0, time.perf_counter()
+    while done < w.B and (done == 0 or time.perf_counter() - t0 < seconds):
+        oracle_stream_steps(orc, inp, [done], kp, vp)
+        done += 1
+    dt = time.perf_counter() - t0
+    return {"value": done * w.q_len / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {w.B} streams of one step (append, attention, head row), "
+                      f"single-threaded C oracle, {dt:.1f} s"}
+
+
+# ------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    orc = oracle.default()
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.make_inputs(w)
+    kp, vp = inp["k_pool"].copy(), inp["v_pool"].copy()
+    # One unit = one stream's step; a step of this arm is a bounded sample of
+    # units sized so that warm-up + timed steps take about two minutes.
+    t0 = time.perf_counter()
+    oracle_stream_steps(orc, inp, [0], kp, vp)
+    unit_s = max(time.perf_counter() - t0, 1e-4)
+    per_step = max(1, min(w.B, int(120.0 / (args.steps + args.warmup) / unit_s)))
+    order = np.random.default_rng(0).permutation(w.B)
+    pos = 0
+
+    def one_step():
+        nonlocal pos
+        streams = [int(order[(pos + i) % w.B]) for i in range(per_step)]
+        pos += per_step
+        oracle_stream_steps(orc, inp, streams, kp, vp)
+
+    for _ in range(args.warmup):
+        one_step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_step()
+    dt = time.perf_counter() - t0
+    tokens = per_step * w.q_len * args.steps
+    value = tokens / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": workload_config(w, 1),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} of {w.B} streams per step, single-threaded C oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(w, world):
+    return {"workload": f"{w.name}: {w.B} streams/GPU, GQA {w.Hq}/{w.Hkv} heads, head_dim {w.D}, "
+                        f"{w.dtype}, q_len {w.q_len}, ctx {w.ctx_dist} [{w.ctx_lo},{w.ctx_hi}], "
+                        f"{'permuted' if w.permute_table else 'ordered'} 16-token block table, "
+                        f"head {w.H}->{w.V} {w.mode}",
+            "global_batch": w.B * world, "seq_len": 1, "l2": "flushed before every timed step",
+            "parallelism": f"replicas x{world} (streams independent, no collective)"}
+
+
+# ---------------------------------------------------------------- native arm
+
+def run_native(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    device = torch.device("cuda", torch.cuda.current_device())
+    from decode_step_gb300.build import build as build_lib
+    build_lib()
+    from decode_step_gb300 import binding as bd
+    from decode_step_gb300.step import DecodeStep
+
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.make_inputs(w, seed=wl.NUMPY_SEED_BASE + w.id + 7919 * rank)
+
+    def dev(x):
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+        if x.dtype == np.uint64:
+            return torch.from_numpy(x.view(np.int64)).to(device)
+        return torch.from_numpy(np.ascontiguousarray(x)).to(device)
+
+    names = ["block_table", "ctx_before", "ctx_lens", "q", "k_new", "v_new"]
+    d = {k: dev(inp[k]) for k in names}
+    seed, stp = dev(inp["seed"]), dev(inp["step"])
+    cache = bd.KVCache(dev(inp["k_pool"]), dev(inp["v_pool"]))
+    W = dev(inp["W"])
+    mode = bd.TTS_GUMBEL if w.mode == "gumbel" else bd.TTS_ARGMAX
+    step = DecodeStep(cache, W, w.Hq, w.B, w.ctx_hi, q_len=w.q_len, causal=w.causal, mode=mode,
+                      temperature=w.T)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    def run_step():
+        return step(d["block_table"], d["ctx_before"], d["ctx_lens"], d["q"], d["k_new"],
+                    d["v_new"], seed=seed, step=stp)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        run_step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    try:
+        uuid = str(torch.cuda.get_device_properties(device).uuid)
+        gpu_id = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+    except Exception:
+        gpu_id = None
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        e = ev[i]
+        e[0].record(stream)
+        bd.tts_kv_append(cache, d["block_table"], d["ctx_before"], d["k_new"], d["v_new"], err=step.err)
+        e[1].record(stream)
+        bd.tts_decode_attn(cache, d["block_table"], d["ctx_lens"], w.ctx_hi, d["q"], step.out,
+                           step.attn_ws, step.scale, w.causal, err=step.err)
+        e[2].record(stream)
+        bd.tts_codebook_head_select(step.out.view(step.R, -1), W, step.ids, step.head_ws, mode=mode,
+                                    temperature=w.T, seed=seed, step=stp)
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    t_app = [e[0].elapsed_time(e[1]) for e in ev]
+    t_att = [e[1].elapsed_time(e[2]) for e in ev]
+    t_head = [e[2].elapsed_time(e[3]) for e in ev]
+    t_step = [e[0].elapsed_time(e[3]) for e in ev]
+    ms_local = statistics.fmean(t_step)
+    all_ms = max_over_ranks(ms_local, world, device)
+    ms, value = combine_rank_times(all_ms, w.B * w.q_len)
+    errflags = int(step.err.item())
+
+    # ---- end to end through the public API with host buffers
+    host = {k: torch.from_numpy(np.ascontiguousarray(inp[k]).view(
+        np.int16 if inp[k].dtype == np.uint16 else inp[k].dtype)).pin_memory() for k in names}
+    ids_host = torch.empty(w.R, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = ids_host.numel() * 4
+    n_e2e = max(10, min(args.e2e_steps, K))
+
+    def e2e_step():
+        for k in names:
+            dst = d[k] if d[k].dtype != torch.bfloat16 else d[k].view(torch.int16)
+            dst.copy_(host[k], non_blocking=True)
+        ids = run_step()
+        ids_host.copy_(ids, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(5):
+        e2e_step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        e2e_step()
+    e2e_s = time.perf_counter() - t0
+    e2e_all = max_over_ranks(e2e_s / n_e2e * 1e3, world, device)
+    _, e2e_value = combine_rank_times(e2e_all, w.B * w.q_len)
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+    peaks, peak_kind = load_peaks()
+    att_us = 1e3 * statistics.fmean(t_att)
+    head_us = 1e3 * statistics.fmean(t_head)
+    app_us = 1e3 * statistics.fmean(t_app)
+    ab = attn_bytes(inp)
+    achieved = ab / (att_us * 1e-6) / 1e9
+    hb = head_bytes(w)
+    head_gbs = hb / (head_us * 1e-6) / 1e9
+    head_tflops = 2.0 * w.R * w.H * w.V / (head_us * 1e-6) / 1e12
+    traffic = recorded_traffic("decode_attn", w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "impl": "native",
+        "config": workload_config(w, world),
+        "roofline": {"bound": "hbm", "kernel": "decode_attn", "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": traffic, "algorithmic_bytes": ab,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback"},
+        "kernels": {
+            "kv_append_us": app_us, "decode_attn_us": att_us, "head_select_us": head_us,
+            "decode_attn_us_median": 1e3 * statistics.median(t_att),
+            "head_select_us_median": 1e3 * statistics.median(t_head),
+            "kv_append_gbs": append_bytes(w) / (app_us * 1e-6) / 1e9,
+            "head_roofline": {"bound": "hbm", "achieved": head_gbs, "peak": peaks["hbm_gbs"],
+                              "unit": "GB/s", "frac": head_gbs / peaks["hbm_gbs"],
+                              "algorithmic_bytes": hb, "tflops": head_tflops},
+        },
+        "gpu_launches": 3 * K,
+        "device_error_flags": errflags,
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": n_e2e, "note": "wall clock; pinned host inputs copied in and ids read "
+                                        "back (with a stream sync) every step"},
+    }
+    if world == 1:
+        line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_native(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

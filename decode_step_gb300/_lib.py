@@ -1,0 +1,95 @@
+"""ctypes declarations of the C ABI in include/tts_decode.h.
+
+Loads the in-tree libttsdecode built by `python -m decode_step_gb300.build`.
+There is no fallback: if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import re
+from pathlib import Path
+
+from . import build as _build
+
+TTS_OK = 0
+TTS_F32, TTS_BF16 = 0, 1
+TTS_ARGMAX, TTS_GUMBEL = 0, 1
+TTS_VERIFY_BONUS = 1
+ERRBIT_BLOCK_ID, ERRBIT_CTX_LEN, ERRBIT_TOKEN, ERRBIT_TIMEOUT = 1, 2, 4, 8
+
+HEADER = Path(__file__).resolve().parents[1] / "include" / "tts_decode.h"
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_sz = ctypes.c_size_t
+_f32 = ctypes.c_float
+
+
+class KVCacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", _i32), ("block_size", _i32), ("num_kv_heads", _i32),
+                ("head_dim", _i32), ("dtype", _i32), ("k_pool", _vp), ("v_pool", _vp)]
+
+
+_SIGNATURES = {
+    "tts_block_pool_create": (ctypes.c_int, [_i32, ctypes.POINTER(_vp)]),
+    "tts_block_pool_alloc": (ctypes.c_int, [_vp, _i32, _vp]),
+    "tts_block_pool_free": (ctypes.c_int, [_vp, _vp, _i32]),
+    "tts_block_pool_num_free": (_i32, [_vp]),
+    "tts_block_pool_destroy": (None, [_vp]),
+    "tts_kv_append": (ctypes.c_int, [ctypes.POINTER(KVCacheDesc), _vp, _i32, _vp, _i32, _i32,
+                                     _vp, _vp, _vp, _vp]),
+    "tts_decode_attn_workspace_size": (_sz, [_i32] * 6),
+    "tts_decode_attn": (ctypes.c_int, [ctypes.POINTER(KVCacheDesc), _vp, _i32, _vp, _i32, _i32,
+                                       _i32, _i32, _f32, _i32, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "tts_head_workspace_size": (_sz, [_i32, _i32]),
+    "tts_codebook_head_select": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32,
+                                                _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "tts_spec_verify": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _f32, _vp, _vp, _i32,
+                                       _vp, _vp, _vp, _vp]),
+    "tts_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "tts_version": (ctypes.c_int, []),
+}
+
+_LIB = None
+
+
+class LibraryMissing(RuntimeError):
+    pass
+
+
+def declared_symbols() -> list[str]:
+    """Function names declared in include/tts_decode.h."""
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tts_[a-z0-9_]+)\s*\(", text)))
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises LibraryMissing if it was not built)."""
+    global _LIB
+    if _LIB is None:
+        path = _build.lib_path()
+        if not path.exists():
+            raise LibraryMissing(f"{path} not built: run `python -m decode_step_gb300.build`")
+        L = ctypes.CDLL(str(path))
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def status_string(code: int) -> str:
+    return lib().tts_status_string(code).decode()
+
+
+class TTSError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {status_string(code)} ({code})")
+        self.code = code
+
+
+def check(fn: str, code: int) -> None:
+    if code != TTS_OK:
+        raise TTSError(fn, code)

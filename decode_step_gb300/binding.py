@@ -1,0 +1,187 @@
+"""Python binding of the C ABI (include/tts_decode.h), same function names.
+
+Argument marshalling only: torch tensors supply device memory and the current
+CUDA stream; every step of the computation runs in the library's kernels.
+Shapes and dtypes are checked here so a mistake raises a Python error before
+anything is launched.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import (TTS_ARGMAX, TTS_BF16, TTS_F32, TTS_GUMBEL, TTS_VERIFY_BONUS,  # noqa: F401
+                   KVCacheDesc, TTSError, check, lib)
+
+_DTYPES = {torch.float32: TTS_F32, torch.bfloat16: TTS_BF16}
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the library must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return _ptr(t)
+
+
+def _keys(t: torch.Tensor | None, name: str, n: int):
+    """uint64 (or same-width int64) key arrays."""
+    if t is None:
+        return None
+    if t.dtype not in (torch.uint64, torch.int64):
+        raise ValueError(f"{name} must be uint64 (or int64 with the same bits)")
+    return _dev(t, name, None, (n,))
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class KVCache:
+    """Paged KV pool: k_pool, v_pool [num_blocks][num_kv_heads][16][head_dim]."""
+
+    def __init__(self, k_pool: torch.Tensor, v_pool: torch.Tensor):
+        if k_pool.shape != v_pool.shape or k_pool.dim() != 4 or k_pool.shape[2] != 16:
+            raise ValueError("pools must be [num_blocks][num_kv_heads][16][head_dim] and alike")
+        if k_pool.dtype != v_pool.dtype or k_pool.dtype not in _DTYPES:
+            raise ValueError("pools must both be float32 or bfloat16")
+        self.k_pool, self.v_pool = k_pool, v_pool
+        nb, hkv, _, d = k_pool.shape
+        self.desc = KVCacheDesc(nb, 16, hkv, d, _DTYPES[k_pool.dtype],
+                                _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"))
+
+    @property
+    def num_blocks(self) -> int:
+        return self.desc.num_blocks
+
+    @property
+    def num_kv_heads(self) -> int:
+        return self.desc.num_kv_heads
+
+    @property
+    def head_dim(self) -> int:
+        return self.desc.head_dim
+
+    @property
+    def dtype(self) -> torch.dtype:
+        return self.k_pool.dtype
+
+
+class BlockPool:
+    """Host free list of KV block ids (tts_block_pool_*)."""
+
+    def __init__(self, num_blocks: int):
+        h = ctypes.c_void_p()
+        check("tts_block_pool_create", lib().tts_block_pool_create(num_blocks, ctypes.byref(h)))
+        self._h = h
+
+    def alloc(self, n: int) -> list[int]:
+        ids = (ctypes.c_int32 * max(n, 1))()
+        check("tts_block_pool_alloc", lib().tts_block_pool_alloc(self._h, n, ids))
+        return list(ids[:n])
+
+    def free(self, ids) -> None:
+        arr = (ctypes.c_int32 * max(len(ids), 1))(*ids)
+        check("tts_block_pool_free", lib().tts_block_pool_free(self._h, arr, len(ids)))
+
+    @property
+    def num_free(self) -> int:
+        n = lib().tts_block_pool_num_free(self._h)
+        if n < 0:
+            check("tts_block_pool_num_free", n)
+        return n
+
+    def close(self) -> None:
+        if self._h:
+            lib().tts_block_pool_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def tts_kv_append(cache: KVCache, block_table, ctx_before, k_new, v_new, err=None, stream=None):
+    B, max_blocks = block_table.shape
+    q_len = k_new.shape[1]
+    shape = (B, q_len, cache.num_kv_heads, cache.head_dim)
+    args = (ctypes.byref(cache.desc), _dev(block_table, "block_table", torch.int32), max_blocks,
+            _dev(ctx_before, "ctx_before", torch.int32, (B,)), B, q_len,
+            _dev(k_new, "k_new", cache.dtype, shape), _dev(v_new, "v_new", cache.dtype, shape),
+            None if err is None else _dev(err, "err", torch.int32), _stream(stream))
+    check("tts_kv_append", lib().tts_kv_append(*args))
+
+
+def tts_decode_attn_workspace_size(B, q_len, num_q_heads, num_kv_heads, head_dim, max_ctx_len) -> int:
+    return int(lib().tts_decode_attn_workspace_size(B, q_len, num_q_heads, num_kv_heads, head_dim,
+                                                   max_ctx_len))
+
+
+def tts_decode_attn(cache: KVCache, block_table, ctx_lens, max_ctx_len, q, out, ws, scale,
+                    causal=False, err=None, stream=None):
+    B, max_blocks = block_table.shape
+    _, q_len, Hq, D = q.shape
+    args = (ctypes.byref(cache.desc), _dev(block_table, "block_table", torch.int32), max_blocks,
+            _dev(ctx_lens, "ctx_lens", torch.int32, (B,)), int(max_ctx_len), B, q_len, Hq,
+            float(scale), int(bool(causal)), _dev(q, "q", cache.dtype, (B, q_len, Hq, cache.head_dim)),
+            _dev(out, "out", cache.dtype, (B, q_len, Hq, cache.head_dim)), _dev(ws, "ws"),
+            ws.numel() * ws.element_size(), None if err is None else _dev(err, "err", torch.int32),
+            _stream(stream))
+    check("tts_decode_attn", lib().tts_decode_attn(*args))
+
+
+def tts_head_workspace_size(R, V) -> int:
+    return int(lib().tts_head_workspace_size(R, V))
+
+
+def tts_codebook_head_select(h, W, ids, ws, mode=TTS_ARGMAX, temperature=0.0, seed=None, step=None,
+                             eos_allowed=None, best=None, logits_out=None, stream=None):
+    R, H = h.shape
+    V = W.shape[0]
+    if h.dtype not in _DTYPES or W.dtype != h.dtype or W.shape[1] != H:
+        raise ValueError("h [R][H] and W [V][H] must share a float32 / bfloat16 dtype")
+    args = (_dev(h, "h"), _dev(W, "W"), _DTYPES[h.dtype], R, H, V, int(mode), float(temperature),
+            _keys(seed, "seed", R), _keys(step, "step", R),
+            None if eos_allowed is None else _dev(eos_allowed, "eos_allowed", torch.uint8, (R,)),
+            _dev(ids, "ids", torch.int32, (R,)),
+            None if best is None else _dev(best, "best", torch.float32, (R,)),
+            None if logits_out is None else _dev(logits_out, "logits_out", torch.float32, (R, V)),
+            _dev(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
+    check("tts_codebook_head_select", lib().tts_codebook_head_select(*args))
+
+
+def tts_spec_verify(target_logits, draft_probs, draft_tokens, temperature, seed, step,
+                    n_accepted, next_token, bonus=False, err=None, stream=None):
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    args = (_dev(target_logits, "target_logits", torch.float32),
+            _dev(draft_probs, "draft_probs", torch.float32, (B, K, V)),
+            _dev(draft_tokens, "draft_tokens", torch.int32, (B, K)), B, K, V, float(temperature),
+            _keys(seed, "seed", B), _keys(step, "step", B),
+            TTS_VERIFY_BONUS if bonus else 0, _dev(n_accepted, "n_accepted", torch.int32, (B,)),
+            _dev(next_token, "next_token", torch.int32, (B,)),
+            None if err is None else _dev(err, "err", torch.int32), _stream(stream))
+    check("tts_spec_verify", lib().tts_spec_verify(*args))
+
+
+def tts_status_string(code: int) -> str:
+    return _lib.status_string(code)
+
+
+def tts_version() -> int:
+    return int(lib().tts_version())

@@ -1,0 +1,524 @@
+// Codebook head with fused token selection ("TontaubeV1: Streaming
+// Text-to-Speech with Hierarchical Codec Modeling and Bounded Context",
+// section 3: each stage scores its codebook (4,096 acoustic or 16,384 semantic
+// entries plus a boundary token) and picks a token, at temperature zero for
+// the later stages):
+//   logits[r][v] = h[r] . W[v];  ids[r] = argmax_v logits[r][v]           (argmax)
+//                                ids[r] = argmax_v logits[r][v] / T + G   (Gumbel-max)
+//
+// bf16: a tcgen05 tensor-core kernel.  The vocabulary is the MMA's M side
+// (128 rows of W per tile) and the batch rows are the N side, so a small
+// batch still fills the 128-row tensor-core tile.  Per CTA: a TMA producer
+// warp streams W and h k-slices (SWIZZLE_128B) through a 4-stage shared-memory
+// ring; one thread issues tcgen05.mma into a TMEM accumulator; four epilogue
+// warps read the accumulator back with tcgen05.ld.  A cluster of CK CTAs
+// splits the hidden dimension of one vocab tile; their partial logits are
+// summed through distributed shared memory, so logits never go to global
+// memory (unless the caller asks for them).  Selection is fused: each CTA
+// reduces its rows to one packed (key, index) per batch row with a 64-bit
+// atomicMax, and the last CTA to finish converts the keys to token ids and
+// clears the workspace.  No CTA ever waits on another CTA outside its cluster.
+//
+// fp32: a CUDA-core kernel (tf32 tensor cores would change the rounding of
+// fp32 inputs), one warp per vocabulary row.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "tts_common.cuh"
+#include "tts_internal.h"
+
+namespace tts {
+namespace {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+constexpr int kTileM = 128;           // vocab rows per MMA tile
+constexpr int kTileK = 64;            // hidden elements per stage (one 128-byte swizzle span)
+constexpr int kStagesTC = 4;
+constexpr int kThreadsTC = 192;       // warps 0-3 epilogue, 4 TMA producer, 5 MMA issuer
+constexpr int kMaxN = 256;            // widest MMA N
+constexpr int kATileBytes = kTileM * kTileK * 2;  // 16 KB
+
+// ------------------------------------------------------------ shared parts
+
+struct HeadWs {
+    unsigned long long *keys;  // [R] packed (key, index), zero between calls
+    unsigned int *ticket;      // CTAs finished, zero between calls
+};
+
+HeadWs head_ws(void *ws, int R) {
+    HeadWs w;
+    w.keys = static_cast<unsigned long long *>(ws);
+    w.ticket = reinterpret_cast<unsigned int *>(static_cast<uint8_t *>(ws) +
+                                                align_up(static_cast<size_t>(R) * 8, 256));
+    return w;
+}
+
+// Called by every thread of every CTA after its keys are published.  The
+// last CTA converts keys to ids and resets the workspace.  No waiting.
+__device__ void finish_selection(const HeadWs &ws, int R, int32_t *ids, float *best, int *flag) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned int total = gridDim.x * gridDim.y;
+        *flag = atomicAdd(ws.ticket, 1u) == total - 1u;
+    }
+    __syncthreads();
+    if (!*flag) return;
+    __threadfence();
+    for (int r = threadIdx.x; r < R; r += blockDim.x) {
+        const unsigned long long k = atomicExch(ws.keys + r, 0ull);
+        ids[r] = k ? unpack_index(k) : -1;
+        if (best) best[r] = k ? unpack_value(k) : -INFINITY;
+    }
+    if (threadIdx.x == 0) *ws.ticket = 0u;
+}
+
+struct HeadArgs {
+    int R, H, V, mode;
+    float temperature;
+    const uint64_t *seed;
+    const uint64_t *step;
+    const uint8_t *eos;
+    float *logits_out;
+    int32_t *ids;
+    float *best;
+    HeadWs ws;
+    int32_t *err;
+};
+
+// Gumbel-max selection key of logit `x` at the vocab entry drawing half `e`
+// of its Philox block `ph` (block = entries 8 * (v / 8) .. 8 * (v / 8) + 7).
+__device__ __forceinline__ float gumbel_key(const HeadArgs &a, float x, int e, const Philox4x64 &ph) {
+    return x / a.temperature + gumbel_from_uniform(bits_to_uniform(ph.half(e)));
+}
+
+// ---------------------------------------------------------------- fp32 SIMT
+
+__global__ void __launch_bounds__(256)
+head_simt_f32_kernel(const float *__restrict__ h, const float *__restrict__ W, const HeadArgs a) {
+    __shared__ int flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warps_total = gridDim.x * (blockDim.x >> 5);
+    for (int v = blockIdx.x * (blockDim.x >> 5) + warp; v < a.V; v += warps_total) {
+        const float *w = W + static_cast<size_t>(v) * a.H;
+        for (int r = 0; r < a.R; ++r) {
+            const float *x = h + static_cast<size_t>(r) * a.H;
+            float acc = 0.0f;
+            for (int k = lane; k < a.H; k += 32) acc = fmaf(__ldg(w + k), __ldg(x + k), acc);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
+            if (lane == (r & 31)) {
+                if (a.logits_out) a.logits_out[static_cast<size_t>(r) * a.V + v] = acc;
+                const int vmax = (a.eos && !a.eos[r]) ? a.V - 1 : a.V;
+                if (v < vmax) {
+                    float key = acc;
+                    if (a.mode == TTS_GUMBEL) {
+                        const Philox4x64 ph(static_cast<uint64_t>(v >> 3), 0, 0, 0, a.seed[r], a.step[r]);
+                        key = gumbel_key(a, acc, v & 7, ph);
+                    }
+                    atomicMax(a.ws.keys + r, pack_argmax(key, v));
+                }
+            }
+        }
+    }
+    finish_selection(a.ws, a.R, a.ids, a.best, &flag);
+}
+
+// --------------------------------------------------------- tcgen05 (bf16)
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+__device__ __forceinline__ uint32_t map_cluster(uint32_t addr, uint32_t rank) {
+    uint32_t out;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
+    return out;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart (tcgen05 descriptor format:
+// start >> 4 in bits 0-13, stride offset >> 4 in bits 32-45, version 1 in
+// bits 46-47, swizzle mode 2 (128B) in bits 61-63).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+    return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A
+// and B (bits 7-9, 10-12 = 1), both K-major, N >> 3 in bits 17-22, M >> 4 in
+// bits 24-28.
+__host__ __device__ constexpr uint32_t mma_idesc(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+struct TcLayout {
+    uint32_t stage_bytes;   // A tile + B tile
+    uint32_t ring_bytes;    // all stages (also hosts the accumulator dump)
+    uint32_t dump_stride;   // floats per dumped row (N + 4)
+    uint32_t bars;          // offset of the mbarriers
+    uint32_t colbest;       // offset of the per-column best keys
+    uint32_t misc;          // TMEM address, flag
+    uint32_t total;
+};
+
+__host__ __device__ inline TcLayout tc_layout(int N) {
+    TcLayout L;
+    L.stage_bytes = kATileBytes + N * kTileK * 2;
+    const uint32_t ring = kStagesTC * L.stage_bytes;
+    L.dump_stride = N + 4;
+    const uint32_t dump = kTileM * L.dump_stride * 4;
+    L.ring_bytes = ring > dump ? ring : dump;
+    L.bars = L.ring_bytes;
+    L.colbest = L.bars + 8 * (2 * kStagesTC + 1);
+    L.misc = L.colbest + 8 * N;
+    L.total = L.misc + 16 + 1024;  // + slack to align the dynamic base to 1024
+    return L;
+}
+
+__global__ void __launch_bounds__(kThreadsTC, 1)
+head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_h,
+               const HeadArgs a, int N, int CK, int alloc_cols) {
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle atoms.
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    const TcLayout Lo = tc_layout(N);
+    const uint32_t bar_full = base + Lo.bars;                 // [kStagesTC]
+    const uint32_t bar_empty = bar_full + 8 * kStagesTC;      // [kStagesTC]
+    const uint32_t bar_acc = bar_empty + 8 * kStagesTC;
+    unsigned long long *colbest = reinterpret_cast<unsigned long long *>(smem + Lo.colbest);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lo.misc);
+    int *flag = reinterpret_cast<int *>(smem + Lo.misc + 4);
+    int *failed = reinterpret_cast<int *>(smem + Lo.misc + 8);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = CK > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int vtile = blockIdx.x / CK;
+    const int rchunk = blockIdx.y;
+    const int v0 = vtile * kTileM;
+    const int r0 = rchunk * N;
+    const int ktiles = a.H / kTileK / CK;     // k-slices of this CTA
+    const int kbase = rank * ktiles * kTileK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStagesTC; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        mbar_init(bar_acc, 1);
+        fence_mbar_init();
+        *failed = 0;
+    }
+    for (int i = threadIdx.x; i < N; i += blockDim.x) colbest[i] = 0ull;
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(tmem_slot)),
+                     "r"(alloc_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4 && lane == 0) {
+        // ---- TMA producer
+        for (int it = 0; it < ktiles; ++it) {
+            const int s = it % kStagesTC;
+            if (it >= kStagesTC && !mbar_wait(bar_empty + 8 * s, ((it / kStagesTC) - 1) & 1)) {
+                flag_error(a.err, TTS_ERRBIT_TIMEOUT);
+                atomicExch(failed, 1);
+                break;
+            }
+            const uint32_t sa = base + s * Lo.stage_bytes;
+            mbar_arrive_expect_tx(bar_full + 8 * s, Lo.stage_bytes);
+            const int k = kbase + it * kTileK;
+            tma_load_2d(sa, &map_w, k, v0, bar_full + 8 * s);
+            tma_load_2d(sa + kATileBytes, &map_h, k, r0, bar_full + 8 * s);
+        }
+    } else if (warp == 5 && lane == 0) {
+        // ---- MMA issuer: D[128 x N] += W_tile[128 x 64] . h_tile[N x 64]^T per stage
+        const uint32_t idesc = mma_idesc(kTileM, N);
+        int it = 0;
+        for (; it < ktiles; ++it) {
+            const int s = it % kStagesTC;
+            if (!mbar_wait(bar_full + 8 * s, (it / kStagesTC) & 1)) {
+                flag_error(a.err, TTS_ERRBIT_TIMEOUT);
+                atomicExch(failed, 1);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t sa = base + s * Lo.stage_bytes;
+#pragma unroll
+            for (int kk = 0; kk < kTileK / 16; ++kk)
+                mma_bf16(tmem, sw128_desc(sa + kk * 32), sw128_desc(sa + kATileBytes + kk * 32), idesc,
+                         (it | kk) != 0);
+            mma_commit(bar_empty + 8 * s);
+        }
+        mma_commit(bar_acc);  // fires when every MMA issued above has completed
+    }
+
+    // ---- epilogue part 1: accumulator -> shared memory (rows 32 w .. 32 w + 31)
+    float *dump = reinterpret_cast<float *>(smem);
+    if (warp < 4) {
+        if (!mbar_wait(bar_acc, 0)) {
+            flag_error(a.err, TTS_ERRBIT_TIMEOUT);
+            atomicExch(failed, 1);
+        } else {
+            tc_fence_after();
+            const int row = warp * 32 + lane;
+            for (int c0 = 0; c0 < N; c0 += 16) {
+                float v[16];
+                tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
+                float4 *dst = reinterpret_cast<float4 *>(dump + row * Lo.dump_stride + c0);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(alloc_cols)
+                     : "memory");
+    }
+    if (CK > 1) cluster_sync();
+
+    // ---- epilogue part 2: sum the cluster's partial tiles for this CTA's
+    // 128 / CK rows, select per batch column.  Work item = (8-row group, column).
+    const int rows_per_cta = kTileM / CK;
+    const int items = (rows_per_cta / 8) * N;
+    const uint32_t dump_addr = base;
+    for (int item = threadIdx.x; item < items; item += blockDim.x) {
+        const int gi = item / N, cn = item % N;
+        const int r = r0 + cn;
+        if (r >= a.R) continue;
+        const int lrow = rank * rows_per_cta + gi * 8;   // local row in the tile
+        float lg[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) lg[e] = 0.0f;
+        for (int src = 0; src < CK; ++src) {
+            const uint32_t sb = CK > 1 ? map_cluster(dump_addr, src) : dump_addr;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                lg[e] += CK > 1 ? ld_cluster_f32(sb + ((lrow + e) * Lo.dump_stride + cn) * 4)
+                                : dump[(lrow + e) * Lo.dump_stride + cn];
+        }
+        const int v = v0 + lrow;  // multiple of 8
+        if (a.logits_out) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (v + e < a.V) a.logits_out[static_cast<size_t>(r) * a.V + v + e] = lg[e];
+        }
+        const int vmax = (a.eos && !a.eos[r]) ? a.V - 1 : a.V;
+        if (v >= vmax) continue;
+        unsigned long long best = 0ull;
+        if (a.mode == TTS_GUMBEL) {
+            const Philox4x64 ph(static_cast<uint64_t>(v >> 3), 0, 0, 0, a.seed[r], a.step[r]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (v + e >= vmax) break;
+                const unsigned long long k = pack_argmax(gumbel_key(a, lg[e], e, ph), v + e);
+                best = k > best ? k : best;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (v + e >= vmax) break;
+                const unsigned long long k = pack_argmax(lg[e], v + e);
+                best = k > best ? k : best;
+            }
+        }
+        atomicMax(colbest + cn, best);
+    }
+    __syncthreads();
+    for (int cn = threadIdx.x; cn < N; cn += blockDim.x)
+        if (r0 + cn < a.R && colbest[cn]) atomicMax(a.ws.keys + r0 + cn, colbest[cn]);
+    if (CK > 1) cluster_sync();  // peers may still read this CTA's dump
+    finish_selection(a.ws, a.R, a.ids, a.best, flag);
+}
+
+// ------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor [rows][cols] (cols contiguous), box [box_rows][64], 128-byte swizzle.
+bool make_map(CUtensorMap *map, const void *ptr, int rows, int cols, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileK), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct TcPlan {
+    int N, chunks, CK, alloc_cols;
+    uint32_t smem;
+};
+
+TcPlan plan_tc(int R, int H, int V) {
+    TcPlan p;
+    p.chunks = (R + kMaxN - 1) / kMaxN;
+    const int per = (R + p.chunks - 1) / p.chunks;
+    p.N = (per + 15) / 16 * 16;
+    p.alloc_cols = 32;
+    while (p.alloc_cols < p.N) p.alloc_cols <<= 1;
+    p.smem = tc_layout(p.N).total;
+    const int sms = sm_count() > 0 ? sm_count() : 148;
+    int per_sm = static_cast<int>((227u * 1024u) / (p.smem + 1024u));
+    per_sm = per_sm < 1 ? 1 : per_sm;
+    const int tmem_fit = 512 / p.alloc_cols;
+    per_sm = per_sm < tmem_fit ? per_sm : tmem_fit;
+    const int vtiles = (V + kTileM - 1) / kTileM;
+    const int ktiles = H / kTileK;
+    p.CK = 1;
+    for (int ck = 2; ck <= 8; ck <<= 1) {
+        if (ktiles % ck != 0) break;
+        if (static_cast<long>(vtiles) * p.chunks * ck > static_cast<long>(sms) * per_sm) break;
+        p.CK = ck;
+    }
+    return p;
+}
+
+}  // namespace
+}  // namespace tts
+
+extern "C" size_t tts_head_workspace_size(int32_t R, int32_t V) {
+    if (R < 1 || R > 4096 || V < 1) return 0;
+    return tts::align_up(static_cast<size_t>(R) * 8, 256) + 256;
+}
+
+extern "C" int tts_codebook_head_select(const void *d_h, const void *d_W, int32_t dtype, int32_t R,
+                                        int32_t H, int32_t V, int32_t mode, float temperature,
+                                        const uint64_t *d_seed, const uint64_t *d_step,
+                                        const uint8_t *d_eos_allowed, int32_t *d_ids, float *d_best,
+                                        float *d_logits_out, void *d_ws, size_t ws_bytes,
+                                        void *stream) {
+    using namespace tts;
+    if (!d_h || !d_W || !d_ids) return TTS_ERR_INVALID;
+    if (R < 1 || R > 4096 || H < 1 || V < 1 || V > (1 << 30)) return TTS_ERR_INVALID;
+    if (mode != TTS_ARGMAX && mode != TTS_GUMBEL) return TTS_ERR_INVALID;
+    if (mode == TTS_GUMBEL && (!d_seed || !d_step || !(temperature > 0.0f) || temperature == INFINITY))
+        return TTS_ERR_INVALID;
+    if (dtype != TTS_F32 && dtype != TTS_BF16) return TTS_ERR_UNSUPPORTED;
+    const size_t need = tts_head_workspace_size(R, V);
+    if (!d_ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(d_ws) & 255u) != 0)
+        return TTS_ERR_WORKSPACE;
+    HeadArgs a;
+    a.R = R; a.H = H; a.V = V; a.mode = mode; a.temperature = temperature;
+    a.seed = d_seed; a.step = d_step; a.eos = d_eos_allowed; a.logits_out = d_logits_out;
+    a.ids = d_ids; a.best = d_best; a.ws = head_ws(d_ws, R); a.err = nullptr;
+    auto s = static_cast<cudaStream_t>(stream);
+    if (dtype == TTS_F32) {
+        const int sms = sm_count() > 0 ? sm_count() : 148;
+        int grid = (V + 7) / 8;
+        grid = grid < 4 * sms ? grid : 4 * sms;
+        head_simt_f32_kernel<<<grid, 256, 0, s>>>(static_cast<const float *>(d_h),
+                                                  static_cast<const float *>(d_W), a);
+        return launch_status();
+    }
+    if (H % kTileK != 0) return TTS_ERR_UNSUPPORTED;
+    if (!aligned16(d_h) || !aligned16(d_W)) return TTS_ERR_INVALID;
+    const TcPlan p = plan_tc(R, H, V);
+    CUtensorMap mw, mh;
+    if (!make_map(&mw, d_W, V, H, kTileM) || !make_map(&mh, d_h, R, H, p.N)) return TTS_ERR_CUDA;
+    if (cudaFuncSetAttribute(head_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(p.smem)) != cudaSuccess)
+        return TTS_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(((V + kTileM - 1) / kTileM) * p.CK),
+                       static_cast<unsigned>(p.chunks), 1);
+    cfg.blockDim = dim3(kThreadsTC, 1, 1);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.CK);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, head_tc_kernel, mw, mh, a, p.N, p.CK, p.alloc_cols) != cudaSuccess) {
+        cudaGetLastError();
+        return TTS_ERR_CUDA;
+    }
+    return launch_status();
+}

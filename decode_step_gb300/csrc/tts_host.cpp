@@ -1,0 +1,117 @@
+// Host-side parts of the C ABI: the KV block pool, status strings, device
+// queries.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "tts_decode.h"
+#include "tts_internal.h"
+
+// ------------------------------------------------------------- block pool
+//
+// A static pool of fixed 16-token KV blocks; a request takes free blocks and
+// gives them back when it finishes or is aborted ("Optimizing Streaming
+// Text-to-Speech Models for Sub-50 Millisecond Latency", section "Dynamic
+// Token-Level Batching"; "TTS Serving, in depth", section "Barge-in and
+// cancellation").  A LIFO stack of free ids plus an allocation bitmap that
+// catches double frees and foreign ids.
+
+struct tts_block_pool {
+    std::mutex mu;
+    std::vector<int32_t> free_ids;   // stack; back() is handed out next
+    std::vector<uint8_t> allocated;  // 1 while a block is out
+};
+
+extern "C" int tts_block_pool_create(int32_t num_blocks, tts_block_pool **out) {
+    if (!out || num_blocks < 1) return TTS_ERR_INVALID;
+    *out = nullptr;
+    auto *p = new (std::nothrow) tts_block_pool;
+    if (!p) return TTS_ERR_INVALID;
+    p->free_ids.resize(num_blocks);
+    // Lowest ids on top of the stack, so a fresh pool hands out 0, 1, 2, ...
+    for (int32_t i = 0; i < num_blocks; ++i) p->free_ids[i] = num_blocks - 1 - i;
+    p->allocated.assign(num_blocks, 0);
+    *out = p;
+    return TTS_OK;
+}
+
+extern "C" int tts_block_pool_alloc(tts_block_pool *pool, int32_t n, int32_t *host_ids_out) {
+    if (!pool || n < 0 || (n > 0 && !host_ids_out)) return TTS_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(pool->mu);
+    if (static_cast<size_t>(n) > pool->free_ids.size()) return TTS_ERR_POOL_EXHAUSTED;
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t id = pool->free_ids.back();
+        pool->free_ids.pop_back();
+        pool->allocated[id] = 1;
+        host_ids_out[i] = id;
+    }
+    return TTS_OK;
+}
+
+extern "C" int tts_block_pool_free(tts_block_pool *pool, const int32_t *host_ids, int32_t n) {
+    if (!pool || n < 0 || (n > 0 && !host_ids)) return TTS_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(pool->mu);
+    const int32_t nb = static_cast<int32_t>(pool->allocated.size());
+    // Validate everything first (all or nothing), marking with 2 to catch repeats.
+    int32_t bad = -1;
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t id = host_ids[i];
+        if (id < 0 || id >= nb || pool->allocated[id] != 1) { bad = i; break; }
+        pool->allocated[id] = 2;
+    }
+    if (bad >= 0) {
+        for (int32_t i = 0; i < bad; ++i) pool->allocated[host_ids[i]] = 1;
+        return TTS_ERR_INVALID;
+    }
+    for (int32_t i = 0; i < n; ++i) {
+        pool->allocated[host_ids[i]] = 0;
+        pool->free_ids.push_back(host_ids[i]);
+    }
+    return TTS_OK;
+}
+
+extern "C" int32_t tts_block_pool_num_free(const tts_block_pool *pool) {
+    if (!pool) return TTS_ERR_INVALID;
+    auto *p = const_cast<tts_block_pool *>(pool);
+    std::lock_guard<std::mutex> lock(p->mu);
+    return static_cast<int32_t>(p->free_ids.size());
+}
+
+extern "C" void tts_block_pool_destroy(tts_block_pool *pool) { delete pool; }
+
+// ------------------------------------------------------------------- misc
+
+extern "C" const char *tts_status_string(int status) {
+    switch (status) {
+        case TTS_OK: return "ok";
+        case TTS_ERR_INVALID: return "invalid argument";
+        case TTS_ERR_UNSUPPORTED: return "unsupported shape or type";
+        case TTS_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case TTS_ERR_CUDA: return "CUDA error";
+        case TTS_ERR_POOL_EXHAUSTED: return "block pool exhausted";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int tts_version(void) { return 100; }
+
+namespace tts {
+
+int sm_count() {
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev < 64) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < 64) cached[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+}  // namespace tts

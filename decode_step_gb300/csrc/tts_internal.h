@@ -1,0 +1,35 @@
+// Host-side helpers shared by the C-ABI entry points.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "tts_decode.h"
+
+namespace tts {
+
+// Number of SMs of the current device (cached per device ordinal).
+int sm_count();
+
+// Maps the last launch error to a status (clears it).
+inline int launch_status() {
+    return cudaGetLastError() == cudaSuccess ? TTS_OK : TTS_ERR_CUDA;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Split-KV policy shared by the workspace query and the launch: tokens of a
+// stream are cut into splits of `blocks` 16-token blocks.
+struct AttnSplit {
+    int blocks;      // KV blocks per split
+    int max_splits;  // splits of the longest context
+    int rows;        // query rows per (stream, KV head), padded to the kernel's template
+};
+bool attn_split_policy(int B, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                       int max_ctx_len, AttnSplit *out);
+size_t attn_workspace_bytes(int B, int num_kv_heads, int head_dim, const AttnSplit &sp);
+
+}  // namespace tts

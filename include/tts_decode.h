@@ -1,0 +1,228 @@
+/*
+ * tts_decode.h — C ABI of the GB300 (sm_103a) batched decode step for
+ * streaming codec-language-model text-to-speech.
+ *
+ * One decode step, per active stream: append this step's key/value rows to a
+ * paged KV cache, attend over the stream's cache with its query rows, score
+ * the result with a codebook head and pick the next codec token; in
+ * speculative mode, verify K draft tokens against the target's logits.
+ *
+ * Sources (web pages on streaming codec-LM text-to-speech):
+ *  [OPT] "Optimizing Streaming Text-to-Speech Models for Sub-50 Millisecond
+ *        Latency" — "Speculative Decoding for Acoustic Tokens" (the verify
+ *        rule), "Dynamic Token-Level Batching" (a static pool of 16-token KV
+ *        blocks; batch membership changes at every step).
+ *  [TTS] "TTS (Text-to-Speech) Serving, in depth" — "Token generation under a
+ *        frame budget" (one decode step per frame, each reading the KV cache).
+ *  [TON] "TontaubeV1: Streaming Text-to-Speech with Hierarchical Codec Modeling
+ *        and Bounded Context" — section 3 (16,384-entry semantic and 4,096-entry
+ *        acoustic codebooks plus a boundary token; later stages run at
+ *        temperature zero).
+ *  [NARI] "How We Made a Text-to-Speech Model Respond in Sub-50 ms" —
+ *        "Additional serving optimizations" (avoid host/device synchronisation).
+ *
+ * Conventions shared by every call:
+ *  - Every call returns a tts_status; negative values are errors.  Argument
+ *    checks happen on the host before anything is launched; a call that
+ *    returns an error has launched nothing.
+ *  - Pointers prefixed d_ are device pointers, host_ are host pointers.  The
+ *    caller allocates and owns all memory; the library keeps no pointer after
+ *    a call returns.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and never synchronise the host [NARI].
+ *  - Data the kernels find invalid (a block id outside the pool, a context
+ *    length out of range, a draft token outside the vocabulary) never causes
+ *    an out-of-bounds access: the kernel skips it, writes the defined value
+ *    stated per call, and ORs a TTS_ERRBIT_* flag into *d_err (nullable,
+ *    caller-owned int32 on the device; the caller reads it whenever it likes).
+ *  - Tensors are dense and row-major with the shapes given per call.
+ *  - Calls on different streams are thread-safe as long as their outputs and
+ *    workspaces are disjoint.
+ */
+#ifndef TTS_DECODE_H
+#define TTS_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TTS_OK = 0,
+    TTS_ERR_INVALID = -1,          /* null pointer, bad size, inconsistent shape */
+    TTS_ERR_UNSUPPORTED = -2,      /* a shape or type this build has no kernel for */
+    TTS_ERR_WORKSPACE = -3,        /* workspace missing, misaligned or too small */
+    TTS_ERR_CUDA = -4,             /* a CUDA launch or runtime call failed */
+    TTS_ERR_POOL_EXHAUSTED = -5    /* block pool has too few free blocks */
+} tts_status;
+
+enum { TTS_F32 = 0, TTS_BF16 = 1 };             /* element types */
+enum { TTS_ARGMAX = 0, TTS_GUMBEL = 1 };        /* head selection modes */
+enum { TTS_VERIFY_BONUS = 1 };                  /* tts_spec_verify flags */
+
+/* Bits ORed into *d_err by the kernels. */
+enum {
+    TTS_ERRBIT_BLOCK_ID = 1,   /* block table entry outside [0, num_blocks) */
+    TTS_ERRBIT_CTX_LEN = 2,    /* context length outside its valid range */
+    TTS_ERRBIT_TOKEN = 4,      /* draft token outside [0, V) */
+    TTS_ERRBIT_TIMEOUT = 8     /* a bounded on-device wait ran out */
+};
+
+#define TTS_BLOCK_TOKENS 16
+
+/* Paged KV cache [OPT, "Dynamic Token-Level Batching"]: a static pool of
+ * num_blocks blocks of 16 tokens.  k_pool and v_pool are device arrays
+ * [num_blocks][num_kv_heads][16][head_dim] of `dtype`, so each (block, head)
+ * tile is contiguous.  Supported: (TTS_BF16, head_dim 128), (TTS_F32,
+ * head_dim 64).  Pool base addresses must be 16-byte aligned. */
+typedef struct tts_kv_cache {
+    int32_t num_blocks;
+    int32_t block_size;     /* must be 16 */
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t dtype;          /* TTS_F32 or TTS_BF16 */
+    void *k_pool;
+    void *v_pool;
+} tts_kv_cache;
+
+/* ------------------------------------------------------------ block pool */
+
+/* Host-side free list of block ids [OPT, "Dynamic Token-Level Batching"]:
+ * a request takes free blocks from the global pool and returns them when it
+ * finishes or is aborted ("TTS Serving, in depth", "Barge-in and
+ * cancellation").  Last-freed blocks are handed out first.  A pool is guarded
+ * by its own mutex.  Returns TTS_ERR_INVALID for num_blocks < 1 or a null
+ * `out`. */
+typedef struct tts_block_pool tts_block_pool;
+int tts_block_pool_create(int32_t num_blocks, tts_block_pool **out);
+
+/* Takes n blocks, writing their ids to host_ids_out[n].  All or nothing:
+ * TTS_ERR_POOL_EXHAUSTED (and no change) when fewer than n are free. */
+int tts_block_pool_alloc(tts_block_pool *pool, int32_t n, int32_t *host_ids_out);
+
+/* Returns n blocks.  All or nothing: TTS_ERR_INVALID (and no change) if any id
+ * is outside the pool, not currently allocated, or repeated. */
+int tts_block_pool_free(tts_block_pool *pool, const int32_t *host_ids, int32_t n);
+
+/* Number of free blocks, or TTS_ERR_INVALID for a null pool. */
+int32_t tts_block_pool_num_free(const tts_block_pool *pool);
+void tts_block_pool_destroy(tts_block_pool *pool);
+
+/* ---------------------------------------------------------------- append */
+
+/* Writes this step's keys and values into the pool [OPT, "Dynamic Token-Level
+ * Batching"]: new token j of stream b has logical position
+ * s = d_ctx_before[b] + j and goes to block d_block_table[b][s / 16],
+ * slot s % 16.
+ *  d_block_table  int32 [B][max_blocks_per_seq]
+ *  d_ctx_before   int32 [B] — tokens already cached before this step
+ *  d_k_new, d_v_new  `cache->dtype` [B][q_len][num_kv_heads][head_dim]
+ * A slot outside the table (TTS_ERRBIT_CTX_LEN) or a block id outside the
+ * pool (TTS_ERRBIT_BLOCK_ID) is skipped. */
+int tts_kv_append(const tts_kv_cache *cache, const int32_t *d_block_table,
+                  int32_t max_blocks_per_seq, const int32_t *d_ctx_before, int32_t B,
+                  int32_t q_len, const void *d_k_new, const void *d_v_new, int32_t *d_err,
+                  void *stream);
+
+/* ------------------------------------------------------------- attention */
+
+/* Bytes of device workspace tts_decode_attn needs for these sizes (0 on bad
+ * arguments).  The workspace must be zero-filled before its first use; every
+ * completed call leaves it zero-filled again, so one zeroed buffer serves any
+ * number of calls on one stream.  Calls that overlap on the GPU need separate
+ * workspaces. */
+size_t tts_decode_attn_workspace_size(int32_t B, int32_t q_len, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t max_ctx_len);
+
+/* Decode attention over the paged cache [TTS, "Token generation under a frame
+ * budget"; OPT, "Speculative Decoding for Acoustic Tokens" for q_len > 1]:
+ * for stream b, query row j < q_len and query head h < num_q_heads,
+ *   out[b][j][h] = sum_t softmax_t(scale * q[b][j][h] . k_t) v_t
+ * over the stream's cached tokens t < limit, where d_ctx_lens[b] counts the
+ * tokens AFTER this step's append and limit = d_ctx_lens[b] - q_len + j + 1
+ * when `causal`, d_ctx_lens[b] otherwise.  Query head h reads KV head
+ * h / (num_q_heads / num_kv_heads).  Runs as split-KV flash decoding with a
+ * log-sum-exp merge of the splits.
+ *  d_q    `cache->dtype` [B][q_len][num_q_heads][head_dim]
+ *  d_out  `cache->dtype` [B][q_len][num_q_heads][head_dim]
+ *  max_ctx_len  host upper bound of d_ctx_lens (sizes the grid and workspace)
+ * Requires num_q_heads % num_kv_heads == 0 and
+ * (num_q_heads / num_kv_heads) * q_len <= 16.  A stream whose context length
+ * is outside [q_len, min(max_ctx_len, 16 * max_blocks_per_seq)] gets zeros
+ * (TTS_ERRBIT_CTX_LEN); tokens in blocks with an invalid id are left out
+ * (TTS_ERRBIT_BLOCK_ID). */
+int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block_table,
+                    int32_t max_blocks_per_seq, const int32_t *d_ctx_lens, int32_t max_ctx_len,
+                    int32_t B, int32_t q_len, int32_t num_q_heads, float scale, int32_t causal,
+                    const void *d_q, void *d_out, void *d_ws, size_t ws_bytes, int32_t *d_err,
+                    void *stream);
+
+/* ------------------------------------------------------------------ head */
+
+/* Bytes of device workspace tts_codebook_head_select needs (0 on bad
+ * arguments).  Zero-filled before first use; left zero-filled by every call;
+ * overlapping calls need separate workspaces. */
+size_t tts_head_workspace_size(int32_t R, int32_t V);
+
+/* Codebook head with fused token choice [TON, section 3]:
+ *   logits[r][v] = sum_k h[r][k] * W[v][k]      (fp32 accumulation)
+ * over V entries, V-1 being the boundary token.
+ *  mode TTS_ARGMAX: ids[r] = argmax_v logits[r][v] (temperature zero).
+ *  mode TTS_GUMBEL: ids[r] = argmax_v (logits[r][v] / temperature + G), G the
+ *    Gumbel noise -log(-log u) of Philox4x64-10 uniform u with key
+ *    (d_seed[r], d_step[r]) and counter (v / 8, 0, 0, 0) — a draw from
+ *    softmax(logits / temperature).
+ * Equal keys resolve to the lowest index.  d_eos_allowed[r] == 0 (nullable
+ * array) removes v = V-1 from the choice.  The logits never leave the chip
+ * unless d_logits_out is given.
+ *  d_h   `dtype` [R][H];  d_W  `dtype` [V][H] (vocab-major)
+ *  d_seed, d_step  uint64 [R] (read in TTS_GUMBEL mode only; may be NULL otherwise)
+ *  d_ids int32 [R];  d_best float [R] (nullable: the winning key)
+ *  d_logits_out float [R][V] (nullable: the speculative-verify path needs them)
+ * bf16 runs on the tcgen05 tensor cores and needs H % 64 == 0 and 16-byte
+ * aligned d_h, d_W; fp32 runs on CUDA cores.  Requires 1 <= R <= 4096. */
+int tts_codebook_head_select(const void *d_h, const void *d_W, int32_t dtype, int32_t R,
+                             int32_t H, int32_t V, int32_t mode, float temperature,
+                             const uint64_t *d_seed, const uint64_t *d_step,
+                             const uint8_t *d_eos_allowed, int32_t *d_ids, float *d_best,
+                             float *d_logits_out, void *d_ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------- verify */
+
+/* Speculative verification of K draft tokens per stream [OPT, "Speculative
+ * Decoding for Acoustic Tokens"], for every stream b:
+ *   p_t = softmax(target_logits[b][i] / temperature), p_d = draft_probs[b][i],
+ *   d = draft_tokens[b][i]; draft i is accepted iff p_d[d] > 0 and
+ *   u_i < p_t[d] / p_d[d], u_i the Philox uniform (key (seed[b], step[b]),
+ *   counter (i / 8, 1, 0, 0)).  At the first rejection the replacement token is
+ *   drawn from max(p_t - p_d, 0), normalised (Gumbel-max, counter
+ *   (v / 8, 2, i, 0); from p_t itself if that residual is zero everywhere) and
+ *   verification stops.  If all K are accepted, next_token = -1, or with
+ *   TTS_VERIFY_BONUS a token drawn from softmax(target_logits[b][K] /
+ *   temperature) (counter (v / 8, 2, K, 0)).
+ *  d_target_logits float [B][K+1][V];  d_draft_probs float [B][K][V]
+ *  d_draft_tokens int32 [B][K];  d_seed, d_step uint64 [B]
+ *  d_n_accepted, d_next_token int32 [B]
+ * A draft token outside [0, V) is rejected without a draw (next_token = -1,
+ * TTS_ERRBIT_TOKEN).  Requires 1 <= K <= 16 and temperature > 0. */
+int tts_spec_verify(const float *d_target_logits, const float *d_draft_probs,
+                    const int32_t *d_draft_tokens, int32_t B, int32_t K, int32_t V,
+                    float temperature, const uint64_t *d_seed, const uint64_t *d_step,
+                    int32_t flags, int32_t *d_n_accepted, int32_t *d_next_token,
+                    int32_t *d_err, void *stream);
+
+/* ----------------------------------------------------------------- misc */
+
+/* Static description of a status code. */
+const char *tts_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int tts_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TTS_DECODE_H */

@@ -95,10 +95,13 @@ class Oracle:
         return float(self.lib.orc_gumbel(int(seed), int(step), int(tag), int(pos), int(idx)))
 
     # ------------------------------------------------------------- append
-    def kv_append(self, k_pool, v_pool, block_table, ctx_before, k_new, v_new):
-        """Writes k_new/v_new [B][q_len][Hkv][D] into copies of the pools; returns them."""
-        k_pool = np.array(k_pool, copy=True, order="C")
-        v_pool = np.array(v_pool, copy=True, order="C")
+    def kv_append(self, k_pool, v_pool, block_table, ctx_before, k_new, v_new, inplace=False):
+        """Writes k_new/v_new [B][q_len][Hkv][D] into the pools (into copies unless
+        `inplace`, which needs C-contiguous arrays); returns them."""
+        if not inplace:
+            k_pool = np.array(k_pool, copy=True, order="C")
+            v_pool = np.array(v_pool, copy=True, order="C")
+        assert k_pool.flags["C_CONTIGUOUS"] and v_pool.flags["C_CONTIGUOUS"]
         num_blocks, Hkv, blk, D = k_pool.shape
         B, q_len = k_new.shape[:2]
         table = np.ascontiguousarray(block_table, dtype=np.int32)

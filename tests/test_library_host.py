@@ -1,0 +1,118 @@
+"""The C-ABI library on the host: it loads without a GPU, exports every
+declared symbol, runs the block pool, and rejects bad arguments before
+launching anything (CPU only; no compute call is made)."""
+import ctypes
+
+import pytest
+
+import decode_step_gb300 as pkg
+from decode_step_gb300 import _lib
+from decode_step_gb300.build import build
+
+
+@pytest.fixture(scope="module")
+def L():
+    build()
+    return pkg.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = pkg.declared_symbols()
+    assert len(names) >= 13
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+    assert L.tts_version() >= 100
+
+
+def test_status_strings(L):
+    for code in (0, -1, -2, -3, -4, -5):
+        assert L.tts_status_string(code)
+    assert L.tts_status_string(-99) == b"unknown status"
+
+
+def test_block_pool_lifo_all_or_nothing(L):
+    from decode_step_gb300.binding import BlockPool, TTSError
+    p = BlockPool(8)
+    a = p.alloc(3)
+    assert a == [0, 1, 2] and p.num_free == 5
+    with pytest.raises(TTSError) as e:
+        p.alloc(6)
+    assert e.value.code == -5 and p.num_free == 5     # exhausted, nothing taken
+    p.free([1])
+    assert p.alloc(1) == [1]                          # last freed, first reused
+    with pytest.raises(TTSError):
+        p.free([0, 0])                                # repeated id
+    with pytest.raises(TTSError):
+        p.free([2, 7])                                # 7 was never handed out
+    with pytest.raises(TTSError):
+        p.free([9])                                   # outside the pool
+    assert p.num_free == 5                            # failed frees changed nothing
+    p.free([0, 1, 2])
+    assert p.num_free == 8
+    assert sorted(p.alloc(8)) == list(range(8))
+    p.close()
+
+
+def test_block_pool_rejects_bad_create(L):
+    h = ctypes.c_void_p()
+    assert L.tts_block_pool_create(0, ctypes.byref(h)) == -1
+    assert L.tts_block_pool_create(5, None) == -1
+    assert L.tts_block_pool_num_free(None) == -1
+
+
+FAKE = ctypes.c_void_p(0x10000)   # never dereferenced: every call below fails validation first
+
+
+def _cache(num_blocks=8, hkv=8, d=128, dtype=1, block=16):
+    return _lib.KVCacheDesc(num_blocks, block, hkv, d, dtype, FAKE, FAKE)
+
+
+def test_workspace_queries(L):
+    assert L.tts_decode_attn_workspace_size(64, 1, 16, 8, 128, 1500) > 0
+    assert L.tts_decode_attn_workspace_size(64, 1, 15, 8, 128, 1500) == 0   # Hq % Hkv
+    assert L.tts_decode_attn_workspace_size(64, 9, 16, 8, 128, 1500) == 0   # 18 query rows
+    assert L.tts_head_workspace_size(0, 10) == 0
+    assert L.tts_head_workspace_size(64, 4097) >= 64 * 8
+
+
+def test_attention_argument_checks(L):
+    c = _cache()
+    args = lambda **k: dict(dict(cache=ctypes.byref(c), table=FAKE, maxb=94, ctx=FAKE, maxctx=1500,  # noqa: E731
+                                  B=4, q_len=1, Hq=16, scale=0.08, causal=0, q=FAKE, out=FAKE,
+                                  ws=FAKE, wsb=0, err=None, stream=None), **k)
+    def call(**k):
+        a = args(**k)
+        return L.tts_decode_attn(a["cache"], a["table"], a["maxb"], a["ctx"], a["maxctx"], a["B"],
+                                 a["q_len"], a["Hq"], a["scale"], a["causal"], a["q"], a["out"],
+                                 a["ws"], a["wsb"], a["err"], a["stream"])
+    assert call(q=None) == -1
+    assert call(Hq=12) == -1                      # not a multiple of Hkv
+    assert call(scale=-1.0) == -1
+    assert call(q_len=9) == -2                    # 18 rows per KV head
+    bad = _cache(d=96)
+    assert call(cache=ctypes.byref(bad)) == -2
+    bad = _cache(block=32)
+    assert call(cache=ctypes.byref(bad)) == -2
+    assert call(wsb=16) == -3                     # workspace too small
+    assert call(B=0, wsb=0) == 0                  # nothing to do
+
+
+def test_append_head_verify_argument_checks(L):
+    c = _cache()
+    assert L.tts_kv_append(ctypes.byref(c), FAKE, 4, None, 2, 1, FAKE, FAKE, None, None) == -1
+    assert L.tts_kv_append(ctypes.byref(c), FAKE, 4, FAKE, 2, 0, FAKE, FAKE, None, None) == -1
+    assert L.tts_kv_append(ctypes.byref(c), FAKE, 4, FAKE, 0, 1, FAKE, FAKE, None, None) == 0
+    head = lambda **k: L.tts_codebook_head_select(  # noqa: E731
+        k.get("h", FAKE), FAKE, k.get("dtype", 1), k.get("R", 4), k.get("H", 2048),
+        k.get("V", 4097), k.get("mode", 0), k.get("T", 0.0), k.get("seed", None), None, None,
+        FAKE, None, None, k.get("ws", FAKE), k.get("wsb", 0), None)
+    assert head(h=None) == -1
+    assert head(R=0) == -1
+    assert head(mode=1) == -1                     # Gumbel needs seeds and T > 0
+    assert head(dtype=5) == -2
+    assert head() == -3                           # workspace too small
+    assert head(H=100, wsb=1 << 20) == -2         # bf16 tensor-core path needs H % 64 == 0
+    ver = lambda **k: L.tts_spec_verify(  # noqa: E731
+        FAKE, FAKE, FAKE, 4, k.get("K", 4), 97, k.get("T", 0.7), FAKE, FAKE, k.get("flags", 0),
+        FAKE, FAKE, None, None)
+    assert ver(K=0) == -1 and ver(K=17) == -1 and ver(T=0.0) == -1 and ver(flags=2) == -1
