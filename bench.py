@@ -199,19 +199,20 @@ def oracle_stream_steps(orc, inp, streams, kp, vp):
 
 
 def cpu_baseline(inp, seconds: float) -> dict:
-    """The oracle, single-threaded, over as many whole streams as fit in `seconds`."""
+    """The oracle, single-threaded, over whole streams of the step (cycling
+    through the batch) until about `seconds` of CPU time are spent."""
     import oracle
     orc = oracle.default()
     w = inp["workload"]
     kp, vp = inp["k_pool"].copy(), inp["v_pool"].copy()
     done, t0 = 0, time.perf_counter()
-    while done < w.B and (done == 0 or time.perf_counter() - t0 < seconds):
-        oracle_stream_steps(orc, inp, [done], kp, vp)
+    while done == 0 or time.perf_counter() - t0 < seconds:
+        oracle_stream_steps(orc, inp, [done % w.B], kp, vp)
         done += 1
     dt = time.perf_counter() - t0
     return {"value": done * w.q_len / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{done} of {w.B} streams of one step (append, attention, head row), "
-                      f"single-threaded C oracle, {dt:.1f} s"}
+            "sample": f"{done} stream-steps (append, attention, head row) cycling over the "
+                      f"{w.B} streams of one step, single-threaded C oracle, {dt:.1f} s"}
 
 
 # ------------------------------------------------------------- reference arm

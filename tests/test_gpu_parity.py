@@ -77,8 +77,8 @@ def test_append_and_attention(orc, wid):
     check_attn(out, ref, w.dtype, w.name)
     assert int(err.item()) == 0
     # the ticket counters at the end of the workspace are back to zero
-    n_ctr = w.B * w.Hkv * 4
-    assert int(ws[-(-n_ctr // 256) * 256:].count_nonzero()) == 0
+    ctr_bytes = -(-(w.B * w.Hkv * 4) // 256) * 256
+    assert int(ws[ws.numel() - ctr_bytes:].count_nonzero()) == 0
 
 
 def _head_rows(w, limit):
