@@ -145,6 +145,21 @@ def tts_decode_attn(cache: KVCache, block_table, ctx_lens, max_ctx_len, q, out, 
     check("tts_decode_attn", lib().tts_decode_attn(*args))
 
 
+def tts_decode_attn_noalloc(cache: KVCache, block_table, ctx_lens, max_ctx_len, q, out, scale,
+                            causal=False, err=None, stream=None):
+    """tts_decode_attn without a workspace: for callers that cannot allocate
+    device memory (graph capture, fully reserved memory); uses the library's
+    16 MiB static scratch, shared by all calls."""
+    B, max_blocks = block_table.shape
+    _, q_len, Hq, D = q.shape
+    args = (ctypes.byref(cache.desc), _dev(block_table, "block_table", torch.int32), max_blocks,
+            _dev(ctx_lens, "ctx_lens", torch.int32, (B,)), int(max_ctx_len), B, q_len, Hq,
+            float(scale), int(bool(causal)), _dev(q, "q", cache.dtype, (B, q_len, Hq, cache.head_dim)),
+            _dev(out, "out", cache.dtype, (B, q_len, Hq, cache.head_dim)),
+            None if err is None else _dev(err, "err", torch.int32), _stream(stream))
+    check("tts_decode_attn_noalloc", lib().tts_decode_attn_noalloc(*args))
+
+
 def tts_head_workspace_size(R, V) -> int:
     return int(lib().tts_head_workspace_size(R, V))
 

@@ -28,6 +28,8 @@
 //    atomic ticket, no waiting — merges the splits (log-sum-exp combine) and
 //    writes the output.  A stream with a single split writes its output
 //    directly.
+#include <mutex>
+
 #include "tts_common.cuh"
 #include "tts_internal.h"
 
@@ -503,4 +505,84 @@ extern "C" int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block
     auto s = static_cast<cudaStream_t>(stream);
     return cache->dtype == TTS_BF16 ? launch_typed<__nv_bfloat16>(a, sp.rows, grid, s)
                                     : launch_typed<float>(a, sp.rows, grid, s);
+}
+
+// ---------------------------------------------------------------------------
+// Decode attention without a caller workspace.
+//
+// Some callers cannot allocate device memory where they run a decode step:
+// code that runs while a CUDA graph is being captured (an allocation there
+// breaks the capture), engines that reserve all free device memory for the KV
+// pool at start-up and so leave nothing for cudaMalloc, hosts that hand a
+// plugin no allocator, and real-time loops that cannot afford the implicit
+// synchronisation and unbounded latency of cudaMalloc / cudaFree inside a
+// frame deadline.  For them the split-KV partials live in one file-scope
+// device array of fixed size instead of a caller workspace.  Every GPU that
+// loads this library holds the array until the process exits.
+
+namespace tts {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_attn_scratch[kStaticScratchBytes];
+
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_attn_scratch on the current device.  The symbol's name
+// in host code is only a host-side handle, so the address is looked up once
+// per device (with that device current) and cached.
+int static_scratch_address(void **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return TTS_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return TTS_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return TTS_ERR_CUDA;
+        }
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return TTS_OK;
+}
+
+}  // namespace
+}  // namespace tts
+
+extern "C" int tts_decode_attn_noalloc(const tts_kv_cache *cache, const int32_t *d_block_table,
+                                       int32_t max_blocks_per_seq, const int32_t *d_ctx_lens,
+                                       int32_t max_ctx_len, int32_t B, int32_t q_len,
+                                       int32_t num_q_heads, float scale, int32_t causal,
+                                       const void *d_q, void *d_out, int32_t *d_err, void *stream) {
+    using namespace tts;
+    if (!cache) return TTS_ERR_INVALID;
+    const size_t need = tts_decode_attn_workspace_size(B, q_len, num_q_heads, cache->num_kv_heads,
+                                                       cache->head_dim, max_ctx_len);
+    if (B == 0 || need == 0)  // nothing to run, or arguments the regular entry point rejects
+        return tts_decode_attn(cache, d_block_table, max_blocks_per_seq, d_ctx_lens, max_ctx_len, B,
+                               q_len, num_q_heads, scale, causal, d_q, d_out, nullptr, 0, d_err,
+                               stream);
+    if (need > kStaticScratchBytes) return TTS_ERR_SCRATCH_LIMIT;
+    void *scratch = nullptr;
+    const int st = static_scratch_address(&scratch);
+    if (st != TTS_OK) return st;
+    // The split tickets must start at zero; they sit at the end of the
+    // workspace layout.  The array keeps whatever the previous call left.
+    const size_t tickets = align_up(static_cast<size_t>(B) * cache->num_kv_heads * sizeof(int32_t), 256);
+    if (cudaMemsetAsync(static_cast<uint8_t *>(scratch) + need - tickets, 0, tickets,
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return TTS_ERR_CUDA;
+    }
+    return tts_decode_attn(cache, d_block_table, max_blocks_per_seq, d_ctx_lens, max_ctx_len, B,
+                           q_len, num_q_heads, scale, causal, d_q, d_out, scratch, need, d_err,
+                           stream);
 }

@@ -92,6 +92,7 @@ extern "C" const char *tts_status_string(int status) {
         case TTS_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
         case TTS_ERR_CUDA: return "CUDA error";
         case TTS_ERR_POOL_EXHAUSTED: return "block pool exhausted";
+        case TTS_ERR_SCRATCH_LIMIT: return "request exceeds the library's static scratch";
         default: return "unknown status";
     }
 }

@@ -55,7 +55,8 @@ typedef enum {
     TTS_ERR_UNSUPPORTED = -2,      /* a shape or type this build has no kernel for */
     TTS_ERR_WORKSPACE = -3,        /* workspace missing, misaligned or too small */
     TTS_ERR_CUDA = -4,             /* a CUDA launch or runtime call failed */
-    TTS_ERR_POOL_EXHAUSTED = -5    /* block pool has too few free blocks */
+    TTS_ERR_POOL_EXHAUSTED = -5,   /* block pool has too few free blocks */
+    TTS_ERR_SCRATCH_LIMIT = -6     /* request larger than the library's static scratch */
 } tts_status;
 
 enum { TTS_F32 = 0, TTS_BF16 = 1 };             /* element types */
@@ -159,6 +160,29 @@ int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block_table,
                     int32_t B, int32_t q_len, int32_t num_q_heads, float scale, int32_t causal,
                     const void *d_q, void *d_out, void *d_ws, size_t ws_bytes, int32_t *d_err,
                     void *stream);
+
+/* Decode attention with no caller workspace and no allocation.
+ * The pages have no counterpart for this entry point; it exists for callers
+ * that cannot allocate device memory where they run a decode step: code
+ * running while a CUDA graph is captured (an allocation breaks the capture),
+ * engines that reserve all free device memory for the KV pool at start-up,
+ * plugin hosts that give a library no allocator, and real-time loops that
+ * cannot absorb cudaMalloc's implicit synchronisation inside a frame budget.
+ * Same arguments and results as tts_decode_attn, without d_ws / ws_bytes.
+ * The split partials live in one 16 MiB file-scope device array that every
+ * GPU loading this library holds until the process exits; a request whose
+ * tts_decode_attn_workspace_size exceeds 16 MiB returns TTS_ERR_SCRATCH_LIMIT
+ * and launches nothing.  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress), so make that first call before any
+ * stream capture.  Every call shares the one array and it keeps the previous
+ * call's contents: each call clears the part that must start at zero, and
+ * calls whose executions overlap on the GPU (other streams, other threads)
+ * race on it.  Calls no cudaMalloc / cudaFree. */
+int tts_decode_attn_noalloc(const tts_kv_cache *cache, const int32_t *d_block_table,
+                            int32_t max_blocks_per_seq, const int32_t *d_ctx_lens,
+                            int32_t max_ctx_len, int32_t B, int32_t q_len, int32_t num_q_heads,
+                            float scale, int32_t causal, const void *d_q, void *d_out,
+                            int32_t *d_err, void *stream);
 
 /* ------------------------------------------------------------------ head */
 
