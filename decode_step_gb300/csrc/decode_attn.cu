@@ -8,26 +8,31 @@
 //   out[b][j][h] = sum_t softmax_t(scale * q[b][j][h] . k_t) v_t,
 // t over the stream's tokens below the row's limit, KV head h / group.
 //
-// How (HBM-bound: each cached byte is used for 2 flops per query row):
-//  - grid (split, KV head, stream); a split is `split_blocks` 16-token blocks.
-//    Every query row of the KV head's group (group x q_len rows) is served by
-//    one read of each K/V tile.
-//  - each warp owns every 4th block of the split and streams its (block, head)
-//    K and V tiles (4 KB each, contiguous in the pool) into a private 2-stage
-//    shared-memory ring with bulk TMA copies (L2 evict-first), completion on
-//    per-stage mbarriers.
-//  - lane (p, c) = (lane / 16, lane % 16) reads 16-byte chunk c of the rows of
-//    tokens p, p + 2, ..., p + 14 (conflict-free 128-bit shared loads).  Dot
-//    products are reduced across the 16 chunk lanes by recursive halving (each
-//    shuffle round halves the values a lane carries), leaving every lane the
-//    full scores of one token for half of the rows.  Online softmax in the
-//    log2 domain with warp-shuffle max reductions; P.V accumulates per lane
-//    into its 16-byte slice of the output rows.
-//  - warps merge in shared memory; a split writes (m, l, unnormalised o) to
-//    the workspace, and the last CTA of a (stream, KV head) — found with an
-//    atomic ticket, no waiting — merges the splits (log-sum-exp combine) and
-//    writes the output.  A stream with a single split writes its output
-//    directly.
+// How (HBM-bound: each cached byte feeds 2 flops per query row):
+//  - The work is the flat list of (stream, KV head, 16-token block) tiles,
+//    stream-major.  A persistent grid of warps splits that list into equal
+//    contiguous ranges (a warp-granular stream-K schedule), so every warp
+//    streams the same number of tiles whatever the context-length mix, and a
+//    (stream, KV head) "segment" is split across warps only where a range
+//    boundary falls inside it.  Each CTA first scans the context lengths into
+//    a per-stream tile prefix in shared memory.
+//  - Each warp streams its tiles' K and V (4 KB each, contiguous in the pool)
+//    through a private 2-stage shared-memory ring with bulk TMA copies (L2
+//    evict-first), completion on per-stage mbarriers; the query rows of a new
+//    segment ride along in the same stage.  Block ids are fetched 32 tiles at
+//    a time, one batch ahead.
+//  - Lane (p, c) = (lane / 16, lane % 16) reads 16-byte chunk c of the rows
+//    of tokens p, p + 2, ..., p + 14 (conflict-free 128-bit shared loads).
+//    Dot products are reduced across the 16 chunk lanes by recursive halving
+//    (each shuffle round halves the values a lane carries), leaving every lane
+//    the full scores of one token for half of the query rows.  Online softmax
+//    in the log2 domain with warp-shuffle max reductions; P.V accumulates per
+//    lane into its 16-byte slice of the output rows.  All group x q_len query
+//    rows of a KV head share one read of each tile.
+//  - A segment wholly inside a warp's range is written out directly.  A split
+//    segment's warps write (m, l, unnormalised o) partials; the last of them
+//    to finish (an atomic ticket, never a wait) merges the partials with a
+//    log-sum-exp combine and writes the output.
 #include <mutex>
 
 #include "tts_common.cuh"
@@ -40,7 +45,7 @@ constexpr int kWarps = 4;          // warps per CTA
 constexpr int kStages = 2;         // pipeline depth per warp
 constexpr int kTileBytes = 4096;   // one (block, KV head) tile of K or V: 16 tokens x 256 B
 constexpr int kRowBytes = 256;     // one token's key (or value) row
-constexpr int kSplitBlocks = 16;   // blocks per split (<= 32 * kWarps)
+constexpr int kMaxStreams = 4096;  // streams per call (shared-memory prefix table)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegBig = -1e30f;  // finite "minus infinity" for running maxima
 constexpr unsigned kFull = 0xFFFFFFFFu;
@@ -54,32 +59,37 @@ struct AttnArgs {
     int max_blocks;
     const int32_t *ctx_lens;
     int max_ctx;
+    int B;
     int q_len;
     int Hq;
     int group;
     int causal;
-    float qscale;  // softmax scale * log2(e)
-    const void *q;
+    float qscale;       // softmax scale * log2(e)
+    const uint8_t *q;
     void *out;
-    float *o_part;   // [B][Hkv][max_splits][NR][D]
-    float2 *ml_part; // [B][Hkv][max_splits][NR]  (running max, sum)
-    int32_t *counters;  // [B][Hkv]
-    int max_splits;
-    int split_blocks;
+    float *part;        // [workers][2][NR * D + 2 * NR]: o, m, l of split segments
+    int32_t *counters;  // [B][Hkv] tickets of split segments
+    int workers;
     int32_t *err;
 };
 
 template <int NR, int D>
 struct AttnSmem {
-    static constexpr size_t stages = size_t(kWarps) * kStages * 2 * kTileBytes;
-    static constexpr size_t bars = stages;
+    static constexpr int stage_bytes = 2 * kTileBytes + NR * kRowBytes;  // K, V, query rows
+    static constexpr size_t stages = 0;
+    static constexpr size_t bars = stages + size_t(kWarps) * kStages * stage_bytes;
     static constexpr size_t pbuf = bars + 8 * kWarps * kStages;
-    static constexpr size_t ms = pbuf + 4 * kWarps * 16 * NR;
-    static constexpr size_t ls = ms + 4 * kWarps * NR;
-    static constexpr size_t os = ls + 4 * kWarps * NR;
-    static constexpr size_t flag = os + 4 * size_t(kWarps) * NR * D;
-    static constexpr size_t total = flag + 16;
+    static constexpr size_t prefix = pbuf + 4 * kWarps * 16 * NR;
+    // then: int prefix[B + 1], int ctxs[B], int scan[kWarps]
+    static size_t total(int B) { return prefix + 4 * (2 * size_t(B) + 1 + kWarps); }
 };
+
+__device__ __forceinline__ int warp_of_tile(long long t, long long T, long long W) {
+    return static_cast<int>(((t + 1) * W - 1) / T);
+}
+__device__ __forceinline__ long long range_start(long long w, long long T, long long W) {
+    return w * T / W;
+}
 
 template <typename T, int NR>
 __global__ void __launch_bounds__(kWarps * 32, NR <= 4 ? 3 : 1)
@@ -88,43 +98,70 @@ decode_attn_kernel(const AttnArgs a) {
     constexpr int EPC = C::N;          // elements per 16-byte chunk
     constexpr int D = 16 * EPC;        // head dim: one 256-byte row per token
     constexpr int HALF = NR / 2;
+    constexpr int SF = NR * D + 2 * NR;  // floats per partial slot
     using S = AttnSmem<NR, D>;
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::bars);
-    float *ms = reinterpret_cast<float *>(smem + S::ms);
-    float *ls = reinterpret_cast<float *>(smem + S::ls);
-    float *os = reinterpret_cast<float *>(smem + S::os);
-    int *flag = reinterpret_cast<int *>(smem + S::flag);
+    int *prefix = reinterpret_cast<int *>(smem + S::prefix);  // [B + 1], in tiles
+    int *ctxs = prefix + a.B + 1;                              // [B], 0 for an invalid stream
+    int *scan = ctxs + a.B;                                    // [kWarps]
 
-    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_rows = a.group * a.q_len;
-    T *out = static_cast<T *>(a.out);
-    auto out_ptr = [&](int r) -> T * {
-        const int j = r / a.group, hh = r % a.group;
-        return out + ((static_cast<size_t>(b) * a.q_len + j) * a.Hq + g * a.group + hh) * D;
-    };
-
-    const int L = __ldg(a.ctx_lens + b);
     const int cap = min(a.max_ctx, a.max_blocks * TTS_BLOCK_TOKENS);
-    if (L < a.q_len || L > cap) {
-        if (split == 0) {
-            if (g == 0 && threadIdx.x == 0) flag_error(a.err, TTS_ERRBIT_CTX_LEN);
-            for (int i = threadIdx.x; i < n_rows * D; i += blockDim.x)
-                store_elem(out_ptr(i / D) + i % D, 0.0f);
-        }
-        return;
-    }
-    const int nblk = (L + TTS_BLOCK_TOKENS - 1) / TTS_BLOCK_TOKENS;
-    const int n_split = (nblk + a.split_blocks - 1) / a.split_blocks;
-    if (split >= n_split) return;
-    const int blk0 = split * a.split_blocks;
-    const int blk1 = min(nblk, blk0 + a.split_blocks);
-    const int my_first = blk0 + warp;
-    const int my_n = my_first < blk1 ? (blk1 - my_first + kWarps - 1) / kWarps : 0;
+    T *out = static_cast<T *>(a.out);
+    const size_t row_stride = static_cast<size_t>(a.Hq) * D;  // elements between query positions
 
-    const uint32_t stage0 = smem_addr(smem) + warp * kStages * 2 * kTileBytes;
-    const uint32_t bar0 = smem_addr(bars + warp * kStages);
+    // ---- 1. context lengths -> per-stream tile prefix (x Hkv, stream-major)
+    {
+        const int per = (a.B + blockDim.x - 1) / blockDim.x;
+        const int i0 = threadIdx.x * per, i1 = min(a.B, i0 + per);
+        int local = 0;
+        for (int i = i0; i < i1; ++i) {
+            const int L = __ldg(a.ctx_lens + i);
+            const bool ok = L >= a.q_len && L <= cap;
+            ctxs[i] = ok ? L : 0;
+            local += ok ? (L + TTS_BLOCK_TOKENS - 1) / TTS_BLOCK_TOKENS : 0;
+            if (!ok && blockIdx.x == 0) {
+                flag_error(a.err, TTS_ERRBIT_CTX_LEN);
+                T *o = out + static_cast<size_t>(i) * a.q_len * row_stride;
+                for (size_t e = 0; e < a.q_len * row_stride; ++e) store_elem(o + e, 0.0f);
+            }
+        }
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) scan[warp] = incl;
+        __syncthreads();
+        int run = incl - local, total = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            if (w < warp) run += scan[w];
+            total += scan[w];
+        }
+        for (int i = i0; i < i1; ++i) {
+            prefix[i] = run * a.Hkv;
+            run += ctxs[i] ? (ctxs[i] + TTS_BLOCK_TOKENS - 1) / TTS_BLOCK_TOKENS : 0;
+        }
+        if (threadIdx.x == 0) prefix[a.B] = total * a.Hkv;
+        __syncthreads();
+    }
+
+    // ---- 2. this warp's tile range
+    // Every participating warp gets at least one tile (warps beyond the tile
+    // count sit out), so a split segment's contributors are consecutive warps.
+    const long long Ttot = prefix[a.B];
+    const long long Wtot = min(static_cast<long long>(a.workers), Ttot);
+    const int wid = blockIdx.x * kWarps + warp;
+    if (Ttot == 0 || wid >= Wtot) return;
+    const int t0 = static_cast<int>(range_start(wid, Ttot, Wtot));
+    const int t1 = static_cast<int>(range_start(wid + 1, Ttot, Wtot));
+    const int n = t1 - t0;
+    if (n <= 0) return;
+
+    const uint32_t stage0 = smem_addr(smem + S::stages) + warp * kStages * S::stage_bytes;
+    const uint32_t bar0 = smem_addr(smem + S::bars) + 8 * warp * kStages;
     float *pbuf = reinterpret_cast<float *>(smem + S::pbuf) + warp * 16 * NR;
     if (lane == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
@@ -132,75 +169,173 @@ decode_attn_kernel(const AttnArgs a) {
     }
     __syncwarp();
 
-    // Physical block of this warp's i-th tile, held by lane i (-1: invalid).
-    int my_id = -1;
-    if (lane < my_n) {
-        const int id = __ldg(a.table + static_cast<size_t>(b) * a.max_blocks + my_first + lane * kWarps);
-        if (id >= 0 && id < a.num_blocks)
-            my_id = id;
-        else
-            flag_error(a.err, TTS_ERRBIT_BLOCK_ID);
-    }
+    // Tile metadata, 32 tiles per batch (lane i holds tile 32 k + i of the
+    // range): raw block id (validated when used), segment = stream * Hkv + head,
+    // block index within the stream.
+    auto load_meta = [&](int k, int &id, int &seg, int &blk) {
+        const int t = t0 + 32 * k + lane;
+        id = -1;
+        seg = -1;
+        blk = 0;
+        if (t < t1) {
+            int lo = 0, hi = a.B;  // prefix[lo] <= t < prefix[hi]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (prefix[mid] <= t) lo = mid; else hi = mid;
+            }
+            const int nb = (prefix[lo + 1] - prefix[lo]) / a.Hkv;
+            const int r = t - prefix[lo];
+            const int g = r / nb;
+            blk = r - g * nb;
+            seg = lo * a.Hkv + g;
+            id = __ldg(a.table + static_cast<size_t>(lo) * a.max_blocks + blk);
+        }
+    };
+    int cur_id, cur_seg, cur_blk, nxt_id = -1, nxt_seg = -1, nxt_blk = 0;
+    load_meta(0, cur_id, cur_seg, cur_blk);
+    if (n > 32) load_meta(1, nxt_id, nxt_seg, nxt_blk);
+    int kc = 0;  // batch of the tile being computed
 
     const uint64_t policy = l2_evict_first_policy();
-    auto issue = [&](int i) {
-        const int id = __shfl_sync(kFull, my_id, i);
+    const int qbytes_per_pos = a.group * D * static_cast<int>(sizeof(T));
+    auto issue = [&](int j) {
+        const bool in_cur = (j >> 5) == kc;
+        const int src = j & 31;
+        int id = __shfl_sync(kFull, in_cur ? cur_id : nxt_id, src);
+        const int seg = __shfl_sync(kFull, in_cur ? cur_seg : nxt_seg, src);
+        const int blk = __shfl_sync(kFull, in_cur ? cur_blk : nxt_blk, src);
         if (lane == 0) {
-            const int st = i % kStages;
+            if (id < 0 || id >= a.num_blocks) {
+                flag_error(a.err, TTS_ERRBIT_BLOCK_ID);
+                id = -1;
+            }
+            const int st = j % kStages;
             const uint32_t bar = bar0 + 8 * st;
-            if (id >= 0) {
-                const size_t off = (static_cast<size_t>(id) * a.Hkv + g) * kTileBytes;
-                mbar_arrive_expect_tx(bar, 2 * kTileBytes);
-                bulk_load(stage0 + st * 2 * kTileBytes, a.k_pool + off, kTileBytes, bar, policy);
-                bulk_load(stage0 + st * 2 * kTileBytes + kTileBytes, a.v_pool + off, kTileBytes, bar,
-                          policy);
-            } else {
+            const uint32_t dst = stage0 + st * S::stage_bytes;
+            const bool need_q = j == 0 || blk == 0;
+            const uint32_t bytes = (id >= 0 ? 2 * kTileBytes : 0) + (need_q ? a.q_len * qbytes_per_pos : 0);
+            if (bytes == 0) {
                 mbar_arrive(bar);
+            } else {
+                mbar_arrive_expect_tx(bar, bytes);
+                if (id >= 0) {
+                    const size_t off = (static_cast<size_t>(id) * a.Hkv + seg % a.Hkv) * kTileBytes;
+                    bulk_load(dst, a.k_pool + off, kTileBytes, bar, policy);
+                    bulk_load(dst + kTileBytes, a.v_pool + off, kTileBytes, bar, policy);
+                }
+                if (need_q) {
+                    const int b = seg / a.Hkv, g = seg % a.Hkv;
+                    for (int jq = 0; jq < a.q_len; ++jq) {
+                        const size_t qoff =
+                            ((static_cast<size_t>(b) * a.q_len + jq) * a.Hq + g * a.group) * D * sizeof(T);
+                        bulk_load_nohint(dst + 2 * kTileBytes + jq * qbytes_per_pos, a.q + qoff,
+                                         qbytes_per_pos, bar);
+                    }
+                }
             }
         }
     };
-    const int n_pre = min(kStages, my_n);
-    for (int i = 0; i < n_pre; ++i) issue(i);
+    for (int j = 0; j < min(kStages, n); ++j) issue(j);
 
-    // Query rows at this lane's chunk, pre-scaled into the log2 domain.
     const int p = lane >> 4, c = lane & 15;
-    float q[NR][EPC];
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-        if (r < n_rows) {
-            const int j = r / a.group, hh = r % a.group;
-            const T *src = static_cast<const T *>(a.q) +
-                           ((static_cast<size_t>(b) * a.q_len + j) * a.Hq + g * a.group + hh) * D +
-                           c * EPC;
-            C::unpack(__ldg(reinterpret_cast<const uint4 *>(src)), q[r]);
-#pragma unroll
-            for (int e = 0; e < EPC; ++e) q[r][e] *= a.qscale;
-        } else {
-#pragma unroll
-            for (int e = 0; e < EPC; ++e) q[r][e] = 0.0f;
-        }
-    }
-    // This lane scores token (p + 2 * ((lane >> 1) & 7)) of a tile for rows
-    // (lane & 1) * HALF + k; the row's visible-token limit:
-    int lim[HALF];
-#pragma unroll
-    for (int k = 0; k < HALF; ++k) {
-        const int r = (lane & 1) * HALF + k;
-        lim[k] = r < n_rows ? (a.causal ? L - a.q_len + r / a.group + 1 : L) : 0;
-    }
     const int my_tok = p + 2 * ((lane >> 1) & 7);
+    // State of the current segment.
+    int seg_id = -1, seg_b = 0, seg_g = 0, seg_L = 0, s0 = 0, s1 = 0;
+    int lim[HALF];
+    float q[NR][EPC], m_run[HALF], l_run[HALF], o[NR][EPC];
 
-    float m_run[HALF], l_run[HALF], o[NR][EPC];
+    auto flush = [&]() {
+        float l_tot[HALF], l_oth[HALF];
 #pragma unroll
-    for (int k = 0; k < HALF; ++k) { m_run[k] = kNegBig; l_run[k] = 0.0f; }
+        for (int k = 0; k < HALF; ++k) {
+            float l = l_run[k];
+            l += __shfl_xor_sync(kFull, l, 2);
+            l += __shfl_xor_sync(kFull, l, 4);
+            l += __shfl_xor_sync(kFull, l, 8);
+            l += __shfl_xor_sync(kFull, l, 16);
+            l_tot[k] = l;
+            l_oth[k] = __shfl_xor_sync(kFull, l, 1);
+        }
 #pragma unroll
-    for (int r = 0; r < NR; ++r)
+        for (int r = 0; r < NR; ++r)
 #pragma unroll
-        for (int e = 0; e < EPC; ++e) o[r][e] = 0.0f;
+            for (int e = 0; e < EPC; ++e) o[r][e] += __shfl_xor_sync(kFull, o[r][e], 16);
+        if (s0 >= t0 && s1 <= t1) {
+            // whole segment in this warp: write the output
+            if (lane < 16) {
+#pragma unroll
+                for (int r = 0; r < NR; ++r) {
+                    if (r >= n_rows) break;
+                    const float l = (r / HALF) == (lane & 1) ? l_tot[r % HALF] : l_oth[r % HALF];
+                    const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+                    const int j = r / a.group, hh = r % a.group;
+                    T *dst = out + (static_cast<size_t>(seg_b) * a.q_len + j) * row_stride +
+                             static_cast<size_t>(seg_g * a.group + hh) * D + c * EPC;
+#pragma unroll
+                    for (int e = 0; e < EPC; ++e) store_elem(dst + e, o[r][e] * inv);
+                }
+            }
+            return;
+        }
+        // split segment: publish this warp's partial, the last contributor merges
+        const int slot = s0 <= t0 ? 0 : 1;
+        float *part = a.part + (static_cast<size_t>(wid) * 2 + slot) * SF;
+        if (lane < 16) {
+#pragma unroll
+            for (int r = 0; r < NR; ++r)
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) part[r * D + c * EPC + e] = o[r][e];
+        }
+        if (lane < 2) {
+#pragma unroll
+            for (int k = 0; k < HALF; ++k) {
+                part[NR * D + lane * HALF + k] = m_run[k];
+                part[NR * D + NR + lane * HALF + k] = l_tot[k];
+            }
+        }
+        __threadfence();
+        __syncwarp();
+        const int w_first = warp_of_tile(s0, Ttot, Wtot);
+        const int w_last = warp_of_tile(s1 - 1, Ttot, Wtot);
+        int last = 0;
+        if (lane == 0) last = atomicAdd(a.counters + seg_id, 1) == w_last - w_first;
+        if (!__shfl_sync(kFull, last, 0)) return;
+        __threadfence();
+        const bool first_shifted = range_start(w_first, Ttot, Wtot) != s0;
+        for (int r = p; r < n_rows; r += 2) {
+            float M = kNegBig;
+            for (int w2 = w_first; w2 <= w_last; ++w2) {
+                const float *pp = a.part + (static_cast<size_t>(w2) * 2 + (w2 == w_first && first_shifted)) * SF;
+                M = fmaxf(M, __ldcg(pp + NR * D + r));
+            }
+            float Ls = 0.0f, O[EPC];
+#pragma unroll
+            for (int e = 0; e < EPC; ++e) O[e] = 0.0f;
+            for (int w2 = w_first; w2 <= w_last; ++w2) {
+                const float *pp = a.part + (static_cast<size_t>(w2) * 2 + (w2 == w_first && first_shifted)) * SF;
+                const float f = exp2f(__ldcg(pp + NR * D + r) - M);
+                Ls = fmaf(__ldcg(pp + NR * D + NR + r), f, Ls);
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) O[e] = fmaf(__ldcg(pp + r * D + c * EPC + e), f, O[e]);
+            }
+            const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
+            const int j = r / a.group, hh = r % a.group;
+            T *dst = out + (static_cast<size_t>(seg_b) * a.q_len + j) * row_stride +
+                     static_cast<size_t>(seg_g * a.group + hh) * D + c * EPC;
+#pragma unroll
+            for (int e = 0; e < EPC; ++e) store_elem(dst + e, O[e] * inv);
+        }
+        if (lane == 0) a.counters[seg_id] = 0;
+    };
 
     bool timed_out = false;
-    int waited = 0;  // tiles whose copies are known complete
-    for (int i = 0; i < my_n; ++i) {
+    int waited = 0;
+    for (int i = 0; i < n; ++i) {
+        if ((i & 31) == 0 && i > 0) {
+            kc = i >> 5;
+            cur_id = nxt_id; cur_seg = nxt_seg; cur_blk = nxt_blk;
+            if (n > 32 * (kc + 1)) load_meta(kc + 1, nxt_id, nxt_seg, nxt_blk);
+        }
         const int st = i % kStages;
         if (!timed_out) {
             const bool ok = mbar_wait(bar0 + 8 * st, (i / kStages) & 1);
@@ -211,10 +346,45 @@ decode_attn_kernel(const AttnArgs a) {
                 waited = i + 1;
             }
         }
-        const int id = __shfl_sync(kFull, my_id, i);
-        if (!timed_out && id >= 0) {
-            const uint32_t ks = stage0 + st * 2 * kTileBytes, vs = ks + kTileBytes;
-            const int base = (my_first + i * kWarps) * TTS_BLOCK_TOKENS;
+        const int src = i & 31;
+        const int t_id = __shfl_sync(kFull, cur_id, src);
+        const int t_seg = __shfl_sync(kFull, cur_seg, src);
+        const int t_blk = __shfl_sync(kFull, cur_blk, src);
+        const uint32_t ks = stage0 + st * S::stage_bytes, vs = ks + kTileBytes;
+        if (i == 0 || t_blk == 0) {
+            // ---- a new segment: finish the previous one, set up this one
+            if (i > 0) flush();
+            seg_id = t_seg;
+            seg_b = t_seg / a.Hkv;
+            seg_g = t_seg % a.Hkv;
+            seg_L = ctxs[seg_b];
+            const int nb = (seg_L + TTS_BLOCK_TOKENS - 1) / TTS_BLOCK_TOKENS;
+            s0 = prefix[seg_b] + seg_g * nb;
+            s1 = s0 + nb;
+#pragma unroll
+            for (int k = 0; k < HALF; ++k) {
+                const int r = (lane & 1) * HALF + k;
+                lim[k] = r < n_rows ? (a.causal ? seg_L - a.q_len + r / a.group + 1 : seg_L) : 0;
+                m_run[k] = kNegBig;
+                l_run[k] = 0.0f;
+            }
+            const uint32_t qs = ks + 2 * kTileBytes;
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                if (r < n_rows && !timed_out) {
+                    C::unpack(lds128(qs + r * kRowBytes + c * 16), q[r]);
+#pragma unroll
+                    for (int e = 0; e < EPC; ++e) q[r][e] *= a.qscale;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < EPC; ++e) q[r][e] = 0.0f;
+                }
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) o[r][e] = 0.0f;
+            }
+        }
+        if (!timed_out && t_id >= 0 && t_id < a.num_blocks) {
+            const int base = t_blk * TTS_BLOCK_TOKENS;
             // ---- scores: partial dots over this lane's chunk, 8 tokens x NR rows
             float acc[8 * NR];
 #pragma unroll
@@ -233,12 +403,12 @@ decode_attn_kernel(const AttnArgs a) {
 #pragma unroll
             for (int step = 0; step < 4; ++step) {
                 const int m = 8 >> step;
-                const int n = (8 * NR) >> step;
+                const int nv = (8 * NR) >> step;
                 const bool upper = (lane & m) != 0;
 #pragma unroll
-                for (int x = 0; x < n / 2; ++x) {
-                    const float send = upper ? acc[x] : acc[x + n / 2];
-                    const float keep = upper ? acc[x + n / 2] : acc[x];
+                for (int x = 0; x < nv / 2; ++x) {
+                    const float send = upper ? acc[x] : acc[x + nv / 2];
+                    const float keep = upper ? acc[x + nv / 2] : acc[x];
                     acc[x] = keep + __shfl_xor_sync(kFull, send, m);
                 }
             }
@@ -274,7 +444,7 @@ decode_attn_kernel(const AttnArgs a) {
             for (int jt = 0; jt < 8; ++jt) {
                 const int t = p + 2 * jt;
                 uint4 raw = lds128(vs + t * kRowBytes + c * 16);
-                if (base + t >= L) raw = make_uint4(0u, 0u, 0u, 0u);  // past the context
+                if (base + t >= seg_L) raw = make_uint4(0u, 0u, 0u, 0u);  // past the context
                 float vf[EPC];
                 C::unpack(raw, vf);
                 const float *pr = pbuf + t * NR;
@@ -287,91 +457,14 @@ decode_attn_kernel(const AttnArgs a) {
             }
         }
         __syncwarp();
-        if (!timed_out && i + kStages < my_n) issue(i + kStages);
+        if (!timed_out && i + kStages < n) issue(i + kStages);
     }
+    flush();
     if (timed_out) {
         // Let copies still in flight land before the CTA's shared memory goes away.
-        const int issued = min(my_n, waited + kStages);
+        const int issued = min(n, waited + kStages);
         for (int i = waited; i < issued; ++i) mbar_wait(bar0 + 8 * (i % kStages), (i / kStages) & 1);
     }
-
-    // ---- warp totals: sums over the 16 lanes of a row half, outputs over parity
-    float l_tot[HALF];
-#pragma unroll
-    for (int k = 0; k < HALF; ++k) {
-        float l = l_run[k];
-        l += __shfl_xor_sync(kFull, l, 2);
-        l += __shfl_xor_sync(kFull, l, 4);
-        l += __shfl_xor_sync(kFull, l, 8);
-        l += __shfl_xor_sync(kFull, l, 16);
-        l_tot[k] = l;
-    }
-#pragma unroll
-    for (int r = 0; r < NR; ++r)
-#pragma unroll
-        for (int e = 0; e < EPC; ++e) o[r][e] += __shfl_xor_sync(kFull, o[r][e], 16);
-    if (lane < 2) {
-#pragma unroll
-        for (int k = 0; k < HALF; ++k) {
-            ms[warp * NR + lane * HALF + k] = m_run[k];
-            ls[warp * NR + lane * HALF + k] = l_tot[k];
-        }
-    }
-    if (lane < 16) {
-#pragma unroll
-        for (int r = 0; r < NR; ++r)
-#pragma unroll
-            for (int e = 0; e < EPC; ++e) os[(warp * NR + r) * D + lane * EPC + e] = o[r][e];
-    }
-    __syncthreads();
-
-    // ---- merge the warps of this split
-    const size_t part = (static_cast<size_t>(b) * a.Hkv + g) * a.max_splits;
-    for (int idx = threadIdx.x; idx < n_rows * D; idx += blockDim.x) {
-        const int r = idx / D, d = idx % D;
-        float M = kNegBig;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ms[w * NR + r]);
-        float Ls = 0.0f, O = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const float f = exp2f(ms[w * NR + r] - M);
-            Ls = fmaf(ls[w * NR + r], f, Ls);
-            O = fmaf(os[(w * NR + r) * D + d], f, O);
-        }
-        if (n_split == 1) {
-            store_elem(out_ptr(r) + d, Ls > 0.0f ? O / Ls : 0.0f);
-        } else {
-            a.o_part[((part + split) * NR + r) * D + d] = O;
-            if (d == 0) a.ml_part[(part + split) * NR + r] = make_float2(M, Ls);
-        }
-    }
-    if (n_split == 1) return;
-
-    // ---- last split to finish merges all splits (log-sum-exp combine)
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const int ticket = atomicAdd(a.counters + b * a.Hkv + g, 1);
-        *flag = ticket == n_split - 1;
-    }
-    __syncthreads();
-    if (!*flag) return;
-    __threadfence();
-    for (int idx = threadIdx.x; idx < n_rows * D; idx += blockDim.x) {
-        const int r = idx / D, d = idx % D;
-        float M = kNegBig;
-        for (int s = 0; s < n_split; ++s) M = fmaxf(M, __ldcg(&a.ml_part[(part + s) * NR + r].x));
-        float Ls = 0.0f, O = 0.0f;
-        for (int s = 0; s < n_split; ++s) {
-            const float2 ml = __ldcg(&a.ml_part[(part + s) * NR + r]);
-            const float f = exp2f(ml.x - M);
-            Ls = fmaf(ml.y, f, Ls);
-            O = fmaf(__ldcg(&a.o_part[((part + s) * NR + r) * D + d]), f, O);
-        }
-        store_elem(out_ptr(r) + d, Ls > 0.0f ? O / Ls : 0.0f);
-    }
-    if (threadIdx.x == 0) a.counters[b * a.Hkv + g] = 0;
 }
 
 // Row templates: group * q_len rows are padded up to one of these.
@@ -383,26 +476,33 @@ int padded_rows(int rows) {
     return 0;
 }
 
+int ctas_per_sm(int nr) { return nr <= 4 ? 3 : 1; }
+
+int device_sms() {
+    const int n = sm_count();
+    return n > 0 ? n : 160;  // no device visible (size queries on a build host)
+}
+
 template <typename T, int NR>
-int launch_nr(const AttnArgs &a, dim3 grid, cudaStream_t stream) {
+int launch_nr(const AttnArgs &a, int ctas, cudaStream_t stream) {
     constexpr int D = 16 * Chunk<T>::N;
-    const size_t smem = AttnSmem<NR, D>::total;
+    const size_t smem = AttnSmem<NR, D>::total(a.B);
     auto kern = decode_attn_kernel<T, NR>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return TTS_ERR_CUDA;
-    kern<<<grid, kWarps * 32, smem, stream>>>(a);
+    kern<<<ctas, kWarps * 32, smem, stream>>>(a);
     return launch_status();
 }
 
 template <typename T>
-int launch_typed(const AttnArgs &a, int nr, dim3 grid, cudaStream_t stream) {
+int launch_typed(const AttnArgs &a, int nr, int ctas, cudaStream_t stream) {
     switch (nr) {
-        case 2: return launch_nr<T, 2>(a, grid, stream);
-        case 4: return launch_nr<T, 4>(a, grid, stream);
-        case 8: return launch_nr<T, 8>(a, grid, stream);
-        case 10: return launch_nr<T, 10>(a, grid, stream);
-        case 16: return launch_nr<T, 16>(a, grid, stream);
+        case 2: return launch_nr<T, 2>(a, ctas, stream);
+        case 4: return launch_nr<T, 4>(a, ctas, stream);
+        case 8: return launch_nr<T, 8>(a, ctas, stream);
+        case 10: return launch_nr<T, 10>(a, ctas, stream);
+        case 16: return launch_nr<T, 16>(a, ctas, stream);
         default: return TTS_ERR_UNSUPPORTED;
     }
 }
@@ -413,24 +513,25 @@ bool supported_head(int dtype, int head_dim) {
 
 }  // namespace
 
-bool attn_split_policy(int B, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
-                       int max_ctx_len, AttnSplit *out) {
+bool attn_plan(int B, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
+               int max_ctx_len, AttnPlan *out) {
     if (B < 1 || q_len < 1 || num_kv_heads < 1 || num_q_heads < num_kv_heads ||
         num_q_heads % num_kv_heads != 0 || head_dim < 1 || max_ctx_len < q_len ||
         max_ctx_len > (1 << 24))
         return false;
     const int rows = padded_rows((num_q_heads / num_kv_heads) * q_len);
-    if (rows == 0) return false;
-    const int nblk = (max_ctx_len + TTS_BLOCK_TOKENS - 1) / TTS_BLOCK_TOKENS;
-    out->blocks = kSplitBlocks;
-    out->max_splits = (nblk + kSplitBlocks - 1) / kSplitBlocks;
+    if (rows == 0 || B > kMaxStreams) return false;
+    const long long nblk = (max_ctx_len + TTS_BLOCK_TOKENS - 1) / TTS_BLOCK_TOKENS;
+    if (static_cast<long long>(B) * num_kv_heads * nblk >= (1LL << 31)) return false;
     out->rows = rows;
+    out->ctas = device_sms() * ctas_per_sm(rows);
+    out->workers = out->ctas * kWarps;
     return true;
 }
 
-size_t attn_workspace_bytes(int B, int num_kv_heads, int head_dim, const AttnSplit &sp) {
-    const size_t units = static_cast<size_t>(B) * num_kv_heads * sp.max_splits * sp.rows;
-    return align_up(units * head_dim * sizeof(float), 256) + align_up(units * sizeof(float2), 256) +
+size_t attn_workspace_bytes(int B, int num_kv_heads, int head_dim, const AttnPlan &pl) {
+    const size_t slot = static_cast<size_t>(pl.rows) * head_dim + 2 * pl.rows;
+    return align_up(static_cast<size_t>(pl.workers) * 2 * slot * sizeof(float), 256) +
            align_up(static_cast<size_t>(B) * num_kv_heads * sizeof(int32_t), 256);
 }
 
@@ -439,10 +540,10 @@ size_t attn_workspace_bytes(int B, int num_kv_heads, int head_dim, const AttnSpl
 extern "C" size_t tts_decode_attn_workspace_size(int32_t B, int32_t q_len, int32_t num_q_heads,
                                                  int32_t num_kv_heads, int32_t head_dim,
                                                  int32_t max_ctx_len) {
-    tts::AttnSplit sp;
-    if (!tts::attn_split_policy(B, q_len, num_q_heads, num_kv_heads, head_dim, max_ctx_len, &sp))
+    tts::AttnPlan pl;
+    if (!tts::attn_plan(B, q_len, num_q_heads, num_kv_heads, head_dim, max_ctx_len, &pl))
         return 0;
-    return tts::attn_workspace_bytes(B, num_kv_heads, head_dim, sp);
+    return tts::attn_workspace_bytes(B, num_kv_heads, head_dim, pl);
 }
 
 extern "C" int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block_table,
@@ -453,16 +554,15 @@ extern "C" int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block
     using namespace tts;
     if (!cache || !d_block_table || !d_ctx_lens || !d_q || !d_out) return TTS_ERR_INVALID;
     if (!cache->k_pool || !cache->v_pool || cache->num_blocks < 1) return TTS_ERR_INVALID;
-    if (B < 0 || B > 65535 || q_len < 1 || max_blocks_per_seq < 1 ||
-        max_blocks_per_seq > (1 << 20) || !(scale > 0.0f) || scale != scale)
+    if (B < 0 || q_len < 1 || max_blocks_per_seq < 1 || max_blocks_per_seq > (1 << 20) ||
+        !(scale > 0.0f) || scale != scale)
         return TTS_ERR_INVALID;
     if (cache->block_size != TTS_BLOCK_TOKENS) return TTS_ERR_UNSUPPORTED;
     if (!supported_head(cache->dtype, cache->head_dim)) return TTS_ERR_UNSUPPORTED;
-    if (cache->num_kv_heads < 1 || cache->num_kv_heads > 65535) return TTS_ERR_INVALID;
+    if (cache->num_kv_heads < 1) return TTS_ERR_INVALID;
     if (B == 0) return TTS_OK;
-    AttnSplit sp;
-    if (!attn_split_policy(B, q_len, num_q_heads, cache->num_kv_heads, cache->head_dim,
-                           max_ctx_len, &sp)) {
+    AttnPlan pl;
+    if (!attn_plan(B, q_len, num_q_heads, cache->num_kv_heads, cache->head_dim, max_ctx_len, &pl)) {
         const int nh = cache->num_kv_heads;
         const bool shape_ok = num_q_heads >= nh && num_q_heads % nh == 0 && max_ctx_len >= q_len &&
                               max_ctx_len <= (1 << 24);
@@ -470,12 +570,10 @@ extern "C" int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block
     }
     if (!aligned16(cache->k_pool) || !aligned16(cache->v_pool) || !aligned16(d_q))
         return TTS_ERR_INVALID;
-    const size_t need = attn_workspace_bytes(B, cache->num_kv_heads, cache->head_dim, sp);
+    const size_t need = attn_workspace_bytes(B, cache->num_kv_heads, cache->head_dim, pl);
     if (!d_ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(d_ws) & 255u) != 0)
         return TTS_ERR_WORKSPACE;
 
-    const size_t units =
-        static_cast<size_t>(B) * cache->num_kv_heads * sp.max_splits * sp.rows;
     uint8_t *ws = static_cast<uint8_t *>(d_ws);
     AttnArgs a;
     a.k_pool = static_cast<const uint8_t *>(cache->k_pool);
@@ -486,25 +584,22 @@ extern "C" int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block
     a.max_blocks = max_blocks_per_seq;
     a.ctx_lens = d_ctx_lens;
     a.max_ctx = max_ctx_len;
+    a.B = B;
     a.q_len = q_len;
     a.Hq = num_q_heads;
     a.group = num_q_heads / cache->num_kv_heads;
     a.causal = causal ? 1 : 0;
     a.qscale = scale * kLog2e;
-    a.q = d_q;
+    a.q = static_cast<const uint8_t *>(d_q);
     a.out = d_out;
-    a.o_part = reinterpret_cast<float *>(ws);
-    a.ml_part = reinterpret_cast<float2 *>(ws + align_up(units * cache->head_dim * sizeof(float), 256));
-    a.counters = reinterpret_cast<int32_t *>(ws + align_up(units * cache->head_dim * sizeof(float), 256) +
-                                             align_up(units * sizeof(float2), 256));
-    a.max_splits = sp.max_splits;
-    a.split_blocks = sp.blocks;
+    a.part = reinterpret_cast<float *>(ws);
+    a.counters = reinterpret_cast<int32_t *>(
+        ws + need - align_up(static_cast<size_t>(B) * cache->num_kv_heads * sizeof(int32_t), 256));
+    a.workers = pl.workers;
     a.err = d_err;
-    const dim3 grid(sp.max_splits, cache->num_kv_heads, B);
-    if (grid.x > 0x7FFFFFFFu) return TTS_ERR_INVALID;
     auto s = static_cast<cudaStream_t>(stream);
-    return cache->dtype == TTS_BF16 ? launch_typed<__nv_bfloat16>(a, sp.rows, grid, s)
-                                    : launch_typed<float>(a, sp.rows, grid, s);
+    return cache->dtype == TTS_BF16 ? launch_typed<__nv_bfloat16>(a, pl.rows, pl.ctas, s)
+                                    : launch_typed<float>(a, pl.rows, pl.ctas, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -523,7 +618,7 @@ extern "C" int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block
 namespace tts {
 namespace {
 
-constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_attn_scratch[kStaticScratchBytes];

@@ -54,15 +54,14 @@ HeadWs head_ws(void *ws, int R) {
     return w;
 }
 
-// Called by every thread of every CTA after its keys are published.  The
-// last CTA converts keys to ids and resets the workspace.  No waiting.
-__device__ void finish_selection(const HeadWs &ws, int R, int32_t *ids, float *best, int *flag) {
+// Called by every thread of each of the `publishers` CTAs that publish keys,
+// after their atomics.  The last of them converts keys to ids and resets the
+// workspace.  No waiting.
+__device__ void finish_selection(const HeadWs &ws, int R, int32_t *ids, float *best, int *flag,
+                                 unsigned int publishers) {
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) {
-        const unsigned int total = gridDim.x * gridDim.y;
-        *flag = atomicAdd(ws.ticket, 1u) == total - 1u;
-    }
+    if (threadIdx.x == 0) *flag = atomicAdd(ws.ticket, 1u) == publishers - 1u;
     __syncthreads();
     if (!*flag) return;
     __threadfence();
@@ -122,7 +121,7 @@ head_simt_f32_kernel(const float *__restrict__ h, const float *__restrict__ W, c
             }
         }
     }
-    finish_selection(a.ws, a.R, a.ids, a.best, &flag);
+    finish_selection(a.ws, a.R, a.ids, a.best, &flag, gridDim.x * gridDim.y);
 }
 
 // --------------------------------------------------------- tcgen05 (bf16)
@@ -141,10 +140,15 @@ __device__ __forceinline__ uint32_t map_cluster(uint32_t addr, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
     return out;
 }
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
+// Generic pointer to the same shared-memory object in cluster CTA `rank`.
+template <typename T>
+__device__ __forceinline__ T *map_cluster_ptr(T *p, uint32_t rank) {
+    uint64_t out;
+    asm volatile("mapa.u64 %0, %1, %2;" : "=l"(out) : "l"(reinterpret_cast<uint64_t>(p)), "r"(rank));
+    return reinterpret_cast<T *>(out);
+}
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
@@ -215,7 +219,7 @@ struct TcLayout {
     uint32_t ring_bytes;    // all stages (also hosts the accumulator dump)
     uint32_t dump_stride;   // floats per dumped row (N + 4)
     uint32_t bars;          // offset of the mbarriers
-    uint32_t colbest;       // offset of the per-column best keys
+    uint32_t colbest;       // offset of the per-column best keys ([8][N]: own, then peers' slots)
     uint32_t misc;          // TMEM address, flag
     uint32_t total;
 };
@@ -229,7 +233,7 @@ __host__ __device__ inline TcLayout tc_layout(int N) {
     L.ring_bytes = ring > dump ? ring : dump;
     L.bars = L.ring_bytes;
     L.colbest = L.bars + 8 * (2 * kStagesTC + 1);
-    L.misc = L.colbest + 8 * N;
+    L.misc = L.colbest + 8 * 8 * N;
     L.total = L.misc + 16 + 1024;  // + slack to align the dynamic base to 1024
     return L;
 }
@@ -269,7 +273,24 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
         fence_mbar_init();
         *failed = 0;
     }
+    if (warp == 4 && lane == 0) {
+        prefetch_tensormap(&map_w);
+        prefetch_tensormap(&map_h);
+    }
     for (int i = threadIdx.x; i < N; i += blockDim.x) colbest[i] = 0ull;
+    __syncthreads();
+    // The first stages need no slot to free up: start streaming W and h now,
+    // while the TMEM accumulator is being allocated.
+    const int prologue = ktiles < kStagesTC ? ktiles : kStagesTC;
+    if (warp == 4 && lane == 0) {
+        for (int it = 0; it < prologue; ++it) {
+            const uint32_t sa = base + it * Lo.stage_bytes;
+            mbar_arrive_expect_tx(bar_full + 8 * it, Lo.stage_bytes);
+            const int k = kbase + it * kTileK;
+            tma_load_2d(sa, &map_w, k, v0, bar_full + 8 * it);
+            tma_load_2d(sa + kATileBytes, &map_h, k, r0, bar_full + 8 * it);
+        }
+    }
     if (warp == 5) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_addr(tmem_slot)),
@@ -283,8 +304,8 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 4 && lane == 0) {
-        // ---- TMA producer
-        for (int it = 0; it < ktiles; ++it) {
+        // ---- TMA producer (the first `prologue` stages are already in flight)
+        for (int it = prologue; it < ktiles; ++it) {
             const int s = it % kStagesTC;
             if (it >= kStagesTC && !mbar_wait(bar_empty + 8 * s, ((it / kStagesTC) - 1) & 1)) {
                 flag_error(a.err, TTS_ERRBIT_TIMEOUT);
@@ -350,21 +371,31 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
     // 128 / CK rows, select per batch column.  Work item = (8-row group, column).
     const int rows_per_cta = kTileM / CK;
     const int items = (rows_per_cta / 8) * N;
-    const uint32_t dump_addr = base;
+    const float *dumps[8];
+#pragma unroll
+    for (int src = 0; src < 8; ++src)
+        dumps[src] = src < CK ? (CK > 1 ? map_cluster_ptr(dump, static_cast<uint32_t>(src)) : dump) : dump;
     for (int item = threadIdx.x; item < items; item += blockDim.x) {
         const int gi = item / N, cn = item % N;
         const int r = r0 + cn;
         if (r >= a.R) continue;
         const int lrow = rank * rows_per_cta + gi * 8;   // local row in the tile
+        float part[8][8];
+#pragma unroll
+        for (int src = 0; src < 8; ++src) {
+            if (src < CK) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) part[src][e] = dumps[src][(lrow + e) * Lo.dump_stride + cn];
+            }
+        }
         float lg[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) lg[e] = 0.0f;
-        for (int src = 0; src < CK; ++src) {
-            const uint32_t sb = CK > 1 ? map_cluster(dump_addr, src) : dump_addr;
+        for (int e = 0; e < 8; ++e) {
+            float acc = 0.0f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                lg[e] += CK > 1 ? ld_cluster_f32(sb + ((lrow + e) * Lo.dump_stride + cn) * 4)
-                                : dump[(lrow + e) * Lo.dump_stride + cn];
+            for (int src = 0; src < 8; ++src)
+                if (src < CK) acc += part[src][e];
+            lg[e] = acc;
         }
         const int v = v0 + lrow;  // multiple of 8
         if (a.logits_out) {
@@ -394,10 +425,26 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
         atomicMax(colbest + cn, best);
     }
     __syncthreads();
-    for (int cn = threadIdx.x; cn < N; cn += blockDim.x)
-        if (r0 + cn < a.R && colbest[cn]) atomicMax(a.ws.keys + r0 + cn, colbest[cn]);
-    if (CK > 1) cluster_sync();  // peers may still read this CTA's dump
-    finish_selection(a.ws, a.R, a.ids, a.best, flag);
+    // One global atomic per column and cluster: every other rank stores its
+    // column maxima into its own slot of rank 0's table (plain remote stores,
+    // ordered by the cluster barrier), and rank 0 folds them.
+    if (CK > 1 && rank != 0) {
+        unsigned long long *slot = map_cluster_ptr(colbest + rank * N, 0u);
+        for (int cn = threadIdx.x; cn < N; cn += blockDim.x) slot[cn] = colbest[cn];
+    }
+    if (CK > 1) cluster_sync();  // peers are done reading this CTA's dump and storing keys
+    // Only rank 0 of each cluster publishes keys, so only those CTAs take a
+    // ticket: the last ticket then comes after every publication.
+    if (rank != 0) return;
+    for (int cn = threadIdx.x; cn < N; cn += blockDim.x) {
+        unsigned long long k = colbest[cn];
+        for (int src = 1; src < CK; ++src) {
+            const unsigned long long o = colbest[src * N + cn];
+            k = o > k ? o : k;
+        }
+        if (r0 + cn < a.R && k) atomicMax(a.ws.keys + r0 + cn, k);
+    }
+    finish_selection(a.ws, a.R, a.ids, a.best, flag, (gridDim.x / CK) * gridDim.y);
 }
 
 // ------------------------------------------------------------- host side

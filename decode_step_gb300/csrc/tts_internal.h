@@ -21,15 +21,15 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Split-KV policy shared by the workspace query and the launch: tokens of a
-// stream are cut into splits of `blocks` 16-token blocks.
-struct AttnSplit {
-    int blocks;      // KV blocks per split
-    int max_splits;  // splits of the longest context
-    int rows;        // query rows per (stream, KV head), padded to the kernel's template
+// Decode-attention launch plan shared by the workspace query and the launch:
+// a persistent grid of `ctas` CTAs (`workers` warps) over the flat tile list.
+struct AttnPlan {
+    int rows;     // query rows per (stream, KV head), padded to the kernel's template
+    int ctas;     // CTAs launched
+    int workers;  // warps, each owning one contiguous range of tiles
 };
-bool attn_split_policy(int B, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
-                       int max_ctx_len, AttnSplit *out);
-size_t attn_workspace_bytes(int B, int num_kv_heads, int head_dim, const AttnSplit &sp);
+bool attn_plan(int B, int q_len, int num_q_heads, int num_kv_heads, int head_dim, int max_ctx_len,
+               AttnPlan *out);
+size_t attn_workspace_bytes(int B, int num_kv_heads, int head_dim, const AttnPlan &pl);
 
 }  // namespace tts

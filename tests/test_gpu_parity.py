@@ -222,7 +222,8 @@ def test_block_permutation_invariance():
 
 
 def test_batch_compaction(orc):
-    """Dropping streams from the batch leaves the others' outputs unchanged."""
+    """Dropping streams from the batch leaves the others' outputs unchanged up to
+    rounding (the work split, and so the summation order, follows the batch)."""
     inp = wl.make_inputs(wl.custom(3, B=12), with_head=False, with_verify=False)
     u = Uploaded(inp)
     cache = gpu_append(u)
@@ -235,7 +236,10 @@ def test_batch_compaction(orc):
     u2.ctx_lens = dev(inp["ctx_lens"][keep])
     u2.q = dev(np.ascontiguousarray(inp["q"][keep]))
     part, _ = gpu_attn(u2, bd.KVCache(u2.k_pool, u2.v_pool))
-    assert torch.equal(part, full[torch.from_numpy(keep).cuda()])
+    a = as_f64(host(part), "bf16")
+    b = as_f64(host(full[torch.from_numpy(keep).cuda()]), "bf16")
+    bad, mx_abs, _ = attn_errors(a, b)
+    assert bad == 0 and mx_abs < 2e-2, f"compaction changed outputs by {mx_abs}"
 
 
 # --------------------------------------------------- invalid data on device
