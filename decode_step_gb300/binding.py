@@ -149,7 +149,7 @@ def tts_decode_attn_noalloc(cache: KVCache, block_table, ctx_lens, max_ctx_len, 
                             causal=False, err=None, stream=None):
     """tts_decode_attn without a workspace: for callers that cannot allocate
     device memory (graph capture, fully reserved memory); uses the library's
-    8 MiB static scratch, shared by all calls."""
+    24 MiB static scratch, shared by all calls."""
     B, max_blocks = block_table.shape
     _, q_len, Hq, D = q.shape
     args = (ctypes.byref(cache.desc), _dev(block_table, "block_table", torch.int32), max_blocks,

@@ -8,31 +8,32 @@
 //   out[b][j][h] = sum_t softmax_t(scale * q[b][j][h] . k_t) v_t,
 // t over the stream's tokens below the row's limit, KV head h / group.
 //
-// How (HBM-bound: each cached byte feeds 2 flops per query row):
-//  - The work is the flat list of (stream, KV head, 16-token block) tiles,
-//    stream-major.  A persistent grid of warps splits that list into equal
-//    contiguous ranges (a warp-granular stream-K schedule), so every warp
-//    streams the same number of tiles whatever the context-length mix, and a
-//    (stream, KV head) "segment" is split across warps only where a range
-//    boundary falls inside it.  Each CTA first scans the context lengths into
-//    a per-stream tile prefix in shared memory.
-//  - Each warp streams its tiles' K and V (4 KB each, contiguous in the pool)
-//    through a private 2-stage shared-memory ring with bulk TMA copies (L2
-//    evict-first), completion on per-stage mbarriers; the query rows of a new
-//    segment ride along in the same stage.  Block ids are fetched 32 tiles at
-//    a time, one batch ahead.
-//  - Lane (p, c) = (lane / 16, lane % 16) reads 16-byte chunk c of the rows
-//    of tokens p, p + 2, ..., p + 14 (conflict-free 128-bit shared loads).
-//    Dot products are reduced across the 16 chunk lanes by recursive halving
-//    (each shuffle round halves the values a lane carries), leaving every lane
-//    the full scores of one token for half of the query rows.  Online softmax
-//    in the log2 domain with warp-shuffle max reductions; P.V accumulates per
-//    lane into its 16-byte slice of the output rows.  All group x q_len query
-//    rows of a KV head share one read of each tile.
-//  - A segment wholly inside a warp's range is written out directly.  A split
-//    segment's warps write (m, l, unnormalised o) partials; the last of them
-//    to finish (an atomic ticket, never a wait) merges the partials with a
-//    log-sum-exp combine and writes the output.
+// Work distribution (shared by both kernels).  The work is the flat list of
+// (stream, KV head, 16-token block) tiles, stream-major.  A persistent grid of
+// warps splits it into equal contiguous ranges (a warp-granular stream-K
+// schedule), so every warp streams the same number of tiles whatever the
+// context-length mix; a (stream, KV head) "segment" is split across warps only
+// where a range boundary falls inside it.  A segment wholly inside one range
+// is written out directly; a split segment's warps publish (m, l, o) partials
+// and the last of them (an atomic ticket, never a wait) merges them with a
+// log-sum-exp combine.  Each warp streams its tiles through a private 2-stage
+// shared-memory ring filled by TMA (L2 evict-first for the cache), completion
+// on per-stage mbarriers; a new segment's query rows ride in the same stage.
+//
+// bf16 (head_dim 128): the per-tile products S = Q K^T and O += P V run as
+// mma.sync m16n8k16 (bf16 in, fp32 accumulate) on all group x q_len query rows
+// of the KV head at once (padded to 16).  Each KV byte is still read once from
+// HBM; the tensor-core instructions only replace the ~8 bf16->fp32 converts
+// and FMAs per element that would otherwise make the kernel issue-bound at
+// GB300's bandwidth per SM.  K/V tiles arrive through 2-D TMA with a 128-byte
+// swizzle, so the ldmatrix fragment loads are bank-conflict free.  Softmax
+// (row max, exp2, running sums) is fp32 with warp shuffles among the four
+// lanes that share a query row.
+//
+// fp32 (head_dim 64): CUDA cores.  Lane (p, c) reads 16-byte chunk c of tokens
+// p, p + 2, ...; dot products are reduced across the 16 chunk lanes by
+// recursive halving, leaving every lane the full scores of one token for half
+// of the query rows.
 #include <mutex>
 
 #include "tts_common.cuh"
@@ -67,21 +68,12 @@ struct AttnArgs {
     float qscale;       // softmax scale * log2(e)
     const uint8_t *q;
     void *out;
-    float *part;        // [workers][2][NR * D + 2 * NR]: o, m, l of split segments
+    float *part;        // [workers][2][nr_slot * D + 2 * nr_slot]: o, m, l of split segments
     int32_t *counters;  // [B][Hkv] tickets of split segments
     int workers;
+    int nr_slot;        // query rows per partial slot (group * q_len padded)
+    int stages;         // ring depth per warp (tensor-core kernel)
     int32_t *err;
-};
-
-template <int NR, int D>
-struct AttnSmem {
-    static constexpr int stage_bytes = 2 * kTileBytes + NR * kRowBytes;  // K, V, query rows
-    static constexpr size_t stages = 0;
-    static constexpr size_t bars = stages + size_t(kWarps) * kStages * stage_bytes;
-    static constexpr size_t pbuf = bars + 8 * kWarps * kStages;
-    static constexpr size_t prefix = pbuf + 4 * kWarps * 16 * NR;
-    // then: int prefix[B + 1], int ctxs[B], int scan[kWarps]
-    static size_t total(int B) { return prefix + 4 * (2 * size_t(B) + 1 + kWarps); }
 };
 
 __device__ __forceinline__ int warp_of_tile(long long t, long long T, long long W) {
@@ -91,66 +83,192 @@ __device__ __forceinline__ long long range_start(long long w, long long T, long 
     return w * T / W;
 }
 
-template <typename T, int NR>
-__global__ void __launch_bounds__(kWarps * 32, NR <= 4 ? 3 : 1)
-decode_attn_kernel(const AttnArgs a) {
-    using C = Chunk<T>;
-    constexpr int EPC = C::N;          // elements per 16-byte chunk
-    constexpr int D = 16 * EPC;        // head dim: one 256-byte row per token
-    constexpr int HALF = NR / 2;
-    constexpr int SF = NR * D + 2 * NR;  // floats per partial slot
-    using S = AttnSmem<NR, D>;
-    extern __shared__ __align__(1024) uint8_t smem[];
-    int *prefix = reinterpret_cast<int *>(smem + S::prefix);  // [B + 1], in tiles
-    int *ctxs = prefix + a.B + 1;                              // [B], 0 for an invalid stream
-    int *scan = ctxs + a.B;                                    // [kWarps]
-
+// Context lengths -> per-stream tile prefix (x Hkv, stream-major) in shared
+// memory; invalid streams get no tiles, zero outputs (CTA 0) and an error bit.
+// Called by every thread of the CTA.
+template <typename T, int D, int WARPS>
+__device__ void scan_streams(const AttnArgs &a, int *prefix, int *ctxs, int *scan) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_rows = a.group * a.q_len;
     const int cap = min(a.max_ctx, a.max_blocks * TTS_BLOCK_TOKENS);
-    T *out = static_cast<T *>(a.out);
-    const size_t row_stride = static_cast<size_t>(a.Hq) * D;  // elements between query positions
+    const int per = (a.B + blockDim.x - 1) / blockDim.x;
+    const int i0 = threadIdx.x * per, i1 = min(a.B, i0 + per);
+    int local = 0;
+    for (int i = i0; i < i1; ++i) {
+        const int L = __ldg(a.ctx_lens + i);
+        const bool ok = L >= a.q_len && L <= cap;
+        ctxs[i] = ok ? L : 0;
+        local += ok ? (L + TTS_BLOCK_TOKENS - 1) / TTS_BLOCK_TOKENS : 0;
+        if (!ok && blockIdx.x == 0) {
+            flag_error(a.err, TTS_ERRBIT_CTX_LEN);
+            T *o = static_cast<T *>(a.out) + static_cast<size_t>(i) * a.q_len * a.Hq * D;
+            for (int e = 0; e < a.q_len * a.Hq * D; ++e) store_elem(o + e, 0.0f);
+        }
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) scan[warp] = incl;
+    __syncthreads();
+    int run = incl - local, total = 0;
+    for (int w = 0; w < WARPS; ++w) {
+        if (w < warp) run += scan[w];
+        total += scan[w];
+    }
+    for (int i = i0; i < i1; ++i) {
+        prefix[i] = run * a.Hkv;
+        run += ctxs[i] ? (ctxs[i] + TTS_BLOCK_TOKENS - 1) / TTS_BLOCK_TOKENS : 0;
+    }
+    if (threadIdx.x == 0) prefix[a.B] = total * a.Hkv;
+    __syncthreads();
+}
 
-    // ---- 1. context lengths -> per-stream tile prefix (x Hkv, stream-major)
-    {
-        const int per = (a.B + blockDim.x - 1) / blockDim.x;
-        const int i0 = threadIdx.x * per, i1 = min(a.B, i0 + per);
-        int local = 0;
-        for (int i = i0; i < i1; ++i) {
-            const int L = __ldg(a.ctx_lens + i);
-            const bool ok = L >= a.q_len && L <= cap;
-            ctxs[i] = ok ? L : 0;
-            local += ok ? (L + TTS_BLOCK_TOKENS - 1) / TTS_BLOCK_TOKENS : 0;
-            if (!ok && blockIdx.x == 0) {
-                flag_error(a.err, TTS_ERRBIT_CTX_LEN);
-                T *o = out + static_cast<size_t>(i) * a.q_len * row_stride;
-                for (size_t e = 0; e < a.q_len * row_stride; ++e) store_elem(o + e, 0.0f);
+// Tile t of the flat list -> (raw block id, segment = stream * Hkv + head,
+// block index in the stream); t must be < prefix[B].  The block id load is
+// left in flight (validated where it is used).
+__device__ __forceinline__ void tile_meta(const AttnArgs &a, const int *prefix, int t, int &id,
+                                          int &seg, int &blk) {
+    int lo = 0, hi = a.B;  // prefix[lo] <= t < prefix[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= t) lo = mid; else hi = mid;
+    }
+    const int nb = (prefix[lo + 1] - prefix[lo]) / a.Hkv;
+    const int r = t - prefix[lo];
+    const int g = r / nb;
+    blk = r - g * nb;
+    seg = lo * a.Hkv + g;
+    id = __ldg(a.table + static_cast<size_t>(lo) * a.max_blocks + blk);
+}
+
+// Output pointer of query row r (= j * group + hh) of segment (b, g).
+template <typename T, int D>
+__device__ __forceinline__ T *out_row(const AttnArgs &a, int b, int g, int r) {
+    const int j = r / a.group, hh = r % a.group;
+    return static_cast<T *>(a.out) + ((static_cast<size_t>(b) * a.q_len + j) * a.Hq + g * a.group + hh) * D;
+}
+
+// The last contributor of a split segment merges the contributors' partials
+// (log-sum-exp combine).  Loads are issued together rather than one
+// contributor at a time: contributors are spread over the lanes (32 at a
+// time) for the row maxima and sums, and each lane reads its D/32-dim slice
+// of the outputs for 8 contributors per batch.
+template <typename T, int D>
+__device__ void merge_split_segment(const AttnArgs &a, int b, int g, int n_rows, int w_first,
+                                    int w_last, bool first_shifted, int lane) {
+    constexpr int DPL = D / 32;  // dims per lane: 4 (bf16, D = 128) or 2 (fp32, D = 64)
+    const int NRS = a.nr_slot;
+    const size_t SF = static_cast<size_t>(NRS) * D + 2 * NRS;
+    const size_t ML = static_cast<size_t>(NRS) * D;  // offset of the maxima; sums follow
+    const int nc = w_last - w_first + 1;
+    auto slot = [&](int i) -> const float * {
+        return a.part + (static_cast<size_t>(w_first + i) * 2 + (i == 0 && first_shifted)) * SF;
+    };
+    for (int r = 0; r < n_rows; ++r) {
+        // row maximum over all contributors
+        float M = kNegBig;
+        for (int c0 = 0; c0 < nc; c0 += 32) {
+            const int ci = c0 + lane;
+            M = fmaxf(M, ci < nc ? __ldcg(slot(ci) + ML + r) : kNegBig);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+        float Ls = 0.0f, O[DPL];
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) O[e] = 0.0f;
+        for (int c0 = 0; c0 < nc; c0 += 32) {
+            const int ci = c0 + lane;
+            float f_i = 0.0f;
+            if (ci < nc) {
+                const float *pp = slot(ci) + ML;
+                f_i = exp2f(__ldcg(pp + r) - M);
+                Ls = fmaf(__ldcg(pp + NRS + r), f_i, Ls);
+            }
+            const int cn = min(32, nc - c0);
+            for (int k0 = 0; k0 < cn; k0 += 8) {
+                float v[8][DPL];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    if (k0 + k < cn) {
+                        const float *src = slot(c0 + k0 + k) + static_cast<size_t>(r) * D + lane * DPL;
+                        if constexpr (DPL == 4) {
+                            const float4 x = __ldcg(reinterpret_cast<const float4 *>(src));
+                            v[k][0] = x.x; v[k][1] = x.y; v[k][2] = x.z; v[k][3] = x.w;
+                        } else {
+                            const float2 x = __ldcg(reinterpret_cast<const float2 *>(src));
+                            v[k][0] = x.x; v[k][1] = x.y;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < DPL; ++e) v[k][e] = 0.0f;
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float f = __shfl_sync(kFull, f_i, (k0 + k) & 31);
+#pragma unroll
+                    for (int e = 0; e < DPL; ++e) O[e] = fmaf(v[k][e], f, O[e]);
+                }
             }
         }
-        int incl = local;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += v;
-        }
-        if (lane == 31) scan[warp] = incl;
-        __syncthreads();
-        int run = incl - local, total = 0;
-        for (int w = 0; w < kWarps; ++w) {
-            if (w < warp) run += scan[w];
-            total += scan[w];
-        }
-        for (int i = i0; i < i1; ++i) {
-            prefix[i] = run * a.Hkv;
-            run += ctxs[i] ? (ctxs[i] + TTS_BLOCK_TOKENS - 1) / TTS_BLOCK_TOKENS : 0;
-        }
-        if (threadIdx.x == 0) prefix[a.B] = total * a.Hkv;
-        __syncthreads();
+        for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(kFull, Ls, o);
+        const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
+        T *dst = out_row<T, D>(a, b, g, r) + lane * DPL;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) store_elem(dst + e, O[e] * inv);
     }
+}
 
-    // ---- 2. this warp's tile range
-    // Every participating warp gets at least one tile (warps beyond the tile
-    // count sit out), so a split segment's contributors are consecutive warps.
+// Publishes a warp's partial of a split segment (already written to `part`
+// by the caller) and, if it is the last one, merges.  Whole warp calls.
+template <typename T, int D>
+__device__ void finish_split_segment(const AttnArgs &a, int seg, int s0, int s1, int n_rows,
+                                     long long Ttot, long long Wtot, int lane) {
+    __threadfence();
+    __syncwarp();
+    const int w_first = warp_of_tile(s0, Ttot, Wtot);
+    const int w_last = warp_of_tile(s1 - 1, Ttot, Wtot);
+    int last = 0;
+    if (lane == 0) last = atomicAdd(a.counters + seg, 1) == w_last - w_first;
+    if (!__shfl_sync(kFull, last, 0)) return;
+    __threadfence();
+    merge_split_segment<T, D>(a, seg / a.Hkv, seg % a.Hkv, n_rows, w_first, w_last,
+                              range_start(w_first, Ttot, Wtot) != s0, lane);
+    if (lane == 0) a.counters[seg] = 0;
+}
+
+// ---------------------------------------------------------------- fp32 kernel
+
+template <int NR>
+struct SimtSmem {
+    static constexpr int stage_bytes = 2 * kTileBytes + NR * kRowBytes;  // K, V, query rows
+    static constexpr size_t stages = 0;
+    static constexpr size_t bars = stages + size_t(kWarps) * kStages * stage_bytes;
+    static constexpr size_t pbuf = bars + 8 * kWarps * kStages;
+    static constexpr size_t prefix = pbuf + 4 * kWarps * 16 * NR;
+    static size_t total(int B) { return prefix + 4 * (2 * size_t(B) + 1 + kWarps); }
+};
+
+template <int NR>
+__global__ void __launch_bounds__(kWarps * 32, NR <= 4 ? 3 : 1)
+decode_attn_simt_kernel(const AttnArgs a) {
+    using T = float;
+    using C = Chunk<T>;
+    constexpr int EPC = C::N;          // 4 fp32 per 16-byte chunk
+    constexpr int D = 16 * EPC;        // 64: one 256-byte row per token
+    constexpr int HALF = NR / 2;
+    using S = SimtSmem<NR>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    int *prefix = reinterpret_cast<int *>(smem + S::prefix);
+    int *ctxs = prefix + a.B + 1;
+    int *scan = ctxs + a.B;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_rows = a.group * a.q_len;
+
+    scan_streams<T, D, kWarps>(a, prefix, ctxs, scan);
     const long long Ttot = prefix[a.B];
     const long long Wtot = min(static_cast<long long>(a.workers), Ttot);
     const int wid = blockIdx.x * kWarps + warp;
@@ -169,35 +287,20 @@ decode_attn_kernel(const AttnArgs a) {
     }
     __syncwarp();
 
-    // Tile metadata, 32 tiles per batch (lane i holds tile 32 k + i of the
-    // range): raw block id (validated when used), segment = stream * Hkv + head,
-    // block index within the stream.
+    int cur_id, cur_seg, cur_blk, nxt_id = -1, nxt_seg = -1, nxt_blk = 0;
     auto load_meta = [&](int k, int &id, int &seg, int &blk) {
         const int t = t0 + 32 * k + lane;
         id = -1;
         seg = -1;
         blk = 0;
-        if (t < t1) {
-            int lo = 0, hi = a.B;  // prefix[lo] <= t < prefix[hi]
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (prefix[mid] <= t) lo = mid; else hi = mid;
-            }
-            const int nb = (prefix[lo + 1] - prefix[lo]) / a.Hkv;
-            const int r = t - prefix[lo];
-            const int g = r / nb;
-            blk = r - g * nb;
-            seg = lo * a.Hkv + g;
-            id = __ldg(a.table + static_cast<size_t>(lo) * a.max_blocks + blk);
-        }
+        if (t < t1) tile_meta(a, prefix, t, id, seg, blk);
     };
-    int cur_id, cur_seg, cur_blk, nxt_id = -1, nxt_seg = -1, nxt_blk = 0;
     load_meta(0, cur_id, cur_seg, cur_blk);
     if (n > 32) load_meta(1, nxt_id, nxt_seg, nxt_blk);
-    int kc = 0;  // batch of the tile being computed
+    int kc = 0;
 
     const uint64_t policy = l2_evict_first_policy();
-    const int qbytes_per_pos = a.group * D * static_cast<int>(sizeof(T));
+    const int qbytes_per_pos = a.group * kRowBytes;
     auto issue = [&](int j) {
         const bool in_cur = (j >> 5) == kc;
         const int src = j & 31;
@@ -227,7 +330,7 @@ decode_attn_kernel(const AttnArgs a) {
                     const int b = seg / a.Hkv, g = seg % a.Hkv;
                     for (int jq = 0; jq < a.q_len; ++jq) {
                         const size_t qoff =
-                            ((static_cast<size_t>(b) * a.q_len + jq) * a.Hq + g * a.group) * D * sizeof(T);
+                            ((static_cast<size_t>(b) * a.q_len + jq) * a.Hq + g * a.group) * kRowBytes;
                         bulk_load_nohint(dst + 2 * kTileBytes + jq * qbytes_per_pos, a.q + qoff,
                                          qbytes_per_pos, bar);
                     }
@@ -239,7 +342,6 @@ decode_attn_kernel(const AttnArgs a) {
 
     const int p = lane >> 4, c = lane & 15;
     const int my_tok = p + 2 * ((lane >> 1) & 7);
-    // State of the current segment.
     int seg_id = -1, seg_b = 0, seg_g = 0, seg_L = 0, s0 = 0, s1 = 0;
     int lim[HALF];
     float q[NR][EPC], m_run[HALF], l_run[HALF], o[NR][EPC];
@@ -261,25 +363,21 @@ decode_attn_kernel(const AttnArgs a) {
 #pragma unroll
             for (int e = 0; e < EPC; ++e) o[r][e] += __shfl_xor_sync(kFull, o[r][e], 16);
         if (s0 >= t0 && s1 <= t1) {
-            // whole segment in this warp: write the output
             if (lane < 16) {
 #pragma unroll
                 for (int r = 0; r < NR; ++r) {
                     if (r >= n_rows) break;
                     const float l = (r / HALF) == (lane & 1) ? l_tot[r % HALF] : l_oth[r % HALF];
                     const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-                    const int j = r / a.group, hh = r % a.group;
-                    T *dst = out + (static_cast<size_t>(seg_b) * a.q_len + j) * row_stride +
-                             static_cast<size_t>(seg_g * a.group + hh) * D + c * EPC;
+                    T *dst = out_row<T, D>(a, seg_b, seg_g, r) + c * EPC;
 #pragma unroll
                     for (int e = 0; e < EPC; ++e) store_elem(dst + e, o[r][e] * inv);
                 }
             }
             return;
         }
-        // split segment: publish this warp's partial, the last contributor merges
-        const int slot = s0 <= t0 ? 0 : 1;
-        float *part = a.part + (static_cast<size_t>(wid) * 2 + slot) * SF;
+        const size_t SF = static_cast<size_t>(NR) * D + 2 * NR;
+        float *part = a.part + (static_cast<size_t>(wid) * 2 + (s0 <= t0 ? 0 : 1)) * SF;
         if (lane < 16) {
 #pragma unroll
             for (int r = 0; r < NR; ++r)
@@ -293,39 +391,7 @@ decode_attn_kernel(const AttnArgs a) {
                 part[NR * D + NR + lane * HALF + k] = l_tot[k];
             }
         }
-        __threadfence();
-        __syncwarp();
-        const int w_first = warp_of_tile(s0, Ttot, Wtot);
-        const int w_last = warp_of_tile(s1 - 1, Ttot, Wtot);
-        int last = 0;
-        if (lane == 0) last = atomicAdd(a.counters + seg_id, 1) == w_last - w_first;
-        if (!__shfl_sync(kFull, last, 0)) return;
-        __threadfence();
-        const bool first_shifted = range_start(w_first, Ttot, Wtot) != s0;
-        for (int r = p; r < n_rows; r += 2) {
-            float M = kNegBig;
-            for (int w2 = w_first; w2 <= w_last; ++w2) {
-                const float *pp = a.part + (static_cast<size_t>(w2) * 2 + (w2 == w_first && first_shifted)) * SF;
-                M = fmaxf(M, __ldcg(pp + NR * D + r));
-            }
-            float Ls = 0.0f, O[EPC];
-#pragma unroll
-            for (int e = 0; e < EPC; ++e) O[e] = 0.0f;
-            for (int w2 = w_first; w2 <= w_last; ++w2) {
-                const float *pp = a.part + (static_cast<size_t>(w2) * 2 + (w2 == w_first && first_shifted)) * SF;
-                const float f = exp2f(__ldcg(pp + NR * D + r) - M);
-                Ls = fmaf(__ldcg(pp + NR * D + NR + r), f, Ls);
-#pragma unroll
-                for (int e = 0; e < EPC; ++e) O[e] = fmaf(__ldcg(pp + r * D + c * EPC + e), f, O[e]);
-            }
-            const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
-            const int j = r / a.group, hh = r % a.group;
-            T *dst = out + (static_cast<size_t>(seg_b) * a.q_len + j) * row_stride +
-                     static_cast<size_t>(seg_g * a.group + hh) * D + c * EPC;
-#pragma unroll
-            for (int e = 0; e < EPC; ++e) store_elem(dst + e, O[e] * inv);
-        }
-        if (lane == 0) a.counters[seg_id] = 0;
+        finish_split_segment<T, D>(a, seg_id, s0, s1, n_rows, Ttot, Wtot, lane);
     };
 
     bool timed_out = false;
@@ -352,7 +418,6 @@ decode_attn_kernel(const AttnArgs a) {
         const int t_blk = __shfl_sync(kFull, cur_blk, src);
         const uint32_t ks = stage0 + st * S::stage_bytes, vs = ks + kTileBytes;
         if (i == 0 || t_blk == 0) {
-            // ---- a new segment: finish the previous one, set up this one
             if (i > 0) flush();
             seg_id = t_seg;
             seg_b = t_seg / a.Hkv;
@@ -385,7 +450,6 @@ decode_attn_kernel(const AttnArgs a) {
         }
         if (!timed_out && t_id >= 0 && t_id < a.num_blocks) {
             const int base = t_blk * TTS_BLOCK_TOKENS;
-            // ---- scores: partial dots over this lane's chunk, 8 tokens x NR rows
             float acc[8 * NR];
 #pragma unroll
             for (int jt = 0; jt < 8; ++jt) {
@@ -399,7 +463,6 @@ decode_attn_kernel(const AttnArgs a) {
                     acc[jt * NR + r] = s;
                 }
             }
-            // ---- recursive halving across the 16 chunk lanes (masks 8, 4, 2, 1)
 #pragma unroll
             for (int step = 0; step < 4; ++step) {
                 const int m = 8 >> step;
@@ -412,7 +475,6 @@ decode_attn_kernel(const AttnArgs a) {
                     acc[x] = keep + __shfl_xor_sync(kFull, send, m);
                 }
             }
-            // ---- online softmax (log2 domain)
             const int tpos = base + my_tok;
             float alpha[HALF], other[HALF];
 #pragma unroll
@@ -432,7 +494,6 @@ decode_attn_kernel(const AttnArgs a) {
                 other[k] = __shfl_xor_sync(kFull, alpha[k], 1);
             }
             __syncwarp();
-            // ---- rescale and accumulate P.V
 #pragma unroll
             for (int r = 0; r < NR; ++r) {
                 const bool mine = (r / HALF) == (lane & 1);
@@ -461,13 +522,384 @@ decode_attn_kernel(const AttnArgs a) {
     }
     flush();
     if (timed_out) {
-        // Let copies still in flight land before the CTA's shared memory goes away.
         const int issued = min(n, waited + kStages);
         for (int i = waited; i < issued; ++i) mbar_wait(bar0 + 8 * (i % kStages), (i / kStages) & 1);
     }
 }
 
-// Row templates: group * q_len rows are padded up to one of these.
+// ------------------------------------------------------- bf16 tensor-core kernel
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+// D[16x8] += A[16x16] . B[16x8], bf16 in, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16_16816(float *d, const uint32_t *a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Launch shape of the tensor-core kernel (measured best: 12 warps per SM with
+// two tiles in flight each; fewer warps with deeper rings were slower).
+constexpr int kTcWarps = 4;
+constexpr int kTcMaxStages = 2;
+constexpr int kTcCtasPerSm = 3;
+
+// One stage of a warp's ring: K and V of one (block, head) tile, each as two
+// 16-row x 64-column boxes (128-byte swizzle, 2 KB each), then the query rows
+// of a new segment (row-major bf16, n_rows x 256 B).
+constexpr int kBoxBytes = 2048;
+constexpr int kKVStageBytes = 4 * kBoxBytes;
+
+// Address of 16-byte chunk `ch` (0..15) of token row `t` (0..15) in a K or V
+// tile stored as two swizzled boxes.
+__device__ __forceinline__ uint32_t swz(uint32_t tile, int t, int ch) {
+    return tile + (ch >> 3) * kBoxBytes + (t >> 3) * 1024 + (t & 7) * 128 + (((ch & 7) ^ (t & 7)) << 4);
+}
+
+struct TcSmem {
+    int stage_bytes;  // K/V boxes + query rows, 1 KB multiple
+    int stages;       // offset of the rings (from the 1 KB-aligned base)
+    int bars;
+    int prefix;       // int prefix[B + 1], ctxs[B], scan[kTcWarps]
+    int total;        // bytes to request (includes 1 KB of alignment slack)
+};
+__host__ __device__ inline TcSmem tc_smem(int n_rows, int B, int stages) {
+    TcSmem s;
+    const int qbytes = ((n_rows * kRowBytes + 1023) / 1024) * 1024;
+    s.stage_bytes = kKVStageBytes + qbytes;
+    s.stages = 0;
+    s.bars = s.stages + kTcWarps * stages * s.stage_bytes;
+    s.prefix = s.bars + 8 * kTcWarps * stages;
+    s.total = s.prefix + 4 * (2 * B + 1 + kTcWarps) + 1024;
+    return s;
+}
+
+// Deepest ring (<= kTcMaxStages) that fits kTcCtasPerSm CTAs per SM; 0 if
+// not even one stage fits.
+__host__ inline int tc_stages(int n_rows, int B) {
+    const int budget = 227 * 1024 / kTcCtasPerSm - 1024;
+    for (int st = kTcMaxStages; st >= 1; --st)
+        if (tc_smem(n_rows, B, st).total <= budget) return st;
+    return 0;
+}
+
+__global__ void __launch_bounds__(kTcWarps * 32, kTcCtasPerSm)
+decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                      const AttnArgs a) {
+    constexpr int D = 128;
+    using T = __nv_bfloat16;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    const int n_rows = a.group * a.q_len;  // <= 16
+    const int n_stages = a.stages;
+    const TcSmem S = tc_smem(n_rows, a.B, n_stages);
+    int *prefix = reinterpret_cast<int *>(smem + S.prefix);
+    int *ctxs = prefix + a.B + 1;
+    int *scan = ctxs + a.B;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    scan_streams<T, D, kTcWarps>(a, prefix, ctxs, scan);
+    const long long Ttot = prefix[a.B];
+    const long long Wtot = min(static_cast<long long>(a.workers), Ttot);
+    const int wid = blockIdx.x * kTcWarps + warp;
+    if (Ttot == 0 || wid >= Wtot) return;
+    const int t0 = static_cast<int>(range_start(wid, Ttot, Wtot));
+    const int t1 = static_cast<int>(range_start(wid + 1, Ttot, Wtot));
+    const int n = t1 - t0;
+    if (n <= 0) return;
+
+    const uint32_t stage0 = base + S.stages + warp * n_stages * S.stage_bytes;
+    const uint32_t bar0 = base + S.bars + 8 * warp * n_stages;
+    if (lane == 0) {
+        for (int s = 0; s < n_stages; ++s) mbar_init(bar0 + 8 * s, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    int cur_id, cur_seg, cur_blk, nxt_id = -1, nxt_seg = -1, nxt_blk = 0;
+    auto load_meta = [&](int k, int &id, int &seg, int &blk) {
+        const int t = t0 + 32 * k + lane;
+        id = -1;
+        seg = -1;
+        blk = 0;
+        if (t < t1) tile_meta(a, prefix, t, id, seg, blk);
+    };
+    load_meta(0, cur_id, cur_seg, cur_blk);
+    if (n > 32) load_meta(1, nxt_id, nxt_seg, nxt_blk);
+    int kc = 0;
+
+    const uint64_t policy = l2_evict_first_policy();
+    const int qbytes_per_pos = a.group * kRowBytes;
+    auto issue = [&](int j) {
+        const bool in_cur = (j >> 5) == kc;
+        const int src = j & 31;
+        int id = __shfl_sync(kFull, in_cur ? cur_id : nxt_id, src);
+        const int seg = __shfl_sync(kFull, in_cur ? cur_seg : nxt_seg, src);
+        const int blk = __shfl_sync(kFull, in_cur ? cur_blk : nxt_blk, src);
+        if (lane == 0) {
+            if (id < 0 || id >= a.num_blocks) {
+                flag_error(a.err, TTS_ERRBIT_BLOCK_ID);
+                id = -1;
+            }
+            const int st = j % n_stages;
+            const uint32_t bar = bar0 + 8 * st;
+            const uint32_t dst = stage0 + st * S.stage_bytes;
+            const bool need_q = j == 0 || blk == 0;
+            const uint32_t bytes = (id >= 0 ? kKVStageBytes : 0) + (need_q ? a.q_len * qbytes_per_pos : 0);
+            if (bytes == 0) {
+                mbar_arrive(bar);
+            } else {
+                mbar_arrive_expect_tx(bar, bytes);
+                if (id >= 0) {
+                    const int row = (id * a.Hkv + seg % a.Hkv) * TTS_BLOCK_TOKENS;
+                    tma_load_2d(dst, &kmap, 0, row, bar, policy);
+                    tma_load_2d(dst + kBoxBytes, &kmap, 64, row, bar, policy);
+                    tma_load_2d(dst + 2 * kBoxBytes, &vmap, 0, row, bar, policy);
+                    tma_load_2d(dst + 3 * kBoxBytes, &vmap, 64, row, bar, policy);
+                }
+                if (need_q) {
+                    const int b = seg / a.Hkv, g = seg % a.Hkv;
+                    for (int jq = 0; jq < a.q_len; ++jq) {
+                        const size_t qoff =
+                            ((static_cast<size_t>(b) * a.q_len + jq) * a.Hq + g * a.group) * kRowBytes;
+                        bulk_load_nohint(dst + kKVStageBytes + jq * qbytes_per_pos, a.q + qoff,
+                                         qbytes_per_pos, bar);
+                    }
+                }
+            }
+        }
+    };
+    for (int j = 0; j < min(n_stages, n); ++j) issue(j);
+
+    // Fragment coordinates: g = lane / 4 (accumulator row, and row g + 8), t = lane % 4.
+    const int fg = lane >> 2, ft = lane & 3;
+    // ldmatrix row-address roles: matrix mi = lane / 8, row mr = lane % 8.
+    const int mi = lane >> 3, mr = lane & 7;
+
+    int seg_id = -1, seg_b = 0, seg_g = 0, seg_L = 0, s0 = 0, s1 = 0;
+    int limA = 0, limB = 0;                 // visible-token limits of rows fg and fg + 8
+    uint32_t qa[8][4];                      // Q A-fragments, 8 k-steps of 16 dims
+    float mA = kNegBig, mB = kNegBig, lA = 0.0f, lB = 0.0f;
+    float o[16][4];                         // O accumulators, 16 n-tiles of 8 dims
+
+    auto flush = [&]() {
+        float la = lA, lb = lB;
+        la += __shfl_xor_sync(kFull, la, 1);
+        la += __shfl_xor_sync(kFull, la, 2);
+        lb += __shfl_xor_sync(kFull, lb, 1);
+        lb += __shfl_xor_sync(kFull, lb, 2);
+        const int rA = fg, rB = fg + 8;
+        if (s0 >= t0 && s1 <= t1) {
+            // whole segment in this warp: write the output rows
+            const float ia = la > 0.0f ? 1.0f / la : 0.0f, ib = lb > 0.0f ? 1.0f / lb : 0.0f;
+            if (rA < n_rows) {
+                uint32_t *dst = reinterpret_cast<uint32_t *>(out_row<T, D>(a, seg_b, seg_g, rA));
+#pragma unroll
+                for (int nt = 0; nt < 16; ++nt) dst[nt * 4 + ft] = pack_bf16x2(o[nt][0] * ia, o[nt][1] * ia);
+            }
+            if (rB < n_rows) {
+                uint32_t *dst = reinterpret_cast<uint32_t *>(out_row<T, D>(a, seg_b, seg_g, rB));
+#pragma unroll
+                for (int nt = 0; nt < 16; ++nt) dst[nt * 4 + ft] = pack_bf16x2(o[nt][2] * ib, o[nt][3] * ib);
+            }
+            return;
+        }
+        const int NRS = a.nr_slot;
+        const size_t SF = static_cast<size_t>(NRS) * D + 2 * NRS;
+        float *part = a.part + (static_cast<size_t>(wid) * 2 + (s0 <= t0 ? 0 : 1)) * SF;
+        if (rA < n_rows) {
+#pragma unroll
+            for (int nt = 0; nt < 16; ++nt)
+                *reinterpret_cast<float2 *>(part + rA * D + nt * 8 + 2 * ft) = make_float2(o[nt][0], o[nt][1]);
+            if (ft == 0) { part[NRS * D + rA] = mA; part[NRS * D + NRS + rA] = la; }
+        }
+        if (rB < n_rows) {
+#pragma unroll
+            for (int nt = 0; nt < 16; ++nt)
+                *reinterpret_cast<float2 *>(part + rB * D + nt * 8 + 2 * ft) = make_float2(o[nt][2], o[nt][3]);
+            if (ft == 0) { part[NRS * D + rB] = mB; part[NRS * D + NRS + rB] = lb; }
+        }
+        finish_split_segment<T, D>(a, seg_id, s0, s1, n_rows, Ttot, Wtot, lane);
+    };
+
+    bool timed_out = false;
+    int waited = 0;
+    for (int i = 0; i < n; ++i) {
+        if ((i & 31) == 0 && i > 0) {
+            kc = i >> 5;
+            cur_id = nxt_id; cur_seg = nxt_seg; cur_blk = nxt_blk;
+            if (n > 32 * (kc + 1)) load_meta(kc + 1, nxt_id, nxt_seg, nxt_blk);
+        }
+        const int st = i % n_stages;
+        if (!timed_out) {
+            const bool ok = mbar_wait(bar0 + 8 * st, (i / n_stages) & 1);
+            if (__any_sync(kFull, !ok)) {
+                timed_out = true;
+                if (lane == 0) flag_error(a.err, TTS_ERRBIT_TIMEOUT);
+            } else {
+                waited = i + 1;
+            }
+        }
+        const int src = i & 31;
+        const int t_id = __shfl_sync(kFull, cur_id, src);
+        const int t_seg = __shfl_sync(kFull, cur_seg, src);
+        const int t_blk = __shfl_sync(kFull, cur_blk, src);
+        const uint32_t kt = stage0 + st * S.stage_bytes;  // K boxes
+        const uint32_t vt = kt + 2 * kBoxBytes;            // V boxes
+        if (i == 0 || t_blk == 0) {
+            // ---- a new segment: finish the previous one, set up this one
+            if (i > 0) flush();
+            seg_id = t_seg;
+            seg_b = t_seg / a.Hkv;
+            seg_g = t_seg % a.Hkv;
+            seg_L = ctxs[seg_b];
+            const int nb = (seg_L + TTS_BLOCK_TOKENS - 1) / TTS_BLOCK_TOKENS;
+            s0 = prefix[seg_b] + seg_g * nb;
+            s1 = s0 + nb;
+            const int rA = fg, rB = fg + 8;
+            limA = rA < n_rows ? (a.causal ? seg_L - a.q_len + rA / a.group + 1 : seg_L) : 0;
+            limB = rB < n_rows ? (a.causal ? seg_L - a.q_len + rB / a.group + 1 : seg_L) : 0;
+            mA = mB = kNegBig;
+            lA = lB = 0.0f;
+            const uint32_t qs = kt + kKVStageBytes;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const int c0 = (16 * ks + 2 * ft) * 2;  // byte offset of dims 2t, 2t+1 in the row
+                qa[ks][0] = (rA < n_rows && !timed_out) ? *reinterpret_cast<const uint32_t *>(smem + (qs - base) + rA * kRowBytes + c0) : 0u;
+                qa[ks][1] = (rB < n_rows && !timed_out) ? *reinterpret_cast<const uint32_t *>(smem + (qs - base) + rB * kRowBytes + c0) : 0u;
+                qa[ks][2] = (rA < n_rows && !timed_out) ? *reinterpret_cast<const uint32_t *>(smem + (qs - base) + rA * kRowBytes + c0 + 16) : 0u;
+                qa[ks][3] = (rB < n_rows && !timed_out) ? *reinterpret_cast<const uint32_t *>(smem + (qs - base) + rB * kRowBytes + c0 + 16) : 0u;
+            }
+#pragma unroll
+            for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[nt][e] = 0.0f;
+        }
+        if (!timed_out && t_id >= 0 && t_id < a.num_blocks) {
+            const int base_tok = t_blk * TTS_BLOCK_TOKENS;
+            // ---- S = Q K^T: 2 n-tiles of 8 tokens x 8 k-steps of 16 dims
+            float s[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[nt][e] = 0.0f;
+#pragma unroll
+                for (int kp = 0; kp < 4; ++kp) {
+                    // matrices: (k-step 2kp, low/high 8 dims), (k-step 2kp+1, low/high)
+                    const int ch = 2 * (2 * kp + (mi >> 1)) + (mi & 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(swz(kt, 8 * nt + mr, ch), b0, b1, b2, b3);
+                    mma_bf16_16816(s[nt], qa[2 * kp], b0, b1);
+                    mma_bf16_16816(s[nt], qa[2 * kp + 1], b2, b3);
+                }
+            }
+            // ---- online softmax in the log2 domain; rows fg (A) and fg + 8 (B)
+            float xa[4], xb[4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int tok = base_tok + 8 * nt + 2 * ft + e;
+                    xa[2 * nt + e] = tok < limA ? s[nt][e] * a.qscale : -INFINITY;
+                    xb[2 * nt + e] = tok < limB ? s[nt][2 + e] * a.qscale : -INFINITY;
+                }
+            }
+            float ma = fmaxf(fmaxf(xa[0], xa[1]), fmaxf(xa[2], xa[3]));
+            float mb = fmaxf(fmaxf(xb[0], xb[1]), fmaxf(xb[2], xb[3]));
+            ma = fmaxf(ma, __shfl_xor_sync(kFull, ma, 1));
+            ma = fmaxf(ma, __shfl_xor_sync(kFull, ma, 2));
+            mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 1));
+            mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 2));
+            const float na = fmaxf(mA, ma), nb2 = fmaxf(mB, mb);
+            const float aa = exp2f(mA - na), ab = exp2f(mB - nb2);
+            mA = na;
+            mB = nb2;
+            float pa[4], pb[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                pa[e] = exp2f(xa[e] - na);
+                pb[e] = exp2f(xb[e] - nb2);
+            }
+            lA = lA * aa + (pa[0] + pa[1]) + (pa[2] + pa[3]);
+            lB = lB * ab + (pb[0] + pb[1]) + (pb[2] + pb[3]);
+            if (__any_sync(kFull, aa != 1.0f || ab != 1.0f)) {
+#pragma unroll
+                for (int nt = 0; nt < 16; ++nt) {
+                    o[nt][0] *= aa; o[nt][1] *= aa;
+                    o[nt][2] *= ab; o[nt][3] *= ab;
+                }
+            }
+            // P as the A operand (rows fg / fg + 8, tokens 2t, 2t+1, 2t+8, 2t+9)
+            uint32_t pf[4];
+            pf[0] = pack_bf16x2(pa[0], pa[1]);
+            pf[1] = pack_bf16x2(pb[0], pb[1]);
+            pf[2] = pack_bf16x2(pa[2], pa[3]);
+            pf[3] = pack_bf16x2(pb[2], pb[3]);
+            // Tokens past the context may hold anything (even NaN): zero their V rows.
+            if (base_tok + TTS_BLOCK_TOKENS > seg_L) {
+                const int first_bad = max(seg_L - base_tok, 0);
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                for (int idx = lane; idx < (TTS_BLOCK_TOKENS - first_bad) * 16; idx += 32) {
+                    const int row = first_bad + idx / 16, ch = idx % 16;
+                    *reinterpret_cast<uint4 *>(smem + (swz(vt, row, ch) - base)) = z;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            // ---- O += P V: 8 pairs of n-tiles (16 dims each), k = 16 tokens
+#pragma unroll
+            for (int np = 0; np < 8; ++np) {
+                const int tok = mr + 8 * (mi & 1);
+                const int ch = 2 * np + (mi >> 1);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(swz(vt, tok, ch), b0, b1, b2, b3);
+                mma_bf16_16816(o[2 * np], pf, b0, b1);
+                mma_bf16_16816(o[2 * np + 1], pf, b2, b3);
+            }
+        }
+        __syncwarp();
+        if (!timed_out && i + n_stages < n) issue(i + n_stages);
+    }
+    flush();
+    if (timed_out) {
+        const int issued = min(n, waited + n_stages);
+        for (int i = waited; i < issued; ++i) mbar_wait(bar0 + 8 * (i % n_stages), (i / n_stages) & 1);
+    }
+}
+
+// ------------------------------------------------------------------- launch
+
+// Query-row counts per (stream, KV head) are padded up to one of these.
 constexpr int kRowTemplates[] = {2, 4, 8, 10, 16};
 
 int padded_rows(int rows) {
@@ -476,18 +908,20 @@ int padded_rows(int rows) {
     return 0;
 }
 
-int ctas_per_sm(int nr) { return nr <= 4 ? 3 : 1; }
+int ctas_per_sm(int dtype, int nr) {
+    if (dtype == TTS_BF16) return kTcCtasPerSm;
+    return nr <= 4 ? 3 : 1;
+}
 
 int device_sms() {
     const int n = sm_count();
     return n > 0 ? n : 160;  // no device visible (size queries on a build host)
 }
 
-template <typename T, int NR>
-int launch_nr(const AttnArgs &a, int ctas, cudaStream_t stream) {
-    constexpr int D = 16 * Chunk<T>::N;
-    const size_t smem = AttnSmem<NR, D>::total(a.B);
-    auto kern = decode_attn_kernel<T, NR>;
+template <int NR>
+int launch_simt_nr(const AttnArgs &a, int ctas, cudaStream_t stream) {
+    const size_t smem = SimtSmem<NR>::total(a.B);
+    auto kern = decode_attn_simt_kernel<NR>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return TTS_ERR_CUDA;
@@ -495,16 +929,55 @@ int launch_nr(const AttnArgs &a, int ctas, cudaStream_t stream) {
     return launch_status();
 }
 
-template <typename T>
-int launch_typed(const AttnArgs &a, int nr, int ctas, cudaStream_t stream) {
+int launch_simt(const AttnArgs &a, int nr, int ctas, cudaStream_t stream) {
     switch (nr) {
-        case 2: return launch_nr<T, 2>(a, ctas, stream);
-        case 4: return launch_nr<T, 4>(a, ctas, stream);
-        case 8: return launch_nr<T, 8>(a, ctas, stream);
-        case 10: return launch_nr<T, 10>(a, ctas, stream);
-        case 16: return launch_nr<T, 16>(a, ctas, stream);
+        case 2: return launch_simt_nr<2>(a, ctas, stream);
+        case 4: return launch_simt_nr<4>(a, ctas, stream);
+        case 8: return launch_simt_nr<8>(a, ctas, stream);
+        case 10: return launch_simt_nr<10>(a, ctas, stream);
+        case 16: return launch_simt_nr<16>(a, ctas, stream);
         default: return TTS_ERR_UNSUPPORTED;
     }
+}
+
+// TMA descriptors of the pools, cached by (address, rows): building one is a
+// driver call, and a serving loop passes the same pools every step.
+struct MapCacheEntry {
+    const void *ptr;
+    uint64_t rows;
+    CUtensorMap map;
+};
+std::mutex g_map_mu;
+MapCacheEntry g_map_cache[8];
+int g_map_next = 0;
+
+bool pool_map(CUtensorMap *out, const void *ptr, uint64_t rows) {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (const auto &e : g_map_cache)
+        if (e.ptr == ptr && e.rows == rows) {
+            *out = e.map;
+            return true;
+        }
+    MapCacheEntry e;
+    e.ptr = ptr;
+    e.rows = rows;
+    if (!make_tma_2d_bf16(&e.map, ptr, rows, 128, TTS_BLOCK_TOKENS, 64)) return false;
+    g_map_cache[g_map_next] = e;
+    g_map_next = (g_map_next + 1) % 8;
+    *out = e.map;
+    return true;
+}
+
+int launch_tc(const AttnArgs &a, int ctas, cudaStream_t stream) {
+    const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * a.Hkv * TTS_BLOCK_TOKENS;
+    CUtensorMap kmap, vmap;
+    if (!pool_map(&kmap, a.k_pool, rows) || !pool_map(&vmap, a.v_pool, rows)) return TTS_ERR_CUDA;
+    const size_t smem = tc_smem(a.group * a.q_len, a.B, a.stages).total;
+    if (cudaFuncSetAttribute(decode_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+        return TTS_ERR_CUDA;
+    decode_attn_tc_kernel<<<ctas, kTcWarps * 32, smem, stream>>>(kmap, vmap, a);
+    return launch_status();
 }
 
 bool supported_head(int dtype, int head_dim) {
@@ -513,7 +986,7 @@ bool supported_head(int dtype, int head_dim) {
 
 }  // namespace
 
-bool attn_plan(int B, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
+bool attn_plan(int dtype, int B, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
                int max_ctx_len, AttnPlan *out) {
     if (B < 1 || q_len < 1 || num_kv_heads < 1 || num_q_heads < num_kv_heads ||
         num_q_heads % num_kv_heads != 0 || head_dim < 1 || max_ctx_len < q_len ||
@@ -524,8 +997,8 @@ bool attn_plan(int B, int q_len, int num_q_heads, int num_kv_heads, int head_dim
     const long long nblk = (max_ctx_len + TTS_BLOCK_TOKENS - 1) / TTS_BLOCK_TOKENS;
     if (static_cast<long long>(B) * num_kv_heads * nblk >= (1LL << 31)) return false;
     out->rows = rows;
-    out->ctas = device_sms() * ctas_per_sm(rows);
-    out->workers = out->ctas * kWarps;
+    out->ctas = device_sms() * ctas_per_sm(dtype, rows);
+    out->workers = out->ctas * (dtype == TTS_BF16 ? kTcWarps : kWarps);
     return true;
 }
 
@@ -541,7 +1014,8 @@ extern "C" size_t tts_decode_attn_workspace_size(int32_t B, int32_t q_len, int32
                                                  int32_t num_kv_heads, int32_t head_dim,
                                                  int32_t max_ctx_len) {
     tts::AttnPlan pl;
-    if (!tts::attn_plan(B, q_len, num_q_heads, num_kv_heads, head_dim, max_ctx_len, &pl))
+    const int dtype = head_dim == 64 ? TTS_F32 : TTS_BF16;
+    if (!tts::attn_plan(dtype, B, q_len, num_q_heads, num_kv_heads, head_dim, max_ctx_len, &pl))
         return 0;
     return tts::attn_workspace_bytes(B, num_kv_heads, head_dim, pl);
 }
@@ -560,9 +1034,12 @@ extern "C" int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block
     if (cache->block_size != TTS_BLOCK_TOKENS) return TTS_ERR_UNSUPPORTED;
     if (!supported_head(cache->dtype, cache->head_dim)) return TTS_ERR_UNSUPPORTED;
     if (cache->num_kv_heads < 1) return TTS_ERR_INVALID;
+    if (static_cast<long long>(cache->num_blocks) * cache->num_kv_heads * TTS_BLOCK_TOKENS >= (1LL << 31))
+        return TTS_ERR_UNSUPPORTED;
     if (B == 0) return TTS_OK;
     AttnPlan pl;
-    if (!attn_plan(B, q_len, num_q_heads, cache->num_kv_heads, cache->head_dim, max_ctx_len, &pl)) {
+    if (!attn_plan(cache->dtype, B, q_len, num_q_heads, cache->num_kv_heads, cache->head_dim,
+                   max_ctx_len, &pl)) {
         const int nh = cache->num_kv_heads;
         const bool shape_ok = num_q_heads >= nh && num_q_heads % nh == 0 && max_ctx_len >= q_len &&
                               max_ctx_len <= (1 << 24);
@@ -596,10 +1073,12 @@ extern "C" int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block
     a.counters = reinterpret_cast<int32_t *>(
         ws + need - align_up(static_cast<size_t>(B) * cache->num_kv_heads * sizeof(int32_t), 256));
     a.workers = pl.workers;
+    a.nr_slot = pl.rows;
+    a.stages = cache->dtype == TTS_BF16 ? tc_stages(a.group * q_len, B) : kStages;
+    if (a.stages < 1) return TTS_ERR_UNSUPPORTED;
     a.err = d_err;
     auto s = static_cast<cudaStream_t>(stream);
-    return cache->dtype == TTS_BF16 ? launch_typed<__nv_bfloat16>(a, pl.rows, pl.ctas, s)
-                                    : launch_typed<float>(a, pl.rows, pl.ctas, s);
+    return cache->dtype == TTS_BF16 ? launch_tc(a, pl.ctas, s) : launch_simt(a, pl.rows, pl.ctas, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -618,7 +1097,7 @@ extern "C" int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block
 namespace tts {
 namespace {
 
-constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB
+constexpr size_t kStaticScratchBytes = size_t(24) << 20;  // 24 MiB
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_attn_scratch[kStaticScratchBytes];

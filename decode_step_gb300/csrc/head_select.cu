@@ -21,10 +21,6 @@
 //
 // fp32: a CUDA-core kernel (tf32 tensor cores would change the rounding of
 // fp32 inputs), one warp per vocabulary row.
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
 #include "tts_common.cuh"
 #include "tts_internal.h"
 
@@ -449,31 +445,10 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
 
 // ------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
 // 2-D bf16 tensor [rows][cols] (cols contiguous), box [box_rows][64], 128-byte swizzle.
 bool make_map(CUtensorMap *map, const void *ptr, int rows, int cols, int box_rows) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileK), static_cast<cuuint32_t>(box_rows)};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return make_tma_2d_bf16(map, ptr, static_cast<uint64_t>(rows), static_cast<uint64_t>(cols),
+                            static_cast<uint32_t>(box_rows), static_cast<uint32_t>(kTileK));
 }
 
 struct TcPlan {

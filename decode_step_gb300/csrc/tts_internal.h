@@ -1,6 +1,7 @@
 // Host-side helpers shared by the C-ABI entry points.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -11,6 +12,13 @@ namespace tts {
 
 // Number of SMs of the current device (cached per device ordinal).
 int sm_count();
+
+// TMA descriptor of a 2-D bf16 tensor [rows][cols] (cols contiguous) read in
+// boxes of box_rows x box_cols with 128-byte swizzle (box_cols * 2 <= 128);
+// out-of-range box elements read as zero.  false if the driver entry point is
+// unavailable or the driver rejects the shape.
+bool make_tma_2d_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols,
+                      uint32_t box_rows, uint32_t box_cols);
 
 // Maps the last launch error to a status (clears it).
 inline int launch_status() {
@@ -28,8 +36,8 @@ struct AttnPlan {
     int ctas;     // CTAs launched
     int workers;  // warps, each owning one contiguous range of tiles
 };
-bool attn_plan(int B, int q_len, int num_q_heads, int num_kv_heads, int head_dim, int max_ctx_len,
-               AttnPlan *out);
+bool attn_plan(int dtype, int B, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
+               int max_ctx_len, AttnPlan *out);
 size_t attn_workspace_bytes(int B, int num_kv_heads, int head_dim, const AttnPlan &pl);
 
 }  // namespace tts
