@@ -320,8 +320,11 @@ def run_native(args):
         run_step()
     torch.cuda.synchronize()
 
+    # ---- timed region: K whole steps (one tts_decode_step call each: append,
+    # attention and head, the later two as programmatic dependents), L2
+    # flushed before every step outside the events.
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     try:
         uuid = str(torch.cuda.get_device_properties(device).uuid)
         gpu_id = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
@@ -334,7 +337,26 @@ def run_native(args):
     torch.cuda.synchronize()
     for i in range(K):
         flush.zero_()
-        e = ev[i]
+        ev[i][0].record(stream)
+        run_step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    t_step = [e[0].elapsed_time(e[1]) for e in ev]
+    ms_local = statistics.fmean(t_step)
+    all_ms = max_over_ranks(ms_local, world, device)
+    ms, value = combine_rank_times(all_ms, w.B * w.q_len)
+    errflags = int(step.err.item())
+
+    # ---- per-kernel durations: the same kernels launched one by one, each
+    # bracketed by events (no overlap between them), L2 flushed per step.
+    K2 = min(K, 1000)
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K2)]
+    for i in range(K2):
+        flush.zero_()
+        e = kev[i]
         e[0].record(stream)
         bd.tts_kv_append(cache, d["block_table"], d["ctx_before"], d["k_new"], d["v_new"], err=step.err)
         e[1].record(stream)
@@ -345,40 +367,26 @@ def run_native(args):
                                     temperature=w.T, seed=seed, step=stp)
         e[3].record(stream)
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    clk = clocks.stop()
-    t_app = [e[0].elapsed_time(e[1]) for e in ev]
-    t_att = [e[1].elapsed_time(e[2]) for e in ev]
-    t_head = [e[2].elapsed_time(e[3]) for e in ev]
-    t_step = [e[0].elapsed_time(e[3]) for e in ev]
-    ms_local = statistics.fmean(t_step)
-    all_ms = max_over_ranks(ms_local, world, device)
-    ms, value = combine_rank_times(all_ms, w.B * w.q_len)
-    errflags = int(step.err.item())
+    t_app = [e[0].elapsed_time(e[1]) for e in kev]
+    t_att = [e[1].elapsed_time(e[2]) for e in kev]
+    t_head = [e[2].elapsed_time(e[3]) for e in kev]
 
-    # ---- end to end through the public API with host buffers
-    host = {k: torch.from_numpy(np.ascontiguousarray(inp[k]).view(
-        np.int16 if inp[k].dtype == np.uint16 else inp[k].dtype)).pin_memory() for k in names}
-    ids_host = torch.empty(w.R, dtype=torch.int32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = ids_host.numel() * 4
+    # ---- end to end through the public API with host buffers: a captured
+    # graph copies the step's inputs in from pinned host memory, runs the
+    # step and copies the ids back; wall clock, synchronised every step.
+    from decode_step_gb300.step import GraphedStep
+    g_inputs = {k: d[k] for k in names}
+    if mode == bd.TTS_GUMBEL:
+        g_inputs["seed"], g_inputs["step"] = seed, stp
+    graphed = GraphedStep(step, g_inputs)
+    h2d = graphed.h2d_bytes
+    d2h = step.R * 4
     n_e2e = max(10, min(args.e2e_steps, K))
-
-    def e2e_step():
-        for k in names:
-            dst = d[k] if d[k].dtype != torch.bfloat16 else d[k].view(torch.int16)
-            dst.copy_(host[k], non_blocking=True)
-        ids = run_step()
-        ids_host.copy_(ids, non_blocking=True)
-        stream.synchronize()
-
     for _ in range(5):
-        e2e_step()
-    torch.cuda.synchronize()
+        graphed()
     t0 = time.perf_counter()
     for _ in range(n_e2e):
-        e2e_step()
+        graphed()
     e2e_s = time.perf_counter() - t0
     e2e_all = max_over_ranks(e2e_s / n_e2e * 1e3, world, device)
     _, e2e_value = combine_rank_times(e2e_all, w.B * w.q_len)
@@ -409,6 +417,8 @@ def run_native(args):
                      if peak_kind == "measured" else "fallback"},
         "kernels": {
             "kv_append_us": app_us, "decode_attn_us": att_us, "head_select_us": head_us,
+            "step_us": 1e3 * ms,
+            "sum_of_kernels_us": app_us + att_us + head_us,
             "decode_attn_us_median": 1e3 * statistics.median(t_att),
             "head_select_us_median": 1e3 * statistics.median(t_head),
             "kv_append_gbs": append_bytes(w) / (app_us * 1e-6) / 1e9,
@@ -417,11 +427,15 @@ def run_native(args):
                               "algorithmic_bytes": hb, "tflops": head_tflops},
         },
         "gpu_launches": 3 * K,
+        "step_note": "each timed step is one tts_decode_step call (append, attention, head; "
+                     "the last two launched as programmatic dependents); per-kernel times come "
+                     "from a separate pass launching the kernels one by one",
         "device_error_flags": errflags,
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": n_e2e, "note": "wall clock; pinned host inputs copied in and ids read "
-                                        "back (with a stream sync) every step"},
+                "steps": n_e2e, "note": "wall clock; a captured CUDA graph copies the inputs in from "
+                                        "pinned host memory, runs the step and copies the ids back; "
+                                        "the host synchronises every step"},
     }
     if world == 1:
         line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)

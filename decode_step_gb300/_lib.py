@@ -48,6 +48,10 @@ _SIGNATURES = {
                                                 _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "tts_spec_verify": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _f32, _vp, _vp, _i32,
                                        _vp, _vp, _vp, _vp]),
+    "tts_decode_step": (ctypes.c_int, [ctypes.POINTER(KVCacheDesc), _vp, _i32, _vp, _vp, _i32, _i32,
+                                       _i32, _i32, _f32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp,
+                                       _i32, _i32, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
+                                       _vp, _vp]),
     "tts_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "tts_version": (ctypes.c_int, []),
 }

@@ -194,6 +194,33 @@ def tts_spec_verify(target_logits, draft_probs, draft_tokens, temperature, seed,
     check("tts_spec_verify", lib().tts_spec_verify(*args))
 
 
+def tts_decode_step(cache: KVCache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new,
+                    attn_out, attn_ws, scale, W, ids, head_ws, causal=False, mode=TTS_ARGMAX,
+                    temperature=0.0, seed=None, step=None, eos_allowed=None, best=None,
+                    logits_out=None, err=None, stream=None):
+    B, max_blocks = block_table.shape
+    _, q_len, Hq, D = q.shape
+    kv_shape = (B, q_len, cache.num_kv_heads, cache.head_dim)
+    R, V = B * q_len, W.shape[0]
+    if W.dtype != cache.dtype or W.shape[1] != Hq * D:
+        raise ValueError("W must be [V][num_q_heads * head_dim] in the cache dtype")
+    args = (ctypes.byref(cache.desc), _dev(block_table, "block_table", torch.int32), max_blocks,
+            _dev(ctx_before, "ctx_before", torch.int32, (B,)), _dev(ctx_lens, "ctx_lens", torch.int32, (B,)),
+            int(max_ctx_len), B, q_len, Hq, float(scale), int(bool(causal)),
+            _dev(q, "q", cache.dtype, (B, q_len, Hq, cache.head_dim)),
+            _dev(k_new, "k_new", cache.dtype, kv_shape), _dev(v_new, "v_new", cache.dtype, kv_shape),
+            _dev(attn_out, "attn_out", cache.dtype, (B, q_len, Hq, cache.head_dim)), _dev(attn_ws, "attn_ws"),
+            attn_ws.numel() * attn_ws.element_size(), _dev(W, "W"), V, int(mode), float(temperature),
+            _keys(seed, "seed", R), _keys(step, "step", R),
+            None if eos_allowed is None else _dev(eos_allowed, "eos_allowed", torch.uint8, (R,)),
+            _dev(ids, "ids", torch.int32, (R,)),
+            None if best is None else _dev(best, "best", torch.float32, (R,)),
+            None if logits_out is None else _dev(logits_out, "logits_out", torch.float32, (R, V)),
+            _dev(head_ws, "head_ws"), head_ws.numel() * head_ws.element_size(),
+            None if err is None else _dev(err, "err", torch.int32), _stream(stream))
+    check("tts_decode_step", lib().tts_decode_step(*args))
+
+
 def tts_status_string(code: int) -> str:
     return _lib.status_string(code)
 

@@ -35,6 +35,7 @@
 // recursive halving, leaving every lane the full scores of one token for half
 // of the query rows.
 #include <mutex>
+#include <new>
 
 #include "tts_common.cuh"
 #include "tts_internal.h"
@@ -268,6 +269,7 @@ decode_attn_simt_kernel(const AttnArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_rows = a.group * a.q_len;
 
+    pdl_allow_dependents();
     scan_streams<T, D, kWarps>(a, prefix, ctxs, scan);
     const long long Ttot = prefix[a.B];
     const long long Wtot = min(static_cast<long long>(a.workers), Ttot);
@@ -338,6 +340,7 @@ decode_attn_simt_kernel(const AttnArgs a) {
             }
         }
     };
+    pdl_wait_prerequisites();  // the pool may have been written by the kernel before
     for (int j = 0; j < min(kStages, n); ++j) issue(j);
 
     const int p = lane >> 4, c = lane & 15;
@@ -628,6 +631,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
     int *scan = ctxs + a.B;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    pdl_allow_dependents();
     scan_streams<T, D, kTcWarps>(a, prefix, ctxs, scan);
     const long long Ttot = prefix[a.B];
     const long long Wtot = min(static_cast<long long>(a.workers), Ttot);
@@ -699,6 +703,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
             }
         }
     };
+    pdl_wait_prerequisites();  // the pool may have been written by the kernel before
     for (int j = 0; j < min(n_stages, n); ++j) issue(j);
 
     // Fragment coordinates: g = lane / 4 (accumulator row, and row g + 8), t = lane % 4.
@@ -918,66 +923,61 @@ int device_sms() {
     return n > 0 ? n : 160;  // no device visible (size queries on a build host)
 }
 
-template <int NR>
-int launch_simt_nr(const AttnArgs &a, int ctas, cudaStream_t stream) {
-    const size_t smem = SimtSmem<NR>::total(a.B);
-    auto kern = decode_attn_simt_kernel<NR>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-        return TTS_ERR_CUDA;
-    kern<<<ctas, kWarps * 32, smem, stream>>>(a);
-    return launch_status();
+cudaLaunchAttribute pdl_attr() {
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at.val.programmaticStreamSerializationAllowed = 1;
+    return at;
 }
 
-int launch_simt(const AttnArgs &a, int nr, int ctas, cudaStream_t stream) {
+template <int NR>
+int launch_simt_nr(const AttnArgs &a, int ctas, LaunchOpts o) {
+    const size_t smem = SimtSmem<NR>::total(a.B);
+    auto kern = decode_attn_simt_kernel<NR>;
+    if (!ensure_dynamic_smem(reinterpret_cast<const void *>(kern), static_cast<int>(smem))) return TTS_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas, 1, 1);
+    cfg.blockDim = dim3(kWarps * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = o.stream;
+    cudaLaunchAttribute attr[1] = {pdl_attr()};
+    cfg.attrs = attr;
+    cfg.numAttrs = o.pdl ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) {
+        cudaGetLastError();
+        return TTS_ERR_CUDA;
+    }
+    return TTS_OK;
+}
+
+int launch_simt(const AttnArgs &a, int nr, int ctas, LaunchOpts o) {
     switch (nr) {
-        case 2: return launch_simt_nr<2>(a, ctas, stream);
-        case 4: return launch_simt_nr<4>(a, ctas, stream);
-        case 8: return launch_simt_nr<8>(a, ctas, stream);
-        case 10: return launch_simt_nr<10>(a, ctas, stream);
-        case 16: return launch_simt_nr<16>(a, ctas, stream);
+        case 2: return launch_simt_nr<2>(a, ctas, o);
+        case 4: return launch_simt_nr<4>(a, ctas, o);
+        case 8: return launch_simt_nr<8>(a, ctas, o);
+        case 10: return launch_simt_nr<10>(a, ctas, o);
+        case 16: return launch_simt_nr<16>(a, ctas, o);
         default: return TTS_ERR_UNSUPPORTED;
     }
 }
 
-// TMA descriptors of the pools, cached by (address, rows): building one is a
-// driver call, and a serving loop passes the same pools every step.
-struct MapCacheEntry {
-    const void *ptr;
-    uint64_t rows;
-    CUtensorMap map;
-};
-std::mutex g_map_mu;
-MapCacheEntry g_map_cache[8];
-int g_map_next = 0;
-
-bool pool_map(CUtensorMap *out, const void *ptr, uint64_t rows) {
-    std::lock_guard<std::mutex> lock(g_map_mu);
-    for (const auto &e : g_map_cache)
-        if (e.ptr == ptr && e.rows == rows) {
-            *out = e.map;
-            return true;
-        }
-    MapCacheEntry e;
-    e.ptr = ptr;
-    e.rows = rows;
-    if (!make_tma_2d_bf16(&e.map, ptr, rows, 128, TTS_BLOCK_TOKENS, 64)) return false;
-    g_map_cache[g_map_next] = e;
-    g_map_next = (g_map_next + 1) % 8;
-    *out = e.map;
-    return true;
-}
-
-int launch_tc(const AttnArgs &a, int ctas, cudaStream_t stream) {
-    const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * a.Hkv * TTS_BLOCK_TOKENS;
-    CUtensorMap kmap, vmap;
-    if (!pool_map(&kmap, a.k_pool, rows) || !pool_map(&vmap, a.v_pool, rows)) return TTS_ERR_CUDA;
+int launch_tc(const AttnArgs &a, const CUtensorMap &kmap, const CUtensorMap &vmap, int ctas, LaunchOpts o) {
     const size_t smem = tc_smem(a.group * a.q_len, a.B, a.stages).total;
-    if (cudaFuncSetAttribute(decode_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
+    if (!ensure_dynamic_smem(reinterpret_cast<const void *>(decode_attn_tc_kernel), static_cast<int>(smem)))
         return TTS_ERR_CUDA;
-    decode_attn_tc_kernel<<<ctas, kTcWarps * 32, smem, stream>>>(kmap, vmap, a);
-    return launch_status();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas, 1, 1);
+    cfg.blockDim = dim3(kTcWarps * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = o.stream;
+    cudaLaunchAttribute attr[1] = {pdl_attr()};
+    cfg.attrs = attr;
+    cfg.numAttrs = o.pdl ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, decode_attn_tc_kernel, kmap, vmap, a) != cudaSuccess) {
+        cudaGetLastError();
+        return TTS_ERR_CUDA;
+    }
+    return TTS_OK;
 }
 
 bool supported_head(int dtype, int head_dim) {
@@ -1020,12 +1020,19 @@ extern "C" size_t tts_decode_attn_workspace_size(int32_t B, int32_t q_len, int32
     return tts::attn_workspace_bytes(B, num_kv_heads, head_dim, pl);
 }
 
-extern "C" int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block_table,
-                               int32_t max_blocks_per_seq, const int32_t *d_ctx_lens,
-                               int32_t max_ctx_len, int32_t B, int32_t q_len, int32_t num_q_heads,
-                               float scale, int32_t causal, const void *d_q, void *d_out,
-                               void *d_ws, size_t ws_bytes, int32_t *d_err, void *stream) {
-    using namespace tts;
+namespace tts {
+
+struct AttnLaunchState {
+    AttnArgs a;
+    CUtensorMap kmap, vmap;
+    int dtype, rows, ctas;
+};
+static_assert(sizeof(AttnLaunchState) <= sizeof(AttnLaunch::storage), "AttnLaunch storage too small");
+
+int prepare_attn(const tts_kv_cache *cache, const int32_t *d_block_table, int32_t max_blocks_per_seq,
+                 const int32_t *d_ctx_lens, int32_t max_ctx_len, int32_t B, int32_t q_len,
+                 int32_t num_q_heads, float scale, int32_t causal, const void *d_q, void *d_out,
+                 void *d_ws, size_t ws_bytes, int32_t *d_err, AttnLaunch *out) {
     if (!cache || !d_block_table || !d_ctx_lens || !d_q || !d_out) return TTS_ERR_INVALID;
     if (!cache->k_pool || !cache->v_pool || cache->num_blocks < 1) return TTS_ERR_INVALID;
     if (B < 0 || q_len < 1 || max_blocks_per_seq < 1 || max_blocks_per_seq > (1 << 20) ||
@@ -1036,6 +1043,8 @@ extern "C" int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block
     if (cache->num_kv_heads < 1) return TTS_ERR_INVALID;
     if (static_cast<long long>(cache->num_blocks) * cache->num_kv_heads * TTS_BLOCK_TOKENS >= (1LL << 31))
         return TTS_ERR_UNSUPPORTED;
+    AttnLaunchState *st = new (out->storage) AttnLaunchState();
+    st->ctas = 0;
     if (B == 0) return TTS_OK;
     AttnPlan pl;
     if (!attn_plan(cache->dtype, B, q_len, num_q_heads, cache->num_kv_heads, cache->head_dim,
@@ -1052,7 +1061,7 @@ extern "C" int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block
         return TTS_ERR_WORKSPACE;
 
     uint8_t *ws = static_cast<uint8_t *>(d_ws);
-    AttnArgs a;
+    AttnArgs &a = st->a;
     a.k_pool = static_cast<const uint8_t *>(cache->k_pool);
     a.v_pool = static_cast<const uint8_t *>(cache->v_pool);
     a.num_blocks = cache->num_blocks;
@@ -1077,8 +1086,37 @@ extern "C" int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block
     a.stages = cache->dtype == TTS_BF16 ? tc_stages(a.group * q_len, B) : kStages;
     if (a.stages < 1) return TTS_ERR_UNSUPPORTED;
     a.err = d_err;
-    auto s = static_cast<cudaStream_t>(stream);
-    return cache->dtype == TTS_BF16 ? launch_tc(a, pl.ctas, s) : launch_simt(a, pl.rows, pl.ctas, s);
+    st->dtype = cache->dtype;
+    st->rows = pl.rows;
+    st->ctas = pl.ctas;
+    if (cache->dtype == TTS_BF16) {
+        const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * a.Hkv * TTS_BLOCK_TOKENS;
+        if (!cached_tma_2d_bf16(&st->kmap, cache->k_pool, rows, 128, TTS_BLOCK_TOKENS, 64) ||
+            !cached_tma_2d_bf16(&st->vmap, cache->v_pool, rows, 128, TTS_BLOCK_TOKENS, 64))
+            return TTS_ERR_CUDA;
+    }
+    return TTS_OK;
+}
+
+int launch_attn(const AttnLaunch &L, LaunchOpts o) {
+    const AttnLaunchState *st = reinterpret_cast<const AttnLaunchState *>(L.storage);
+    if (st->ctas == 0) return TTS_OK;  // empty batch
+    return st->dtype == TTS_BF16 ? launch_tc(st->a, st->kmap, st->vmap, st->ctas, o)
+                                 : launch_simt(st->a, st->rows, st->ctas, o);
+}
+
+}  // namespace tts
+
+extern "C" int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block_table,
+                               int32_t max_blocks_per_seq, const int32_t *d_ctx_lens,
+                               int32_t max_ctx_len, int32_t B, int32_t q_len, int32_t num_q_heads,
+                               float scale, int32_t causal, const void *d_q, void *d_out,
+                               void *d_ws, size_t ws_bytes, int32_t *d_err, void *stream) {
+    tts::AttnLaunch L;
+    const int st = tts::prepare_attn(cache, d_block_table, max_blocks_per_seq, d_ctx_lens, max_ctx_len, B,
+                                     q_len, num_q_heads, scale, causal, d_q, d_out, d_ws, ws_bytes, d_err, &L);
+    if (st != TTS_OK) return st;
+    return tts::launch_attn(L, {static_cast<cudaStream_t>(stream), false});
 }
 
 // ---------------------------------------------------------------------------

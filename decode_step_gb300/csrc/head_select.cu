@@ -21,6 +21,8 @@
 //
 // fp32: a CUDA-core kernel (tf32 tensor cores would change the rounding of
 // fp32 inputs), one warp per vocabulary row.
+#include <new>
+
 #include "tts_common.cuh"
 #include "tts_internal.h"
 
@@ -82,6 +84,10 @@ struct HeadArgs {
     int32_t *err;
 };
 
+// Margin (in Gumbel units) kept when skipping entries that cannot win; far
+// larger than the rounding of the threshold's exponentials.
+constexpr float kGumbelSlack = 0.01f;
+
 // Gumbel-max selection key of logit `x` at the vocab entry drawing half `e`
 // of its Philox block `ph` (block = entries 8 * (v / 8) .. 8 * (v / 8) + 7).
 __device__ __forceinline__ float gumbel_key(const HeadArgs &a, float x, int e, const Philox4x64 &ph) {
@@ -93,6 +99,8 @@ __device__ __forceinline__ float gumbel_key(const HeadArgs &a, float x, int e, c
 __global__ void __launch_bounds__(256)
 head_simt_f32_kernel(const float *__restrict__ h, const float *__restrict__ W, const HeadArgs a) {
     __shared__ int flag;
+    pdl_wait_prerequisites();
+    pdl_allow_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int warps_total = gridDim.x * (blockDim.x >> 5);
     for (int v = blockIdx.x * (blockDim.x >> 5) + warp; v < a.V; v += warps_total) {
@@ -269,6 +277,7 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
         fence_mbar_init();
         *failed = 0;
     }
+    pdl_allow_dependents();
     if (warp == 4 && lane == 0) {
         prefetch_tensormap(&map_w);
         prefetch_tensormap(&map_h);
@@ -277,15 +286,19 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
     __syncthreads();
     // The first stages need no slot to free up: start streaming W and h now,
     // while the TMEM accumulator is being allocated.
+    // The weights never depend on the previous kernel, so they are requested
+    // before waiting for it; h (its output) only after.
     const int prologue = ktiles < kStagesTC ? ktiles : kStagesTC;
     if (warp == 4 && lane == 0) {
         for (int it = 0; it < prologue; ++it) {
             const uint32_t sa = base + it * Lo.stage_bytes;
             mbar_arrive_expect_tx(bar_full + 8 * it, Lo.stage_bytes);
-            const int k = kbase + it * kTileK;
-            tma_load_2d(sa, &map_w, k, v0, bar_full + 8 * it);
-            tma_load_2d(sa + kATileBytes, &map_h, k, r0, bar_full + 8 * it);
+            tma_load_2d(sa, &map_w, kbase + it * kTileK, v0, bar_full + 8 * it);
         }
+        pdl_wait_prerequisites();
+        for (int it = 0; it < prologue; ++it)
+            tma_load_2d(base + it * Lo.stage_bytes + kATileBytes, &map_h, kbase + it * kTileK, r0,
+                        bar_full + 8 * it);
     }
     if (warp == 5) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -336,22 +349,31 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
         mma_commit(bar_acc);  // fires when every MMA issued above has completed
     }
 
-    // ---- epilogue part 1: accumulator -> shared memory (rows 32 w .. 32 w + 31)
-    float *dump = reinterpret_cast<float *>(smem);
-    if (warp < 4) {
-        if (!mbar_wait(bar_acc, 0)) {
-            flag_error(a.err, TTS_ERRBIT_TIMEOUT);
-            atomicExch(failed, 1);
-        } else {
-            tc_fence_after();
-            const int row = warp * 32 + lane;
-            for (int c0 = 0; c0 < N; c0 += 16) {
-                float v[16];
-                tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
-                float4 *dst = reinterpret_cast<float4 *>(dump + row * Lo.dump_stride + c0);
+    // ---- epilogue part 1: every row of the accumulator goes to the cluster CTA
+    // that owns it (rows [rank * RS, (rank + 1) * RS)), into that CTA's receive
+    // table recv[source rank][row % RS][column] (it reuses the ring, so every
+    // CTA's MMAs must be done first).  Remote stores need no round trip.
+    const int RS = kTileM / CK;  // rows owned per CTA
+    float *recv = reinterpret_cast<float *>(smem);
+    bool acc_ready = true;
+    if (warp < 4 && !mbar_wait(bar_acc, 0)) {
+        flag_error(a.err, TTS_ERRBIT_TIMEOUT);
+        atomicExch(failed, 1);
+        acc_ready = false;
+    }
+    if (CK > 1) cluster_sync();
+    if (warp < 4 && acc_ready) {
+        tc_fence_after();
+        const int row = warp * 32 + lane;
+        const int owner = row / RS;
+        float *dst_row = recv + (static_cast<size_t>(rank) * RS + row % RS) * Lo.dump_stride;
+        if (CK > 1) dst_row = map_cluster_ptr(dst_row, static_cast<uint32_t>(owner));
+        for (int c0 = 0; c0 < N; c0 += 16) {
+            float v[16];
+            tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
+            float4 *dst = reinterpret_cast<float4 *>(dst_row + c0);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            }
+            for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         }
     }
     tc_fence_before();
@@ -361,39 +383,25 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(alloc_cols)
                      : "memory");
     }
-    if (CK > 1) cluster_sync();
+    if (CK > 1) cluster_sync();  // every row has arrived at its owner
 
-    // ---- epilogue part 2: sum the cluster's partial tiles for this CTA's
-    // 128 / CK rows, select per batch column.  Work item = (8-row group, column).
-    const int rows_per_cta = kTileM / CK;
-    const int items = (rows_per_cta / 8) * N;
-    const float *dumps[8];
-#pragma unroll
-    for (int src = 0; src < 8; ++src)
-        dumps[src] = src < CK ? (CK > 1 ? map_cluster_ptr(dump, static_cast<uint32_t>(src)) : dump) : dump;
+    // ---- epilogue part 2: sum the CK partial copies of this CTA's RS rows and
+    // select per batch column.  Work item = (8-row group, column); consecutive
+    // threads take consecutive columns.
+    const int items = (RS / 8) * N;
     for (int item = threadIdx.x; item < items; item += blockDim.x) {
         const int gi = item / N, cn = item % N;
         const int r = r0 + cn;
         if (r >= a.R) continue;
-        const int lrow = rank * rows_per_cta + gi * 8;   // local row in the tile
-        float part[8][8];
-#pragma unroll
-        for (int src = 0; src < 8; ++src) {
-            if (src < CK) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) part[src][e] = dumps[src][(lrow + e) * Lo.dump_stride + cn];
-            }
-        }
         float lg[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            float acc = 0.0f;
+        for (int e = 0; e < 8; ++e) lg[e] = 0.0f;
+        for (int src = 0; src < CK; ++src) {
+            const float *col = recv + (static_cast<size_t>(src) * RS + gi * 8) * Lo.dump_stride + cn;
 #pragma unroll
-            for (int src = 0; src < 8; ++src)
-                if (src < CK) acc += part[src][e];
-            lg[e] = acc;
+            for (int e = 0; e < 8; ++e) lg[e] += col[e * Lo.dump_stride];
         }
-        const int v = v0 + lrow;  // multiple of 8
+        const int v = v0 + rank * RS + gi * 8;  // multiple of 8
         if (a.logits_out) {
 #pragma unroll
             for (int e = 0; e < 8; ++e)
@@ -403,11 +411,29 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
         if (v >= vmax) continue;
         unsigned long long best = 0ull;
         if (a.mode == TTS_GUMBEL) {
+            // An entry can only beat the column's current best z_cur if its
+            // noise exceeds z_cur - logit / T.  With the group's largest logit
+            // that gives one uniform threshold for all 8 entries: below it
+            // (with a safety margin far above rounding) an entry cannot win,
+            // and its logarithms are skipped.  Exact for the entries kept.
+            float lmax = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (v + e < vmax) lmax = fmaxf(lmax, lg[e]);
+            const unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(colbest + cn);
+            float thr = 0.0f;  // uniforms <= thr cannot win
+            if (cur) {
+                const float g0 = unpack_value(cur) - lmax / a.temperature - kGumbelSlack;
+                thr = expf(-expf(-g0));
+            }
             const Philox4x64 ph(static_cast<uint64_t>(v >> 3), 0, 0, 0, a.seed[r], a.step[r]);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 if (v + e >= vmax) break;
-                const unsigned long long k = pack_argmax(gumbel_key(a, lg[e], e, ph), v + e);
+                const float u = bits_to_uniform(ph.half(e));
+                if (!(u > thr)) continue;
+                const float key = lg[e] / a.temperature + gumbel_from_uniform(u);
+                const unsigned long long k = pack_argmax(key, v + e);
                 best = k > best ? k : best;
             }
         } else {
@@ -418,7 +444,7 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
                 best = k > best ? k : best;
             }
         }
-        atomicMax(colbest + cn, best);
+        if (best) atomicMax(colbest + cn, best);
     }
     __syncthreads();
     // One global atomic per column and cluster: every other rank stores its
@@ -428,7 +454,7 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
         unsigned long long *slot = map_cluster_ptr(colbest + rank * N, 0u);
         for (int cn = threadIdx.x; cn < N; cn += blockDim.x) slot[cn] = colbest[cn];
     }
-    if (CK > 1) cluster_sync();  // peers are done reading this CTA's dump and storing keys
+    if (CK > 1) cluster_sync();  // keys have arrived at rank 0
     // Only rank 0 of each cluster publishes keys, so only those CTAs take a
     // ticket: the last ticket then comes after every publication.
     if (rank != 0) return;
@@ -444,12 +470,6 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
 }
 
 // ------------------------------------------------------------- host side
-
-// 2-D bf16 tensor [rows][cols] (cols contiguous), box [box_rows][64], 128-byte swizzle.
-bool make_map(CUtensorMap *map, const void *ptr, int rows, int cols, int box_rows) {
-    return make_tma_2d_bf16(map, ptr, static_cast<uint64_t>(rows), static_cast<uint64_t>(cols),
-                            static_cast<uint32_t>(box_rows), static_cast<uint32_t>(kTileK));
-}
 
 struct TcPlan {
     int N, chunks, CK, alloc_cols;
@@ -488,13 +508,22 @@ extern "C" size_t tts_head_workspace_size(int32_t R, int32_t V) {
     return tts::align_up(static_cast<size_t>(R) * 8, 256) + 256;
 }
 
-extern "C" int tts_codebook_head_select(const void *d_h, const void *d_W, int32_t dtype, int32_t R,
-                                        int32_t H, int32_t V, int32_t mode, float temperature,
-                                        const uint64_t *d_seed, const uint64_t *d_step,
-                                        const uint8_t *d_eos_allowed, int32_t *d_ids, float *d_best,
-                                        float *d_logits_out, void *d_ws, size_t ws_bytes,
-                                        void *stream) {
-    using namespace tts;
+namespace tts {
+
+struct HeadLaunchState {
+    HeadArgs a;
+    CUtensorMap mw, mh;
+    TcPlan p;
+    int dtype;
+    int simt_grid;
+    const void *h, *W;
+};
+static_assert(sizeof(HeadLaunchState) <= sizeof(HeadLaunch::storage), "HeadLaunch storage too small");
+
+int prepare_head(const void *d_h, const void *d_W, int32_t dtype, int32_t R, int32_t H, int32_t V,
+                 int32_t mode, float temperature, const uint64_t *d_seed, const uint64_t *d_step,
+                 const uint8_t *d_eos_allowed, int32_t *d_ids, float *d_best, float *d_logits_out,
+                 void *d_ws, size_t ws_bytes, HeadLaunch *out) {
     if (!d_h || !d_W || !d_ids) return TTS_ERR_INVALID;
     if (R < 1 || R > 4096 || H < 1 || V < 1 || V > (1 << 30)) return TTS_ERR_INVALID;
     if (mode != TTS_ARGMAX && mode != TTS_GUMBEL) return TTS_ERR_INVALID;
@@ -504,43 +533,84 @@ extern "C" int tts_codebook_head_select(const void *d_h, const void *d_W, int32_
     const size_t need = tts_head_workspace_size(R, V);
     if (!d_ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(d_ws) & 255u) != 0)
         return TTS_ERR_WORKSPACE;
-    HeadArgs a;
+    HeadLaunchState *st = new (out->storage) HeadLaunchState();
+    HeadArgs &a = st->a;
     a.R = R; a.H = H; a.V = V; a.mode = mode; a.temperature = temperature;
     a.seed = d_seed; a.step = d_step; a.eos = d_eos_allowed; a.logits_out = d_logits_out;
     a.ids = d_ids; a.best = d_best; a.ws = head_ws(d_ws, R); a.err = nullptr;
-    auto s = static_cast<cudaStream_t>(stream);
+    st->dtype = dtype;
+    st->h = d_h;
+    st->W = d_W;
     if (dtype == TTS_F32) {
         const int sms = sm_count() > 0 ? sm_count() : 148;
-        int grid = (V + 7) / 8;
-        grid = grid < 4 * sms ? grid : 4 * sms;
-        head_simt_f32_kernel<<<grid, 256, 0, s>>>(static_cast<const float *>(d_h),
-                                                  static_cast<const float *>(d_W), a);
-        return launch_status();
+        const int grid = (V + 7) / 8;
+        st->simt_grid = grid < 4 * sms ? grid : 4 * sms;
+        return TTS_OK;
     }
     if (H % kTileK != 0) return TTS_ERR_UNSUPPORTED;
     if (!aligned16(d_h) || !aligned16(d_W)) return TTS_ERR_INVALID;
-    const TcPlan p = plan_tc(R, H, V);
-    CUtensorMap mw, mh;
-    if (!make_map(&mw, d_W, V, H, kTileM) || !make_map(&mh, d_h, R, H, p.N)) return TTS_ERR_CUDA;
-    if (cudaFuncSetAttribute(head_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(p.smem)) != cudaSuccess)
+    st->p = plan_tc(R, H, V);
+    if (!cached_tma_2d_bf16(&st->mw, d_W, static_cast<uint64_t>(V), static_cast<uint64_t>(H), kTileM, kTileK) ||
+        !cached_tma_2d_bf16(&st->mh, d_h, static_cast<uint64_t>(R), static_cast<uint64_t>(H),
+                            static_cast<uint32_t>(st->p.N), kTileK))
         return TTS_ERR_CUDA;
+    return TTS_OK;
+}
+
+int launch_head(const HeadLaunch &L, LaunchOpts o) {
+    const HeadLaunchState *st = reinterpret_cast<const HeadLaunchState *>(L.storage);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(((V + kTileM - 1) / kTileM) * p.CK),
-                       static_cast<unsigned>(p.chunks), 1);
-    cfg.blockDim = dim3(kThreadsTC, 1, 1);
-    cfg.dynamicSmemBytes = p.smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(p.CK);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, head_tc_kernel, mw, mh, a, p.N, p.CK, p.alloc_cols) != cudaSuccess) {
+    cfg.stream = o.stream;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (o.pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cudaError_t e;
+    if (st->dtype == TTS_F32) {
+        cfg.gridDim = dim3(st->simt_grid, 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.attrs = attr;
+        cfg.numAttrs = na;
+        e = cudaLaunchKernelEx(&cfg, head_simt_f32_kernel, static_cast<const float *>(st->h),
+                               static_cast<const float *>(st->W), st->a);
+    } else {
+        const TcPlan &p = st->p;
+        if (!ensure_dynamic_smem(reinterpret_cast<const void *>(head_tc_kernel), static_cast<int>(p.smem)))
+            return TTS_ERR_CUDA;
+        cfg.gridDim = dim3(static_cast<unsigned>(((st->a.V + kTileM - 1) / kTileM) * p.CK),
+                           static_cast<unsigned>(p.chunks), 1);
+        cfg.blockDim = dim3(kThreadsTC, 1, 1);
+        cfg.dynamicSmemBytes = p.smem;
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = static_cast<unsigned>(p.CK);
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+        cfg.attrs = attr;
+        cfg.numAttrs = na;
+        e = cudaLaunchKernelEx(&cfg, head_tc_kernel, st->mw, st->mh, st->a, p.N, p.CK, p.alloc_cols);
+    }
+    if (e != cudaSuccess) {
         cudaGetLastError();
         return TTS_ERR_CUDA;
     }
-    return launch_status();
+    return TTS_OK;
+}
+
+}  // namespace tts
+
+extern "C" int tts_codebook_head_select(const void *d_h, const void *d_W, int32_t dtype, int32_t R,
+                                        int32_t H, int32_t V, int32_t mode, float temperature,
+                                        const uint64_t *d_seed, const uint64_t *d_step,
+                                        const uint8_t *d_eos_allowed, int32_t *d_ids, float *d_best,
+                                        float *d_logits_out, void *d_ws, size_t ws_bytes,
+                                        void *stream) {
+    tts::HeadLaunch L;
+    const int st = tts::prepare_head(d_h, d_W, dtype, R, H, V, mode, temperature, d_seed, d_step,
+                                     d_eos_allowed, d_ids, d_best, d_logits_out, d_ws, ws_bytes, &L);
+    if (st != TTS_OK) return st;
+    return tts::launch_head(L, {static_cast<cudaStream_t>(stream), false});
 }

@@ -17,6 +17,8 @@ kv_append_kernel(const int32_t *__restrict__ table, int max_blocks,
                  const int32_t *__restrict__ ctx_before, int q_len, int Hkv, int num_blocks,
                  int row_vecs, const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
                  uint4 *__restrict__ k_pool, uint4 *__restrict__ v_pool, int32_t *err) {
+    pdl_wait_prerequisites();
+    pdl_allow_dependents();
     const int b = blockIdx.x / q_len;
     const int j = blockIdx.x % q_len;
     const int before = ctx_before[b];
@@ -51,15 +53,15 @@ kv_append_kernel(const int32_t *__restrict__ table, int max_blocks,
 }  // namespace
 }  // namespace tts
 
-extern "C" int tts_kv_append(const tts_kv_cache *cache, const int32_t *d_block_table,
-                             int32_t max_blocks_per_seq, const int32_t *d_ctx_before, int32_t B,
-                             int32_t q_len, const void *d_k_new, const void *d_v_new,
-                             int32_t *d_err, void *stream) {
-    using namespace tts;
+namespace tts {
+
+int prepare_append(const tts_kv_cache *cache, const int32_t *d_block_table, int32_t max_blocks_per_seq,
+                   const int32_t *d_ctx_before, int32_t B, int32_t q_len, const void *d_k_new,
+                   const void *d_v_new, int32_t *d_err, AppendLaunch *out) {
     if (!cache || !d_block_table || !d_ctx_before || !d_k_new || !d_v_new) return TTS_ERR_INVALID;
     if (!cache->k_pool || !cache->v_pool) return TTS_ERR_INVALID;
-    if (B < 0 || q_len < 1 || max_blocks_per_seq < 1 || cache->num_blocks < 1 ||
-        cache->num_kv_heads < 1 || cache->head_dim < 1)
+    if (B < 0 || q_len < 1 || max_blocks_per_seq < 1 || max_blocks_per_seq > (1 << 20) ||
+        cache->num_blocks < 1 || cache->num_kv_heads < 1 || cache->head_dim < 1)
         return TTS_ERR_INVALID;
     if (cache->block_size != TTS_BLOCK_TOKENS) return TTS_ERR_UNSUPPORTED;
     if (cache->dtype != TTS_F32 && cache->dtype != TTS_BF16) return TTS_ERR_UNSUPPORTED;
@@ -69,13 +71,44 @@ extern "C" int tts_kv_append(const tts_kv_cache *cache, const int32_t *d_block_t
     if (!aligned16(cache->k_pool) || !aligned16(cache->v_pool) || !aligned16(d_k_new) ||
         !aligned16(d_v_new))
         return TTS_ERR_INVALID;
-    if (B == 0) return TTS_OK;
-    const long ctas = static_cast<long>(B) * q_len;
-    if (ctas > 0x7FFFFFFFL) return TTS_ERR_INVALID;
-    kv_append_kernel<<<static_cast<unsigned>(ctas), 128, 0, static_cast<cudaStream_t>(stream)>>>(
-        d_block_table, max_blocks_per_seq, d_ctx_before, q_len, cache->num_kv_heads,
-        cache->num_blocks, static_cast<int>(row_bytes / 16), static_cast<const uint4 *>(d_k_new),
-        static_cast<const uint4 *>(d_v_new), static_cast<uint4 *>(cache->k_pool),
-        static_cast<uint4 *>(cache->v_pool), d_err);
-    return launch_status();
+    if (static_cast<long>(B) * q_len > 0x7FFFFFFFL) return TTS_ERR_INVALID;
+    *out = AppendLaunch{cache, d_block_table, max_blocks_per_seq, d_ctx_before, B, q_len, d_k_new, d_v_new, d_err};
+    return TTS_OK;
+}
+
+int launch_append(const AppendLaunch &L, LaunchOpts o) {
+    if (L.B == 0) return TTS_OK;
+    const int elem = L.cache->dtype == TTS_F32 ? 4 : 2;
+    const int row_vecs = L.cache->head_dim * elem / 16;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long>(L.B) * L.q_len), 1, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.stream = o.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = o.pdl ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, kv_append_kernel, L.table, L.max_blocks, L.ctx_before, L.q_len,
+                           static_cast<int>(L.cache->num_kv_heads), static_cast<int>(L.cache->num_blocks),
+                           row_vecs, static_cast<const uint4 *>(L.k_new), static_cast<const uint4 *>(L.v_new),
+                           static_cast<uint4 *>(L.cache->k_pool), static_cast<uint4 *>(L.cache->v_pool),
+                           L.err) != cudaSuccess) {
+        cudaGetLastError();
+        return TTS_ERR_CUDA;
+    }
+    return TTS_OK;
+}
+
+}  // namespace tts
+
+extern "C" int tts_kv_append(const tts_kv_cache *cache, const int32_t *d_block_table,
+                             int32_t max_blocks_per_seq, const int32_t *d_ctx_before, int32_t B,
+                             int32_t q_len, const void *d_k_new, const void *d_v_new,
+                             int32_t *d_err, void *stream) {
+    tts::AppendLaunch L;
+    const int st = tts::prepare_append(cache, d_block_table, max_blocks_per_seq, d_ctx_before, B, q_len,
+                                       d_k_new, d_v_new, d_err, &L);
+    if (st != TTS_OK) return st;
+    return tts::launch_append(L, {static_cast<cudaStream_t>(stream), false});
 }

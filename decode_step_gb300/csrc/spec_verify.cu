@@ -39,6 +39,8 @@ spec_verify_kernel(const float *__restrict__ tl, const float *__restrict__ dp,
     __shared__ float row_max[kMaxK], row_sum[kMaxK];
     __shared__ int s_reject, s_accepted, s_draw;
     __shared__ unsigned long long s_best;
+    pdl_wait_prerequisites();
+    pdl_allow_dependents();
     const int b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float *tl_b = tl + static_cast<size_t>(b) * (K + 1) * V;

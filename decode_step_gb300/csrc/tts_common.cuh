@@ -18,6 +18,19 @@ __device__ __forceinline__ void flag_error(int32_t *err, int bit) {
 // A bounded wait gives up after this many SM clock cycles (about one second).
 constexpr long long kWaitLimitCycles = 2000000000LL;
 
+// ------------------------------------------------- programmatic launch
+
+// Lets the next kernel in the stream (if launched as a programmatic
+// dependent) start now; its griddepcontrol.wait still waits for this grid.
+__device__ __forceinline__ void pdl_allow_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the previous kernel in the stream has completed and its writes
+// are visible (returns at once when this grid was launched normally).
+__device__ __forceinline__ void pdl_wait_prerequisites() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------ element types
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

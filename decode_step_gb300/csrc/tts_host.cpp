@@ -146,4 +146,74 @@ bool make_tma_2d_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace {
+struct MapEntry {
+    const void *ptr;
+    uint64_t rows, cols;
+    uint32_t box_rows, box_cols;
+    int device;
+    CUtensorMap map;
+};
+std::mutex g_map_mu;
+MapEntry g_maps[16];
+int g_maps_used = 0, g_maps_next = 0;
+}  // namespace
+
+bool cached_tma_2d_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols,
+                        uint32_t box_rows, uint32_t box_cols) {
+    int dev = -1;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (int i = 0; i < g_maps_used; ++i) {
+        const MapEntry &e = g_maps[i];
+        if (e.ptr == ptr && e.rows == rows && e.cols == cols && e.box_rows == box_rows &&
+            e.box_cols == box_cols && e.device == dev) {
+            *map = e.map;
+            return true;
+        }
+    }
+    MapEntry e;
+    e.ptr = ptr;
+    e.rows = rows;
+    e.cols = cols;
+    e.box_rows = box_rows;
+    e.box_cols = box_cols;
+    e.device = dev;
+    if (!make_tma_2d_bf16(&e.map, ptr, rows, cols, box_rows, box_cols)) return false;
+    g_maps[g_maps_next] = e;
+    g_maps_next = (g_maps_next + 1) % 16;
+    if (g_maps_used < 16) ++g_maps_used;
+    *map = e.map;
+    return true;
+}
+
+namespace {
+struct SmemEntry {
+    const void *func;
+    int device;
+    int bytes;
+};
+std::mutex g_smem_mu;
+std::vector<SmemEntry> g_smem;
+}  // namespace
+
+bool ensure_dynamic_smem(const void *func, int bytes) {
+    if (bytes <= 48 * 1024) return true;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(g_smem_mu);
+    for (auto &e : g_smem)
+        if (e.func == func && e.device == dev) {
+            if (e.bytes >= bytes) return true;
+            if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+                return false;
+            e.bytes = bytes;
+            return true;
+        }
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return false;
+    g_smem.push_back({func, dev, bytes});
+    return true;
+}
+
 }  // namespace tts

@@ -29,6 +29,24 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Same, cached by (address, shape, box): building a descriptor is a driver
+// call, and a serving loop passes the same tensors every step.
+bool cached_tma_2d_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols,
+                        uint32_t box_rows, uint32_t box_cols);
+
+// Raises a kernel's dynamic shared-memory limit on the current device to at
+// least `bytes`, calling the runtime only when the limit has to grow.
+bool ensure_dynamic_smem(const void *func, int bytes);
+
+// How a kernel is launched.  `pdl` (programmatic dependent launch) lets it
+// start while the previous kernel in the stream is finishing; only set where
+// the kernel runs griddepcontrol.wait before touching anything that kernel
+// writes.
+struct LaunchOpts {
+    cudaStream_t stream;
+    bool pdl;
+};
+
 // Decode-attention launch plan shared by the workspace query and the launch:
 // a persistent grid of `ctas` CTAs (`workers` warps) over the flat tile list.
 struct AttnPlan {
@@ -39,5 +57,41 @@ struct AttnPlan {
 bool attn_plan(int dtype, int B, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
                int max_ctx_len, AttnPlan *out);
 size_t attn_workspace_bytes(int B, int num_kv_heads, int head_dim, const AttnPlan &pl);
+
+// ---- validated launches, shared by the single-kernel entry points and
+// tts_decode_step (which chains them with programmatic dependent launch)
+
+struct AppendLaunch {
+    const tts_kv_cache *cache;
+    const int32_t *table;
+    int max_blocks;
+    const int32_t *ctx_before;
+    int B, q_len;
+    const void *k_new, *v_new;
+    int32_t *err;
+};
+int prepare_append(const tts_kv_cache *cache, const int32_t *d_block_table, int32_t max_blocks_per_seq,
+                   const int32_t *d_ctx_before, int32_t B, int32_t q_len, const void *d_k_new,
+                   const void *d_v_new, int32_t *d_err, AppendLaunch *out);
+int launch_append(const AppendLaunch &L, LaunchOpts o);
+
+struct AttnLaunchState;  // defined in decode_attn.cu
+struct AttnLaunch {
+    alignas(64) unsigned char storage[1024];  // AttnLaunchState
+};
+int prepare_attn(const tts_kv_cache *cache, const int32_t *d_block_table, int32_t max_blocks_per_seq,
+                 const int32_t *d_ctx_lens, int32_t max_ctx_len, int32_t B, int32_t q_len,
+                 int32_t num_q_heads, float scale, int32_t causal, const void *d_q, void *d_out,
+                 void *d_ws, size_t ws_bytes, int32_t *d_err, AttnLaunch *out);
+int launch_attn(const AttnLaunch &L, LaunchOpts o);
+
+struct HeadLaunch {
+    alignas(64) unsigned char storage[1024];  // HeadLaunchState (tensor maps included)
+};
+int prepare_head(const void *d_h, const void *d_W, int32_t dtype, int32_t R, int32_t H, int32_t V,
+                 int32_t mode, float temperature, const uint64_t *d_seed, const uint64_t *d_step,
+                 const uint8_t *d_eos_allowed, int32_t *d_ids, float *d_best, float *d_logits_out,
+                 void *d_ws, size_t ws_bytes, HeadLaunch *out);
+int launch_head(const HeadLaunch &L, LaunchOpts o);
 
 }  // namespace tts

@@ -1,9 +1,16 @@
 """One batched decode step through the C ABI: append, attend, score and pick.
 
 `DecodeStep` owns the workspaces and output buffers for a fixed batch shape
-and issues tts_kv_append -> tts_decode_attn -> tts_codebook_head_select on one
-stream.  The attention output [B][q_len][Hq][D] is read by the head as
-h [B * q_len][Hq * D], so Hq * D must equal the head's hidden width.
+and issues tts_decode_step (append -> attention -> head, the later kernels
+launched as programmatic dependents) on one stream.  The attention output
+[B][q_len][Hq][D] is read by the head as h [B * q_len][Hq * D], so Hq * D must
+equal the head's hidden width.
+
+`GraphedStep` captures, once, a CUDA graph of a whole serving step for fixed
+buffers: the host-to-device copies of the step's inputs from pinned host
+memory, the decode step, and the copy of the chosen ids back to pinned host
+memory.  Each step then is: write the pinned inputs, replay, synchronise,
+read the pinned ids.
 """
 from __future__ import annotations
 
@@ -42,12 +49,57 @@ class DecodeStep:
     def __call__(self, block_table, ctx_before, ctx_lens, q, k_new, v_new, seed=None, step=None,
                  eos_allowed=None, logits_out=None, best=None, stream=None) -> torch.Tensor:
         """Runs the step; returns the device tensor of chosen ids [B * q_len]."""
-        bd.tts_kv_append(self.cache, block_table, ctx_before, k_new, v_new, err=self.err, stream=stream)
-        bd.tts_decode_attn(self.cache, block_table, ctx_lens, self.max_ctx_len, q, self.out,
-                           self.attn_ws, self.scale, self.causal, err=self.err, stream=stream)
-        h = self.out.view(self.R, self.Hq * self.cache.head_dim)
-        bd.tts_codebook_head_select(h, self.W, self.ids, self.head_ws, mode=self.mode,
-                                    temperature=self.temperature, seed=seed, step=step,
-                                    eos_allowed=eos_allowed, best=best, logits_out=logits_out,
-                                    stream=stream)
+        bd.tts_decode_step(self.cache, block_table, ctx_before, ctx_lens, self.max_ctx_len, q, k_new,
+                           v_new, self.out, self.attn_ws, self.scale, self.W, self.ids, self.head_ws,
+                           causal=self.causal, mode=self.mode, temperature=self.temperature,
+                           seed=seed, step=step, eos_allowed=eos_allowed, best=best,
+                           logits_out=logits_out, err=self.err, stream=stream)
         return self.ids
+
+
+class GraphedStep:
+    """A captured serving step: pinned host inputs -> device -> step -> pinned ids.
+
+    `inputs` maps names of DecodeStep's call arguments (block_table, ctx_before,
+    ctx_lens, q, k_new, v_new, and optionally seed, step) to device tensors
+    used as the step's input buffers; a pinned host twin of each is made.
+    """
+
+    NAMES = ("block_table", "ctx_before", "ctx_lens", "q", "k_new", "v_new", "seed", "step")
+
+    def __init__(self, step: DecodeStep, inputs: dict):
+        self.step = step
+        self.dev = dict(inputs)
+        self.host = {}
+        for k, t in self.dev.items():
+            if k not in self.NAMES:
+                raise ValueError(f"unknown step input {k}")
+            h = torch.empty(t.shape, dtype=t.dtype, device="cpu").pin_memory()
+            h.copy_(t.cpu())
+            self.host[k] = h
+        self.ids_host = torch.empty(step.R, dtype=torch.int32, device="cpu").pin_memory()
+        self.stream = torch.cuda.Stream()
+        self.graph = torch.cuda.CUDAGraph()
+        self.stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(self.stream):
+            self._body()  # warm-up outside capture (one-time set-up of the library)
+        self.stream.synchronize()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            self._body()
+
+    def _body(self):
+        for k, t in self.dev.items():
+            t.copy_(self.host[k], non_blocking=True)
+        ids = self.step(**self.dev)
+        self.ids_host.copy_(ids, non_blocking=True)
+
+    @property
+    def h2d_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in self.host.values())
+
+    def __call__(self) -> torch.Tensor:
+        """Replays the step and returns the (pinned, host) ids once they are there."""
+        with torch.cuda.stream(self.stream):  # replay() launches on the current stream
+            self.graph.replay()
+        self.stream.synchronize()
+        return self.ids_host

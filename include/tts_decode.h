@@ -238,6 +238,29 @@ int tts_spec_verify(const float *d_target_logits, const float *d_draft_probs,
                     int32_t flags, int32_t *d_n_accepted, int32_t *d_next_token,
                     int32_t *d_err, void *stream);
 
+/* ----------------------------------------------------------- full step */
+
+/* One decode step in one call: tts_kv_append, then tts_decode_attn into
+ * d_attn_out, then tts_codebook_head_select with h = d_attn_out read as
+ * [B * q_len][num_q_heads * head_dim] (dtype cache->dtype, R = B * q_len).
+ * Arguments mean what they mean for those three calls; all of them are
+ * checked before anything is launched.  The attention and head kernels are
+ * launched as programmatic dependents of the kernel before them: each starts
+ * its set-up (tile map; weight stream) while its predecessor finishes, and
+ * waits for it before reading the KV pool or the attention output.  So the
+ * caller must not write the step's inputs (q, k_new, v_new, tables, lengths,
+ * weights, seeds) from the kernels of this same call — only before it. */
+int tts_decode_step(const tts_kv_cache *cache, const int32_t *d_block_table,
+                    int32_t max_blocks_per_seq, const int32_t *d_ctx_before,
+                    const int32_t *d_ctx_lens, int32_t max_ctx_len, int32_t B, int32_t q_len,
+                    int32_t num_q_heads, float scale, int32_t causal, const void *d_q,
+                    const void *d_k_new, const void *d_v_new, void *d_attn_out, void *d_attn_ws,
+                    size_t attn_ws_bytes, const void *d_W, int32_t V, int32_t mode,
+                    float temperature, const uint64_t *d_seed, const uint64_t *d_step,
+                    const uint8_t *d_eos_allowed, int32_t *d_ids, float *d_best,
+                    float *d_logits_out, void *d_head_ws, size_t head_ws_bytes, int32_t *d_err,
+                    void *stream);
+
 /* ----------------------------------------------------------------- misc */
 
 /* Static description of a status code. */

@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
     from decode_step_gb300 import binding as bd
-    from decode_step_gb300.step import DecodeStep
+    from decode_step_gb300.step import DecodeStep, GraphedStep
 
 
 # ------------------------------------------------------------------ helpers
@@ -332,3 +332,19 @@ def test_head_boundary_token_mask(orc):
     bd.tts_codebook_head_select(dev(h), dev(W), ids, ws, eos_allowed=dev(eos))
     torch.cuda.synchronize()
     assert list(host(ids)) == [V - 1, 100] * 4
+
+
+def test_graphed_step_matches_direct_step():
+    """The captured serving step (host copies in, step, ids out) gives the same ids."""
+    inp = wl.make_inputs(wl.custom(3, B=24), with_verify=False)
+    w = inp["workload"]
+    u = Uploaded(inp)
+    cache = bd.KVCache(u.k_pool, u.v_pool)
+    step = DecodeStep(cache, u.W, w.Hq, w.B, w.ctx_hi)
+    direct = step(u.table, u.ctx_before, u.ctx_lens, u.q, u.k_new, u.v_new).clone()
+    g = GraphedStep(step, {"block_table": u.table, "ctx_before": u.ctx_before, "ctx_lens": u.ctx_lens,
+                           "q": u.q, "k_new": u.k_new, "v_new": u.v_new})
+    for _ in range(3):
+        g.ids_host.fill_(-7)           # a replay that did not finish would leave this
+        assert torch.equal(g().clone(), direct.cpu())
+    assert int(step.err.item()) == 0
