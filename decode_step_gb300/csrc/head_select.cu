@@ -220,26 +220,50 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
 
 struct TcLayout {
     uint32_t stage_bytes;   // A tile + B tile
-    uint32_t ring_bytes;    // all stages (also hosts the accumulator dump)
-    uint32_t dump_stride;   // floats per dumped row (N + 4)
+    uint32_t dump_stride;   // floats per accumulator row in shared memory (N + 4)
+    uint32_t recv;          // offset of the receive table (after the dump; both reuse the ring)
+    uint32_t region;        // ring, or dump + receive table if larger
     uint32_t bars;          // offset of the mbarriers
     uint32_t colbest;       // offset of the per-column best keys ([8][N]: own, then peers' slots)
     uint32_t misc;          // TMEM address, flag
     uint32_t total;
 };
 
-__host__ __device__ inline TcLayout tc_layout(int N) {
+// The ring holds the k-slices while the MMAs run; afterwards the same bytes
+// hold this CTA's accumulator (the dump, 128 rows) and, with CK > 1, the
+// receive table recv[source rank][RS rows] of the rows this CTA owns.
+__host__ __device__ inline TcLayout tc_layout(int N, int CK) {
     TcLayout L;
     L.stage_bytes = kATileBytes + N * kTileK * 2;
     const uint32_t ring = kStagesTC * L.stage_bytes;
     L.dump_stride = N + 4;
     const uint32_t dump = kTileM * L.dump_stride * 4;
-    L.ring_bytes = ring > dump ? ring : dump;
-    L.bars = L.ring_bytes;
-    L.colbest = L.bars + 8 * (2 * kStagesTC + 1);
+    L.recv = dump;
+    const uint32_t after = CK > 1 ? 2 * dump : dump;  // CK * RS = 128 rows received
+    L.region = ring > after ? ring : after;
+    L.bars = L.region;
+    L.colbest = L.bars + 8 * (2 * kStagesTC + 3);
     L.misc = L.colbest + 8 * 8 * N;
     L.total = L.misc + 16 + 1024;  // + slack to align the dynamic base to 1024
     return L;
+}
+
+// Bulk copy shared::cta -> shared::cluster (another CTA of the cluster),
+// completing on an mbarrier of the destination CTA.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                                  uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst_cluster),
+        "r"(src), "r"(bytes), "r"(bar_cluster)
+        : "memory");
+}
+
+// Asynchronous remote store of 8 bytes, completing on the destination CTA's mbarrier.
+__device__ __forceinline__ void st_async_u64(uint32_t dst_cluster, unsigned long long v, uint32_t bar_cluster) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(dst_cluster),
+                 "l"(v), "r"(bar_cluster)
+                 : "memory");
 }
 
 __global__ void __launch_bounds__(kThreadsTC, 1)
@@ -250,10 +274,12 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base - raw);
-    const TcLayout Lo = tc_layout(N);
+    const TcLayout Lo = tc_layout(N, CK);
     const uint32_t bar_full = base + Lo.bars;                 // [kStagesTC]
     const uint32_t bar_empty = bar_full + 8 * kStagesTC;      // [kStagesTC]
     const uint32_t bar_acc = bar_empty + 8 * kStagesTC;
+    const uint32_t bar_recv = bar_acc + 8;                    // peers' rows have arrived
+    const uint32_t bar_fold = bar_recv + 8;                   // peers' column keys have arrived (rank 0)
     unsigned long long *colbest = reinterpret_cast<unsigned long long *>(smem + Lo.colbest);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lo.misc);
     int *flag = reinterpret_cast<int *>(smem + Lo.misc + 4);
@@ -274,6 +300,8 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
             mbar_init(bar_empty + 8 * s, 1);
         }
         mbar_init(bar_acc, 1);
+        mbar_init(bar_recv, 1);
+        mbar_init(bar_fold, 1);
         fence_mbar_init();
         *failed = 0;
     }
@@ -349,45 +377,75 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
         mma_commit(bar_acc);  // fires when every MMA issued above has completed
     }
 
-    // ---- epilogue part 1: every row of the accumulator goes to the cluster CTA
-    // that owns it (rows [rank * RS, (rank + 1) * RS)), into that CTA's receive
-    // table recv[source rank][row % RS][column] (it reuses the ring, so every
-    // CTA's MMAs must be done first).  Remote stores need no round trip.
+    // ---- epilogue part 1: the accumulator goes to shared memory (the dump,
+    // reusing the ring, so every MMA of this CTA must be done), then each
+    // cluster CTA's block of rows (RS rows starting at rank * RS) is moved to
+    // it by one bulk copy per warp and owner, completing on the owner's
+    // mbarrier; the cluster barrier first makes sure every CTA's ring is free.
     const int RS = kTileM / CK;  // rows owned per CTA
-    float *recv = reinterpret_cast<float *>(smem);
+    float *dump = reinterpret_cast<float *>(smem);
+    const uint32_t stride_b = Lo.dump_stride * 4;
     bool acc_ready = true;
+    if (threadIdx.x == 0 && CK > 1)
+        mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>(CK - 1) * RS * stride_b);
+    if (threadIdx.x == 0 && CK > 1 && rank == 0)
+        mbar_arrive_expect_tx(bar_fold, static_cast<uint32_t>(CK - 1) * N * 8);
     if (warp < 4 && !mbar_wait(bar_acc, 0)) {
         flag_error(a.err, TTS_ERRBIT_TIMEOUT);
         atomicExch(failed, 1);
         acc_ready = false;
     }
-    if (CK > 1) cluster_sync();
     if (warp < 4 && acc_ready) {
         tc_fence_after();
         const int row = warp * 32 + lane;
-        const int owner = row / RS;
-        float *dst_row = recv + (static_cast<size_t>(rank) * RS + row % RS) * Lo.dump_stride;
-        if (CK > 1) dst_row = map_cluster_ptr(dst_row, static_cast<uint32_t>(owner));
-        for (int c0 = 0; c0 < N; c0 += 16) {
-            float v[16];
-            tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
+        float *dst_row = dump + static_cast<size_t>(row) * Lo.dump_stride;
+        for (int c0 = 0; c0 < N; c0 += 32) {
+            float v[32];
+            const uint32_t t = tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0;
+            tmem_ld16(t, v);
+            if (c0 + 16 < N) tmem_ld16(t + 16, v + 16);
             float4 *dst = reinterpret_cast<float4 *>(dst_row + c0);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            for (int q = 0; q < 8; ++q)
+                if (c0 + 4 * q < N) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         }
+        // the bulk copies read the dump through the async proxy
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     tc_fence_before();
-    __syncthreads();
+    if (CK > 1) cluster_sync();  // every CTA's MMAs are done: rings are free to receive
+    else __syncthreads();
     if (warp == 5) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(alloc_cols)
                      : "memory");
     }
-    if (CK > 1) cluster_sync();  // every row has arrived at its owner
+    if (CK > 1 && warp < 4 && lane == 0 && acc_ready) {
+        // this warp's 32 rows, split at owner boundaries; own rows stay in the dump
+        for (int row = warp * 32; row < warp * 32 + 32;) {
+            const int owner = row / RS;
+            const int end = min(warp * 32 + 32, (owner + 1) * RS);
+            if (owner != rank) {
+                const uint32_t dst = base + Lo.recv + (static_cast<uint32_t>(rank) * RS + row % RS) * stride_b;
+                bulk_copy_to_peer(map_cluster(dst, owner), base + row * stride_b, (end - row) * stride_b,
+                                  map_cluster(bar_recv, owner));
+            }
+            row = end;
+        }
+    }
+    if (CK > 1 && !mbar_wait(bar_recv, 0)) {
+        flag_error(a.err, TTS_ERRBIT_TIMEOUT);
+        atomicExch(failed, 1);
+    }
+    // Every row sent to this CTA has landed, so every copy reading this CTA's
+    // dump that targets it is done; the matching wait before exit keeps each
+    // CTA's shared memory alive until all copies of the cluster have landed.
+    if (CK > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
     // ---- epilogue part 2: sum the CK partial copies of this CTA's RS rows and
     // select per batch column.  Work item = (8-row group, column); consecutive
-    // threads take consecutive columns.
+    // threads take consecutive columns.  Source `rank` is this CTA's own dump.
+    const float *recv = reinterpret_cast<const float *>(smem + Lo.recv);
     const int items = (RS / 8) * N;
     for (int item = threadIdx.x; item < items; item += blockDim.x) {
         const int gi = item / N, cn = item % N;
@@ -397,7 +455,9 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
 #pragma unroll
         for (int e = 0; e < 8; ++e) lg[e] = 0.0f;
         for (int src = 0; src < CK; ++src) {
-            const float *col = recv + (static_cast<size_t>(src) * RS + gi * 8) * Lo.dump_stride + cn;
+            const float *col = src == rank
+                                   ? dump + (static_cast<size_t>(rank) * RS + gi * 8) * Lo.dump_stride + cn
+                                   : recv + (static_cast<size_t>(src) * RS + gi * 8) * Lo.dump_stride + cn;
 #pragma unroll
             for (int e = 0; e < 8; ++e) lg[e] += col[e * Lo.dump_stride];
         }
@@ -447,17 +507,22 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
         if (best) atomicMax(colbest + cn, best);
     }
     __syncthreads();
-    // One global atomic per column and cluster: every other rank stores its
-    // column maxima into its own slot of rank 0's table (plain remote stores,
-    // ordered by the cluster barrier), and rank 0 folds them.
+    // One global atomic per column and cluster: every other rank sends its
+    // column maxima into its own slot of rank 0's table (asynchronous remote
+    // stores completing on rank 0's mbarrier), and rank 0 folds them.
     if (CK > 1 && rank != 0) {
-        unsigned long long *slot = map_cluster_ptr(colbest + rank * N, 0u);
-        for (int cn = threadIdx.x; cn < N; cn += blockDim.x) slot[cn] = colbest[cn];
+        const uint32_t slot = map_cluster(base + Lo.colbest + static_cast<uint32_t>(rank) * N * 8, 0u);
+        const uint32_t fold = map_cluster(bar_fold, 0u);
+        for (int cn = threadIdx.x; cn < N; cn += blockDim.x) st_async_u64(slot + cn * 8, colbest[cn], fold);
     }
-    if (CK > 1) cluster_sync();  // keys have arrived at rank 0
+    if (CK > 1) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
     // Only rank 0 of each cluster publishes keys, so only those CTAs take a
     // ticket: the last ticket then comes after every publication.
     if (rank != 0) return;
+    if (CK > 1 && !mbar_wait(bar_fold, 0)) {
+        flag_error(a.err, TTS_ERRBIT_TIMEOUT);
+        atomicExch(failed, 1);
+    }
     for (int cn = threadIdx.x; cn < N; cn += blockDim.x) {
         unsigned long long k = colbest[cn];
         for (int src = 1; src < CK; ++src) {
@@ -483,19 +548,21 @@ TcPlan plan_tc(int R, int H, int V) {
     p.N = (per + 15) / 16 * 16;
     p.alloc_cols = 32;
     while (p.alloc_cols < p.N) p.alloc_cols <<= 1;
-    p.smem = tc_layout(p.N).total;
     const int sms = sm_count() > 0 ? sm_count() : 148;
-    int per_sm = static_cast<int>((227u * 1024u) / (p.smem + 1024u));
-    per_sm = per_sm < 1 ? 1 : per_sm;
     const int tmem_fit = 512 / p.alloc_cols;
-    per_sm = per_sm < tmem_fit ? per_sm : tmem_fit;
     const int vtiles = (V + kTileM - 1) / kTileM;
     const int ktiles = H / kTileK;
     p.CK = 1;
+    p.smem = tc_layout(p.N, 1).total;
+    // widest cluster split of the hidden dimension that still runs in one wave
     for (int ck = 2; ck <= 8; ck <<= 1) {
         if (ktiles % ck != 0) break;
-        if (static_cast<long>(vtiles) * p.chunks * ck > static_cast<long>(sms) * per_sm) break;
+        const uint32_t smem = tc_layout(p.N, ck).total;
+        int per_sm = static_cast<int>((227u * 1024u) / (smem + 1024u));
+        per_sm = per_sm < tmem_fit ? per_sm : tmem_fit;
+        if (per_sm < 1 || static_cast<long>(vtiles) * p.chunks * ck > static_cast<long>(sms) * per_sm) break;
         p.CK = ck;
+        p.smem = smem;
     }
     return p;
 }
