@@ -53,6 +53,10 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle baseline in the native line")
     ap.add_argument("--e2e-steps", type=int, default=1000)
+    ap.add_argument("--sweep", default="2,4,5",
+                    help="other workloads whose kernels are timed one by one into the line's "
+                         "'workloads' object (comma-separated ids; empty: none)")
+    ap.add_argument("--sweep-reps", type=int, default=30)
     return ap.parse_args(argv)
 
 
@@ -124,6 +128,18 @@ def attn_bytes(inp) -> int:
 
 def head_bytes(w) -> int:
     return w.V * w.H * w.elem_bytes + w.R * w.H * w.elem_bytes + 4 * w.R
+
+
+def head_line_bytes(w) -> int:
+    """Head bytes including the fp32 logits the verify path writes out."""
+    return head_bytes(w) + (w.R * w.V * 4 if w.logits_out else 0)
+
+
+def verify_bytes(w) -> int:
+    """Algorithmic bytes of one spec-verify launch without the bonus draw: the
+    K target rows and K draft rows of every stream (fp32), the draft tokens,
+    the two outputs."""
+    return 2 * w.B * w.K * w.V * 4 + w.B * w.K * 4 + 2 * w.B * 4
 
 
 def append_bytes(w) -> int:
@@ -261,6 +277,81 @@ def run_reference(args):
     }
     print(json.dumps(line))
     return 0
+
+
+def kernel_sweep(ids, reps, flush_l2, peaks, device) -> dict:
+    """Each kernel of the other workloads launched alone `reps` times, L2
+    flushed before every launch, CUDA events around it (mean over launches),
+    with its roofline fraction against the measured HBM peak (tensor peak too
+    for the head).  The pool is appended to once first, so attention reads
+    the step's own new tokens."""
+    import torch
+    from decode_step_gb300 import binding as bd
+
+    def dev(x):
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+        if x.dtype == np.uint64:
+            return torch.from_numpy(x.view(np.int64)).to(device)
+        return torch.from_numpy(np.ascontiguousarray(x)).to(device)
+
+    def timed(fn):
+        ts = []
+        for _ in range(reps):
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.fmean(ts[2:])
+
+    hbm = peaks["hbm_gbs"]
+    out = {}
+    for wid in ids:
+        w = wl.WORKLOADS[wid]
+        inp = wl.make_inputs(w)
+        d = {k: dev(inp[k]) for k in ("block_table", "ctx_before", "ctx_lens", "q", "k_new", "v_new", "h", "W",
+                                       "seed", "step")}
+        cache = bd.KVCache(dev(inp["k_pool"]), dev(inp["v_pool"]))
+        bd.tts_kv_append(cache, d["block_table"], d["ctx_before"], d["k_new"], d["v_new"])
+        attn_out = torch.empty_like(d["q"])
+        ws = torch.zeros(bd.tts_decode_attn_workspace_size(w.B, w.q_len, w.Hq, w.Hkv, w.D, w.ctx_hi),
+                         dtype=torch.uint8, device=device)
+        t_att = timed(lambda: bd.tts_decode_attn(cache, d["block_table"], d["ctx_lens"], w.ctx_hi, d["q"],
+                                                 attn_out, ws, inp["scale"], w.causal))
+        ab = attn_bytes(inp)
+        ids_t = torch.empty(w.R, dtype=torch.int32, device=device)
+        hws = torch.zeros(bd.tts_head_workspace_size(w.R, w.V), dtype=torch.uint8, device=device)
+        logits = torch.empty(w.R, w.V, dtype=torch.float32, device=device) if w.logits_out else None
+        mode = bd.TTS_GUMBEL if w.mode == "gumbel" else bd.TTS_ARGMAX
+        t_head = timed(lambda: bd.tts_codebook_head_select(d["h"], d["W"], ids_t, hws, mode=mode,
+                                                           temperature=w.T, seed=d["seed"], step=d["step"],
+                                                           logits_out=logits))
+        hb = head_line_bytes(w)
+        flops = 2.0 * w.R * w.H * w.V
+        entry = {
+            "decode_attn_us": t_att, "decode_attn_gbs": ab / t_att / 1e3, "decode_attn_frac": ab / t_att / 1e3 / hbm,
+            "decode_attn_bytes": ab,
+            "head_select_us": t_head, "head_gbs": hb / t_head / 1e3, "head_frac_hbm": hb / t_head / 1e3 / hbm,
+            "head_tflops": flops / t_head / 1e6,
+            "head_frac_tensor": flops / t_head / 1e6 / peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]),
+            "head_bytes": hb, "head_mode": w.mode,
+        }
+        if w.K > 0:
+            tl, dp = dev(inp["target_logits"]), dev(inp["draft_probs"])
+            dt, vs, vt = dev(inp["draft_tokens"]), dev(inp["vseed"]), dev(inp["vstep"])
+            n_acc = torch.empty(w.B, dtype=torch.int32, device=device)
+            nxt = torch.empty(w.B, dtype=torch.int32, device=device)
+            t_ver = timed(lambda: bd.tts_spec_verify(tl, dp, dt, w.T, vs, vt, n_acc, nxt))
+            vb = verify_bytes(w)
+            entry.update({"spec_verify_us": t_ver, "spec_verify_gbs": vb / t_ver / 1e3,
+                          "spec_verify_frac": vb / t_ver / 1e3 / hbm, "spec_verify_bytes": vb})
+        out[w.name] = entry
+        del cache, d, attn_out, ws
+        torch.cuda.empty_cache()
+    return out
 
 
 def workload_config(w, world):
@@ -460,6 +551,11 @@ def run_native(args):
     }
     if world == 1:
         line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
+        ids = [int(x) for x in args.sweep.split(",") if x.strip()]
+        if ids:
+            del step, graphed, cache, W, d
+            torch.cuda.empty_cache()
+            line["workloads"] = kernel_sweep(ids, args.sweep_reps, flush_l2, peaks, device)
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

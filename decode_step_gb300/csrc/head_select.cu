@@ -33,7 +33,11 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr int kTileM = 128;           // vocab rows per MMA tile
 constexpr int kTileK = 64;            // hidden elements per stage (one 128-byte swizzle span)
 constexpr int kStagesTC = 4;
-constexpr int kThreadsTC = 192;       // warps 0-3 epilogue, 4 TMA producer, 5 MMA issuer
+// Warps 0-3 read the accumulator, 4 is the TMA producer, 5 the MMA issuer;
+// all twelve share the token-selection loop, whose Gumbel path (one
+// Philox4x64-10 block per 8 vocabulary entries) is bound by the latency of its
+// 64-bit multiply chains and wants many warps.
+constexpr int kThreadsTC = 384;
 constexpr int kMaxN = 256;            // widest MMA N
 constexpr int kATileBytes = kTileM * kTileK * 2;  // 16 KB
 
@@ -266,7 +270,7 @@ __device__ __forceinline__ void st_async_u64(uint32_t dst_cluster, unsigned long
                  : "memory");
 }
 
-__global__ void __launch_bounds__(kThreadsTC, 1)
+__global__ void __launch_bounds__(kThreadsTC, 2)
 head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_h,
                const HeadArgs a, int N, int CK, int alloc_cols) {
     extern __shared__ uint8_t smem_raw[];
@@ -447,11 +451,14 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
     // threads take consecutive columns.  Source `rank` is this CTA's own dump.
     const float *recv = reinterpret_cast<const float *>(smem + Lo.recv);
     const int items = (RS / 8) * N;
-    for (int item = threadIdx.x; item < items; item += blockDim.x) {
-        const int gi = item / N, cn = item % N;
-        const int r = r0 + cn;
-        if (r >= a.R) continue;
-        float lg[8];
+    // Item `item` -> its column, batch row, first vocabulary entry, the end of
+    // the entries it may select, and its 8 summed logits (written out too if
+    // asked).  False if the item selects nothing.
+    auto load_item = [&](int item, int &cn, int &r, int &v, int &vmax, float *lg) -> bool {
+        const int gi = item / N;
+        cn = item - gi * N;
+        r = r0 + cn;
+        if (r >= a.R) return false;
 #pragma unroll
         for (int e = 0; e < 8; ++e) lg[e] = 0.0f;
         for (int src = 0; src < CK; ++src) {
@@ -461,21 +468,24 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
 #pragma unroll
             for (int e = 0; e < 8; ++e) lg[e] += col[e * Lo.dump_stride];
         }
-        const int v = v0 + rank * RS + gi * 8;  // multiple of 8
+        v = v0 + rank * RS + gi * 8;  // multiple of 8
         if (a.logits_out) {
 #pragma unroll
             for (int e = 0; e < 8; ++e)
                 if (v + e < a.V) a.logits_out[static_cast<size_t>(r) * a.V + v + e] = lg[e];
         }
-        const int vmax = (a.eos && !a.eos[r]) ? a.V - 1 : a.V;
-        if (v >= vmax) continue;
-        unsigned long long best = 0ull;
-        if (a.mode == TTS_GUMBEL) {
-            // An entry can only beat the column's current best z_cur if its
-            // noise exceeds z_cur - logit / T.  With the group's largest logit
-            // that gives one uniform threshold for all 8 entries: below it
-            // (with a safety margin far above rounding) an entry cannot win,
-            // and its logarithms are skipped.  Exact for the entries kept.
+        vmax = (a.eos && !a.eos[r]) ? a.V - 1 : a.V;
+        return v < vmax;
+    };
+    if (a.mode == TTS_GUMBEL) {
+        // An entry can only beat the column's current best z_cur if its noise
+        // exceeds z_cur - logit / T.  With the group's largest logit that gives
+        // one uniform threshold for all 8 entries: below it (with a safety
+        // margin far above rounding) an entry cannot win, and its logarithms
+        // are skipped.  Exact for the entries kept.  Two items per pass, so
+        // each thread runs two independent Philox chains.
+        auto select = [&](bool live, int cn, int v, int vmax, const float *lg, const Philox4x64 &ph) {
+            if (!live) return;
             float lmax = -INFINITY;
 #pragma unroll
             for (int e = 0; e < 8; ++e)
@@ -486,7 +496,7 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
                 const float g0 = unpack_value(cur) - lmax / a.temperature - kGumbelSlack;
                 thr = expf(-expf(-g0));
             }
-            const Philox4x64 ph(static_cast<uint64_t>(v >> 3), 0, 0, 0, a.seed[r], a.step[r]);
+            unsigned long long best = 0ull;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 if (v + e >= vmax) break;
@@ -496,15 +506,34 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
                 const unsigned long long k = pack_argmax(key, v + e);
                 best = k > best ? k : best;
             }
-        } else {
+            if (best) atomicMax(colbest + cn, best);
+        };
+        for (int i0 = threadIdx.x; i0 < items; i0 += 2 * blockDim.x) {
+            const int i1 = i0 + blockDim.x;
+            int cn0, r0i, va, vmax0, cn1 = 0, r1i = 0, vb = 0, vmax1 = 0;
+            float lg0[8], lg1[8];
+            const bool live0 = load_item(i0, cn0, r0i, va, vmax0, lg0);
+            const bool live1 = i1 < items && load_item(i1, cn1, r1i, vb, vmax1, lg1);
+            const int ra = live0 ? r0i : r0, rb = live1 ? r1i : r0;
+            const Philox4x64 pa(static_cast<uint64_t>(va >> 3), 0, 0, 0, a.seed[ra], a.step[ra]);
+            const Philox4x64 pb(static_cast<uint64_t>(vb >> 3), 0, 0, 0, a.seed[rb], a.step[rb]);
+            select(live0, cn0, va, vmax0, lg0, pa);
+            select(live1, cn1, vb, vmax1, lg1, pb);
+        }
+    } else {
+        for (int item = threadIdx.x; item < items; item += blockDim.x) {
+            int cn, r, v, vmax;
+            float lg[8];
+            if (!load_item(item, cn, r, v, vmax, lg)) continue;
+            unsigned long long best = 0ull;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 if (v + e >= vmax) break;
                 const unsigned long long k = pack_argmax(lg[e], v + e);
                 best = k > best ? k : best;
             }
+            if (best) atomicMax(colbest + cn, best);
         }
-        if (best) atomicMax(colbest + cn, best);
     }
     __syncthreads();
     // One global atomic per column and cluster: every other rank sends its
@@ -560,6 +589,7 @@ TcPlan plan_tc(int R, int H, int V) {
         const uint32_t smem = tc_layout(p.N, ck).total;
         int per_sm = static_cast<int>((227u * 1024u) / (smem + 1024u));
         per_sm = per_sm < tmem_fit ? per_sm : tmem_fit;
+        per_sm = per_sm < 2 ? per_sm : 2;  // registers: the kernel is built for two CTAs per SM
         if (per_sm < 1 || static_cast<long>(vtiles) * p.chunks * ck > static_cast<long>(sms) * per_sm) break;
         p.CK = ck;
         p.smem = smem;

@@ -138,6 +138,55 @@ def test_spec_verify(orc):
         assert int(err.item()) == 0
 
 
+def _verify_case(B, K, V, seed):
+    """Seeded verify inputs of any shape: N(0,1) target logits, draft-model
+    probabilities and tokens, per-stream Philox keys."""
+    rng = np.random.default_rng(seed)
+    tl = rng.standard_normal((B, K + 1, V), dtype=np.float32)
+    dp, dt = wl.draft_model_outputs(B, K, V, rng)
+    vseed = (wl.PHILOX_SEED_MUL * 11 + np.arange(B)).astype(np.uint64)
+    vstep = np.full(B, 3, dtype=np.uint64)
+    return tl, dp, dt, vseed, vstep
+
+
+# Shapes around both verify kernels: shared-memory staged (small rows, ragged
+# 16-byte ends, one to sixteen drafts) and streaming (rows too large to stage).
+@pytest.mark.parametrize("B,K,V", [(8, 1, 37), (16, 3, 4097), (8, 7, 1000), (6, 16, 513), (4, 4, 16385),
+                                   (3, 2, 3)])
+def test_spec_verify_shapes(orc, B, K, V):
+    tl, dp, dt, vseed, vstep = _verify_case(B, K, V, 1234 + B * K + V)
+    T = 0.7
+    for bonus in (False, True):
+        n_acc = torch.empty(B, dtype=torch.int32, device="cuda")
+        nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        bd.tts_spec_verify(dev(tl), dev(dp), dev(dt), T, dev(vseed), dev(vstep), n_acc, nxt, bonus=bonus, err=err)
+        torch.cuda.synchronize()
+        ref = orc.spec_verify(tl, dp, dt, T, vseed, vstep, bonus=bonus)
+        tie = (ref["gap_accept"] < NEAR_TIE) | (ref["gap_resid"] < NEAR_TIE)
+        bad = (host(n_acc) != ref["n_accepted"]) | (host(nxt) != ref["next_token"])
+        assert not (bad & ~tie).any(), f"verify B={B} K={K} V={V} bonus={bonus} differs at {np.nonzero(bad & ~tie)[0]}"
+        assert int(err.item()) == 0
+
+
+def test_spec_verify_bad_token():
+    """A draft token outside the vocabulary where the walk reaches it stops the
+    walk there with no draw and sets the token error bit."""
+    B, K, V = 4, 3, 4097
+    tl, dp, dt, vseed, vstep = _verify_case(B, K, V, 77)
+    dt = dt.copy()
+    dt[1, 0] = V
+    dt[2, 0] = -5
+    n_acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bd.tts_spec_verify(dev(tl), dev(dp), dev(dt), 0.7, dev(vseed), dev(vstep), n_acc, nxt, err=err)
+    torch.cuda.synchronize()
+    assert host(n_acc)[1] == 0 and host(nxt)[1] == -1
+    assert host(n_acc)[2] == 0 and host(nxt)[2] == -1
+    assert int(err.item()) & bd._lib.ERRBIT_TOKEN
+
+
 @pytest.mark.parametrize("wid", [3, 5])
 def test_full_step_chain(orc, wid):
     """Append -> attention -> head on one stream, as the benchmark runs it."""
