@@ -130,9 +130,12 @@ int tts_kv_append(const tts_kv_cache *cache, const int32_t *d_block_table,
 /* ------------------------------------------------------------- attention */
 
 /* Bytes of device workspace tts_decode_attn needs for these sizes (0 on bad
- * arguments).  The workspace must be zero-filled before its first use; every
- * completed call leaves it zero-filled again, so one zeroed buffer serves any
- * number of calls on one stream.  Calls that overlap on the GPU need separate
+ * arguments).  Layout: scratch for the partial results of split (stream, KV
+ * head) segments, then one int32 ticket per (stream, KV head) in the last
+ * 256-byte-aligned part.  The workspace must be zero-filled before its first
+ * use; every completed call leaves the tickets zero again (the scratch part
+ * needs no particular contents), so one zeroed buffer serves any number of
+ * calls on one stream.  Calls that overlap on the GPU need separate
  * workspaces. */
 size_t tts_decode_attn_workspace_size(int32_t B, int32_t q_len, int32_t num_q_heads,
                                       int32_t num_kv_heads, int32_t head_dim,
