@@ -61,22 +61,34 @@ class GraphedStep:
     """A captured serving step: pinned host inputs -> device -> step -> pinned ids.
 
     `inputs` maps names of DecodeStep's call arguments (block_table, ctx_before,
-    ctx_lens, q, k_new, v_new, and optionally seed, step) to device tensors
-    used as the step's input buffers; a pinned host twin of each is made.
+    ctx_lens, q, k_new, v_new, and optionally seed, step) to tensors giving
+    each input's shape, dtype and first contents.  The step's inputs live in
+    one pinned host buffer mirrored by one device buffer (`host[name]` and
+    `dev[name]` are views into them, 256-byte aligned), so a replay moves all
+    of them with a single host-to-device copy: each copy in a graph pays a
+    fixed latency of its own.  Write a step's inputs into `host[...]`, call
+    the object, read the ids it returns.
     """
 
     NAMES = ("block_table", "ctx_before", "ctx_lens", "q", "k_new", "v_new", "seed", "step")
 
     def __init__(self, step: DecodeStep, inputs: dict):
         self.step = step
-        self.dev = dict(inputs)
-        self.host = {}
-        for k, t in self.dev.items():
+        offsets, total = {}, 0
+        for k, t in inputs.items():
             if k not in self.NAMES:
                 raise ValueError(f"unknown step input {k}")
-            h = torch.empty(t.shape, dtype=t.dtype, device="cpu").pin_memory()
-            h.copy_(t.cpu())
-            self.host[k] = h
+            offsets[k] = total
+            total += -(-(t.numel() * t.element_size()) // 256) * 256
+        device = next(iter(inputs.values())).device
+        self.host_blob = torch.empty(total, dtype=torch.uint8, device="cpu").pin_memory()
+        self.dev_blob = torch.empty(total, dtype=torch.uint8, device=device)
+        self.host, self.dev = {}, {}
+        for k, t in inputs.items():
+            n = t.numel() * t.element_size()
+            self.host[k] = self.host_blob[offsets[k]:offsets[k] + n].view(t.dtype).view(t.shape)
+            self.dev[k] = self.dev_blob[offsets[k]:offsets[k] + n].view(t.dtype).view(t.shape)
+            self.host[k].copy_(t.detach().cpu())
         self.ids_host = torch.empty(step.R, dtype=torch.int32, device="cpu").pin_memory()
         self.stream = torch.cuda.Stream()
         self.graph = torch.cuda.CUDAGraph()
@@ -88,14 +100,14 @@ class GraphedStep:
             self._body()
 
     def _body(self):
-        for k, t in self.dev.items():
-            t.copy_(self.host[k], non_blocking=True)
+        self.dev_blob.copy_(self.host_blob, non_blocking=True)
         ids = self.step(**self.dev)
         self.ids_host.copy_(ids, non_blocking=True)
 
     @property
     def h2d_bytes(self) -> int:
-        return sum(t.numel() * t.element_size() for t in self.host.values())
+        """Bytes of the one host-to-device copy a replay makes (inputs and padding)."""
+        return self.host_blob.numel()
 
     def __call__(self) -> torch.Tensor:
         """Replays the step and returns the (pinned, host) ids once they are there."""

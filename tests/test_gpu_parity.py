@@ -396,4 +396,11 @@ def test_graphed_step_matches_direct_step():
     for _ in range(3):
         g.ids_host.fill_(-7)           # a replay that did not finish would leave this
         assert torch.equal(g().clone(), direct.cpu())
+    # new inputs written into the pinned host views reach the step
+    q2 = torch.randn(u.q.shape, device="cuda").to(u.q.dtype)
+    direct2 = step(u.table, u.ctx_before, u.ctx_lens, q2, u.k_new, u.v_new).clone()
+    g.host["q"].copy_(q2.cpu())
+    g.ids_host.fill_(-7)
+    assert torch.equal(g().clone(), direct2.cpu())
+    assert not torch.equal(direct2, direct)
     assert int(step.err.item()) == 0
