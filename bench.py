@@ -480,9 +480,9 @@ def run_native(args):
     t_att_w = [e[1].elapsed_time(e[2]) for e in kev[K2:]]
     t_head_w = [e[2].elapsed_time(e[3]) for e in kev[K2:]]
 
-    # ---- end to end through the public API with host buffers: a captured
-    # graph copies the step's inputs in from pinned host memory, runs the
-    # step and copies the ids back; wall clock, synchronised every step.
+    # ---- end to end through the public API with host buffers: the library's
+    # captured step copies the step's inputs in from pinned host memory, runs
+    # the step and writes the ids back; wall clock, synchronised every step.
     from decode_step_gb300.step import GraphedStep
     g_inputs = {k: d[k] for k in names}
     if mode == bd.TTS_GUMBEL:
@@ -545,9 +545,11 @@ def run_native(args):
         "device_error_flags": errflags,
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": n_e2e, "note": "wall clock; a captured CUDA graph copies the inputs in from "
-                                        "pinned host memory, runs the step and copies the ids back; "
-                                        "the host synchronises every step"},
+                "steps": n_e2e, "note": "wall clock; tts_step_graph (one CUDA graph captured by the "
+                                        "library): a copy kernel reads the step's packed inputs from "
+                                        "pinned host memory, the step runs, the ids and a boundary-token "
+                                        "count are written to pinned host memory; the host launches and "
+                                        "synchronises every step"},
     }
     if world == 1:
         line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)

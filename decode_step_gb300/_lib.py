@@ -30,6 +30,18 @@ class KVCacheDesc(ctypes.Structure):
                 ("head_dim", _i32), ("dtype", _i32), ("k_pool", _vp), ("v_pool", _vp)]
 
 
+class StepGraphDesc(ctypes.Structure):
+    """tts_step_graph_desc."""
+    _fields_ = [("cache", ctypes.POINTER(KVCacheDesc)), ("d_block_table", _vp), ("max_blocks_per_seq", _i32),
+                ("d_ctx_before", _vp), ("d_ctx_lens", _vp), ("max_ctx_len", _i32), ("B", _i32), ("q_len", _i32),
+                ("num_q_heads", _i32), ("scale", _f32), ("causal", _i32), ("d_q", _vp), ("d_k_new", _vp),
+                ("d_v_new", _vp), ("d_attn_out", _vp), ("d_attn_ws", _vp), ("attn_ws_bytes", _sz), ("d_W", _vp),
+                ("V", _i32), ("mode", _i32), ("temperature", _f32), ("d_seed", _vp), ("d_step", _vp),
+                ("d_eos_allowed", _vp), ("d_ids", _vp), ("d_best", _vp), ("d_logits_out", _vp),
+                ("d_head_ws", _vp), ("head_ws_bytes", _sz), ("d_err", _vp), ("h_inputs", _vp), ("d_inputs", _vp),
+                ("input_bytes", _sz), ("h_ids", _vp), ("h_boundary_count", _vp)]
+
+
 _SIGNATURES = {
     "tts_block_pool_create": (ctypes.c_int, [_i32, ctypes.POINTER(_vp)]),
     "tts_block_pool_alloc": (ctypes.c_int, [_vp, _i32, _vp]),
@@ -52,6 +64,9 @@ _SIGNATURES = {
                                        _i32, _i32, _f32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp,
                                        _i32, _i32, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
                                        _vp, _vp]),
+    "tts_step_graph_create": (ctypes.c_int, [ctypes.POINTER(StepGraphDesc), ctypes.POINTER(_vp)]),
+    "tts_step_graph_launch": (ctypes.c_int, [_vp, _vp]),
+    "tts_step_graph_destroy": (None, [_vp]),
     "tts_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "tts_version": (ctypes.c_int, []),
 }

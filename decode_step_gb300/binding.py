@@ -194,10 +194,10 @@ def tts_spec_verify(target_logits, draft_probs, draft_tokens, temperature, seed,
     check("tts_spec_verify", lib().tts_spec_verify(*args))
 
 
-def tts_decode_step(cache: KVCache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new,
-                    attn_out, attn_ws, scale, W, ids, head_ws, causal=False, mode=TTS_ARGMAX,
-                    temperature=0.0, seed=None, step=None, eos_allowed=None, best=None,
-                    logits_out=None, err=None, stream=None):
+def _step_args(cache: KVCache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new,
+               attn_out, attn_ws, scale, W, ids, head_ws, causal, mode, temperature, seed, step,
+               eos_allowed, best, logits_out, err, stream):
+    """tts_decode_step's argument tuple (the cache as a byref, the stream last)."""
     B, max_blocks = block_table.shape
     _, q_len, Hq, D = q.shape
     kv_shape = (B, q_len, cache.num_kv_heads, cache.head_dim)
@@ -218,7 +218,80 @@ def tts_decode_step(cache: KVCache, block_table, ctx_before, ctx_lens, max_ctx_l
             None if logits_out is None else _dev(logits_out, "logits_out", torch.float32, (R, V)),
             _dev(head_ws, "head_ws"), head_ws.numel() * head_ws.element_size(),
             None if err is None else _dev(err, "err", torch.int32), _stream(stream))
+    return args
+
+
+def tts_decode_step(cache: KVCache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new,
+                    attn_out, attn_ws, scale, W, ids, head_ws, causal=False, mode=TTS_ARGMAX,
+                    temperature=0.0, seed=None, step=None, eos_allowed=None, best=None,
+                    logits_out=None, err=None, stream=None):
+    args = _step_args(cache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new, attn_out,
+                      attn_ws, scale, W, ids, head_ws, causal, mode, temperature, seed, step, eos_allowed,
+                      best, logits_out, err, stream)
     check("tts_decode_step", lib().tts_decode_step(*args))
+
+
+def _pinned(t: torch.Tensor, name: str, dtype=None, numel=None):
+    if t.is_cuda or not t.is_pinned():
+        raise ValueError(f"{name} must be a pinned host tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} must have {numel} elements")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+class StepGraph:
+    """tts_step_graph_*: a decode step captured once as a CUDA graph.
+
+    Takes tts_decode_step's arguments (its input tensors normally views into
+    `d_inputs`) plus the host side: `h_inputs` (pinned, copied to `d_inputs`
+    by every launch), `h_ids` (pinned int32 [B * q_len], written by every
+    launch) and optionally `h_boundary_count` (pinned int32 [1]: rows whose id
+    is the boundary token V - 1).  Every tensor passed must outlive the graph;
+    the object keeps references to them.
+    """
+
+    def __init__(self, cache: KVCache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new,
+                 attn_out, attn_ws, scale, W, ids, head_ws, h_inputs, d_inputs, h_ids,
+                 h_boundary_count=None, causal=False, mode=TTS_ARGMAX, temperature=0.0, seed=None,
+                 step=None, eos_allowed=None, best=None, logits_out=None, err=None):
+        args = _step_args(cache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new, attn_out,
+                          attn_ws, scale, W, ids, head_ws, causal, mode, temperature, seed, step,
+                          eos_allowed, best, logits_out, err, None)
+        R = ids.numel()
+        nbytes = h_inputs.numel() * h_inputs.element_size()
+        if d_inputs.numel() * d_inputs.element_size() != nbytes or not d_inputs.is_cuda:
+            raise ValueError("d_inputs must be a device tensor of h_inputs' size")
+        host = (_pinned(h_inputs, "h_inputs"), _dev(d_inputs, "d_inputs"), nbytes,
+                _pinned(h_ids, "h_ids", torch.int32, R),
+                None if h_boundary_count is None else _pinned(h_boundary_count, "h_boundary_count",
+                                                              torch.int32, 1))
+        desc = _lib.StepGraphDesc(ctypes.pointer(cache.desc), *args[1:-1], *host)
+        handle = ctypes.c_void_p()
+        check("tts_step_graph_create", lib().tts_step_graph_create(ctypes.byref(desc), ctypes.byref(handle)))
+        self._handle = handle
+        self._keep = (cache, block_table, ctx_before, ctx_lens, q, k_new, v_new, attn_out, attn_ws, W, ids,
+                      head_ws, h_inputs, d_inputs, h_ids, h_boundary_count, seed, step, eos_allowed, best,
+                      logits_out, err)
+
+    def launch(self, stream=None) -> None:
+        if self._handle is None:
+            raise ValueError("graph destroyed")
+        check("tts_step_graph_launch", lib().tts_step_graph_launch(self._handle, _stream(stream)))
+
+    def close(self) -> None:
+        if getattr(self, "_handle", None) is not None:
+            lib().tts_step_graph_destroy(self._handle)
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def tts_status_string(code: int) -> str:

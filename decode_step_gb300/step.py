@@ -6,11 +6,11 @@ launched as programmatic dependents) on one stream.  The attention output
 [B][q_len][Hq][D] is read by the head as h [B * q_len][Hq * D], so Hq * D must
 equal the head's hidden width.
 
-`GraphedStep` captures, once, a CUDA graph of a whole serving step for fixed
-buffers: the host-to-device copies of the step's inputs from pinned host
-memory, the decode step, and the copy of the chosen ids back to pinned host
-memory.  Each step then is: write the pinned inputs, replay, synchronise,
-read the pinned ids.
+`GraphedStep` wraps tts_step_graph: a whole serving step captured once by the
+library for fixed buffers (the copy of the step's inputs from pinned host
+memory, the decode step, the chosen ids and a boundary-token count back to
+pinned host memory).  Each step then is: write the pinned inputs, launch,
+synchronise, read the pinned ids.
 """
 from __future__ import annotations
 
@@ -64,15 +64,17 @@ class GraphedStep:
     ctx_lens, q, k_new, v_new, and optionally seed, step) to tensors giving
     each input's shape, dtype and first contents.  The step's inputs live in
     one pinned host buffer mirrored by one device buffer (`host[name]` and
-    `dev[name]` are views into them, 256-byte aligned), so a replay moves all
-    of them with a single host-to-device copy: each copy in a graph pays a
-    fixed latency of its own.  Write a step's inputs into `host[...]`, call
-    the object, read the ids it returns.
+    `dev[name]` are views into them, 256-byte aligned).  The library captures
+    the whole step once (tts_step_graph_create): a launch copies the packed
+    inputs with one kernel reading the pinned buffer, runs the step, and writes
+    the ids and the count of rows that picked the boundary token into pinned
+    host memory.  Write a step's inputs into `host[...]`, call the object, read
+    the ids it returns (`boundary_count` holds the count).
     """
 
     NAMES = ("block_table", "ctx_before", "ctx_lens", "q", "k_new", "v_new", "seed", "step")
 
-    def __init__(self, step: DecodeStep, inputs: dict):
+    def __init__(self, step: DecodeStep, inputs: dict, stream: torch.cuda.Stream | None = None):
         self.step = step
         offsets, total = {}, 0
         for k, t in inputs.items():
@@ -89,29 +91,29 @@ class GraphedStep:
             self.host[k] = self.host_blob[offsets[k]:offsets[k] + n].view(t.dtype).view(t.shape)
             self.dev[k] = self.dev_blob[offsets[k]:offsets[k] + n].view(t.dtype).view(t.shape)
             self.host[k].copy_(t.detach().cpu())
-        self.ids_host = torch.empty(step.R, dtype=torch.int32, device="cpu").pin_memory()
-        self.stream = torch.cuda.Stream()
-        self.graph = torch.cuda.CUDAGraph()
-        self.stream.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(self.stream):
-            self._body()  # warm-up outside capture (one-time set-up of the library)
-        self.stream.synchronize()
-        with torch.cuda.graph(self.graph, stream=self.stream):
-            self._body()
-
-    def _body(self):
-        self.dev_blob.copy_(self.host_blob, non_blocking=True)
-        ids = self.step(**self.dev)
-        self.ids_host.copy_(ids, non_blocking=True)
+        self.ids_host = torch.zeros(step.R, dtype=torch.int32, device="cpu").pin_memory()
+        self.boundary_host = torch.zeros(1, dtype=torch.int32, device="cpu").pin_memory()
+        self.stream = torch.cuda.Stream() if stream is None else stream
+        d = self.dev
+        self.graph = bd.StepGraph(
+            step.cache, d["block_table"], d["ctx_before"], d["ctx_lens"], step.max_ctx_len, d["q"],
+            d["k_new"], d["v_new"], step.out, step.attn_ws, step.scale, step.W, step.ids, step.head_ws,
+            self.host_blob, self.dev_blob, self.ids_host, self.boundary_host, causal=step.causal,
+            mode=step.mode, temperature=step.temperature, seed=d.get("seed"), step=d.get("step"),
+            err=step.err)
 
     @property
     def h2d_bytes(self) -> int:
-        """Bytes of the one host-to-device copy a replay makes (inputs and padding)."""
+        """Bytes a launch copies from the pinned input buffer (inputs and padding)."""
         return self.host_blob.numel()
 
+    @property
+    def boundary_count(self) -> int:
+        """Rows whose id is the boundary token in the last completed launch."""
+        return int(self.boundary_host.item())
+
     def __call__(self) -> torch.Tensor:
-        """Replays the step and returns the (pinned, host) ids once they are there."""
-        with torch.cuda.stream(self.stream):  # replay() launches on the current stream
-            self.graph.replay()
+        """Runs the captured step and returns the (pinned, host) ids once they are there."""
+        self.graph.launch(self.stream)
         self.stream.synchronize()
         return self.ids_host

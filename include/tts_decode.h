@@ -264,6 +264,81 @@ int tts_decode_step(const tts_kv_cache *cache, const int32_t *d_block_table,
                     float *d_logits_out, void *d_head_ws, size_t head_ws_bytes, int32_t *d_err,
                     void *stream);
 
+/* ------------------------------------------------------- captured step */
+
+/* A decode step captured once as a CUDA graph for fixed shapes and fixed
+ * buffers ("How We Made a TTS Model Respond in Sub-50 ms", section
+ * "Additional serving optimizations": graphs captured for a predefined set of
+ * batch sizes; "Optimizing Streaming Text-to-Speech Models for Sub-50
+ * Millisecond Latency", section "Engine-Level Optimizations with
+ * TensorRT-LLM": the CPU only starts the graph).  No counterpart API on the
+ * pages.  Each launch:
+ *   1. copies input_bytes from h_inputs (pinned host memory) to d_inputs with
+ *      a kernel reading the host buffer through unified addressing;
+ *   2. runs tts_decode_step with the fields below (the step's input pointers
+ *      normally point into d_inputs, so step 1 refreshes them);
+ *   3. writes d_ids[0..R) to h_ids (pinned host memory, R = B * q_len) and,
+ *      if h_boundary_count is not NULL, the number of rows whose id is the
+ *      boundary token V - 1 to *h_boundary_count (a device-side end-of-stream
+ *      flag: the host tests one word instead of scanning the ids).
+ * The caller writes a step's inputs into h_inputs, launches, synchronises the
+ * stream (or an event after the launch), and reads h_ids.  Every buffer is
+ * owned by the caller and must outlive the graph; the descriptor is read only
+ * by tts_step_graph_create.  Fields mean what tts_decode_step's arguments
+ * mean. */
+typedef struct {
+    const tts_kv_cache *cache;
+    const int32_t *d_block_table;
+    int32_t max_blocks_per_seq;
+    const int32_t *d_ctx_before;
+    const int32_t *d_ctx_lens;
+    int32_t max_ctx_len;
+    int32_t B;
+    int32_t q_len;
+    int32_t num_q_heads;
+    float scale;
+    int32_t causal;
+    const void *d_q;
+    const void *d_k_new;
+    const void *d_v_new;
+    void *d_attn_out;
+    void *d_attn_ws;
+    size_t attn_ws_bytes;
+    const void *d_W;
+    int32_t V;
+    int32_t mode;
+    float temperature;
+    const uint64_t *d_seed;
+    const uint64_t *d_step;
+    const uint8_t *d_eos_allowed;
+    int32_t *d_ids;
+    float *d_best;
+    float *d_logits_out;
+    void *d_head_ws;
+    size_t head_ws_bytes;
+    int32_t *d_err;
+    const void *h_inputs;       /* pinned host, 16-byte aligned */
+    void *d_inputs;             /* device, 16-byte aligned */
+    size_t input_bytes;         /* multiple of 16 */
+    int32_t *h_ids;             /* pinned host [R] */
+    int32_t *h_boundary_count;  /* pinned host, nullable */
+} tts_step_graph_desc;
+
+typedef struct tts_step_graph tts_step_graph;
+
+/* Checks every field (TTS_ERR_INVALID / _UNSUPPORTED / _WORKSPACE as
+ * tts_decode_step; TTS_ERR_INVALID for host buffers that are not pinned or
+ * misaligned transfer buffers), captures and instantiates the graph.  On
+ * success *out owns it.  Does not launch anything; the attention and head
+ * workspaces must be zero-filled before the first launch. */
+int tts_step_graph_create(const tts_step_graph_desc *desc, tts_step_graph **out);
+
+/* Launches the captured step on `stream` (asynchronous). */
+int tts_step_graph_launch(tts_step_graph *graph, void *stream);
+
+/* Frees the graph (no GPU work of it may still be pending).  NULL is a no-op. */
+void tts_step_graph_destroy(tts_step_graph *graph);
+
 /* ----------------------------------------------------------------- misc */
 
 /* Static description of a status code. */

@@ -403,4 +403,31 @@ def test_graphed_step_matches_direct_step():
     g.ids_host.fill_(-7)
     assert torch.equal(g().clone(), direct2.cpu())
     assert not torch.equal(direct2, direct)
+    assert g.boundary_count == int((direct2 == w.V - 1).sum())
     assert int(step.err.item()) == 0
+
+
+def test_graphed_step_boundary_count():
+    """The captured step counts the rows whose id is the boundary token V - 1
+    on the device: a boundary row of W aligned with half the streams'
+    attention outputs makes exactly those streams end."""
+    inp = wl.make_inputs(wl.custom(3, B=32), with_verify=False)
+    w = inp["workload"]
+    u = Uploaded(inp)
+    cache = bd.KVCache(u.k_pool, u.v_pool)
+    W = u.W.clone()
+    step = DecodeStep(cache, W, w.Hq, w.B, w.ctx_hi)
+    step(u.table, u.ctx_before, u.ctx_lens, u.q, u.k_new, u.v_new)  # fills the attention output
+    out = step.out.view(w.B, -1).float()
+    # boundary row: a large multiple of stream 0..15's mean output direction
+    direction = out[:16].mean(0)
+    W[w.V - 1] = (50.0 * direction / direction.norm()).to(W.dtype)
+    step.W = W
+    direct = step(u.table, u.ctx_before, u.ctx_lens, u.q, u.k_new, u.v_new).clone()
+    expect = int((direct == w.V - 1).sum())
+    assert expect > 0
+    g = GraphedStep(step, {"block_table": u.table, "ctx_before": u.ctx_before, "ctx_lens": u.ctx_lens,
+                           "q": u.q, "k_new": u.k_new, "v_new": u.v_new})
+    ids = g().clone()
+    assert torch.equal(ids, direct.cpu())
+    assert g.boundary_count == expect

@@ -116,3 +116,36 @@ def test_append_head_verify_argument_checks(L):
         FAKE, FAKE, FAKE, 4, k.get("K", 4), 97, k.get("T", 0.7), FAKE, FAKE, k.get("flags", 0),
         FAKE, FAKE, None, None)
     assert ver(K=0) == -1 and ver(K=17) == -1 and ver(T=0.0) == -1 and ver(flags=2) == -1
+
+
+def test_struct_layouts_match_header(tmp_path):
+    """The ctypes mirrors of tts_kv_cache and tts_step_graph_desc have the C
+    layout the header gives (compiled here against the header)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = [f for f, _ in _lib.StepGraphDesc._fields_]
+    src = ["#include <stdio.h>", "#include <stddef.h>", '#include "tts_decode.h"', "int main(void) {",
+           'printf("%zu %zu\\n", sizeof(tts_kv_cache), offsetof(tts_kv_cache, v_pool));',
+           'printf("%zu\\n", sizeof(tts_step_graph_desc));']
+    src += [f'printf("%zu\\n", offsetof(tts_step_graph_desc, {f}));' for f in fields]
+    src += ["return 0; }"]
+    (tmp_path / "lay.c").write_text("\n".join(src) + "\n")
+    subprocess.run([cc, "-I", str(_lib.HEADER.parent), "-o", str(tmp_path / "lay"), str(tmp_path / "lay.c")],
+                   check=True)
+    out = subprocess.run([str(tmp_path / "lay")], capture_output=True, text=True, check=True).stdout.split()
+    vals = [int(x) for x in out]
+    assert vals[0] == ctypes.sizeof(_lib.KVCacheDesc) and vals[1] == _lib.KVCacheDesc.v_pool.offset
+    assert vals[2] == ctypes.sizeof(_lib.StepGraphDesc)
+    assert vals[3:] == [getattr(_lib.StepGraphDesc, f).offset for f in fields]
+
+
+def test_step_graph_rejects_bad_descriptors(L):
+    handle = ctypes.c_void_p()
+    assert L.tts_step_graph_create(None, ctypes.byref(handle)) == -1
+    desc = _lib.StepGraphDesc()  # all null
+    assert L.tts_step_graph_create(ctypes.byref(desc), ctypes.byref(handle)) == -1
+    assert L.tts_step_graph_launch(None, None) == -1
+    L.tts_step_graph_destroy(None)
