@@ -132,19 +132,25 @@ int orc_kv_append(int num_blocks, int Hkv, int D, int elem_bytes, void *k_pool, 
 
 /* --------------------------------------------------------------- attention */
 
-/* One decode step's attention [TTS, "Token generation under a frame budget"]:
- * every query row of stream b attends over that stream's cached keys/values
- * (gathered through the block table), softmax(scale * q.k) weighted sum of v.
- * ctx_lens[b] counts tokens after the append.  Query row j of a q_len-row
- * block sees tokens t < ctx_lens[b] - q_len + j + 1 when causal, all
- * ctx_lens[b] tokens otherwise.  GQA: query head h reads KV head
- * h / (Hq / Hkv).  Output out[B][q_len][Hq][D] in double.
- * Returns 0, or -1 on an invalid block id or context length. */
-int orc_decode_attn(int num_blocks, int Hkv, int D, int is_bf16,
-                    const void *k_pool, const void *v_pool,
-                    const int32_t *block_table, int max_blocks, const int32_t *ctx_lens,
-                    int B, int q_len, int Hq, double scale, int causal,
-                    const void *q, double *out) {
+/* Element d of the cached key (is_v = 0) or value (is_v = 1) row of token slot
+ * `slot` of KV head g in physical block blk. */
+typedef double (*orc_kv_loader)(const void *ctx, int is_v, int blk, int g, int slot, int d);
+
+typedef struct {
+    int Hkv, D, is_bf16;
+    const void *k_pool, *v_pool;
+} orc_plain_pool;
+
+static double plain_kv(const void *ctx, int is_v, int blk, int g, int slot, int d) {
+    const orc_plain_pool *p = (const orc_plain_pool *)ctx;
+    const size_t off = (((size_t)blk * p->Hkv + g) * ORC_BLOCK + slot) * p->D + d;
+    return load_elem(is_v ? p->v_pool : p->k_pool, off, p->is_bf16);
+}
+
+static int attend(int num_blocks, int Hkv, int D, orc_kv_loader kv, const void *ctx,
+                  const int32_t *block_table, int max_blocks, const int32_t *ctx_lens,
+                  int B, int q_len, int Hq, double scale, int causal,
+                  const void *q, int q_is_bf16, double *out) {
     const int group = Hq / Hkv;
     double *s = (double *)malloc(sizeof(double) * (size_t)max_blocks * ORC_BLOCK);
     if (!s) return -1;
@@ -160,10 +166,9 @@ int orc_decode_attn(int num_blocks, int Hkv, int D, int is_bf16,
                 for (int t = 0; t < limit; ++t) {
                     const int blk = block_table[(size_t)b * max_blocks + t / ORC_BLOCK];
                     if (blk < 0 || blk >= num_blocks) { free(s); return -1; }
-                    const size_t koff = (((size_t)blk * Hkv + g) * ORC_BLOCK + t % ORC_BLOCK) * D;
                     double dot = 0.0;
                     for (int d = 0; d < D; ++d)
-                        dot += load_elem(q, qoff + d, is_bf16) * load_elem(k_pool, koff + d, is_bf16);
+                        dot += load_elem(q, qoff + d, q_is_bf16) * kv(ctx, 0, blk, g, t % ORC_BLOCK, d);
                     s[t] = scale * dot;
                     if (s[t] > m) m = s[t];
                 }
@@ -176,15 +181,147 @@ int orc_decode_attn(int num_blocks, int Hkv, int D, int is_bf16,
                 for (int d = 0; d < D; ++d) o[d] = 0.0;
                 for (int t = 0; t < limit; ++t) {
                     const int blk = block_table[(size_t)b * max_blocks + t / ORC_BLOCK];
-                    const size_t voff = (((size_t)blk * Hkv + g) * ORC_BLOCK + t % ORC_BLOCK) * D;
                     const double p = s[t] / denom;
-                    for (int d = 0; d < D; ++d) o[d] += p * load_elem(v_pool, voff + d, is_bf16);
+                    for (int d = 0; d < D; ++d) o[d] += p * kv(ctx, 1, blk, g, t % ORC_BLOCK, d);
                 }
             }
         }
     }
     free(s);
     return 0;
+}
+
+/* One decode step's attention [TTS, "Token generation under a frame budget"]:
+ * every query row of stream b attends over that stream's cached keys/values
+ * (gathered through the block table), softmax(scale * q.k) weighted sum of v.
+ * ctx_lens[b] counts tokens after the append.  Query row j of a q_len-row
+ * block sees tokens t < ctx_lens[b] - q_len + j + 1 when causal, all
+ * ctx_lens[b] tokens otherwise.  GQA: query head h reads KV head
+ * h / (Hq / Hkv).  Output out[B][q_len][Hq][D] in double.
+ * Returns 0, or -1 on an invalid block id or context length. */
+int orc_decode_attn(int num_blocks, int Hkv, int D, int is_bf16,
+                    const void *k_pool, const void *v_pool,
+                    const int32_t *block_table, int max_blocks, const int32_t *ctx_lens,
+                    int B, int q_len, int Hq, double scale, int causal,
+                    const void *q, double *out) {
+    const orc_plain_pool pool = {Hkv, D, is_bf16, k_pool, v_pool};
+    return attend(num_blocks, Hkv, D, plain_kv, &pool, block_table, max_blocks, ctx_lens, B, q_len, Hq,
+                  scale, causal, q, is_bf16, out);
+}
+
+/* ---------------------------------------------------------------- FP8 cache */
+
+/* FP8 E4M3 ("e4m3fn"): 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits,
+ * no infinities; exponent and mantissa all ones (0x7F / 0xFF) is NaN, so the
+ * largest finite magnitude is 1.75 * 2^8 = 448; exponent field 0 holds the
+ * subnormals m * 2^-9. */
+float orc_e4m3_decode(uint8_t c) {
+    const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double mag = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return (float)(sign ? -mag : mag);
+}
+
+/* Nearest E4M3 value to x, ties to the code with an even mantissa, magnitudes
+ * above 448 saturating to +-448 (the largest finite value); NaN -> 0x7F.
+ * Written as a search over the 127 non-negative finite codes. */
+uint8_t orc_e4m3_encode(float x) {
+    if (x != x) return 0x7F;
+    const double a = fabs((double)x);
+    int best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        const double err = fabs((double)orc_e4m3_decode((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)((x < 0.0f ? 0x80 : 0) | best);
+}
+
+void orc_e4m3_encode_n(const float *x, size_t n, uint8_t *out) {
+    for (size_t i = 0; i < n; ++i) out[i] = orc_e4m3_encode(x[i]);
+}
+
+void orc_e4m3_decode_n(const uint8_t *c, size_t n, float *out) {
+    for (size_t i = 0; i < n; ++i) out[i] = orc_e4m3_decode(c[i]);
+}
+
+/* Quantises one row of n values: scale = max|x| / 448 (fp32), codes =
+ * E4M3(x / scale) computed in fp32; an all-zero row gets scale 0 and codes 0. */
+static void quantize_row(const float *x, int n, uint8_t *codes, int code_stride, float *scale_out) {
+    float amax = 0.0f;
+    for (int d = 0; d < n; ++d) {
+        const float a = fabsf(x[d]);
+        if (a > amax) amax = a;
+    }
+    const float scale = amax / 448.0f;
+    for (int d = 0; d < n; ++d) codes[(size_t)d * code_stride] = scale > 0.0f ? orc_e4m3_encode(x[d] / scale) : 0;
+    *scale_out = scale;
+}
+
+/* KV append into an FP8 cache (the KV cache in FP8: "Optimizing Streaming
+ * Text-to-Speech Models for Sub-50 Millisecond Latency", section
+ * "Engine-Level Optimizations with TensorRT-LLM").  Each new key and value row
+ * (one token, one KV head: D bf16 values) is one quantisation block with its
+ * own fp32 scale.  Layouts: k_codes [num_blocks][Hkv][16][D] (token-major),
+ * v_codes [num_blocks][Hkv][D][16] (dimension-major), k_scale and v_scale
+ * [num_blocks][Hkv][16].  Returns 0, or -1 if a slot falls outside the table
+ * or the pool. */
+int orc_kv_append_fp8(int num_blocks, int Hkv, int D, uint8_t *k_codes, uint8_t *v_codes,
+                      float *k_scale, float *v_scale, const int32_t *block_table, int max_blocks,
+                      const int32_t *ctx_before, int B, int q_len, const uint16_t *k_new,
+                      const uint16_t *v_new) {
+    float *row = (float *)malloc(sizeof(float) * (size_t)D);
+    if (!row) return -1;
+    for (int b = 0; b < B; ++b) {
+        for (int j = 0; j < q_len; ++j) {
+            const int s = ctx_before[b] + j;
+            if (s < 0 || s / ORC_BLOCK >= max_blocks) { free(row); return -1; }
+            const int blk = block_table[(size_t)b * max_blocks + s / ORC_BLOCK];
+            if (blk < 0 || blk >= num_blocks) { free(row); return -1; }
+            const int slot = s % ORC_BLOCK;
+            for (int g = 0; g < Hkv; ++g) {
+                const size_t src = (((size_t)b * q_len + j) * Hkv + g) * D;
+                const size_t tile = (size_t)blk * Hkv + g;
+                for (int d = 0; d < D; ++d) row[d] = (float)load_elem(k_new, src + d, 1);
+                quantize_row(row, D, k_codes + (tile * ORC_BLOCK + slot) * D, 1, k_scale + tile * ORC_BLOCK + slot);
+                for (int d = 0; d < D; ++d) row[d] = (float)load_elem(v_new, src + d, 1);
+                quantize_row(row, D, v_codes + tile * ORC_BLOCK * D + slot, ORC_BLOCK,
+                             v_scale + tile * ORC_BLOCK + slot);
+            }
+        }
+    }
+    free(row);
+    return 0;
+}
+
+typedef struct {
+    int Hkv, D;
+    const uint8_t *k_codes, *v_codes;
+    const float *k_scale, *v_scale;
+} orc_fp8_pool;
+
+static double fp8_kv(const void *ctx, int is_v, int blk, int g, int slot, int d) {
+    const orc_fp8_pool *p = (const orc_fp8_pool *)ctx;
+    const size_t tile = (size_t)blk * p->Hkv + g;
+    if (is_v)
+        return (double)orc_e4m3_decode(p->v_codes[(tile * p->D + d) * ORC_BLOCK + slot]) *
+               (double)p->v_scale[tile * ORC_BLOCK + slot];
+    return (double)orc_e4m3_decode(p->k_codes[(tile * ORC_BLOCK + slot) * p->D + d]) *
+           (double)p->k_scale[tile * ORC_BLOCK + slot];
+}
+
+/* Attention over an FP8 cache: orc_decode_attn on the dequantised rows
+ * (code value times the row's scale); q is bf16. */
+int orc_decode_attn_fp8(int num_blocks, int Hkv, int D, const uint8_t *k_codes, const uint8_t *v_codes,
+                        const float *k_scale, const float *v_scale, const int32_t *block_table,
+                        int max_blocks, const int32_t *ctx_lens, int B, int q_len, int Hq, double scale,
+                        int causal, const uint16_t *q, double *out) {
+    const orc_fp8_pool pool = {Hkv, D, k_codes, v_codes, k_scale, v_scale};
+    return attend(num_blocks, Hkv, D, fp8_kv, &pool, block_table, max_blocks, ctx_lens, B, q_len, Hq,
+                  scale, causal, q, 1, out);
 }
 
 /* -------------------------------------------------------------------- head */

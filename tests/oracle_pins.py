@@ -415,4 +415,133 @@ def check_verify_bonus_token(o):
     assert (r["next_token"] == -1).all(), "no bonus token unless asked for"
 
 
+# ---------------------------------------------------------------- FP8 cache
+
+def _torch_e4m3_table():
+    import torch
+    return torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+
+
+def check_e4m3_decode_matches_torch(o):
+    """Every one of the 256 codes decodes to torch's float8_e4m3fn value (NaN at 0x7F, 0xFF)."""
+    ref = _torch_e4m3_table()
+    got = o.e4m3_decode(np.arange(256, dtype=np.uint8))
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(got[~np.isnan(got)], ref[~np.isnan(ref)])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6
+
+
+def check_e4m3_encode_matches_torch(o):
+    """Encoding agrees with torch's conversion over magnitudes from the
+    subnormals to 448; exact midpoints go to the even code; magnitudes above
+    448 saturate to +-448."""
+    import torch
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal(50000) * np.exp(rng.uniform(-13, 7, 50000))).astype(np.float32)
+    x = np.clip(x, -448, 448)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(o.e4m3_encode(x), ref)
+    tab = _torch_e4m3_table()[:0x7F].astype(np.float64)  # non-negative finite values, increasing
+    mid = ((tab[:-1] + tab[1:]) / 2).astype(np.float32)
+    assert np.array_equal(mid.astype(np.float64), (tab[:-1] + tab[1:]) / 2)  # midpoints exact in fp32
+    codes = o.e4m3_encode(mid)
+    lo = np.arange(0x7E, dtype=np.uint8)
+    expect = np.where(lo % 2 == 0, lo, lo + 1).astype(np.uint8)  # the neighbour with an even mantissa
+    assert np.array_equal(codes, expect)
+    assert np.array_equal(o.e4m3_encode(-mid), expect | 0x80)
+    big = np.array([448.0, 449.0, 463.9, 1e4, 3e38], dtype=np.float32)
+    assert np.array_equal(o.e4m3_encode(big), np.full(5, 0x7E, np.uint8))
+    assert np.array_equal(o.e4m3_encode(-big), np.full(5, 0xFE, np.uint8))
+
+
+def fp8_case(seed, B, Hkv, D, ctx_lens, permute=True):
+    """Random FP8 cache arrays for every slot (no NaN codes) and the table."""
+    rng = np.random.default_rng(seed)
+    L = np.asarray(ctx_lens, dtype=np.int32)
+    max_blocks = int(-(-L.max() // wl.BLOCK))
+    num_blocks, table = wl.layout_blocks(L, max_blocks, spare=2, permute=permute, rng=rng)
+    codes = np.concatenate([np.arange(0x7F), np.arange(0x80, 0xFF)]).astype(np.uint8)
+    kc = rng.choice(codes, size=(num_blocks, Hkv, wl.BLOCK, D))
+    vc = rng.choice(codes, size=(num_blocks, Hkv, D, wl.BLOCK))
+    ks = rng.uniform(1e-3, 2e-2, (num_blocks, Hkv, wl.BLOCK)).astype(np.float32)
+    vs = rng.uniform(1e-3, 2e-2, (num_blocks, Hkv, wl.BLOCK)).astype(np.float32)
+    return dict(k_codes=kc, v_codes=vc, k_scale=ks, v_scale=vs, block_table=table, ctx_lens=L, rng=rng)
+
+
+def check_kv_append_fp8_quantization(o):
+    """Each appended row: scale = max|x| / 448 in fp32, codes = torch's E4M3 of
+    x / scale, K token-major and V dimension-major at the row's slot; the
+    largest entry maps to +-448; the rest of the cache is untouched."""
+    import torch
+    B, Hkv, D, q_len = 3, 2, 16, 2
+    c = fp8_case(21, B, Hkv, D, [5, 17, 32])
+    before = (c["ctx_lens"] - q_len).astype(np.int32)
+    rng = c["rng"]
+    k_new = wl.f32_to_bf16(rng.standard_normal((B, q_len, Hkv, D), dtype=np.float32))
+    v_new = wl.f32_to_bf16(3 * rng.standard_normal((B, q_len, Hkv, D), dtype=np.float32))
+    v_new[0, 0, 0] = 0  # an all-zero row: scale 0, codes 0
+    kc, vc, ks, vs = o.kv_append_fp8(c["k_codes"], c["v_codes"], c["k_scale"], c["v_scale"],
+                                     c["block_table"], before, k_new, v_new)
+    touched = np.zeros(c["k_scale"].shape, dtype=bool)
+    for b in range(B):
+        for j in range(q_len):
+            s = before[b] + j
+            blk, slot = c["block_table"][b, s // wl.BLOCK], s % wl.BLOCK
+            for g in range(Hkv):
+                touched[blk, g, slot] = True
+                for x_bits, codes, scale in ((k_new[b, j, g], kc[blk, g, slot, :], ks[blk, g, slot]),
+                                             (v_new[b, j, g], vc[blk, g, :, slot], vs[blk, g, slot])):
+                    x = wl.bf16_to_f32(x_bits)
+                    amax = np.float32(np.abs(x).max())
+                    assert scale == np.float32(amax / np.float32(448.0))
+                    if amax == 0:
+                        assert not codes.any()
+                        continue
+                    ref = torch.from_numpy((x / scale).astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8)
+                    assert np.array_equal(codes, ref.numpy())
+                    assert (codes[np.argmax(np.abs(x))] & 0x7F) == 0x7E
+                    deq = o.e4m3_decode(codes).astype(np.float64) * scale
+                    normal = np.abs(x) >= scale * 2.0 ** -6
+                    assert np.all(np.abs(deq - x)[normal] <= 2.0 ** -4 * np.abs(x)[normal])
+                    assert np.all(np.abs(deq - x)[~normal] <= 2.0 ** -10 * scale)
+    assert np.array_equal(ks[~touched], c["k_scale"][~touched])
+    assert np.array_equal(vs[~touched], c["v_scale"][~touched])
+    kt = np.broadcast_to(touched[..., None], kc.shape)
+    assert np.array_equal(kc[~kt], c["k_codes"][~kt])
+    vt = np.broadcast_to(touched[:, :, None, :], vc.shape)
+    assert np.array_equal(vc[~vt], c["v_codes"][~vt])
+
+
+def check_attn_fp8_matches_sdpa(o):
+    """Attention over an FP8 cache equals torch's scaled_dot_product_attention
+    (float64) on the cache dequantised with torch's E4M3 table."""
+    import torch
+    import torch.nn.functional as F
+    tab = torch.from_numpy(_torch_e4m3_table().astype(np.float64))
+    for (Hq, Hkv, D, q_len, causal, L, seed) in [(4, 2, 32, 1, False, [17, 1, 40], 31),
+                                                  (8, 2, 16, 5, True, [5, 33, 20], 32)]:
+        c = fp8_case(seed, len(L), Hkv, D, L)
+        q = wl.f32_to_bf16(c["rng"].standard_normal((len(L), q_len, Hq, D), dtype=np.float32))
+        scale = 1.0 / math.sqrt(D)
+        out = o.decode_attn_fp8(c["k_codes"], c["v_codes"], c["k_scale"], c["v_scale"], c["block_table"],
+                                c["ctx_lens"], q, scale, causal)
+        g = Hq // Hkv
+        for b, Lb in enumerate(L):
+            t = np.arange(Lb)
+            blocks, slots = c["block_table"][b, t // wl.BLOCK], t % wl.BLOCK
+            kcod = torch.from_numpy(c["k_codes"][blocks, :, slots, :].astype(np.int64))          # [L][Hkv][D]
+            vcod = torch.from_numpy(c["v_codes"][blocks, :, :, slots].astype(np.int64))          # [L][Hkv][D]
+            k = tab[kcod] * torch.from_numpy(c["k_scale"][blocks, :, slots].astype(np.float64))[..., None]
+            v = tab[vcod] * torch.from_numpy(c["v_scale"][blocks, :, slots].astype(np.float64))[..., None]
+            k = k.permute(1, 0, 2).repeat_interleave(g, dim=0)
+            v = v.permute(1, 0, 2).repeat_interleave(g, dim=0)
+            qq = torch.from_numpy(wl.bf16_to_f32(q[b]).astype(np.float64)).permute(1, 0, 2)
+            mask = None
+            if causal:
+                mask = torch.arange(Lb)[None, :] < (Lb - q_len + torch.arange(q_len)[:, None] + 1)
+            ref = F.scaled_dot_product_attention(qq, k, v, attn_mask=mask, scale=scale)
+            err = (torch.from_numpy(out[b]).permute(1, 0, 2) - ref).abs().max().item()
+            assert err < 1e-10, f"fp8 attention vs SDPA: {err}"
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

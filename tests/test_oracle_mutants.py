@@ -32,15 +32,16 @@ MUTANTS = [
      "const uint64_t ctr[4] = {idx / 4u, tag, pos, 0};"),
     ("gumbel: sign", "return -logf(-logf(u));", "return logf(-logf(u));"),
     ("append: slot offset", "+ s % ORC_BLOCK) * row;", "+ (s + 1) % ORC_BLOCK) * row;"),
-    ("append: logical block", "block_table[(size_t)b * max_blocks + s / ORC_BLOCK];",
-     "block_table[(size_t)b * max_blocks + (s + 1) / ORC_BLOCK];"),
+    ("append: logical block", "s / ORC_BLOCK];\n            if (blk < 0 || blk >= num_blocks) return -1;",
+     "(s + 1) / ORC_BLOCK];\n            if (blk < 0 || blk >= num_blocks) return -1;"),
+    ("fp8 append: logical block", "s / ORC_BLOCK];\n            if (blk < 0 || blk >= num_blocks) { free(row)",
+     "(s + 1) / ORC_BLOCK];\n            if (blk < 0 || blk >= num_blocks) { free(row)"),
     ("attn: scale dropped", "s[t] = scale * dot;", "s[t] = dot;"),
     ("attn: GQA head mapping", "const int g = h / group;", "const int g = h % Hkv;"),
     ("attn: causal limit off by one", "causal ? L - q_len + j + 1 : L", "causal ? L - q_len + j + 2 : L"),
     ("attn: causal limit short", "causal ? L - q_len + j + 1 : L", "causal ? L - q_len + j : L + 0"),
-    ("attn: key slot", "+ t % ORC_BLOCK) * D;\n                    double dot",
-     "+ (t + 1) % ORC_BLOCK) * D;\n                    double dot"),
-    ("attn: values from the key pool", "o[d] += p * load_elem(v_pool,", "o[d] += p * load_elem(k_pool,"),
+    ("attn: key slot", "kv(ctx, 0, blk, g, t % ORC_BLOCK, d)", "kv(ctx, 0, blk, g, (t + 1) % ORC_BLOCK, d)"),
+    ("attn: values from the key pool", "o[d] += p * kv(ctx, 1,", "o[d] += p * kv(ctx, 0,"),
     ("attn: unnormalised weights", "const double p = s[t] / denom;", "const double p = s[t];"),
     ("head: W transposed", "load_elem(W, (size_t)v * H + k, is_bf16)", "load_elem(W, (size_t)k * V + v, is_bf16)"),
     ("head: highest index wins ties", "if (arg < 0 || key > top) {", "if (arg < 0 || key >= top) {"),
@@ -54,6 +55,14 @@ MUTANTS = [
     ("verify: residual ignores the draft", "fmaxf(pt[v] - dp[v], 0.0f)", "pt[v]"),
     ("verify: does not stop at the first rejection", "rejected = 1;\n            break;", "rejected = 1;"),
     ("verify: temperature dropped", "row_probs(tl, V, T, pt);", "row_probs(tl, V, 1.0f, pt);"),
+    ("e4m3: ties to the later code", "(err == best_err && (c & 1) == 0)", "(err == best_err)"),
+    ("e4m3: largest finite code excluded", "for (int c = 0; c <= 0x7E; ++c)", "for (int c = 0; c < 0x7E; ++c)"),
+    ("e4m3: subnormal exponent", "ldexp((double)m, -9)", "ldexp((double)m, -10)"),
+    ("fp8 append: scale for a maximum of 240", "amax / 448.0f", "amax / 240.0f"),
+    ("fp8 append: values stored token-major", "v_codes + tile * ORC_BLOCK * D + slot, ORC_BLOCK,",
+     "v_codes + (tile * ORC_BLOCK + slot) * D, 1,"),
+    ("fp8 attn: values scaled by the key scale", "(double)p->v_scale[tile * ORC_BLOCK + slot];",
+     "(double)p->k_scale[tile * ORC_BLOCK + slot];"),
     ("verify: bonus always drawn", "if (!rejected && (flags & 1)) {", "if (!rejected) {"),
     ("verify: bonus from the last draft row",
      "target_logits + ((size_t)b * (K + 1) + K) * V;", "target_logits + ((size_t)b * (K + 1) + K - 1) * V;"),
