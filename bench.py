@@ -53,9 +53,10 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle baseline in the native line")
     ap.add_argument("--e2e-steps", type=int, default=1000)
-    ap.add_argument("--sweep", default="2,4,5",
+    ap.add_argument("--sweep", default="2,4,5,3f",
                     help="other workloads whose kernels are timed one by one into the line's "
-                         "'workloads' object (comma-separated ids; empty: none)")
+                         "'workloads' object (comma-separated ids, 'f' suffix: FP8 E4M3 KV cache; "
+                         "empty: none)")
     ap.add_argument("--sweep-reps", type=int, default=30)
     return ap.parse_args(argv)
 
@@ -122,6 +123,18 @@ def attn_bytes(inp) -> int:
     L = inp["ctx_lens"].astype(np.int64)
     kv = int(L.sum()) * w.Hkv * w.D * w.elem_bytes * 2
     qo = 2 * w.B * w.q_len * w.Hq * w.D * w.elem_bytes
+    table = int((-(-L // wl.BLOCK)).sum()) * 4
+    return kv + qo + table + 4 * w.B
+
+
+def attn_bytes_fp8(inp) -> int:
+    """Algorithmic bytes of one attention launch over an FP8 cache: every
+    cached key and value row once as codes plus its fp32 scale, q and out
+    (bf16), the used block-table entries and the context lengths."""
+    w = inp["workload"]
+    L = inp["ctx_lens"].astype(np.int64)
+    kv = int(L.sum()) * w.Hkv * (w.D + 4) * 2
+    qo = 2 * w.B * w.q_len * w.Hq * w.D * 2
     table = int((-(-L // wl.BLOCK)).sum()) * 4
     return kv + qo + table + 4 * w.B
 
@@ -310,18 +323,39 @@ def kernel_sweep(ids, reps, flush_l2, peaks, device) -> dict:
     hbm = peaks["hbm_gbs"]
     out = {}
     for wid in ids:
-        w = wl.WORKLOADS[wid]
+        fp8 = str(wid).endswith("f")
+        w = wl.WORKLOADS[int(str(wid).rstrip("f"))]
         inp = wl.make_inputs(w)
         d = {k: dev(inp[k]) for k in ("block_table", "ctx_before", "ctx_lens", "q", "k_new", "v_new", "h", "W",
                                        "seed", "step")}
-        cache = bd.KVCache(dev(inp["k_pool"]), dev(inp["v_pool"]))
+        if fp8:
+            # the context quantised by the library's own append, one stream at a time
+            kp, vp = dev(inp["k_pool"]), dev(inp["v_pool"])
+            nb = kp.shape[0]
+            cache = bd.KVCache(torch.zeros((nb, w.Hkv, 16, w.D), dtype=torch.uint8, device=device),
+                               torch.zeros((nb, w.Hkv, w.D, 16), dtype=torch.uint8, device=device),
+                               torch.zeros((nb, w.Hkv, 16), dtype=torch.float32, device=device),
+                               torch.zeros((nb, w.Hkv, 16), dtype=torch.float32, device=device))
+            zero = torch.zeros(1, dtype=torch.int32, device=device)
+            for b in range(w.B):
+                n = int(inp["ctx_before"][b])
+                if n == 0:
+                    continue
+                t = torch.arange(n, device=device)
+                blocks = d["block_table"][b, t // wl.BLOCK].long()
+                rows_k = kp[blocks, :, t % wl.BLOCK, :].unsqueeze(0).contiguous()
+                rows_v = vp[blocks, :, t % wl.BLOCK, :].unsqueeze(0).contiguous()
+                bd.tts_kv_append(cache, d["block_table"][b:b + 1].contiguous(), zero, rows_k, rows_v)
+            del kp, vp
+        else:
+            cache = bd.KVCache(dev(inp["k_pool"]), dev(inp["v_pool"]))
         bd.tts_kv_append(cache, d["block_table"], d["ctx_before"], d["k_new"], d["v_new"])
         attn_out = torch.empty_like(d["q"])
         ws = torch.zeros(bd.tts_decode_attn_workspace_size(w.B, w.q_len, w.Hq, w.Hkv, w.D, w.ctx_hi),
                          dtype=torch.uint8, device=device)
         t_att = timed(lambda: bd.tts_decode_attn(cache, d["block_table"], d["ctx_lens"], w.ctx_hi, d["q"],
                                                  attn_out, ws, inp["scale"], w.causal))
-        ab = attn_bytes(inp)
+        ab = attn_bytes_fp8(inp) if fp8 else attn_bytes(inp)
         ids_t = torch.empty(w.R, dtype=torch.int32, device=device)
         hws = torch.zeros(bd.tts_head_workspace_size(w.R, w.V), dtype=torch.uint8, device=device)
         logits = torch.empty(w.R, w.V, dtype=torch.float32, device=device) if w.logits_out else None
@@ -337,8 +371,15 @@ def kernel_sweep(ids, reps, flush_l2, peaks, device) -> dict:
             "head_select_us": t_head, "head_gbs": hb / t_head / 1e3, "head_frac_hbm": hb / t_head / 1e3 / hbm,
             "head_tflops": flops / t_head / 1e6,
             "head_frac_tensor": flops / t_head / 1e6 / peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]),
-            "head_bytes": hb, "head_mode": w.mode,
+            "head_bytes": hb, "head_mode": w.mode, "kv_cache": "fp8_e4m3" if fp8 else w.dtype,
         }
+        if fp8:
+            from decode_step_gb300.step import DecodeStep
+            stp = DecodeStep(cache, d["W"], w.Hq, w.B, w.ctx_hi, q_len=w.q_len, causal=w.causal,
+                             mode=bd.TTS_GUMBEL if w.mode == "gumbel" else bd.TTS_ARGMAX, temperature=w.T)
+            t_step = timed(lambda: stp(d["block_table"], d["ctx_before"], d["ctx_lens"], d["q"], d["k_new"],
+                                       d["v_new"], seed=d["seed"], step=d["step"]))
+            entry.update({"step_us": t_step, "tokens_per_s": w.B * w.q_len / (t_step * 1e-6)})
         if w.K > 0:
             tl, dp = dev(inp["target_logits"]), dev(inp["draft_probs"])
             dt, vs, vt = dev(inp["draft_tokens"]), dev(inp["vseed"]), dev(inp["vstep"])
@@ -348,7 +389,7 @@ def kernel_sweep(ids, reps, flush_l2, peaks, device) -> dict:
             vb = verify_bytes(w)
             entry.update({"spec_verify_us": t_ver, "spec_verify_gbs": vb / t_ver / 1e3,
                           "spec_verify_frac": vb / t_ver / 1e3 / hbm, "spec_verify_bytes": vb})
-        out[w.name] = entry
+        out[w.name + ("-fp8" if fp8 else "")] = entry
         del cache, d, attn_out, ws
         torch.cuda.empty_cache()
     return out
@@ -553,7 +594,7 @@ def run_native(args):
     }
     if world == 1:
         line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
-        ids = [int(x) for x in args.sweep.split(",") if x.strip()]
+        ids = [x.strip() for x in args.sweep.split(",") if x.strip()]
         if ids:
             del step, graphed, cache, W, d
             torch.cuda.empty_cache()

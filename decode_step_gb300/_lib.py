@@ -12,7 +12,7 @@ from pathlib import Path
 from . import build as _build
 
 TTS_OK = 0
-TTS_F32, TTS_BF16 = 0, 1
+TTS_F32, TTS_BF16, TTS_FP8_E4M3 = 0, 1, 2
 TTS_ARGMAX, TTS_GUMBEL = 0, 1
 TTS_VERIFY_BONUS = 1
 ERRBIT_BLOCK_ID, ERRBIT_CTX_LEN, ERRBIT_TOKEN, ERRBIT_TIMEOUT = 1, 2, 4, 8
@@ -27,7 +27,8 @@ _f32 = ctypes.c_float
 
 class KVCacheDesc(ctypes.Structure):
     _fields_ = [("num_blocks", _i32), ("block_size", _i32), ("num_kv_heads", _i32),
-                ("head_dim", _i32), ("dtype", _i32), ("k_pool", _vp), ("v_pool", _vp)]
+                ("head_dim", _i32), ("dtype", _i32), ("k_pool", _vp), ("v_pool", _vp),
+                ("k_scale", _vp), ("v_scale", _vp)]
 
 
 class StepGraphDesc(ctypes.Structure):

@@ -74,6 +74,8 @@ struct AttnArgs {
     int workers;
     int nr_slot;        // query rows per partial slot (group * q_len padded)
     int stages;         // ring depth per warp (tensor-core kernel)
+    const float *k_scale;  // FP8 cache: row scales [num_blocks][Hkv][16]
+    const float *v_scale;
     int32_t *err;
 };
 
@@ -580,6 +582,18 @@ constexpr int kTcCtasPerSm = 3;
 // of a new segment (row-major bf16, n_rows x 256 B).
 constexpr int kBoxBytes = 2048;
 constexpr int kKVStageBytes = 4 * kBoxBytes;
+// FP8 cache: K codes (16 rows x 128 B, one 128-byte-swizzled box), V codes
+// (128 dimension rows x 16 B, as stored), the 16 key scales and 16 value
+// scales, then the query rows.
+constexpr int kFp8VOff = 2048;
+constexpr int kFp8ScaleOff = 4096;
+constexpr int kFp8KVStageBytes = kFp8ScaleOff + 2 * 64;
+// The codes enter the MMAs as bf16 values times 2^-120 (see e4m3x4_to_bf16);
+// queries are scaled by 2^16 (exact) to keep the products clear of fp32
+// denormals; S is rescaled by 2^104 and P by 2^120 with the row scales.
+constexpr float kFp8QBoost = 65536.0f;
+constexpr float kFp8SFix = 0x1p104f;
+constexpr float kFp8PFix = 0x1p120f;
 
 // Address of 16-byte chunk `ch` (0..15) of token row `t` (0..15) in a K or V
 // tile stored as two swizzled boxes.
@@ -594,10 +608,10 @@ struct TcSmem {
     int prefix;       // int prefix[B + 1], ctxs[B], scan[kTcWarps]
     int total;        // bytes to request (includes 1 KB of alignment slack)
 };
-__host__ __device__ inline TcSmem tc_smem(int n_rows, int B, int stages) {
+__host__ __device__ inline TcSmem tc_smem(int n_rows, int B, int stages, bool fp8) {
     TcSmem s;
-    const int qbytes = ((n_rows * kRowBytes + 1023) / 1024) * 1024;
-    s.stage_bytes = kKVStageBytes + qbytes;
+    const int kv = fp8 ? kFp8KVStageBytes : kKVStageBytes;
+    s.stage_bytes = ((kv + n_rows * kRowBytes + 1023) / 1024) * 1024;
     s.stages = 0;
     s.bars = s.stages + kTcWarps * stages * s.stage_bytes;
     s.prefix = s.bars + 8 * kTcWarps * stages;
@@ -607,13 +621,30 @@ __host__ __device__ inline TcSmem tc_smem(int n_rows, int B, int stages) {
 
 // Deepest ring (<= kTcMaxStages) that fits kTcCtasPerSm CTAs per SM; 0 if
 // not even one stage fits.
-__host__ inline int tc_stages(int n_rows, int B) {
+__host__ inline int tc_stages(int n_rows, int B, bool fp8) {
     const int budget = 227 * 1024 / kTcCtasPerSm - 1024;
     for (int st = kTcMaxStages; st >= 1; --st)
-        if (tc_smem(n_rows, B, st).total <= budget) return st;
+        if (tc_smem(n_rows, B, st, fp8).total <= budget) return st;
     return 0;
 }
 
+// Four E4M3 codes (bytes of w, low first) as two bf16 pairs (codes 0, 1 and
+// 2, 3, low half first), each value times 2^-120: the sign goes to bit 15 and
+// the exponent and mantissa bits to bits 4-10, so a normal code's exponent
+// field (bias 7) becomes the bf16 exponent field (bias 127) and a subnormal
+// code a bf16 subnormal of the same scaled value.  Exact for every code.
+__device__ __forceinline__ void e4m3x4_to_bf16(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t a = __byte_perm(w, 0u, 0x1404);  // [0, c0, 0, c1]
+    const uint32_t b = __byte_perm(w, 0u, 0x3424);  // [0, c2, 0, c3]
+    lo = (a & 0x80008000u) | ((a & 0x7F007F00u) >> 4);
+    hi = (b & 0x80008000u) | ((b & 0x7F007F00u) >> 4);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_scaled(uint32_t w, float f) {
+    return pack_bf16x2(bf16_lo(w) * f, bf16_hi(w) * f);
+}
+
+template <bool kFp8>
 __global__ void __launch_bounds__(kTcWarps * 32, kTcCtasPerSm)
 decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                       const AttnArgs a) {
@@ -625,7 +656,9 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
     uint8_t *smem = smem_raw + (base - raw);
     const int n_rows = a.group * a.q_len;  // <= 16
     const int n_stages = a.stages;
-    const TcSmem S = tc_smem(n_rows, a.B, n_stages);
+    const TcSmem S = tc_smem(n_rows, a.B, n_stages, kFp8);
+    constexpr int kQOff = kFp8 ? kFp8KVStageBytes : kKVStageBytes;  // query rows within a stage
+    constexpr int kStageKV = kFp8 ? kFp8KVStageBytes : kKVStageBytes;
     int *prefix = reinterpret_cast<int *>(smem + S.prefix);
     int *ctxs = prefix + a.B + 1;
     int *scan = ctxs + a.B;
@@ -679,25 +712,33 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
             const uint32_t bar = bar0 + 8 * st;
             const uint32_t dst = stage0 + st * S.stage_bytes;
             const bool need_q = j == 0 || blk == 0;
-            const uint32_t bytes = (id >= 0 ? kKVStageBytes : 0) + (need_q ? a.q_len * qbytes_per_pos : 0);
+            const uint32_t bytes = (id >= 0 ? kStageKV : 0) + (need_q ? a.q_len * qbytes_per_pos : 0);
             if (bytes == 0) {
                 mbar_arrive(bar);
             } else {
                 mbar_arrive_expect_tx(bar, bytes);
                 if (id >= 0) {
-                    const int row = (id * a.Hkv + seg % a.Hkv) * TTS_BLOCK_TOKENS;
-                    tma_load_2d(dst, &kmap, 0, row, bar, policy);
-                    tma_load_2d(dst + kBoxBytes, &kmap, 64, row, bar, policy);
-                    tma_load_2d(dst + 2 * kBoxBytes, &vmap, 0, row, bar, policy);
-                    tma_load_2d(dst + 3 * kBoxBytes, &vmap, 64, row, bar, policy);
+                    const int tile = id * a.Hkv + seg % a.Hkv;
+                    const int row = tile * TTS_BLOCK_TOKENS;
+                    if constexpr (kFp8) {
+                        tma_load_2d(dst, &kmap, 0, row, bar, policy);
+                        bulk_load(dst + kFp8VOff, a.v_pool + static_cast<size_t>(tile) * 2048, 2048, bar, policy);
+                        bulk_load(dst + kFp8ScaleOff, a.k_scale + static_cast<size_t>(tile) * 16, 64, bar, policy);
+                        bulk_load(dst + kFp8ScaleOff + 64, a.v_scale + static_cast<size_t>(tile) * 16, 64, bar,
+                                  policy);
+                    } else {
+                        tma_load_2d(dst, &kmap, 0, row, bar, policy);
+                        tma_load_2d(dst + kBoxBytes, &kmap, 64, row, bar, policy);
+                        tma_load_2d(dst + 2 * kBoxBytes, &vmap, 0, row, bar, policy);
+                        tma_load_2d(dst + 3 * kBoxBytes, &vmap, 64, row, bar, policy);
+                    }
                 }
                 if (need_q) {
                     const int b = seg / a.Hkv, g = seg % a.Hkv;
                     for (int jq = 0; jq < a.q_len; ++jq) {
                         const size_t qoff =
                             ((static_cast<size_t>(b) * a.q_len + jq) * a.Hq + g * a.group) * kRowBytes;
-                        bulk_load_nohint(dst + kKVStageBytes + jq * qbytes_per_pos, a.q + qoff,
-                                         qbytes_per_pos, bar);
+                        bulk_load_nohint(dst + kQOff + jq * qbytes_per_pos, a.q + qoff, qbytes_per_pos, bar);
                     }
                 }
             }
@@ -779,8 +820,8 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
         const int t_id = __shfl_sync(kFull, cur_id, src);
         const int t_seg = __shfl_sync(kFull, cur_seg, src);
         const int t_blk = __shfl_sync(kFull, cur_blk, src);
-        const uint32_t kt = stage0 + st * S.stage_bytes;  // K boxes
-        const uint32_t vt = kt + 2 * kBoxBytes;            // V boxes
+        const uint32_t kt = stage0 + st * S.stage_bytes;                  // K boxes / codes
+        const uint32_t vt = kt + (kFp8 ? kFp8VOff : 2 * kBoxBytes);        // V boxes / codes
         if (i == 0 || t_blk == 0) {
             // ---- a new segment: finish the previous one, set up this one
             if (i > 0) flush();
@@ -796,14 +837,24 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
             limB = rB < n_rows ? (a.causal ? seg_L - a.q_len + rB / a.group + 1 : seg_L) : 0;
             mA = mB = kNegBig;
             lA = lB = 0.0f;
-            const uint32_t qs = kt + kKVStageBytes;
+            const uint32_t qs = kt + kQOff;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-                const int c0 = (16 * ks + 2 * ft) * 2;  // byte offset of dims 2t, 2t+1 in the row
-                qa[ks][0] = (rA < n_rows && !timed_out) ? *reinterpret_cast<const uint32_t *>(smem + (qs - base) + rA * kRowBytes + c0) : 0u;
-                qa[ks][1] = (rB < n_rows && !timed_out) ? *reinterpret_cast<const uint32_t *>(smem + (qs - base) + rB * kRowBytes + c0) : 0u;
-                qa[ks][2] = (rA < n_rows && !timed_out) ? *reinterpret_cast<const uint32_t *>(smem + (qs - base) + rA * kRowBytes + c0 + 16) : 0u;
-                qa[ks][3] = (rB < n_rows && !timed_out) ? *reinterpret_cast<const uint32_t *>(smem + (qs - base) + rB * kRowBytes + c0 + 16) : 0u;
+                // bf16: dims (2t, 2t+1) and (2t+8, 2t+9) of the k-step; FP8: the
+                // k-step's dims permuted to (4t, 4t+1) and (4t+2, 4t+3), the
+                // order in which a 16-bit ldmatrix row read hands out the codes
+                const int c0 = kFp8 ? (16 * ks + 4 * ft) * 2 : (16 * ks + 2 * ft) * 2;
+                const int c1 = kFp8 ? c0 + 4 : c0 + 16;
+                const uint8_t *qrA = smem + (qs - base) + rA * kRowBytes;
+                const uint8_t *qrB = smem + (qs - base) + rB * kRowBytes;
+                qa[ks][0] = (rA < n_rows && !timed_out) ? *reinterpret_cast<const uint32_t *>(qrA + c0) : 0u;
+                qa[ks][1] = (rB < n_rows && !timed_out) ? *reinterpret_cast<const uint32_t *>(qrB + c0) : 0u;
+                qa[ks][2] = (rA < n_rows && !timed_out) ? *reinterpret_cast<const uint32_t *>(qrA + c1) : 0u;
+                qa[ks][3] = (rB < n_rows && !timed_out) ? *reinterpret_cast<const uint32_t *>(qrB + c1) : 0u;
+                if constexpr (kFp8) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) qa[ks][e] = bf16x2_scaled(qa[ks][e], kFp8QBoost);
+                }
             }
 #pragma unroll
             for (int nt = 0; nt < 16; ++nt)
@@ -814,6 +865,34 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
             const int base_tok = t_blk * TTS_BLOCK_TOKENS;
             // ---- S = Q K^T: 2 n-tiles of 8 tokens x 8 k-steps of 16 dims
             float s[2][4];
+            // FP8: this lane's key and value scales (tokens 2t, 2t+1 | 2t+8, 2t+9)
+            float2 ksc[2], vsc[2];
+            if constexpr (kFp8) {
+                const float *sc = reinterpret_cast<const float *>(smem + (kt - base) + kFp8ScaleOff);
+                ksc[0] = *reinterpret_cast<const float2 *>(sc + 2 * ft);
+                ksc[1] = *reinterpret_cast<const float2 *>(sc + 8 + 2 * ft);
+                vsc[0] = *reinterpret_cast<const float2 *>(sc + 16 + 2 * ft);
+                vsc[1] = *reinterpret_cast<const float2 *>(sc + 24 + 2 * ft);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) s[nt][e] = 0.0f;
+#pragma unroll
+                    for (int kq = 0; kq < 2; ++kq) {
+                        // matrix i = k-step 4 kq + i (16 dims) of tokens 8 nt .. 8 nt + 7
+                        const int tok = 8 * nt + (lane & 7);
+                        const int ch = 4 * kq + (lane >> 3);
+                        uint32_t w[4];
+                        ldsm_x4(kt + tok * 128 + ((ch ^ (tok & 7)) << 4), w[0], w[1], w[2], w[3]);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            uint32_t b0, b1;
+                            e4m3x4_to_bf16(w[i], b0, b1);
+                            mma_bf16_16816(s[nt], qa[4 * kq + i], b0, b1);
+                        }
+                    }
+                }
+            } else {
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
@@ -828,6 +907,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
                     mma_bf16_16816(s[nt], qa[2 * kp + 1], b2, b3);
                 }
             }
+            }
             // ---- online softmax in the log2 domain; rows fg (A) and fg + 8 (B)
             float xa[4], xb[4];
 #pragma unroll
@@ -835,8 +915,10 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int tok = base_tok + 8 * nt + 2 * ft + e;
-                    xa[2 * nt + e] = tok < limA ? s[nt][e] * a.qscale : -INFINITY;
-                    xb[2 * nt + e] = tok < limB ? s[nt][2 + e] * a.qscale : -INFINITY;
+                    float f = a.qscale;
+                    if constexpr (kFp8) f *= (e == 0 ? ksc[nt].x : ksc[nt].y) * kFp8SFix;
+                    xa[2 * nt + e] = tok < limA ? s[nt][e] * f : -INFINITY;
+                    xb[2 * nt + e] = tok < limB ? s[nt][2 + e] * f : -INFINITY;
                 }
             }
             float ma = fmaxf(fmaxf(xa[0], xa[1]), fmaxf(xa[2], xa[3]));
@@ -866,12 +948,30 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
             }
             // P as the A operand (rows fg / fg + 8, tokens 2t, 2t+1, 2t+8, 2t+9)
             uint32_t pf[4];
-            pf[0] = pack_bf16x2(pa[0], pa[1]);
-            pf[1] = pack_bf16x2(pb[0], pb[1]);
-            pf[2] = pack_bf16x2(pa[2], pa[3]);
-            pf[3] = pack_bf16x2(pb[2], pb[3]);
-            // Tokens past the context may hold anything (even NaN): zero their V rows.
-            if (base_tok + TTS_BLOCK_TOKENS > seg_L) {
+            if constexpr (kFp8) {
+                // times each token's value scale and 2^120; slots past the
+                // context may hold any scale (even NaN), so they give 0
+                float qa_[4], qb_[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int tok = base_tok + 8 * (e >> 1) + 2 * ft + (e & 1);
+                    const float vs = ((e & 1) ? vsc[e >> 1].y : vsc[e >> 1].x) * kFp8PFix;
+                    qa_[e] = tok < limA ? pa[e] * vs : 0.0f;
+                    qb_[e] = tok < limB ? pb[e] * vs : 0.0f;
+                }
+                pf[0] = pack_bf16x2(qa_[0], qa_[1]);
+                pf[1] = pack_bf16x2(qb_[0], qb_[1]);
+                pf[2] = pack_bf16x2(qa_[2], qa_[3]);
+                pf[3] = pack_bf16x2(qb_[2], qb_[3]);
+            } else {
+                pf[0] = pack_bf16x2(pa[0], pa[1]);
+                pf[1] = pack_bf16x2(pb[0], pb[1]);
+                pf[2] = pack_bf16x2(pa[2], pa[3]);
+                pf[3] = pack_bf16x2(pb[2], pb[3]);
+            }
+            // Tokens past the context may hold anything (even NaN): zero their
+            // V rows (bf16; FP8 codes widen to finite values and meet P = 0).
+            if (!kFp8 && base_tok + TTS_BLOCK_TOKENS > seg_L) {
                 const int first_bad = max(seg_L - base_tok, 0);
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
                 for (int idx = lane; idx < (TTS_BLOCK_TOKENS - first_bad) * 16; idx += 32) {
@@ -882,14 +982,30 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
                 __syncwarp();
             }
             // ---- O += P V: 8 pairs of n-tiles (16 dims each), k = 16 tokens
+            if constexpr (kFp8) {
 #pragma unroll
-            for (int np = 0; np < 8; ++np) {
-                const int tok = mr + 8 * (mi & 1);
-                const int ch = 2 * np + (mi >> 1);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(swz(vt, tok, ch), b0, b1, b2, b3);
-                mma_bf16_16816(o[2 * np], pf, b0, b1);
-                mma_bf16_16816(o[2 * np + 1], pf, b2, b3);
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    // matrix i = dims 8 (4 q4 + i) .. + 7, each row the 16 codes of one
+                    // dimension in the slot order that gives lane t slots 2t, 2t+1, 2t+8, 2t+9
+                    uint32_t w[4];
+                    ldsm_x4(vt + (8 * (4 * q4 + (lane >> 3)) + (lane & 7)) * 16, w[0], w[1], w[2], w[3]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t b0, b1;
+                        e4m3x4_to_bf16(w[i], b0, b1);
+                        mma_bf16_16816(o[4 * q4 + i], pf, b0, b1);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int np = 0; np < 8; ++np) {
+                    const int tok = mr + 8 * (mi & 1);
+                    const int ch = 2 * np + (mi >> 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(swz(vt, tok, ch), b0, b1, b2, b3);
+                    mma_bf16_16816(o[2 * np], pf, b0, b1);
+                    mma_bf16_16816(o[2 * np + 1], pf, b2, b3);
+                }
             }
         }
         __syncwarp();
@@ -914,7 +1030,7 @@ int padded_rows(int rows) {
 }
 
 int ctas_per_sm(int dtype, int nr) {
-    if (dtype == TTS_BF16) return kTcCtasPerSm;
+    if (dtype == TTS_BF16 || dtype == TTS_FP8_E4M3) return kTcCtasPerSm;
     return nr <= 4 ? 3 : 1;
 }
 
@@ -961,9 +1077,11 @@ int launch_simt(const AttnArgs &a, int nr, int ctas, LaunchOpts o) {
     }
 }
 
+template <bool kFp8>
 int launch_tc(const AttnArgs &a, const CUtensorMap &kmap, const CUtensorMap &vmap, int ctas, LaunchOpts o) {
-    const size_t smem = tc_smem(a.group * a.q_len, a.B, a.stages).total;
-    if (!ensure_dynamic_smem(reinterpret_cast<const void *>(decode_attn_tc_kernel), static_cast<int>(smem)))
+    const size_t smem = tc_smem(a.group * a.q_len, a.B, a.stages, kFp8).total;
+    auto kern = decode_attn_tc_kernel<kFp8>;
+    if (!ensure_dynamic_smem(reinterpret_cast<const void *>(kern), static_cast<int>(smem)))
         return TTS_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas, 1, 1);
@@ -973,7 +1091,7 @@ int launch_tc(const AttnArgs &a, const CUtensorMap &kmap, const CUtensorMap &vma
     cudaLaunchAttribute attr[1] = {pdl_attr()};
     cfg.attrs = attr;
     cfg.numAttrs = o.pdl ? 1 : 0;
-    if (cudaLaunchKernelEx(&cfg, decode_attn_tc_kernel, kmap, vmap, a) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a) != cudaSuccess) {
         cudaGetLastError();
         return TTS_ERR_CUDA;
     }
@@ -981,7 +1099,7 @@ int launch_tc(const AttnArgs &a, const CUtensorMap &kmap, const CUtensorMap &vma
 }
 
 bool supported_head(int dtype, int head_dim) {
-    return (dtype == TTS_BF16 && head_dim == 128) || (dtype == TTS_F32 && head_dim == 64);
+    return ((dtype == TTS_BF16 || dtype == TTS_FP8_E4M3) && head_dim == 128) || (dtype == TTS_F32 && head_dim == 64);
 }
 
 }  // namespace
@@ -998,7 +1116,7 @@ bool attn_plan(int dtype, int B, int q_len, int num_q_heads, int num_kv_heads, i
     if (static_cast<long long>(B) * num_kv_heads * nblk >= (1LL << 31)) return false;
     out->rows = rows;
     out->ctas = device_sms() * ctas_per_sm(dtype, rows);
-    out->workers = out->ctas * (dtype == TTS_BF16 ? kTcWarps : kWarps);
+    out->workers = out->ctas * (dtype == TTS_F32 ? kWarps : kTcWarps);
     return true;
 }
 
@@ -1056,6 +1174,9 @@ int prepare_attn(const tts_kv_cache *cache, const int32_t *d_block_table, int32_
     }
     if (!aligned16(cache->k_pool) || !aligned16(cache->v_pool) || !aligned16(d_q))
         return TTS_ERR_INVALID;
+    const bool fp8 = cache->dtype == TTS_FP8_E4M3;
+    if (fp8 && (!cache->k_scale || !cache->v_scale || !aligned16(cache->k_scale) || !aligned16(cache->v_scale)))
+        return TTS_ERR_INVALID;
     const size_t need = attn_workspace_bytes(B, cache->num_kv_heads, cache->head_dim, pl);
     if (!d_ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(d_ws) & 255u) != 0)
         return TTS_ERR_WORKSPACE;
@@ -1083,7 +1204,9 @@ int prepare_attn(const tts_kv_cache *cache, const int32_t *d_block_table, int32_
         ws + need - align_up(static_cast<size_t>(B) * cache->num_kv_heads * sizeof(int32_t), 256));
     a.workers = pl.workers;
     a.nr_slot = pl.rows;
-    a.stages = cache->dtype == TTS_BF16 ? tc_stages(a.group * q_len, B) : kStages;
+    a.stages = cache->dtype == TTS_F32 ? kStages : tc_stages(a.group * q_len, B, fp8);
+    a.k_scale = cache->k_scale;
+    a.v_scale = cache->v_scale;
     if (a.stages < 1) return TTS_ERR_UNSUPPORTED;
     a.err = d_err;
     st->dtype = cache->dtype;
@@ -1094,6 +1217,12 @@ int prepare_attn(const tts_kv_cache *cache, const int32_t *d_block_table, int32_
         if (!cached_tma_2d_bf16(&st->kmap, cache->k_pool, rows, 128, TTS_BLOCK_TOKENS, 64) ||
             !cached_tma_2d_bf16(&st->vmap, cache->v_pool, rows, 128, TTS_BLOCK_TOKENS, 64))
             return TTS_ERR_CUDA;
+    } else if (fp8) {
+        // key codes: rows of 128 bytes, one 16-row box per tile; value codes
+        // and scales move by plain bulk copies
+        const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * a.Hkv * TTS_BLOCK_TOKENS;
+        if (!cached_tma_2d(&st->kmap, cache->k_pool, rows, 128, TTS_BLOCK_TOKENS, 128, 1)) return TTS_ERR_CUDA;
+        st->vmap = st->kmap;
     }
     return TTS_OK;
 }
@@ -1101,8 +1230,9 @@ int prepare_attn(const tts_kv_cache *cache, const int32_t *d_block_table, int32_
 int launch_attn(const AttnLaunch &L, LaunchOpts o) {
     const AttnLaunchState *st = reinterpret_cast<const AttnLaunchState *>(L.storage);
     if (st->ctas == 0) return TTS_OK;  // empty batch
-    return st->dtype == TTS_BF16 ? launch_tc(st->a, st->kmap, st->vmap, st->ctas, o)
-                                 : launch_simt(st->a, st->rows, st->ctas, o);
+    if (st->dtype == TTS_BF16) return launch_tc<false>(st->a, st->kmap, st->vmap, st->ctas, o);
+    if (st->dtype == TTS_FP8_E4M3) return launch_tc<true>(st->a, st->kmap, st->vmap, st->ctas, o);
+    return launch_simt(st->a, st->rows, st->ctas, o);
 }
 
 }  // namespace tts

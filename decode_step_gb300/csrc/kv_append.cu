@@ -6,6 +6,16 @@
 // One CTA per (stream, new token); its threads copy the token's Hkv rows of K
 // and of V as 16-byte vectors.  Pure data movement: bytes per launch =
 // 2 (read + write) x 2 (K, V) x B x q_len x Hkv x row bytes.
+//
+// FP8 cache ("Optimizing Streaming Text-to-Speech Models for Sub-50
+// Millisecond Latency", section "Engine-Level Optimizations with
+// TensorRT-LLM": the KV cache in FP8): one warp per (K or V, KV head) row of a
+// new token; the row is one quantisation block, scale = max|x| / 448 and
+// codes = E4M3(x / scale) (IEEE fp32 division, round to nearest even,
+// saturating).  Keys are stored token-major, values dimension-major with the
+// cache layout's slot order.
+#include <cuda_fp8.h>
+
 #include "tts_common.cuh"
 #include "tts_internal.h"
 
@@ -50,6 +60,68 @@ kv_append_kernel(const int32_t *__restrict__ table, int max_blocks,
     }
 }
 
+// Byte of token slot s within a dimension's 16 value codes (slot order
+// 0 1 8 9 2 3 10 11 4 5 12 13 6 7 14 15: lane t of a 16-bit ldmatrix row read
+// then holds the slots 2t, 2t+1, 2t+8, 2t+9 its attention fragment needs).
+__device__ __forceinline__ int v_code_pos(int s) { return 4 * ((s & 7) >> 1) + (s & 1) + 2 * (s >> 3); }
+
+constexpr int kFp8D = 128;
+
+__global__ void __launch_bounds__(128)
+kv_append_fp8_kernel(const int32_t *__restrict__ table, int max_blocks, const int32_t *__restrict__ ctx_before,
+                     int q_len, int Hkv, int num_blocks, const __nv_bfloat16 *__restrict__ k_new,
+                     const __nv_bfloat16 *__restrict__ v_new, uint8_t *__restrict__ k_codes,
+                     uint8_t *__restrict__ v_codes, float *__restrict__ k_scale, float *__restrict__ v_scale,
+                     int32_t *err) {
+    pdl_wait_prerequisites();
+    pdl_allow_dependents();
+    const int b = blockIdx.x / q_len;
+    const int j = blockIdx.x % q_len;
+    const int before = ctx_before[b];
+    const int cap = max_blocks * TTS_BLOCK_TOKENS;
+    if (before < 0 || before >= cap || j >= cap - before) {
+        if (threadIdx.x == 0) flag_error(err, TTS_ERRBIT_CTX_LEN);
+        return;
+    }
+    const int s = before + j;
+    const int blk = table[static_cast<size_t>(b) * max_blocks + s / TTS_BLOCK_TOKENS];
+    if (blk < 0 || blk >= num_blocks) {
+        if (threadIdx.x == 0) flag_error(err, TTS_ERRBIT_BLOCK_ID);
+        return;
+    }
+    const int slot = s % TTS_BLOCK_TOKENS;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int row = warp; row < 2 * Hkv; row += blockDim.x >> 5) {
+        const bool is_v = row >= Hkv;
+        const int g = is_v ? row - Hkv : row;
+        const __nv_bfloat16 *src = (is_v ? v_new : k_new) + (static_cast<size_t>(blockIdx.x) * Hkv + g) * kFp8D;
+        const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(src) + lane);  // values 4 lane .. 4 lane + 3
+        const float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
+        float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const float scale = amax / 448.0f;
+        uint32_t codes = 0;
+        if (scale > 0.0f) {
+            const __nv_fp8x2_storage_t c01 =
+                __nv_cvt_float2_to_fp8x2(make_float2(x[0] / scale, x[1] / scale), __NV_SATFINITE, __NV_E4M3);
+            const __nv_fp8x2_storage_t c23 =
+                __nv_cvt_float2_to_fp8x2(make_float2(x[2] / scale, x[3] / scale), __NV_SATFINITE, __NV_E4M3);
+            codes = static_cast<uint32_t>(c01) | (static_cast<uint32_t>(c23) << 16);
+        }
+        const size_t tile = static_cast<size_t>(blk) * Hkv + g;
+        if (!is_v) {
+            *reinterpret_cast<uint32_t *>(k_codes + (tile * TTS_BLOCK_TOKENS + slot) * kFp8D + 4 * lane) = codes;
+            if (lane == 0) k_scale[tile * TTS_BLOCK_TOKENS + slot] = scale;
+        } else {
+            uint8_t *dst = v_codes + (tile * kFp8D + 4 * lane) * TTS_BLOCK_TOKENS + v_code_pos(slot);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i * TTS_BLOCK_TOKENS] = static_cast<uint8_t>(codes >> (8 * i));
+            if (lane == 0) v_scale[tile * TTS_BLOCK_TOKENS + slot] = scale;
+        }
+    }
+}
+
 }  // namespace
 }  // namespace tts
 
@@ -64,6 +136,17 @@ int prepare_append(const tts_kv_cache *cache, const int32_t *d_block_table, int3
         cache->num_blocks < 1 || cache->num_kv_heads < 1 || cache->head_dim < 1)
         return TTS_ERR_INVALID;
     if (cache->block_size != TTS_BLOCK_TOKENS) return TTS_ERR_UNSUPPORTED;
+    if (cache->dtype == TTS_FP8_E4M3) {
+        if (cache->head_dim != kFp8D) return TTS_ERR_UNSUPPORTED;
+        if (!cache->k_scale || !cache->v_scale) return TTS_ERR_INVALID;
+        if (!aligned16(cache->k_pool) || !aligned16(cache->v_pool) || !aligned16(cache->k_scale) ||
+            !aligned16(cache->v_scale) || !aligned16(d_k_new) || !aligned16(d_v_new))
+            return TTS_ERR_INVALID;
+        if (static_cast<long>(B) * q_len > 0x7FFFFFFFL) return TTS_ERR_INVALID;
+        *out = AppendLaunch{cache, d_block_table, max_blocks_per_seq, d_ctx_before, B, q_len, d_k_new, d_v_new,
+                            d_err};
+        return TTS_OK;
+    }
     if (cache->dtype != TTS_F32 && cache->dtype != TTS_BF16) return TTS_ERR_UNSUPPORTED;
     const int elem = cache->dtype == TTS_F32 ? 4 : 2;
     const long row_bytes = static_cast<long>(cache->head_dim) * elem;
@@ -78,8 +161,6 @@ int prepare_append(const tts_kv_cache *cache, const int32_t *d_block_table, int3
 
 int launch_append(const AppendLaunch &L, LaunchOpts o) {
     if (L.B == 0) return TTS_OK;
-    const int elem = L.cache->dtype == TTS_F32 ? 4 : 2;
-    const int row_vecs = L.cache->head_dim * elem / 16;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long>(L.B) * L.q_len), 1, 1);
     cfg.blockDim = dim3(128, 1, 1);
@@ -89,6 +170,19 @@ int launch_append(const AppendLaunch &L, LaunchOpts o) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = o.pdl ? 1 : 0;
+    if (L.cache->dtype == TTS_FP8_E4M3) {
+        if (cudaLaunchKernelEx(&cfg, kv_append_fp8_kernel, L.table, L.max_blocks, L.ctx_before, L.q_len,
+                               static_cast<int>(L.cache->num_kv_heads), static_cast<int>(L.cache->num_blocks),
+                               static_cast<const __nv_bfloat16 *>(L.k_new), static_cast<const __nv_bfloat16 *>(L.v_new),
+                               static_cast<uint8_t *>(L.cache->k_pool), static_cast<uint8_t *>(L.cache->v_pool),
+                               L.cache->k_scale, L.cache->v_scale, L.err) != cudaSuccess) {
+            cudaGetLastError();
+            return TTS_ERR_CUDA;
+        }
+        return TTS_OK;
+    }
+    const int elem = L.cache->dtype == TTS_F32 ? 4 : 2;
+    const int row_vecs = L.cache->head_dim * elem / 16;
     if (cudaLaunchKernelEx(&cfg, kv_append_kernel, L.table, L.max_blocks, L.ctx_before, L.q_len,
                            static_cast<int>(L.cache->num_kv_heads), static_cast<int>(L.cache->num_blocks),
                            row_vecs, static_cast<const uint4 *>(L.k_new), static_cast<const uint4 *>(L.v_new),

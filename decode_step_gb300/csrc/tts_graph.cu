@@ -116,7 +116,7 @@ extern "C" int tts_step_graph_create(const tts_step_graph_desc *d, tts_step_grap
     if (st != TTS_OK) return st;
     const long long H = static_cast<long long>(d->num_q_heads) * c->head_dim;
     if (H > 0x7FFFFFFF) return TTS_ERR_INVALID;
-    st = prepare_head(d->d_attn_out, d->d_W, c->dtype, static_cast<int32_t>(R), static_cast<int32_t>(H), d->V,
+    st = prepare_head(d->d_attn_out, d->d_W, c->dtype == TTS_FP8_E4M3 ? TTS_BF16 : c->dtype, static_cast<int32_t>(R), static_cast<int32_t>(H), d->V,
                       d->mode, d->temperature, d->d_seed, d->d_step, d->d_eos_allowed, d->d_ids, d->d_best,
                       d->d_logits_out, d->d_head_ws, d->head_ws_bytes, &hd);
     if (st != TTS_OK) return st;

@@ -133,17 +133,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 }  // namespace
 
-bool make_tma_2d_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols,
-                      uint32_t box_rows, uint32_t box_cols) {
+bool make_tma_2d(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                 uint32_t box_cols, int elem_bytes) {
     auto fn = encode_fn();
-    if (!fn) return false;
+    if (!fn || (elem_bytes != 1 && elem_bytes != 2)) return false;
     const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint64_t strides[1] = {cols * static_cast<cuuint64_t>(elem_bytes)};
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return fn(map, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+              const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tma_2d_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols,
+                      uint32_t box_rows, uint32_t box_cols) {
+    return make_tma_2d(map, ptr, rows, cols, box_rows, box_cols, 2);
 }
 
 namespace {
@@ -151,6 +157,7 @@ struct MapEntry {
     const void *ptr;
     uint64_t rows, cols;
     uint32_t box_rows, box_cols;
+    int elem_bytes;
     int device;
     CUtensorMap map;
 };
@@ -159,15 +166,15 @@ MapEntry g_maps[16];
 int g_maps_used = 0, g_maps_next = 0;
 }  // namespace
 
-bool cached_tma_2d_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols,
-                        uint32_t box_rows, uint32_t box_cols) {
+bool cached_tma_2d(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                   uint32_t box_cols, int elem_bytes) {
     int dev = -1;
     cudaGetDevice(&dev);
     std::lock_guard<std::mutex> lock(g_map_mu);
     for (int i = 0; i < g_maps_used; ++i) {
         const MapEntry &e = g_maps[i];
         if (e.ptr == ptr && e.rows == rows && e.cols == cols && e.box_rows == box_rows &&
-            e.box_cols == box_cols && e.device == dev) {
+            e.box_cols == box_cols && e.elem_bytes == elem_bytes && e.device == dev) {
             *map = e.map;
             return true;
         }
@@ -178,13 +185,19 @@ bool cached_tma_2d_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64
     e.cols = cols;
     e.box_rows = box_rows;
     e.box_cols = box_cols;
+    e.elem_bytes = elem_bytes;
     e.device = dev;
-    if (!make_tma_2d_bf16(&e.map, ptr, rows, cols, box_rows, box_cols)) return false;
+    if (!make_tma_2d(&e.map, ptr, rows, cols, box_rows, box_cols, elem_bytes)) return false;
     g_maps[g_maps_next] = e;
     g_maps_next = (g_maps_next + 1) % 16;
     if (g_maps_used < 16) ++g_maps_used;
     *map = e.map;
     return true;
+}
+
+bool cached_tma_2d_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols,
+                        uint32_t box_rows, uint32_t box_cols) {
+    return cached_tma_2d(map, ptr, rows, cols, box_rows, box_cols, 2);
 }
 
 namespace {

@@ -13,10 +13,17 @@ namespace tts {
 // Number of SMs of the current device (cached per device ordinal).
 int sm_count();
 
-// TMA descriptor of a 2-D bf16 tensor [rows][cols] (cols contiguous) read in
-// boxes of box_rows x box_cols with 128-byte swizzle (box_cols * 2 <= 128);
-// out-of-range box elements read as zero.  false if the driver entry point is
-// unavailable or the driver rejects the shape.
+// TMA descriptor of a 2-D tensor [rows][cols] (cols contiguous) of 1-byte
+// (uint8) or 2-byte (bf16) elements, read in boxes of box_rows x box_cols with
+// 128-byte swizzle (box_cols * elem_bytes <= 128); out-of-range box elements
+// read as zero.  false if the driver entry point is unavailable or the driver
+// rejects the shape.  cached_tma_2d caches descriptors by (address, shape,
+// box, element size, device).
+bool make_tma_2d(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                 uint32_t box_cols, int elem_bytes);
+bool cached_tma_2d(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                   uint32_t box_cols, int elem_bytes);
+// bf16 forms of the two.
 bool make_tma_2d_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols,
                       uint32_t box_rows, uint32_t box_cols);
 

@@ -37,7 +37,7 @@ extern "C" int tts_decode_step(const tts_kv_cache *cache, const int32_t *d_block
     const long long R = static_cast<long long>(B) * q_len;
     const long long H = static_cast<long long>(num_q_heads) * cache->head_dim;
     if (R > 0x7FFFFFFF || H > 0x7FFFFFFF) return TTS_ERR_INVALID;
-    st = prepare_head(d_attn_out, d_W, cache->dtype, static_cast<int32_t>(R), static_cast<int32_t>(H), V,
+    st = prepare_head(d_attn_out, d_W, cache->dtype == TTS_FP8_E4M3 ? TTS_BF16 : cache->dtype, static_cast<int32_t>(R), static_cast<int32_t>(H), V,
                       mode, temperature, d_seed, d_step, d_eos_allowed, d_ids, d_best, d_logits_out,
                       d_head_ws, head_ws_bytes, &hd);
     if (st != TTS_OK) return st;

@@ -59,7 +59,7 @@ typedef enum {
     TTS_ERR_SCRATCH_LIMIT = -6     /* request larger than the library's static scratch */
 } tts_status;
 
-enum { TTS_F32 = 0, TTS_BF16 = 1 };             /* element types */
+enum { TTS_F32 = 0, TTS_BF16 = 1, TTS_FP8_E4M3 = 2 };  /* element types */
 enum { TTS_ARGMAX = 0, TTS_GUMBEL = 1 };        /* head selection modes */
 enum { TTS_VERIFY_BONUS = 1 };                  /* tts_spec_verify flags */
 
@@ -74,18 +74,33 @@ enum {
 #define TTS_BLOCK_TOKENS 16
 
 /* Paged KV cache [OPT, "Dynamic Token-Level Batching"]: a static pool of
- * num_blocks blocks of 16 tokens.  k_pool and v_pool are device arrays
- * [num_blocks][num_kv_heads][16][head_dim] of `dtype`, so each (block, head)
- * tile is contiguous.  Supported: (TTS_BF16, head_dim 128), (TTS_F32,
- * head_dim 64).  Pool base addresses must be 16-byte aligned. */
+ * num_blocks blocks of 16 tokens.  For TTS_F32 and TTS_BF16, k_pool and
+ * v_pool are device arrays [num_blocks][num_kv_heads][16][head_dim] of
+ * `dtype`, so each (block, head) tile is contiguous; k_scale and v_scale are
+ * unused.  Supported: (TTS_BF16, head_dim 128), (TTS_F32, head_dim 64).
+ *
+ * TTS_FP8_E4M3 (head_dim 128; the KV cache in FP8: [OPT, "Engine-Level
+ * Optimizations with TensorRT-LLM"]): every cached key or value row (one
+ * token, one KV head, head_dim values) is one quantisation block, stored as
+ * E4M3 codes with one fp32 scale, value = code * scale.
+ *   k_pool  uint8 [num_blocks][num_kv_heads][16][head_dim]  (token-major)
+ *   v_pool  uint8 [num_blocks][num_kv_heads][head_dim][16]  (dimension-major;
+ *           within a dimension's 16 bytes, token slot s sits at byte
+ *           4 * ((s % 8) / 2) + (s % 2) + 2 * (s / 8), i.e. the slot order
+ *           0 1 8 9 2 3 10 11 4 5 12 13 6 7 14 15)
+ *   k_scale, v_scale  float [num_blocks][num_kv_heads][16]
+ * The step's activations (q, k_new, v_new, the attention output) are bf16.
+ * All base addresses must be 16-byte aligned. */
 typedef struct tts_kv_cache {
     int32_t num_blocks;
     int32_t block_size;     /* must be 16 */
     int32_t num_kv_heads;
     int32_t head_dim;
-    int32_t dtype;          /* TTS_F32 or TTS_BF16 */
+    int32_t dtype;          /* TTS_F32, TTS_BF16 or TTS_FP8_E4M3 */
     void *k_pool;
     void *v_pool;
+    float *k_scale;         /* TTS_FP8_E4M3 only */
+    float *v_scale;         /* TTS_FP8_E4M3 only */
 } tts_kv_cache;
 
 /* ------------------------------------------------------------ block pool */
@@ -120,6 +135,11 @@ void tts_block_pool_destroy(tts_block_pool *pool);
  *  d_block_table  int32 [B][max_blocks_per_seq]
  *  d_ctx_before   int32 [B] — tokens already cached before this step
  *  d_k_new, d_v_new  `cache->dtype` [B][q_len][num_kv_heads][head_dim]
+ *                    (bf16 for a TTS_FP8_E4M3 cache)
+ * FP8 cache: each new row x (head_dim values) is quantised with scale =
+ * max|x| / 448 (fp32) and codes = E4M3(x / scale) (fp32 division, round to
+ * nearest even, saturating at +-448); an all-zero row stores scale 0 and
+ * codes 0.  The codes and the scale go to the layouts of tts_kv_cache.
  * A slot outside the table (TTS_ERRBIT_CTX_LEN) or a block id outside the
  * pool (TTS_ERRBIT_BLOCK_ID) is skipped. */
 int tts_kv_append(const tts_kv_cache *cache, const int32_t *d_block_table,
@@ -245,7 +265,8 @@ int tts_spec_verify(const float *d_target_logits, const float *d_draft_probs,
 
 /* One decode step in one call: tts_kv_append, then tts_decode_attn into
  * d_attn_out, then tts_codebook_head_select with h = d_attn_out read as
- * [B * q_len][num_q_heads * head_dim] (dtype cache->dtype, R = B * q_len).
+ * [B * q_len][num_q_heads * head_dim] (dtype cache->dtype; bf16 for an FP8
+ * cache; R = B * q_len).
  * Arguments mean what they mean for those three calls; all of them are
  * checked before anything is launched.  The attention and head kernels are
  * launched as programmatic dependents of the kernel before them: each starts

@@ -454,6 +454,12 @@ def check_e4m3_encode_matches_torch(o):
     assert np.array_equal(o.e4m3_encode(-big), np.full(5, 0xFE, np.uint8))
 
 
+def v_pos(s):
+    """Byte of token slot s within a dimension's 16 value codes (cache layout)."""
+    order = [0, 1, 8, 9, 2, 3, 10, 11, 4, 5, 12, 13, 6, 7, 14, 15]
+    return order.index(s)
+
+
 def fp8_case(seed, B, Hkv, D, ctx_lens, permute=True):
     """Random FP8 cache arrays for every slot (no NaN codes) and the table."""
     rng = np.random.default_rng(seed)
@@ -483,14 +489,16 @@ def check_kv_append_fp8_quantization(o):
     kc, vc, ks, vs = o.kv_append_fp8(c["k_codes"], c["v_codes"], c["k_scale"], c["v_scale"],
                                      c["block_table"], before, k_new, v_new)
     touched = np.zeros(c["k_scale"].shape, dtype=bool)
+    vtouched = np.zeros(c["k_scale"].shape, dtype=bool)
     for b in range(B):
         for j in range(q_len):
             s = before[b] + j
             blk, slot = c["block_table"][b, s // wl.BLOCK], s % wl.BLOCK
             for g in range(Hkv):
                 touched[blk, g, slot] = True
+                vtouched[blk, g, v_pos(slot)] = True
                 for x_bits, codes, scale in ((k_new[b, j, g], kc[blk, g, slot, :], ks[blk, g, slot]),
-                                             (v_new[b, j, g], vc[blk, g, :, slot], vs[blk, g, slot])):
+                                             (v_new[b, j, g], vc[blk, g, :, v_pos(slot)], vs[blk, g, slot])):
                     x = wl.bf16_to_f32(x_bits)
                     amax = np.float32(np.abs(x).max())
                     assert scale == np.float32(amax / np.float32(448.0))
@@ -508,7 +516,7 @@ def check_kv_append_fp8_quantization(o):
     assert np.array_equal(vs[~touched], c["v_scale"][~touched])
     kt = np.broadcast_to(touched[..., None], kc.shape)
     assert np.array_equal(kc[~kt], c["k_codes"][~kt])
-    vt = np.broadcast_to(touched[:, :, None, :], vc.shape)
+    vt = np.broadcast_to(vtouched[:, :, None, :], vc.shape)
     assert np.array_equal(vc[~vt], c["v_codes"][~vt])
 
 
@@ -530,7 +538,7 @@ def check_attn_fp8_matches_sdpa(o):
             t = np.arange(Lb)
             blocks, slots = c["block_table"][b, t // wl.BLOCK], t % wl.BLOCK
             kcod = torch.from_numpy(c["k_codes"][blocks, :, slots, :].astype(np.int64))          # [L][Hkv][D]
-            vcod = torch.from_numpy(c["v_codes"][blocks, :, :, slots].astype(np.int64))          # [L][Hkv][D]
+            vcod = torch.from_numpy(c["v_codes"][blocks, :, :, [v_pos(x) for x in slots]].astype(np.int64))
             k = tab[kcod] * torch.from_numpy(c["k_scale"][blocks, :, slots].astype(np.float64))[..., None]
             v = tab[vcod] * torch.from_numpy(c["v_scale"][blocks, :, slots].astype(np.float64))[..., None]
             k = k.permute(1, 0, 2).repeat_interleave(g, dim=0)

@@ -59,8 +59,10 @@ MUTANTS = [
     ("e4m3: largest finite code excluded", "for (int c = 0; c <= 0x7E; ++c)", "for (int c = 0; c < 0x7E; ++c)"),
     ("e4m3: subnormal exponent", "ldexp((double)m, -9)", "ldexp((double)m, -10)"),
     ("fp8 append: scale for a maximum of 240", "amax / 448.0f", "amax / 240.0f"),
-    ("fp8 append: values stored token-major", "v_codes + tile * ORC_BLOCK * D + slot, ORC_BLOCK,",
+    ("fp8 append: values stored token-major", "v_codes + tile * ORC_BLOCK * D + v_pos(slot), ORC_BLOCK,",
      "v_codes + (tile * ORC_BLOCK + slot) * D, 1,"),
+    ("fp8 append: value slots in natural order", "v_codes + tile * ORC_BLOCK * D + v_pos(slot), ORC_BLOCK,",
+     "v_codes + tile * ORC_BLOCK * D + slot, ORC_BLOCK,"),
     ("fp8 attn: values scaled by the key scale", "(double)p->v_scale[tile * ORC_BLOCK + slot];",
      "(double)p->k_scale[tile * ORC_BLOCK + slot];"),
     ("verify: bonus always drawn", "if (!rejected && (flags & 1)) {", "if (!rejected) {"),
