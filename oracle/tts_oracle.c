@@ -248,6 +248,11 @@ void orc_e4m3_decode_n(const uint8_t *c, size_t n, float *out) {
     for (size_t i = 0; i < n; ++i) out[i] = orc_e4m3_decode(c[i]);
 }
 
+/* Byte of token slot s within a dimension's 16 value codes: the slot order
+ * 0 1 8 9 2 3 10 11 4 5 12 13 6 7 14 15 (a storage-order choice of the cache
+ * layout, not part of the arithmetic). */
+static int v_pos(int s) { return 4 * ((s % 8) / 2) + (s % 2) + 2 * (s / 8); }
+
 /* Quantises one row of n values: scale = max|x| / 448 (fp32), codes =
  * E4M3(x / scale) computed in fp32; an all-zero row gets scale 0 and codes 0. */
 static void quantize_row(const float *x, int n, uint8_t *codes, int code_stride, float *scale_out) {
@@ -266,9 +271,9 @@ static void quantize_row(const float *x, int n, uint8_t *codes, int code_stride,
  * "Engine-Level Optimizations with TensorRT-LLM").  Each new key and value row
  * (one token, one KV head: D bf16 values) is one quantisation block with its
  * own fp32 scale.  Layouts: k_codes [num_blocks][Hkv][16][D] (token-major),
- * v_codes [num_blocks][Hkv][D][16] (dimension-major), k_scale and v_scale
- * [num_blocks][Hkv][16].  Returns 0, or -1 if a slot falls outside the table
- * or the pool. */
+ * v_codes [num_blocks][Hkv][D][16] (dimension-major, token slot s at byte
+ * v_pos(s) of the dimension's 16), k_scale and v_scale [num_blocks][Hkv][16].
+ * Returns 0, or -1 if a slot falls outside the table or the pool. */
 int orc_kv_append_fp8(int num_blocks, int Hkv, int D, uint8_t *k_codes, uint8_t *v_codes,
                       float *k_scale, float *v_scale, const int32_t *block_table, int max_blocks,
                       const int32_t *ctx_before, int B, int q_len, const uint16_t *k_new,
@@ -288,7 +293,7 @@ int orc_kv_append_fp8(int num_blocks, int Hkv, int D, uint8_t *k_codes, uint8_t 
                 for (int d = 0; d < D; ++d) row[d] = (float)load_elem(k_new, src + d, 1);
                 quantize_row(row, D, k_codes + (tile * ORC_BLOCK + slot) * D, 1, k_scale + tile * ORC_BLOCK + slot);
                 for (int d = 0; d < D; ++d) row[d] = (float)load_elem(v_new, src + d, 1);
-                quantize_row(row, D, v_codes + tile * ORC_BLOCK * D + slot, ORC_BLOCK,
+                quantize_row(row, D, v_codes + tile * ORC_BLOCK * D + v_pos(slot), ORC_BLOCK,
                              v_scale + tile * ORC_BLOCK + slot);
             }
         }
@@ -307,7 +312,7 @@ static double fp8_kv(const void *ctx, int is_v, int blk, int g, int slot, int d)
     const orc_fp8_pool *p = (const orc_fp8_pool *)ctx;
     const size_t tile = (size_t)blk * p->Hkv + g;
     if (is_v)
-        return (double)orc_e4m3_decode(p->v_codes[(tile * p->D + d) * ORC_BLOCK + slot]) *
+        return (double)orc_e4m3_decode(p->v_codes[(tile * p->D + d) * ORC_BLOCK + v_pos(slot)]) *
                (double)p->v_scale[tile * ORC_BLOCK + slot];
     return (double)orc_e4m3_decode(p->k_codes[(tile * ORC_BLOCK + slot) * p->D + d]) *
            (double)p->k_scale[tile * ORC_BLOCK + slot];
