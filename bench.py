@@ -129,8 +129,9 @@ def attn_bytes(inp) -> int:
 
 def attn_bytes_fp8(inp) -> int:
     """Algorithmic bytes of one attention launch over an FP8 cache: every
-    cached key and value row once as codes plus its fp32 scale, q and out
-    (bf16), the used block-table entries and the context lengths."""
+    cached key and value row once as codes plus its fp32 scale (4224 bytes per
+    16 tokens and KV head), q and out (bf16), the used block-table entries and
+    the context lengths."""
     w = inp["workload"]
     L = inp["ctx_lens"].astype(np.int64)
     kv = int(L.sum()) * w.Hkv * (w.D + 4) * 2
@@ -332,10 +333,7 @@ def kernel_sweep(ids, reps, flush_l2, peaks, device) -> dict:
             # the context quantised by the library's own append, one stream at a time
             kp, vp = dev(inp["k_pool"]), dev(inp["v_pool"])
             nb = kp.shape[0]
-            cache = bd.KVCache(torch.zeros((nb, w.Hkv, 16, w.D), dtype=torch.uint8, device=device),
-                               torch.zeros((nb, w.Hkv, w.D, 16), dtype=torch.uint8, device=device),
-                               torch.zeros((nb, w.Hkv, 16), dtype=torch.float32, device=device),
-                               torch.zeros((nb, w.Hkv, 16), dtype=torch.float32, device=device))
+            cache = bd.KVCache(torch.zeros((nb, w.Hkv, bd.KVCache.FP8_TILE_BYTES), dtype=torch.uint8, device=device))
             zero = torch.zeros(1, dtype=torch.int32, device=device)
             for b in range(w.B):
                 n = int(inp["ctx_before"][b])

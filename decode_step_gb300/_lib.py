@@ -27,8 +27,7 @@ _f32 = ctypes.c_float
 
 class KVCacheDesc(ctypes.Structure):
     _fields_ = [("num_blocks", _i32), ("block_size", _i32), ("num_kv_heads", _i32),
-                ("head_dim", _i32), ("dtype", _i32), ("k_pool", _vp), ("v_pool", _vp),
-                ("k_scale", _vp), ("v_scale", _vp)]
+                ("head_dim", _i32), ("dtype", _i32), ("k_pool", _vp), ("v_pool", _vp)]
 
 
 class StepGraphDesc(ctypes.Structure):

@@ -54,35 +54,33 @@ class KVCache:
     """Paged KV pool.
 
     float32 / bfloat16: k_pool, v_pool [num_blocks][num_kv_heads][16][head_dim].
-    FP8 E4M3 (uint8 codes, or torch.float8_e4m3fn): k_pool [num_blocks][Hkv][16][D]
-    (token-major), v_pool [num_blocks][Hkv][D][16] (dimension-major, the
-    slot order of tts_kv_cache), k_scale, v_scale float32 [num_blocks][Hkv][16];
-    the step's activations are bfloat16.
+    FP8 E4M3: k_pool uint8 [num_blocks][num_kv_heads][4224], one record per
+    (block, KV head) in the layout of tts_kv_cache (key codes, value codes,
+    key and value scales), v_pool None; head_dim is 128 and the step's
+    activations are bfloat16.
     """
 
-    def __init__(self, k_pool: torch.Tensor, v_pool: torch.Tensor, k_scale: torch.Tensor | None = None,
-                 v_scale: torch.Tensor | None = None):
-        self.fp8 = k_pool.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8))
+    FP8_TILE_BYTES = 4224
+
+    def __init__(self, k_pool: torch.Tensor, v_pool: torch.Tensor | None = None):
+        self.fp8 = k_pool.dtype == torch.uint8
         if self.fp8:
-            nb, hkv, blk, d = k_pool.shape
-            if blk != 16 or tuple(v_pool.shape) != (nb, hkv, d, 16) or v_pool.dtype != k_pool.dtype:
-                raise ValueError("FP8 pools must be k [nb][Hkv][16][D] and v [nb][Hkv][D][16]")
-            if k_scale is None or v_scale is None:
-                raise ValueError("an FP8 cache needs k_scale and v_scale")
-            scales = (_dev(k_scale, "k_scale", torch.float32, (nb, hkv, 16)),
-                      _dev(v_scale, "v_scale", torch.float32, (nb, hkv, 16)))
+            if v_pool is not None or k_pool.dim() != 3 or k_pool.shape[2] != self.FP8_TILE_BYTES:
+                raise ValueError("an FP8 cache is one uint8 tensor [num_blocks][num_kv_heads][4224]")
+            nb, hkv, _ = k_pool.shape
+            d = 128
             dtype = TTS_FP8_E4M3
+            vptr = None
         else:
-            if k_pool.shape != v_pool.shape or k_pool.dim() != 4 or k_pool.shape[2] != 16:
+            if v_pool is None or k_pool.shape != v_pool.shape or k_pool.dim() != 4 or k_pool.shape[2] != 16:
                 raise ValueError("pools must be [num_blocks][num_kv_heads][16][head_dim] and alike")
             if k_pool.dtype != v_pool.dtype or k_pool.dtype not in _DTYPES:
-                raise ValueError("pools must both be float32, bfloat16 or FP8 E4M3")
+                raise ValueError("pools must both be float32 or bfloat16 (or an FP8 uint8 tile array)")
             nb, hkv, _, d = k_pool.shape
-            scales = (None, None)
             dtype = _DTYPES[k_pool.dtype]
-        self.k_pool, self.v_pool, self.k_scale, self.v_scale = k_pool, v_pool, k_scale, v_scale
-        self.desc = KVCacheDesc(nb, 16, hkv, d, dtype, _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
-                                *scales)
+            vptr = _dev(v_pool, "v_pool")
+        self.k_pool, self.v_pool = k_pool, v_pool
+        self.desc = KVCacheDesc(nb, 16, hkv, d, dtype, _dev(k_pool, "k_pool"), vptr)
 
     @property
     def num_blocks(self) -> int:

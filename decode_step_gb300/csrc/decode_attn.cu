@@ -74,8 +74,6 @@ struct AttnArgs {
     int workers;
     int nr_slot;        // query rows per partial slot (group * q_len padded)
     int stages;         // ring depth per warp (tensor-core kernel)
-    const float *k_scale;  // FP8 cache: row scales [num_blocks][Hkv][16]
-    const float *v_scale;
     int32_t *err;
 };
 
@@ -567,6 +565,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
         : "memory");
 }
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -582,9 +588,9 @@ constexpr int kTcCtasPerSm = 3;
 // of a new segment (row-major bf16, n_rows x 256 B).
 constexpr int kBoxBytes = 2048;
 constexpr int kKVStageBytes = 4 * kBoxBytes;
-// FP8 cache: K codes (16 rows x 128 B, one 128-byte-swizzled box), V codes
-// (128 dimension rows x 16 B, as stored), the 16 key scales and 16 value
-// scales, then the query rows.
+// FP8 cache: the (block, head) record as stored (K codes: 16 rows x 128 B with
+// the 16-byte chunks swizzled; V codes: 128 dimension rows x 16 B; the 16 key
+// scales and 16 value scales), one bulk copy, then the query rows.
 constexpr int kFp8VOff = 2048;
 constexpr int kFp8ScaleOff = 4096;
 constexpr int kFp8KVStageBytes = kFp8ScaleOff + 2 * 64;
@@ -721,16 +727,12 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
                     const int tile = id * a.Hkv + seg % a.Hkv;
                     const int row = tile * TTS_BLOCK_TOKENS;
                     if constexpr (kFp8) {
-                        tma_load_2d(dst, &kmap, 0, row, bar, policy);
-                        bulk_load(dst + kFp8VOff, a.v_pool + static_cast<size_t>(tile) * 2048, 2048, bar, policy);
-                        bulk_load(dst + kFp8ScaleOff, a.k_scale + static_cast<size_t>(tile) * 16, 64, bar, policy);
-                        bulk_load(dst + kFp8ScaleOff + 64, a.v_scale + static_cast<size_t>(tile) * 16, 64, bar,
+                        bulk_load(dst, a.k_pool + static_cast<size_t>(tile) * kFp8KVStageBytes, kFp8KVStageBytes, bar,
                                   policy);
                     } else {
-                        tma_load_2d(dst, &kmap, 0, row, bar, policy);
-                        tma_load_2d(dst + kBoxBytes, &kmap, 64, row, bar, policy);
-                        tma_load_2d(dst + 2 * kBoxBytes, &vmap, 0, row, bar, policy);
-                        tma_load_2d(dst + 3 * kBoxBytes, &vmap, 64, row, bar, policy);
+                        // one 3-D box per tensor: both 64-column halves of the 16 rows
+                        tma_load_3d(dst, &kmap, 0, row, 0, bar, policy);
+                        tma_load_3d(dst + 2 * kBoxBytes, &vmap, 0, row, 0, bar, policy);
                     }
                 }
                 if (need_q) {
@@ -1152,7 +1154,8 @@ int prepare_attn(const tts_kv_cache *cache, const int32_t *d_block_table, int32_
                  int32_t num_q_heads, float scale, int32_t causal, const void *d_q, void *d_out,
                  void *d_ws, size_t ws_bytes, int32_t *d_err, AttnLaunch *out) {
     if (!cache || !d_block_table || !d_ctx_lens || !d_q || !d_out) return TTS_ERR_INVALID;
-    if (!cache->k_pool || !cache->v_pool || cache->num_blocks < 1) return TTS_ERR_INVALID;
+    if (!cache->k_pool || (!cache->v_pool && cache->dtype != TTS_FP8_E4M3) || cache->num_blocks < 1)
+        return TTS_ERR_INVALID;
     if (B < 0 || q_len < 1 || max_blocks_per_seq < 1 || max_blocks_per_seq > (1 << 20) ||
         !(scale > 0.0f) || scale != scale)
         return TTS_ERR_INVALID;
@@ -1172,10 +1175,8 @@ int prepare_attn(const tts_kv_cache *cache, const int32_t *d_block_table, int32_
                               max_ctx_len <= (1 << 24);
         return shape_ok ? TTS_ERR_UNSUPPORTED : TTS_ERR_INVALID;
     }
-    if (!aligned16(cache->k_pool) || !aligned16(cache->v_pool) || !aligned16(d_q))
-        return TTS_ERR_INVALID;
     const bool fp8 = cache->dtype == TTS_FP8_E4M3;
-    if (fp8 && (!cache->k_scale || !cache->v_scale || !aligned16(cache->k_scale) || !aligned16(cache->v_scale)))
+    if (!aligned16(cache->k_pool) || (!fp8 && !aligned16(cache->v_pool)) || !aligned16(d_q))
         return TTS_ERR_INVALID;
     const size_t need = attn_workspace_bytes(B, cache->num_kv_heads, cache->head_dim, pl);
     if (!d_ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(d_ws) & 255u) != 0)
@@ -1205,8 +1206,7 @@ int prepare_attn(const tts_kv_cache *cache, const int32_t *d_block_table, int32_
     a.workers = pl.workers;
     a.nr_slot = pl.rows;
     a.stages = cache->dtype == TTS_F32 ? kStages : tc_stages(a.group * q_len, B, fp8);
-    a.k_scale = cache->k_scale;
-    a.v_scale = cache->v_scale;
+
     if (a.stages < 1) return TTS_ERR_UNSUPPORTED;
     a.err = d_err;
     st->dtype = cache->dtype;
@@ -1214,15 +1214,9 @@ int prepare_attn(const tts_kv_cache *cache, const int32_t *d_block_table, int32_
     st->ctas = pl.ctas;
     if (cache->dtype == TTS_BF16) {
         const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * a.Hkv * TTS_BLOCK_TOKENS;
-        if (!cached_tma_2d_bf16(&st->kmap, cache->k_pool, rows, 128, TTS_BLOCK_TOKENS, 64) ||
-            !cached_tma_2d_bf16(&st->vmap, cache->v_pool, rows, 128, TTS_BLOCK_TOKENS, 64))
+        if (!make_tma_rows_in_halves_bf16(&st->kmap, cache->k_pool, rows, TTS_BLOCK_TOKENS) ||
+            !make_tma_rows_in_halves_bf16(&st->vmap, cache->v_pool, rows, TTS_BLOCK_TOKENS))
             return TTS_ERR_CUDA;
-    } else if (fp8) {
-        // key codes: rows of 128 bytes, one 16-row box per tile; value codes
-        // and scales move by plain bulk copies
-        const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * a.Hkv * TTS_BLOCK_TOKENS;
-        if (!cached_tma_2d(&st->kmap, cache->k_pool, rows, 128, TTS_BLOCK_TOKENS, 128, 1)) return TTS_ERR_CUDA;
-        st->vmap = st->kmap;
     }
     return TTS_OK;
 }

@@ -12,8 +12,9 @@
 // TensorRT-LLM": the KV cache in FP8): one warp per (K or V, KV head) row of a
 // new token; the row is one quantisation block, scale = max|x| / 448 and
 // codes = E4M3(x / scale) (IEEE fp32 division, round to nearest even,
-// saturating).  Keys are stored token-major, values dimension-major with the
-// cache layout's slot order.
+// saturating).  Codes and scale go to the (block, head) record of the cache
+// layout: keys token-major with 16-byte chunks swizzled, values
+// dimension-major in the layout's slot order, then the scales.
 #include <cuda_fp8.h>
 
 #include "tts_common.cuh"
@@ -66,13 +67,12 @@ kv_append_kernel(const int32_t *__restrict__ table, int max_blocks,
 __device__ __forceinline__ int v_code_pos(int s) { return 4 * ((s & 7) >> 1) + (s & 1) + 2 * (s >> 3); }
 
 constexpr int kFp8D = 128;
+constexpr int kFp8Tile = 4224;  // bytes of one (block, head) record
 
 __global__ void __launch_bounds__(128)
 kv_append_fp8_kernel(const int32_t *__restrict__ table, int max_blocks, const int32_t *__restrict__ ctx_before,
                      int q_len, int Hkv, int num_blocks, const __nv_bfloat16 *__restrict__ k_new,
-                     const __nv_bfloat16 *__restrict__ v_new, uint8_t *__restrict__ k_codes,
-                     uint8_t *__restrict__ v_codes, float *__restrict__ k_scale, float *__restrict__ v_scale,
-                     int32_t *err) {
+                     const __nv_bfloat16 *__restrict__ v_new, uint8_t *__restrict__ tiles, int32_t *err) {
     pdl_wait_prerequisites();
     pdl_allow_dependents();
     const int b = blockIdx.x / q_len;
@@ -109,15 +109,16 @@ kv_append_fp8_kernel(const int32_t *__restrict__ table, int max_blocks, const in
                 __nv_cvt_float2_to_fp8x2(make_float2(x[2] / scale, x[3] / scale), __NV_SATFINITE, __NV_E4M3);
             codes = static_cast<uint32_t>(c01) | (static_cast<uint32_t>(c23) << 16);
         }
-        const size_t tile = static_cast<size_t>(blk) * Hkv + g;
+        uint8_t *tile = tiles + (static_cast<size_t>(blk) * Hkv + g) * kFp8Tile;
         if (!is_v) {
-            *reinterpret_cast<uint32_t *>(k_codes + (tile * TTS_BLOCK_TOKENS + slot) * kFp8D + 4 * lane) = codes;
-            if (lane == 0) k_scale[tile * TTS_BLOCK_TOKENS + slot] = scale;
+            // dims 4 lane .. 4 lane + 3: chunk lane / 4 of the slot's 128-byte row
+            *reinterpret_cast<uint32_t *>(tile + 128 * slot + 16 * ((lane >> 2) ^ (slot & 7)) + 4 * (lane & 3)) = codes;
+            if (lane == 0) *reinterpret_cast<float *>(tile + 4096 + 4 * slot) = scale;
         } else {
-            uint8_t *dst = v_codes + (tile * kFp8D + 4 * lane) * TTS_BLOCK_TOKENS + v_code_pos(slot);
+            uint8_t *dst = tile + 2048 + 16 * (4 * lane) + v_code_pos(slot);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i * TTS_BLOCK_TOKENS] = static_cast<uint8_t>(codes >> (8 * i));
-            if (lane == 0) v_scale[tile * TTS_BLOCK_TOKENS + slot] = scale;
+            for (int i = 0; i < 4; ++i) dst[16 * i] = static_cast<uint8_t>(codes >> (8 * i));
+            if (lane == 0) *reinterpret_cast<float *>(tile + 4160 + 4 * slot) = scale;
         }
     }
 }
@@ -131,17 +132,14 @@ int prepare_append(const tts_kv_cache *cache, const int32_t *d_block_table, int3
                    const int32_t *d_ctx_before, int32_t B, int32_t q_len, const void *d_k_new,
                    const void *d_v_new, int32_t *d_err, AppendLaunch *out) {
     if (!cache || !d_block_table || !d_ctx_before || !d_k_new || !d_v_new) return TTS_ERR_INVALID;
-    if (!cache->k_pool || !cache->v_pool) return TTS_ERR_INVALID;
+    if (!cache->k_pool || (!cache->v_pool && cache->dtype != TTS_FP8_E4M3)) return TTS_ERR_INVALID;
     if (B < 0 || q_len < 1 || max_blocks_per_seq < 1 || max_blocks_per_seq > (1 << 20) ||
         cache->num_blocks < 1 || cache->num_kv_heads < 1 || cache->head_dim < 1)
         return TTS_ERR_INVALID;
     if (cache->block_size != TTS_BLOCK_TOKENS) return TTS_ERR_UNSUPPORTED;
     if (cache->dtype == TTS_FP8_E4M3) {
         if (cache->head_dim != kFp8D) return TTS_ERR_UNSUPPORTED;
-        if (!cache->k_scale || !cache->v_scale) return TTS_ERR_INVALID;
-        if (!aligned16(cache->k_pool) || !aligned16(cache->v_pool) || !aligned16(cache->k_scale) ||
-            !aligned16(cache->v_scale) || !aligned16(d_k_new) || !aligned16(d_v_new))
-            return TTS_ERR_INVALID;
+        if (!aligned16(cache->k_pool) || !aligned16(d_k_new) || !aligned16(d_v_new)) return TTS_ERR_INVALID;
         if (static_cast<long>(B) * q_len > 0x7FFFFFFFL) return TTS_ERR_INVALID;
         *out = AppendLaunch{cache, d_block_table, max_blocks_per_seq, d_ctx_before, B, q_len, d_k_new, d_v_new,
                             d_err};
@@ -174,8 +172,7 @@ int launch_append(const AppendLaunch &L, LaunchOpts o) {
         if (cudaLaunchKernelEx(&cfg, kv_append_fp8_kernel, L.table, L.max_blocks, L.ctx_before, L.q_len,
                                static_cast<int>(L.cache->num_kv_heads), static_cast<int>(L.cache->num_blocks),
                                static_cast<const __nv_bfloat16 *>(L.k_new), static_cast<const __nv_bfloat16 *>(L.v_new),
-                               static_cast<uint8_t *>(L.cache->k_pool), static_cast<uint8_t *>(L.cache->v_pool),
-                               L.cache->k_scale, L.cache->v_scale, L.err) != cudaSuccess) {
+                               static_cast<uint8_t *>(L.cache->k_pool), L.err) != cudaSuccess) {
             cudaGetLastError();
             return TTS_ERR_CUDA;
         }

@@ -152,6 +152,18 @@ bool make_tma_2d_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t
     return make_tma_2d(map, ptr, rows, cols, box_rows, box_cols, 2);
 }
 
+bool make_tma_rows_in_halves_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {64, rows, 2};
+    const cuuint64_t strides[2] = {256, 128};  // next row, next half
+    const cuuint32_t box[3] = {64, box_rows, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 namespace {
 struct MapEntry {
     const void *ptr;

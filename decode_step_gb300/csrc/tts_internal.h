@@ -23,6 +23,11 @@ bool make_tma_2d(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols
                  uint32_t box_cols, int elem_bytes);
 bool cached_tma_2d(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
                    uint32_t box_cols, int elem_bytes);
+// 3-D descriptor over bf16 rows of 128 elements seen as two 64-element halves:
+// dims {64, rows, 2} with strides {256 B, 128 B}, box {64, box_rows, 2}, so one
+// copy lands a tile of box_rows rows as [half][row][64] (each half 128-byte
+// swizzled), the layout two 2-D boxes of 64 columns would give.
+bool make_tma_rows_in_halves_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uint32_t box_rows);
 // bf16 forms of the two.
 bool make_tma_2d_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols,
                       uint32_t box_rows, uint32_t box_cols);

@@ -81,15 +81,18 @@ enum {
  *
  * TTS_FP8_E4M3 (head_dim 128; the KV cache in FP8: [OPT, "Engine-Level
  * Optimizations with TensorRT-LLM"]): every cached key or value row (one
- * token, one KV head, head_dim values) is one quantisation block, stored as
- * E4M3 codes with one fp32 scale, value = code * scale.
- *   k_pool  uint8 [num_blocks][num_kv_heads][16][head_dim]  (token-major)
- *   v_pool  uint8 [num_blocks][num_kv_heads][head_dim][16]  (dimension-major;
- *           within a dimension's 16 bytes, token slot s sits at byte
- *           4 * ((s % 8) / 2) + (s % 2) + 2 * (s / 8), i.e. the slot order
- *           0 1 8 9 2 3 10 11 4 5 12 13 6 7 14 15)
- *   k_scale, v_scale  float [num_blocks][num_kv_heads][16]
- * The step's activations (q, k_new, v_new, the attention output) are bf16.
+ * token, one KV head, 128 values) is one quantisation block, stored as E4M3
+ * codes with one fp32 scale, value = code * scale.  k_pool holds one
+ * 4224-byte record per (block, KV head): uint8 [num_blocks][num_kv_heads][4224]
+ *   bytes    0..2047  key codes: slot s, dimension d at 128 s + 16 ((d / 16)
+ *                     xor (s % 8)) + d % 16 (rows of 128 bytes, 16-byte
+ *                     chunks permuted as a 128-byte swizzle would)
+ *   bytes 2048..4095  value codes: dimension d, slot s at 2048 + 16 d + p(s),
+ *                     p(s) = 4 ((s % 8) / 2) + (s % 2) + 2 (s / 8), i.e. each
+ *                     dimension's 16 slots in the order 0 1 8 9 2 3 10 11 ...
+ *   bytes 4096..4159  the 16 key scales (float), 4160..4223 the value scales
+ * so a tile moves with one bulk copy; v_pool is unused (NULL).  The step's
+ * activations (q, k_new, v_new, the attention output) are bf16.
  * All base addresses must be 16-byte aligned. */
 typedef struct tts_kv_cache {
     int32_t num_blocks;
@@ -99,8 +102,6 @@ typedef struct tts_kv_cache {
     int32_t dtype;          /* TTS_F32, TTS_BF16 or TTS_FP8_E4M3 */
     void *k_pool;
     void *v_pool;
-    float *k_scale;         /* TTS_FP8_E4M3 only */
-    float *v_scale;         /* TTS_FP8_E4M3 only */
 } tts_kv_cache;
 
 /* ------------------------------------------------------------ block pool */

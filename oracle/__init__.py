@@ -82,10 +82,10 @@ class Oracle:
         L.orc_e4m3_encode_n.restype = None
         L.orc_e4m3_decode_n.argtypes = [_vp, ctypes.c_size_t, _vp]
         L.orc_e4m3_decode_n.restype = None
-        L.orc_kv_append_fp8.argtypes = ([ctypes.c_int] * 3 + [_vp] * 4 + [_vp, ctypes.c_int, _vp]
+        L.orc_kv_append_fp8.argtypes = ([ctypes.c_int] * 3 + [_vp, _vp, ctypes.c_int, _vp]
                                         + [ctypes.c_int] * 2 + [_vp, _vp])
         L.orc_kv_append_fp8.restype = ctypes.c_int
-        L.orc_decode_attn_fp8.argtypes = ([ctypes.c_int] * 3 + [_vp] * 4 + [_vp, ctypes.c_int, _vp]
+        L.orc_decode_attn_fp8.argtypes = ([ctypes.c_int] * 3 + [_vp, _vp, ctypes.c_int, _vp]
                                           + [ctypes.c_int] * 3 + [ctypes.c_double, ctypes.c_int, _vp, _vp])
         L.orc_decode_attn_fp8.restype = ctypes.c_int
         self.lib = L
@@ -158,38 +158,32 @@ class Oracle:
         self.lib.orc_e4m3_decode_n(_ptr(c), c.size, _ptr(out))
         return out
 
-    def kv_append_fp8(self, k_codes, v_codes, k_scale, v_scale, block_table, ctx_before, k_new, v_new):
-        """FP8 append into copies of the cache arrays (k_codes [nb][Hkv][16][D],
-        v_codes [nb][Hkv][D][16] uint8, scales [nb][Hkv][16] float32; k_new /
-        v_new bf16 bits [B][q_len][Hkv][D]); returns the four arrays."""
-        kc, vc = np.array(k_codes, dtype=np.uint8, copy=True, order="C"), np.array(v_codes, dtype=np.uint8, copy=True, order="C")
-        ks, vs = np.array(k_scale, dtype=np.float32, copy=True, order="C"), np.array(v_scale, dtype=np.float32, copy=True, order="C")
-        num_blocks, Hkv, blk, D = kc.shape
-        assert blk == 16 and vc.shape == (num_blocks, Hkv, D, 16) and ks.shape == (num_blocks, Hkv, 16)
-        B, q_len = k_new.shape[:2]
+    def kv_append_fp8(self, tiles, block_table, ctx_before, k_new, v_new):
+        """FP8 append into a copy of the tile array (uint8 [num_blocks][Hkv][4224],
+        the layout of orc_kv_append_fp8); k_new / v_new bf16 bits
+        [B][q_len][Hkv][128].  Returns the new tiles."""
+        t = np.array(tiles, dtype=np.uint8, copy=True, order="C")
+        num_blocks, Hkv, nbytes = t.shape
+        assert nbytes == 4224
+        B, q_len, _, D = k_new.shape
         table = np.ascontiguousarray(block_table, dtype=np.int32)
         cb = np.ascontiguousarray(ctx_before, dtype=np.int32)
-        rc = self.lib.orc_kv_append_fp8(num_blocks, Hkv, D, _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs),
-                                        _ptr(table), table.shape[1], _ptr(cb), B, q_len,
-                                        _ptr(np.ascontiguousarray(k_new, dtype=np.uint16)),
+        rc = self.lib.orc_kv_append_fp8(num_blocks, Hkv, D, _ptr(t), _ptr(table), table.shape[1], _ptr(cb), B,
+                                        q_len, _ptr(np.ascontiguousarray(k_new, dtype=np.uint16)),
                                         _ptr(np.ascontiguousarray(v_new, dtype=np.uint16)))
         if rc != 0:
             raise ValueError("oracle kv_append_fp8: slot outside the block table or pool")
-        return kc, vc, ks, vs
+        return t
 
-    def decode_attn_fp8(self, k_codes, v_codes, k_scale, v_scale, block_table, ctx_lens, q, scale,
-                        causal=False):
-        """out[B][q_len][Hq][D] float64 over an FP8 cache; q bf16 bits."""
-        num_blocks, Hkv, blk, D = k_codes.shape
-        B, q_len, Hq, Dq = q.shape
-        assert Dq == D and blk == 16 and Hq % Hkv == 0
+    def decode_attn_fp8(self, tiles, block_table, ctx_lens, q, scale, causal=False):
+        """out[B][q_len][Hq][128] float64 over an FP8 tile array; q bf16 bits."""
+        num_blocks, Hkv, nbytes = tiles.shape
+        B, q_len, Hq, D = q.shape
+        assert nbytes == 4224 and D == 128 and Hq % Hkv == 0
         table = np.ascontiguousarray(block_table, dtype=np.int32)
         L = np.ascontiguousarray(ctx_lens, dtype=np.int32)
         out = np.zeros((B, q_len, Hq, D), dtype=np.float64)
-        rc = self.lib.orc_decode_attn_fp8(num_blocks, Hkv, D, _ptr(np.ascontiguousarray(k_codes, dtype=np.uint8)),
-                                          _ptr(np.ascontiguousarray(v_codes, dtype=np.uint8)),
-                                          _ptr(np.ascontiguousarray(k_scale, dtype=np.float32)),
-                                          _ptr(np.ascontiguousarray(v_scale, dtype=np.float32)),
+        rc = self.lib.orc_decode_attn_fp8(num_blocks, Hkv, D, _ptr(np.ascontiguousarray(tiles, dtype=np.uint8)),
                                           _ptr(table), table.shape[1], _ptr(L), B, q_len, Hq, float(scale),
                                           int(bool(causal)), _ptr(np.ascontiguousarray(q, dtype=np.uint16)),
                                           _ptr(out))

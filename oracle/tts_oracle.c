@@ -255,76 +255,85 @@ static int v_pos(int s) { return 4 * ((s % 8) / 2) + (s % 2) + 2 * (s / 8); }
 
 /* Quantises one row of n values: scale = max|x| / 448 (fp32), codes =
  * E4M3(x / scale) computed in fp32; an all-zero row gets scale 0 and codes 0. */
-static void quantize_row(const float *x, int n, uint8_t *codes, int code_stride, float *scale_out) {
+static float quantize_row(const float *x, int n, uint8_t *codes) {
     float amax = 0.0f;
     for (int d = 0; d < n; ++d) {
         const float a = fabsf(x[d]);
         if (a > amax) amax = a;
     }
     const float scale = amax / 448.0f;
-    for (int d = 0; d < n; ++d) codes[(size_t)d * code_stride] = scale > 0.0f ? orc_e4m3_encode(x[d] / scale) : 0;
-    *scale_out = scale;
+    for (int d = 0; d < n; ++d) codes[d] = scale > 0.0f ? orc_e4m3_encode(x[d] / scale) : 0;
+    return scale;
 }
+
+/* Storage of one (block, KV head) tile of an FP8 cache (D = 128), 4224 bytes:
+ * key codes, token slot s and dimension d at byte 128 s + 16 ((d / 16) xor
+ * (s % 8)) + d % 16; value codes, dimension d and slot s at byte
+ * 2048 + 16 d + v_pos(s); the 16 key scales (fp32) at byte 4096, the 16 value
+ * scales at byte 4160.  (A storage-order choice of the cache layout.) */
+#define ORC_FP8_TILE 4224
+static size_t k_byte(int s, int d) { return (size_t)(128 * s + 16 * ((d / 16) ^ (s % 8)) + d % 16); }
+static size_t v_byte(int s, int d) { return (size_t)(2048 + 16 * d + v_pos(s)); }
 
 /* KV append into an FP8 cache (the KV cache in FP8: "Optimizing Streaming
  * Text-to-Speech Models for Sub-50 Millisecond Latency", section
  * "Engine-Level Optimizations with TensorRT-LLM").  Each new key and value row
- * (one token, one KV head: D bf16 values) is one quantisation block with its
- * own fp32 scale.  Layouts: k_codes [num_blocks][Hkv][16][D] (token-major),
- * v_codes [num_blocks][Hkv][D][16] (dimension-major, token slot s at byte
- * v_pos(s) of the dimension's 16), k_scale and v_scale [num_blocks][Hkv][16].
- * Returns 0, or -1 if a slot falls outside the table or the pool. */
-int orc_kv_append_fp8(int num_blocks, int Hkv, int D, uint8_t *k_codes, uint8_t *v_codes,
-                      float *k_scale, float *v_scale, const int32_t *block_table, int max_blocks,
-                      const int32_t *ctx_before, int B, int q_len, const uint16_t *k_new,
+ * (one token, one KV head: D = 128 bf16 values) is one quantisation block
+ * with its own fp32 scale, stored in the tile layout above; tiles
+ * [num_blocks][Hkv][4224 bytes].  Returns 0, or -1 if a slot falls outside
+ * the table or the pool, or D != 128. */
+int orc_kv_append_fp8(int num_blocks, int Hkv, int D, uint8_t *tiles, const int32_t *block_table,
+                      int max_blocks, const int32_t *ctx_before, int B, int q_len, const uint16_t *k_new,
                       const uint16_t *v_new) {
-    float *row = (float *)malloc(sizeof(float) * (size_t)D);
-    if (!row) return -1;
+    if (D != 128) return -1;
+    float row[128];
+    uint8_t codes[128];
     for (int b = 0; b < B; ++b) {
         for (int j = 0; j < q_len; ++j) {
             const int s = ctx_before[b] + j;
-            if (s < 0 || s / ORC_BLOCK >= max_blocks) { free(row); return -1; }
-            const int blk = block_table[(size_t)b * max_blocks + s / ORC_BLOCK];
-            if (blk < 0 || blk >= num_blocks) { free(row); return -1; }
+            const int logical = s / ORC_BLOCK;
+            if (s < 0 || logical >= max_blocks) return -1;
+            const int blk = block_table[(size_t)b * max_blocks + logical];
+            if (blk < 0 || blk >= num_blocks) return -1;
             const int slot = s % ORC_BLOCK;
             for (int g = 0; g < Hkv; ++g) {
                 const size_t src = (((size_t)b * q_len + j) * Hkv + g) * D;
-                const size_t tile = (size_t)blk * Hkv + g;
+                uint8_t *tile = tiles + ((size_t)blk * Hkv + g) * ORC_FP8_TILE;
                 for (int d = 0; d < D; ++d) row[d] = (float)load_elem(k_new, src + d, 1);
-                quantize_row(row, D, k_codes + (tile * ORC_BLOCK + slot) * D, 1, k_scale + tile * ORC_BLOCK + slot);
+                const float ks = quantize_row(row, D, codes);
+                for (int d = 0; d < D; ++d) tile[k_byte(slot, d)] = codes[d];
+                memcpy(tile + 4096 + 4 * slot, &ks, 4);
                 for (int d = 0; d < D; ++d) row[d] = (float)load_elem(v_new, src + d, 1);
-                quantize_row(row, D, v_codes + tile * ORC_BLOCK * D + v_pos(slot), ORC_BLOCK,
-                             v_scale + tile * ORC_BLOCK + slot);
+                const float vs = quantize_row(row, D, codes);
+                for (int d = 0; d < D; ++d) tile[v_byte(slot, d)] = codes[d];
+                memcpy(tile + 4160 + 4 * slot, &vs, 4);
             }
         }
     }
-    free(row);
     return 0;
 }
 
 typedef struct {
-    int Hkv, D;
-    const uint8_t *k_codes, *v_codes;
-    const float *k_scale, *v_scale;
+    int Hkv;
+    const uint8_t *tiles;
 } orc_fp8_pool;
 
 static double fp8_kv(const void *ctx, int is_v, int blk, int g, int slot, int d) {
     const orc_fp8_pool *p = (const orc_fp8_pool *)ctx;
-    const size_t tile = (size_t)blk * p->Hkv + g;
-    if (is_v)
-        return (double)orc_e4m3_decode(p->v_codes[(tile * p->D + d) * ORC_BLOCK + v_pos(slot)]) *
-               (double)p->v_scale[tile * ORC_BLOCK + slot];
-    return (double)orc_e4m3_decode(p->k_codes[(tile * ORC_BLOCK + slot) * p->D + d]) *
-           (double)p->k_scale[tile * ORC_BLOCK + slot];
+    const uint8_t *tile = p->tiles + ((size_t)blk * p->Hkv + g) * ORC_FP8_TILE;
+    float sc;
+    memcpy(&sc, tile + (is_v ? 4160 : 4096) + 4 * slot, 4);
+    const uint8_t code = tile[is_v ? v_byte(slot, d) : k_byte(slot, d)];
+    return (double)orc_e4m3_decode(code) * (double)sc;
 }
 
 /* Attention over an FP8 cache: orc_decode_attn on the dequantised rows
- * (code value times the row's scale); q is bf16. */
-int orc_decode_attn_fp8(int num_blocks, int Hkv, int D, const uint8_t *k_codes, const uint8_t *v_codes,
-                        const float *k_scale, const float *v_scale, const int32_t *block_table,
+ * (code value times the row's scale); q is bf16; D = 128. */
+int orc_decode_attn_fp8(int num_blocks, int Hkv, int D, const uint8_t *tiles, const int32_t *block_table,
                         int max_blocks, const int32_t *ctx_lens, int B, int q_len, int Hq, double scale,
                         int causal, const uint16_t *q, double *out) {
-    const orc_fp8_pool pool = {Hkv, D, k_codes, v_codes, k_scale, v_scale};
+    if (D != 128) return -1;
+    const orc_fp8_pool pool = {Hkv, tiles};
     return attend(num_blocks, Hkv, D, fp8_kv, &pool, block_table, max_blocks, ctx_lens, B, q_len, Hq,
                   scale, causal, q, 1, out);
 }

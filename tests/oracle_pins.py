@@ -454,51 +454,62 @@ def check_e4m3_encode_matches_torch(o):
     assert np.array_equal(o.e4m3_encode(-big), np.full(5, 0xFE, np.uint8))
 
 
-def v_pos(s):
-    """Byte of token slot s within a dimension's 16 value codes (cache layout)."""
-    order = [0, 1, 8, 9, 2, 3, 10, 11, 4, 5, 12, 13, 6, 7, 14, 15]
-    return order.index(s)
+V_ORDER = [0, 1, 8, 9, 2, 3, 10, 11, 4, 5, 12, 13, 6, 7, 14, 15]  # token slot at each value byte
 
 
-def fp8_case(seed, B, Hkv, D, ctx_lens, permute=True):
-    """Random FP8 cache arrays for every slot (no NaN codes) and the table."""
+def fp8_tile_views(tiles):
+    """Key codes [nb][Hkv][16][128], value codes [nb][Hkv][128][16] (natural slot
+    order), key and value scales [nb][Hkv][16] read out of FP8 tiles, following
+    the layout as the header defines it."""
+    s = np.arange(16)[:, None]
+    d = np.arange(128)[None, :]
+    kb = 128 * s + 16 * ((d // 16) ^ (s % 8)) + d % 16               # [16][128]
+    vpos = np.array([V_ORDER.index(x) for x in range(16)])
+    vb = 2048 + 16 * d.T + vpos[None, :]                               # [128][16]
+    k = tiles[:, :, kb]
+    v = tiles[:, :, vb]
+    ks = np.ascontiguousarray(tiles[:, :, 4096:4160]).view(np.float32)
+    vs = np.ascontiguousarray(tiles[:, :, 4160:4224]).view(np.float32)
+    return k, v, ks, vs
+
+
+def fp8_case(seed, B, Hkv, ctx_lens, permute=True):
+    """Random FP8 tiles for every slot (no NaN codes) and the table."""
     rng = np.random.default_rng(seed)
     L = np.asarray(ctx_lens, dtype=np.int32)
     max_blocks = int(-(-L.max() // wl.BLOCK))
     num_blocks, table = wl.layout_blocks(L, max_blocks, spare=2, permute=permute, rng=rng)
     codes = np.concatenate([np.arange(0x7F), np.arange(0x80, 0xFF)]).astype(np.uint8)
-    kc = rng.choice(codes, size=(num_blocks, Hkv, wl.BLOCK, D))
-    vc = rng.choice(codes, size=(num_blocks, Hkv, D, wl.BLOCK))
-    ks = rng.uniform(1e-3, 2e-2, (num_blocks, Hkv, wl.BLOCK)).astype(np.float32)
-    vs = rng.uniform(1e-3, 2e-2, (num_blocks, Hkv, wl.BLOCK)).astype(np.float32)
-    return dict(k_codes=kc, v_codes=vc, k_scale=ks, v_scale=vs, block_table=table, ctx_lens=L, rng=rng)
+    tiles = rng.choice(codes, size=(num_blocks, Hkv, 4224)).astype(np.uint8)
+    sc = rng.uniform(1e-3, 2e-2, (num_blocks, Hkv, 32)).astype(np.float32)
+    tiles[:, :, 4096:] = sc.view(np.uint8).reshape(num_blocks, Hkv, 128)
+    return dict(tiles=tiles, block_table=table, ctx_lens=L, rng=rng)
 
 
 def check_kv_append_fp8_quantization(o):
     """Each appended row: scale = max|x| / 448 in fp32, codes = torch's E4M3 of
-    x / scale, K token-major and V dimension-major at the row's slot; the
-    largest entry maps to +-448; the rest of the cache is untouched."""
+    x / scale, keys and values at the row's slot of the tile layout; the largest
+    entry maps to +-448; every other byte of the tiles is untouched."""
     import torch
-    B, Hkv, D, q_len = 3, 2, 16, 2
-    c = fp8_case(21, B, Hkv, D, [5, 17, 32])
+    B, Hkv, D, q_len = 3, 2, 128, 2
+    c = fp8_case(21, B, Hkv, [5, 17, 32])
     before = (c["ctx_lens"] - q_len).astype(np.int32)
     rng = c["rng"]
     k_new = wl.f32_to_bf16(rng.standard_normal((B, q_len, Hkv, D), dtype=np.float32))
     v_new = wl.f32_to_bf16(3 * rng.standard_normal((B, q_len, Hkv, D), dtype=np.float32))
     v_new[0, 0, 0] = 0  # an all-zero row: scale 0, codes 0
-    kc, vc, ks, vs = o.kv_append_fp8(c["k_codes"], c["v_codes"], c["k_scale"], c["v_scale"],
-                                     c["block_table"], before, k_new, v_new)
-    touched = np.zeros(c["k_scale"].shape, dtype=bool)
-    vtouched = np.zeros(c["k_scale"].shape, dtype=bool)
+    out = o.kv_append_fp8(c["tiles"], c["block_table"], before, k_new, v_new)
+    kc, vc, ks, vs = fp8_tile_views(out)
+    kc0, vc0, ks0, vs0 = fp8_tile_views(c["tiles"])
+    touched = np.zeros(ks.shape, dtype=bool)
     for b in range(B):
         for j in range(q_len):
             s = before[b] + j
             blk, slot = c["block_table"][b, s // wl.BLOCK], s % wl.BLOCK
             for g in range(Hkv):
                 touched[blk, g, slot] = True
-                vtouched[blk, g, v_pos(slot)] = True
                 for x_bits, codes, scale in ((k_new[b, j, g], kc[blk, g, slot, :], ks[blk, g, slot]),
-                                             (v_new[b, j, g], vc[blk, g, :, v_pos(slot)], vs[blk, g, slot])):
+                                             (v_new[b, j, g], vc[blk, g, :, slot], vs[blk, g, slot])):
                     x = wl.bf16_to_f32(x_bits)
                     amax = np.float32(np.abs(x).max())
                     assert scale == np.float32(amax / np.float32(448.0))
@@ -512,12 +523,14 @@ def check_kv_append_fp8_quantization(o):
                     normal = np.abs(x) >= scale * 2.0 ** -6
                     assert np.all(np.abs(deq - x)[normal] <= 2.0 ** -4 * np.abs(x)[normal])
                     assert np.all(np.abs(deq - x)[~normal] <= 2.0 ** -10 * scale)
-    assert np.array_equal(ks[~touched], c["k_scale"][~touched])
-    assert np.array_equal(vs[~touched], c["v_scale"][~touched])
-    kt = np.broadcast_to(touched[..., None], kc.shape)
-    assert np.array_equal(kc[~kt], c["k_codes"][~kt])
-    vt = np.broadcast_to(vtouched[:, :, None, :], vc.shape)
-    assert np.array_equal(vc[~vt], c["v_codes"][~vt])
+    assert np.array_equal(ks[~touched], ks0[~touched]) and np.array_equal(vs[~touched], vs0[~touched])
+    assert np.array_equal(kc[~touched], kc0[~touched])
+    assert np.array_equal(vc.transpose(0, 1, 3, 2)[~touched], vc0.transpose(0, 1, 3, 2)[~touched])
+    # the views cover every byte of a tile exactly once
+    idx = np.arange(4224, dtype=np.int64)[None, None, :]
+    kb, vb, ksb, vsb = fp8_tile_views(np.broadcast_to(idx, (1, 1, 4224)).astype(np.int64))[:2] + (None, None)
+    covered = np.concatenate([kb.ravel(), vb.ravel(), np.arange(4096, 4224)])
+    assert np.array_equal(np.sort(covered), np.arange(4224))
 
 
 def check_attn_fp8_matches_sdpa(o):
@@ -526,21 +539,21 @@ def check_attn_fp8_matches_sdpa(o):
     import torch
     import torch.nn.functional as F
     tab = torch.from_numpy(_torch_e4m3_table().astype(np.float64))
-    for (Hq, Hkv, D, q_len, causal, L, seed) in [(4, 2, 32, 1, False, [17, 1, 40], 31),
-                                                  (8, 2, 16, 5, True, [5, 33, 20], 32)]:
-        c = fp8_case(seed, len(L), Hkv, D, L)
+    for (Hq, Hkv, q_len, causal, L, seed) in [(4, 2, 1, False, [17, 1, 40], 31), (8, 2, 5, True, [5, 33, 20], 32)]:
+        D = 128
+        c = fp8_case(seed, len(L), Hkv, L)
+        kc, vc, ks, vs = fp8_tile_views(c["tiles"])
         q = wl.f32_to_bf16(c["rng"].standard_normal((len(L), q_len, Hq, D), dtype=np.float32))
         scale = 1.0 / math.sqrt(D)
-        out = o.decode_attn_fp8(c["k_codes"], c["v_codes"], c["k_scale"], c["v_scale"], c["block_table"],
-                                c["ctx_lens"], q, scale, causal)
+        out = o.decode_attn_fp8(c["tiles"], c["block_table"], c["ctx_lens"], q, scale, causal)
         g = Hq // Hkv
         for b, Lb in enumerate(L):
             t = np.arange(Lb)
             blocks, slots = c["block_table"][b, t // wl.BLOCK], t % wl.BLOCK
-            kcod = torch.from_numpy(c["k_codes"][blocks, :, slots, :].astype(np.int64))          # [L][Hkv][D]
-            vcod = torch.from_numpy(c["v_codes"][blocks, :, :, [v_pos(x) for x in slots]].astype(np.int64))
-            k = tab[kcod] * torch.from_numpy(c["k_scale"][blocks, :, slots].astype(np.float64))[..., None]
-            v = tab[vcod] * torch.from_numpy(c["v_scale"][blocks, :, slots].astype(np.float64))[..., None]
+            k = tab[torch.from_numpy(kc[blocks, :, slots, :].astype(np.int64))] * \
+                torch.from_numpy(ks[blocks, :, slots].astype(np.float64))[..., None]
+            v = tab[torch.from_numpy(vc[blocks, :, :, slots].astype(np.int64))] * \
+                torch.from_numpy(vs[blocks, :, slots].astype(np.float64))[..., None]
             k = k.permute(1, 0, 2).repeat_interleave(g, dim=0)
             v = v.permute(1, 0, 2).repeat_interleave(g, dim=0)
             qq = torch.from_numpy(wl.bf16_to_f32(q[b]).astype(np.float64)).permute(1, 0, 2)

@@ -28,13 +28,12 @@ def bd():
 
 
 def fp8_cache_for(orc, inp):
-    """The context cached before this step, quantised into an FP8 cache by the oracle."""
+    """The context cached before this step, quantised into FP8 tiles by the
+    oracle; every other code is NaN (0x7F) and every other scale NaN."""
     w = inp["workload"]
     nb, table = inp["num_blocks"], inp["block_table"]
-    kc = np.full((nb, w.Hkv, 16, w.D), 0x7F, np.uint8)
-    vc = np.full((nb, w.Hkv, w.D, 16), 0x7F, np.uint8)
-    ks = np.full((nb, w.Hkv, 16), np.nan, np.float32)
-    vs = np.full((nb, w.Hkv, 16), np.nan, np.float32)
+    tiles = np.full((nb, w.Hkv, 4224), 0x7F, np.uint8)
+    tiles[:, :, 4096:] = np.full(32, np.nan, np.float32).view(np.uint8)
     for b in range(w.B):
         n = int(inp["ctx_before"][b])
         if n == 0:
@@ -43,12 +42,12 @@ def fp8_cache_for(orc, inp):
         blocks, slots = table[b, t // wl.BLOCK], t % wl.BLOCK
         krows = np.ascontiguousarray(inp["k_pool"][blocks, :, slots, :])[None]
         vrows = np.ascontiguousarray(inp["v_pool"][blocks, :, slots, :])[None]
-        kc, vc, ks, vs = orc.kv_append_fp8(kc, vc, ks, vs, table[b:b + 1], np.zeros(1, np.int32), krows, vrows)
-    return kc, vc, ks, vs
+        tiles = orc.kv_append_fp8(tiles, table[b:b + 1], np.zeros(1, np.int32), krows, vrows)
+    return tiles
 
 
-def upload_cache(bd, kc, vc, ks, vs):
-    return bd.KVCache(dev(kc), dev(vc), dev(ks), dev(vs))
+def upload_cache(bd, tiles):
+    return bd.KVCache(dev(tiles))
 
 
 CASES = [
@@ -73,16 +72,13 @@ def test_fp8_append_matches_oracle_bytes(orc, bd, case):
     k_new, v_new = inp["k_new"].copy(), inp["v_new"].copy()
     k_new[0, 0, 0] = 0                                   # an all-zero row: scale 0, codes 0
     v_new[-1, -1, -1, :4] = wl.f32_to_bf16(np.array([3e38, -3e38, 1e-30, 0], np.float32))
-    kc, vc, ks, vs = fp8_cache_for(orc, inp)
-    ref = orc.kv_append_fp8(kc, vc, ks, vs, inp["block_table"], inp["ctx_before"], k_new, v_new)
-    cache = upload_cache(bd, kc, vc, ks, vs)
+    tiles = fp8_cache_for(orc, inp)
+    ref = orc.kv_append_fp8(tiles, inp["block_table"], inp["ctx_before"], k_new, v_new)
+    cache = upload_cache(bd, tiles)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     bd.tts_kv_append(cache, dev(inp["block_table"]), dev(inp["ctx_before"]), dev(k_new), dev(v_new), err=err)
     torch.cuda.synchronize()
-    assert np.array_equal(host(cache.k_pool), ref[0])
-    assert np.array_equal(host(cache.v_pool), ref[1])
-    assert np.array_equal(host(cache.k_scale).view(np.uint32), ref[2].view(np.uint32))
-    assert np.array_equal(host(cache.v_scale).view(np.uint32), ref[3].view(np.uint32))
+    assert np.array_equal(host(cache.k_pool), ref)
     assert int(err.item()) == 0
 
 
@@ -90,9 +86,9 @@ def test_fp8_append_matches_oracle_bytes(orc, bd, case):
 def test_fp8_attention_matches_oracle(orc, bd, case):
     inp = _inputs(*case, seed=600 + CASES.index(case))
     w = inp["workload"]
-    kc, vc, ks, vs = orc.kv_append_fp8(*fp8_cache_for(orc, inp), inp["block_table"], inp["ctx_before"],
-                                       inp["k_new"], inp["v_new"])
-    cache = upload_cache(bd, kc, vc, ks, vs)
+    tiles = orc.kv_append_fp8(fp8_cache_for(orc, inp), inp["block_table"], inp["ctx_before"], inp["k_new"],
+                              inp["v_new"])
+    cache = upload_cache(bd, tiles)
     out = torch.empty((w.B, w.q_len, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
     ws = torch.zeros(bd.tts_decode_attn_workspace_size(w.B, w.q_len, w.Hq, w.Hkv, w.D, w.ctx_hi),
                      dtype=torch.uint8, device="cuda")
@@ -102,7 +98,7 @@ def test_fp8_attention_matches_oracle(orc, bd, case):
         bd.tts_decode_attn(cache, dev(inp["block_table"]), dev(inp["ctx_lens"]), w.ctx_hi, dev(inp["q"]), out, ws,
                            scale, w.causal, err=err)
         torch.cuda.synchronize()
-        ref = orc.decode_attn_fp8(kc, vc, ks, vs, inp["block_table"], inp["ctx_lens"], inp["q"], scale, w.causal)
+        ref = orc.decode_attn_fp8(tiles, inp["block_table"], inp["ctx_lens"], inp["q"], scale, w.causal)
         got = wl.bf16_to_f32(host(out)).astype(np.float64)
         assert np.isfinite(got).all()
         bad, emax, rel = attn_errors(got, ref)
@@ -117,16 +113,16 @@ def test_fp8_decode_step_ids(orc, bd):
     from decode_step_gb300.step import DecodeStep, GraphedStep
     w = wl.custom(3, B=16, ctx_lo=30, ctx_hi=400, permute_table=True)
     inp = wl.make_inputs(w, seed=777, with_verify=False)
-    kc, vc, ks, vs = fp8_cache_for(orc, inp)
-    cache = upload_cache(bd, kc, vc, ks, vs)
+    tiles = fp8_cache_for(orc, inp)
+    cache = upload_cache(bd, tiles)
     step = DecodeStep(cache, dev(inp["W"]), w.Hq, w.B, w.ctx_hi)
     table, cb, cl = dev(inp["block_table"]), dev(inp["ctx_before"]), dev(inp["ctx_lens"])
     q, kn, vn = dev(inp["q"]), dev(inp["k_new"]), dev(inp["v_new"])
     ids = step(table, cb, cl, q, kn, vn).clone()
     torch.cuda.synchronize()
-    ref_cache = orc.kv_append_fp8(kc, vc, ks, vs, inp["block_table"], inp["ctx_before"], inp["k_new"], inp["v_new"])
-    assert np.array_equal(host(cache.k_pool), ref_cache[0]) and np.array_equal(host(cache.v_pool), ref_cache[1])
-    attn = orc.decode_attn_fp8(*ref_cache, inp["block_table"], inp["ctx_lens"], inp["q"], inp["scale"])
+    ref_tiles = orc.kv_append_fp8(tiles, inp["block_table"], inp["ctx_before"], inp["k_new"], inp["v_new"])
+    assert np.array_equal(host(cache.k_pool), ref_tiles)
+    attn = orc.decode_attn_fp8(ref_tiles, inp["block_table"], inp["ctx_lens"], inp["q"], inp["scale"])
     h = wl.f32_to_bf16(attn.reshape(w.R, w.Hq * w.D).astype(np.float32))
     ref = orc.head_select(h, inp["W"], "argmax")
     hard, ties = compare_ids(host(ids), ref)

@@ -128,8 +128,7 @@ def test_struct_layouts_match_header(tmp_path):
         pytest.skip("no C compiler")
     fields = [f for f, _ in _lib.StepGraphDesc._fields_]
     src = ["#include <stdio.h>", "#include <stddef.h>", '#include "tts_decode.h"', "int main(void) {",
-           'printf("%zu %zu %zu %zu\\n", sizeof(tts_kv_cache), offsetof(tts_kv_cache, v_pool), '
-           'offsetof(tts_kv_cache, k_scale), offsetof(tts_kv_cache, v_scale));',
+           'printf("%zu %zu\\n", sizeof(tts_kv_cache), offsetof(tts_kv_cache, v_pool));',
            'printf("%zu\\n", sizeof(tts_step_graph_desc));']
     src += [f'printf("%zu\\n", offsetof(tts_step_graph_desc, {f}));' for f in fields]
     src += ["return 0; }"]
@@ -139,9 +138,9 @@ def test_struct_layouts_match_header(tmp_path):
     out = subprocess.run([str(tmp_path / "lay")], capture_output=True, text=True, check=True).stdout.split()
     vals = [int(x) for x in out]
     K = _lib.KVCacheDesc
-    assert vals[:4] == [ctypes.sizeof(K), K.v_pool.offset, K.k_scale.offset, K.v_scale.offset]
-    assert vals[4] == ctypes.sizeof(_lib.StepGraphDesc)
-    assert vals[5:] == [getattr(_lib.StepGraphDesc, f).offset for f in fields]
+    assert vals[:2] == [ctypes.sizeof(K), K.v_pool.offset]
+    assert vals[2] == ctypes.sizeof(_lib.StepGraphDesc)
+    assert vals[3:] == [getattr(_lib.StepGraphDesc, f).offset for f in fields]
 
 
 def test_step_graph_rejects_bad_descriptors(L):

@@ -34,8 +34,7 @@ MUTANTS = [
     ("append: slot offset", "+ s % ORC_BLOCK) * row;", "+ (s + 1) % ORC_BLOCK) * row;"),
     ("append: logical block", "s / ORC_BLOCK];\n            if (blk < 0 || blk >= num_blocks) return -1;",
      "(s + 1) / ORC_BLOCK];\n            if (blk < 0 || blk >= num_blocks) return -1;"),
-    ("fp8 append: logical block", "s / ORC_BLOCK];\n            if (blk < 0 || blk >= num_blocks) { free(row)",
-     "(s + 1) / ORC_BLOCK];\n            if (blk < 0 || blk >= num_blocks) { free(row)"),
+    ("fp8 append: logical block", "const int logical = s / ORC_BLOCK;", "const int logical = (s + 1) / ORC_BLOCK;"),
     ("attn: scale dropped", "s[t] = scale * dot;", "s[t] = dot;"),
     ("attn: GQA head mapping", "const int g = h / group;", "const int g = h % Hkv;"),
     ("attn: causal limit off by one", "causal ? L - q_len + j + 1 : L", "causal ? L - q_len + j + 2 : L"),
@@ -59,12 +58,11 @@ MUTANTS = [
     ("e4m3: largest finite code excluded", "for (int c = 0; c <= 0x7E; ++c)", "for (int c = 0; c < 0x7E; ++c)"),
     ("e4m3: subnormal exponent", "ldexp((double)m, -9)", "ldexp((double)m, -10)"),
     ("fp8 append: scale for a maximum of 240", "amax / 448.0f", "amax / 240.0f"),
-    ("fp8 append: values stored token-major", "v_codes + tile * ORC_BLOCK * D + v_pos(slot), ORC_BLOCK,",
-     "v_codes + (tile * ORC_BLOCK + slot) * D, 1,"),
-    ("fp8 append: value slots in natural order", "v_codes + tile * ORC_BLOCK * D + v_pos(slot), ORC_BLOCK,",
-     "v_codes + tile * ORC_BLOCK * D + slot, ORC_BLOCK,"),
-    ("fp8 attn: values scaled by the key scale", "(double)p->v_scale[tile * ORC_BLOCK + slot];",
-     "(double)p->k_scale[tile * ORC_BLOCK + slot];"),
+    ("fp8 append: value slots in natural order", "return (size_t)(2048 + 16 * d + v_pos(s));",
+     "return (size_t)(2048 + 16 * d + s);"),
+    ("fp8 append: keys unswizzled", "16 * ((d / 16) ^ (s % 8))", "16 * (d / 16)"),
+    ("fp8 attn: values scaled by the key scale", "memcpy(&sc, tile + (is_v ? 4160 : 4096) + 4 * slot, 4);",
+     "memcpy(&sc, tile + 4096 + 4 * slot, 4);"),
     ("verify: bonus always drawn", "if (!rejected && (flags & 1)) {", "if (!rejected) {"),
     ("verify: bonus from the last draft row",
      "target_logits + ((size_t)b * (K + 1) + K) * V;", "target_logits + ((size_t)b * (K + 1) + K - 1) * V;"),
