@@ -552,6 +552,13 @@ __device__ __forceinline__ void mma_bf16_16816(float *d, const uint32_t *a, uint
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+__device__ __forceinline__ void mma_f16_16816(float *d, const uint32_t *a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -594,11 +601,10 @@ constexpr int kKVStageBytes = 4 * kBoxBytes;
 constexpr int kFp8VOff = 2048;
 constexpr int kFp8ScaleOff = 4096;
 constexpr int kFp8KVStageBytes = kFp8ScaleOff + 2 * 64;
-// The codes enter the MMAs as bf16 values times 2^-120 (see e4m3x4_to_bf16);
-// queries are scaled by 2^16 (exact) to keep the products clear of fp32
-// denormals; S is rescaled by 2^104 and P by 2^120 with the row scales.
-constexpr float kFp8QBoost = 65536.0f;
-constexpr float kFp8SFix = 0x1p104f;
+// Key codes enter S = Q K^T as f16 (the hardware conversion is exact) with the
+// queries in f16; value codes enter O += P V as bf16 values times 2^-120 (see
+// e4m3x4_to_bf16, so that P, scaled by each token's value scale, keeps bf16's
+// exponent range), and P is rescaled by 2^120.
 constexpr float kFp8PFix = 0x1p120f;
 
 // Address of 16-byte chunk `ch` (0..15) of token row `t` (0..15) in a K or V
@@ -646,11 +652,26 @@ __device__ __forceinline__ void e4m3x4_to_bf16(uint32_t w, uint32_t &lo, uint32_
     hi = (b & 0x80008000u) | ((b & 0x7F007F00u) >> 4);
 }
 
-__device__ __forceinline__ uint32_t bf16x2_scaled(uint32_t w, float f) {
-    return pack_bf16x2(bf16_lo(w) * f, bf16_hi(w) * f);
+// Four E4M3 codes (bytes of w, low first) as two f16 pairs (codes 0, 1 and
+// 2, 3, low half first): exact.
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 
-template <bool kFp8>
+// A bf16 pair as an f16 pair (round to nearest; bf16 values outside f16's
+// range saturate to infinity, below it become f16 subnormals or zero).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(bf16_hi(w)), "f"(bf16_lo(w)));
+    return r;
+}
+
+template <bool kFp8, int kRing>
 __global__ void __launch_bounds__(kTcWarps * 32, kTcCtasPerSm)
 decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                       const AttnArgs a) {
@@ -661,7 +682,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base - raw);
     const int n_rows = a.group * a.q_len;  // <= 16
-    const int n_stages = a.stages;
+    constexpr int n_stages = kRing;  // ring depth (a.stages), a compile-time constant
     const TcSmem S = tc_smem(n_rows, a.B, n_stages, kFp8);
     constexpr int kQOff = kFp8 ? kFp8KVStageBytes : kKVStageBytes;  // query rows within a stage
     constexpr int kStageKV = kFp8 ? kFp8KVStageBytes : kKVStageBytes;
@@ -855,7 +876,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
                 qa[ks][3] = (rB < n_rows && !timed_out) ? *reinterpret_cast<const uint32_t *>(qrB + c1) : 0u;
                 if constexpr (kFp8) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) qa[ks][e] = bf16x2_scaled(qa[ks][e], kFp8QBoost);
+                    for (int e = 0; e < 4; ++e) qa[ks][e] = bf16x2_to_f16x2(qa[ks][e]);
                 }
             }
 #pragma unroll
@@ -889,8 +910,8 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             uint32_t b0, b1;
-                            e4m3x4_to_bf16(w[i], b0, b1);
-                            mma_bf16_16816(s[nt], qa[4 * kq + i], b0, b1);
+                            e4m3x4_to_f16(w[i], b0, b1);
+                            mma_f16_16816(s[nt], qa[4 * kq + i], b0, b1);
                         }
                     }
                 }
@@ -918,7 +939,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
                 for (int e = 0; e < 2; ++e) {
                     const int tok = base_tok + 8 * nt + 2 * ft + e;
                     float f = a.qscale;
-                    if constexpr (kFp8) f *= (e == 0 ? ksc[nt].x : ksc[nt].y) * kFp8SFix;
+                    if constexpr (kFp8) f *= (e == 0 ? ksc[nt].x : ksc[nt].y);
                     xa[2 * nt + e] = tok < limA ? s[nt][e] * f : -INFINITY;
                     xb[2 * nt + e] = tok < limB ? s[nt][2 + e] * f : -INFINITY;
                 }
@@ -1081,8 +1102,9 @@ int launch_simt(const AttnArgs &a, int nr, int ctas, LaunchOpts o) {
 
 template <bool kFp8>
 int launch_tc(const AttnArgs &a, const CUtensorMap &kmap, const CUtensorMap &vmap, int ctas, LaunchOpts o) {
+    static_assert(kTcMaxStages == 2, "ring depths instantiated: 1 and 2");
     const size_t smem = tc_smem(a.group * a.q_len, a.B, a.stages, kFp8).total;
-    auto kern = decode_attn_tc_kernel<kFp8>;
+    auto kern = a.stages == 2 ? decode_attn_tc_kernel<kFp8, 2> : decode_attn_tc_kernel<kFp8, 1>;
     if (!ensure_dynamic_smem(reinterpret_cast<const void *>(kern), static_cast<int>(smem)))
         return TTS_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
