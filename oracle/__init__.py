@@ -83,7 +83,9 @@ class Oracle:
         L.orc_e4m3_decode_n.argtypes = [_vp, ctypes.c_size_t, _vp]
         L.orc_e4m3_decode_n.restype = None
         L.orc_kv_append_fp8.argtypes = ([ctypes.c_int] * 3 + [_vp, _vp, ctypes.c_int, _vp]
-                                        + [ctypes.c_int] * 2 + [_vp, _vp])
+                                        + [ctypes.c_int] * 2 + [_vp, _vp, ctypes.c_int])
+        L.orc_rope_rows.argtypes = [_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, ctypes.c_double, _vp]
+        L.orc_rope_rows.restype = None
         L.orc_kv_append_fp8.restype = ctypes.c_int
         L.orc_decode_attn_fp8.argtypes = ([ctypes.c_int] * 3 + [_vp, _vp, ctypes.c_int, _vp]
                                           + [ctypes.c_int] * 3 + [ctypes.c_double, ctypes.c_int, _vp, _vp])
@@ -158,19 +160,35 @@ class Oracle:
         self.lib.orc_e4m3_decode_n(_ptr(c), c.size, _ptr(out))
         return out
 
+    def rope(self, x, pos, base=10000.0) -> np.ndarray:
+        """Rotary embedding of rows x [..., D] (bf16 bits or float32) at positions
+        pos (broadcast over x's leading dims); float32 result."""
+        is_bf16 = int(x.dtype == np.uint16)
+        xx = np.ascontiguousarray(x, dtype=np.uint16 if is_bf16 else np.float32)
+        D = xx.shape[-1]
+        rows = xx.size // D
+        p = np.ascontiguousarray(np.broadcast_to(np.asarray(pos, dtype=np.int32).reshape(
+            np.asarray(pos).shape + (1,) * (xx.ndim - 1 - np.asarray(pos).ndim)), xx.shape[:-1])).reshape(rows)
+        out = np.zeros(xx.shape, dtype=np.float32)
+        self.lib.orc_rope_rows(_ptr(xx), is_bf16, rows, D, _ptr(np.ascontiguousarray(p, dtype=np.int32)),
+                               float(base), _ptr(out))
+        return out
+
     def kv_append_fp8(self, tiles, block_table, ctx_before, k_new, v_new):
         """FP8 append into a copy of the tile array (uint8 [num_blocks][Hkv][4224],
-        the layout of orc_kv_append_fp8); k_new / v_new bf16 bits
-        [B][q_len][Hkv][128].  Returns the new tiles."""
+        the layout of orc_kv_append_fp8); k_new / v_new [B][q_len][Hkv][128] as
+        bf16 bits (uint16) or float32.  Returns the new tiles."""
         t = np.array(tiles, dtype=np.uint8, copy=True, order="C")
         num_blocks, Hkv, nbytes = t.shape
         assert nbytes == 4224
         B, q_len, _, D = k_new.shape
         table = np.ascontiguousarray(block_table, dtype=np.int32)
         cb = np.ascontiguousarray(ctx_before, dtype=np.int32)
+        is_bf16 = int(k_new.dtype == np.uint16)
+        assert v_new.dtype == k_new.dtype and k_new.dtype in (np.uint16, np.float32)
         rc = self.lib.orc_kv_append_fp8(num_blocks, Hkv, D, _ptr(t), _ptr(table), table.shape[1], _ptr(cb), B,
-                                        q_len, _ptr(np.ascontiguousarray(k_new, dtype=np.uint16)),
-                                        _ptr(np.ascontiguousarray(v_new, dtype=np.uint16)))
+                                        q_len, _ptr(np.ascontiguousarray(k_new)), _ptr(np.ascontiguousarray(v_new)),
+                                        is_bf16)
         if rc != 0:
             raise ValueError("oracle kv_append_fp8: slot outside the block table or pool")
         return t

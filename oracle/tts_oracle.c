@@ -209,6 +209,32 @@ int orc_decode_attn(int num_blocks, int Hkv, int D, int is_bf16,
                   scale, causal, q, is_bf16, out);
 }
 
+/* ------------------------------------------------------------------- RoPE */
+
+/* Rotary position embedding (Su et al., "RoFormer: Enhanced Transformer with
+ * Rotary Position Embedding", 2021, section 3.4, in the rotate-half
+ * arrangement that pairs dimension i with i + D/2), fused with the KV cache
+ * write on the pages ("Optimizing Streaming Text-to-Speech Models for Sub-50
+ * Millisecond Latency", section "Engine-Level Optimizations with
+ * TensorRT-LLM").  Row r (D values, bf16 or fp32 input) at position pos[r]:
+ * for i < D/2 with angle a = pos * base^(-2i/D),
+ *   out[i]       = x[i] cos a - x[i + D/2] sin a
+ *   out[i + D/2] = x[i + D/2] cos a + x[i] sin a,
+ * in double, rounded to float. */
+void orc_rope_rows(const void *x, int is_bf16, int rows, int D, const int32_t *pos, double base, float *out) {
+    const int h = D / 2;
+    for (int r = 0; r < rows; ++r) {
+        for (int i = 0; i < h; ++i) {
+            const double a = (double)pos[r] * pow(base, -2.0 * i / D);
+            const double c = cos(a), sn = sin(a);
+            const double x1 = load_elem(x, (size_t)r * D + i, is_bf16);
+            const double x2 = load_elem(x, (size_t)r * D + i + h, is_bf16);
+            out[(size_t)r * D + i] = (float)(x1 * c - x2 * sn);
+            out[(size_t)r * D + i + h] = (float)(x2 * c + x1 * sn);
+        }
+    }
+}
+
 /* ---------------------------------------------------------------- FP8 cache */
 
 /* FP8 E4M3 ("e4m3fn"): 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits,
@@ -278,13 +304,14 @@ static size_t v_byte(int s, int d) { return (size_t)(2048 + 16 * d + v_pos(s)); 
 /* KV append into an FP8 cache (the KV cache in FP8: "Optimizing Streaming
  * Text-to-Speech Models for Sub-50 Millisecond Latency", section
  * "Engine-Level Optimizations with TensorRT-LLM").  Each new key and value row
- * (one token, one KV head: D = 128 bf16 values) is one quantisation block
+ * (one token, one KV head: D = 128 values, bf16 or fp32 as rows_are_bf16
+ * says) is one quantisation block
  * with its own fp32 scale, stored in the tile layout above; tiles
  * [num_blocks][Hkv][4224 bytes].  Returns 0, or -1 if a slot falls outside
  * the table or the pool, or D != 128. */
 int orc_kv_append_fp8(int num_blocks, int Hkv, int D, uint8_t *tiles, const int32_t *block_table,
-                      int max_blocks, const int32_t *ctx_before, int B, int q_len, const uint16_t *k_new,
-                      const uint16_t *v_new) {
+                      int max_blocks, const int32_t *ctx_before, int B, int q_len, const void *k_new,
+                      const void *v_new, int rows_are_bf16) {
     if (D != 128) return -1;
     float row[128];
     uint8_t codes[128];
@@ -299,11 +326,11 @@ int orc_kv_append_fp8(int num_blocks, int Hkv, int D, uint8_t *tiles, const int3
             for (int g = 0; g < Hkv; ++g) {
                 const size_t src = (((size_t)b * q_len + j) * Hkv + g) * D;
                 uint8_t *tile = tiles + ((size_t)blk * Hkv + g) * ORC_FP8_TILE;
-                for (int d = 0; d < D; ++d) row[d] = (float)load_elem(k_new, src + d, 1);
+                for (int d = 0; d < D; ++d) row[d] = (float)load_elem(k_new, src + d, rows_are_bf16);
                 const float ks = quantize_row(row, D, codes);
                 for (int d = 0; d < D; ++d) tile[k_byte(slot, d)] = codes[d];
                 memcpy(tile + 4096 + 4 * slot, &ks, 4);
-                for (int d = 0; d < D; ++d) row[d] = (float)load_elem(v_new, src + d, 1);
+                for (int d = 0; d < D; ++d) row[d] = (float)load_elem(v_new, src + d, rows_are_bf16);
                 const float vs = quantize_row(row, D, codes);
                 for (int d = 0; d < D; ++d) tile[v_byte(slot, d)] = codes[d];
                 memcpy(tile + 4160 + 4 * slot, &vs, 4);

@@ -565,4 +565,65 @@ def check_attn_fp8_matches_sdpa(o):
             assert err < 1e-10, f"fp8 attention vs SDPA: {err}"
 
 
+# --------------------------------------------------------------------- RoPE
+
+def check_rope_identity_at_position_zero(o):
+    """Position 0 rotates by angle 0 in every pair: the rows come back unchanged."""
+    x = np.random.default_rng(41).standard_normal((4, 128)).astype(np.float32)
+    assert np.array_equal(o.rope(x, np.zeros(4, np.int32)), x)
+    xb = wl.f32_to_bf16(x)
+    assert np.array_equal(o.rope(xb, np.zeros(4, np.int32)), wl.bf16_to_f32(xb))
+
+
+def check_rope_matches_complex_rotation(o):
+    """Rotate-half RoPE equals multiplying z_i = x_i + i x_(i+D/2) by
+    exp(i pos base^(-2i/D)) (numpy complex arithmetic, float64)."""
+    rng = np.random.default_rng(42)
+    for D, base in ((128, 10000.0), (64, 500000.0)):
+        x = rng.standard_normal((6, D)).astype(np.float32)
+        pos = np.array([0, 1, 7, 100, 2047, 4095], np.int32)
+        h = D // 2
+        z = x[:, :h].astype(np.float64) + 1j * x[:, h:].astype(np.float64)
+        theta = base ** (-2.0 * np.arange(h) / D)
+        zr = z * np.exp(1j * pos[:, None] * theta[None, :])
+        ref = np.concatenate([zr.real, zr.imag], axis=1)
+        got = o.rope(x, pos, base).astype(np.float64)
+        assert np.abs(got - ref).max() <= 4e-7 * max(1.0, np.abs(ref).max())
+
+
+def check_rope_relative_position(o):
+    """<rope(q, m), rope(k, n)> depends only on m - n: it equals <rope(q, m - n), k>."""
+    rng = np.random.default_rng(43)
+    q = rng.standard_normal((5, 128)).astype(np.float32)
+    k = rng.standard_normal((5, 128)).astype(np.float32)
+    m = np.array([10, 300, 4000, 17, 2], np.int32)
+    n = np.array([3, 299, 1, 17, 0], np.int32)
+    lhs = np.einsum("rd,rd->r", o.rope(q, m).astype(np.float64), o.rope(k, n).astype(np.float64))
+    rhs = np.einsum("rd,rd->r", o.rope(q, m - n).astype(np.float64), k.astype(np.float64))
+    assert np.abs(lhs - rhs).max() < 1e-4, np.abs(lhs - rhs).max()
+
+
+def check_rope_pairs_keep_their_norm(o):
+    """Each (i, i + D/2) pair is rotated, not scaled."""
+    rng = np.random.default_rng(44)
+    x = rng.standard_normal((3, 128)).astype(np.float32)
+    r = o.rope(x, np.array([5, 999, 3000], np.int32)).astype(np.float64)
+    n0 = np.hypot(x[:, :64].astype(np.float64), x[:, 64:].astype(np.float64))
+    n1 = np.hypot(r[:, :64], r[:, 64:])
+    assert np.abs(n1 - n0).max() < 1e-5
+
+
+def check_fp8_append_from_float_rows(o):
+    """FP8 rows given in float32 quantise the same way as bf16 rows holding the
+    same values."""
+    c = fp8_case(45, 2, 2, [3, 20])
+    rng = c["rng"]
+    kb = wl.f32_to_bf16(rng.standard_normal((2, 1, 2, 128), dtype=np.float32))
+    vb = wl.f32_to_bf16(rng.standard_normal((2, 1, 2, 128), dtype=np.float32))
+    before = (c["ctx_lens"] - 1).astype(np.int32)
+    a = o.kv_append_fp8(c["tiles"], c["block_table"], before, kb, vb)
+    b = o.kv_append_fp8(c["tiles"], c["block_table"], before, wl.bf16_to_f32(kb), wl.bf16_to_f32(vb))
+    assert np.array_equal(a, b)
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

@@ -54,6 +54,12 @@ MUTANTS = [
     ("verify: residual ignores the draft", "fmaxf(pt[v] - dp[v], 0.0f)", "pt[v]"),
     ("verify: does not stop at the first rejection", "rejected = 1;\n            break;", "rejected = 1;"),
     ("verify: temperature dropped", "row_probs(tl, V, T, pt);", "row_probs(tl, V, 1.0f, pt);"),
+    ("rope: rotation sign", "out[(size_t)r * D + i] = (float)(x1 * c - x2 * sn);",
+     "out[(size_t)r * D + i] = (float)(x1 * c + x2 * sn);"),
+    ("rope: frequency exponent", "pow(base, -2.0 * i / D)", "pow(base, -1.0 * i / D)"),
+    ("rope: pairs of neighbours", "const double x2 = load_elem(x, (size_t)r * D + i + h, is_bf16);",
+     "const double x2 = load_elem(x, (size_t)r * D + (i ^ 1), is_bf16);"),
+    ("rope: position off by one", "const double a = (double)pos[r] * pow", "const double a = (double)(pos[r] + 1) * pow"),
     ("e4m3: ties to the later code", "(err == best_err && (c & 1) == 0)", "(err == best_err)"),
     ("e4m3: largest finite code excluded", "for (int c = 0; c <= 0x7E; ++c)", "for (int c = 0; c < 0x7E; ++c)"),
     ("e4m3: subnormal exponent", "ldexp((double)m, -9)", "ldexp((double)m, -10)"),
