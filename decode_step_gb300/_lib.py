@@ -50,6 +50,8 @@ _SIGNATURES = {
     "tts_block_pool_destroy": (None, [_vp]),
     "tts_kv_append": (ctypes.c_int, [ctypes.POINTER(KVCacheDesc), _vp, _i32, _vp, _i32, _i32,
                                      _vp, _vp, _vp, _vp]),
+    "tts_kv_append_rope": (ctypes.c_int, [ctypes.POINTER(KVCacheDesc), _vp, _i32, _vp, _i32, _i32, _i32,
+                                          _f32, _vp, _vp, _vp, _vp, _vp]),
     "tts_decode_attn_workspace_size": (_sz, [_i32] * 6),
     "tts_decode_attn": (ctypes.c_int, [ctypes.POINTER(KVCacheDesc), _vp, _i32, _vp, _i32, _i32,
                                        _i32, _i32, _f32, _i32, _vp, _vp, _vp, _sz, _vp, _vp]),

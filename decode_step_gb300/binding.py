@@ -147,6 +147,21 @@ def tts_kv_append(cache: KVCache, block_table, ctx_before, k_new, v_new, err=Non
     check("tts_kv_append", lib().tts_kv_append(*args))
 
 
+def tts_kv_append_rope(cache: KVCache, block_table, ctx_before, q, k_new, v_new, rope_base=10000.0,
+                       err=None, stream=None):
+    """tts_kv_append with the rotary embedding of q (in place) and k_new at
+    positions ctx_before[b] + j; q is [B][q_len][Hq][head_dim] bf16."""
+    B, max_blocks = block_table.shape
+    q_len, Hq = k_new.shape[1], q.shape[2]
+    shape = (B, q_len, cache.num_kv_heads, cache.head_dim)
+    args = (ctypes.byref(cache.desc), _dev(block_table, "block_table", torch.int32), max_blocks,
+            _dev(ctx_before, "ctx_before", torch.int32, (B,)), B, q_len, Hq, float(rope_base),
+            _dev(q, "q", cache.dtype, (B, q_len, Hq, cache.head_dim)),
+            _dev(k_new, "k_new", cache.dtype, shape), _dev(v_new, "v_new", cache.dtype, shape),
+            None if err is None else _dev(err, "err", torch.int32), _stream(stream))
+    check("tts_kv_append_rope", lib().tts_kv_append_rope(*args))
+
+
 def tts_decode_attn_workspace_size(B, q_len, num_q_heads, num_kv_heads, head_dim, max_ctx_len) -> int:
     return int(lib().tts_decode_attn_workspace_size(B, q_len, num_q_heads, num_kv_heads, head_dim,
                                                    max_ctx_len))

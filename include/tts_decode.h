@@ -148,6 +148,26 @@ int tts_kv_append(const tts_kv_cache *cache, const int32_t *d_block_table,
                   int32_t q_len, const void *d_k_new, const void *d_v_new, int32_t *d_err,
                   void *stream);
 
+/* Append with rotary position embedding fused in.  The engine of [OPT,
+ * "Engine-Level Optimizations with TensorRT-LLM"] writes the KV cache and
+ * applies the rotary embedding in one kernel; the rotation is RoFormer's
+ * (Su et al. 2021, section 3.4) in the rotate-half arrangement.  New token j of stream b has position s = d_ctx_before[b] + j;
+ * for i < 64 with angle a = s * rope_base^(-2i/128), every query and key row
+ * x (128 values) becomes
+ *   x[i] cos a - x[i + 64] sin a,   x[i + 64] cos a + x[i] sin a
+ * (cos a and sin a from double precision, the rotation in fp32).  The query
+ * rows are rewritten in place (round to nearest bf16); the rotated key rows
+ * are stored as tts_kv_append stores key rows (bf16, or for an FP8 cache
+ * quantised from the fp32 rotated row); value rows as tts_kv_append.
+ *  d_q  bf16 [B][q_len][num_q_heads][128], in/out
+ * Supported: TTS_BF16 and TTS_FP8_E4M3 caches, head_dim 128; rope_base > 1.
+ * Errors as tts_kv_append; the rows of a skipped slot (TTS_ERRBIT_CTX_LEN /
+ * _BLOCK_ID) are left unrotated. */
+int tts_kv_append_rope(const tts_kv_cache *cache, const int32_t *d_block_table, int32_t max_blocks_per_seq,
+                       const int32_t *d_ctx_before, int32_t B, int32_t q_len, int32_t num_q_heads,
+                       float rope_base, void *d_q, const void *d_k_new, const void *d_v_new, int32_t *d_err,
+                       void *stream);
+
 /* ------------------------------------------------------------- attention */
 
 /* Bytes of device workspace tts_decode_attn needs for these sizes (0 on bad
