@@ -371,13 +371,24 @@ def kernel_sweep(ids, reps, flush_l2, peaks, device) -> dict:
             "head_frac_tensor": flops / t_head / 1e6 / peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]),
             "head_bytes": hb, "head_mode": w.mode, "kv_cache": "fp8_e4m3" if fp8 else w.dtype,
         }
+        # the append alone, plain and with the rotary embedding of q and k_new
+        # (q rotated in place again on every launch: only its timing is used)
+        entry["kv_append_us"] = timed(lambda: bd.tts_kv_append(cache, d["block_table"], d["ctx_before"],
+                                                               d["k_new"], d["v_new"]))
+        entry["kv_append_rope_us"] = timed(lambda: bd.tts_kv_append_rope(cache, d["block_table"], d["ctx_before"],
+                                                                         d["q"], d["k_new"], d["v_new"]))
         if fp8:
             from decode_step_gb300.step import DecodeStep
-            stp = DecodeStep(cache, d["W"], w.Hq, w.B, w.ctx_hi, q_len=w.q_len, causal=w.causal,
-                             mode=bd.TTS_GUMBEL if w.mode == "gumbel" else bd.TTS_ARGMAX, temperature=w.T)
+            kw = dict(q_len=w.q_len, causal=w.causal, mode=bd.TTS_GUMBEL if w.mode == "gumbel" else bd.TTS_ARGMAX,
+                      temperature=w.T)
+            stp = DecodeStep(cache, d["W"], w.Hq, w.B, w.ctx_hi, **kw)
+            stp_rope = DecodeStep(cache, d["W"], w.Hq, w.B, w.ctx_hi, rope_base=10000.0, **kw)
             t_step = timed(lambda: stp(d["block_table"], d["ctx_before"], d["ctx_lens"], d["q"], d["k_new"],
                                        d["v_new"], seed=d["seed"], step=d["step"]))
-            entry.update({"step_us": t_step, "tokens_per_s": w.B * w.q_len / (t_step * 1e-6)})
+            t_rope = timed(lambda: stp_rope(d["block_table"], d["ctx_before"], d["ctx_lens"], d["q"], d["k_new"],
+                                            d["v_new"], seed=d["seed"], step=d["step"]))
+            entry.update({"step_us": t_step, "tokens_per_s": w.B * w.q_len / (t_step * 1e-6),
+                          "step_rope_us": t_rope, "tokens_per_s_rope": w.B * w.q_len / (t_rope * 1e-6)})
         if w.K > 0:
             tl, dp = dev(inp["target_logits"]), dev(inp["draft_probs"])
             dt, vs, vt = dev(inp["draft_tokens"]), dev(inp["vseed"]), dev(inp["vstep"])

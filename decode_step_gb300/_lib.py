@@ -34,7 +34,7 @@ class StepGraphDesc(ctypes.Structure):
     """tts_step_graph_desc."""
     _fields_ = [("cache", ctypes.POINTER(KVCacheDesc)), ("d_block_table", _vp), ("max_blocks_per_seq", _i32),
                 ("d_ctx_before", _vp), ("d_ctx_lens", _vp), ("max_ctx_len", _i32), ("B", _i32), ("q_len", _i32),
-                ("num_q_heads", _i32), ("scale", _f32), ("causal", _i32), ("d_q", _vp), ("d_k_new", _vp),
+                ("num_q_heads", _i32), ("scale", _f32), ("causal", _i32), ("rope_base", _f32), ("d_q", _vp), ("d_k_new", _vp),
                 ("d_v_new", _vp), ("d_attn_out", _vp), ("d_attn_ws", _vp), ("attn_ws_bytes", _sz), ("d_W", _vp),
                 ("V", _i32), ("mode", _i32), ("temperature", _f32), ("d_seed", _vp), ("d_step", _vp),
                 ("d_eos_allowed", _vp), ("d_ids", _vp), ("d_best", _vp), ("d_logits_out", _vp),
@@ -63,7 +63,7 @@ _SIGNATURES = {
     "tts_spec_verify": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _f32, _vp, _vp, _i32,
                                        _vp, _vp, _vp, _vp]),
     "tts_decode_step": (ctypes.c_int, [ctypes.POINTER(KVCacheDesc), _vp, _i32, _vp, _vp, _i32, _i32,
-                                       _i32, _i32, _f32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp,
+                                       _i32, _i32, _f32, _i32, _f32, _vp, _vp, _vp, _vp, _vp, _sz, _vp,
                                        _i32, _i32, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
                                        _vp, _vp]),
     "tts_step_graph_create": (ctypes.c_int, [ctypes.POINTER(StepGraphDesc), ctypes.POINTER(_vp)]),

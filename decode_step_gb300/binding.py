@@ -230,7 +230,7 @@ def tts_spec_verify(target_logits, draft_probs, draft_tokens, temperature, seed,
 
 
 def _step_args(cache: KVCache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new,
-               attn_out, attn_ws, scale, W, ids, head_ws, causal, mode, temperature, seed, step,
+               attn_out, attn_ws, scale, W, ids, head_ws, causal, rope_base, mode, temperature, seed, step,
                eos_allowed, best, logits_out, err, stream):
     """tts_decode_step's argument tuple (the cache as a byref, the stream last)."""
     B, max_blocks = block_table.shape
@@ -241,7 +241,7 @@ def _step_args(cache: KVCache, block_table, ctx_before, ctx_lens, max_ctx_len, q
         raise ValueError("W must be [V][num_q_heads * head_dim] in the cache dtype")
     args = (ctypes.byref(cache.desc), _dev(block_table, "block_table", torch.int32), max_blocks,
             _dev(ctx_before, "ctx_before", torch.int32, (B,)), _dev(ctx_lens, "ctx_lens", torch.int32, (B,)),
-            int(max_ctx_len), B, q_len, Hq, float(scale), int(bool(causal)),
+            int(max_ctx_len), B, q_len, Hq, float(scale), int(bool(causal)), float(rope_base),
             _dev(q, "q", cache.dtype, (B, q_len, Hq, cache.head_dim)),
             _dev(k_new, "k_new", cache.dtype, kv_shape), _dev(v_new, "v_new", cache.dtype, kv_shape),
             _dev(attn_out, "attn_out", cache.dtype, (B, q_len, Hq, cache.head_dim)), _dev(attn_ws, "attn_ws"),
@@ -259,10 +259,11 @@ def _step_args(cache: KVCache, block_table, ctx_before, ctx_lens, max_ctx_len, q
 def tts_decode_step(cache: KVCache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new,
                     attn_out, attn_ws, scale, W, ids, head_ws, causal=False, mode=TTS_ARGMAX,
                     temperature=0.0, seed=None, step=None, eos_allowed=None, best=None,
-                    logits_out=None, err=None, stream=None):
+                    logits_out=None, err=None, stream=None, rope_base=0.0):
+    """rope_base != 0 rotates q (in place) and k_new at positions ctx_before[b] + j."""
     args = _step_args(cache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new, attn_out,
-                      attn_ws, scale, W, ids, head_ws, causal, mode, temperature, seed, step, eos_allowed,
-                      best, logits_out, err, stream)
+                      attn_ws, scale, W, ids, head_ws, causal, rope_base, mode, temperature, seed, step,
+                      eos_allowed, best, logits_out, err, stream)
     check("tts_decode_step", lib().tts_decode_step(*args))
 
 
@@ -292,9 +293,9 @@ class StepGraph:
     def __init__(self, cache: KVCache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new,
                  attn_out, attn_ws, scale, W, ids, head_ws, h_inputs, d_inputs, h_ids,
                  h_boundary_count=None, causal=False, mode=TTS_ARGMAX, temperature=0.0, seed=None,
-                 step=None, eos_allowed=None, best=None, logits_out=None, err=None):
+                 step=None, eos_allowed=None, best=None, logits_out=None, err=None, rope_base=0.0):
         args = _step_args(cache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new, attn_out,
-                          attn_ws, scale, W, ids, head_ws, causal, mode, temperature, seed, step,
+                          attn_ws, scale, W, ids, head_ws, causal, rope_base, mode, temperature, seed, step,
                           eos_allowed, best, logits_out, err, None)
         R = ids.numel()
         nbytes = h_inputs.numel() * h_inputs.element_size()

@@ -107,8 +107,8 @@ extern "C" int tts_step_graph_create(const tts_step_graph_desc *d, tts_step_grap
     AttnLaunch at;
     HeadLaunch hd;
     const tts_kv_cache *c = d->cache;
-    int st = prepare_append(c, d->d_block_table, d->max_blocks_per_seq, d->d_ctx_before, d->B, d->q_len,
-                            d->d_k_new, d->d_v_new, d->d_err, &ap);
+    int st = prepare_append_rope(c, d->d_block_table, d->max_blocks_per_seq, d->d_ctx_before, d->B, d->q_len,
+                                 d->num_q_heads, d->rope_base, d->d_q, d->d_k_new, d->d_v_new, d->d_err, &ap);
     if (st != TTS_OK) return st;
     st = prepare_attn(c, d->d_block_table, d->max_blocks_per_seq, d->d_ctx_lens, d->max_ctx_len, d->B, d->q_len,
                       d->num_q_heads, d->scale, d->causal, d->d_q, d->d_attn_out, d->d_attn_ws, d->attn_ws_bytes,

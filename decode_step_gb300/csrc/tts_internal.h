@@ -73,6 +73,12 @@ size_t attn_workspace_bytes(int B, int num_kv_heads, int head_dim, const AttnPla
 // ---- validated launches, shared by the single-kernel entry points and
 // tts_decode_step (which chains them with programmatic dependent launch)
 
+// Inverse frequencies of the rotary embedding for head_dim 128:
+// theta[i] = base^(-2i/128), i < 64, in double.
+struct RopeFreqs {
+    double theta[64];
+};
+
 struct AppendLaunch {
     const tts_kv_cache *cache;
     const int32_t *table;
@@ -81,10 +87,20 @@ struct AppendLaunch {
     int B, q_len;
     const void *k_new, *v_new;
     int32_t *err;
+    // rotary embedding (rope == false: none): q [B][q_len][Hq][128] rotated in place
+    bool rope;
+    int Hq;
+    void *q;
+    RopeFreqs freqs;
 };
 int prepare_append(const tts_kv_cache *cache, const int32_t *d_block_table, int32_t max_blocks_per_seq,
                    const int32_t *d_ctx_before, int32_t B, int32_t q_len, const void *d_k_new,
                    const void *d_v_new, int32_t *d_err, AppendLaunch *out);
+// prepare_append plus the rotary embedding's checks; rope_base == 0 means none.
+int prepare_append_rope(const tts_kv_cache *cache, const int32_t *d_block_table, int32_t max_blocks_per_seq,
+                        const int32_t *d_ctx_before, int32_t B, int32_t q_len, int32_t num_q_heads,
+                        float rope_base, void *d_q, const void *d_k_new, const void *d_v_new, int32_t *d_err,
+                        AppendLaunch *out);
 int launch_append(const AppendLaunch &L, LaunchOpts o);
 
 struct AttnLaunchState;  // defined in decode_attn.cu

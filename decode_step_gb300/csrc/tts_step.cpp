@@ -15,7 +15,7 @@ extern "C" int tts_decode_step(const tts_kv_cache *cache, const int32_t *d_block
                                int32_t max_blocks_per_seq, const int32_t *d_ctx_before,
                                const int32_t *d_ctx_lens, int32_t max_ctx_len, int32_t B,
                                int32_t q_len, int32_t num_q_heads, float scale, int32_t causal,
-                               const void *d_q, const void *d_k_new, const void *d_v_new,
+                               float rope_base, void *d_q, const void *d_k_new, const void *d_v_new,
                                void *d_attn_out, void *d_attn_ws, size_t attn_ws_bytes,
                                const void *d_W, int32_t V, int32_t mode, float temperature,
                                const uint64_t *d_seed, const uint64_t *d_step,
@@ -28,8 +28,8 @@ extern "C" int tts_decode_step(const tts_kv_cache *cache, const int32_t *d_block
     AppendLaunch ap;
     AttnLaunch at;
     HeadLaunch hd;
-    int st = prepare_append(cache, d_block_table, max_blocks_per_seq, d_ctx_before, B, q_len, d_k_new,
-                            d_v_new, d_err, &ap);
+    int st = prepare_append_rope(cache, d_block_table, max_blocks_per_seq, d_ctx_before, B, q_len, num_q_heads,
+                                 rope_base, d_q, d_k_new, d_v_new, d_err, &ap);
     if (st != TTS_OK) return st;
     st = prepare_attn(cache, d_block_table, max_blocks_per_seq, d_ctx_lens, max_ctx_len, B, q_len,
                       num_q_heads, scale, causal, d_q, d_attn_out, d_attn_ws, attn_ws_bytes, d_err, &at);

@@ -24,12 +24,14 @@ from . import binding as bd
 class DecodeStep:
     def __init__(self, cache: bd.KVCache, W: torch.Tensor, num_q_heads: int, B: int,
                  max_ctx_len: int, q_len: int = 1, causal: bool = False,
-                 mode: int = bd.TTS_ARGMAX, temperature: float = 0.0, scale: float | None = None):
+                 mode: int = bd.TTS_ARGMAX, temperature: float = 0.0, scale: float | None = None,
+                 rope_base: float = 0.0):
         dev = cache.k_pool.device
         self.cache, self.W = cache, W
         self.B, self.q_len, self.Hq = B, q_len, num_q_heads
         self.max_ctx_len, self.causal = max_ctx_len, causal
         self.mode, self.temperature = mode, temperature
+        self.rope_base = rope_base  # != 0: q and k_new rotated at their positions (q in place)
         self.scale = 1.0 / math.sqrt(cache.head_dim) if scale is None else scale
         H = num_q_heads * cache.head_dim
         if W.shape[1] != H:
@@ -53,7 +55,7 @@ class DecodeStep:
                            v_new, self.out, self.attn_ws, self.scale, self.W, self.ids, self.head_ws,
                            causal=self.causal, mode=self.mode, temperature=self.temperature,
                            seed=seed, step=step, eos_allowed=eos_allowed, best=best,
-                           logits_out=logits_out, err=self.err, stream=stream)
+                           logits_out=logits_out, err=self.err, stream=stream, rope_base=self.rope_base)
         return self.ids
 
 
@@ -100,7 +102,7 @@ class GraphedStep:
             d["k_new"], d["v_new"], step.out, step.attn_ws, step.scale, step.W, step.ids, step.head_ws,
             self.host_blob, self.dev_blob, self.ids_host, self.boundary_host, causal=step.causal,
             mode=step.mode, temperature=step.temperature, seed=d.get("seed"), step=d.get("step"),
-            err=step.err)
+            err=step.err, rope_base=step.rope_base)
 
     @property
     def h2d_bytes(self) -> int:

@@ -284,11 +284,13 @@ int tts_spec_verify(const float *d_target_logits, const float *d_draft_probs,
 
 /* ----------------------------------------------------------- full step */
 
-/* One decode step in one call: tts_kv_append, then tts_decode_attn into
- * d_attn_out, then tts_codebook_head_select with h = d_attn_out read as
+/* One decode step in one call: tts_kv_append (tts_kv_append_rope when
+ * rope_base != 0: d_q is then rotated in place, so a repeated call on the same
+ * d_q rotates it again), then tts_decode_attn into d_attn_out, then
+ * tts_codebook_head_select with h = d_attn_out read as
  * [B * q_len][num_q_heads * head_dim] (dtype cache->dtype; bf16 for an FP8
  * cache; R = B * q_len).
- * Arguments mean what they mean for those three calls; all of them are
+ * Arguments mean what they mean for those calls; all of them are
  * checked before anything is launched.  The attention and head kernels are
  * launched as programmatic dependents of the kernel before them: each starts
  * its set-up (tile map; weight stream) while its predecessor finishes, and
@@ -298,7 +300,7 @@ int tts_spec_verify(const float *d_target_logits, const float *d_draft_probs,
 int tts_decode_step(const tts_kv_cache *cache, const int32_t *d_block_table,
                     int32_t max_blocks_per_seq, const int32_t *d_ctx_before,
                     const int32_t *d_ctx_lens, int32_t max_ctx_len, int32_t B, int32_t q_len,
-                    int32_t num_q_heads, float scale, int32_t causal, const void *d_q,
+                    int32_t num_q_heads, float scale, int32_t causal, float rope_base, void *d_q,
                     const void *d_k_new, const void *d_v_new, void *d_attn_out, void *d_attn_ws,
                     size_t attn_ws_bytes, const void *d_W, int32_t V, int32_t mode,
                     float temperature, const uint64_t *d_seed, const uint64_t *d_step,
@@ -340,7 +342,8 @@ typedef struct {
     int32_t num_q_heads;
     float scale;
     int32_t causal;
-    const void *d_q;
+    float rope_base;
+    void *d_q;
     const void *d_k_new;
     const void *d_v_new;
     void *d_attn_out;

@@ -240,3 +240,45 @@ def test_rope_append_errors(bd):
         with pytest.raises(bd.TTSError) as e:
             bd.tts_kv_append_rope(*args, rope_base=base)
         assert e.value.code == ERR_INVALID
+
+
+@pytest.mark.parametrize("fp8", [False, True], ids=["bf16", "fp8"])
+def test_rope_decode_step_ids(orc, bd, fp8):
+    """The fused step with the rotation (tts_decode_step, rope_base != 0) and its
+    captured form: ids as the oracle head picks them on the oracle's attention
+    over the oracle-rotated queries and keys."""
+    from decode_step_gb300.step import DecodeStep, GraphedStep
+    from gpu_util import compare_ids
+    w = wl.custom(3, B=16, ctx_lo=30, ctx_hi=400, permute_table=True)
+    inp = wl.make_inputs(w, seed=1234 + fp8, with_verify=False)
+    pos = _positions(inp)
+    q_rot = wl.f32_to_bf16(orc.rope(inp["q"], pos))
+    k_rot = orc.rope(inp["k_new"], pos)
+    if fp8:
+        tiles = fp8_cache_for(orc, inp)
+        ref_tiles = orc.kv_append_fp8(tiles, inp["block_table"], inp["ctx_before"], k_rot,
+                                      wl.bf16_to_f32(inp["v_new"]))
+        attn = orc.decode_attn_fp8(ref_tiles, inp["block_table"], inp["ctx_lens"], q_rot, inp["scale"])
+        cache = bd.KVCache(dev(tiles))
+    else:
+        rk, rv = orc.kv_append(inp["k_pool"], inp["v_pool"], inp["block_table"], inp["ctx_before"],
+                               wl.f32_to_bf16(k_rot), inp["v_new"])
+        attn = orc.decode_attn(rk, rv, inp["block_table"], inp["ctx_lens"], q_rot, inp["scale"])
+        cache = bd.KVCache(dev(inp["k_pool"]), dev(inp["v_pool"]))
+    h = wl.f32_to_bf16(attn.reshape(w.R, w.Hq * w.D).astype(np.float32))
+    ref = orc.head_select(h, inp["W"], "argmax")
+    step = DecodeStep(cache, dev(inp["W"]), w.Hq, w.B, w.ctx_hi, rope_base=10000.0)
+    table, cb, cl = dev(inp["block_table"]), dev(inp["ctx_before"]), dev(inp["ctx_lens"])
+    q, kn, vn = dev(inp["q"]), dev(inp["k_new"]), dev(inp["v_new"])
+    ids = step(table, cb, cl, q, kn, vn).clone()
+    torch.cuda.synchronize()
+    check_bf16_rounding(host(q), orc.rope(inp["q"], pos), _pair_mag(inp["q"]), "step q")
+    hard, ties = compare_ids(host(ids), ref)
+    print(f"[rope step fp8={fp8}] near-ties {ties}, hard mismatches {len(hard)}")
+    assert not hard
+    # captured: every launch copies the unrotated q from pinned memory and rotates it again
+    g = GraphedStep(step, {"block_table": table, "ctx_before": cb, "ctx_lens": cl, "q": dev(inp["q"]),
+                           "k_new": kn, "v_new": vn})
+    for _ in range(2):
+        assert torch.equal(g().clone(), ids.cpu())
+    assert int(step.err.item()) == 0
