@@ -61,14 +61,20 @@ HeadWs head_ws(void *ws, int R) {
 // workspace.  No waiting.
 __device__ void finish_selection(const HeadWs &ws, int R, int32_t *ids, float *best, int *flag,
                                  unsigned int publishers) {
-    __threadfence();
+    // The barrier orders every thread's key atomics before thread 0's fence
+    // (fences are cumulative), so one fence per CTA publishes them all.
     __syncthreads();
-    if (threadIdx.x == 0) *flag = atomicAdd(ws.ticket, 1u) == publishers - 1u;
+    if (threadIdx.x == 0) {
+        __threadfence();
+        *flag = atomicAdd(ws.ticket, 1u) == publishers - 1u;
+        if (*flag) __threadfence();
+    }
     __syncthreads();
     if (!*flag) return;
-    __threadfence();
+    // The last CTA alone reads and clears the keys (L2 reads: the atomics live there).
     for (int r = threadIdx.x; r < R; r += blockDim.x) {
-        const unsigned long long k = atomicExch(ws.keys + r, 0ull);
+        const unsigned long long k = __ldcg(ws.keys + r);
+        ws.keys[r] = 0ull;
         ids[r] = k ? unpack_index(k) : -1;
         if (best) best[r] = k ? unpack_value(k) : -INFINITY;
     }
@@ -583,8 +589,10 @@ TcPlan plan_tc(int R, int H, int V) {
     const int ktiles = H / kTileK;
     p.CK = 1;
     p.smem = tc_layout(p.N, 1).total;
-    // widest cluster split of the hidden dimension that still runs in one wave
-    for (int ck = 2; ck <= 8; ck <<= 1) {
+    // widest cluster split of the hidden dimension, up to 4, that still runs
+    // in one wave (8-CTA clusters start and synchronise more slowly than the
+    // extra SMs they bring save: measured 1.5 us slower at 64 x 2048 x 4097)
+    for (int ck = 2; ck <= 4; ck <<= 1) {
         if (ktiles % ck != 0) break;
         const uint32_t smem = tc_layout(p.N, ck).total;
         int per_sm = static_cast<int>((227u * 1024u) / (smem + 1024u));
