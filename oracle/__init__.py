@@ -90,6 +90,15 @@ class Oracle:
         L.orc_decode_attn_fp8.argtypes = ([ctypes.c_int] * 3 + [_vp, _vp, ctypes.c_int, _vp]
                                           + [ctypes.c_int] * 3 + [ctypes.c_double, ctypes.c_int, _vp, _vp])
         L.orc_decode_attn_fp8.restype = ctypes.c_int
+        L.orc_mish.argtypes = [ctypes.c_double]
+        L.orc_mish.restype = ctypes.c_double
+        L.orc_bf16_round.argtypes = [ctypes.c_double]
+        L.orc_bf16_round.restype = ctypes.c_uint16
+        L.orc_audio_expand.argtypes = [_vp, _vp, _vp] + [ctypes.c_int] * 3 + [_vp, _vp]
+        L.orc_audio_expand.restype = ctypes.c_int
+        L.orc_head_select_masked.argtypes = ([_vp, _vp, ctypes.c_int, _vp] + [ctypes.c_int] * 4
+                                             + [ctypes.c_float, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp])
+        L.orc_head_select_masked.restype = ctypes.c_int
         self.lib = L
 
     # ------------------------------------------------------------- random
@@ -237,6 +246,67 @@ class Oracle:
         out = dict(ids=ids, best=best, second=second)
         if want_logits:
             out["logits"] = logits
+        return out
+
+    # --------------------------------------------------------- audio head
+    def mish(self, x) -> np.ndarray:
+        """Mish of every element (float64)."""
+        xs = np.asarray(x, dtype=np.float64)
+        return np.vectorize(self.lib.orc_mish, otypes=[np.float64])(xs) if xs.size else xs.copy()
+
+    def bf16_round(self, x) -> np.ndarray:
+        """Nearest bfloat16 (ties to even) of float64 values, as uint16 bits."""
+        xs = np.asarray(x, dtype=np.float64)
+        return np.vectorize(self.lib.orc_bf16_round, otypes=[np.uint16])(xs) if xs.size else xs.astype(np.uint16)
+
+    def audio_expand(self, h, W1, b1=None):
+        """First audio-head layer: (z as bf16 bits [R][F], Mish values before rounding [R][F])."""
+        R, H = h.shape
+        F, HW = W1.shape
+        assert HW == H and h.dtype == np.uint16 and W1.dtype == np.uint16
+        z = np.zeros((R, F), dtype=np.uint16)
+        m = np.zeros((R, F), dtype=np.float64)
+        b = None if b1 is None else np.ascontiguousarray(b1, dtype=np.float32)
+        rc = self.lib.orc_audio_expand(_ptr(np.ascontiguousarray(h)), _ptr(np.ascontiguousarray(W1)), _ptr(b),
+                                       R, H, F, _ptr(z), _ptr(m))
+        if rc != 0:
+            raise ValueError("oracle audio_expand: bad arguments")
+        return z, m
+
+    def head_select_masked(self, h, W, b=None, mode="argmax", T=0.0, seed=None, step=None, n_tail=0,
+                           tail_allowed=None, want_logits=False):
+        """Head selection with bias b [V] and the last n_tail ids masked per row
+        by tail_allowed [R] (uint32 bits).  Returns dict(ids, best, second, logits?)."""
+        is_bf16 = int(W.dtype == np.uint16)
+        R, H = h.shape
+        V, HW = W.shape
+        assert HW == H and h.dtype == W.dtype
+        m = {"argmax": 0, "gumbel": 1}[mode]
+        seed = np.zeros(R, np.uint64) if seed is None else np.ascontiguousarray(seed, dtype=np.uint64)
+        step = np.zeros(R, np.uint64) if step is None else np.ascontiguousarray(step, dtype=np.uint64)
+        bb = None if b is None else np.ascontiguousarray(b, dtype=np.float32)
+        ta = None if tail_allowed is None else np.ascontiguousarray(tail_allowed, dtype=np.uint32)
+        ids = np.zeros(R, dtype=np.int32)
+        best = np.zeros(R, dtype=np.float32)
+        second = np.zeros(R, dtype=np.float32)
+        logits = np.zeros((R, V), dtype=np.float32) if want_logits else None
+        rc = self.lib.orc_head_select_masked(_ptr(np.ascontiguousarray(h)), _ptr(np.ascontiguousarray(W)), is_bf16,
+                                             _ptr(bb), R, H, V, m, float(T), _ptr(seed), _ptr(step), int(n_tail),
+                                             _ptr(ta), _ptr(ids), _ptr(best), _ptr(second), _ptr(logits))
+        if rc != 0:
+            raise ValueError("oracle head_select_masked: bad arguments")
+        out = dict(ids=ids, best=best, second=second)
+        if want_logits:
+            out["logits"] = logits
+        return out
+
+    def audio_head(self, h, W1, b1, W2, b2, mode="argmax", T=0.0, seed=None, step=None, n_tail=0,
+                   tail_allowed=None, want_logits=False):
+        """The two-layer audio head: z = bf16(Mish(h W1^T + b1)), then the masked
+        selection over z W2^T + b2.  Returns the selection dict plus z."""
+        z, _ = self.audio_expand(h, W1, b1)
+        out = self.head_select_masked(z, W2, b2, mode, T, seed, step, n_tail, tail_allowed, want_logits)
+        out["z"] = z
         return out
 
     # ------------------------------------------------------------- verify

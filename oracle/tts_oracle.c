@@ -22,6 +22,8 @@
  *         4,096 entries, boundary token, later stages at temperature zero).
  *  [SAL]  Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
  *         1, 2, 3", SC'11: the Philox4x64-10 bijection.
+ *  [MIS]  Misra, "Mish: A Self Regularized Non-Monotonic Activation Function"
+ *         (2019): Mish(x) = x tanh(ln(1 + e^x)).
  *
  * Readings where the pages are silent (each is also listed in the design
  * notes): softmax scale 1/sqrt(D); query head h uses KV head h/(Hq/Hkv); the
@@ -29,7 +31,10 @@
  * prefix and new tokens 0..j; the boundary token is vocab index V-1; equal
  * keys resolve to the lowest index; the rejection draw samples the clamped
  * residual by Gumbel-max; with every draft accepted no bonus token is drawn
- * unless asked for.
+ * unless asked for; the two-layer audio head's intermediate is rounded to
+ * bfloat16 once (the precision its second product reads) and its layers'
+ * biases are optional; a stage's structural tokens are the last ids of its
+ * vocabulary, each allowed per row by one mask bit.
  */
 #include <math.h>
 #include <stdint.h>
@@ -367,31 +372,82 @@ int orc_decode_attn_fp8(int num_blocks, int Hkv, int D, const uint8_t *tiles, co
 
 /* -------------------------------------------------------------------- head */
 
-/* Codebook head and token choice [TON, section 3]: logits[r][v] = h[r] . W[v]
- * over the stage vocabulary (V entries, the last one the boundary token).
- * mode 0 (temperature zero): id = argmax_v logits.  mode 1: id =
- * argmax_v (logits / T + G_v) with G_v Gumbel noise (tag 0, pos 0, idx v), a
- * draw from softmax(logits / T).  eos_allowed[r] == 0 removes v = V-1.
- * Equal keys resolve to the lowest index.  best / second receive the top two
- * keys (second = -inf when V == 1); logits_out (nullable) receives the fp32
- * logits [R][V].  Returns 0, or -1 on bad arguments. */
-int orc_head_select(const void *h, const void *W, int is_bf16, int R, int H, int V, int mode,
-                    float T, const uint64_t *seed, const uint64_t *step,
-                    const uint8_t *eos_allowed, int32_t *ids, float *best, float *second,
-                    float *logits_out) {
-    if (R < 0 || H <= 0 || V <= 0 || (mode != 0 && mode != 1)) return -1;
+/* -------------------------------------------------------------- audio head */
+
+/* Mish [MIS]: x * tanh(softplus(x)), softplus(x) = ln(1 + e^x), in
+ * double.  Past x = 40, ln(1 + e^x) equals x to double precision. */
+double orc_mish(double x) {
+    const double sp = x > 40.0 ? x : log1p(exp(x));
+    return x * tanh(sp);
+}
+
+/* Round a double to the nearest bfloat16 (8 significant bits; below 2^-126
+ * the fixed spacing 2^-133 of its subnormals), ties to the even significand;
+ * returns the bit pattern. */
+uint16_t orc_bf16_round(double x) {
+    float f;
+    if (isnan(x) || isinf(x)) {
+        f = (float)x;
+    } else if (fabs(x) < 0x1p-126) {
+        f = (float)ldexp(nearbyint(ldexp(x, 133)), -133);  /* exact: on the float grid */
+    } else {
+        int e;
+        const double m = frexp(x, &e);           /* x = m * 2^e, 0.5 <= |m| < 1 */
+        const double q = nearbyint(ldexp(m, 8));  /* 8 significant bits, ties to even */
+        f = (float)ldexp(q, e - 8);                /* exact: fits in a float */
+    }
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    return (uint16_t)(bits >> 16);
+}
+
+/* The first layer of the two-layer audio head ([TON], section 3: the state
+ * is expanded to width 4,096 and passed through Mish): for every row r and
+ * feature f, pre = sum_k h[r][k] * W1[f][k] + b1[f] (b1 may be NULL), and
+ * z[r][f] = bfloat16(Mish(pre)) — the kernel keeps z as the bfloat16 operand
+ * of the second layer, so the oracle rounds the exact value once.  h and W1
+ * are bf16 bit patterns; mish_out (nullable) receives Mish(pre) unrounded. */
+int orc_audio_expand(const uint16_t *h, const uint16_t *W1, const float *b1, int R, int H, int F,
+                     uint16_t *z, double *mish_out) {
+    if (R < 0 || H <= 0 || F <= 0) return -1;
+    for (int r = 0; r < R; ++r) {
+        for (int f = 0; f < F; ++f) {
+            double acc = b1 ? (double)b1[f] : 0.0;
+            for (int k = 0; k < H; ++k)
+                acc += load_elem(h, (size_t)r * H + k, 1) * load_elem(W1, (size_t)f * H + k, 1);
+            const double m = orc_mish(acc);
+            if (mish_out) mish_out[(size_t)r * F + f] = m;
+            z[(size_t)r * F + f] = orc_bf16_round(m);
+        }
+    }
+    return 0;
+}
+
+/* Head selection with a bias and a vocabulary mask ([TON], section 3: each
+ * stage emits its codebook plus the structural tokens it may produce; logits
+ * outside the target vocabulary are masked at sampling).  logit[v] =
+ * float(sum_k h[r][k] * W[v][k] + b[v]) (b nullable).  The last n_tail ids
+ * V - n_tail .. V - 1 are the structural tokens; id V - n_tail + j may be
+ * chosen for row r only if bit j of tail_allowed[r] is set (tail_allowed NULL:
+ * all may).  Selection as orc_head_select over the allowed ids. */
+int orc_head_select_masked(const void *h, const void *W, int is_bf16, const float *b, int R, int H, int V,
+                           int mode, float T, const uint64_t *seed, const uint64_t *step, int n_tail,
+                           const uint32_t *tail_allowed, int32_t *ids, float *best, float *second,
+                           float *logits_out) {
+    if (R < 0 || H <= 0 || V <= 0 || (mode != 0 && mode != 1) || n_tail < 0 || n_tail > 32 || n_tail > V)
+        return -1;
     if (mode == 1 && !(T > 0.0f)) return -1;
     for (int r = 0; r < R; ++r) {
-        const int vmax = (eos_allowed && !eos_allowed[r]) ? V - 1 : V;
         int arg = -1;
         float top = -INFINITY, next = -INFINITY;
         for (int v = 0; v < V; ++v) {
-            double acc = 0.0;
+            double acc = b ? (double)b[v] : 0.0;
             for (int k = 0; k < H; ++k)
                 acc += load_elem(h, (size_t)r * H + k, is_bf16) * load_elem(W, (size_t)v * H + k, is_bf16);
             const float logit = (float)acc;
             if (logits_out) logits_out[(size_t)r * V + v] = logit;
-            if (v >= vmax) continue;
+            const int j = v - (V - n_tail);
+            if (j >= 0 && tail_allowed && !((tail_allowed[r] >> j) & 1u)) continue;
             float key = logit;
             if (mode == 1) key = logit / T + orc_gumbel(seed[r], step[r], 0u, 0u, (uint32_t)v);
             if (arg < 0 || key > top) {
@@ -407,6 +463,32 @@ int orc_head_select(const void *h, const void *W, int is_bf16, int R, int H, int
         if (second) second[r] = next;
     }
     return 0;
+}
+
+/* Codebook head and token choice [TON, section 3]: logits[r][v] = h[r] . W[v]
+ * over the stage vocabulary (V entries, the last one the boundary token).
+ * mode 0 (temperature zero): id = argmax_v logits.  mode 1: id =
+ * argmax_v (logits / T + G_v) with G_v Gumbel noise (tag 0, pos 0, idx v), a
+ * draw from softmax(logits / T).  eos_allowed[r] == 0 removes v = V-1 (the
+ * one-id case of the stage vocabulary mask below: a tail of one id whose
+ * mask bit is eos_allowed[r]).
+ * Equal keys resolve to the lowest index.  best / second receive the top two
+ * keys (second = -inf when V == 1); logits_out (nullable) receives the fp32
+ * logits [R][V].  Returns 0, or -1 on bad arguments. */
+int orc_head_select(const void *h, const void *W, int is_bf16, int R, int H, int V, int mode,
+                    float T, const uint64_t *seed, const uint64_t *step,
+                    const uint8_t *eos_allowed, int32_t *ids, float *best, float *second,
+                    float *logits_out) {
+    uint32_t *mask = NULL;
+    if (eos_allowed && R > 0) {
+        mask = (uint32_t *)malloc((size_t)R * sizeof *mask);
+        if (!mask) return -1;
+        for (int r = 0; r < R; ++r) mask[r] = eos_allowed[r] ? 1u : 0u;
+    }
+    const int rc = orc_head_select_masked(h, W, is_bf16, NULL, R, H, V, mode, T, seed, step, eos_allowed ? 1 : 0,
+                                          mask, ids, best, second, logits_out);
+    free(mask);
+    return rc;
 }
 
 /* ------------------------------------------------------------------ verify */

@@ -626,4 +626,158 @@ def check_fp8_append_from_float_rows(o):
     assert np.array_equal(a, b)
 
 
+# ------------------------------------------------------------- audio head
+
+def _mish_identity(x):
+    """Mish through tanh(ln n) = (n^2 - 1) / (n^2 + 1) with n = 1 + e^x."""
+    x = np.asarray(x, dtype=np.float64)
+    n2 = (1.0 + np.exp(np.minimum(x, 300.0))) ** 2
+    return x * (n2 - 1.0) / (n2 + 1.0)
+
+
+def check_mish_closed_forms(o):
+    """Mish against the algebraic form of tanh(softplus), its published minimum
+    (about -0.30884 at x = -1.1924), slope 0.6 at zero (tanh(ln 2)), and its
+    limits (x for large x, x e^x for very negative x)."""
+    x = np.linspace(-20.0, 20.0, 4001)
+    m = o.mish(x)
+    ref = _mish_identity(x)
+    assert np.all(np.abs(m - ref) <= 1e-13 * np.maximum(1.0, np.abs(ref)))
+    assert o.mish([0.0])[0] == 0.0
+    i = int(np.argmin(m))
+    assert abs(x[i] - (-1.1924)) < 0.011 and abs(m[i] - (-0.30884)) < 1e-4
+    eps = 1e-7
+    slope = (o.mish([eps])[0] - o.mish([-eps])[0]) / (2 * eps)
+    assert abs(slope - 0.6) < 1e-8
+    assert o.mish([50.0])[0] == 50.0
+    big = o.mish([-40.0])[0]
+    assert abs(big / (-40.0 * math.exp(-40.0)) - 1.0) < 1e-12
+
+
+def check_bf16_round_matches_torch(o):
+    """Rounding to bfloat16 equals torch's conversion for float32-exact inputs
+    (one rounding either way), ties to the even significand, specials kept."""
+    import torch
+    rng = np.random.default_rng(61)
+    x = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.uniform(-6, 6, 20000),
+                        # exact midpoints between neighbouring bfloat16 values
+                        (np.arange(1, 2000) * 2 + 1).astype(np.float64) * 2.0 ** -9,
+                        -(np.arange(1, 2000) * 2 + 1).astype(np.float64) * 2.0 ** -9,
+                        [0.0, -0.0, 1e-40, -3e-39, 3.3e38]]).astype(np.float32)
+    got = o.bf16_round(x.astype(np.float64))
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+    assert o.bf16_round([1.0 + 2.0 ** -8])[0] == 0x3F80      # tie -> even (1.0)
+    assert o.bf16_round([1.0 + 3 * 2.0 ** -8])[0] == 0x3F82  # tie -> even (1.015625)
+    assert o.bf16_round([math.inf])[0] == 0x7F80 and o.bf16_round([-math.inf])[0] == 0xFF80
+
+
+def check_audio_expand_matches_matmul(o):
+    """z = bf16(Mish(h W1^T + b1)) against a numpy float64 matmul, the algebraic
+    Mish and a nearest-value test of the rounding; the bias shifts the input."""
+    rng = np.random.default_rng(62)
+    R, H, F = 3, 64, 40
+    h = wl.f32_to_bf16(rng.standard_normal((R, H), dtype=np.float32))
+    W1 = wl.f32_to_bf16((rng.standard_normal((F, H)) / 8).astype(np.float32))
+    b1 = rng.standard_normal(F).astype(np.float32)
+    pre = wl.bf16_to_f32(h).astype(np.float64) @ wl.bf16_to_f32(W1).astype(np.float64).T + b1
+    z, m = o.audio_expand(h, W1, b1)
+    assert np.all(np.abs(m - _mish_identity(pre)) <= 1e-12 * np.maximum(1.0, np.abs(m)))
+    zf = wl.bf16_to_f32(z).astype(np.float64)
+    # every z is a nearest bfloat16 of m: no neighbour one step away is closer
+    bits = z.astype(np.int64)
+    for step in (-1, 1):
+        nb = wl.bf16_to_f32((bits + step).astype(np.uint16)).astype(np.float64)
+        assert np.all(np.abs(zf - m) <= np.abs(nb - m))
+    z0, m0 = o.audio_expand(h, W1, None)
+    assert np.allclose(m0, _mish_identity(pre - b1), rtol=1e-12, atol=1e-12)
+    z1, _ = o.audio_expand(h, W1, np.zeros(F, np.float32))
+    assert np.array_equal(z0, z1)
+
+
+def _masked_reference(h, W, b, n_tail, tail_allowed):
+    """numpy: float32 logits, masked tail ids removed, lowest index on ties."""
+    lg = (wl.bf16_to_f32(h).astype(np.float64) @ wl.bf16_to_f32(W).astype(np.float64).T
+          + (0.0 if b is None else b.astype(np.float64))).astype(np.float32)
+    V = W.shape[0]
+    keep = np.ones(lg.shape, bool)
+    if tail_allowed is not None:
+        for j in range(n_tail):
+            keep[:, V - n_tail + j] = (tail_allowed >> j) & 1 == 1
+    masked = np.where(keep, lg.astype(np.float64), -np.inf)
+    return lg, masked, np.argmax(masked, axis=1)
+
+
+def check_head_masked_bias_and_tail(o):
+    """Biased, masked selection against numpy's argmax over the allowed ids;
+    a tail id with a dominant bias wins exactly when its mask bit is set, and
+    mask bit j governs id V - n_tail + j."""
+    rng = np.random.default_rng(63)
+    R, H, V, n_tail = 6, 32, 50, 3
+    h = wl.f32_to_bf16(rng.standard_normal((R, H), dtype=np.float32))
+    W = wl.f32_to_bf16((rng.standard_normal((V, H)) / 4).astype(np.float32))
+    b = (rng.standard_normal(V) / 10).astype(np.float32)
+    ta = rng.integers(0, 8, R).astype(np.uint32)
+    res = o.head_select_masked(h, W, b, n_tail=n_tail, tail_allowed=ta, want_logits=True)
+    lg, masked, ref_ids = _masked_reference(h, W, b, n_tail, ta)
+    assert np.array_equal(res["logits"], lg)
+    assert np.array_equal(res["ids"], ref_ids)
+    # dominant tail biases: row r picks the highest allowed tail id bit
+    b2 = b.copy()
+    b2[V - n_tail:] = [100.0, 200.0, 300.0]
+    ta2 = np.array([0, 1, 2, 4, 3, 7], np.uint32)
+    res2 = o.head_select_masked(h, W, b2, n_tail=n_tail, tail_allowed=ta2)
+    expect = []
+    for r, m in enumerate(ta2):
+        allowed = [j for j in range(n_tail) if (m >> j) & 1]
+        # no tail id allowed: the codebook's own argmax (its biases are unchanged)
+        expect.append(V - n_tail + max(allowed) if allowed else int(np.argmax(lg[r, :V - n_tail])))
+    assert list(res2["ids"]) == expect
+    # no mask and no bias: plain selection over the matmul
+    res3 = o.head_select_masked(h, W)
+    assert np.array_equal(res3["ids"], np.argmax(_masked_reference(h, W, None, 0, None)[0], axis=1))
+
+
+def check_head_masked_gumbel(o):
+    """Gumbel selection with a mask draws from softmax(logits / T) restricted to
+    the allowed ids: the keys are the oracle's noise added to logits / T, and
+    the frequencies pass a chi-square test with masked ids never drawn."""
+    rng = np.random.default_rng(64)
+    H, V, n_tail, T = 16, 12, 2, 0.8
+    W = wl.f32_to_bf16((rng.standard_normal((V, H)) / 2).astype(np.float32))
+    h1 = wl.f32_to_bf16(rng.standard_normal((1, H), dtype=np.float32))
+    rows = 3000
+    h = np.repeat(h1, rows, axis=0)
+    ta = np.full(rows, 0b10, np.uint32)   # id V-2 masked, id V-1 allowed
+    seeds = np.arange(rows, dtype=np.uint64) + 7
+    res = o.head_select_masked(h, W, None, "gumbel", T, seeds, np.zeros(rows, np.uint64), n_tail, ta,
+                               want_logits=True)
+    lg = res["logits"][0].astype(np.float64)
+    assert not np.any(res["ids"] == V - 2)
+    p = _softmax64(np.where(np.arange(V) == V - 2, -np.inf, lg), T)
+    counts = np.bincount(res["ids"], minlength=V)
+    keep = p > 0
+    assert _chi2_p(counts[keep], p[keep]) > 1e-3
+    # row 0's key is its logit / T plus the oracle's Gumbel noise for that id
+    v = int(res["ids"][0])
+    key = np.float32(np.float32(res["logits"][0, v]) / np.float32(T)) + np.float32(o.gumbel(int(seeds[0]), 0, 0, 0, v))
+    assert res["best"][0] == np.float32(key)
+
+
+def check_audio_head_composition(o):
+    """The two-layer head selects over z W2^T + b2 with z from the first layer."""
+    rng = np.random.default_rng(65)
+    R, H, F, V = 4, 32, 24, 20
+    h = wl.f32_to_bf16(rng.standard_normal((R, H), dtype=np.float32))
+    W1 = wl.f32_to_bf16((rng.standard_normal((F, H)) / 6).astype(np.float32))
+    W2 = wl.f32_to_bf16((rng.standard_normal((V, F)) / 5).astype(np.float32))
+    b1 = rng.standard_normal(F).astype(np.float32)
+    b2 = rng.standard_normal(V).astype(np.float32)
+    out = o.audio_head(h, W1, b1, W2, b2, n_tail=2, tail_allowed=np.array([0, 1, 2, 3], np.uint32))
+    z, _ = o.audio_expand(h, W1, b1)
+    assert np.array_equal(out["z"], z)
+    _, _, ref = _masked_reference(z, W2, b2, 2, np.array([0, 1, 2, 3], np.uint32))
+    assert np.array_equal(out["ids"], ref)
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

@@ -44,7 +44,7 @@ MUTANTS = [
     ("attn: unnormalised weights", "const double p = s[t] / denom;", "const double p = s[t];"),
     ("head: W transposed", "load_elem(W, (size_t)v * H + k, is_bf16)", "load_elem(W, (size_t)k * V + v, is_bf16)"),
     ("head: highest index wins ties", "if (arg < 0 || key > top) {", "if (arg < 0 || key >= top) {"),
-    ("head: eos mask ignored", "? V - 1 : V;", "? V : V;"),
+    ("head: eos mask ignored", "mask[r] = eos_allowed[r] ? 1u : 0u;", "mask[r] = 1u;"),
     ("head: temperature multiplies", "key = logit / T + orc_gumbel", "key = logit * T + orc_gumbel"),
     ("head: noise indexed by row", "orc_gumbel(seed[r], step[r], 0u, 0u, (uint32_t)v)",
      "orc_gumbel(seed[r], step[r], 0u, 0u, (uint32_t)r)"),
@@ -69,6 +69,16 @@ MUTANTS = [
     ("fp8 append: keys unswizzled", "16 * ((d / 16) ^ (s % 8))", "16 * (d / 16)"),
     ("fp8 attn: values scaled by the key scale", "memcpy(&sc, tile + (is_v ? 4160 : 4096) + 4 * slot, 4);",
      "memcpy(&sc, tile + 4096 + 4 * slot, 4);"),
+    ("mish: softplus without the logarithm", "log1p(exp(x))", "exp(x)"),
+    ("mish: sign inside tanh", "return x * tanh(sp);", "return x * tanh(-sp);"),
+    ("bf16 rounding: truncation", "nearbyint(ldexp(m, 8))", "trunc(ldexp(m, 8))"),
+    ("bf16 rounding: one bit too many", "nearbyint(ldexp(m, 8))", "nearbyint(ldexp(m, 9))"),
+    ("audio expand: bias dropped", "double acc = b1 ? (double)b1[f] : 0.0;", "double acc = 0.0;"),
+    ("audio expand: W1 transposed", "load_elem(W1, (size_t)f * H + k, 1)", "load_elem(W1, (size_t)k * F + f, 1)"),
+    ("masked head: bias dropped", "double acc = b ? (double)b[v] : 0.0;", "double acc = 0.0;"),
+    ("masked head: tail offset", "const int j = v - (V - n_tail);", "const int j = v - (V - n_tail) - 1;"),
+    ("masked head: mask bits reversed", "!((tail_allowed[r] >> j) & 1u)",
+     "!((tail_allowed[r] >> (n_tail - 1 - j)) & 1u)"),
     ("verify: bonus always drawn", "if (!rejected && (flags & 1)) {", "if (!rejected) {"),
     ("verify: bonus from the last draft row",
      "target_logits + ((size_t)b * (K + 1) + K) * V;", "target_logits + ((size_t)b * (K + 1) + K - 1) * V;"),
