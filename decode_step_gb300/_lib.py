@@ -60,6 +60,8 @@ _SIGNATURES = {
     "tts_head_workspace_size": (_sz, [_i32, _i32]),
     "tts_codebook_head_select": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32,
                                                 _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "tts_audio_head_select": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _i32,
+                                             _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "tts_spec_verify": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _f32, _vp, _vp, _i32,
                                        _vp, _vp, _vp, _vp]),
     "tts_decode_step": (ctypes.c_int, [ctypes.POINTER(KVCacheDesc), _vp, _i32, _vp, _vp, _i32, _i32,

@@ -215,6 +215,30 @@ def tts_codebook_head_select(h, W, ids, ws, mode=TTS_ARGMAX, temperature=0.0, se
     check("tts_codebook_head_select", lib().tts_codebook_head_select(*args))
 
 
+def tts_audio_head_select(h, W1, b1, W2, b2, z, ids, ws, mode=TTS_ARGMAX, temperature=0.0, seed=None, step=None,
+                          n_tail=0, tail_allowed=None, best=None, logits_out=None, stream=None):
+    """The two-layer audio head: z = bf16(Mish(h W1^T + b1)) written to `z`
+    [R][F], then the head over z W2^T + b2 with the last n_tail ids masked per
+    row by tail_allowed (uint32 bits; None: all allowed).  bf16 weights; b1 / b2
+    float32 or None."""
+    R, H = h.shape
+    F, V = W1.shape[0], W2.shape[0]
+    for t, n in ((h, "h"), (W1, "W1"), (W2, "W2"), (z, "z")):
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{n} must be bfloat16")
+    if W1.shape[1] != H or W2.shape[1] != F:
+        raise ValueError("W1 must be [F][H] and W2 [V][F]")
+    args = (_dev(h, "h"), _dev(W1, "W1"), None if b1 is None else _dev(b1, "b1", torch.float32, (F,)),
+            _dev(W2, "W2"), None if b2 is None else _dev(b2, "b2", torch.float32, (V,)), R, H, F, V, int(n_tail),
+            None if tail_allowed is None else _dev(tail_allowed, "tail_allowed", torch.int32, (R,)),
+            int(mode), float(temperature), _keys(seed, "seed", R), _keys(step, "step", R),
+            _dev(z, "z", torch.bfloat16, (R, F)), _dev(ids, "ids", torch.int32, (R,)),
+            None if best is None else _dev(best, "best", torch.float32, (R,)),
+            None if logits_out is None else _dev(logits_out, "logits_out", torch.float32, (R, V)),
+            _dev(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
+    check("tts_audio_head_select", lib().tts_audio_head_select(*args))
+
+
 def tts_spec_verify(target_logits, draft_probs, draft_tokens, temperature, seed, step,
                     n_accepted, next_token, bonus=False, err=None, stream=None):
     B, K1, V = target_logits.shape

@@ -81,6 +81,10 @@ __device__ void finish_selection(const HeadWs &ws, int R, int32_t *ids, float *b
     if (threadIdx.x == 0) *ws.ticket = 0u;
 }
 
+// Head modes beyond the public TTS_ARGMAX / TTS_GUMBEL: the first layer of
+// the two-layer audio head writes Mish(h W^T + b) as bf16 instead of selecting.
+constexpr int kModeExpand = 2;
+
 struct HeadArgs {
     int R, H, V, mode;
     float temperature;
@@ -92,7 +96,17 @@ struct HeadArgs {
     float *best;
     HeadWs ws;
     int32_t *err;
+    const float *bias;        // [V] added to the logits (nullable)
+    const uint32_t *tail;     // [R] mask bits of the last n_tail ids (nullable: eos, else all allowed)
+    int n_tail;
+    __nv_bfloat16 *z_out;     // kModeExpand: [R][V] bf16
 };
+
+// Mish(x) = x tanh(ln(1 + e^x)) in fp32 (past x = 20, ln(1 + e^x) rounds to x).
+__device__ __forceinline__ float mish_f(float x) {
+    const float sp = x > 20.0f ? x : log1pf(expf(x));
+    return x * tanhf(sp);
+}
 
 // Margin (in Gumbel units) kept when skipping entries that cannot win; far
 // larger than the rounding of the threshold's exponentials.
@@ -460,7 +474,7 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
     // Item `item` -> its column, batch row, first vocabulary entry, the end of
     // the entries it may select, and its 8 summed logits (written out too if
     // asked).  False if the item selects nothing.
-    auto load_item = [&](int item, int &cn, int &r, int &v, int &vmax, float *lg) -> bool {
+    auto load_item = [&](int item, int &cn, int &r, int &v, uint32_t &allow, float *lg) -> bool {
         const int gi = item / N;
         cn = item - gi * N;
         r = r0 + cn;
@@ -475,14 +489,54 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
             for (int e = 0; e < 8; ++e) lg[e] += col[e * Lo.dump_stride];
         }
         v = v0 + rank * RS + gi * 8;  // multiple of 8
+        if (a.bias) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (v + e < a.V) lg[e] += a.bias[v + e];
+        }
         if (a.logits_out) {
 #pragma unroll
             for (int e = 0; e < 8; ++e)
                 if (v + e < a.V) a.logits_out[static_cast<size_t>(r) * a.V + v + e] = lg[e];
         }
-        vmax = (a.eos && !a.eos[r]) ? a.V - 1 : a.V;
-        return v < vmax;
+        // ids this row may choose: below the structural tail, or a tail id
+        // whose mask bit is set (the boundary token alone with eos_allowed)
+        int tail0 = a.V;
+        uint32_t tm = 0u;
+        if (a.tail) {
+            tail0 = a.V - a.n_tail;
+            tm = a.tail[r];
+        } else if (a.eos && !a.eos[r]) {
+            tail0 = a.V - 1;
+        }
+        allow = 0u;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int id = v + e;
+            const bool ok = id < a.V && (id < tail0 || ((tm >> (id - tail0)) & 1u));
+            allow |= ok ? 1u << e : 0u;
+        }
+        return allow != 0u;
     };
+    if (a.mode == kModeExpand) {
+        // first layer of the audio head: 8 features of one row per item, one
+        // 16-byte store of Mish(x + b) as bf16
+        for (int item = threadIdx.x; item < items; item += blockDim.x) {
+            int cn, r, v;
+            uint32_t allow;
+            float lg[8];
+            if (!load_item(item, cn, r, v, allow, lg)) continue;
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const __nv_bfloat162 p = __floats2bfloat162_rn(mish_f(lg[2 * q]), mish_f(lg[2 * q + 1]));
+                w[q] = *reinterpret_cast<const uint32_t *>(&p);
+            }
+            *reinterpret_cast<uint4 *>(a.z_out + static_cast<size_t>(r) * a.V + v) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        if (CK > 1) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+        return;
+    }
     if (a.mode == TTS_GUMBEL) {
         // An entry can only beat the column's current best z_cur if its noise
         // exceeds z_cur - logit / T.  With the group's largest logit that gives
@@ -490,12 +544,12 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
         // margin far above rounding) an entry cannot win, and its logarithms
         // are skipped.  Exact for the entries kept.  Two items per pass, so
         // each thread runs two independent Philox chains.
-        auto select = [&](bool live, int cn, int v, int vmax, const float *lg, const Philox4x64 &ph) {
+        auto select = [&](bool live, int cn, int v, uint32_t allow, const float *lg, const Philox4x64 &ph) {
             if (!live) return;
             float lmax = -INFINITY;
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                if (v + e < vmax) lmax = fmaxf(lmax, lg[e]);
+                if ((allow >> e) & 1u) lmax = fmaxf(lmax, lg[e]);
             const unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(colbest + cn);
             float thr = 0.0f;  // uniforms <= thr cannot win
             if (cur) {
@@ -505,7 +559,7 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
             unsigned long long best = 0ull;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                if (v + e >= vmax) break;
+                if (!((allow >> e) & 1u)) continue;
                 const float u = bits_to_uniform(ph.half(e));
                 if (!(u > thr)) continue;
                 const float key = lg[e] / a.temperature + gumbel_from_uniform(u);
@@ -516,25 +570,27 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
         };
         for (int i0 = threadIdx.x; i0 < items; i0 += 2 * blockDim.x) {
             const int i1 = i0 + blockDim.x;
-            int cn0, r0i, va, vmax0, cn1 = 0, r1i = 0, vb = 0, vmax1 = 0;
+            int cn0, r0i, va, cn1 = 0, r1i = 0, vb = 0;
+            uint32_t allow0, allow1 = 0u;
             float lg0[8], lg1[8];
-            const bool live0 = load_item(i0, cn0, r0i, va, vmax0, lg0);
-            const bool live1 = i1 < items && load_item(i1, cn1, r1i, vb, vmax1, lg1);
+            const bool live0 = load_item(i0, cn0, r0i, va, allow0, lg0);
+            const bool live1 = i1 < items && load_item(i1, cn1, r1i, vb, allow1, lg1);
             const int ra = live0 ? r0i : r0, rb = live1 ? r1i : r0;
             const Philox4x64 pa(static_cast<uint64_t>(va >> 3), 0, 0, 0, a.seed[ra], a.step[ra]);
             const Philox4x64 pb(static_cast<uint64_t>(vb >> 3), 0, 0, 0, a.seed[rb], a.step[rb]);
-            select(live0, cn0, va, vmax0, lg0, pa);
-            select(live1, cn1, vb, vmax1, lg1, pb);
+            select(live0, cn0, va, allow0, lg0, pa);
+            select(live1, cn1, vb, allow1, lg1, pb);
         }
     } else {
         for (int item = threadIdx.x; item < items; item += blockDim.x) {
-            int cn, r, v, vmax;
+            int cn, r, v;
+            uint32_t allow;
             float lg[8];
-            if (!load_item(item, cn, r, v, vmax, lg)) continue;
+            if (!load_item(item, cn, r, v, allow, lg)) continue;
             unsigned long long best = 0ull;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                if (v + e >= vmax) break;
+                if (!((allow >> e) & 1u)) continue;
                 const unsigned long long k = pack_argmax(lg[e], v + e);
                 best = k > best ? k : best;
             }
@@ -629,20 +685,37 @@ int prepare_head(const void *d_h, const void *d_W, int32_t dtype, int32_t R, int
                  int32_t mode, float temperature, const uint64_t *d_seed, const uint64_t *d_step,
                  const uint8_t *d_eos_allowed, int32_t *d_ids, float *d_best, float *d_logits_out,
                  void *d_ws, size_t ws_bytes, HeadLaunch *out) {
-    if (!d_h || !d_W || !d_ids) return TTS_ERR_INVALID;
+    return prepare_head_ex(d_h, d_W, dtype, R, H, V, mode, temperature, d_seed, d_step, d_eos_allowed, d_ids, d_best,
+                           d_logits_out, d_ws, ws_bytes, HeadExtras{}, out);
+}
+
+int prepare_head_ex(const void *d_h, const void *d_W, int32_t dtype, int32_t R, int32_t H, int32_t V,
+                    int32_t mode, float temperature, const uint64_t *d_seed, const uint64_t *d_step,
+                    const uint8_t *d_eos_allowed, int32_t *d_ids, float *d_best, float *d_logits_out,
+                    void *d_ws, size_t ws_bytes, const HeadExtras &x, HeadLaunch *out) {
+    const bool expand = mode == kModeExpand;
+    if (!d_h || !d_W || (!expand && !d_ids)) return TTS_ERR_INVALID;
     if (R < 1 || R > 4096 || H < 1 || V < 1 || V > (1 << 30)) return TTS_ERR_INVALID;
-    if (mode != TTS_ARGMAX && mode != TTS_GUMBEL) return TTS_ERR_INVALID;
+    if (mode != TTS_ARGMAX && mode != TTS_GUMBEL && !expand) return TTS_ERR_INVALID;
     if (mode == TTS_GUMBEL && (!d_seed || !d_step || !(temperature > 0.0f) || temperature == INFINITY))
         return TTS_ERR_INVALID;
+    if (x.n_tail < 0 || x.n_tail > 32 || x.n_tail > V) return TTS_ERR_INVALID;
     if (dtype != TTS_F32 && dtype != TTS_BF16) return TTS_ERR_UNSUPPORTED;
-    const size_t need = tts_head_workspace_size(R, V);
-    if (!d_ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(d_ws) & 255u) != 0)
-        return TTS_ERR_WORKSPACE;
+    if (dtype == TTS_F32 && (x.bias || x.tail || expand)) return TTS_ERR_UNSUPPORTED;
+    if (expand) {
+        // the first audio-head layer: 8 features per 16-byte store of z
+        if (!x.z_out || !aligned16(x.z_out) || V % 8 != 0) return TTS_ERR_INVALID;
+    } else {
+        const size_t need = tts_head_workspace_size(R, V);
+        if (!d_ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(d_ws) & 255u) != 0)
+            return TTS_ERR_WORKSPACE;
+    }
     HeadLaunchState *st = new (out->storage) HeadLaunchState();
     HeadArgs &a = st->a;
     a.R = R; a.H = H; a.V = V; a.mode = mode; a.temperature = temperature;
     a.seed = d_seed; a.step = d_step; a.eos = d_eos_allowed; a.logits_out = d_logits_out;
-    a.ids = d_ids; a.best = d_best; a.ws = head_ws(d_ws, R); a.err = nullptr;
+    a.ids = d_ids; a.best = d_best; a.ws = expand ? HeadWs{nullptr, nullptr} : head_ws(d_ws, R); a.err = nullptr;
+    a.bias = x.bias; a.tail = x.tail; a.n_tail = x.n_tail; a.z_out = static_cast<__nv_bfloat16 *>(x.z_out);
     st->dtype = dtype;
     st->h = d_h;
     st->W = d_W;
@@ -718,4 +791,38 @@ extern "C" int tts_codebook_head_select(const void *d_h, const void *d_W, int32_
                                      d_eos_allowed, d_ids, d_best, d_logits_out, d_ws, ws_bytes, &L);
     if (st != TTS_OK) return st;
     return tts::launch_head(L, {static_cast<cudaStream_t>(stream), false});
+}
+
+// The two-layer audio head ("TontaubeV1", section 3): z = Mish(h W1^T + b1)
+// as bf16, then the codebook head over z W2^T + b2 with the stage's
+// structural tail masked per row.  Two launches of the tcgen05 head; the
+// second is a programmatic dependent of the first (its W2 stream starts while
+// the first finishes; it reads z only after waiting).
+extern "C" int tts_audio_head_select(const void *d_h, const void *d_W1, const float *d_b1, const void *d_W2,
+                                     const float *d_b2, int32_t R, int32_t H, int32_t F, int32_t V, int32_t n_tail,
+                                     const uint32_t *d_tail_allowed, int32_t mode, float temperature,
+                                     const uint64_t *d_seed, const uint64_t *d_step, void *d_z, int32_t *d_ids,
+                                     float *d_best, float *d_logits_out, void *d_ws, size_t ws_bytes,
+                                     void *stream) {
+    using namespace tts;
+    if (mode != TTS_ARGMAX && mode != TTS_GUMBEL) return TTS_ERR_INVALID;
+    if (F < 8 || F % kTileK != 0) return TTS_ERR_UNSUPPORTED;  // F is the second layer's reduction
+    HeadExtras x1;
+    x1.bias = d_b1;
+    x1.z_out = d_z;
+    HeadLaunch L1, L2;
+    int st = prepare_head_ex(d_h, d_W1, TTS_BF16, R, H, F, kModeExpand, 0.0f, nullptr, nullptr, nullptr, nullptr,
+                             nullptr, nullptr, nullptr, 0, x1, &L1);
+    if (st != TTS_OK) return st;
+    HeadExtras x2;
+    x2.bias = d_b2;
+    x2.tail = n_tail > 0 ? d_tail_allowed : nullptr;
+    x2.n_tail = n_tail;
+    st = prepare_head_ex(d_z, d_W2, TTS_BF16, R, F, V, mode, temperature, d_seed, d_step, nullptr, d_ids, d_best,
+                         d_logits_out, d_ws, ws_bytes, x2, &L2);
+    if (st != TTS_OK) return st;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = launch_head(L1, {s, false});
+    if (st != TTS_OK) return st;
+    return launch_head(L2, {s, true});
 }

@@ -120,6 +120,18 @@ int prepare_head(const void *d_h, const void *d_W, int32_t dtype, int32_t R, int
                  int32_t mode, float temperature, const uint64_t *d_seed, const uint64_t *d_step,
                  const uint8_t *d_eos_allowed, int32_t *d_ids, float *d_best, float *d_logits_out,
                  void *d_ws, size_t ws_bytes, HeadLaunch *out);
+// The head with a bias, a mask over the last n_tail ids, or (mode 2) the
+// first audio-head layer writing Mish(h W^T + bias) as bf16 to z_out [R][V].
+struct HeadExtras {
+    const float *bias = nullptr;
+    const uint32_t *tail = nullptr;
+    int n_tail = 0;
+    void *z_out = nullptr;
+};
+int prepare_head_ex(const void *d_h, const void *d_W, int32_t dtype, int32_t R, int32_t H, int32_t V,
+                    int32_t mode, float temperature, const uint64_t *d_seed, const uint64_t *d_step,
+                    const uint8_t *d_eos_allowed, int32_t *d_ids, float *d_best, float *d_logits_out,
+                    void *d_ws, size_t ws_bytes, const HeadExtras &x, HeadLaunch *out);
 int launch_head(const HeadLaunch &L, LaunchOpts o);
 
 }  // namespace tts

@@ -282,6 +282,35 @@ int tts_spec_verify(const float *d_target_logits, const float *d_draft_probs,
                     int32_t flags, int32_t *d_n_accepted, int32_t *d_next_token,
                     int32_t *d_err, void *stream);
 
+/* ------------------------------------------------------------ audio head */
+
+/* The two-layer audio head ("TontaubeV1", section 3: each stage expands the
+ * transformer state to width 4,096, applies Mish and projects to its
+ * vocabulary; logits outside the stage's target vocabulary are masked at
+ * sampling), batched over R rows:
+ *   z[r][f] = bfloat16(Mish(sum_k h[r][k] W1[f][k] + b1[f])),
+ *             Mish(x) = x tanh(ln(1 + e^x)), computed in fp32;
+ *   logit[r][v] = fp32(sum_f z[r][f] W2[v][f] + b2[v]);
+ * then the choice of tts_codebook_head_select over the ids row r may take:
+ * every id below V - n_tail, and id V - n_tail + j when bit j of
+ * d_tail_allowed[r] is set (the stage's structural tokens; NULL: all
+ * allowed).  E.g. CB0: V = 16386 with n_tail = 2 (row terminator,
+ * <|audio_split|>); an acoustic stage: V = 4097, n_tail = 1 (the boundary).
+ *  d_h bf16 [R][H];  d_W1 bf16 [F][H];  d_b1 float [F] or NULL;
+ *  d_W2 bf16 [V][F];  d_b2 float [V] or NULL;  d_tail_allowed uint32 [R];
+ *  d_z bf16 [R][F], written (caller-owned, 16-byte aligned);
+ *  d_ids, d_best, d_logits_out, d_seed, d_step, mode, temperature, d_ws and
+ *  ws_bytes as tts_codebook_head_select (workspace tts_head_workspace_size(R, V)).
+ * Requires H and F multiples of 64, 0 <= n_tail <= 32.  Two kernels on
+ * `stream`; the projection starts streaming W2 while the first layer finishes.
+ * TTS_ERR_UNSUPPORTED for other shapes; TTS_ERR_INVALID for bad pointers or
+ * arguments. */
+int tts_audio_head_select(const void *d_h, const void *d_W1, const float *d_b1, const void *d_W2,
+                          const float *d_b2, int32_t R, int32_t H, int32_t F, int32_t V, int32_t n_tail,
+                          const uint32_t *d_tail_allowed, int32_t mode, float temperature,
+                          const uint64_t *d_seed, const uint64_t *d_step, void *d_z, int32_t *d_ids,
+                          float *d_best, float *d_logits_out, void *d_ws, size_t ws_bytes, void *stream);
+
 /* ----------------------------------------------------------- full step */
 
 /* One decode step in one call: tts_kv_append (tts_kv_append_rope when

@@ -223,3 +223,34 @@ def draft_model_outputs(B: int, K: int, V: int, rng: np.random.Generator):
     u = rng.random((B, K, 1)) * cdf[..., -1:]
     tokens = np.minimum((cdf < u).sum(axis=-1), V - 1).astype(np.int32)
     return probs, tokens
+
+
+# Two-layer audio head ("TontaubeV1", section 3): the transformer state is
+# expanded to width 4,096 through Mish, then projected to the stage's
+# vocabulary, whose last ids are the stage's structural tokens.
+AUDIO_HEAD_SHAPES = {
+    # name: (R, H, F, V, n_tail)
+    "acoustic-b64": (64, 2048, 4096, 4097, 1),   # an acoustic stage: 4,096 codes + the boundary
+    "semantic-cb0-b16": (16, 2048, 4096, 16386, 2),  # CB0: 16,384 codes + row terminator + <|audio_split|>
+}
+
+
+def audio_head_inputs(R: int, H: int, F: int, V: int, n_tail: int, seed: int = 4242) -> dict:
+    """Seeded inputs of the two-layer audio head: state h ~ N(0, 1); weights
+    and biases of both layers uniform in +-1/sqrt(fan_in), the usual
+    initialisation of a fresh linear layer (the pages' heads are newly
+    initialised; no trained weights exist here); per-row mask bits of the
+    structural tail drawn uniformly; Philox keys per row."""
+    rng = np.random.default_rng(seed)
+    a1, a2 = 1.0 / math.sqrt(H), 1.0 / math.sqrt(F)
+    out = dict(
+        h=f32_to_bf16(rng.standard_normal((R, H), dtype=np.float32)),
+        W1=f32_to_bf16(rng.uniform(-a1, a1, (F, H)).astype(np.float32)),
+        b1=rng.uniform(-a1, a1, F).astype(np.float32),
+        W2=f32_to_bf16(rng.uniform(-a2, a2, (V, F)).astype(np.float32)),
+        b2=rng.uniform(-a2, a2, V).astype(np.float32),
+        tail_allowed=rng.integers(0, 1 << n_tail, R).astype(np.uint32) if n_tail else np.zeros(R, np.uint32),
+        seed=(PHILOX_SEED_MUL * 97 + np.arange(R)).astype(np.uint64),
+        step=np.zeros(R, dtype=np.uint64),
+    )
+    return out
