@@ -58,6 +58,8 @@ def parse_args(argv=None):
                          "'workloads' object (comma-separated ids, 'f' suffix: FP8 E4M3 KV cache; "
                          "empty: none)")
     ap.add_argument("--sweep-reps", type=int, default=30)
+    ap.add_argument("--audio-heads", default="acoustic-b64,semantic-cb0-b16",
+                    help="two-layer audio-head shapes timed alone (names of workloads.AUDIO_HEAD_SHAPES; '' for none)")
     return ap.parse_args(argv)
 
 
@@ -404,6 +406,61 @@ def kernel_sweep(ids, reps, flush_l2, peaks, device) -> dict:
     return out
 
 
+def audio_head_bytes(R, H, F, V) -> int:
+    """Algorithmic bytes of one two-layer audio head: both weight matrices and
+    biases once, h, z written by the first layer and read by the second, the
+    row masks and the ids."""
+    return 2 * F * H + 4 * F + 2 * V * F + 4 * V + 2 * R * H + 2 * (2 * R * F) + 4 * R + 4 * R
+
+
+def audio_head_sweep(names, reps, flush_l2, peaks, device) -> dict:
+    """tts_audio_head_select (expansion + Mish, then the masked head) launched
+    alone `reps` times, L2 flushed before each, CUDA events around the call."""
+    import torch
+    from decode_step_gb300 import binding as bd
+
+    def dev(x):
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+        if x.dtype in (np.uint64, np.uint32):
+            return torch.from_numpy(x.view(np.int64 if x.dtype == np.uint64 else np.int32)).to(device)
+        return torch.from_numpy(np.ascontiguousarray(x)).to(device)
+
+    out = {}
+    for name in names:
+        R, H, F, V, n_tail = wl.AUDIO_HEAD_SHAPES[name]
+        inp = wl.audio_head_inputs(R, H, F, V, n_tail)
+        d = {k: dev(v) for k, v in inp.items()}
+        z = torch.empty((R, F), dtype=torch.bfloat16, device=device)
+        ids = torch.empty(R, dtype=torch.int32, device=device)
+        ws = torch.zeros(bd.tts_head_workspace_size(R, V), dtype=torch.uint8, device=device)
+        res = {}
+        for mode in ("argmax", "gumbel"):
+            m = bd.TTS_GUMBEL if mode == "gumbel" else bd.TTS_ARGMAX
+
+            def call():
+                bd.tts_audio_head_select(d["h"], d["W1"], d["b1"], d["W2"], d["b2"], z, ids, ws, mode=m,
+                                         temperature=0.7, seed=d["seed"], step=d["step"], n_tail=n_tail,
+                                         tail_allowed=d["tail_allowed"])
+            ts = []
+            for _ in range(reps):
+                flush_l2()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                call()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e3)
+            t = statistics.fmean(ts[2:])
+            nb = audio_head_bytes(R, H, F, V)
+            res[mode] = {"us": t, "gbs": nb / t / 1e3, "frac_hbm": nb / t / 1e3 / peaks["hbm_gbs"], "bytes": nb,
+                         "tflops": 2.0 * R * (H * F + F * V) / t / 1e6}
+        out[name] = {"shape": {"R": R, "H": H, "F": F, "V": V, "n_tail": n_tail}, **res}
+        del d, z, ids, ws
+        torch.cuda.empty_cache()
+    return out
+
+
 def workload_config(w, world):
     return {"workload": f"{w.name}: {w.B} streams/GPU, GQA {w.Hq}/{w.Hkv} heads, head_dim {w.D}, "
                         f"{w.dtype}, q_len {w.q_len}, ctx {w.ctx_dist} [{w.ctx_lo},{w.ctx_hi}], "
@@ -608,6 +665,9 @@ def run_native(args):
             del step, graphed, cache, W, d
             torch.cuda.empty_cache()
             line["workloads"] = kernel_sweep(ids, args.sweep_reps, flush_l2, peaks, device)
+        heads = [x.strip() for x in args.audio_heads.split(",") if x.strip()]
+        if heads:
+            line["audio_heads"] = audio_head_sweep(heads, args.sweep_reps, flush_l2, peaks, device)
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
