@@ -303,6 +303,22 @@ def _pinned(t: torch.Tensor, name: str, dtype=None, numel=None):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _graph_desc(cache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new, attn_out, attn_ws, scale,
+                W, ids, head_ws, h_inputs, d_inputs, h_ids, h_boundary_count, causal, mode, temperature, seed, step,
+                eos_allowed, best, logits_out, err, rope_base):
+    args = _step_args(cache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new, attn_out,
+                      attn_ws, scale, W, ids, head_ws, causal, rope_base, mode, temperature, seed, step,
+                      eos_allowed, best, logits_out, err, None)
+    R = ids.numel()
+    nbytes = h_inputs.numel() * h_inputs.element_size()
+    if d_inputs.numel() * d_inputs.element_size() != nbytes or not d_inputs.is_cuda:
+        raise ValueError("d_inputs must be a device tensor of h_inputs' size")
+    host = (_pinned(h_inputs, "h_inputs"), _dev(d_inputs, "d_inputs"), nbytes,
+            _pinned(h_ids, "h_ids", torch.int32, R),
+            None if h_boundary_count is None else _pinned(h_boundary_count, "h_boundary_count", torch.int32, 1))
+    return _lib.StepGraphDesc(ctypes.pointer(cache.desc), *args[1:-1], *host)
+
+
 class StepGraph:
     """tts_step_graph_*: a decode step captured once as a CUDA graph.
 
@@ -318,18 +334,9 @@ class StepGraph:
                  attn_out, attn_ws, scale, W, ids, head_ws, h_inputs, d_inputs, h_ids,
                  h_boundary_count=None, causal=False, mode=TTS_ARGMAX, temperature=0.0, seed=None,
                  step=None, eos_allowed=None, best=None, logits_out=None, err=None, rope_base=0.0):
-        args = _step_args(cache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new, attn_out,
-                          attn_ws, scale, W, ids, head_ws, causal, rope_base, mode, temperature, seed, step,
-                          eos_allowed, best, logits_out, err, None)
-        R = ids.numel()
-        nbytes = h_inputs.numel() * h_inputs.element_size()
-        if d_inputs.numel() * d_inputs.element_size() != nbytes or not d_inputs.is_cuda:
-            raise ValueError("d_inputs must be a device tensor of h_inputs' size")
-        host = (_pinned(h_inputs, "h_inputs"), _dev(d_inputs, "d_inputs"), nbytes,
-                _pinned(h_ids, "h_ids", torch.int32, R),
-                None if h_boundary_count is None else _pinned(h_boundary_count, "h_boundary_count",
-                                                              torch.int32, 1))
-        desc = _lib.StepGraphDesc(ctypes.pointer(cache.desc), *args[1:-1], *host)
+        desc = _graph_desc(cache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new, attn_out,
+                           attn_ws, scale, W, ids, head_ws, h_inputs, d_inputs, h_ids, h_boundary_count, causal,
+                           mode, temperature, seed, step, eos_allowed, best, logits_out, err, rope_base)
         handle = ctypes.c_void_p()
         check("tts_step_graph_create", lib().tts_step_graph_create(ctypes.byref(desc), ctypes.byref(handle)))
         self._handle = handle
@@ -345,6 +352,55 @@ class StepGraph:
     def close(self) -> None:
         if getattr(self, "_handle", None) is not None:
             lib().tts_step_graph_destroy(self._handle)
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class StepGraphSet:
+    """tts_step_graph_set_*: the step captured for several batch sizes.
+
+    Takes StepGraph's arguments for the largest size (every per-stream tensor
+    holding that many streams) plus `sizes` (increasing, the last the largest)
+    and the packed input regions: `regions` is a list of (byte offset, bytes
+    per stream) in h_inputs / d_inputs.  launch(n) runs the graph of the
+    smallest size >= n and returns that size."""
+
+    def __init__(self, cache: KVCache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new,
+                 attn_out, attn_ws, scale, W, ids, head_ws, h_inputs, d_inputs, h_ids, sizes, regions,
+                 h_boundary_count=None, causal=False, mode=TTS_ARGMAX, temperature=0.0, seed=None,
+                 step=None, eos_allowed=None, best=None, logits_out=None, err=None, rope_base=0.0):
+        desc = _graph_desc(cache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new, attn_out,
+                           attn_ws, scale, W, ids, head_ws, h_inputs, d_inputs, h_ids, h_boundary_count, causal,
+                           mode, temperature, seed, step, eos_allowed, best, logits_out, err, rope_base)
+        sz = (ctypes.c_int32 * len(sizes))(*[int(x) for x in sizes])
+        off = (ctypes.c_size_t * len(regions))(*[int(o) for o, _ in regions])
+        rb = (ctypes.c_size_t * len(regions))(*[int(b) for _, b in regions])
+        handle = ctypes.c_void_p()
+        check("tts_step_graph_set_create",
+              lib().tts_step_graph_set_create(ctypes.byref(desc), sz, len(sizes), off, rb, len(regions),
+                                              ctypes.byref(handle)))
+        self._handle = handle
+        self.sizes = [int(x) for x in sizes]
+        self._keep = (cache, block_table, ctx_before, ctx_lens, q, k_new, v_new, attn_out, attn_ws, W, ids,
+                      head_ws, h_inputs, d_inputs, h_ids, h_boundary_count, seed, step, eos_allowed, best,
+                      logits_out, err)
+
+    def launch(self, n_streams: int, stream=None) -> int:
+        if self._handle is None:
+            raise ValueError("graph set destroyed")
+        chosen = ctypes.c_int32(0)
+        check("tts_step_graph_set_launch",
+              lib().tts_step_graph_set_launch(self._handle, int(n_streams), ctypes.byref(chosen), _stream(stream)))
+        return chosen.value
+
+    def close(self) -> None:
+        if getattr(self, "_handle", None) is not None:
+            lib().tts_step_graph_set_destroy(self._handle)
             self._handle = None
 
     def __del__(self):

@@ -40,6 +40,32 @@ __global__ void __launch_bounds__(kCopyThreads) copy_from_host_kernel(uint4 *__r
     for (; i < n; i += stride) dst[i] = src[i];
 }
 
+// Up to kMaxSegs regions of the packed inputs: region i starts at byte
+// offset off[i] (a multiple of 16) of both buffers and spans bytes[i] bytes (a
+// multiple of 4).  A step for B streams copies the first B rows of each input.
+constexpr int kMaxSegs = 16;
+struct CopySegs {
+    unsigned long long off[kMaxSegs];
+    unsigned long long bytes[kMaxSegs];
+    int n;
+};
+
+__global__ void __launch_bounds__(kCopyThreads) copy_segments_from_host_kernel(uint8_t *__restrict__ dst,
+                                                                               const uint8_t *__restrict__ src,
+                                                                               const CopySegs segs) {
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    const size_t t0 = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (int i = 0; i < segs.n; ++i) {
+        const size_t words = segs.bytes[i] / 16, tail = (segs.bytes[i] % 16) / 4;
+        const uint4 *s16 = reinterpret_cast<const uint4 *>(src + segs.off[i]);
+        uint4 *d16 = reinterpret_cast<uint4 *>(dst + segs.off[i]);
+        for (size_t w = t0; w < words; w += stride) d16[w] = s16[w];
+        const uint32_t *s4 = reinterpret_cast<const uint32_t *>(src + segs.off[i] + words * 16);
+        uint32_t *d4 = reinterpret_cast<uint32_t *>(dst + segs.off[i] + words * 16);
+        if (t0 < tail) d4[t0] = s4[t0];
+    }
+}
+
 // h_ids[r] = d_ids[r]; *h_count = #{r : d_ids[r] == boundary} (if h_count).
 __global__ void __launch_bounds__(kCopyThreads) ids_to_host_kernel(const int32_t *__restrict__ d_ids, int R,
                                                                    int32_t boundary, int32_t *h_ids,
@@ -87,11 +113,17 @@ struct tts_step_graph {
     cudaGraphExec_t exec = nullptr;
 };
 
-extern "C" int tts_step_graph_create(const tts_step_graph_desc *d, tts_step_graph **out) {
-    using namespace tts;
-    if (!d || !out || !d->cache) return TTS_ERR_INVALID;
-    *out = nullptr;
-    if (d->B < 1) return TTS_ERR_INVALID;
+namespace tts {
+namespace {
+
+// Checks every argument of the step described by d (B streams), captures the
+// step and instantiates it.  With segs, the input copy moves those regions;
+// without, all of input_bytes.
+int capture_step(const tts_step_graph_desc *d, const CopySegs *segs, cudaGraph_t *graph_out,
+                 cudaGraphExec_t *exec_out) {
+    *graph_out = nullptr;
+    *exec_out = nullptr;
+    if (!d->cache || d->B < 1) return TTS_ERR_INVALID;
     // host transfers
     if (!d->h_inputs || !d->d_inputs || d->input_bytes == 0 || (d->input_bytes & 15u) != 0 ||
         !aligned16(d->h_inputs) || !aligned16(d->d_inputs) || !d->h_ids || !d->d_ids)
@@ -116,30 +148,36 @@ extern "C" int tts_step_graph_create(const tts_step_graph_desc *d, tts_step_grap
     if (st != TTS_OK) return st;
     const long long H = static_cast<long long>(d->num_q_heads) * c->head_dim;
     if (H > 0x7FFFFFFF) return TTS_ERR_INVALID;
-    st = prepare_head(d->d_attn_out, d->d_W, c->dtype == TTS_FP8_E4M3 ? TTS_BF16 : c->dtype, static_cast<int32_t>(R), static_cast<int32_t>(H), d->V,
-                      d->mode, d->temperature, d->d_seed, d->d_step, d->d_eos_allowed, d->d_ids, d->d_best,
-                      d->d_logits_out, d->d_head_ws, d->head_ws_bytes, &hd);
+    st = prepare_head(d->d_attn_out, d->d_W, c->dtype == TTS_FP8_E4M3 ? TTS_BF16 : c->dtype, static_cast<int32_t>(R),
+                      static_cast<int32_t>(H), d->V, d->mode, d->temperature, d->d_seed, d->d_step, d->d_eos_allowed,
+                      d->d_ids, d->d_best, d->d_logits_out, d->d_head_ws, d->head_ws_bytes, &hd);
     if (st != TTS_OK) return st;
 
-    tts_step_graph *g = new (std::nothrow) tts_step_graph();
-    if (!g) return TTS_ERR_CUDA;
     cudaStream_t s;
     if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) {
-        delete g;
         cudaGetLastError();
         return TTS_ERR_CUDA;
     }
     const int sms = sm_count() > 0 ? sm_count() : 148;
-    const size_t words = d->input_bytes / 16;
+    size_t words = d->input_bytes / 16;
+    if (segs) {
+        words = 0;
+        for (int i = 0; i < segs->n; ++i) words = segs->bytes[i] / 16 > words ? segs->bytes[i] / 16 : words;
+    }
     const size_t want = (words + kCopyThreads - 1) / kCopyThreads;
     const unsigned copy_ctas = static_cast<unsigned>(want < static_cast<size_t>(sms) * 4 ? (want > 0 ? want : 1)
                                                                                          : static_cast<size_t>(sms) * 4);
     // Relaxed capture: the launch helpers set function attributes, which is
     // not a stream operation.
+    cudaGraph_t graph = nullptr;
     bool ok = cudaStreamBeginCapture(s, cudaStreamCaptureModeRelaxed) == cudaSuccess;
     if (ok) {
-        copy_from_host_kernel<<<copy_ctas, kCopyThreads, 0, s>>>(static_cast<uint4 *>(d->d_inputs),
-                                                                 static_cast<const uint4 *>(d->h_inputs), words);
+        if (segs)
+            copy_segments_from_host_kernel<<<copy_ctas, kCopyThreads, 0, s>>>(
+                static_cast<uint8_t *>(d->d_inputs), static_cast<const uint8_t *>(d->h_inputs), *segs);
+        else
+            copy_from_host_kernel<<<copy_ctas, kCopyThreads, 0, s>>>(static_cast<uint4 *>(d->d_inputs),
+                                                                     static_cast<const uint4 *>(d->h_inputs), words);
         ok = cudaGetLastError() == cudaSuccess;
         ok = ok && launch_append(ap, {s, false}) == TTS_OK;
         ok = ok && launch_attn(at, {s, true}) == TTS_OK;
@@ -149,19 +187,35 @@ extern "C" int tts_step_graph_create(const tts_step_graph_desc *d, tts_step_grap
                                                           d->h_boundary_count);
             ok = cudaGetLastError() == cudaSuccess;
         }
-        cudaGraph_t graph = nullptr;
         const bool ended = cudaStreamEndCapture(s, &graph) == cudaSuccess;
         ok = ok && ended;
-        g->graph = graph;
-        if (ok) ok = cudaGraphInstantiate(&g->exec, g->graph, 0) == cudaSuccess;
+        if (ok) ok = cudaGraphInstantiate(exec_out, graph, 0) == cudaSuccess;
     }
     cudaStreamDestroy(s);
     if (!ok) {
         cudaGetLastError();
-        if (g->exec) cudaGraphExecDestroy(g->exec);
-        if (g->graph) cudaGraphDestroy(g->graph);
-        delete g;
+        if (*exec_out) cudaGraphExecDestroy(*exec_out);
+        if (graph) cudaGraphDestroy(graph);
+        *exec_out = nullptr;
         return TTS_ERR_CUDA;
+    }
+    *graph_out = graph;
+    return TTS_OK;
+}
+
+}  // namespace
+}  // namespace tts
+
+extern "C" int tts_step_graph_create(const tts_step_graph_desc *d, tts_step_graph **out) {
+    using namespace tts;
+    if (!d || !out) return TTS_ERR_INVALID;
+    *out = nullptr;
+    tts_step_graph *g = new (std::nothrow) tts_step_graph();
+    if (!g) return TTS_ERR_CUDA;
+    const int st = capture_step(d, nullptr, &g->graph, &g->exec);
+    if (st != TTS_OK) {
+        delete g;
+        return st;
     }
     *out = g;
     return TTS_OK;
@@ -181,4 +235,71 @@ extern "C" void tts_step_graph_destroy(tts_step_graph *g) {
     if (g->exec) cudaGraphExecDestroy(g->exec);
     if (g->graph) cudaGraphDestroy(g->graph);
     delete g;
+}
+
+// ------------------------------------------------------------ graph sets
+
+struct tts_step_graph_set {
+    int n = 0;
+    int32_t sizes[TTS_GRAPH_SET_MAX];
+    tts_step_graph graphs[TTS_GRAPH_SET_MAX];
+};
+
+extern "C" int tts_step_graph_set_create(const tts_step_graph_desc *d, const int32_t *sizes, int32_t n_sizes,
+                                         const size_t *seg_offset, const size_t *seg_row_bytes, int32_t n_segs,
+                                         tts_step_graph_set **out) {
+    using namespace tts;
+    if (!d || !out || !sizes || n_sizes < 1 || n_sizes > TTS_GRAPH_SET_MAX) return TTS_ERR_INVALID;
+    *out = nullptr;
+    if (!seg_offset || !seg_row_bytes || n_segs < 1 || n_segs > kMaxSegs) return TTS_ERR_INVALID;
+    for (int i = 0; i < n_sizes; ++i)
+        if (sizes[i] < 1 || sizes[i] > d->B || (i > 0 && sizes[i] <= sizes[i - 1])) return TTS_ERR_INVALID;
+    if (sizes[n_sizes - 1] != d->B) return TTS_ERR_INVALID;
+    // every region of B rows lies inside the packed buffers
+    for (int i = 0; i < n_segs; ++i) {
+        if ((seg_offset[i] & 15u) != 0 || (seg_row_bytes[i] & 3u) != 0 || seg_row_bytes[i] == 0) return TTS_ERR_INVALID;
+        if (seg_offset[i] >= d->input_bytes ||
+            seg_row_bytes[i] > (d->input_bytes - seg_offset[i]) / static_cast<size_t>(d->B))
+            return TTS_ERR_INVALID;
+    }
+    tts_step_graph_set *set = new (std::nothrow) tts_step_graph_set();
+    if (!set) return TTS_ERR_CUDA;
+    for (int k = 0; k < n_sizes; ++k) {
+        tts_step_graph_desc dk = *d;
+        dk.B = sizes[k];
+        CopySegs segs{};
+        segs.n = n_segs;
+        for (int i = 0; i < n_segs; ++i) {
+            segs.off[i] = seg_offset[i];
+            segs.bytes[i] = seg_row_bytes[i] * static_cast<size_t>(sizes[k]);
+        }
+        const int st = capture_step(&dk, &segs, &set->graphs[k].graph, &set->graphs[k].exec);
+        if (st != TTS_OK) {
+            tts_step_graph_set_destroy(set);
+            return st;
+        }
+        set->sizes[k] = sizes[k];
+        set->n = k + 1;
+    }
+    *out = set;
+    return TTS_OK;
+}
+
+extern "C" int tts_step_graph_set_launch(tts_step_graph_set *set, int32_t n_streams, int32_t *chosen_B,
+                                         void *stream) {
+    if (!set || n_streams < 1) return TTS_ERR_INVALID;
+    int k = 0;
+    while (k < set->n && set->sizes[k] < n_streams) ++k;
+    if (k == set->n) return TTS_ERR_INVALID;  // more streams than the largest size: split the cohort
+    if (chosen_B) *chosen_B = set->sizes[k];
+    return tts_step_graph_launch(&set->graphs[k], stream);
+}
+
+extern "C" void tts_step_graph_set_destroy(tts_step_graph_set *set) {
+    if (!set) return;
+    for (int k = 0; k < set->n; ++k) {
+        if (set->graphs[k].exec) cudaGraphExecDestroy(set->graphs[k].exec);
+        if (set->graphs[k].graph) cudaGraphDestroy(set->graphs[k].graph);
+    }
+    delete set;
 }

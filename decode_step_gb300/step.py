@@ -119,3 +119,106 @@ class GraphedStep:
         self.graph.launch(self.stream)
         self.stream.synchronize()
         return self.ids_host
+
+
+def choose_size(sizes, n: int):
+    """The smallest captured size that holds n streams, or None."""
+    for s in sizes:
+        if s >= n:
+            return s
+    return None
+
+
+def cohorts(n: int, largest: int):
+    """Split n streams into consecutive cohorts of at most `largest`: (first, count)."""
+    return [(s, min(largest, n - s)) for s in range(0, n, largest)]
+
+
+class GraphedStepSet:
+    """Captured serving steps for a set of batch sizes (tts_step_graph_set).
+
+    `step` is a DecodeStep for the largest size B; `inputs` maps input names
+    (as GraphedStep) to tensors with B streams in their first dimension.  One
+    pinned host buffer and its device mirror hold every input, one region per
+    name laid out for B streams; the graph of size b copies the first b rows
+    of each region.  `scratch_block` is a KV block no stream uses: streams past
+    the active ones of a launch get a table row of it, one new token at
+    position 0 and zero rows, so their work is harmless; their ids are
+    dropped.  `step_streams(arrays)` runs any number of streams: each cohort of
+    at most B streams is copied into the first rows, padded to the smallest
+    captured size, launched and read back.
+    """
+
+    PAD = {"ctx_before": 0, "q": 0, "k_new": 0, "v_new": 0, "seed": 0, "step": 0}
+
+    def __init__(self, step: DecodeStep, inputs: dict, sizes, scratch_block: int,
+                 stream: torch.cuda.Stream | None = None):
+        self.step, self.B = step, step.B
+        self.sizes = sorted(int(s) for s in sizes)
+        if self.sizes[-1] != self.B:
+            raise ValueError("the largest size must be the DecodeStep's batch")
+        offsets, total, rows = {}, 0, {}
+        for k, t in inputs.items():
+            if k not in GraphedStep.NAMES:
+                raise ValueError(f"unknown step input {k}")
+            if t.shape[0] != self.B:
+                raise ValueError(f"{k} must hold {self.B} streams in its first dimension")
+            offsets[k] = total
+            rows[k] = t.numel() * t.element_size() // self.B
+            total += -(-(t.numel() * t.element_size()) // 256) * 256
+        device = next(iter(inputs.values())).device
+        self.host_blob = torch.empty(total, dtype=torch.uint8, device="cpu").pin_memory()
+        self.dev_blob = torch.empty(total, dtype=torch.uint8, device=device)
+        self.host, self.dev = {}, {}
+        for k, t in inputs.items():
+            n = t.numel() * t.element_size()
+            self.host[k] = self.host_blob[offsets[k]:offsets[k] + n].view(t.dtype).view(t.shape)
+            self.dev[k] = self.dev_blob[offsets[k]:offsets[k] + n].view(t.dtype).view(t.shape)
+            self.host[k].copy_(t.detach().cpu())
+        self.regions = [(offsets[k], rows[k]) for k in inputs]
+        self.scratch_block = int(scratch_block)
+        self.ids_host = torch.zeros(step.R, dtype=torch.int32, device="cpu").pin_memory()
+        self.boundary_host = torch.zeros(1, dtype=torch.int32, device="cpu").pin_memory()
+        self.stream = torch.cuda.Stream() if stream is None else stream
+        d = self.dev
+        self.graphs = bd.StepGraphSet(
+            step.cache, d["block_table"], d["ctx_before"], d["ctx_lens"], step.max_ctx_len, d["q"],
+            d["k_new"], d["v_new"], step.out, step.attn_ws, step.scale, step.W, step.ids, step.head_ws,
+            self.host_blob, self.dev_blob, self.ids_host, self.sizes, self.regions, self.boundary_host,
+            causal=step.causal, mode=step.mode, temperature=step.temperature, seed=d.get("seed"),
+            step=d.get("step"), err=step.err, rope_base=step.rope_base)
+
+    def _pad(self, n: int, b: int) -> None:
+        """Streams n..b-1: the scratch block, one new token at position 0, zero rows."""
+        if b <= n:
+            return
+        h = self.host
+        h["block_table"][n:b] = self.scratch_block
+        h["ctx_lens"][n:b] = self.step.q_len
+        for k, v in self.PAD.items():
+            if k in h:
+                h[k][n:b] = v
+
+    def launch(self, n: int) -> torch.Tensor:
+        """Runs the first n streams as currently written in `host` (n at most
+        the largest size); returns the pinned ids of those streams."""
+        b = choose_size(self.sizes, n)
+        if b is None:
+            raise ValueError(f"{n} streams exceed the largest captured size {self.sizes[-1]}")
+        self._pad(n, b)
+        chosen = self.graphs.launch(n, self.stream)
+        assert chosen == b
+        self.stream.synchronize()
+        return self.ids_host[:n * self.step.q_len]
+
+    def step_streams(self, arrays: dict) -> torch.Tensor:
+        """One decode step for every stream of `arrays` (host tensors keyed
+        like `inputs`, streams in the first dimension, any count): cohorts of
+        at most the largest size run one after another.  Returns the ids."""
+        n = next(iter(arrays.values())).shape[0]
+        out = []
+        for first, count in cohorts(n, self.B):
+            for k, t in arrays.items():
+                self.host[k][:count] = t[first:first + count]
+            out.append(self.launch(count).clone())
+        return torch.cat(out) if out else torch.empty(0, dtype=torch.int32)

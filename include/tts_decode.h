@@ -413,6 +413,37 @@ int tts_step_graph_launch(tts_step_graph *graph, void *stream);
 /* Frees the graph (no GPU work of it may still be pending).  NULL is a no-op. */
 void tts_step_graph_destroy(tts_step_graph *graph);
 
+/* Captured steps for a set of batch sizes ("How We Made a TTS Model Respond
+ * in Sub-50 ms", section "Additional serving optimizations": graphs are
+ * captured for a predefined set of batch sizes, and an oversize cohort is
+ * split rather than run eagerly).  `desc` describes the step for the largest
+ * size (desc->B); every per-stream array it points to (and h_inputs /
+ * d_inputs) is laid out for desc->B streams.  The packed inputs consist of
+ * n_segs regions: region i starts at byte seg_offset[i] (a multiple of 16) of
+ * h_inputs and d_inputs and holds seg_row_bytes[i] bytes (a multiple of 4) per
+ * stream, streams in order.  For each size b in sizes[] (strictly increasing,
+ * the last equal to desc->B, at most TTS_GRAPH_SET_MAX of them) one graph is
+ * captured that runs the step on the first b streams: it copies the first b
+ * rows of every region, runs tts_decode_step with B = b on the same buffers,
+ * and writes b * q_len ids (and their boundary count) to h_ids.
+ * Errors as tts_step_graph_create; TTS_ERR_INVALID for bad sizes or regions
+ * outside input_bytes. */
+#define TTS_GRAPH_SET_MAX 16
+typedef struct tts_step_graph_set tts_step_graph_set;
+int tts_step_graph_set_create(const tts_step_graph_desc *desc, const int32_t *sizes, int32_t n_sizes,
+                              const size_t *seg_offset, const size_t *seg_row_bytes, int32_t n_segs,
+                              tts_step_graph_set **out);
+
+/* Launches the graph of the smallest captured size b >= n_streams (its size
+ * in *chosen_B if not NULL).  The caller has written the inputs of streams
+ * 0..n_streams-1 and made streams n_streams..b-1 harmless (e.g. a table row
+ * holding a scratch block, ctx_before 0); their ids are to be ignored.
+ * TTS_ERR_INVALID if n_streams exceeds the largest size (split the cohort). */
+int tts_step_graph_set_launch(tts_step_graph_set *set, int32_t n_streams, int32_t *chosen_B, void *stream);
+
+/* Frees every graph of the set (no GPU work of it may still be pending). */
+void tts_step_graph_set_destroy(tts_step_graph_set *set);
+
 /* ----------------------------------------------------------------- misc */
 
 /* Static description of a status code. */
