@@ -53,6 +53,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle baseline in the native line")
     ap.add_argument("--e2e-steps", type=int, default=1000)
+    ap.add_argument("--e2e-sizes", default="1,4,16,64",
+                    help="active-stream counts timed end to end through the captured-step set ('' for none)")
     ap.add_argument("--sweep", default="2,4,5,3f",
                     help="other workloads whose kernels are timed one by one into the line's "
                          "'workloads' object (comma-separated ids, 'f' suffix: FP8 E4M3 KV cache; "
@@ -607,6 +609,36 @@ def run_native(args):
     e2e_all = max_over_ranks(e2e_s / n_e2e * 1e3, world, device)
     _, e2e_value = combine_rank_times(e2e_all, w.B * w.q_len)
 
+    # ---- the captured-step set: graphs for batch sizes 1, 2, 4, ..., B; a
+    # step with n active streams runs the smallest size >= n (the rest padded
+    # onto a spare block); wall clock per step, host writes included.
+    e2e_sizes = {}
+    sizes_req = [int(x) for x in args.e2e_sizes.split(",") if x.strip()] if rank == 0 else []
+    if sizes_req:
+        from decode_step_gb300.step import GraphedStepSet
+        used = set(int(x) for x in inp["block_table"][inp["block_table"] >= 0].ravel())
+        spare = sorted(set(range(inp["num_blocks"])) - used)
+        sizes = [s for s in (1, 2, 4, 8, 16, 32, 64, 128, 256) if s < w.B] + [w.B]
+        if spare:
+            gset = GraphedStepSet(step, g_inputs, sizes, scratch_block=spare[0])
+            host_arrays = {k: t.detach().cpu() for k, t in g_inputs.items()}
+            for n in sizes_req:
+                if not 1 <= n <= w.B:
+                    continue
+                # the n streams' inputs written into the pinned views once (as
+                # the single-graph e2e above); each step: launch, sync, read ids
+                gset.step_streams({k: t[:n] for k, t in host_arrays.items()})
+                for _ in range(5):
+                    gset.launch(n)
+                reps = max(20, n_e2e // 4)
+                t0 = time.perf_counter()
+                for _ in range(reps):
+                    gset.launch(n)
+                us = (time.perf_counter() - t0) / reps * 1e6
+                e2e_sizes[str(n)] = {"us_per_step": us, "tokens_per_s": n * w.q_len / (us * 1e-6),
+                                     "graph_size": next(s for s in sizes if s >= n)}
+            del gset
+
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -651,6 +683,7 @@ def run_native(args):
                      "from a separate pass launching the kernels one by one",
         "device_error_flags": errflags,
         "clocks": clk,
+        "e2e_by_active_streams": e2e_sizes,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": n_e2e, "note": "wall clock; tts_step_graph (one CUDA graph captured by the "
                                         "library): a copy kernel reads the step's packed inputs from "

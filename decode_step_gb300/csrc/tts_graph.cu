@@ -53,16 +53,28 @@ struct CopySegs {
 __global__ void __launch_bounds__(kCopyThreads) copy_segments_from_host_kernel(uint8_t *__restrict__ dst,
                                                                                const uint8_t *__restrict__ src,
                                                                                const CopySegs segs) {
+    // One index space over every region's 16-byte words, so the reads of all
+    // regions are in flight together (each is a round trip to host memory).
+    size_t start[kMaxSegs + 1];
+    start[0] = 0;
+    for (int i = 0; i < segs.n; ++i) start[i + 1] = start[i] + segs.bytes[i] / 16;
+    const size_t total = start[segs.n];
     const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
     const size_t t0 = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    for (int i = 0; i < segs.n; ++i) {
+    for (size_t w = t0; w < total; w += stride) {
+        int i = 0;
+        while (w >= start[i + 1]) ++i;
+        const size_t o = segs.off[i] + (w - start[i]) * 16;
+        *reinterpret_cast<uint4 *>(dst + o) = *reinterpret_cast<const uint4 *>(src + o);
+    }
+    // 4-byte tails of the regions (at most 3 words each)
+    if (t0 < static_cast<size_t>(3 * segs.n)) {
+        const int i = static_cast<int>(t0 / 3), k = static_cast<int>(t0 % 3);
         const size_t words = segs.bytes[i] / 16, tail = (segs.bytes[i] % 16) / 4;
-        const uint4 *s16 = reinterpret_cast<const uint4 *>(src + segs.off[i]);
-        uint4 *d16 = reinterpret_cast<uint4 *>(dst + segs.off[i]);
-        for (size_t w = t0; w < words; w += stride) d16[w] = s16[w];
-        const uint32_t *s4 = reinterpret_cast<const uint32_t *>(src + segs.off[i] + words * 16);
-        uint32_t *d4 = reinterpret_cast<uint32_t *>(dst + segs.off[i] + words * 16);
-        if (t0 < tail) d4[t0] = s4[t0];
+        if (static_cast<size_t>(k) < tail) {
+            const size_t o = segs.off[i] + words * 16 + 4 * k;
+            *reinterpret_cast<uint32_t *>(dst + o) = *reinterpret_cast<const uint32_t *>(src + o);
+        }
     }
 }
 
@@ -162,7 +174,7 @@ int capture_step(const tts_step_graph_desc *d, const CopySegs *segs, cudaGraph_t
     size_t words = d->input_bytes / 16;
     if (segs) {
         words = 0;
-        for (int i = 0; i < segs->n; ++i) words = segs->bytes[i] / 16 > words ? segs->bytes[i] / 16 : words;
+        for (int i = 0; i < segs->n; ++i) words += segs->bytes[i] / 16;
     }
     const size_t want = (words + kCopyThreads - 1) / kCopyThreads;
     const unsigned copy_ctas = static_cast<unsigned>(want < static_cast<size_t>(sms) * 4 ? (want > 0 ? want : 1)
