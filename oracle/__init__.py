@@ -99,6 +99,8 @@ class Oracle:
         L.orc_head_select_masked.argtypes = ([_vp, _vp, ctypes.c_int, _vp] + [ctypes.c_int] * 4
                                              + [ctypes.c_float, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp])
         L.orc_head_select_masked.restype = ctypes.c_int
+        L.orc_code_predictor.argtypes = [ctypes.c_int] * 7 + [_vp] * 4 + [ctypes.c_int, ctypes.c_float] + [_vp] * 6
+        L.orc_code_predictor.restype = ctypes.c_int
         self.lib = L
 
     # ------------------------------------------------------------- random
@@ -307,6 +309,36 @@ class Oracle:
         z, _ = self.audio_expand(h, W1, b1)
         out = self.head_select_masked(z, W2, b2, mode, T, seed, step, n_tail, tail_allowed, want_logits)
         out["z"] = z
+        return out
+
+    # ----------------------------------------------------- code predictor
+    def code_predictor(self, x0, Wqkv, W, E, Hq, Hkv, mode="argmax", T=0.0, seed=None, step=None,
+                       want_trace=False):
+        """The code predictor's frame loop.  x0 [R][H], Wqkv [(Hq+2Hkv)D][H],
+        W [n_steps][V][Hq D], E [n_steps][V][H], all bf16 bits.  Returns
+        dict(tokens, best, second) [n_steps][R] and, with want_trace, trace
+        [n_steps][R][(Hq+2Hkv)D + Hq D] (bf16 values of q, k, v, o)."""
+        R, H = x0.shape
+        F = Wqkv.shape[0]
+        n_steps, V, HO = W.shape
+        D = HO // Hq
+        assert F == (Hq + 2 * Hkv) * D and E.shape == (n_steps, V, H) and Wqkv.shape[1] == H
+        m = {"argmax": 0, "gumbel": 1}[mode]
+        seed = np.zeros(R, np.uint64) if seed is None else np.ascontiguousarray(seed, dtype=np.uint64)
+        step = np.zeros(R, np.uint64) if step is None else np.ascontiguousarray(step, dtype=np.uint64)
+        tokens = np.zeros((n_steps, R), np.int32)
+        best = np.zeros((n_steps, R), np.float32)
+        second = np.zeros((n_steps, R), np.float32)
+        trace = np.zeros((n_steps, R, F + HO), np.float64) if want_trace else None
+        rc = self.lib.orc_code_predictor(R, H, Hq, Hkv, D, V, n_steps, _ptr(np.ascontiguousarray(x0)),
+                                         _ptr(np.ascontiguousarray(Wqkv)), _ptr(np.ascontiguousarray(W)),
+                                         _ptr(np.ascontiguousarray(E)), m, float(T), _ptr(seed), _ptr(step),
+                                         _ptr(tokens), _ptr(best), _ptr(second), _ptr(trace))
+        if rc != 0:
+            raise ValueError("oracle code_predictor: bad arguments")
+        out = dict(tokens=tokens, best=best, second=second)
+        if want_trace:
+            out["trace"] = trace
         return out
 
     # ------------------------------------------------------------- verify

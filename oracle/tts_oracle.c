@@ -22,6 +22,8 @@
  *         4,096 entries, boundary token, later stages at temperature zero).
  *  [SAL]  Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
  *         1, 2, 3", SC'11: the Philox4x64-10 bijection.
+ *  [NAR]  "How We Made a TTS Model Respond in Sub-50 ms" (the code predictor's
+ *         fixed loop and its captured graph).
  *  [MIS]  Misra, "Mish: A Self Regularized Non-Monotonic Activation Function"
  *         (2019): Mish(x) = x tanh(ln(1 + e^x)).
  *
@@ -430,10 +432,10 @@ int orc_audio_expand(const uint16_t *h, const uint16_t *W1, const float *b1, int
  * V - n_tail .. V - 1 are the structural tokens; id V - n_tail + j may be
  * chosen for row r only if bit j of tail_allowed[r] is set (tail_allowed NULL:
  * all may).  Selection as orc_head_select over the allowed ids. */
-int orc_head_select_masked(const void *h, const void *W, int is_bf16, const float *b, int R, int H, int V,
-                           int mode, float T, const uint64_t *seed, const uint64_t *step, int n_tail,
-                           const uint32_t *tail_allowed, int32_t *ids, float *best, float *second,
-                           float *logits_out) {
+static int head_select_at(const void *h, const void *W, int is_bf16, const float *b, int R, int H, int V,
+                          int mode, float T, const uint64_t *seed, const uint64_t *step, uint32_t pos, int n_tail,
+                          const uint32_t *tail_allowed, int32_t *ids, float *best, float *second,
+                          float *logits_out) {
     if (R < 0 || H <= 0 || V <= 0 || (mode != 0 && mode != 1) || n_tail < 0 || n_tail > 32 || n_tail > V)
         return -1;
     if (mode == 1 && !(T > 0.0f)) return -1;
@@ -449,7 +451,7 @@ int orc_head_select_masked(const void *h, const void *W, int is_bf16, const floa
             const int j = v - (V - n_tail);
             if (j >= 0 && tail_allowed && !((tail_allowed[r] >> j) & 1u)) continue;
             float key = logit;
-            if (mode == 1) key = logit / T + orc_gumbel(seed[r], step[r], 0u, 0u, (uint32_t)v);
+            if (mode == 1) key = logit / T + orc_gumbel(seed[r], step[r], 0u, pos, (uint32_t)v);
             if (arg < 0 || key > top) {
                 next = top;
                 top = key;
@@ -463,6 +465,16 @@ int orc_head_select_masked(const void *h, const void *W, int is_bf16, const floa
         if (second) second[r] = next;
     }
     return 0;
+}
+
+/* The selection above with the Gumbel counter's position 0 (one draw per
+ * vocabulary entry and step). */
+int orc_head_select_masked(const void *h, const void *W, int is_bf16, const float *b, int R, int H, int V,
+                           int mode, float T, const uint64_t *seed, const uint64_t *step, int n_tail,
+                           const uint32_t *tail_allowed, int32_t *ids, float *best, float *second,
+                           float *logits_out) {
+    return head_select_at(h, W, is_bf16, b, R, H, V, mode, T, seed, step, 0u, n_tail, tail_allowed, ids, best,
+                          second, logits_out);
 }
 
 /* Codebook head and token choice [TON, section 3]: logits[r][v] = h[r] . W[v]
@@ -489,6 +501,100 @@ int orc_head_select(const void *h, const void *W, int is_bf16, int R, int H, int
                                           mask, ids, best, second, logits_out);
     free(mask);
     return rc;
+}
+
+/* ---------------------------------------------------------- code predictor */
+
+/* The code predictor's frame loop ([NAR], "Exploiting the regular building of
+ * the Code Predictor" / "Turn a fixed predictor loop into one GPU program": a
+ * fixed number of autoregressive steps per frame, one per remaining codebook,
+ * over a short bounded context held in a preallocated KV cache).  The pages
+ * give no architecture; the reading is the smallest loop on this path's
+ * primitives.  For every stream r, with x = x0[r] (the talker's state for the
+ * frame) and an empty cache, for step i = 0 .. n_steps-1:
+ *   qkv = bf16(x Wqkv^T)            q [Hq][D], k and v [Hkv][D]
+ *   cache position i <- k, v
+ *   o_h = bf16(sum_t softmax_t(scale q_h . k_t[g(h)]) v_t[g(h)]), t = 0..i,
+ *         g(h) = h / (Hq / Hkv), scale = 1 / sqrt(D)
+ *   logit[v] = float(o . W_i[v]), token = argmax of logit (mode 0) or of
+ *         logit / T + Gumbel noise (tag 0, pos i + 1, idx v) (mode 1)
+ *   x = E_i[token]                  (the embedding of step i's codebook)
+ * x0, Wqkv [(Hq + 2 Hkv) D][H], W [n_steps][V][Hq D] and E [n_steps][V][H] are
+ * bf16 bit patterns; tokens, best and second are [n_steps][R].  With trace
+ * (nullable, doubles): per step and stream the bf16 values of q, k, v and o
+ * ([n_steps][R][(Hq + 2 Hkv) D + Hq D]). */
+int orc_code_predictor(int R, int H, int Hq, int Hkv, int D, int V, int n_steps, const uint16_t *x0,
+                       const uint16_t *Wqkv, const uint16_t *W, const uint16_t *E, int mode, float T,
+                       const uint64_t *seed, const uint64_t *step, int32_t *tokens, float *best, float *second,
+                       double *trace) {
+    if (R < 0 || H <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || V <= 0 || n_steps <= 0 ||
+        n_steps > ORC_BLOCK || (mode != 0 && mode != 1) || (mode == 1 && !(T > 0.0f)))
+        return -1;
+    const int F = (Hq + 2 * Hkv) * D, HO = Hq * D, group = Hq / Hkv;
+    const double scale = 1.0 / sqrt((double)D);
+    double *x = malloc(sizeof(double) * (size_t)H);
+    double *qkv = malloc(sizeof(double) * (size_t)F);
+    double *kc = malloc(sizeof(double) * (size_t)n_steps * Hkv * D);
+    double *vc = malloc(sizeof(double) * (size_t)n_steps * Hkv * D);
+    double *o = malloc(sizeof(double) * (size_t)HO);
+    double *sc = malloc(sizeof(double) * (size_t)n_steps);
+    uint16_t *ob = malloc(sizeof(uint16_t) * (size_t)HO);
+    if (!x || !qkv || !kc || !vc || !o || !sc || !ob) {
+        free(x); free(qkv); free(kc); free(vc); free(o); free(sc); free(ob);
+        return -1;
+    }
+    for (int r = 0; r < R; ++r) {
+        for (int k = 0; k < H; ++k) x[k] = load_elem(x0, (size_t)r * H + k, 1);
+        for (int i = 0; i < n_steps; ++i) {
+            for (int f = 0; f < F; ++f) {
+                double acc = 0.0;
+                for (int k = 0; k < H; ++k) acc += x[k] * load_elem(Wqkv, (size_t)f * H + k, 1);
+                const uint16_t b = orc_bf16_round(acc);
+                qkv[f] = load_elem(&b, 0, 1);
+            }
+            const double *q = qkv, *kn = qkv + HO, *vn = qkv + HO + Hkv * D;
+            memcpy(kc + (size_t)i * Hkv * D, kn, sizeof(double) * (size_t)Hkv * D);
+            memcpy(vc + (size_t)i * Hkv * D, vn, sizeof(double) * (size_t)Hkv * D);
+            for (int h = 0; h < Hq; ++h) {
+                const int kvh = h / group;
+                double m = -INFINITY;
+                for (int t = 0; t <= i; ++t) {
+                    double dot = 0.0;
+                    for (int d = 0; d < D; ++d) dot += q[h * D + d] * kc[((size_t)t * Hkv + kvh) * D + d];
+                    sc[t] = scale * dot;
+                    if (sc[t] > m) m = sc[t];
+                }
+                double denom = 0.0;
+                for (int t = 0; t <= i; ++t) {
+                    sc[t] = exp(sc[t] - m);
+                    denom += sc[t];
+                }
+                for (int d = 0; d < D; ++d) {
+                    double acc = 0.0;
+                    for (int t = 0; t <= i; ++t) acc += sc[t] / denom * vc[((size_t)t * Hkv + kvh) * D + d];
+                    ob[h * D + d] = orc_bf16_round(acc);
+                    o[h * D + d] = load_elem(ob, (size_t)(h * D + d), 1);
+                }
+            }
+            if (trace) {
+                double *tr = trace + ((size_t)i * R + r) * (size_t)(F + HO);
+                memcpy(tr, qkv, sizeof(double) * (size_t)F);
+                memcpy(tr + F, o, sizeof(double) * (size_t)HO);
+            }
+            const size_t at = (size_t)i * R + r;
+            int32_t arg;
+            float top, next;
+            head_select_at(ob, W + (size_t)i * V * HO, 1, NULL, 1, HO, V, mode, T, seed ? seed + r : NULL,
+                           step ? step + r : NULL, (uint32_t)(i + 1), 0, NULL, &arg, &top, &next, NULL);
+            tokens[at] = arg;
+            if (best) best[at] = top;
+            if (second) second[at] = next;
+            const uint16_t *Ei = E + (size_t)i * V * H;
+            for (int k = 0; k < H; ++k) x[k] = load_elem(Ei, (size_t)arg * H + k, 1);
+        }
+    }
+    free(x); free(qkv); free(kc); free(vc); free(o); free(sc); free(ob);
+    return 0;
 }
 
 /* ------------------------------------------------------------------ verify */

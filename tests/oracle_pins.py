@@ -780,4 +780,99 @@ def check_audio_head_composition(o):
     assert np.array_equal(out["ids"], ref)
 
 
+# --------------------------------------------------------- code predictor
+
+def predictor_case(seed, R=3, H=64, Hq=4, Hkv=2, D=16, V=40, n_steps=15):
+    rng = np.random.default_rng(seed)
+    F = (Hq + 2 * Hkv) * D
+    return dict(
+        x0=wl.f32_to_bf16(rng.standard_normal((R, H), dtype=np.float32)),
+        Wqkv=wl.f32_to_bf16((rng.standard_normal((F, H)) / 6).astype(np.float32)),
+        W=wl.f32_to_bf16((rng.standard_normal((n_steps, V, Hq * D)) / 4).astype(np.float32)),
+        E=wl.f32_to_bf16(rng.standard_normal((n_steps, V, H)).astype(np.float32)),
+        Hq=Hq, Hkv=Hkv, D=D)
+
+
+def check_code_predictor_stages(o):
+    """Each step of the loop against library routines: the projection is a
+    numpy float64 matmul rounded to bf16, the attention torch's float64 SDPA
+    (GQA, keys and values of steps 0..i) rounded to bf16, the token numpy's
+    argmax of float32 logits, and the next input the chosen token's row of
+    that step's embedding; step 0 attends to one token, so o equals its v."""
+    import torch
+    c = predictor_case(71)
+    Hq, Hkv, D = c["Hq"], c["Hkv"], c["D"]
+    res = o.code_predictor(c["x0"], c["Wqkv"], c["W"], c["E"], Hq, Hkv, want_trace=True)
+    n_steps, R = res["tokens"].shape
+    HO, F = Hq * D, (Hq + 2 * Hkv) * D
+    f64 = lambda b: wl.bf16_to_f32(b).astype(np.float64)
+    Wqkv, W, E = f64(c["Wqkv"]), f64(c["W"]), f64(c["E"])
+    for r in range(R):
+        x = f64(c["x0"][r])
+        ks, vs = [], []
+        for i in range(n_steps):
+            tr = res["trace"][i, r]
+            qkv = f64(o.bf16_round(Wqkv @ x))
+            assert np.array_equal(tr[:F], qkv)
+            q = qkv[:HO].reshape(Hq, D)
+            ks.append(qkv[HO:HO + Hkv * D].reshape(Hkv, D))
+            vs.append(qkv[HO + Hkv * D:].reshape(Hkv, D))
+            K = torch.from_numpy(np.repeat(np.stack(ks, 1), Hq // Hkv, axis=0))   # [Hq][t][D]
+            Vv = torch.from_numpy(np.repeat(np.stack(vs, 1), Hq // Hkv, axis=0))
+            att = torch.nn.functional.scaled_dot_product_attention(
+                torch.from_numpy(q)[:, None, :], K, Vv, scale=1.0 / math.sqrt(D))[:, 0, :].numpy()
+            ob = o.bf16_round(att.reshape(-1))
+            assert np.array_equal(tr[F:], f64(ob))
+            if i == 0:
+                assert np.array_equal(tr[F:], np.repeat(vs[0], Hq // Hkv, axis=0).reshape(-1))
+            logits = (W[i] @ tr[F:]).astype(np.float32)
+            assert res["tokens"][i, r] == int(np.argmax(logits))
+            x = E[i, res["tokens"][i, r]]
+
+
+def check_code_predictor_gumbel_keys(o):
+    """Gumbel mode: step i's token maximises float32(logit) / T plus the noise
+    of counter position i + 1, and best holds that key."""
+    c = predictor_case(72, R=2, V=24, n_steps=6)
+    T = 0.8
+    seed = np.array([11, 12], np.uint64)
+    step = np.array([5, 9], np.uint64)
+    res = o.code_predictor(c["x0"], c["Wqkv"], c["W"], c["E"], c["Hq"], c["Hkv"], "gumbel", T, seed, step,
+                           want_trace=True)
+    F = (c["Hq"] + 2 * c["Hkv"]) * c["D"]
+    W = wl.bf16_to_f32(c["W"]).astype(np.float64)
+    for i in range(6):
+        for r in range(2):
+            logits = (W[i] @ res["trace"][i, r, F:]).astype(np.float32)
+            keys = np.array([np.float32(logits[v] / np.float32(T)) +
+                             np.float32(o.gumbel(int(seed[r]), int(step[r]), 0, i + 1, v)) for v in range(24)],
+                            np.float32)
+            assert res["tokens"][i, r] == int(np.argmax(keys))
+            assert res["best"][i, r] == keys.max()
+
+
+def check_code_predictor_uniform_attention(o):
+    """Zero key projections make every score zero: o is the bf16 mean of the
+    values of steps 0..i (per KV head)."""
+    c = predictor_case(73, R=2, n_steps=8)
+    Hq, Hkv, D = c["Hq"], c["Hkv"], c["D"]
+    HO = Hq * D
+    Wqkv = c["Wqkv"].copy()
+    Wqkv[HO:HO + Hkv * D] = 0
+    res = o.code_predictor(c["x0"], Wqkv, c["W"], c["E"], Hq, Hkv, want_trace=True)
+    F = (Hq + 2 * Hkv) * D
+    for r in range(2):
+        vs = []
+        for i in range(8):
+            tr = res["trace"][i, r]
+            assert not tr[HO:HO + Hkv * D].any()
+            vs.append(tr[HO + Hkv * D:F].reshape(Hkv, D))
+            mean = np.repeat(np.mean(np.stack(vs), axis=0), Hq // Hkv, axis=0).reshape(-1)
+            # a nearest bf16 of the mean (the mean of bf16 values can sit on a
+            # rounding midpoint, where the summation order picks the side)
+            got = tr[F:]
+            half_ulp = np.abs(wl.bf16_to_f32(o.bf16_round(mean)).astype(np.float64)) * 2.0 ** -8
+            assert np.all(np.abs(got - mean) <= half_ulp * (1 + 1e-9) + 1e-300)
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

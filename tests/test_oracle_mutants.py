@@ -46,8 +46,18 @@ MUTANTS = [
     ("head: highest index wins ties", "if (arg < 0 || key > top) {", "if (arg < 0 || key >= top) {"),
     ("head: eos mask ignored", "mask[r] = eos_allowed[r] ? 1u : 0u;", "mask[r] = 1u;"),
     ("head: temperature multiplies", "key = logit / T + orc_gumbel", "key = logit * T + orc_gumbel"),
-    ("head: noise indexed by row", "orc_gumbel(seed[r], step[r], 0u, 0u, (uint32_t)v)",
-     "orc_gumbel(seed[r], step[r], 0u, 0u, (uint32_t)r)"),
+    ("head: noise indexed by row", "orc_gumbel(seed[r], step[r], 0u, pos, (uint32_t)v)",
+     "orc_gumbel(seed[r], step[r], 0u, pos, (uint32_t)r)"),
+    ("head: counter position ignored", "return head_select_at(h, W, is_bf16, b, R, H, V, mode, T, seed, step, 0u,",
+     "return head_select_at(h, W, is_bf16, b, R, H, V, mode, T, seed, step, 1u,"),
+    ("predictor: attention one token short", "for (int t = 0; t <= i; ++t) {\n                    double dot",
+     "for (int t = 0; t < i || t == 0; ++t) {\n                    double dot"),
+    ("predictor: embedding of the next codebook", "const uint16_t *Ei = E + (size_t)i * V * H;",
+     "const uint16_t *Ei = E + (size_t)(i + 1 < n_steps ? i + 1 : i) * V * H;"),
+    ("predictor: Gumbel position of the step", "(uint32_t)(i + 1), 0, NULL", "(uint32_t)i, 0, NULL"),
+    ("predictor: projection not rounded", "qkv[f] = load_elem(&b, 0, 1);", "qkv[f] = acc + 0.0 * b;"),
+    ("predictor: values read from the keys", "acc += sc[t] / denom * vc[", "acc += sc[t] / denom * kc["),
+    ("predictor: GQA map", "const int kvh = h / group;", "const int kvh = h % Hkv;"),
     ("verify: accept test reversed", "accepted = u < ratio;", "accepted = u > ratio;"),
     ("verify: zero draft probability accepted", "if (dp[d] > 0.0f) {", "if (dp[d] >= 0.0f) {"),
     ("verify: residual not clamped", "fmaxf(pt[v] - dp[v], 0.0f)", "fabsf(pt[v] - dp[v])"),
