@@ -42,6 +42,14 @@ class StepGraphDesc(ctypes.Structure):
                 ("input_bytes", _sz), ("h_ids", _vp), ("h_boundary_count", _vp)]
 
 
+class CodePredictorDesc(ctypes.Structure):
+    """tts_code_predictor_desc."""
+    _fields_ = [("R", _i32), ("H", _i32), ("num_q_heads", _i32), ("num_kv_heads", _i32), ("head_dim", _i32),
+                ("V", _i32), ("n_steps", _i32), ("mode", _i32), ("temperature", _f32), ("d_x0", _vp),
+                ("d_Wqkv", _vp), ("d_W", _vp), ("d_E", _vp), ("d_seed", _vp), ("d_step", _vp), ("d_tokens", _vp),
+                ("d_ws", _vp), ("ws_bytes", _sz), ("d_err", _vp)]
+
+
 _SIGNATURES = {
     "tts_block_pool_create": (ctypes.c_int, [_i32, ctypes.POINTER(_vp)]),
     "tts_block_pool_alloc": (ctypes.c_int, [_vp, _i32, _vp]),
@@ -75,6 +83,11 @@ _SIGNATURES = {
                                                  ctypes.POINTER(_vp)]),
     "tts_step_graph_set_launch": (ctypes.c_int, [_vp, _i32, _vp, _vp]),
     "tts_step_graph_set_destroy": (None, [_vp]),
+    "tts_code_predictor_workspace_size": (_sz, [_i32] * 7),
+    "tts_code_predictor_run": (ctypes.c_int, [ctypes.POINTER(CodePredictorDesc), _vp]),
+    "tts_code_predictor_graph_create": (ctypes.c_int, [ctypes.POINTER(CodePredictorDesc), ctypes.POINTER(_vp)]),
+    "tts_code_predictor_graph_launch": (ctypes.c_int, [_vp, _vp]),
+    "tts_code_predictor_graph_destroy": (None, [_vp]),
     "tts_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "tts_version": (ctypes.c_int, []),
 }

@@ -410,6 +410,59 @@ class StepGraphSet:
             pass
 
 
+class CodePredictor:
+    """tts_code_predictor_*: the code predictor's frame loop on caller tensors.
+
+    x0 [R][H], Wqkv [(Hq + 2 Hkv) * 128][H], W [n_steps][V][H], E
+    [n_steps][V][H] (bf16, device); tokens int32 [n_steps][R] is written by
+    each run.  The workspace is allocated here.  With graph=True the loop is
+    captured once and run() launches the graph."""
+
+    def __init__(self, x0, Wqkv, W, E, num_q_heads, num_kv_heads, tokens, mode=TTS_ARGMAX, temperature=0.0,
+                 seed=None, step=None, err=None, graph=False):
+        R, H = x0.shape
+        n_steps, V, HW = W.shape
+        D = H // num_q_heads
+        for t, n in ((x0, "x0"), (Wqkv, "Wqkv"), (W, "W"), (E, "E")):
+            if t.dtype != torch.bfloat16:
+                raise ValueError(f"{n} must be bfloat16")
+        if HW != H or tuple(E.shape) != (n_steps, V, H) or Wqkv.shape[1] != H:
+            raise ValueError("W and E must be [n_steps][V][H], Wqkv [F][H]")
+        nbytes = lib().tts_code_predictor_workspace_size(R, H, num_q_heads, num_kv_heads, D, V, n_steps)
+        if nbytes == 0:
+            raise ValueError("unsupported code predictor shape")
+        self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=x0.device)
+        self.desc = _lib.CodePredictorDesc(
+            R, H, num_q_heads, num_kv_heads, D, V, n_steps, int(mode), float(temperature), _dev(x0, "x0"),
+            _dev(Wqkv, "Wqkv"), _dev(W, "W"), _dev(E, "E"), _keys(seed, "seed", R), _keys(step, "step", R),
+            _dev(tokens, "tokens", torch.int32, (n_steps, R)), _dev(self.ws, "ws"), nbytes,
+            None if err is None else _dev(err, "err", torch.int32))
+        self._keep = (x0, Wqkv, W, E, tokens, seed, step, err)
+        self._graph = None
+        if graph:
+            handle = ctypes.c_void_p()
+            check("tts_code_predictor_graph_create",
+                  lib().tts_code_predictor_graph_create(ctypes.byref(self.desc), ctypes.byref(handle)))
+            self._graph = handle
+
+    def run(self, stream=None) -> None:
+        if self._graph is not None:
+            check("tts_code_predictor_graph_launch", lib().tts_code_predictor_graph_launch(self._graph, _stream(stream)))
+        else:
+            check("tts_code_predictor_run", lib().tts_code_predictor_run(ctypes.byref(self.desc), _stream(stream)))
+
+    def close(self) -> None:
+        if getattr(self, "_graph", None) is not None:
+            lib().tts_code_predictor_graph_destroy(self._graph)
+            self._graph = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 def tts_status_string(code: int) -> str:
     return _lib.status_string(code)
 

@@ -22,7 +22,7 @@ INCLUDE = ROOT / "include"
 BUILD = PKG / "_build"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["kv_append.cu", "decode_attn.cu", "head_select.cu", "spec_verify.cu", "tts_host.cpp",
-           "tts_step.cpp", "tts_graph.cu"]
+           "tts_step.cpp", "tts_graph.cu", "code_predictor.cu"]
 
 
 def lib_path() -> Path:

@@ -82,8 +82,11 @@ __device__ void finish_selection(const HeadWs &ws, int R, int32_t *ids, float *b
 }
 
 // Head modes beyond the public TTS_ARGMAX / TTS_GUMBEL: the first layer of
-// the two-layer audio head writes Mish(h W^T + b) as bf16 instead of selecting.
+// the two-layer audio head writes Mish(h W^T + b) as bf16 instead of
+// selecting; the linear mode writes h W^T as bf16 into up to three outputs
+// (consecutive feature ranges, e.g. the q, k and v of a projection).
 constexpr int kModeExpand = 2;
+constexpr int kModeLinear = 3;
 
 struct HeadArgs {
     int R, H, V, mode;
@@ -100,6 +103,9 @@ struct HeadArgs {
     const uint32_t *tail;     // [R] mask bits of the last n_tail ids (nullable: eos, else all allowed)
     int n_tail;
     __nv_bfloat16 *z_out;     // kModeExpand: [R][V] bf16
+    uint32_t pos;             // Gumbel noise counter position (tag 0, pos, idx)
+    int seg_start[4];         // kModeLinear: feature range j = [seg_start[j], seg_start[j + 1])
+    __nv_bfloat16 *seg_out[3];  //   written to seg_out[j] [R][seg_start[j + 1] - seg_start[j]]
 };
 
 // Mish(x) = x tanh(ln(1 + e^x)) in fp32 (past x = 20, ln(1 + e^x) rounds to x).
@@ -518,9 +524,10 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
         }
         return allow != 0u;
     };
-    if (a.mode == kModeExpand) {
-        // first layer of the audio head: 8 features of one row per item, one
-        // 16-byte store of Mish(x + b) as bf16
+    if (a.mode == kModeExpand || a.mode == kModeLinear) {
+        // 8 features of one row per item, one 16-byte store of bf16 values:
+        // Mish(x + b) for the audio head's first layer, x for a projection
+        const bool mish = a.mode == kModeExpand;
         for (int item = threadIdx.x; item < items; item += blockDim.x) {
             int cn, r, v;
             uint32_t allow;
@@ -529,10 +536,20 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
             uint32_t w[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const __nv_bfloat162 p = __floats2bfloat162_rn(mish_f(lg[2 * q]), mish_f(lg[2 * q + 1]));
+                const float x0 = mish ? mish_f(lg[2 * q]) : lg[2 * q];
+                const float x1 = mish ? mish_f(lg[2 * q + 1]) : lg[2 * q + 1];
+                const __nv_bfloat162 p = __floats2bfloat162_rn(x0, x1);
                 w[q] = *reinterpret_cast<const uint32_t *>(&p);
             }
-            *reinterpret_cast<uint4 *>(a.z_out + static_cast<size_t>(r) * a.V + v) = make_uint4(w[0], w[1], w[2], w[3]);
+            __nv_bfloat16 *dst;
+            if (mish) {
+                dst = a.z_out + static_cast<size_t>(r) * a.V + v;
+            } else {
+                const int j = v < a.seg_start[1] ? 0 : (v < a.seg_start[2] ? 1 : 2);
+                const int width = a.seg_start[j + 1] - a.seg_start[j];
+                dst = a.seg_out[j] + static_cast<size_t>(r) * width + (v - a.seg_start[j]);
+            }
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
         }
         if (CK > 1) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
         return;
@@ -576,8 +593,8 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
             const bool live0 = load_item(i0, cn0, r0i, va, allow0, lg0);
             const bool live1 = i1 < items && load_item(i1, cn1, r1i, vb, allow1, lg1);
             const int ra = live0 ? r0i : r0, rb = live1 ? r1i : r0;
-            const Philox4x64 pa(static_cast<uint64_t>(va >> 3), 0, 0, 0, a.seed[ra], a.step[ra]);
-            const Philox4x64 pb(static_cast<uint64_t>(vb >> 3), 0, 0, 0, a.seed[rb], a.step[rb]);
+            const Philox4x64 pa(static_cast<uint64_t>(va >> 3), 0, a.pos, 0, a.seed[ra], a.step[ra]);
+            const Philox4x64 pb(static_cast<uint64_t>(vb >> 3), 0, a.pos, 0, a.seed[rb], a.step[rb]);
             select(live0, cn0, va, allow0, lg0, pa);
             select(live1, cn1, vb, allow1, lg1, pb);
         }
@@ -693,7 +710,8 @@ int prepare_head_ex(const void *d_h, const void *d_W, int32_t dtype, int32_t R, 
                     int32_t mode, float temperature, const uint64_t *d_seed, const uint64_t *d_step,
                     const uint8_t *d_eos_allowed, int32_t *d_ids, float *d_best, float *d_logits_out,
                     void *d_ws, size_t ws_bytes, const HeadExtras &x, HeadLaunch *out) {
-    const bool expand = mode == kModeExpand;
+    const bool linear = mode == kModeLinear;
+    const bool expand = mode == kModeExpand || linear;  // both write bf16 features instead of selecting
     if (!d_h || !d_W || (!expand && !d_ids)) return TTS_ERR_INVALID;
     if (R < 1 || R > 4096 || H < 1 || V < 1 || V > (1 << 30)) return TTS_ERR_INVALID;
     if (mode != TTS_ARGMAX && mode != TTS_GUMBEL && !expand) return TTS_ERR_INVALID;
@@ -701,8 +719,16 @@ int prepare_head_ex(const void *d_h, const void *d_W, int32_t dtype, int32_t R, 
         return TTS_ERR_INVALID;
     if (x.n_tail < 0 || x.n_tail > 32 || x.n_tail > V) return TTS_ERR_INVALID;
     if (dtype != TTS_F32 && dtype != TTS_BF16) return TTS_ERR_UNSUPPORTED;
-    if (dtype == TTS_F32 && (x.bias || x.tail || expand)) return TTS_ERR_UNSUPPORTED;
-    if (expand) {
+    if (dtype == TTS_F32 && (x.bias || x.tail || expand || x.pos)) return TTS_ERR_UNSUPPORTED;
+    if (linear) {
+        // up to three outputs over consecutive feature ranges, 8 features per store
+        if (x.seg_start[0] != 0 || x.seg_start[3] != V || V % 8 != 0) return TTS_ERR_INVALID;
+        for (int j = 0; j < 3; ++j) {
+            const int width = x.seg_start[j + 1] - x.seg_start[j];
+            if (width < 0 || width % 8 != 0) return TTS_ERR_INVALID;
+            if (width > 0 && (!x.seg_out[j] || !aligned16(x.seg_out[j]))) return TTS_ERR_INVALID;
+        }
+    } else if (expand) {
         // the first audio-head layer: 8 features per 16-byte store of z
         if (!x.z_out || !aligned16(x.z_out) || V % 8 != 0) return TTS_ERR_INVALID;
     } else {
@@ -716,6 +742,9 @@ int prepare_head_ex(const void *d_h, const void *d_W, int32_t dtype, int32_t R, 
     a.seed = d_seed; a.step = d_step; a.eos = d_eos_allowed; a.logits_out = d_logits_out;
     a.ids = d_ids; a.best = d_best; a.ws = expand ? HeadWs{nullptr, nullptr} : head_ws(d_ws, R); a.err = nullptr;
     a.bias = x.bias; a.tail = x.tail; a.n_tail = x.n_tail; a.z_out = static_cast<__nv_bfloat16 *>(x.z_out);
+    a.pos = x.pos;
+    for (int j = 0; j < 4; ++j) a.seg_start[j] = x.seg_start[j];
+    for (int j = 0; j < 3; ++j) a.seg_out[j] = static_cast<__nv_bfloat16 *>(x.seg_out[j]);
     st->dtype = dtype;
     st->h = d_h;
     st->W = d_W;

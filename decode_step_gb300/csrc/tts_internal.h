@@ -122,11 +122,19 @@ int prepare_head(const void *d_h, const void *d_W, int32_t dtype, int32_t R, int
                  void *d_ws, size_t ws_bytes, HeadLaunch *out);
 // The head with a bias, a mask over the last n_tail ids, or (mode 2) the
 // first audio-head layer writing Mish(h W^T + bias) as bf16 to z_out [R][V].
+constexpr int kHeadModeExpand = 2;
+constexpr int kHeadModeLinear = 3;
+// Mode 3 (linear): h W^T as bf16, features [seg_start[j], seg_start[j + 1])
+// written to seg_out[j] (rows of that width).  pos: the Gumbel noise's
+// counter position.
 struct HeadExtras {
     const float *bias = nullptr;
     const uint32_t *tail = nullptr;
     int n_tail = 0;
     void *z_out = nullptr;
+    uint32_t pos = 0;
+    int seg_start[4] = {0, 0, 0, 0};
+    void *seg_out[3] = {nullptr, nullptr, nullptr};
 };
 int prepare_head_ex(const void *d_h, const void *d_W, int32_t dtype, int32_t R, int32_t H, int32_t V,
                     int32_t mode, float temperature, const uint64_t *d_seed, const uint64_t *d_step,

@@ -444,6 +444,69 @@ int tts_step_graph_set_launch(tts_step_graph_set *set, int32_t n_streams, int32_
 /* Frees every graph of the set (no GPU work of it may still be pending). */
 void tts_step_graph_set_destroy(tts_step_graph_set *set);
 
+/* ------------------------------------------------------ code predictor */
+
+/* The code predictor's frame loop ("How We Made a TTS Model Respond in
+ * Sub-50 ms", sections "Exploiting the regular building of the Code
+ * Predictor" and "Turn a fixed predictor loop into one GPU program": a fixed
+ * number of autoregressive steps per frame, one per remaining codebook, over
+ * a short bounded context in a preallocated KV cache).  For every stream r,
+ * with x = x0[r] and an empty cache, step i = 0 .. n_steps-1 computes
+ *   q, k, v = bf16(x Wqkv^T)      (q: the first Hq*D features, then k, v)
+ *   k, v appended at position i of the stream's cache
+ *   o = bf16(attention of q over positions 0..i), scale 1/sqrt(head_dim),
+ *       query head h reading KV head h / (Hq/Hkv)
+ *   tokens[i][r] = argmax_v (o . W_i[v]), or with TTS_GUMBEL the argmax of
+ *       logit / T + Gumbel noise (Philox key (seed[r], step[r]), counter
+ *       (v / 8, 0, i + 1, 0), half v % 8)
+ *   x = E_i[tokens[i][r]]
+ * Fields: R streams; H = num_q_heads * head_dim (the width of x and of o);
+ * head_dim 128; n_steps <= 16 (one 16-token block per stream);
+ *  d_x0 bf16 [R][H];  d_Wqkv bf16 [(Hq + 2 Hkv) * head_dim][H];
+ *  d_W bf16 [n_steps][V][H];  d_E bf16 [n_steps][V][H];
+ *  d_tokens int32 [n_steps][R] (written);  d_seed, d_step uint64 [R] (Gumbel);
+ *  d_ws: workspace of tts_code_predictor_workspace_size bytes, 256-byte
+ *  aligned, caller-owned; it holds x, q, k, v, o, the cache and the kernels'
+ *  workspaces (any contents on entry).  d_err as tts_decode_step. */
+typedef struct {
+    int32_t R;
+    int32_t H;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t V;
+    int32_t n_steps;
+    int32_t mode;
+    float temperature;
+    const void *d_x0;
+    const void *d_Wqkv;
+    const void *d_W;
+    const void *d_E;
+    const uint64_t *d_seed;
+    const uint64_t *d_step;
+    int32_t *d_tokens;
+    void *d_ws;
+    size_t ws_bytes;
+    int32_t *d_err;
+} tts_code_predictor_desc;
+
+/* Workspace bytes for the loop (0 for unsupported sizes). */
+size_t tts_code_predictor_workspace_size(int32_t R, int32_t H, int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t V, int32_t n_steps);
+
+/* Runs one frame's loop on `stream` (4 or 5 kernels per step, each a
+ * programmatic dependent of the one before).  TTS_ERR_INVALID /
+ * _UNSUPPORTED / _WORKSPACE as the step's calls. */
+int tts_code_predictor_run(const tts_code_predictor_desc *desc, void *stream);
+
+/* The same loop captured once as a CUDA graph for the descriptor's buffers
+ * (the caller writes x0, seeds and steps before each launch; the workspace
+ * and outputs must outlive the graph). */
+typedef struct tts_code_predictor_graph tts_code_predictor_graph;
+int tts_code_predictor_graph_create(const tts_code_predictor_desc *desc, tts_code_predictor_graph **out);
+int tts_code_predictor_graph_launch(tts_code_predictor_graph *graph, void *stream);
+void tts_code_predictor_graph_destroy(tts_code_predictor_graph *graph);
+
 /* ----------------------------------------------------------------- misc */
 
 /* Static description of a status code. */

@@ -119,18 +119,22 @@ def test_append_head_verify_argument_checks(L):
 
 
 def test_struct_layouts_match_header(tmp_path):
-    """The ctypes mirrors of tts_kv_cache and tts_step_graph_desc have the C
-    layout the header gives (compiled here against the header)."""
+    """The ctypes mirrors of tts_kv_cache, tts_step_graph_desc and
+    tts_code_predictor_desc have the C layout the header gives (compiled here
+    against the header)."""
     import shutil
     import subprocess
     cc = shutil.which("gcc") or shutil.which("cc")
     if cc is None:
         pytest.skip("no C compiler")
     fields = [f for f, _ in _lib.StepGraphDesc._fields_]
+    pfields = [f for f, _ in _lib.CodePredictorDesc._fields_]
     src = ["#include <stdio.h>", "#include <stddef.h>", '#include "tts_decode.h"', "int main(void) {",
            'printf("%zu %zu\\n", sizeof(tts_kv_cache), offsetof(tts_kv_cache, v_pool));',
            'printf("%zu\\n", sizeof(tts_step_graph_desc));']
     src += [f'printf("%zu\\n", offsetof(tts_step_graph_desc, {f}));' for f in fields]
+    src += ['printf("%zu\\n", sizeof(tts_code_predictor_desc));']
+    src += [f'printf("%zu\\n", offsetof(tts_code_predictor_desc, {f}));' for f in pfields]
     src += ["return 0; }"]
     (tmp_path / "lay.c").write_text("\n".join(src) + "\n")
     subprocess.run([cc, "-I", str(_lib.HEADER.parent), "-o", str(tmp_path / "lay"), str(tmp_path / "lay.c")],
@@ -140,7 +144,11 @@ def test_struct_layouts_match_header(tmp_path):
     K = _lib.KVCacheDesc
     assert vals[:2] == [ctypes.sizeof(K), K.v_pool.offset]
     assert vals[2] == ctypes.sizeof(_lib.StepGraphDesc)
-    assert vals[3:] == [getattr(_lib.StepGraphDesc, f).offset for f in fields]
+    n = 3 + len(fields)
+    assert vals[3:n] == [getattr(_lib.StepGraphDesc, f).offset for f in fields]
+    P = _lib.CodePredictorDesc
+    assert vals[n] == ctypes.sizeof(P)
+    assert vals[n + 1:] == [getattr(P, f).offset for f in pfields]
 
 
 def test_step_graph_rejects_bad_descriptors(L):

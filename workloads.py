@@ -254,3 +254,29 @@ def audio_head_inputs(R: int, H: int, F: int, V: int, n_tail: int, seed: int = 4
         step=np.zeros(R, dtype=np.uint64),
     )
     return out
+
+
+# Code predictor ("How We Made a TTS Model Respond in Sub-50 ms": a fixed loop
+# of autoregressive steps per frame, one per remaining codebook, over a short
+# bounded context).  The pages give no architecture; the loop here is one
+# projection, attention and codebook head per step.
+CODE_PREDICTOR = dict(R=64, H=1024, Hq=8, Hkv=4, D=128, V=2048, n_steps=15)
+
+
+def code_predictor_inputs(R: int, H: int, Hq: int, Hkv: int, D: int, V: int, n_steps: int,
+                          seed: int = 5150) -> dict:
+    """Seeded inputs of the predictor's frame loop: the talker's states
+    x0 ~ N(0, 1); projection and per-codebook head weights uniform in
+    +-1/sqrt(H) (a fresh linear layer's initialisation); codebook embeddings
+    ~ N(0, 1); all bf16.  Philox keys per stream (step = the frame index)."""
+    rng = np.random.default_rng(seed)
+    a = 1.0 / math.sqrt(H)
+    F = (Hq + 2 * Hkv) * D
+    return dict(
+        x0=f32_to_bf16(rng.standard_normal((R, H), dtype=np.float32)),
+        Wqkv=f32_to_bf16(rng.uniform(-a, a, (F, H)).astype(np.float32)),
+        W=f32_to_bf16(rng.uniform(-a, a, (n_steps, V, Hq * D)).astype(np.float32)),
+        E=f32_to_bf16(rng.standard_normal((n_steps, V, H), dtype=np.float32)),
+        seed=(PHILOX_SEED_MUL * 131 + np.arange(R)).astype(np.uint64),
+        step=np.full(R, 3, dtype=np.uint64),
+    )
