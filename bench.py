@@ -60,6 +60,8 @@ def parse_args(argv=None):
                          "'workloads' object (comma-separated ids, 'f' suffix: FP8 E4M3 KV cache; "
                          "empty: none)")
     ap.add_argument("--sweep-reps", type=int, default=30)
+    ap.add_argument("--code-predictor", type=int, default=1,
+                    help="time the code predictor's frame loop (workloads.CODE_PREDICTOR; 0 to skip)")
     ap.add_argument("--audio-heads", default="acoustic-b64,semantic-cb0-b16",
                     help="two-layer audio-head shapes timed alone (names of workloads.AUDIO_HEAD_SHAPES; '' for none)")
     return ap.parse_args(argv)
@@ -463,6 +465,54 @@ def audio_head_sweep(names, reps, flush_l2, peaks, device) -> dict:
     return out
 
 
+def predictor_bytes(R, H, Hq, Hkv, D, V, n_steps) -> int:
+    """Algorithmic bytes of one frame of the code predictor: the projection
+    weights once (they stay in L2 across the steps), every codebook head once,
+    the gathered embedding rows, the talker states, the cache rows written and
+    read, and the tokens."""
+    F = (Hq + 2 * Hkv) * D
+    return (2 * F * H + 2 * n_steps * V * H + 2 * (n_steps - 1) * R * H + 2 * R * H
+            + 2 * n_steps * R * 2 * Hkv * D * 2 + 4 * n_steps * R)
+
+
+def predictor_sweep(reps, flush_l2, peaks, device) -> dict:
+    """The frame loop for workloads.CODE_PREDICTOR, eager and captured, L2
+    flushed before each run, CUDA events around it."""
+    import torch
+    from decode_step_gb300 import binding as bd
+    c = wl.CODE_PREDICTOR
+    R, H, Hq, Hkv, D, V, n = c["R"], c["H"], c["Hq"], c["Hkv"], c["D"], c["V"], c["n_steps"]
+    inp = wl.code_predictor_inputs(R, H, Hq, Hkv, D, V, n)
+
+    def dev(x):
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+        return torch.from_numpy(x.view(np.int64) if x.dtype == np.uint64 else x).to(device)
+
+    args = [dev(inp[k]) for k in ("x0", "Wqkv", "W", "E")]
+    tokens = torch.empty((n, R), dtype=torch.int32, device=device)
+    nb = predictor_bytes(R, H, Hq, Hkv, D, V, n)
+    out = {"shape": dict(c), "bytes": nb, "kernels_per_frame": 1 + 5 * n - 1}
+    for kind in ("graph", "eager"):
+        cp = bd.CodePredictor(*args, Hq, Hkv, tokens, graph=kind == "graph")
+        for _ in range(3):
+            cp.run()
+        ts = []
+        for _ in range(reps):
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            cp.run()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        t = statistics.fmean(ts[2:])
+        out[kind] = {"us_per_frame_batch": t, "frames_per_s": R / (t * 1e-6), "tokens_per_s": R * n / (t * 1e-6),
+                     "gbs": nb / t / 1e3, "frac_hbm": nb / t / 1e3 / peaks["hbm_gbs"]}
+        cp.close()
+    return out
+
+
 def workload_config(w, world):
     return {"workload": f"{w.name}: {w.B} streams/GPU, GQA {w.Hq}/{w.Hkv} heads, head_dim {w.D}, "
                         f"{w.dtype}, q_len {w.q_len}, ctx {w.ctx_dist} [{w.ctx_lo},{w.ctx_hi}], "
@@ -698,6 +748,8 @@ def run_native(args):
             del step, graphed, cache, W, d
             torch.cuda.empty_cache()
             line["workloads"] = kernel_sweep(ids, args.sweep_reps, flush_l2, peaks, device)
+        if args.code_predictor:
+            line["code_predictor"] = predictor_sweep(args.sweep_reps, flush_l2, peaks, device)
         heads = [x.strip() for x in args.audio_heads.split(",") if x.strip()]
         if heads:
             line["audio_heads"] = audio_head_sweep(heads, args.sweep_reps, flush_l2, peaks, device)
