@@ -59,8 +59,11 @@ HeadWs head_ws(void *ws, int R) {
 // Called by every thread of each of the `publishers` CTAs that publish keys,
 // after their atomics.  The last of them converts keys to ids and resets the
 // workspace.  No waiting.
+// ids_host / count_host (nullable, pinned host memory): the ids again and the
+// number of rows whose id is `boundary`, written by the last CTA.
 __device__ void finish_selection(const HeadWs &ws, int R, int32_t *ids, float *best, int *flag,
-                                 unsigned int publishers) {
+                                 unsigned int publishers, int32_t *ids_host = nullptr, int32_t *count_host = nullptr,
+                                 int32_t boundary = -1) {
     // The barrier orders every thread's key atomics before thread 0's fence
     // (fences are cumulative), so one fence per CTA publishes them all.
     __syncthreads();
@@ -72,13 +75,27 @@ __device__ void finish_selection(const HeadWs &ws, int R, int32_t *ids, float *b
     __syncthreads();
     if (!*flag) return;
     // The last CTA alone reads and clears the keys (L2 reads: the atomics live there).
+    int hits = 0;
     for (int r = threadIdx.x; r < R; r += blockDim.x) {
         const unsigned long long k = __ldcg(ws.keys + r);
         ws.keys[r] = 0ull;
-        ids[r] = k ? unpack_index(k) : -1;
+        const int32_t id = k ? unpack_index(k) : -1;
+        ids[r] = id;
+        if (ids_host) ids_host[r] = id;
+        hits += id == boundary;
         if (best) best[r] = k ? unpack_value(k) : -INFINITY;
     }
     if (threadIdx.x == 0) *ws.ticket = 0u;
+    if (count_host) {
+        // the flag word is free again: reuse it as the CTA's counter
+        __syncthreads();
+        if (threadIdx.x == 0) *flag = 0;
+        __syncthreads();
+        hits = __reduce_add_sync(0xFFFFFFFFu, hits);
+        if ((threadIdx.x & 31) == 0 && hits) atomicAdd(flag, hits);
+        __syncthreads();
+        if (threadIdx.x == 0) *count_host = *flag;
+    }
 }
 
 // Head modes beyond the public TTS_ARGMAX / TTS_GUMBEL: the first layer of
@@ -106,6 +123,8 @@ struct HeadArgs {
     uint32_t pos;             // Gumbel noise counter position (tag 0, pos, idx)
     int seg_start[4];         // kModeLinear: feature range j = [seg_start[j], seg_start[j + 1])
     __nv_bfloat16 *seg_out[3];  //   written to seg_out[j] [R][seg_start[j + 1] - seg_start[j]]
+    int32_t *ids_host;        // selection: the ids again, in pinned host memory (nullable)
+    int32_t *count_host;      //   and the count of rows choosing id V - 1 (nullable)
 };
 
 // Mish(x) = x tanh(ln(1 + e^x)) in fp32 (past x = 20, ln(1 + e^x) rounds to x).
@@ -639,7 +658,8 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
         }
         if (r0 + cn < a.R && k) atomicMax(a.ws.keys + r0 + cn, k);
     }
-    finish_selection(a.ws, a.R, a.ids, a.best, flag, (gridDim.x / CK) * gridDim.y);
+    finish_selection(a.ws, a.R, a.ids, a.best, flag, (gridDim.x / CK) * gridDim.y, a.ids_host, a.count_host,
+                     a.V - 1);
 }
 
 // ------------------------------------------------------------- host side
@@ -719,7 +739,8 @@ int prepare_head_ex(const void *d_h, const void *d_W, int32_t dtype, int32_t R, 
         return TTS_ERR_INVALID;
     if (x.n_tail < 0 || x.n_tail > 32 || x.n_tail > V) return TTS_ERR_INVALID;
     if (dtype != TTS_F32 && dtype != TTS_BF16) return TTS_ERR_UNSUPPORTED;
-    if (dtype == TTS_F32 && (x.bias || x.tail || expand || x.pos)) return TTS_ERR_UNSUPPORTED;
+    if (dtype == TTS_F32 && (x.bias || x.tail || expand || x.pos || x.ids_host || x.count_host))
+        return TTS_ERR_UNSUPPORTED;
     if (linear) {
         // up to three outputs over consecutive feature ranges, 8 features per store
         if (x.seg_start[0] != 0 || x.seg_start[3] != V || V % 8 != 0) return TTS_ERR_INVALID;
@@ -743,6 +764,8 @@ int prepare_head_ex(const void *d_h, const void *d_W, int32_t dtype, int32_t R, 
     a.ids = d_ids; a.best = d_best; a.ws = expand ? HeadWs{nullptr, nullptr} : head_ws(d_ws, R); a.err = nullptr;
     a.bias = x.bias; a.tail = x.tail; a.n_tail = x.n_tail; a.z_out = static_cast<__nv_bfloat16 *>(x.z_out);
     a.pos = x.pos;
+    a.ids_host = x.ids_host;
+    a.count_host = x.count_host;
     for (int j = 0; j < 4; ++j) a.seg_start[j] = x.seg_start[j];
     for (int j = 0; j < 3; ++j) a.seg_out[j] = static_cast<__nv_bfloat16 *>(x.seg_out[j]);
     st->dtype = dtype;

@@ -8,9 +8,10 @@
 // One launch: a copy kernel brings the step's packed inputs from pinned host
 // memory (read through unified addressing, no copy-engine round trip), the
 // fused step runs (append; attention and head as programmatic dependents),
-// and a second small kernel writes the token ids to pinned host memory and
+// and the head's last CTA writes the token ids to pinned host memory and
 // counts the rows that picked the boundary token, so the host learns that a
-// stream ended from one word instead of scanning the ids.
+// stream ended from one word instead of scanning the ids (an fp32 head leaves
+// that to a small kernel).
 #include <cuda_runtime.h>
 
 #include <new>
@@ -27,6 +28,7 @@ constexpr int kCopyThreads = 256;
 __global__ void __launch_bounds__(kCopyThreads) copy_from_host_kernel(uint4 *__restrict__ dst,
                                                                       const uint4 *__restrict__ src,
                                                                       size_t n) {
+    pdl_allow_dependents();  // the step's append may launch now; it waits for this copy
     const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
     size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     // four loads in flight per thread before the stores
@@ -53,6 +55,7 @@ struct CopySegs {
 __global__ void __launch_bounds__(kCopyThreads) copy_segments_from_host_kernel(uint8_t *__restrict__ dst,
                                                                                const uint8_t *__restrict__ src,
                                                                                const CopySegs segs) {
+    pdl_allow_dependents();  // the step's append may launch now; it waits for this copy
     // One index space over every region's 16-byte words, so the reads of all
     // regions are in flight together (each is a round trip to host memory).
     size_t start[kMaxSegs + 1];
@@ -160,9 +163,18 @@ int capture_step(const tts_step_graph_desc *d, const CopySegs *segs, cudaGraph_t
     if (st != TTS_OK) return st;
     const long long H = static_cast<long long>(d->num_q_heads) * c->head_dim;
     if (H > 0x7FFFFFFF) return TTS_ERR_INVALID;
-    st = prepare_head(d->d_attn_out, d->d_W, c->dtype == TTS_FP8_E4M3 ? TTS_BF16 : c->dtype, static_cast<int32_t>(R),
-                      static_cast<int32_t>(H), d->V, d->mode, d->temperature, d->d_seed, d->d_step, d->d_eos_allowed,
-                      d->d_ids, d->d_best, d->d_logits_out, d->d_head_ws, d->head_ws_bytes, &hd);
+    // The tensor-core head's last CTA writes the ids and the boundary count to
+    // pinned host memory itself; the fp32 head leaves that to a small kernel.
+    const bool host_ids = c->dtype != TTS_F32;
+    HeadExtras hx;
+    if (host_ids) {
+        hx.ids_host = d->h_ids;
+        hx.count_host = d->h_boundary_count;
+    }
+    st = prepare_head_ex(d->d_attn_out, d->d_W, c->dtype == TTS_FP8_E4M3 ? TTS_BF16 : c->dtype,
+                         static_cast<int32_t>(R), static_cast<int32_t>(H), d->V, d->mode, d->temperature, d->d_seed,
+                         d->d_step, d->d_eos_allowed, d->d_ids, d->d_best, d->d_logits_out, d->d_head_ws,
+                         d->head_ws_bytes, hx, &hd);
     if (st != TTS_OK) return st;
 
     cudaStream_t s;
@@ -191,10 +203,10 @@ int capture_step(const tts_step_graph_desc *d, const CopySegs *segs, cudaGraph_t
             copy_from_host_kernel<<<copy_ctas, kCopyThreads, 0, s>>>(static_cast<uint4 *>(d->d_inputs),
                                                                      static_cast<const uint4 *>(d->h_inputs), words);
         ok = cudaGetLastError() == cudaSuccess;
-        ok = ok && launch_append(ap, {s, false}) == TTS_OK;
+        ok = ok && launch_append(ap, {s, true}) == TTS_OK;
         ok = ok && launch_attn(at, {s, true}) == TTS_OK;
         ok = ok && launch_head(hd, {s, true}) == TTS_OK;
-        if (ok) {
+        if (ok && !host_ids) {
             ids_to_host_kernel<<<1, kCopyThreads, 0, s>>>(d->d_ids, static_cast<int>(R), d->V - 1, d->h_ids,
                                                           d->h_boundary_count);
             ok = cudaGetLastError() == cudaSuccess;
