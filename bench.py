@@ -476,8 +476,9 @@ def predictor_bytes(R, H, Hq, Hkv, D, V, n_steps) -> int:
 
 
 def predictor_sweep(reps, flush_l2, peaks, device) -> dict:
-    """The frame loop for workloads.CODE_PREDICTOR, eager and captured, L2
-    flushed before each run, CUDA events around it."""
+    """The frame loop for workloads.CODE_PREDICTOR: the persistent kernel
+    (launched, and captured with its control-word reset) and the
+    kernel-per-stage graph; L2 flushed before each run, CUDA events around it."""
     import torch
     from decode_step_gb300 import binding as bd
     c = wl.CODE_PREDICTOR
@@ -492,9 +493,11 @@ def predictor_sweep(reps, flush_l2, peaks, device) -> dict:
     args = [dev(inp[k]) for k in ("x0", "Wqkv", "W", "E")]
     tokens = torch.empty((n, R), dtype=torch.int32, device=device)
     nb = predictor_bytes(R, H, Hq, Hkv, D, V, n)
-    out = {"shape": dict(c), "bytes": nb, "kernels_per_frame": 1 + 5 * n - 1}
-    for kind in ("graph", "eager"):
-        cp = bd.CodePredictor(*args, Hq, Hkv, tokens, graph=kind == "graph")
+    out = {"shape": dict(c), "bytes": nb,
+           "kernels_per_frame": {"persistent": 1, "multi_kernel": 1 + 5 * n - 1}}
+    for kind in ("persistent", "persistent_graph", "multi_kernel_graph"):
+        cp = bd.CodePredictor(*args, Hq, Hkv, tokens, graph=kind.endswith("graph"),
+                              multi_kernel=kind.startswith("multi"))
         for _ in range(3):
             cp.run()
         ts = []
@@ -733,6 +736,9 @@ def run_native(args):
                      "from a separate pass launching the kernels one by one",
         "device_error_flags": errflags,
         "clocks": clk,
+        # context: a voice at 12.5 frames/s over 4 retained codebook streams
+        # consumes 50 codec tokens/s per layer-step
+        "realtime_voice_equivalents": value / (12.5 * 4),
         "e2e_by_active_streams": e2e_sizes,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": n_e2e, "note": "wall clock; tts_step_graph (one CUDA graph captured by the "

@@ -47,7 +47,7 @@ class CodePredictorDesc(ctypes.Structure):
     _fields_ = [("R", _i32), ("H", _i32), ("num_q_heads", _i32), ("num_kv_heads", _i32), ("head_dim", _i32),
                 ("V", _i32), ("n_steps", _i32), ("mode", _i32), ("temperature", _f32), ("d_x0", _vp),
                 ("d_Wqkv", _vp), ("d_W", _vp), ("d_E", _vp), ("d_seed", _vp), ("d_step", _vp), ("d_tokens", _vp),
-                ("d_ws", _vp), ("ws_bytes", _sz), ("d_err", _vp)]
+                ("d_ws", _vp), ("ws_bytes", _sz), ("d_err", _vp), ("flags", _i32)]
 
 
 _SIGNATURES = {

@@ -416,10 +416,11 @@ class CodePredictor:
     x0 [R][H], Wqkv [(Hq + 2 Hkv) * 128][H], W [n_steps][V][H], E
     [n_steps][V][H] (bf16, device); tokens int32 [n_steps][R] is written by
     each run.  The workspace is allocated here.  With graph=True the loop is
-    captured once and run() launches the graph."""
+    captured once and run() launches the graph; multi_kernel=True runs one
+    kernel per stage instead of the persistent kernel."""
 
     def __init__(self, x0, Wqkv, W, E, num_q_heads, num_kv_heads, tokens, mode=TTS_ARGMAX, temperature=0.0,
-                 seed=None, step=None, err=None, graph=False):
+                 seed=None, step=None, err=None, graph=False, multi_kernel=False):
         R, H = x0.shape
         n_steps, V, HW = W.shape
         D = H // num_q_heads
@@ -436,7 +437,7 @@ class CodePredictor:
             R, H, num_q_heads, num_kv_heads, D, V, n_steps, int(mode), float(temperature), _dev(x0, "x0"),
             _dev(Wqkv, "Wqkv"), _dev(W, "W"), _dev(E, "E"), _keys(seed, "seed", R), _keys(step, "step", R),
             _dev(tokens, "tokens", torch.int32, (n_steps, R)), _dev(self.ws, "ws"), nbytes,
-            None if err is None else _dev(err, "err", torch.int32))
+            None if err is None else _dev(err, "err", torch.int32), 1 if multi_kernel else 0)
         self._keep = (x0, Wqkv, W, E, tokens, seed, step, err)
         self._graph = None
         if graph:

@@ -488,14 +488,21 @@ typedef struct {
     void *d_ws;
     size_t ws_bytes;
     int32_t *d_err;
+    int32_t flags;  /* TTS_PREDICTOR_MULTI_KERNEL: one kernel per stage, not one launch */
 } tts_code_predictor_desc;
+
+/* By default the frame runs as one cooperative persistent kernel (one CTA
+ * per SM, three grid barriers per step) when R <= 64, H <= 1024, head_dim is
+ * 128 and (Hq + 2 Hkv) * 128 and V are multiples of 16; otherwise, or with
+ * this flag, as 4-5 kernels per step. */
+#define TTS_PREDICTOR_MULTI_KERNEL 1
 
 /* Workspace bytes for the loop (0 for unsupported sizes). */
 size_t tts_code_predictor_workspace_size(int32_t R, int32_t H, int32_t num_q_heads, int32_t num_kv_heads,
                                          int32_t head_dim, int32_t V, int32_t n_steps);
 
-/* Runs one frame's loop on `stream` (4 or 5 kernels per step, each a
- * programmatic dependent of the one before).  TTS_ERR_INVALID /
+/* Runs one frame's loop on `stream` (the persistent kernel, or 4-5 kernels
+ * per step, each a programmatic dependent of the one before).  TTS_ERR_INVALID /
  * _UNSUPPORTED / _WORKSPACE as the step's calls. */
 int tts_code_predictor_run(const tts_code_predictor_desc *desc, void *stream);
 

@@ -35,15 +35,17 @@ def compare_tokens(gpu, ref):
 
 CASES = [
     # (R, Hq, Hkv, V, n_steps, mode, T)
-    (5, 2, 1, 100, 15, "argmax", 0.0),
+    (5, 2, 1, 112, 15, "argmax", 0.0),
     (16, 8, 4, 2048, 15, "argmax", 0.0),
     (16, 8, 4, 2048, 15, "gumbel", 0.8),
-    (3, 4, 4, 300, 16, "gumbel", 1.2),   # 16 steps fill the block; one query head per KV head
+    (3, 4, 4, 304, 16, "gumbel", 1.2),   # 16 steps fill the block; one query head per KV head
+    (5, 2, 1, 100, 15, "argmax", 0.0),   # V not a multiple of 16: always the multi-kernel path
 ]
 
 
+@pytest.mark.parametrize("multi", [False, True], ids=["persistent", "multi-kernel"])
 @pytest.mark.parametrize("case", CASES, ids=[f"R{c[0]}-Hq{c[1]}-V{c[3]}-{c[5]}" for c in CASES])
-def test_code_predictor_matches_oracle(orc, case):
+def test_code_predictor_matches_oracle(orc, case, multi):
     from decode_step_gb300 import binding as bd
     R, Hq, Hkv, V, n_steps, mode, T = case
     D = 128
@@ -56,7 +58,7 @@ def test_code_predictor_matches_oracle(orc, case):
     tok_e = torch.full((n_steps, R), -7, dtype=torch.int32, device="cuda")
     tok_g = torch.full((n_steps, R), -7, dtype=torch.int32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    kw = dict(mode=m, temperature=T, seed=dev(inp["seed"]), step=dev(inp["step"]), err=err)
+    kw = dict(mode=m, temperature=T, seed=dev(inp["seed"]), step=dev(inp["step"]), err=err, multi_kernel=multi)
     eager = bd.CodePredictor(*args, Hq, Hkv, tok_e, **kw)
     eager.run()
     graph = bd.CodePredictor(*args, Hq, Hkv, tok_g, graph=True, **kw)
@@ -68,7 +70,8 @@ def test_code_predictor_matches_oracle(orc, case):
     assert np.array_equal(te, tg)
     assert te.min() >= 0 and te.max() < V
     compared, diverged = compare_tokens(te, ref)
-    print(f"[code predictor {case}] {compared} tokens compared, {diverged} streams diverged at a near-tie")
+    print(f"[code predictor {case} {'multi' if multi else 'persistent'}] {compared} tokens compared, "
+          f"{diverged} streams diverged at a near-tie")
     assert diverged <= max(1, R // 8)
 
 
