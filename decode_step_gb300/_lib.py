@@ -39,7 +39,10 @@ class StepGraphDesc(ctypes.Structure):
                 ("V", _i32), ("mode", _i32), ("temperature", _f32), ("d_seed", _vp), ("d_step", _vp),
                 ("d_eos_allowed", _vp), ("d_ids", _vp), ("d_best", _vp), ("d_logits_out", _vp),
                 ("d_head_ws", _vp), ("head_ws_bytes", _sz), ("d_err", _vp), ("h_inputs", _vp), ("d_inputs", _vp),
-                ("input_bytes", _sz), ("h_ids", _vp), ("h_boundary_count", _vp)]
+                ("input_bytes", _sz), ("h_ids", _vp), ("h_boundary_count", _vp),
+                ("d_draft_probs", _vp), ("d_draft_tokens", _vp), ("verify_temperature", _f32),
+                ("verify_flags", _i32), ("d_vseed", _vp), ("d_vstep", _vp), ("d_n_accepted", _vp),
+                ("d_next_token", _vp), ("h_n_accepted", _vp), ("h_next_token", _vp)]
 
 
 class CodePredictorDesc(ctypes.Structure):

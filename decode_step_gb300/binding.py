@@ -305,7 +305,7 @@ def _pinned(t: torch.Tensor, name: str, dtype=None, numel=None):
 
 def _graph_desc(cache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new, attn_out, attn_ws, scale,
                 W, ids, head_ws, h_inputs, d_inputs, h_ids, h_boundary_count, causal, mode, temperature, seed, step,
-                eos_allowed, best, logits_out, err, rope_base):
+                eos_allowed, best, logits_out, err, rope_base, verify=None):
     args = _step_args(cache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new, attn_out,
                       attn_ws, scale, W, ids, head_ws, causal, rope_base, mode, temperature, seed, step,
                       eos_allowed, best, logits_out, err, None)
@@ -316,7 +316,25 @@ def _graph_desc(cache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new,
     host = (_pinned(h_inputs, "h_inputs"), _dev(d_inputs, "d_inputs"), nbytes,
             _pinned(h_ids, "h_ids", torch.int32, R),
             None if h_boundary_count is None else _pinned(h_boundary_count, "h_boundary_count", torch.int32, 1))
-    return _lib.StepGraphDesc(ctypes.pointer(cache.desc), *args[1:-1], *host)
+    desc = _lib.StepGraphDesc(ctypes.pointer(cache.desc), *args[1:-1], *host)
+    if verify is not None:
+        B = block_table.shape[0]
+        K = q.shape[1] - 1
+        V = W.shape[0]
+        v = verify
+        desc.d_draft_probs = _dev(v["draft_probs"], "draft_probs", torch.float32, (B, K, V))
+        desc.d_draft_tokens = _dev(v["draft_tokens"], "draft_tokens", torch.int32, (B, K))
+        desc.verify_temperature = float(v["temperature"])
+        desc.verify_flags = TTS_VERIFY_BONUS if v.get("bonus") else 0
+        desc.d_vseed = _keys(v["vseed"], "vseed", B)
+        desc.d_vstep = _keys(v["vstep"], "vstep", B)
+        desc.d_n_accepted = _dev(v["n_accepted"], "n_accepted", torch.int32, (B,))
+        desc.d_next_token = _dev(v["next_token"], "next_token", torch.int32, (B,))
+        if v.get("h_n_accepted") is not None:
+            desc.h_n_accepted = _pinned(v["h_n_accepted"], "h_n_accepted", torch.int32, B)
+        if v.get("h_next_token") is not None:
+            desc.h_next_token = _pinned(v["h_next_token"], "h_next_token", torch.int32, B)
+    return desc
 
 
 class StepGraph:
@@ -326,17 +344,21 @@ class StepGraph:
     `d_inputs`) plus the host side: `h_inputs` (pinned, copied to `d_inputs`
     by every launch), `h_ids` (pinned int32 [B * q_len], written by every
     launch) and optionally `h_boundary_count` (pinned int32 [1]: rows whose id
-    is the boundary token V - 1).  Every tensor passed must outlive the graph;
-    the object keeps references to them.
+    is the boundary token V - 1).  `verify` (optional dict: draft_probs,
+    draft_tokens, temperature, bonus, vseed, vstep, n_accepted, next_token and
+    pinned h_n_accepted / h_next_token) adds the speculative verify over the
+    head's logits (logits_out required) to the captured step.  Every tensor
+    passed must outlive the graph; the object keeps references to them.
     """
 
     def __init__(self, cache: KVCache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new,
                  attn_out, attn_ws, scale, W, ids, head_ws, h_inputs, d_inputs, h_ids,
                  h_boundary_count=None, causal=False, mode=TTS_ARGMAX, temperature=0.0, seed=None,
-                 step=None, eos_allowed=None, best=None, logits_out=None, err=None, rope_base=0.0):
+                 step=None, eos_allowed=None, best=None, logits_out=None, err=None, rope_base=0.0, verify=None):
         desc = _graph_desc(cache, block_table, ctx_before, ctx_lens, max_ctx_len, q, k_new, v_new, attn_out,
                            attn_ws, scale, W, ids, head_ws, h_inputs, d_inputs, h_ids, h_boundary_count, causal,
-                           mode, temperature, seed, step, eos_allowed, best, logits_out, err, rope_base)
+                           mode, temperature, seed, step, eos_allowed, best, logits_out, err, rope_base, verify)
+        self._verify = verify
         handle = ctypes.c_void_p()
         check("tts_step_graph_create", lib().tts_step_graph_create(ctypes.byref(desc), ctypes.byref(handle)))
         self._handle = handle

@@ -102,6 +102,16 @@ __global__ void __launch_bounds__(kCopyThreads) ids_to_host_kernel(const int32_t
     }
 }
 
+// dst_a[b] = src_a[b], dst_b[b] = src_b[b] for b < n (pinned host destinations).
+__global__ void __launch_bounds__(kCopyThreads) pair_to_host_kernel(const int32_t *__restrict__ src_a,
+                                                                    const int32_t *__restrict__ src_b, int n,
+                                                                    int32_t *dst_a, int32_t *dst_b) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        if (dst_a) dst_a[i] = src_a[i];
+        if (dst_b) dst_b[i] = src_b[i];
+    }
+}
+
 bool device_accessible(const void *p) {
     cudaPointerAttributes at;
     if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
@@ -176,6 +186,18 @@ int capture_step(const tts_step_graph_desc *d, const CopySegs *segs, cudaGraph_t
                          d->d_step, d->d_eos_allowed, d->d_ids, d->d_best, d->d_logits_out, d->d_head_ws,
                          d->head_ws_bytes, hx, &hd);
     if (st != TTS_OK) return st;
+    // the optional verify stage reads the head's logits for K + 1 rows per stream
+    const bool verify = d->d_n_accepted != nullptr;
+    if (verify) {
+        if (!d->d_logits_out || d->q_len < 2 || !d->d_next_token || !d->d_draft_probs || !d->d_draft_tokens ||
+            !d->d_vseed || !d->d_vstep)
+            return TTS_ERR_INVALID;
+        if ((d->h_n_accepted && !pinned_host(d->h_n_accepted)) || (d->h_next_token && !pinned_host(d->h_next_token)))
+            return TTS_ERR_INVALID;
+        if (!(d->verify_temperature > 0.0f) || d->verify_temperature == INFINITY || d->q_len - 1 > 16 ||
+            (d->verify_flags & ~TTS_VERIFY_BONUS) != 0)
+            return TTS_ERR_INVALID;
+    }
 
     cudaStream_t s;
     if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) {
@@ -210,6 +232,16 @@ int capture_step(const tts_step_graph_desc *d, const CopySegs *segs, cudaGraph_t
             ids_to_host_kernel<<<1, kCopyThreads, 0, s>>>(d->d_ids, static_cast<int>(R), d->V - 1, d->h_ids,
                                                           d->h_boundary_count);
             ok = cudaGetLastError() == cudaSuccess;
+        }
+        if (ok && verify) {
+            ok = tts_spec_verify(d->d_logits_out, d->d_draft_probs, d->d_draft_tokens, d->B, d->q_len - 1, d->V,
+                                 d->verify_temperature, d->d_vseed, d->d_vstep, d->verify_flags, d->d_n_accepted,
+                                 d->d_next_token, d->d_err, s) == TTS_OK;
+            if (ok && (d->h_n_accepted || d->h_next_token)) {
+                pair_to_host_kernel<<<1, kCopyThreads, 0, s>>>(d->d_n_accepted, d->d_next_token, d->B,
+                                                               d->h_n_accepted, d->h_next_token);
+                ok = cudaGetLastError() == cudaSuccess;
+            }
         }
         const bool ended = cudaStreamEndCapture(s, &graph) == cudaSuccess;
         ok = ok && ended;

@@ -71,12 +71,17 @@ class GraphedStep:
     inputs with one kernel reading the pinned buffer, runs the step, and writes
     the ids and the count of rows that picked the boundary token into pinned
     host memory.  Write a step's inputs into `host[...]`, call the object, read
-    the ids it returns (`boundary_count` holds the count).
+    the ids it returns (`boundary_count` holds the count).  With draft_probs,
+    draft_tokens, vseed and vstep among the inputs (a q_len = K + 1 step) the
+    captured step also verifies the drafts against the head's logits;
+    `n_accepted_host` / `next_token_host` then hold the result.
     """
 
-    NAMES = ("block_table", "ctx_before", "ctx_lens", "q", "k_new", "v_new", "seed", "step")
+    NAMES = ("block_table", "ctx_before", "ctx_lens", "q", "k_new", "v_new", "seed", "step",
+             "draft_probs", "draft_tokens", "vseed", "vstep")
 
-    def __init__(self, step: DecodeStep, inputs: dict, stream: torch.cuda.Stream | None = None):
+    def __init__(self, step: DecodeStep, inputs: dict, stream: torch.cuda.Stream | None = None,
+                 verify_temperature: float | None = None, bonus: bool = False):
         self.step = step
         offsets, total = {}, 0
         for k, t in inputs.items():
@@ -97,12 +102,26 @@ class GraphedStep:
         self.boundary_host = torch.zeros(1, dtype=torch.int32, device="cpu").pin_memory()
         self.stream = torch.cuda.Stream() if stream is None else stream
         d = self.dev
+        # speculative verify inside the captured step: the head keeps its
+        # logits for the K + 1 rows of every stream and verify reads them
+        verify, self.logits = None, None
+        self.n_accepted_host = self.next_token_host = None
+        if "draft_probs" in inputs:
+            B = step.B
+            self.logits = torch.empty((step.R, step.V), dtype=torch.float32, device=device)
+            self.n_accepted_host = torch.zeros(B, dtype=torch.int32, device="cpu").pin_memory()
+            self.next_token_host = torch.zeros(B, dtype=torch.int32, device="cpu").pin_memory()
+            verify = dict(draft_probs=d["draft_probs"], draft_tokens=d["draft_tokens"],
+                          temperature=verify_temperature, bonus=bonus, vseed=d["vseed"], vstep=d["vstep"],
+                          n_accepted=torch.empty(B, dtype=torch.int32, device=device),
+                          next_token=torch.empty(B, dtype=torch.int32, device=device),
+                          h_n_accepted=self.n_accepted_host, h_next_token=self.next_token_host)
         self.graph = bd.StepGraph(
             step.cache, d["block_table"], d["ctx_before"], d["ctx_lens"], step.max_ctx_len, d["q"],
             d["k_new"], d["v_new"], step.out, step.attn_ws, step.scale, step.W, step.ids, step.head_ws,
             self.host_blob, self.dev_blob, self.ids_host, self.boundary_host, causal=step.causal,
             mode=step.mode, temperature=step.temperature, seed=d.get("seed"), step=d.get("step"),
-            err=step.err, rope_base=step.rope_base)
+            err=step.err, rope_base=step.rope_base, logits_out=self.logits, verify=verify)
 
     @property
     def h2d_bytes(self) -> int:

@@ -396,6 +396,21 @@ typedef struct {
     size_t input_bytes;         /* multiple of 16 */
     int32_t *h_ids;             /* pinned host [R] */
     int32_t *h_boundary_count;  /* pinned host, nullable */
+    /* Optional verify stage (when d_n_accepted is not NULL): the captured
+     * step ends with tts_spec_verify over the head's logits (d_logits_out,
+     * [B][q_len][V] with q_len = K + 1), and the accepted counts and next
+     * tokens are also written to h_n_accepted / h_next_token (pinned host,
+     * nullable).  Fields mean what tts_spec_verify's arguments mean. */
+    const float *d_draft_probs;     /* [B][K][V] */
+    const int32_t *d_draft_tokens;  /* [B][K] */
+    float verify_temperature;
+    int32_t verify_flags;
+    const uint64_t *d_vseed;        /* [B] */
+    const uint64_t *d_vstep;        /* [B] */
+    int32_t *d_n_accepted;          /* [B] */
+    int32_t *d_next_token;          /* [B] */
+    int32_t *h_n_accepted;          /* pinned host [B], nullable */
+    int32_t *h_next_token;          /* pinned host [B], nullable */
 } tts_step_graph_desc;
 
 typedef struct tts_step_graph tts_step_graph;
