@@ -404,6 +404,26 @@ def kernel_sweep(ids, reps, flush_l2, peaks, device) -> dict:
             vb = verify_bytes(w)
             entry.update({"spec_verify_us": t_ver, "spec_verify_gbs": vb / t_ver / 1e3,
                           "spec_verify_frac": vb / t_ver / 1e3 / hbm, "spec_verify_bytes": vb})
+            # the whole speculative step captured once (inputs from pinned
+            # memory, append, causal attention over K + 1 rows, Gumbel head
+            # keeping its logits, verify, results to pinned memory): wall
+            # clock per step, synchronised every step
+            from decode_step_gb300.step import DecodeStep, GraphedStep
+            vstep_ = DecodeStep(cache, d["W"], w.Hq, w.B, w.ctx_hi, q_len=w.q_len, causal=w.causal,
+                                mode=bd.TTS_GUMBEL, temperature=w.T)
+            gin = {k: d[k] for k in ("block_table", "ctx_before", "ctx_lens", "q", "k_new", "v_new", "seed", "step")}
+            gin.update({"draft_probs": dp, "draft_tokens": dt, "vseed": vs, "vstep": vt})
+            gv = GraphedStep(vstep_, gin, verify_temperature=w.T)
+            for _ in range(5):
+                gv()
+            t0 = time.perf_counter()
+            for _ in range(reps * 4):
+                gv()
+            us = (time.perf_counter() - t0) / (reps * 4) * 1e6
+            entry.update({"verify_step_e2e_us": us,
+                          "verify_step_note": "captured step with verify, host sync per step; each stream "
+                                              "advances 1 + accepted tokens"})
+            del gv, vstep_
         out[w.name + ("-fp8" if fp8 else "")] = entry
         del cache, d, attn_out, ws
         torch.cuda.empty_cache()
