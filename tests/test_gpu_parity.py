@@ -342,7 +342,10 @@ def test_draft_token_outside_vocab_is_flagged():
 # ------------------------------------------------------------ head shapes
 
 HEAD_SHAPES = [(1, 64, 300), (17, 128, 1000), (256, 64, 129), (257, 64, 200), (320, 128, 257),
-               (5, 2048, 4097)]
+               (5, 2048, 4097),
+               (3, 64, 1),      # one entry: rows whose boundary is masked choose nothing (-1)
+               (9, 64, 7),      # fewer entries than one 8-entry selection group
+               (4096, 64, 64)]  # the largest batch: 16 chunks of 256 rows
 
 
 @pytest.mark.parametrize("R,H,V", HEAD_SHAPES)
@@ -363,7 +366,13 @@ def test_head_shapes(orc, R, H, V, mode):
     torch.cuda.synchronize()
     ref = orc.head_select(h, W, mode, 0.8, seed, step, eos_allowed=eos, want_logits=True)
     assert np.allclose(host(logits), ref["logits"], rtol=1e-4, atol=1e-4)
-    hard, ties = compare_ids(host(ids), ref)
+    gids = host(ids)
+    none = ref["ids"] < 0                       # every entry masked: no choice either side
+    assert np.array_equal(gids[none], ref["ids"][none])
+    hard, ties = compare_ids(np.where(none, 0, gids), {k: np.where(none, 0, v) if k == "ids" else
+                                                       np.where(none, 1.0, v) if k == "best" else
+                                                       np.where(none, 0.0, v) for k, v in ref.items()
+                                                       if k in ("ids", "best", "second")})
     assert not hard, f"rows {hard[:10]}"
     assert int(ws.count_nonzero()) == 0
 
