@@ -684,8 +684,11 @@ TcPlan plan_tc(int R, int H, int V) {
     p.smem = tc_layout(p.N, 1).total;
     // widest cluster split of the hidden dimension, up to 4, that still runs
     // in one wave (8-CTA clusters start and synchronise more slowly than the
-    // extra SMs they bring save: measured 1.5 us slower at 64 x 2048 x 4097)
-    for (int ck = 2; ck <= 4; ck <<= 1) {
+    // extra SMs they bring save: measured 1.5 us slower at 64 x 2048 x 4097);
+    // up to 8 for H >= 4096, where a 4-way split leaves 256 KB of W per CTA
+    // (measured 4 us faster at 64 x 4096 x 4097)
+    const int ck_max = H >= 4096 ? 8 : 4;  // wide reductions: every CTA's W slice stays small
+    for (int ck = 2; ck <= ck_max; ck <<= 1) {
         if (ktiles % ck != 0) break;
         const uint32_t smem = tc_layout(p.N, ck).total;
         int per_sm = static_cast<int>((227u * 1024u) / (smem + 1024u));
