@@ -315,6 +315,10 @@ __device__ __forceinline__ void st_async_u64(uint32_t dst_cluster, unsigned long
                  : "memory");
 }
 
+// kFeatures: the build for the modes that write bf16 features (the audio
+// head's first layer, projections); the other build selects tokens.  Kept
+// apart so each epilogue is compiled without the other's code.
+template <bool kFeatures>
 __global__ void __launch_bounds__(kThreadsTC, 2)
 head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_h,
                const HeadArgs a, int N, int CK, int alloc_cols) {
@@ -534,6 +538,10 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
         } else if (a.eos && !a.eos[r]) {
             tail0 = a.V - 1;
         }
+        if (v + 8 <= tail0) {  // every entry below the structural tail (nearly all items)
+            allow = 0xFFu;
+            return true;
+        }
         allow = 0u;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -543,7 +551,7 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
         }
         return allow != 0u;
     };
-    if (a.mode == kModeExpand || a.mode == kModeLinear) {
+    if constexpr (kFeatures) {
         // 8 features of one row per item, one 16-byte store of bf16 values:
         // Mish(x + b) for the audio head's first layer, x for a projection
         const bool mish = a.mode == kModeExpand;
@@ -811,7 +819,9 @@ int launch_head(const HeadLaunch &L, LaunchOpts o) {
                                static_cast<const float *>(st->W), st->a);
     } else {
         const TcPlan &p = st->p;
-        if (!ensure_dynamic_smem(reinterpret_cast<const void *>(head_tc_kernel), static_cast<int>(p.smem)))
+        const bool features = st->a.mode == kModeExpand || st->a.mode == kModeLinear;
+        const auto kernel = features ? head_tc_kernel<true> : head_tc_kernel<false>;
+        if (!ensure_dynamic_smem(reinterpret_cast<const void *>(kernel), static_cast<int>(p.smem)))
             return TTS_ERR_CUDA;
         cfg.gridDim = dim3(static_cast<unsigned>(((st->a.V + kTileM - 1) / kTileM) * p.CK),
                            static_cast<unsigned>(p.chunks), 1);
@@ -824,7 +834,7 @@ int launch_head(const HeadLaunch &L, LaunchOpts o) {
         ++na;
         cfg.attrs = attr;
         cfg.numAttrs = na;
-        e = cudaLaunchKernelEx(&cfg, head_tc_kernel, st->mw, st->mh, st->a, p.N, p.CK, p.alloc_cols);
+        e = cudaLaunchKernelEx(&cfg, kernel, st->mw, st->mh, st->a, p.N, p.CK, p.alloc_cols);
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
