@@ -151,6 +151,14 @@ __device__ __forceinline__ T *out_row(const AttnArgs &a, int b, int g, int r) {
     return static_cast<T *>(a.out) + ((static_cast<size_t>(b) * a.q_len + j) * a.Hq + g * a.group + hh) * D;
 }
 
+// Warps given tiles: at least kMinTilesPerWarp each when the work is small
+// (fewer split segments to publish and merge), else every warp of the grid.
+constexpr long long kMinTilesPerWarp = 4;
+__device__ __forceinline__ long long active_workers(int workers, long long Ttot) {
+    const long long by_work = (Ttot + kMinTilesPerWarp - 1) / kMinTilesPerWarp;
+    return min(static_cast<long long>(workers), by_work > 0 ? by_work : 1);
+}
+
 // The last contributor of a split segment merges the contributors' partials
 // (log-sum-exp combine).  Loads are issued together rather than one
 // contributor at a time: contributors are spread over the lanes (32 at a
@@ -272,7 +280,7 @@ decode_attn_simt_kernel(const AttnArgs a) {
     pdl_allow_dependents();
     scan_streams<T, D, kWarps>(a, prefix, ctxs, scan);
     const long long Ttot = prefix[a.B];
-    const long long Wtot = min(static_cast<long long>(a.workers), Ttot);
+    const long long Wtot = active_workers(a.workers, Ttot);
     const int wid = blockIdx.x * kWarps + warp;
     if (Ttot == 0 || wid >= Wtot) return;
     const int t0 = static_cast<int>(range_start(wid, Ttot, Wtot));
@@ -686,7 +694,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
     pdl_allow_dependents();
     scan_streams<T, D, kTcWarps>(a, prefix, ctxs, scan);
     const long long Ttot = prefix[a.B];
-    const long long Wtot = min(static_cast<long long>(a.workers), Ttot);
+    const long long Wtot = active_workers(a.workers, Ttot);
     const int wid = blockIdx.x * kTcWarps + warp;
     if (Ttot == 0 || wid >= Wtot) return;
     const int t0 = static_cast<int>(range_start(wid, Ttot, Wtot));
