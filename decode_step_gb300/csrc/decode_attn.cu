@@ -567,6 +567,11 @@ __device__ __forceinline__ void mma_f16_16816(float *d, const uint32_t *a, uint3
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -602,10 +607,12 @@ constexpr int kFp8VOff = 2048;
 constexpr int kFp8ScaleOff = 4096;
 constexpr int kFp8KVStageBytes = kFp8ScaleOff + 2 * 64;
 // Key codes enter S = Q K^T as f16 (the hardware conversion is exact) with the
-// queries in f16; value codes enter O += P V as bf16 values times 2^-120 (see
-// e4m3x4_to_bf16, so that P, scaled by each token's value scale, keeps bf16's
-// exponent range), and P is rescaled by 2^120.
-constexpr float kFp8PFix = 0x1p120f;
+// queries in f16; value codes enter O += P V as f16 too (exact), against P
+// times each token's value scale times 2^8 in f16 (11 bits, where bf16 keeps
+// 8), and the softmax sum carries the same 2^8.  The factor keeps products of
+// scales above about 2^-14 out of f16's subnormals; value scales must stay
+// below 256 (the products below f16's largest value).
+constexpr float kFp8PFix = 0x1p8f;
 
 // Address of 16-byte chunk `ch` (0..15) of token row `t` (0..15) in a K or V
 // tile stored as two swizzled boxes.
@@ -638,18 +645,6 @@ __host__ inline int tc_stages(int n_rows, int B, bool fp8) {
     for (int st = kTcMaxStages; st >= 1; --st)
         if (tc_smem(n_rows, B, st, fp8).total <= budget) return st;
     return 0;
-}
-
-// Four E4M3 codes (bytes of w, low first) as two bf16 pairs (codes 0, 1 and
-// 2, 3, low half first), each value times 2^-120: the sign goes to bit 15 and
-// the exponent and mantissa bits to bits 4-10, so a normal code's exponent
-// field (bias 7) becomes the bf16 exponent field (bias 127) and a subnormal
-// code a bf16 subnormal of the same scaled value.  Exact for every code.
-__device__ __forceinline__ void e4m3x4_to_bf16(uint32_t w, uint32_t &lo, uint32_t &hi) {
-    const uint32_t a = __byte_perm(w, 0u, 0x1404);  // [0, c0, 0, c1]
-    const uint32_t b = __byte_perm(w, 0u, 0x3424);  // [0, c2, 0, c3]
-    lo = (a & 0x80008000u) | ((a & 0x7F007F00u) >> 4);
-    hi = (b & 0x80008000u) | ((b & 0x7F007F00u) >> 4);
 }
 
 // Four E4M3 codes (bytes of w, low first) as two f16 pairs (codes 0, 1 and
@@ -787,6 +782,10 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
         la += __shfl_xor_sync(kFull, la, 2);
         lb += __shfl_xor_sync(kFull, lb, 1);
         lb += __shfl_xor_sync(kFull, lb, 2);
+        if constexpr (kFp8) {  // O carries P's factor 2^8 (kFp8PFix)
+            la *= kFp8PFix;
+            lb *= kFp8PFix;
+        }
         const int rA = fg, rB = fg + 8;
         if (s0 >= t0 && s1 <= t1) {
             // whole segment in this warp: write the output rows
@@ -972,8 +971,8 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
             // P as the A operand (rows fg / fg + 8, tokens 2t, 2t+1, 2t+8, 2t+9)
             uint32_t pf[4];
             if constexpr (kFp8) {
-                // times each token's value scale and 2^120; slots past the
-                // context may hold any scale (even NaN), so they give 0
+                // times each token's value scale and 2^8, in f16; slots past
+                // the context may hold any scale (even NaN), so they give 0
                 float qa_[4], qb_[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -982,24 +981,43 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
                     qa_[e] = tok < limA ? pa[e] * vs : 0.0f;
                     qb_[e] = tok < limB ? pb[e] * vs : 0.0f;
                 }
-                pf[0] = pack_bf16x2(qa_[0], qa_[1]);
-                pf[1] = pack_bf16x2(qb_[0], qb_[1]);
-                pf[2] = pack_bf16x2(qa_[2], qa_[3]);
-                pf[3] = pack_bf16x2(qb_[2], qb_[3]);
+                pf[0] = pack_f16x2(qa_[0], qa_[1]);
+                pf[1] = pack_f16x2(qb_[0], qb_[1]);
+                pf[2] = pack_f16x2(qa_[2], qa_[3]);
+                pf[3] = pack_f16x2(qb_[2], qb_[3]);
             } else {
                 pf[0] = pack_bf16x2(pa[0], pa[1]);
                 pf[1] = pack_bf16x2(pb[0], pb[1]);
                 pf[2] = pack_bf16x2(pa[2], pa[3]);
                 pf[3] = pack_bf16x2(pb[2], pb[3]);
             }
-            // Tokens past the context may hold anything (even NaN): zero their
-            // V rows (bf16; FP8 codes widen to finite values and meet P = 0).
-            if (!kFp8 && base_tok + TTS_BLOCK_TOKENS > seg_L) {
+            // Tokens past the context may hold anything (even NaN, which the
+            // MMA would spread as 0 * NaN): zero their values in the tile.
+            if (base_tok + TTS_BLOCK_TOKENS > seg_L) {
                 const int first_bad = max(seg_L - base_tok, 0);
-                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                for (int idx = lane; idx < (TTS_BLOCK_TOKENS - first_bad) * 16; idx += 32) {
-                    const int row = first_bad + idx / 16, ch = idx % 16;
-                    *reinterpret_cast<uint4 *>(smem + (swz(vt, row, ch) - base)) = z;
+                if constexpr (kFp8) {
+                    // each dimension's 16 codes: byte 4j + k holds slot 2j + (k & 1) + 8 (k >> 1)
+                    uint32_t keep[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        keep[j] = 0u;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            if (2 * j + (k & 1) + 8 * (k >> 1) < first_bad) keep[j] |= 0xFFu << (8 * k);
+                    }
+                    uint4 *rows = reinterpret_cast<uint4 *>(smem + (vt - base));
+#pragma unroll
+                    for (int d = lane; d < D; d += 32) {
+                        uint4 v = rows[d];
+                        v.x &= keep[0]; v.y &= keep[1]; v.z &= keep[2]; v.w &= keep[3];
+                        rows[d] = v;
+                    }
+                } else {
+                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                    for (int idx = lane; idx < (TTS_BLOCK_TOKENS - first_bad) * 16; idx += 32) {
+                        const int row = first_bad + idx / 16, ch = idx % 16;
+                        *reinterpret_cast<uint4 *>(smem + (swz(vt, row, ch) - base)) = z;
+                    }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -1015,8 +1033,8 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         uint32_t b0, b1;
-                        e4m3x4_to_bf16(w[i], b0, b1);
-                        mma_bf16_16816(o[4 * q4 + i], pf, b0, b1);
+                        e4m3x4_to_f16(w[i], b0, b1);
+                        mma_f16_16816(o[4 * q4 + i], pf, b0, b1);
                     }
                 }
             } else {

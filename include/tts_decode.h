@@ -93,6 +93,12 @@ enum {
  *   bytes 4096..4159  the 16 key scales (float), 4160..4223 the value scales
  * so a tile moves with one bulk copy; v_pool is unused (NULL).  The step's
  * activations (q, k_new, v_new, the attention output) are bf16.
+ * Attention on this cache runs its products in f16 on the tensor cores: the
+ * queries must lie within f16's range, and every value scale below 256 (a
+ * value row's largest magnitude below 114,688), else outputs are not finite.
+ * Where a softmax weight times a value scale falls below 2^-22 its product
+ * enters f16's subnormals: an absolute error below 2^-33 x 448 per token
+ * before the division by the softmax sum.
  * All base addresses must be 16-byte aligned. */
 typedef struct tts_kv_cache {
     int32_t num_blocks;

@@ -107,6 +107,56 @@ def test_fp8_attention_matches_oracle(orc, bd, case):
     assert int(err.item()) == 0
 
 
+MAGNITUDES = [
+    # (base workload, changes, value factor: a power of two, or "mixed" per row)
+    (3, dict(B=6, ctx_lo=20, ctx_hi=300), 2.0 ** -12),
+    (3, dict(B=6, ctx_lo=20, ctx_hi=300), 2.0 ** 14),
+    (3, dict(B=6, ctx_lo=20, ctx_hi=300), "mixed"),
+    (5, dict(B=4, ctx_lo=6, ctx_hi=200), "mixed"),
+]
+
+
+@pytest.mark.parametrize("case", MAGNITUDES, ids=[f"m{i}" for i in range(len(MAGNITUDES))])
+def test_fp8_attention_value_magnitudes(orc, bd, case):
+    """Values far from unit size (value scales from about 2^-20 up to 2^7.5,
+    just below the interface's limit of 256), all alike or a different power
+    of two per row (2^-6 .. 2^6): each output element is within 1% of itself
+    plus 1% of the same attention over |V| (the scale of the sum it comes
+    from), so the test does not depend on the values' size."""
+    base, changes, factor = case
+    inp = _inputs(base, changes, seed=650 + MAGNITUDES.index(case))
+    w = inp["workload"]
+    rng = np.random.default_rng(651 + MAGNITUDES.index(case))
+    for key in ("v_pool", "v_new"):                 # powers of two keep bf16 values exact
+        v = wl.bf16_to_f32(inp[key])
+        f = 2.0 ** rng.integers(-6, 7, size=v.shape[:-1] + (1,)) if factor == "mixed" else factor
+        inp[key] = wl.f32_to_bf16((v * f).astype(np.float32))
+    vmax = np.nanmax(np.abs(wl.bf16_to_f32(inp["v_pool"])))
+    assert vmax / 448 < 256                           # inside the interface's range
+    tiles = orc.kv_append_fp8(fp8_cache_for(orc, inp), inp["block_table"], inp["ctx_before"], inp["k_new"],
+                              inp["v_new"])
+    cache = upload_cache(bd, tiles)
+    out = torch.empty((w.B, w.q_len, w.Hq, w.D), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(bd.tts_decode_attn_workspace_size(w.B, w.q_len, w.Hq, w.Hkv, w.D, w.ctx_hi),
+                     dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scale = 1.0 / math.sqrt(w.D)
+    bd.tts_decode_attn(cache, dev(inp["block_table"]), dev(inp["ctx_lens"]), w.ctx_hi, dev(inp["q"]), out, ws,
+                       scale, w.causal, err=err)
+    torch.cuda.synchronize()
+    ref = orc.decode_attn_fp8(tiles, inp["block_table"], inp["ctx_lens"], inp["q"], scale, w.causal)
+    absv = tiles.copy()
+    absv[:, :, 2048:4096] &= 0x7F                    # |code|; the NaN code 0x7F stays NaN
+    mag = orc.decode_attn_fp8(absv, inp["block_table"], inp["ctx_lens"], inp["q"], scale, w.causal)
+    got = wl.bf16_to_f32(host(out)).astype(np.float64)
+    assert np.isfinite(got).all()
+    e = np.abs(got - ref)
+    ok = e <= 1e-2 * (np.abs(ref) + mag)
+    print(f"[fp8 attn magnitudes {factor}] max error / |V| attention {float((e / mag).max()):.3g}")
+    assert ok.all(), f"{int((~ok).sum())} elements off"
+    assert int(err.item()) == 0
+
+
 def test_fp8_decode_step_ids(orc, bd):
     """The fused step on an FP8 cache: GPU append, attention and head; ids as
     the oracle head picks them on the oracle's attention output (bf16)."""
