@@ -297,6 +297,17 @@ __host__ __device__ inline TcLayout tc_layout(int N, int CK) {
     return L;
 }
 
+__device__ __forceinline__ float2 lds_f32x2(uint32_t addr) {
+    float2 x;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(x.x), "=f"(x.y) : "r"(addr));
+    return x;
+}
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+    float x;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(x) : "r"(addr));
+    return x;
+}
+
 // Bulk copy shared::cta -> shared::cluster (another CTA of the cluster),
 // completing on an mbarrier of the destination CTA.
 __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
@@ -496,47 +507,52 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
     if (CK > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
     // ---- epilogue part 2: sum the CK partial copies of this CTA's RS rows and
-    // select per batch column.  Work item = (8-row group, column); consecutive
-    // threads take consecutive columns.  Source `rank` is this CTA's own dump.
-    const float *recv = reinterpret_cast<const float *>(smem + Lo.recv);
-    const int items = (RS / 8) * N;
-    // Item `item` -> its column, batch row, first vocabulary entry, the end of
-    // the entries it may select, and its 8 summed logits (written out too if
-    // asked).  False if the item selects nothing.
-    auto load_item = [&](int item, int &cn, int &r, int &v, uint32_t &allow, float *lg) -> bool {
-        const int gi = item / N;
-        cn = item - gi * N;
-        r = r0 + cn;
-        if (r >= a.R) return false;
+    // select per batch column.  A group is 8 consecutive vocabulary rows of
+    // one column; consecutive threads take consecutive columns.  Source
+    // `rank` is this CTA's own dump.
+    const int groups = RS / 8;
+    const int items = groups * N;
+    // The arguments read per group, in registers (a read through the kernel
+    // argument inside the loops costs a dependent load per group).
+    const int aR = a.R, aV = a.V;
+    const float *const a_bias = a.bias;
+    float *const a_logits = a.logits_out;
+    // Row r's selectable ids: below tail0, or a tail id whose bit is set in tm
+    // (the structural tail, or the boundary token alone with eos_allowed).
+    auto row_limits = [&](int r, int &tail0, uint32_t &tm) {
+        tail0 = aV;
+        tm = 0u;
+        if (a.tail) {
+            tail0 = aV - a.n_tail;
+            tm = a.tail[r];
+        } else if (a.eos && !a.eos[r]) {
+            tail0 = aV - 1;
+        }
+    };
+    // Group `gi` of column `cn` (batch row r, limits from row_limits) -> its
+    // first vocabulary entry, the mask of entries it may select, and its 8
+    // summed logits (written out too if asked).  False if the group selects
+    // nothing.
+    auto load_group = [&](int gi, int cn, int r, int tail0, uint32_t tm, int &v, uint32_t &allow,
+                          float *lg) -> bool {
 #pragma unroll
         for (int e = 0; e < 8; ++e) lg[e] = 0.0f;
         for (int src = 0; src < CK; ++src) {
-            const float *col = src == rank
-                                   ? dump + (static_cast<size_t>(rank) * RS + gi * 8) * Lo.dump_stride + cn
-                                   : recv + (static_cast<size_t>(src) * RS + gi * 8) * Lo.dump_stride + cn;
+            const uint32_t col = (src == rank ? base : base + Lo.recv) +
+                                 static_cast<uint32_t>(src * RS + gi * 8) * stride_b + 4u * static_cast<uint32_t>(cn);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) lg[e] += col[e * Lo.dump_stride];
+            for (int e = 0; e < 8; ++e) lg[e] += lds_f32(col + e * stride_b);
         }
         v = v0 + rank * RS + gi * 8;  // multiple of 8
-        if (a.bias) {
+        if (a_bias) {
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                if (v + e < a.V) lg[e] += a.bias[v + e];
+                if (v + e < aV) lg[e] += a_bias[v + e];
         }
-        if (a.logits_out) {
+        if (a_logits) {
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                if (v + e < a.V) a.logits_out[static_cast<size_t>(r) * a.V + v + e] = lg[e];
-        }
-        // ids this row may choose: below the structural tail, or a tail id
-        // whose mask bit is set (the boundary token alone with eos_allowed)
-        int tail0 = a.V;
-        uint32_t tm = 0u;
-        if (a.tail) {
-            tail0 = a.V - a.n_tail;
-            tm = a.tail[r];
-        } else if (a.eos && !a.eos[r]) {
-            tail0 = a.V - 1;
+                if (v + e < aV) a_logits[static_cast<size_t>(r) * aV + v + e] = lg[e];
         }
         if (v + 8 <= tail0) {  // every entry below the structural tail (nearly all items)
             allow = 0xFFu;
@@ -546,10 +562,21 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int id = v + e;
-            const bool ok = id < a.V && (id < tail0 || ((tm >> (id - tail0)) & 1u));
+            const bool ok = id < aV && (id < tail0 || ((tm >> (id - tail0)) & 1u));
             allow |= ok ? 1u << e : 0u;
         }
         return allow != 0u;
+    };
+    // The same for work item `item` = (group, column), column fastest.
+    auto load_item = [&](int item, int &cn, int &r, int &v, uint32_t &allow, float *lg) -> bool {
+        const int gi = item / N;
+        cn = item - gi * N;
+        r = r0 + cn;
+        if (r >= aR) return false;
+        int tail0;
+        uint32_t tm;
+        row_limits(r, tail0, tm);
+        return load_group(gi, cn, r, tail0, tm, v, allow, lg);
     };
     if constexpr (kFeatures) {
         // 8 features of one row per item, one 16-byte store of bf16 values:
@@ -588,6 +615,7 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
         // margin far above rounding) an entry cannot win, and its logarithms
         // are skipped.  Exact for the entries kept.  Two items per pass, so
         // each thread runs two independent Philox chains.
+        const float temperature = a.temperature;
         auto select = [&](bool live, int cn, int v, uint32_t allow, const float *lg, const Philox4x64 &ph) {
             if (!live) return;
             float lmax = -INFINITY;
@@ -597,7 +625,7 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
             const unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(colbest + cn);
             float thr = 0.0f;  // uniforms <= thr cannot win
             if (cur) {
-                const float g0 = unpack_value(cur) - lmax / a.temperature - kGumbelSlack;
+                const float g0 = unpack_value(cur) - lmax / temperature - kGumbelSlack;
                 thr = expf(-expf(-g0));
             }
             unsigned long long best = 0ull;
@@ -606,7 +634,7 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
                 if (!((allow >> e) & 1u)) continue;
                 const float u = bits_to_uniform(ph.half(e));
                 if (!(u > thr)) continue;
-                const float key = lg[e] / a.temperature + gumbel_from_uniform(u);
+                const float key = lg[e] / temperature + gumbel_from_uniform(u);
                 const unsigned long long k = pack_argmax(key, v + e);
                 best = k > best ? k : best;
             }
@@ -626,19 +654,93 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
             select(live1, cn1, vb, allow1, lg1, pb);
         }
     } else {
-        for (int item = threadIdx.x; item < items; item += blockDim.x) {
-            int cn, r, v;
-            uint32_t allow;
-            float lg[8];
-            if (!load_item(item, cn, r, v, allow, lg)) continue;
-            unsigned long long best = 0ull;
+        // Argmax: a thread takes 2 adjacent columns (one 8-byte read per
+        // vocabulary row) and every PQ-th group of them, so it runs 2
+        // independent chains.  Logits become 32-bit order keys (larger logit,
+        // larger key; 0 = not selectable) reduced by a max tree per group and
+        // column; the index is looked up only when a group improves its
+        // column's best, and a strict improvement keeps the lowest index among
+        // equal keys, as the packed key does.
+        const int NQ = N / 2;
+        const int PQ = max(1, min(groups, static_cast<int>(blockDim.x) / NQ));
+        if (static_cast<int>(threadIdx.x) < NQ * PQ) {
+            const int q = static_cast<int>(threadIdx.x) % NQ;
+            const int part = static_cast<int>(threadIdx.x) / NQ;
+            int tail0[2];
+            uint32_t tm[2];
+            bool live[2];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                if (!((allow >> e) & 1u)) continue;
-                const unsigned long long k = pack_argmax(lg[e], v + e);
-                best = k > best ? k : best;
+            for (int c = 0; c < 2; ++c) {
+                const int r = r0 + 2 * q + c;
+                live[c] = r < aR;
+                row_limits(live[c] ? r : r0, tail0[c], tm[c]);
             }
-            if (best) atomicMax(colbest + cn, best);
+            uint32_t bk[2] = {0u, 0u};
+            int bi[2] = {0, 0};
+            for (int gi = part; gi < groups; gi += PQ) {
+                const int v = v0 + rank * RS + gi * 8;
+                float x[8][2];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e][0] = x[e][1] = 0.0f;
+                for (int src = 0; src < CK; ++src) {
+                    const uint32_t row0 = (src == rank ? base : base + Lo.recv) +
+                                          static_cast<uint32_t>(src * RS + gi * 8) * stride_b + 8u * q;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float2 w = lds_f32x2(row0 + e * stride_b);
+                        x[e][0] += w.x;
+                        x[e][1] += w.y;
+                    }
+                }
+                if (a_bias) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float b = v + e < aV ? a_bias[v + e] : 0.0f;
+                        x[e][0] += b;
+                        x[e][1] += b;
+                    }
+                }
+                if (a_logits) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        if (!live[c]) continue;
+                        float *dst = a_logits + static_cast<size_t>(r0 + 2 * q + c) * aV;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            if (v + e < aV) dst[v + e] = x[e][c];
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t k[8];
+                    if (v + 8 <= tail0[c]) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) k[e] = float_order_key(x[e][c]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int id = v + e;
+                            const bool ok = id < aV && (id < tail0[c] || ((tm[c] >> (id - tail0[c])) & 1u));
+                            k[e] = ok ? float_order_key(x[e][c]) : 0u;
+                        }
+                    }
+                    const uint32_t gk = max(max(max(k[0], k[1]), max(k[2], k[3])),
+                                            max(max(k[4], k[5]), max(k[6], k[7])));
+                    if (gk > bk[c]) {
+                        int ef = 7;
+#pragma unroll
+                        for (int e = 6; e >= 0; --e)
+                            if (k[e] == gk) ef = e;
+                        bk[c] = gk;
+                        bi[c] = v + ef;
+                    }
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+                if (live[c] && bk[c])
+                    atomicMax(colbest + 2 * q + c, (static_cast<unsigned long long>(bk[c]) << 32) |
+                                                       static_cast<unsigned long long>(~static_cast<uint32_t>(bi[c])));
         }
     }
     __syncthreads();
