@@ -302,11 +302,6 @@ __device__ __forceinline__ float2 lds_f32x2(uint32_t addr) {
     asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(x.x), "=f"(x.y) : "r"(addr));
     return x;
 }
-__device__ __forceinline__ float lds_f32(uint32_t addr) {
-    float x;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(x) : "r"(addr));
-    return x;
-}
 
 // Bulk copy shared::cta -> shared::cluster (another CTA of the cluster),
 // completing on an mbarrier of the destination CTA.
@@ -327,9 +322,12 @@ __device__ __forceinline__ void st_async_u64(uint32_t dst_cluster, unsigned long
 }
 
 // kFeatures: the build for the modes that write bf16 features (the audio
-// head's first layer, projections); the other build selects tokens.  Kept
-// apart so each epilogue is compiled without the other's code.
-template <bool kFeatures>
+// head's first layer, projections); the other builds select tokens.  kWide:
+// the argmax build for wide batches (N >= 128), whose scan of each column
+// runs long enough to pay for its larger code; the narrow build's epilogue
+// runs once per CTA, where every instruction line is fetched cold.  Kept
+// apart so each epilogue is compiled without the others' code.
+template <bool kFeatures, bool kWide>
 __global__ void __launch_bounds__(kThreadsTC, 2)
 head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_h,
                const HeadArgs a, int N, int CK, int alloc_cols) {
@@ -507,52 +505,47 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
     if (CK > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
     // ---- epilogue part 2: sum the CK partial copies of this CTA's RS rows and
-    // select per batch column.  A group is 8 consecutive vocabulary rows of
-    // one column; consecutive threads take consecutive columns.  Source
-    // `rank` is this CTA's own dump.
-    const int groups = RS / 8;
-    const int items = groups * N;
-    // The arguments read per group, in registers (a read through the kernel
-    // argument inside the loops costs a dependent load per group).
-    const int aR = a.R, aV = a.V;
-    const float *const a_bias = a.bias;
-    float *const a_logits = a.logits_out;
-    // Row r's selectable ids: below tail0, or a tail id whose bit is set in tm
-    // (the structural tail, or the boundary token alone with eos_allowed).
-    auto row_limits = [&](int r, int &tail0, uint32_t &tm) {
-        tail0 = aV;
-        tm = 0u;
-        if (a.tail) {
-            tail0 = aV - a.n_tail;
-            tm = a.tail[r];
-        } else if (a.eos && !a.eos[r]) {
-            tail0 = aV - 1;
-        }
-    };
-    // Group `gi` of column `cn` (batch row r, limits from row_limits) -> its
-    // first vocabulary entry, the mask of entries it may select, and its 8
-    // summed logits (written out too if asked).  False if the group selects
-    // nothing.
-    auto load_group = [&](int gi, int cn, int r, int tail0, uint32_t tm, int &v, uint32_t &allow,
-                          float *lg) -> bool {
+    // select per batch column.  Work item = (8-row group, column); consecutive
+    // threads take consecutive columns.  Source `rank` is this CTA's own dump.
+    const float *recv = reinterpret_cast<const float *>(smem + Lo.recv);
+    const int items = (RS / 8) * N;
+    // Item `item` -> its column, batch row, first vocabulary entry, the end of
+    // the entries it may select, and its 8 summed logits (written out too if
+    // asked).  False if the item selects nothing.
+    auto load_item = [&](int item, int &cn, int &r, int &v, uint32_t &allow, float *lg) -> bool {
+        const int gi = item / N;
+        cn = item - gi * N;
+        r = r0 + cn;
+        if (r >= a.R) return false;
 #pragma unroll
         for (int e = 0; e < 8; ++e) lg[e] = 0.0f;
         for (int src = 0; src < CK; ++src) {
-            const uint32_t col = (src == rank ? base : base + Lo.recv) +
-                                 static_cast<uint32_t>(src * RS + gi * 8) * stride_b + 4u * static_cast<uint32_t>(cn);
+            const float *col = src == rank
+                                   ? dump + (static_cast<size_t>(rank) * RS + gi * 8) * Lo.dump_stride + cn
+                                   : recv + (static_cast<size_t>(src) * RS + gi * 8) * Lo.dump_stride + cn;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) lg[e] += lds_f32(col + e * stride_b);
+            for (int e = 0; e < 8; ++e) lg[e] += col[e * Lo.dump_stride];
         }
         v = v0 + rank * RS + gi * 8;  // multiple of 8
-        if (a_bias) {
+        if (a.bias) {
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                if (v + e < aV) lg[e] += a_bias[v + e];
+                if (v + e < a.V) lg[e] += a.bias[v + e];
         }
-        if (a_logits) {
+        if (a.logits_out) {
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                if (v + e < aV) a_logits[static_cast<size_t>(r) * aV + v + e] = lg[e];
+                if (v + e < a.V) a.logits_out[static_cast<size_t>(r) * a.V + v + e] = lg[e];
+        }
+        // ids this row may choose: below the structural tail, or a tail id
+        // whose mask bit is set (the boundary token alone with eos_allowed)
+        int tail0 = a.V;
+        uint32_t tm = 0u;
+        if (a.tail) {
+            tail0 = a.V - a.n_tail;
+            tm = a.tail[r];
+        } else if (a.eos && !a.eos[r]) {
+            tail0 = a.V - 1;
         }
         if (v + 8 <= tail0) {  // every entry below the structural tail (nearly all items)
             allow = 0xFFu;
@@ -562,21 +555,10 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int id = v + e;
-            const bool ok = id < aV && (id < tail0 || ((tm >> (id - tail0)) & 1u));
+            const bool ok = id < a.V && (id < tail0 || ((tm >> (id - tail0)) & 1u));
             allow |= ok ? 1u << e : 0u;
         }
         return allow != 0u;
-    };
-    // The same for work item `item` = (group, column), column fastest.
-    auto load_item = [&](int item, int &cn, int &r, int &v, uint32_t &allow, float *lg) -> bool {
-        const int gi = item / N;
-        cn = item - gi * N;
-        r = r0 + cn;
-        if (r >= aR) return false;
-        int tail0;
-        uint32_t tm;
-        row_limits(r, tail0, tm);
-        return load_group(gi, cn, r, tail0, tm, v, allow, lg);
     };
     if constexpr (kFeatures) {
         // 8 features of one row per item, one 16-byte store of bf16 values:
@@ -608,59 +590,20 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
         if (CK > 1) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
         return;
     }
-    if (a.mode == TTS_GUMBEL) {
-        // An entry can only beat the column's current best z_cur if its noise
-        // exceeds z_cur - logit / T.  With the group's largest logit that gives
-        // one uniform threshold for all 8 entries: below it (with a safety
-        // margin far above rounding) an entry cannot win, and its logarithms
-        // are skipped.  Exact for the entries kept.  Two items per pass, so
-        // each thread runs two independent Philox chains.
-        const float temperature = a.temperature;
-        auto select = [&](bool live, int cn, int v, uint32_t allow, const float *lg, const Philox4x64 &ph) {
-            if (!live) return;
-            float lmax = -INFINITY;
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                if ((allow >> e) & 1u) lmax = fmaxf(lmax, lg[e]);
-            const unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(colbest + cn);
-            float thr = 0.0f;  // uniforms <= thr cannot win
-            if (cur) {
-                const float g0 = unpack_value(cur) - lmax / temperature - kGumbelSlack;
-                thr = expf(-expf(-g0));
-            }
-            unsigned long long best = 0ull;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                if (!((allow >> e) & 1u)) continue;
-                const float u = bits_to_uniform(ph.half(e));
-                if (!(u > thr)) continue;
-                const float key = lg[e] / temperature + gumbel_from_uniform(u);
-                const unsigned long long k = pack_argmax(key, v + e);
-                best = k > best ? k : best;
-            }
-            if (best) atomicMax(colbest + cn, best);
-        };
-        for (int i0 = threadIdx.x; i0 < items; i0 += 2 * blockDim.x) {
-            const int i1 = i0 + blockDim.x;
-            int cn0, r0i, va, cn1 = 0, r1i = 0, vb = 0;
-            uint32_t allow0, allow1 = 0u;
-            float lg0[8], lg1[8];
-            const bool live0 = load_item(i0, cn0, r0i, va, allow0, lg0);
-            const bool live1 = i1 < items && load_item(i1, cn1, r1i, vb, allow1, lg1);
-            const int ra = live0 ? r0i : r0, rb = live1 ? r1i : r0;
-            const Philox4x64 pa(static_cast<uint64_t>(va >> 3), 0, a.pos, 0, a.seed[ra], a.step[ra]);
-            const Philox4x64 pb(static_cast<uint64_t>(vb >> 3), 0, a.pos, 0, a.seed[rb], a.step[rb]);
-            select(live0, cn0, va, allow0, lg0, pa);
-            select(live1, cn1, vb, allow1, lg1, pb);
-        }
-    } else {
-        // Argmax: a thread takes 2 adjacent columns (one 8-byte read per
-        // vocabulary row) and every PQ-th group of them, so it runs 2
-        // independent chains.  Logits become 32-bit order keys (larger logit,
-        // larger key; 0 = not selectable) reduced by a max tree per group and
-        // column; the index is looked up only when a group improves its
-        // column's best, and a strict improvement keeps the lowest index among
-        // equal keys, as the packed key does.
+    if constexpr (kWide) {
+        // Argmax over wide batches: a thread takes 2 adjacent columns (one
+        // 8-byte read per vocabulary row) and every PQ-th 8-row group of them,
+        // so it runs 2 independent chains.  Logits become 32-bit order keys
+        // (larger logit, larger key; 0 = not selectable) reduced by a max tree
+        // per group and column; the index is looked up only when a group raises
+        // its column's best, and a strict raise keeps the lowest index among
+        // equal keys, as the packed key does.  The arguments used per group
+        // are read once (a read through the kernel argument in the loop costs
+        // a dependent load per group).
+        const int aR = a.R, aV = a.V;
+        const float *const a_bias = a.bias;
+        float *const a_logits = a.logits_out;
+        const int groups = RS / 8;
         const int NQ = N / 2;
         const int PQ = max(1, min(groups, static_cast<int>(blockDim.x) / NQ));
         if (static_cast<int>(threadIdx.x) < NQ * PQ) {
@@ -673,7 +616,15 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
             for (int c = 0; c < 2; ++c) {
                 const int r = r0 + 2 * q + c;
                 live[c] = r < aR;
-                row_limits(live[c] ? r : r0, tail0[c], tm[c]);
+                // ids this row may choose: below tail0, or a tail id whose bit is set
+                tail0[c] = aV;
+                tm[c] = 0u;
+                if (live[c] && a.tail) {
+                    tail0[c] = aV - a.n_tail;
+                    tm[c] = a.tail[r];
+                } else if (live[c] && a.eos && !a.eos[r]) {
+                    tail0[c] = aV - 1;
+                }
             }
             uint32_t bk[2] = {0u, 0u};
             int bi[2] = {0, 0};
@@ -741,6 +692,65 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
                 if (live[c] && bk[c])
                     atomicMax(colbest + 2 * q + c, (static_cast<unsigned long long>(bk[c]) << 32) |
                                                        static_cast<unsigned long long>(~static_cast<uint32_t>(bi[c])));
+        }
+    } else if (a.mode == TTS_GUMBEL) {
+        // An entry can only beat the column's current best z_cur if its noise
+        // exceeds z_cur - logit / T.  With the group's largest logit that gives
+        // one uniform threshold for all 8 entries: below it (with a safety
+        // margin far above rounding) an entry cannot win, and its logarithms
+        // are skipped.  Exact for the entries kept.  Two items per pass, so
+        // each thread runs two independent Philox chains.
+        auto select = [&](bool live, int cn, int v, uint32_t allow, const float *lg, const Philox4x64 &ph) {
+            if (!live) return;
+            float lmax = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if ((allow >> e) & 1u) lmax = fmaxf(lmax, lg[e]);
+            const unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(colbest + cn);
+            float thr = 0.0f;  // uniforms <= thr cannot win
+            if (cur) {
+                const float g0 = unpack_value(cur) - lmax / a.temperature - kGumbelSlack;
+                thr = expf(-expf(-g0));
+            }
+            unsigned long long best = 0ull;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (!((allow >> e) & 1u)) continue;
+                const float u = bits_to_uniform(ph.half(e));
+                if (!(u > thr)) continue;
+                const float key = lg[e] / a.temperature + gumbel_from_uniform(u);
+                const unsigned long long k = pack_argmax(key, v + e);
+                best = k > best ? k : best;
+            }
+            if (best) atomicMax(colbest + cn, best);
+        };
+        for (int i0 = threadIdx.x; i0 < items; i0 += 2 * blockDim.x) {
+            const int i1 = i0 + blockDim.x;
+            int cn0, r0i, va, cn1 = 0, r1i = 0, vb = 0;
+            uint32_t allow0, allow1 = 0u;
+            float lg0[8], lg1[8];
+            const bool live0 = load_item(i0, cn0, r0i, va, allow0, lg0);
+            const bool live1 = i1 < items && load_item(i1, cn1, r1i, vb, allow1, lg1);
+            const int ra = live0 ? r0i : r0, rb = live1 ? r1i : r0;
+            const Philox4x64 pa(static_cast<uint64_t>(va >> 3), 0, a.pos, 0, a.seed[ra], a.step[ra]);
+            const Philox4x64 pb(static_cast<uint64_t>(vb >> 3), 0, a.pos, 0, a.seed[rb], a.step[rb]);
+            select(live0, cn0, va, allow0, lg0, pa);
+            select(live1, cn1, vb, allow1, lg1, pb);
+        }
+    } else {
+        for (int item = threadIdx.x; item < items; item += blockDim.x) {
+            int cn, r, v;
+            uint32_t allow;
+            float lg[8];
+            if (!load_item(item, cn, r, v, allow, lg)) continue;
+            unsigned long long best = 0ull;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (!((allow >> e) & 1u)) continue;
+                const unsigned long long k = pack_argmax(lg[e], v + e);
+                best = k > best ? k : best;
+            }
+            if (best) atomicMax(colbest + cn, best);
         }
     }
     __syncthreads();
@@ -922,7 +932,9 @@ int launch_head(const HeadLaunch &L, LaunchOpts o) {
     } else {
         const TcPlan &p = st->p;
         const bool features = st->a.mode == kModeExpand || st->a.mode == kModeLinear;
-        const auto kernel = features ? head_tc_kernel<true> : head_tc_kernel<false>;
+        const bool wide = !features && st->a.mode == TTS_ARGMAX && p.N >= 128;
+        const auto kernel = features ? head_tc_kernel<true, false>
+                                     : (wide ? head_tc_kernel<false, true> : head_tc_kernel<false, false>);
         if (!ensure_dynamic_smem(reinterpret_cast<const void *>(kernel), static_cast<int>(p.smem)))
             return TTS_ERR_CUDA;
         cfg.gridDim = dim3(static_cast<unsigned>(((st->a.V + kTileM - 1) / kTileM) * p.CK),
