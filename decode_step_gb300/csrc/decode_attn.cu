@@ -152,11 +152,14 @@ __device__ __forceinline__ T *out_row(const AttnArgs &a, int b, int g, int r) {
 }
 
 // Warps given tiles: at least kMinTilesPerWarp each when the work is small
-// (fewer split segments to publish and merge), else every warp of the grid.
+// (fewer split segments to publish and merge), but never fewer warps than
+// segments (B x Hkv): short segments gain nothing from sharing a warp and
+// would only run one after another; else every warp of the grid.
 constexpr long long kMinTilesPerWarp = 4;
-__device__ __forceinline__ long long active_workers(int workers, long long Ttot) {
-    const long long by_work = (Ttot + kMinTilesPerWarp - 1) / kMinTilesPerWarp;
-    return min(static_cast<long long>(workers), by_work > 0 ? by_work : 1);
+__device__ __forceinline__ long long active_workers(int workers, long long Ttot, long long segments) {
+    long long w = (Ttot + kMinTilesPerWarp - 1) / kMinTilesPerWarp;
+    w = w > segments ? w : segments;
+    return min(static_cast<long long>(workers), w > 0 ? w : 1);
 }
 
 // The last contributor of a split segment merges the contributors' partials
@@ -280,7 +283,7 @@ decode_attn_simt_kernel(const AttnArgs a) {
     pdl_allow_dependents();
     scan_streams<T, D, kWarps>(a, prefix, ctxs, scan);
     const long long Ttot = prefix[a.B];
-    const long long Wtot = active_workers(a.workers, Ttot);
+    const long long Wtot = active_workers(a.workers, Ttot, static_cast<long long>(a.B) * a.Hkv);
     const int wid = blockIdx.x * kWarps + warp;
     if (Ttot == 0 || wid >= Wtot) return;
     const int t0 = static_cast<int>(range_start(wid, Ttot, Wtot));
@@ -689,7 +692,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
     pdl_allow_dependents();
     scan_streams<T, D, kTcWarps>(a, prefix, ctxs, scan);
     const long long Ttot = prefix[a.B];
-    const long long Wtot = active_workers(a.workers, Ttot);
+    const long long Wtot = active_workers(a.workers, Ttot, static_cast<long long>(a.B) * a.Hkv);
     const int wid = blockIdx.x * kTcWarps + warp;
     if (Ttot == 0 || wid >= Wtot) return;
     const int t0 = static_cast<int>(range_start(wid, Ttot, Wtot));
