@@ -72,6 +72,7 @@ CASES = [
     (16, 2048, 4096, 16386, 2, "argmax", 0.0),       # CB0: 16,384 codes + row terminator + <|audio_split|>
     (16, 2048, 4096, 16386, 2, "gumbel", 0.7),
     (40, 512, 1024, 777, 0, "gumbel", 1.3),          # no structural tail
+    (160, 256, 512, 1000, 3, "argmax", 0.0),         # 160 rows: the wide argmax build, with tail masks and bias
 ]
 
 
