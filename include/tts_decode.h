@@ -52,7 +52,7 @@ extern "C" {
 typedef enum {
     TTS_OK = 0,
     TTS_ERR_INVALID = -1,          /* null pointer, bad size, inconsistent shape */
-    TTS_ERR_UNSUPPORTED = -2,      /* a shape or type this build has no kernel for */
+    TTS_ERR_UNSUPPORTED = -2,      /* a shape or type the library has no kernel for */
     TTS_ERR_WORKSPACE = -3,        /* workspace missing, misaligned or too small */
     TTS_ERR_CUDA = -4,             /* a CUDA launch or runtime call failed */
     TTS_ERR_POOL_EXHAUSTED = -5,   /* block pool has too few free blocks */
