@@ -158,3 +158,86 @@ def test_step_graph_rejects_bad_descriptors(L):
     assert L.tts_step_graph_create(ctypes.byref(desc), ctypes.byref(handle)) == -1
     assert L.tts_step_graph_launch(None, None) == -1
     L.tts_step_graph_destroy(None)
+
+
+def test_rope_append_and_noalloc_attention_argument_checks(L):
+    c = _cache()
+    rope = lambda **k: L.tts_kv_append_rope(  # noqa: E731
+        ctypes.byref(k.get("cache", c)), FAKE, 4, FAKE, k.get("B", 2), 1, k.get("Hq", 16),
+        k.get("base", 10000.0), k.get("q", FAKE), FAKE, FAKE, None, None)
+    assert rope(base=0.0) == -1                       # the plain append is tts_kv_append
+    assert rope(base=1.0) == -1 and rope(base=float("inf")) == -1
+    assert rope(q=None) == -1
+    assert rope(Hq=12) == -1                          # not a multiple of Hkv
+    assert rope(cache=_cache(dtype=0, d=64)) == -2    # fp32 rows have no rotary build
+    assert rope(cache=_cache(d=64)) == -2
+    assert rope(B=0) == 0                             # nothing to do
+    noalloc = lambda **k: L.tts_decode_attn_noalloc(  # noqa: E731
+        k.get("cache", ctypes.byref(c)), FAKE, 94, FAKE, 1500, k.get("B", 4), 1, k.get("Hq", 16), 0.08, 0,
+        k.get("q", FAKE), FAKE, None, None)
+    assert noalloc(cache=None) == -1
+    assert noalloc(Hq=12) == -1                       # rejected before the static scratch is looked up
+    assert noalloc(B=0) == 0
+
+
+def test_audio_head_argument_checks(L):
+    def audio(**k):
+        return L.tts_audio_head_select(
+            k.get("h", FAKE), FAKE, None, FAKE, None, k.get("R", 4), 2048, k.get("F", 4096), 4097, 1, None,
+            k.get("mode", 0), 0.0, None, None, k.get("z", FAKE), FAKE, None, None, FAKE, 0, None)
+    assert audio(mode=5) == -1
+    assert audio(F=100) == -2                         # the second layer reduces over F: F % 64 == 0
+    assert audio(F=0) == -2
+    assert audio(h=None) == -1
+    assert audio(z=None) == -1                        # the first layer writes z
+    assert audio(R=0) == -1 and audio(R=5000) == -1
+
+
+def test_code_predictor_argument_checks(L):
+    assert L.tts_code_predictor_workspace_size(64, 1024, 8, 4, 128, 2048, 15) > 0
+    assert L.tts_code_predictor_workspace_size(0, 1024, 8, 4, 128, 2048, 15) == 0
+    assert L.tts_code_predictor_workspace_size(64, 1024, 8, 4, 128, 2048, 0) == 0
+
+    def desc(**k):
+        f = dict(R=64, H=1024, num_q_heads=8, num_kv_heads=4, head_dim=128, V=2048, n_steps=15, mode=0,
+                 temperature=0.0, d_x0=FAKE.value, d_Wqkv=FAKE.value, d_W=FAKE.value, d_E=FAKE.value,
+                 d_seed=None, d_step=None, d_tokens=FAKE.value, d_ws=FAKE.value, ws_bytes=0, d_err=None, flags=0)
+        f.update(k)
+        return _lib.CodePredictorDesc(**f)
+    run = lambda **k: L.tts_code_predictor_run(ctypes.byref(desc(**k)), None)  # noqa: E731
+    assert L.tts_code_predictor_run(None, None) == -1
+    assert run(d_x0=None) == -1
+    assert run(R=0) == -1
+    assert run(num_q_heads=6) == -1                   # not a multiple of the KV heads
+    assert run(num_q_heads=12) == -2                  # heads x head_dim must equal H
+    assert run() == -3                                # workspace too small
+    handle = ctypes.c_void_p()
+    assert L.tts_code_predictor_graph_create(ctypes.byref(desc(d_E=None)), ctypes.byref(handle)) == -1
+    assert L.tts_code_predictor_graph_launch(None, None) == -1
+    L.tts_code_predictor_graph_destroy(None)
+
+
+def test_step_graph_set_rejects_bad_sizes(L):
+    desc = _lib.StepGraphDesc()
+    desc.B = 64
+    desc.input_bytes = 64 * 1024
+    handle = ctypes.c_void_p()
+    i32 = lambda *v: (ctypes.c_int32 * len(v))(*v)    # noqa: E731
+    sz = lambda *v: (ctypes.c_size_t * len(v))(*v)    # noqa: E731
+
+    def create(sizes, offs=(0,), rows=(16,), d=desc):
+        s = i32(*sizes) if sizes else None
+        return L.tts_step_graph_set_create(ctypes.byref(d) if d is not None else None, s, len(sizes),
+                                           sz(*offs), sz(*rows), len(offs), ctypes.byref(handle))
+    assert create([1, 4, 64], d=None) == -1
+    assert create([]) == -1                            # no size
+    assert create(list(range(1, 18))) == -1            # more than TTS_GRAPH_SET_MAX sizes
+    assert create([4, 4, 64]) == -1                    # not strictly increasing
+    assert create([1, 4, 32]) == -1                    # the largest size must be B
+    assert create([1, 4, 65]) == -1                    # beyond B
+    assert create([1, 64], offs=(8,)) == -1            # a region not 16-byte aligned
+    assert create([1, 64], rows=(6,)) == -1            # row bytes not a multiple of 4
+    assert create([1, 64], rows=(2048,)) == -1         # B rows of 2 KB overrun 64 KB
+    assert create([1, 64], offs=(64 * 1024,)) == -1    # starts past the buffers
+    assert L.tts_step_graph_set_launch(None, 4, None, None) == -1
+    L.tts_step_graph_set_destroy(None)
