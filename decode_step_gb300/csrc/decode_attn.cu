@@ -34,6 +34,8 @@
 // p, p + 2, ...; dot products are reduced across the 16 chunk lanes by
 // recursive halving, leaving every lane the full scores of one token for half
 // of the query rows.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 #include <new>
 
@@ -1290,10 +1292,9 @@ extern "C" int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block
 // Decode attention without a caller workspace.
 //
 // Some callers cannot allocate device memory where they run a decode step:
-// code that runs while a CUDA graph is being captured (an allocation there
-// breaks the capture), engines that reserve all free device memory for the KV
-// pool at start-up and so leave nothing for cudaMalloc, hosts that hand a
-// plugin no allocator, and real-time loops that cannot afford the implicit
+// engines that hand all free device memory to the KV pool at start-up and so
+// leave nothing for cudaMalloc, plugin hosts that give a library no
+// allocator, and real-time loops that cannot absorb the implicit
 // synchronisation and unbounded latency of cudaMalloc / cudaFree inside a
 // frame deadline.  For them the split-KV partials live in one file-scope
 // device array of fixed size instead of a caller workspace.  Every GPU that
@@ -1307,12 +1308,48 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_attn_scratch[kStaticScratchBytes];
 
+// The array's device address, cached per device together with the id of the
+// CUDA context it was looked up in.  Context ids are never reused within a
+// process, so a context replaced after cudaDeviceReset (or a context made
+// current through the driver API) triggers a fresh lookup instead of reusing
+// an address of a module that is gone.
+struct ScratchAddr {
+    unsigned long long ctx_id;
+    void *addr;
+};
 std::mutex g_scratch_mu;
-void *g_scratch_addr[kMaxDevices] = {};
+ScratchAddr g_scratch_addr[kMaxDevices] = {};
 
-// Device address of g_attn_scratch on the current device.  The symbol's name
-// in host code is only a host-side handle, so the address is looked up once
-// per device (with that device current) and cached.
+PFN_cuCtxGetCurrent_v4000 g_ctx_get_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_get_id = nullptr;
+
+// Id of the current CUDA context, or 0 if none is current or the driver
+// calls are unavailable.
+unsigned long long current_context_id() {
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    if (!g_ctx_get_current || !g_ctx_get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    if (g_ctx_get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of g_attn_scratch in the current context.  The symbol's
+// name in host code is only a host-side handle, so the address is looked up
+// with cudaGetSymbolAddress (with the device current) the first time a
+// context uses it, and cached for that context.
 int static_scratch_address(void **out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -1321,15 +1358,20 @@ int static_scratch_address(void **out) {
     }
     if (dev < 0 || dev >= kMaxDevices) return TTS_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    ScratchAddr &e = g_scratch_addr[dev];
+    const unsigned long long id = current_context_id();
+    if (!e.addr || id == 0 || id != e.ctx_id) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || !p) {
             cudaGetLastError();
+            e.addr = nullptr;
             return TTS_ERR_CUDA;
         }
-        g_scratch_addr[dev] = p;
+        e.addr = p;
+        // the lookup made the device's primary context current if none was
+        e.ctx_id = id != 0 ? id : current_context_id();
     }
-    *out = g_scratch_addr[dev];
+    *out = e.addr;
     return TTS_OK;
 }
 
@@ -1351,17 +1393,21 @@ extern "C" int tts_decode_attn_noalloc(const tts_kv_cache *cache, const int32_t 
                                stream);
     if (need > kStaticScratchBytes) return TTS_ERR_SCRATCH_LIMIT;
     void *scratch = nullptr;
-    const int st = static_scratch_address(&scratch);
+    int st = static_scratch_address(&scratch);
+    if (st != TTS_OK) return st;
+    // Every argument is checked before anything is queued, so a rejected call
+    // leaves the shared array untouched.
+    AttnLaunch L;
+    st = prepare_attn(cache, d_block_table, max_blocks_per_seq, d_ctx_lens, max_ctx_len, B, q_len, num_q_heads,
+                      scale, causal, d_q, d_out, scratch, need, d_err, &L);
     if (st != TTS_OK) return st;
     // The split tickets must start at zero; they sit at the end of the
     // workspace layout.  The array keeps whatever the previous call left.
     const size_t tickets = align_up(static_cast<size_t>(B) * cache->num_kv_heads * sizeof(int32_t), 256);
-    if (cudaMemsetAsync(static_cast<uint8_t *>(scratch) + need - tickets, 0, tickets,
-                        static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(static_cast<uint8_t *>(scratch) + need - tickets, 0, tickets, s) != cudaSuccess) {
         cudaGetLastError();
         return TTS_ERR_CUDA;
     }
-    return tts_decode_attn(cache, d_block_table, max_blocks_per_seq, d_ctx_lens, max_ctx_len, B,
-                           q_len, num_q_heads, scale, causal, d_q, d_out, scratch, need, d_err,
-                           stream);
+    return launch_attn(L, {s, false});
 }

@@ -212,22 +212,25 @@ int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block_table,
                     void *stream);
 
 /* Decode attention with no caller workspace and no allocation.
- * The pages have no counterpart for this entry point; it exists for callers
- * that cannot allocate device memory where they run a decode step: code
- * running while a CUDA graph is captured (an allocation breaks the capture),
- * engines that reserve all free device memory for the KV pool at start-up,
- * plugin hosts that give a library no allocator, and real-time loops that
- * cannot absorb cudaMalloc's implicit synchronisation inside a frame budget.
- * Same arguments and results as tts_decode_attn, without d_ws / ws_bytes.
- * The split partials live in one 24 MiB file-scope device array that every
- * GPU loading this library holds until the process exits; a request whose
- * tts_decode_attn_workspace_size exceeds 24 MiB returns TTS_ERR_SCRATCH_LIMIT
- * and launches nothing.  The first call on a device looks up the array's
- * device address (cudaGetSymbolAddress), so make that first call before any
- * stream capture.  Every call shares the one array and it keeps the previous
- * call's contents: each call clears the part that must start at zero, and
- * calls whose executions overlap on the GPU (other streams, other threads)
- * race on it.  Calls no cudaMalloc / cudaFree. */
+ * The pages have no counterpart for this entry point.  It is for callers that
+ * cannot call cudaMalloc where they run a decode step: engines that hand all
+ * free device memory to the KV pool at start-up and so have none left to
+ * allocate, plugin hosts that give a library no allocator, and real-time
+ * loops that cannot absorb cudaMalloc's implicit synchronisation inside a
+ * frame budget.  Same arguments and results as tts_decode_attn, without
+ * d_ws / ws_bytes.  The split partials live in one 24 MiB file-scope device
+ * array that every GPU loading this library holds until the process exits; a
+ * request whose tts_decode_attn_workspace_size exceeds 24 MiB returns
+ * TTS_ERR_SCRATCH_LIMIT and launches nothing.  The first call in a CUDA
+ * context (per device, and again after that context is replaced, e.g. by
+ * cudaDeviceReset) looks up the array's device address with
+ * cudaGetSymbolAddress; make that first call before any stream capture.
+ * Arguments are validated before anything is queued, so a rejected call
+ * leaves the array untouched.  Every call shares the one array and it keeps
+ * the previous call's contents: each call clears the part that must start at
+ * zero, and calls whose executions overlap on the GPU (other streams, other
+ * threads) race on it.  Calls no cudaMalloc / cudaFree and no allocating
+ * library routine. */
 int tts_decode_attn_noalloc(const tts_kv_cache *cache, const int32_t *d_block_table,
                             int32_t max_blocks_per_seq, const int32_t *d_ctx_lens,
                             int32_t max_ctx_len, int32_t B, int32_t q_len, int32_t num_q_heads,

@@ -1,8 +1,9 @@
-"""tts_decode_attn_noalloc: decode attention for callers that cannot allocate
-device memory (for example code running under CUDA graph capture, or an engine
-that has reserved all free memory for its KV pool).  It must give the same
-output as tts_decode_attn with a caller workspace, call after call, although
-every call reuses the one static scratch array.
+"""tts_decode_attn_noalloc: decode attention for callers that cannot call
+cudaMalloc where they run a step (an engine that has handed all free device
+memory to its KV pool, a plugin host that gives the library no allocator, a
+real-time loop that cannot absorb cudaMalloc's synchronisation).  It must give
+the same output as tts_decode_attn with a caller workspace, call after call,
+although every call reuses the one static scratch array.
 
 Kept in a file of its own that pytest collects last, so a run that stops at
 the first failure has already run every other test.
@@ -35,8 +36,7 @@ def _attn_with_workspace(u, cache, w):
 CASES = {"acoustic-b64": wl.WORKLOADS[3], "verify-b64": wl.WORKLOADS[5]}
 
 
-@pytest.mark.parametrize("name", sorted(CASES))
-def test_noalloc_matches_workspace_entry_point(name):
+def _check_noalloc_twice(name):
     inp = wl.make_inputs(CASES[name], with_head=False, with_verify=False)
     w = inp["workload"]
     u = Uploaded(inp)
@@ -50,10 +50,24 @@ def test_noalloc_matches_workspace_entry_point(name):
                                    1.0 / math.sqrt(w.D), w.causal, err=err)
         torch.cuda.synchronize()
         got = as_f64(host(out), w.dtype)
-        assert np.isfinite(got).all(), f"call {call}: non-finite output"
+        assert np.isfinite(got).all(), f"{name} call {call}: non-finite output"
         bad, mx_abs, _ = attn_errors(got, ref)
-        assert bad == 0, f"call {call}: {bad} elements differ (max abs {mx_abs})"
+        assert bad == 0, f"{name} call {call}: {bad} elements differ (max abs {mx_abs})"
     assert int(err.item()) == 0
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_noalloc_matches_workspace_entry_point(name):
+    _check_noalloc_twice(name)
+
+
+def test_noalloc_clears_tickets_left_by_a_larger_call():
+    # verify-b64's 10-row partial slots reach ~19 MB into the array, across
+    # the offset where acoustic-b64's split tickets sit (~3.8 MB), and leave
+    # nonzero floats there.  The acoustic call must still start from zeroed
+    # tickets and match the workspace entry point.
+    _check_noalloc_twice("verify-b64")
+    _check_noalloc_twice("acoustic-b64")
 
 
 def test_noalloc_rejects_requests_beyond_the_static_scratch():
