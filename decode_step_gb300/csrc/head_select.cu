@@ -21,6 +21,7 @@
 //
 // fp32: a CUDA-core kernel (tf32 tensor cores would change the rounding of
 // fp32 inputs), one warp per vocabulary row.
+#include <mutex>
 #include <new>
 
 #include "tts_common.cuh"
@@ -782,6 +783,248 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
                      a.V - 1);
 }
 
+// ------------------------------------------- split build (narrow batches)
+//
+// For batches of up to 64 rows.  A cluster of CK CTAs owns one 128-row vocab
+// tile; CTA rank r reduces the hidden range [r H / CK, (r + 1) H / CK).  Every
+// W and h k-slice of the CTA is requested at once (no ring reuse: at 64 x
+// 2048 x 4097 the CTA's 128 KB of W and 64 KB of h are all in flight), so the
+// load time is the HBM burst itself.  The epilogue is kept short because it
+// runs once per CTA with its instructions fetched cold: each accumulator row
+// (one vocab row, read from TMEM by the thread of that lane) is stored
+// straight into the shared memory of the CTA that owns the row, one cluster
+// barrier publishes all partials, and every CTA then sums its 32 rows over
+// the CK sources, selects per batch row, and folds its best keys into the
+// global keys; the last CTA converts keys to ids.
+constexpr int kSplitThreads = 256;
+constexpr int kSplitMaxN = 64;
+
+struct SplitLayout {
+    uint32_t hslot;    // bytes of one h k-slice (N rows x 128 B)
+    uint32_t h;        // offset of the h slices (after the W slices)
+    uint32_t recv;     // offset of recv[CK][RS][N] fp32 partials
+    uint32_t bars;     // kch full barriers, then the accumulator barrier
+    uint32_t colbest;  // [N] packed keys
+    uint32_t misc;     // TMEM address, flag, failure word
+    uint32_t total;
+};
+
+__host__ __device__ inline SplitLayout split_layout(int N, int kch, int CK, int RS) {
+    SplitLayout L;
+    L.hslot = static_cast<uint32_t>(N) * 128u;
+    L.h = static_cast<uint32_t>(kch) * kATileBytes;
+    L.recv = L.h + static_cast<uint32_t>(kch) * L.hslot;
+    L.bars = L.recv + static_cast<uint32_t>(CK * RS * N) * 4u;
+    L.colbest = L.bars + 8u * (kch + 1);
+    L.misc = L.colbest + 8u * N;
+    L.total = L.misc + 16u + 1024u;  // + slack to align the dynamic base to 1024
+    return L;
+}
+
+// Position of float n within a partial row i of recv: the row's 16-byte
+// chunks are rotated by i, so the 32 lanes of a warp storing 32 different rows
+// spread over all banks, and a warp reading one row's consecutive columns
+// still touches distinct banks.
+__device__ __forceinline__ int split_pos(int i, int n, int N) {
+    const int nc = N >> 2;
+    return ((((n >> 2) + i) % nc) << 2) | (n & 3);
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+template <bool kGumbel>
+__global__ void __launch_bounds__(kSplitThreads, 1)
+head_split_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_h,
+                  const HeadArgs a, int N, int CK, int RS, int alloc_cols) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    const int kch = a.H / kTileK / CK;
+    const SplitLayout Lo = split_layout(N, kch, CK, RS);
+    const uint32_t bar_full = base + Lo.bars;        // [kch]
+    const uint32_t bar_acc = bar_full + 8u * kch;
+    unsigned long long *colbest = reinterpret_cast<unsigned long long *>(smem + Lo.colbest);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lo.misc);
+    int *flag = reinterpret_cast<int *>(smem + Lo.misc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int v0 = (blockIdx.x / CK) * kTileM;  // first vocab row of the cluster's tile
+    const int kbase = rank * kch * kTileK;
+
+    if (threadIdx.x == 0) {
+        for (int c = 0; c <= kch; ++c) mbar_init(bar_full + 8u * c, 1);
+        fence_mbar_init();
+    }
+    pdl_allow_dependents();
+    for (int i = threadIdx.x; i < N; i += blockDim.x) colbest[i] = 0ull;
+    __syncthreads();
+    if (warp == 0 && lane == 0) {
+        // Every slice at once: W (independent of the previous kernel) first,
+        // h (its output) after the programmatic-launch wait.
+        prefetch_tensormap(&map_w);
+        prefetch_tensormap(&map_h);
+        for (int c = 0; c < kch; ++c) {
+            mbar_arrive_expect_tx(bar_full + 8u * c, kATileBytes + Lo.hslot);
+            tma_load_2d(base + c * kATileBytes, &map_w, kbase + c * kTileK, v0, bar_full + 8u * c);
+        }
+        pdl_wait_prerequisites();
+        for (int c = 0; c < kch; ++c)
+            tma_load_2d(base + Lo.h + c * Lo.hslot, &map_h, kbase + c * kTileK, 0, bar_full + 8u * c);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(tmem_slot)),
+                     "r"(alloc_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 1 && lane == 0) {
+        // D[128 x N] += W_slice[128 x 64] . h_slice[N x 64]^T per slice, in arrival order
+        const uint32_t idesc = mma_idesc(kTileM, N);
+        bool ok = true;
+        for (int c = 0; c < kch; ++c) {
+            if (ok && !mbar_wait(bar_full + 8u * c, 0)) {
+                flag_error(a.err, TTS_ERRBIT_TIMEOUT);
+                ok = false;
+            }
+            if (!ok) continue;  // no MMA on a slice that never arrived
+            tc_fence_after();
+            const uint32_t wa = base + c * kATileBytes, ha = base + Lo.h + c * Lo.hslot;
+#pragma unroll
+            for (int kk = 0; kk < kTileK / 16; ++kk)
+                mma_bf16(tmem, sw128_desc(wa + kk * 32), sw128_desc(ha + kk * 32), idesc, (c | kk) != 0);
+        }
+        mma_commit(bar_acc);  // fires once every MMA issued above has completed
+    }
+    __syncwarp();
+
+    // ---- accumulator row (vocab row 32 w + lane of the tile) -> its owner
+    if (warp < 4) {
+        const int vl = warp * 32 + lane;
+        const int owner = vl / RS;
+        bool ready = true;
+        if (!mbar_wait(bar_acc, 0)) {
+            flag_error(a.err, TTS_ERRBIT_TIMEOUT);
+            ready = false;
+        }
+        tc_fence_after();
+        if (__all_sync(kFull, ready)) {
+            const int i = vl - owner * RS;
+            const uint32_t row = base + Lo.recv + static_cast<uint32_t>((rank * RS + i) * N) * 4u;
+            const uint32_t dst = map_cluster(row, static_cast<uint32_t>(owner < CK ? owner : 0));
+            for (int c0 = 0; c0 < N; c0 += 16) {
+                float v[16];
+                tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
+                if (owner < CK) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        st_cluster_v4(dst + 4u * split_pos(i, c0 + 4 * q, N), v[4 * q], v[4 * q + 1], v[4 * q + 2],
+                                      v[4 * q + 3]);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    // every partial row is in its owner's shared memory after this barrier
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(alloc_cols)
+                     : "memory");
+    }
+
+    // ---- sum the CK partials of this CTA's rows and select per batch row.
+    // Item = (8-row group, batch row); consecutive threads take consecutive
+    // batch rows, so each recv row is read with consecutive addresses.
+    const float *recv = reinterpret_cast<const float *>(smem + Lo.recv);
+    const int items = (RS / 8) * N;
+    const int aR = a.R, aV = a.V;
+    for (int item = threadIdx.x; item < items; item += blockDim.x) {
+        const int n = item % N, g = item / N;
+        const int r = n;
+        const int v = v0 + rank * RS + 8 * g;
+        if (r >= aR || v >= aV) continue;
+        float lg[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int i = 8 * g + e;
+            float x = 0.0f;
+            for (int src = 0; src < CK; ++src) x += recv[(src * RS + i) * N + split_pos(i, n, N)];
+            lg[e] = x;
+        }
+        if (a.bias) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (v + e < aV) lg[e] += a.bias[v + e];
+        }
+        // ids this row may choose: below the structural tail, or a tail id
+        // whose mask bit is set (the boundary token alone with eos_allowed)
+        int tail0 = aV;
+        uint32_t tm = 0u;
+        if (a.tail) {
+            tail0 = aV - a.n_tail;
+            tm = a.tail[r];
+        } else if (a.eos && !a.eos[r]) {
+            tail0 = aV - 1;
+        }
+        uint32_t allow = 0xFFu;
+        if (v + 8 > tail0) {
+            allow = 0u;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int id = v + e;
+                const bool ok = id < aV && (id < tail0 || ((tm >> (id - tail0)) & 1u));
+                allow |= ok ? 1u << e : 0u;
+            }
+        }
+        unsigned long long best = 0ull;
+        if constexpr (kGumbel) {
+            // skip the logarithms of entries whose uniform cannot beat the
+            // batch row's current best (exact for the entries kept)
+            float lmax = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if ((allow >> e) & 1u) lmax = fmaxf(lmax, lg[e]);
+            const unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(colbest + n);
+            float thr = 0.0f;
+            if (cur) thr = expf(-expf(-(unpack_value(cur) - lmax / a.temperature - kGumbelSlack)));
+            const Philox4x64 ph(static_cast<uint64_t>(v >> 3), 0, a.pos, 0, a.seed[r], a.step[r]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (!((allow >> e) & 1u)) continue;
+                const float u = bits_to_uniform(ph.half(e));
+                if (!(u > thr)) continue;
+                const unsigned long long k = pack_argmax(lg[e] / a.temperature + gumbel_from_uniform(u), v + e);
+                best = k > best ? k : best;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (!((allow >> e) & 1u)) continue;
+                const unsigned long long k = pack_argmax(lg[e], v + e);
+                best = k > best ? k : best;
+            }
+        }
+        if (best) atomicMax(colbest + n, best);
+    }
+    __syncthreads();
+    for (int n = threadIdx.x; n < N; n += blockDim.x) {
+        const unsigned long long k = colbest[n];
+        if (n < aR && k) atomicMax(a.ws.keys + n, k);
+    }
+    finish_selection(a.ws, a.R, a.ids, a.best, flag, gridDim.x, a.ids_host, a.count_host, a.V - 1);
+}
+
 // ------------------------------------------------------------- host side
 
 struct TcPlan {
@@ -821,6 +1064,77 @@ TcPlan plan_tc(int R, int H, int V) {
     return p;
 }
 
+// The split build, if it takes this shape: batches of up to 64 rows whose
+// vocab tiles all run as co-resident clusters (one wave) with every k-slice
+// in shared memory at once.  Cluster widths tried in order of measured speed.
+struct SplitPlan {
+    int N, CK, RS, ncl, alloc_cols;
+    uint32_t smem;
+};
+
+int max_active_clusters(const void *kernel, int ck, uint32_t smem) {
+    struct Entry {
+        const void *kernel;
+        int device, ck;
+        uint32_t smem;
+        int n;
+    };
+    static std::mutex mu;
+    static Entry cache[32];
+    static int used = 0;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (cache[i].kernel == kernel && cache[i].device == dev && cache[i].ck == ck && cache[i].smem == smem)
+            return cache[i].n;
+    if (!ensure_dynamic_smem(kernel, static_cast<int>(smem))) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ck), 1, 1);
+    cfg.blockDim = dim3(kSplitThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = static_cast<unsigned>(ck);
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    if (used < 32) cache[used++] = {kernel, dev, ck, smem, n};
+    return n;
+}
+
+bool plan_split(int R, int H, int V, bool gumbel, SplitPlan *p) {
+    if (R > kSplitMaxN || H % kTileK != 0) return false;
+    p->N = (R + 15) / 16 * 16;
+    p->alloc_cols = 32;
+    while (p->alloc_cols < p->N) p->alloc_cols <<= 1;
+    p->ncl = (V + kTileM - 1) / kTileM;
+    const void *kernel = gumbel ? reinterpret_cast<const void *>(head_split_kernel<true>)
+                                : reinterpret_cast<const void *>(head_split_kernel<false>);
+    for (int ck : {4, 8, 2}) {
+        if (H % (kTileK * ck) != 0) continue;
+        const int kch = H / kTileK / ck;
+        const int RS = kTileM / ck;
+        const uint32_t smem = split_layout(p->N, kch, ck, RS).total;
+        if (smem > 227u * 1024u) continue;
+        if (p->ncl > max_active_clusters(kernel, ck, smem)) continue;
+        p->CK = ck;
+        p->RS = RS;
+        p->smem = smem;
+        return true;
+    }
+    return false;
+}
+
 }  // namespace
 }  // namespace tts
 
@@ -835,6 +1149,8 @@ struct HeadLaunchState {
     HeadArgs a;
     CUtensorMap mw, mh;
     TcPlan p;
+    SplitPlan sp;
+    bool split;  // the split build (narrow batches) instead of head_tc_kernel
     int dtype;
     int simt_grid;
     const void *h, *W;
@@ -902,6 +1218,14 @@ int prepare_head_ex(const void *d_h, const void *d_W, int32_t dtype, int32_t R, 
     }
     if (H % kTileK != 0) return TTS_ERR_UNSUPPORTED;
     if (!aligned16(d_h) || !aligned16(d_W)) return TTS_ERR_INVALID;
+    st->split = !expand && !d_logits_out && plan_split(R, H, V, mode == TTS_GUMBEL, &st->sp);
+    if (st->split) {
+        if (!cached_tma_2d_bf16(&st->mw, d_W, static_cast<uint64_t>(V), static_cast<uint64_t>(H), kTileM, kTileK) ||
+            !cached_tma_2d_bf16(&st->mh, d_h, static_cast<uint64_t>(R), static_cast<uint64_t>(H),
+                                static_cast<uint32_t>(st->sp.N), kTileK))
+            return TTS_ERR_CUDA;
+        return TTS_OK;
+    }
     st->p = plan_tc(R, H, V);
     if (!cached_tma_2d_bf16(&st->mw, d_W, static_cast<uint64_t>(V), static_cast<uint64_t>(H), kTileM, kTileK) ||
         !cached_tma_2d_bf16(&st->mh, d_h, static_cast<uint64_t>(R), static_cast<uint64_t>(H),
@@ -929,6 +1253,22 @@ int launch_head(const HeadLaunch &L, LaunchOpts o) {
         cfg.numAttrs = na;
         e = cudaLaunchKernelEx(&cfg, head_simt_f32_kernel, static_cast<const float *>(st->h),
                                static_cast<const float *>(st->W), st->a);
+    } else if (st->split) {
+        const SplitPlan &p = st->sp;
+        const auto kernel = st->a.mode == TTS_GUMBEL ? head_split_kernel<true> : head_split_kernel<false>;
+        if (!ensure_dynamic_smem(reinterpret_cast<const void *>(kernel), static_cast<int>(p.smem)))
+            return TTS_ERR_CUDA;
+        cfg.gridDim = dim3(static_cast<unsigned>(p.ncl * p.CK), 1, 1);
+        cfg.blockDim = dim3(kSplitThreads, 1, 1);
+        cfg.dynamicSmemBytes = p.smem;
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = static_cast<unsigned>(p.CK);
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+        cfg.attrs = attr;
+        cfg.numAttrs = na;
+        e = cudaLaunchKernelEx(&cfg, kernel, st->mw, st->mh, st->a, p.N, p.CK, p.RS, p.alloc_cols);
     } else {
         const TcPlan &p = st->p;
         const bool features = st->a.mode == kModeExpand || st->a.mode == kModeLinear;

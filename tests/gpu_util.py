@@ -45,6 +45,13 @@ def attn_errors(gpu: np.ndarray, ref: np.ndarray):
     return bad, float(err.max()) if err.size else 0.0, rel
 
 
+def rel_where_binding(gpu: np.ndarray, ref: np.ndarray) -> float:
+    """Max relative error over the elements where the relative bound is the
+    larger one (|ref| >= ATOL / RTOL); 0 if there are none."""
+    big = np.abs(ref) >= ATOL / RTOL
+    return float((np.abs(gpu - ref)[big] / np.abs(ref[big])).max()) if big.any() else 0.0
+
+
 def compare_ids(gpu_ids, ref, near=NEAR_TIE):
     """Mismatched rows that are not near-ties, and the near-tie count."""
     gap = ref["best"].astype(np.float64) - ref["second"].astype(np.float64)

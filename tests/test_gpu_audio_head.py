@@ -97,6 +97,22 @@ def test_audio_head_matches_oracle(orc, bd, case):
             assert (int(inp["tail_allowed"][r]) >> j) & 1
 
 
+@pytest.mark.parametrize("case", [c for c in CASES if c[0] <= 64],
+                         ids=[f"R{c[0]}-F{c[2]}-V{c[3]}-{c[5]}" for c in CASES if c[0] <= 64])
+def test_audio_head_ids_without_logits(orc, bd, case):
+    """The same heads without the logits written out: narrow batches then
+    select in the split build (bias, tail masks and Gumbel noise included)."""
+    R, H, F, V, n_tail, mode, T = case
+    inp = wl.audio_head_inputs(R, H, F, V, n_tail, seed=3000 + CASES.index(case))
+    z_ref, _ = orc.audio_expand(inp["h"], inp["W1"], inp["b1"])
+    z, ids, best, _ = _run(bd, inp, R, F, V, n_tail, mode, T, logits=False)
+    # the second layer selects over the GPU's own z (exact inputs)
+    ref = orc.head_select_masked(z, inp["W2"], inp["b2"], mode, T, inp["seed"], inp["step"], n_tail,
+                                 inp["tail_allowed"])
+    hard, ties = compare_ids(ids, ref)
+    assert not hard, f"rows {hard[:10]} (near-ties {ties})"
+
+
 def test_audio_head_tail_mask_decides(orc, bd):
     """Structural ids made dominant by their bias win exactly where their bit
     is set: the highest allowed tail id, else the codebook's argmax."""

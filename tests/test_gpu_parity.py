@@ -13,7 +13,8 @@ import pytest
 import torch
 
 import workloads as wl
-from gpu_util import ATOL, NEAR_TIE, Uploaded, as_f64, attn_errors, compare_ids, dev, host
+from gpu_util import (ATOL, NEAR_TIE, RTOL, Uploaded, as_f64, attn_errors, compare_ids, dev, host,
+                      rel_where_binding)
 
 pytestmark = pytest.mark.gpu
 
@@ -51,12 +52,19 @@ def oracle_step_attn(orc, inp):
     return kp, vp, out
 
 
-def check_attn(gpu_out, ref, dtype, label):
+def check_attn(gpu_out, ref, dtype, label, parity=None):
     g = as_f64(host(gpu_out), dtype)
     assert np.isfinite(g).all(), f"{label}: non-finite attention output"
     bad, mx_abs, mx_rel = attn_errors(g, ref)
-    print(f"[{label}] attention max-abs {mx_abs:.3e} max-rel {mx_rel:.3e}")
+    if parity is not None:
+        parity(f"attention {label}", max_abs=mx_abs, max_rel=mx_rel, elements=int(g.size))
     assert bad == 0, f"{label}: {bad} elements outside tolerance (max-abs {mx_abs})"
+    # The absolute bound holds on every element (so reading the tolerance as
+    # "absolute or relative" admits nothing more), and the relative bound
+    # holds wherever it is the larger of the two.
+    assert mx_abs <= ATOL, f"{label}: max-abs {mx_abs} above {ATOL}"
+    rb = rel_where_binding(g, ref)
+    assert rb <= RTOL, f"{label}: relative error {rb} above {RTOL} where |o| >= {ATOL / RTOL}"
     if dtype == "f32":
         assert mx_abs < 1e-4, f"{label}: fp32 attention error {mx_abs}"
 
@@ -64,7 +72,7 @@ def check_attn(gpu_out, ref, dtype, label):
 # ------------------------------------------------------- full-size workloads
 
 @pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
-def test_append_and_attention(orc, wid):
+def test_append_and_attention(orc, parity, wid):
     inp = wl.make_inputs(wid, with_head=False, with_verify=False)
     w = inp["workload"]
     u = Uploaded(inp)
@@ -74,21 +82,15 @@ def test_append_and_attention(orc, wid):
     kp, vp, ref = oracle_step_attn(orc, inp)
     assert np.array_equal(host(u.k_pool).view(np.uint8), kp.view(np.uint8)), "K pool after append"
     assert np.array_equal(host(u.v_pool).view(np.uint8), vp.view(np.uint8)), "V pool after append"
-    check_attn(out, ref, w.dtype, w.name)
+    check_attn(out, ref, w.dtype, w.name, parity)
     assert int(err.item()) == 0
     # the ticket counters at the end of the workspace are back to zero
     ctr_bytes = -(-(w.B * w.Hkv * 4) // 256) * 256
     assert int(ws[ws.numel() - ctr_bytes:].count_nonzero()) == 0
 
 
-def _head_rows(w, limit):
-    if w.R <= limit:
-        return np.arange(w.R)
-    return np.linspace(0, w.R - 1, limit).round().astype(np.int64)
-
-
 @pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
-def test_head_select(orc, wid):
+def test_head_select(orc, parity, wid):
     inp = wl.make_inputs(wid, with_verify=False)
     w = inp["workload"]
     u = Uploaded(inp)
@@ -102,12 +104,12 @@ def test_head_select(orc, wid):
                                     step=u.step, best=best, logits_out=logits)
         torch.cuda.synchronize()
         assert int(ws.count_nonzero()) == 0, "head workspace not left zeroed"
-    rows = _head_rows(w, 48)
+    rows = np.arange(w.R)  # every row
     ref = orc.head_select(np.ascontiguousarray(inp["h"][rows]), inp["W"], w.mode, w.T,
                           inp["seed"][rows], inp["step"][rows], want_logits=w.logits_out)
     got = host(ids)[rows]
     hard, ties = compare_ids(got, ref)
-    print(f"[{w.name}] head rows checked {len(rows)}, near-ties {ties}, hard mismatches {len(hard)}")
+    parity(f"head {w.name}", rows=len(rows), near_ties=ties, hard=len(hard))
     assert not hard, f"ids differ outside near-ties at rows {hard[:10]}"
     fin = ref["best"] - ref["second"] >= NEAR_TIE
     assert np.allclose(host(best)[rows][fin], ref["best"][fin], rtol=1e-4, atol=1e-3)
@@ -117,7 +119,7 @@ def test_head_select(orc, wid):
             f"logits max err {np.abs(gl - ref['logits']).max()}"
 
 
-def test_spec_verify(orc):
+def test_spec_verify(orc, parity):
     inp = wl.make_inputs(5, with_head=False)
     w = inp["workload"]
     u = Uploaded(inp)
@@ -132,8 +134,8 @@ def test_spec_verify(orc):
                               inp["vseed"], inp["vstep"], bonus=bonus)
         tie = (ref["gap_accept"] < NEAR_TIE) | (ref["gap_resid"] < NEAR_TIE)
         bad = (host(n_acc) != ref["n_accepted"]) | (host(nxt) != ref["next_token"])
-        print(f"[verify bonus={bonus}] accepted mean {ref['n_accepted'].mean():.2f}, "
-              f"near-ties {int(tie.sum())}, mismatches {int(bad.sum())}")
+        parity(f"verify {w.name} bonus={int(bonus)}", streams=w.B, near_ties=int(tie.sum()),
+               hard=int((bad & ~tie).sum()), accepted_mean=float(ref["n_accepted"].mean()))
         assert not (bad & ~tie).any(), f"verify differs at streams {np.nonzero(bad & ~tie)[0][:10]}"
         assert int(err.item()) == 0
 
@@ -188,7 +190,7 @@ def test_spec_verify_bad_token():
 
 
 @pytest.mark.parametrize("wid", [3, 5])
-def test_full_step_chain(orc, wid):
+def test_full_step_chain(orc, parity, wid):
     """Append -> attention -> head on one stream, as the benchmark runs it."""
     inp = wl.make_inputs(wid, with_verify=False)
     w = inp["workload"]
@@ -201,11 +203,11 @@ def test_full_step_chain(orc, wid):
     torch.cuda.synchronize()
     _, _, attn = oracle_step_attn(orc, inp)
     h = wl.f32_to_bf16(attn.reshape(w.R, w.Hq * w.D).astype(np.float32))
-    rows = _head_rows(w, 64)
+    rows = np.arange(w.R)  # every row
     ref = orc.head_select(np.ascontiguousarray(h[rows]), inp["W"], w.mode, w.T, inp["seed"][rows],
                           inp["step"][rows])
     hard, ties = compare_ids(host(ids)[rows], ref)
-    print(f"[{w.name} chain] near-ties {ties}, hard mismatches {len(hard)}")
+    parity(f"step chain {w.name}", rows=len(rows), near_ties=ties, hard=len(hard))
     assert not hard
     assert int(step.err.item()) == 0
 
@@ -229,7 +231,7 @@ SMALL = [
 
 
 @pytest.mark.parametrize("case", SMALL, ids=[f"s{i}" for i in range(len(SMALL))])
-def test_small_shapes(orc, case):
+def test_small_shapes(orc, parity, case):
     base, B, Hq, Hkv, q_len, causal, ctx, permute = case
     w = wl.custom(base, B=B, Hq=Hq, Hkv=Hkv, q_len=q_len, causal=causal, ctx_lo=1,
                   ctx_hi=max(ctx), permute_table=permute)
@@ -239,7 +241,7 @@ def test_small_shapes(orc, case):
     cache = gpu_append(u, err)
     out, _ = gpu_attn(u, cache, err=err)
     _, _, ref = oracle_step_attn(orc, inp)
-    check_attn(out, ref, w.dtype, f"small {case}")
+    check_attn(out, ref, w.dtype, f"small {case}", parity)
     assert int(err.item()) == 0
 
 
@@ -377,6 +379,46 @@ def test_head_shapes(orc, R, H, V, mode):
     assert int(ws.count_nonzero()) == 0
 
 
+# Shapes of the split build (at most 64 rows, no logits written, vocab tiles
+# all in one wave): one to 64 rows, hidden widths 256 to 4096 (4- and 8-CTA
+# cluster splits), ragged and exact vocab tiles, fewer entries than one
+# selection group, a single entry.
+SPLIT_SHAPES = [(1, 256, 300), (16, 2048, 4097), (17, 512, 1000), (33, 1024, 2049), (64, 2048, 4097),
+                (64, 2048, 129), (48, 4096, 513), (5, 256, 7), (3, 256, 1), (64, 256, 4224)]
+
+
+@pytest.mark.parametrize("R,H,V", SPLIT_SHAPES)
+@pytest.mark.parametrize("mode", ["argmax", "gumbel"])
+def test_head_split_shapes(orc, parity, R, H, V, mode):
+    rng = np.random.default_rng(R * 11 + V + H)
+    h = wl.f32_to_bf16(rng.standard_normal((R, H), dtype=np.float32))
+    W = wl.f32_to_bf16((0.5 / math.sqrt(H)) * rng.standard_normal((V, H), dtype=np.float32))
+    seed = np.arange(R, dtype=np.uint64) + 501
+    step = np.full(R, 9, dtype=np.uint64)
+    eos = (np.arange(R) % 4 != 1).astype(np.uint8)
+    ids = torch.empty(R, dtype=torch.int32, device="cuda")
+    best = torch.empty(R, dtype=torch.float32, device="cuda")
+    ws = torch.zeros(bd.tts_head_workspace_size(R, V), dtype=torch.uint8, device="cuda")
+    m = bd.TTS_GUMBEL if mode == "gumbel" else bd.TTS_ARGMAX
+    ref = orc.head_select(h, W, mode, 0.9, seed, step, eos_allowed=eos)
+    for rep in range(2):  # the workspace as the first call left it
+        ids.fill_(-9)
+        bd.tts_codebook_head_select(dev(h), dev(W), ids, ws, mode=m, temperature=0.9, seed=dev(seed),
+                                    step=dev(step), eos_allowed=dev(eos), best=best)
+        torch.cuda.synchronize()
+        gids = host(ids)
+        none = ref["ids"] < 0
+        assert np.array_equal(gids[none], ref["ids"][none])
+        hard, ties = compare_ids(np.where(none, 0, gids), {k: np.where(none, 0, v) if k == "ids" else
+                                                           np.where(none, 1.0, v) if k == "best" else
+                                                           np.where(none, 0.0, v) for k, v in ref.items()})
+        assert not hard, f"rows {hard[:10]}"
+        fin = ~none & (ref["best"] - ref["second"] >= NEAR_TIE)
+        assert np.allclose(host(best)[fin], ref["best"][fin], rtol=1e-4, atol=1e-3)
+        assert int(ws.count_nonzero()) == 0
+    parity(f"split head R{R} H{H} V{V} {mode}", near_ties=ties, hard=len(hard))
+
+
 def test_head_boundary_token_mask(orc):
     R, H, V = 8, 64, 513
     h = wl.f32_to_bf16(np.ones((R, H), dtype=np.float32))
@@ -392,8 +434,10 @@ def test_head_boundary_token_mask(orc):
     assert list(host(ids)) == [V - 1, 100] * 4
 
 
-def test_graphed_step_matches_direct_step():
-    """The captured serving step (host copies in, step, ids out) gives the same ids."""
+def test_graphed_step_matches_direct_step(orc, parity):
+    """The captured serving step (host copies in, step, ids out) gives the same
+    ids as the direct step, and both match the oracle: its attention on the
+    same inputs, its head on the step's own attention output."""
     inp = wl.make_inputs(wl.custom(3, B=24), with_verify=False)
     w = inp["workload"]
     u = Uploaded(inp)
@@ -405,6 +449,14 @@ def test_graphed_step_matches_direct_step():
     for _ in range(3):
         g.ids_host.fill_(-7)           # a replay that did not finish would leave this
         assert torch.equal(g().clone(), direct.cpu())
+    # the captured step against the oracle directly
+    _, _, ref_attn = oracle_step_attn(orc, inp)
+    check_attn(step.out, ref_attn, w.dtype, "captured step custom-b24", parity)
+    h = host(step.out).reshape(w.R, -1)
+    ref = orc.head_select(h, inp["W"])
+    hard, ties = compare_ids(g.ids_host.numpy().copy(), ref)
+    parity("captured step custom-b24 head", rows=w.R, near_ties=ties, hard=len(hard))
+    assert not hard, f"captured step ids differ from the oracle at rows {hard}"
     # new inputs written into the pinned host views reach the step
     q2 = torch.randn(u.q.shape, device="cuda").to(u.q.dtype)
     direct2 = step(u.table, u.ctx_before, u.ctx_lens, q2, u.k_new, u.v_new).clone()
