@@ -219,8 +219,10 @@ class ClockSampler:
 
 # ------------------------------------------------------------- CPU oracle
 
-def oracle_stream_steps(orc, inp, streams, kp, vp):
-    """The oracle's decode step for a list of streams (append, attention, head row)."""
+def oracle_stream_steps(orc, inp, streams, kp, vp, keep=None):
+    """The oracle's decode step for a list of streams (append, attention, head
+    row).  keep (a dict, optional) receives stream -> (attention output, head
+    result) of the streams run."""
     w = inp["workload"]
     for b in streams:
         sl = slice(b, b + 1)
@@ -230,25 +232,102 @@ def oracle_stream_steps(orc, inp, streams, kp, vp):
                               inp["scale"], w.causal)
         h = wl.f32_to_bf16(att.reshape(w.q_len, -1).astype(np.float32)) if w.dtype == "bf16" \
             else att.reshape(w.q_len, -1).astype(np.float32)
-        orc.head_select(h, inp["W"], w.mode, w.T, inp["seed"][b * w.q_len:(b + 1) * w.q_len],
-                        inp["step"][b * w.q_len:(b + 1) * w.q_len])
+        res = orc.head_select(h, inp["W"], w.mode, w.T, inp["seed"][b * w.q_len:(b + 1) * w.q_len],
+                              inp["step"][b * w.q_len:(b + 1) * w.q_len])
+        if keep is not None:
+            keep[b] = (att, res)
 
 
-def cpu_baseline(inp, seconds: float) -> dict:
-    """The oracle, single-threaded, over whole streams of the step (cycling
-    through the batch) until about `seconds` of CPU time are spent."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def oracle_throughput(orc, inp, seconds: float, threads: int, keep=None) -> tuple[float, int]:
+    """Stream-steps per second of the oracle over about `seconds` of wall time:
+    `threads` Python threads (the oracle is C behind ctypes, which releases
+    the interpreter lock) each cycling over its own share of the streams
+    (thread t takes streams t, t + threads, ...), all writing one copy of the
+    pool (every stream appends to its own slots).  Returns (stream-steps/s,
+    stream-steps run)."""
+    import threading
+    w = inp["workload"]
+    kp, vp = inp["k_pool"].copy(), inp["v_pool"].copy()
+    counts = [0] * threads
+    stop = time.perf_counter() + seconds
+
+    def work(t):
+        mine = list(range(t, w.B, threads)) or [t % w.B]
+        i = 0
+        while counts[t] == 0 or time.perf_counter() < stop:
+            b = mine[i % len(mine)]
+            oracle_stream_steps(orc, inp, [b], kp, vp, keep if (keep is not None and i < len(mine)) else None)
+            counts[t] += 1
+            i += 1
+
+    t0 = time.perf_counter()
+    if threads == 1:
+        work(0)
+    else:
+        pool = [threading.Thread(target=work, args=(t,)) for t in range(threads)]
+        for th in pool:
+            th.start()
+        for th in pool:
+            th.join()
+    dt = time.perf_counter() - t0
+    return sum(counts) * w.q_len / dt, sum(counts)
+
+
+def parity_against(inp, keep, gpu_out, gpu_ids) -> dict:
+    """The GPU step's attention output and ids against the oracle's, for the
+    streams the CPU baseline ran (attention: max-abs / max-rel and elements
+    outside max(2e-2, 1e-2 |o|); ids: near-ties, where the oracle's top two
+    keys are closer than 1e-3, and mismatches outside them)."""
+    w = inp["workload"]
+    if not keep:
+        return {}
+    mx_abs = mx_rel = 0.0
+    bad = elements = ties = hard = 0
+    for b, (att, res) in keep.items():
+        g = gpu_out[b].astype(np.float64)
+        err = np.abs(g - att)
+        bad += int((~(err <= np.maximum(2e-2, 1e-2 * np.abs(att)))).sum())
+        elements += att.size
+        mx_abs = max(mx_abs, float(err.max()))
+        big = np.abs(att) >= 2e-2
+        if big.any():
+            mx_rel = max(mx_rel, float((err[big] / np.abs(att[big])).max()))
+        gid = gpu_ids[b * w.q_len:(b + 1) * w.q_len]
+        tie = (res["best"].astype(np.float64) - res["second"].astype(np.float64)) < 1e-3
+        ties += int(tie.sum())
+        hard += int(((gid != res["ids"]) & ~tie).sum())
+    return {"streams": len(keep), "attention_max_abs": mx_abs, "attention_max_rel": mx_rel,
+            "attention_outside_tolerance": bad, "attention_elements": elements, "id_rows": len(keep) * w.q_len,
+            "id_near_ties": ties, "id_mismatches_outside_near_ties": hard,
+            "note": "the step's GPU outputs against the oracle for the streams the CPU baseline ran"}
+
+
+def cpu_baseline(inp, seconds: float, gpu_out=None, gpu_ids=None) -> tuple[dict, dict]:
+    """The oracle over whole stream-steps (append, attention, head row) of this
+    workload: single-threaded for half of `seconds`, then one thread per host
+    core (os.sched_getaffinity) for the other half.  Returns (cpu_baseline,
+    parity of the GPU outputs for the streams run single-threaded)."""
     import oracle
     orc = oracle.default()
     w = inp["workload"]
-    kp, vp = inp["k_pool"].copy(), inp["v_pool"].copy()
-    done, t0 = 0, time.perf_counter()
-    while done == 0 or time.perf_counter() - t0 < seconds:
-        oracle_stream_steps(orc, inp, [done % w.B], kp, vp)
-        done += 1
-    dt = time.perf_counter() - t0
-    return {"value": done * w.q_len / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{done} stream-steps (append, attention, head row) cycling over the "
-                      f"{w.B} streams of one step, single-threaded C oracle, {dt:.1f} s"}
+    keep = {} if gpu_out is not None else None
+    v1, n1 = oracle_throughput(orc, inp, seconds / 2, 1, keep)
+    cores = host_cores()
+    vn, nn = oracle_throughput(orc, inp, seconds / 2, cores)
+    base = {"value": vn, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "single_thread_value": v1,
+            "sample": f"stream-steps (append, attention, head row) cycling over the {w.B} streams of one step: "
+                      f"{nn} on {cores} threads (one per host core in the affinity mask) and {n1} single-threaded, "
+                      f"about {seconds / 2:.0f} s each; C oracle"}
+    par = parity_against(inp, keep, gpu_out, gpu_ids) if keep is not None else {}
+    return base, par
 
 
 # ------------------------------------------------------------- reference arm
@@ -257,17 +336,20 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
+    import threading
     import oracle
     orc = oracle.default()
     w = wl.WORKLOADS[args.workload]
     inp = wl.make_inputs(w)
     kp, vp = inp["k_pool"].copy(), inp["v_pool"].copy()
+    cores = host_cores()
     # One unit = one stream's step; a step of this arm is a bounded sample of
-    # units sized so that warm-up + timed steps take about two minutes.
+    # units (spread over one thread per host core) sized so that warm-up +
+    # timed steps take about two minutes.
     t0 = time.perf_counter()
     oracle_stream_steps(orc, inp, [0], kp, vp)
     unit_s = max(time.perf_counter() - t0, 1e-4)
-    per_step = max(1, min(w.B, int(120.0 / (args.steps + args.warmup) / unit_s)))
+    per_step = max(1, min(w.B, int(cores * 120.0 / (args.steps + args.warmup) / unit_s)))
     order = np.random.default_rng(0).permutation(w.B)
     pos = 0
 
@@ -275,7 +357,13 @@ def run_reference(args):
         nonlocal pos
         streams = [int(order[(pos + i) % w.B]) for i in range(per_step)]
         pos += per_step
-        oracle_stream_steps(orc, inp, streams, kp, vp)
+        n = min(cores, len(streams))
+        parts = [streams[t::n] for t in range(n)]
+        ths = [threading.Thread(target=oracle_stream_steps, args=(orc, inp, part, kp, vp)) for part in parts]
+        for th in ths:
+            th.start()
+        for th in ths:
+            th.join()
 
     for _ in range(args.warmup):
         one_step()
@@ -291,8 +379,9 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": workload_config(w, 1),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{per_step} of {w.B} streams per step, single-threaded C oracle"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{per_step} of {w.B} streams per step, split over {min(cores, per_step)} threads "
+                                   f"(one per host core in the affinity mask), C oracle"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -662,6 +751,52 @@ def run_native(args):
     t_att_w = [e[1].elapsed_time(e[2]) for e in kev[K2:]]
     t_head_w = [e[2].elapsed_time(e[3]) for e in kev[K2:]]
 
+    # ---- per-kernel durations with the launch latency hidden, as inside the
+    # fused step: each kernel launched back to back as a programmatic
+    # dependent of the one before (tts_set_launch_flags), over inputs larger
+    # than L2 so that no launch finds its bytes cached: attention alternates
+    # two copies of the cache, tables and queries; the head rotates 16 copies
+    # of W.  One pair of events around each run; mean per launch.
+    gpu_out = step.out.detach().cpu()
+    gpu_ids = step.ids.detach().cpu().numpy()
+    cache2 = bd.KVCache(cache.k_pool.clone(), cache.v_pool.clone())
+    d2 = {k: d[k].clone() for k in ("block_table", "ctx_lens", "q")}
+    attn_sets = [(cache, d["block_table"], d["ctx_lens"], d["q"], step.attn_ws),
+                 (cache2, d2["block_table"], d2["ctx_lens"], d2["q"], torch.zeros_like(step.attn_ws))]
+    out2 = torch.empty_like(step.out)
+    W_copies = [W] + [W.clone() for _ in range(15)]
+    n_chain = min(K, 400)
+
+    def chained(fn):
+        for i in range(4):
+            fn(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        prev = bd.tts_set_launch_flags(bd._lib.LAUNCH_PROGRAMMATIC)
+        try:
+            e0.record(stream)
+            for i in range(n_chain):
+                fn(i)
+            e1.record(stream)
+            torch.cuda.synchronize()
+        finally:
+            bd.tts_set_launch_flags(prev)
+        return e0.elapsed_time(e1) * 1e3 / n_chain
+
+    def attn_i(i):
+        c, tbl, lens, q, ws = attn_sets[i & 1]
+        bd.tts_decode_attn(c, tbl, lens, w.ctx_hi, q, step.out if i & 1 == 0 else out2, ws, step.scale, w.causal,
+                           err=step.err)
+
+    def head_i(i):
+        bd.tts_codebook_head_select(step.out.view(step.R, -1), W_copies[i % len(W_copies)], step.ids, step.head_ws,
+                                    mode=mode, temperature=w.T, seed=seed, step=stp)
+
+    att_chain_us = chained(attn_i)
+    head_chain_us = chained(head_i)
+    del cache2, d2, out2, W_copies, attn_sets
+    torch.cuda.empty_cache()
+
     # ---- end to end through the public API with host buffers: the library's
     # captured step copies the step's inputs in from pinned host memory, runs
     # the step and writes the ids back; wall clock, synchronised every step.
@@ -721,10 +856,10 @@ def run_native(args):
     head_us = 1e3 * statistics.fmean(t_head)
     app_us = 1e3 * statistics.fmean(t_app)
     ab = attn_bytes(inp)
-    achieved = ab / (att_us * 1e-6) / 1e9
+    achieved = ab / (att_chain_us * 1e-6) / 1e9
     hb = head_bytes(w)
-    head_gbs = hb / (head_us * 1e-6) / 1e9
-    head_tflops = 2.0 * w.R * w.H * w.V / (head_us * 1e-6) / 1e12
+    head_gbs = hb / (head_chain_us * 1e-6) / 1e9
+    head_tflops = 2.0 * w.R * w.H * w.V / (head_chain_us * 1e-6) / 1e12
     traffic = recorded_traffic("decode_attn", w.name)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
@@ -733,10 +868,19 @@ def run_native(args):
         "config": workload_config(w, world),
         "roofline": {"bound": "hbm", "kernel": "decode_attn", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": traffic, "algorithmic_bytes": ab,
+                     "traffic": traffic, "algorithmic_bytes": ab, "launch_us": att_chain_us,
+                     "timing": f"{n_chain} launches back to back as programmatic dependents, alternating two "
+                               "copies of the inputs (2 x 205 MB > L2); CUDA events around the run",
+                     "achieved_isolated": ab / (att_us * 1e-6) / 1e9,
+                     "frac_isolated": ab / (att_us * 1e-6) / 1e9 / peaks["hbm_gbs"],
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback"},
         "kernels": {
+            "decode_attn_us_chained": att_chain_us, "head_select_us_chained": head_chain_us,
+            "chained_note": "per-kernel time with the launch latency hidden (launches back to back as "
+                            "programmatic dependents, inputs rotated beyond L2); the *_us keys below are "
+                            "single launches after an L2 flush, each bracketed by events (launch latency "
+                            "included)",
             "kv_append_us": app_us, "decode_attn_us": att_us, "head_select_us": head_us,
             "step_us": 1e3 * ms,
             "sum_of_kernels_us": app_us + att_us + head_us,
@@ -748,7 +892,8 @@ def run_native(args):
                                  "launches": K3},
             "head_roofline": {"bound": "hbm", "achieved": head_gbs, "peak": peaks["hbm_gbs"],
                               "unit": "GB/s", "frac": head_gbs / peaks["hbm_gbs"],
-                              "algorithmic_bytes": hb, "tflops": head_tflops},
+                              "algorithmic_bytes": hb, "tflops": head_tflops, "launch_us": head_chain_us,
+                              "frac_isolated": hb / (head_us * 1e-6) / 1e9 / peaks["hbm_gbs"]},
         },
         "gpu_launches": 3 * K,
         "step_note": "each timed step is one tts_decode_step call (append, attention, head; "
@@ -768,7 +913,9 @@ def run_native(args):
                                         "synchronises every step"},
     }
     if world == 1:
-        line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
+        g_out = wl.to_f32(gpu_out.view(torch.int16).numpy().view(np.uint16), w.dtype) if w.dtype == "bf16" \
+            else gpu_out.numpy()
+        line["cpu_baseline"], line["parity"] = cpu_baseline(inp, args.cpu_seconds, g_out.astype(np.float64), gpu_ids)
         ids = [x.strip() for x in args.sweep.split(",") if x.strip()]
         if ids:
             del step, graphed, cache, W, d

@@ -16,6 +16,8 @@ TTS_F32, TTS_BF16, TTS_FP8_E4M3 = 0, 1, 2
 TTS_ARGMAX, TTS_GUMBEL = 0, 1
 TTS_VERIFY_BONUS = 1
 ERRBIT_BLOCK_ID, ERRBIT_CTX_LEN, ERRBIT_TOKEN, ERRBIT_TIMEOUT = 1, 2, 4, 8
+LAUNCH_PROGRAMMATIC = 1
+TEST_STALL_NONE, TEST_STALL_ATTN_RING, TEST_STALL_PREDICTOR_GRID = 0, 1, 2
 
 HEADER = Path(__file__).resolve().parents[1] / "include" / "tts_decode.h"
 
@@ -91,6 +93,8 @@ _SIGNATURES = {
     "tts_code_predictor_graph_create": (ctypes.c_int, [ctypes.POINTER(CodePredictorDesc), ctypes.POINTER(_vp)]),
     "tts_code_predictor_graph_launch": (ctypes.c_int, [_vp, _vp]),
     "tts_code_predictor_graph_destroy": (None, [_vp]),
+    "tts_set_launch_flags": (_i32, [_i32]),
+    "tts_test_set_stall": (ctypes.c_int, [_i32, ctypes.c_int64]),
     "tts_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "tts_version": (ctypes.c_int, []),
 }

@@ -492,3 +492,16 @@ def tts_status_string(code: int) -> str:
 
 def tts_version() -> int:
     return int(lib().tts_version())
+
+
+def tts_set_launch_flags(flags: int) -> int:
+    """Launch options of this thread's later single-kernel calls
+    (_lib.LAUNCH_PROGRAMMATIC: programmatic dependents of the previous kernel
+    in the stream).  Returns the previous flags."""
+    return int(lib().tts_set_launch_flags(int(flags)))
+
+
+def tts_test_set_stall(what: int, wait_limit_cycles: int = 2_000_000_000) -> None:
+    """Test support: make a bounded on-device wait of the next kernels this
+    thread launches run out (_lib.TEST_STALL_*), with the given wait limit."""
+    check("tts_test_set_stall", lib().tts_test_set_stall(int(what), int(wait_limit_cycles)))

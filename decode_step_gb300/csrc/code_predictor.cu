@@ -86,6 +86,8 @@ struct PersistArgs {
     unsigned long long *keys;  // [2][R]
     unsigned int *bar;         // [0] barrier count, [1] abort
     int32_t *err;
+    long long wait_limit;      // SM clock cycles per bounded wait
+    int stall;                 // test support: the first grid barrier waits for one CTA too many
 };
 
 __device__ __forceinline__ void p_ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
@@ -115,7 +117,7 @@ __device__ bool p_grid_sync(const PersistArgs &a, unsigned int k) {
         ok = 1;
         __threadfence();
         atomicAdd(a.bar, 1u);
-        const unsigned int target = k * gridDim.x;
+        const unsigned int target = k * gridDim.x + (a.stall && k == 1 ? 1u : 0u);
         const long long t0 = clock64();
         for (uint32_t n = 0;; ++n) {
             if (ld_acquire_u32(a.bar) >= target) break;
@@ -123,7 +125,7 @@ __device__ bool p_grid_sync(const PersistArgs &a, unsigned int k) {
                 ok = 0;
                 break;
             }
-            if ((n & 63u) == 0 && clock64() - t0 > kWaitLimitCycles) {
+            if ((n & 63u) == 0 && clock64() - t0 > a.wait_limit) {
                 flag_error(a.err, TTS_ERRBIT_TIMEOUT);
                 atomicExch(a.bar + 1, 1u);
                 ok = 0;
@@ -196,7 +198,7 @@ __global__ void __launch_bounds__(kPThreads, 1) predictor_persistent_kernel(cons
             else
                 bulk_load_nohint(wsm + (j - nx) * stride, wrow0 + static_cast<size_t>(j - nx) * a.H, rowb, bar);
         }
-        const bool ok = mbar_wait(bar, phase & 1u);
+        const bool ok = mbar_wait(bar, phase & 1u, a.wait_limit);
         ++phase;
         if (!ok && lane == 0) flag_error(a.err, TTS_ERRBIT_TIMEOUT);
         return ok;
@@ -486,6 +488,8 @@ int plan_predictor(const tts_code_predictor_desc *d, PredictorPlan *P) {
                          reinterpret_cast<__nv_bfloat16 *>(ws + L.kpool), reinterpret_cast<__nv_bfloat16 *>(ws + L.vpool),
                          reinterpret_cast<__nv_bfloat16 *>(ws + L.o), reinterpret_cast<unsigned long long *>(ws + L.keys),
                          reinterpret_cast<unsigned int *>(ws + L.bar), d->d_err};
+        pa.wait_limit = thread_opts().wait_limit;
+        pa.stall = thread_opts().stall == TTS_TEST_STALL_PREDICTOR_GRID;
         P->grid = static_cast<unsigned>(grid);
         P->ctrl = ws + L.keys;
         P->ctrl_bytes = L.bar + 8 - L.keys;

@@ -77,6 +77,8 @@ struct AttnArgs {
     int nr_slot;        // query rows per partial slot (group * q_len padded)
     int stages;         // ring depth per warp (tensor-core kernel)
     int32_t *err;
+    long long wait_limit;  // SM clock cycles per bounded wait
+    int stall;             // test support: first ring stage expects 16 bytes that never come
 };
 
 __device__ __forceinline__ int warp_of_tile(long long t, long long T, long long W) {
@@ -165,14 +167,16 @@ __device__ __forceinline__ long long active_workers(int workers, long long Ttot,
 }
 
 // The last contributor of a split segment merges the contributors' partials
-// (log-sum-exp combine).  Loads are issued together rather than one
-// contributor at a time: contributors are spread over the lanes (32 at a
-// time) for the row maxima and sums, and each lane reads its D/32-dim slice
-// of the outputs for 8 contributors per batch.
+// (log-sum-exp combine).  Output unit = 4 dims of one query row; a lane takes
+// units u, u + 32, ... and, per batch of 8 contributors, issues every load
+// it needs (each contributor's row maximum, row sum and 4 output dims) before
+// using any, so a merge costs one dependent round trip per batch instead of
+// one per row for the maxima and another for the outputs.  Batches fold in
+// with a running maximum (one batch for up to 8 contributors).
 template <typename T, int D>
 __device__ void merge_split_segment(const AttnArgs &a, int b, int g, int n_rows, int w_first,
                                     int w_last, bool first_shifted, int lane) {
-    constexpr int DPL = D / 32;  // dims per lane: 4 (bf16, D = 128) or 2 (fp32, D = 64)
+    constexpr int UPR = D / 4;  // float4 units per row
     const int NRS = a.nr_slot;
     const size_t SF = static_cast<size_t>(NRS) * D + 2 * NRS;
     const size_t ML = static_cast<size_t>(NRS) * D;  // offset of the maxima; sums follow
@@ -180,75 +184,73 @@ __device__ void merge_split_segment(const AttnArgs &a, int b, int g, int n_rows,
     auto slot = [&](int i) -> const float * {
         return a.part + (static_cast<size_t>(w_first + i) * 2 + (i == 0 && first_shifted)) * SF;
     };
-    for (int r = 0; r < n_rows; ++r) {
-        // row maximum over all contributors
-        float M = kNegBig;
-        for (int c0 = 0; c0 < nc; c0 += 32) {
-            const int ci = c0 + lane;
-            M = fmaxf(M, ci < nc ? __ldcg(slot(ci) + ML + r) : kNegBig);
-        }
+    for (int u = lane; u < n_rows * UPR; u += 32) {
+        const int r = u / UPR, c = u - r * UPR;
+        float M = kNegBig, L = 0.0f;
+        float4 O = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int c0 = 0; c0 < nc; c0 += 8) {
+            float mi[8], li[8];
+            float4 oi[8];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-        float Ls = 0.0f, O[DPL];
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) O[e] = 0.0f;
-        for (int c0 = 0; c0 < nc; c0 += 32) {
-            const int ci = c0 + lane;
-            float f_i = 0.0f;
-            if (ci < nc) {
-                const float *pp = slot(ci) + ML;
-                f_i = exp2f(__ldcg(pp + r) - M);
-                Ls = fmaf(__ldcg(pp + NRS + r), f_i, Ls);
-            }
-            const int cn = min(32, nc - c0);
-            for (int k0 = 0; k0 < cn; k0 += 8) {
-                float v[8][DPL];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    if (k0 + k < cn) {
-                        const float *src = slot(c0 + k0 + k) + static_cast<size_t>(r) * D + lane * DPL;
-                        if constexpr (DPL == 4) {
-                            const float4 x = __ldcg(reinterpret_cast<const float4 *>(src));
-                            v[k][0] = x.x; v[k][1] = x.y; v[k][2] = x.z; v[k][3] = x.w;
-                        } else {
-                            const float2 x = __ldcg(reinterpret_cast<const float2 *>(src));
-                            v[k][0] = x.x; v[k][1] = x.y;
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < DPL; ++e) v[k][e] = 0.0f;
-                    }
-                }
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float f = __shfl_sync(kFull, f_i, (k0 + k) & 31);
-#pragma unroll
-                    for (int e = 0; e < DPL; ++e) O[e] = fmaf(v[k][e], f, O[e]);
+            for (int k = 0; k < 8; ++k) {
+                if (c0 + k < nc) {
+                    const float *p = slot(c0 + k);
+                    mi[k] = __ldcg(p + ML + r);
+                    li[k] = __ldcg(p + ML + NRS + r);
+                    oi[k] = __ldcg(reinterpret_cast<const float4 *>(p + static_cast<size_t>(r) * D) + c);
+                } else {
+                    mi[k] = kNegBig;
+                    li[k] = 0.0f;
+                    oi[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                 }
             }
+            float Mn = M;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) Mn = fmaxf(Mn, mi[k]);
+            const float sc = exp2f(M - Mn);
+            L *= sc;
+            O.x *= sc; O.y *= sc; O.z *= sc; O.w *= sc;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float f = exp2f(mi[k] - Mn);
+                L = fmaf(li[k], f, L);
+                O.x = fmaf(oi[k].x, f, O.x);
+                O.y = fmaf(oi[k].y, f, O.y);
+                O.z = fmaf(oi[k].z, f, O.z);
+                O.w = fmaf(oi[k].w, f, O.w);
+            }
+            M = Mn;
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(kFull, Ls, o);
-        const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
-        T *dst = out_row<T, D>(a, b, g, r) + lane * DPL;
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) store_elem(dst + e, O[e] * inv);
+        const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+        T *dst = out_row<T, D>(a, b, g, r) + 4 * c;
+        store_elem(dst + 0, O.x * inv);
+        store_elem(dst + 1, O.y * inv);
+        store_elem(dst + 2, O.z * inv);
+        store_elem(dst + 3, O.w * inv);
     }
 }
 
 // Publishes a warp's partial of a split segment (already written to `part`
-// by the caller) and, if it is the last one, merges.  Whole warp calls.
+// by the caller's lanes) and, if it is the last one, merges.  Whole warp
+// calls.  The warp barrier orders every lane's partial stores before lane
+// 0's ticket, whose release makes them visible with it (and whose acquire,
+// for the last contributor, makes the others' partials visible before the
+// warp barrier that precedes the merge's loads).
 template <typename T, int D>
 __device__ void finish_split_segment(const AttnArgs &a, int seg, int s0, int s1, int n_rows,
                                      long long Ttot, long long Wtot, int lane) {
-    __threadfence();
     __syncwarp();
     const int w_first = warp_of_tile(s0, Ttot, Wtot);
     const int w_last = warp_of_tile(s1 - 1, Ttot, Wtot);
     int last = 0;
-    if (lane == 0) last = atomicAdd(a.counters + seg, 1) == w_last - w_first;
-    if (!__shfl_sync(kFull, last, 0)) return;
-    __threadfence();
+    if (lane == 0) {
+        int old;
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(a.counters + seg) : "memory");
+        last = old == w_last - w_first;
+    }
+    last = __shfl_sync(kFull, last, 0);
+    if (!last) return;
+    __syncwarp();
     merge_split_segment<T, D>(a, seg / a.Hkv, seg % a.Hkv, n_rows, w_first, w_last,
                               range_start(w_first, Ttot, Wtot) != s0, lane);
     if (lane == 0) a.counters[seg] = 0;
@@ -420,7 +422,7 @@ decode_attn_simt_kernel(const AttnArgs a) {
         }
         const int st = i % kStages;
         if (!timed_out) {
-            const bool ok = mbar_wait(bar0 + 8 * st, (i / kStages) & 1);
+            const bool ok = mbar_wait(bar0 + 8 * st, (i / kStages) & 1, a.wait_limit);
             if (__any_sync(kFull, !ok)) {
                 timed_out = true;
                 if (lane == 0) flag_error(a.err, TTS_ERRBIT_TIMEOUT);
@@ -539,7 +541,7 @@ decode_attn_simt_kernel(const AttnArgs a) {
     flush();
     if (timed_out) {
         const int issued = min(n, waited + kStages);
-        for (int i = waited; i < issued; ++i) mbar_wait(bar0 + 8 * (i % kStages), (i / kStages) & 1);
+        for (int i = waited; i < issued; ++i) mbar_wait(bar0 + 8 * (i % kStages), (i / kStages) & 1, a.wait_limit);
     }
 }
 
@@ -739,7 +741,8 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
             const uint32_t bar = bar0 + 8 * st;
             const uint32_t dst = stage0 + st * S.stage_bytes;
             const bool need_q = j == 0 || blk == 0;
-            const uint32_t bytes = (id >= 0 ? kStageKV : 0) + (need_q ? a.q_len * qbytes_per_pos : 0);
+            uint32_t bytes = (id >= 0 ? kStageKV : 0) + (need_q ? a.q_len * qbytes_per_pos : 0);
+            if (a.stall && j == 0) bytes += 16;  // test support: this stage never completes
             if (bytes == 0) {
                 mbar_arrive(bar);
             } else {
@@ -835,7 +838,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
         }
         const int st = i % n_stages;
         if (!timed_out) {
-            const bool ok = mbar_wait(bar0 + 8 * st, (i / n_stages) & 1);
+            const bool ok = mbar_wait(bar0 + 8 * st, (i / n_stages) & 1, a.wait_limit);
             if (__any_sync(kFull, !ok)) {
                 timed_out = true;
                 if (lane == 0) flag_error(a.err, TTS_ERRBIT_TIMEOUT);
@@ -1060,7 +1063,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
     flush();
     if (timed_out) {
         const int issued = min(n, waited + n_stages);
-        for (int i = waited; i < issued; ++i) mbar_wait(bar0 + 8 * (i % n_stages), (i / n_stages) & 1);
+        for (int i = waited; i < issued; ++i) mbar_wait(bar0 + 8 * (i % n_stages), (i / n_stages) & 1, a.wait_limit);
     }
 }
 
@@ -1254,6 +1257,8 @@ int prepare_attn(const tts_kv_cache *cache, const int32_t *d_block_table, int32_
 
     if (a.stages < 1) return TTS_ERR_UNSUPPORTED;
     a.err = d_err;
+    a.wait_limit = thread_opts().wait_limit;
+    a.stall = thread_opts().stall == TTS_TEST_STALL_ATTN_RING && cache->dtype != TTS_F32;
     st->dtype = cache->dtype;
     st->rows = pl.rows;
     st->ctas = pl.ctas;
@@ -1285,7 +1290,7 @@ extern "C" int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block
     const int st = tts::prepare_attn(cache, d_block_table, max_blocks_per_seq, d_ctx_lens, max_ctx_len, B,
                                      q_len, num_q_heads, scale, causal, d_q, d_out, d_ws, ws_bytes, d_err, &L);
     if (st != TTS_OK) return st;
-    return tts::launch_attn(L, {static_cast<cudaStream_t>(stream), false});
+    return tts::launch_attn(L, {static_cast<cudaStream_t>(stream), tts::thread_pdl()});
 }
 
 // ---------------------------------------------------------------------------

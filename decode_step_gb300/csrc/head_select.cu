@@ -789,56 +789,67 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
 // tile; CTA rank r reduces the hidden range [r H / CK, (r + 1) H / CK).  Every
 // W and h k-slice of the CTA is requested at once (no ring reuse: at 64 x
 // 2048 x 4097 the CTA's 128 KB of W and 64 KB of h are all in flight), so the
-// load time is the HBM burst itself.  The epilogue is kept short because it
-// runs once per CTA with its instructions fetched cold: each accumulator row
-// (one vocab row, read from TMEM by the thread of that lane) is stored
-// straight into the shared memory of the CTA that owns the row, one cluster
-// barrier publishes all partials, and every CTA then sums its 32 rows over
-// the CK sources, selects per batch row, and folds its best keys into the
-// global keys; the last CTA converts keys to ids.
+// load time is the HBM burst itself.  The epilogue runs once per CTA with its
+// instructions fetched cold, so it is short and has one wait: each
+// accumulator row (one vocab row, read from TMEM by the thread of that lane)
+// goes by asynchronous remote stores into the shared memory of the CTA that
+// owns the row, completing on that CTA's mbarrier; each CTA waits for its own
+// 32 rows from all CK sources, sums them, selects per batch row and folds its
+// best keys into the global keys; the last CTA converts keys to ids.
 constexpr int kSplitThreads = 256;
 constexpr int kSplitMaxN = 64;
 
 struct SplitLayout {
     uint32_t hslot;    // bytes of one h k-slice (N rows x 128 B)
     uint32_t h;        // offset of the h slices (after the W slices)
-    uint32_t recv;     // offset of recv[CK][RS][N] fp32 partials
-    uint32_t bars;     // kch full barriers, then the accumulator barrier
+    uint32_t recv;     // offset of recv[CK][RS][NR] fp32 partials
+    uint32_t bars;     // kch full barriers, the accumulator barrier, the receive barrier
     uint32_t colbest;  // [N] packed keys
-    uint32_t misc;     // TMEM address, flag, failure word
+    uint32_t misc;     // TMEM address, flag
     uint32_t total;
 };
+
+// Floats per partial row in recv: N rounded up to a power of two, so the
+// chunk swizzle below is a mask.
+__host__ __device__ constexpr int split_row(int N) { return N <= 16 ? 16 : (N <= 32 ? 32 : 64); }
 
 __host__ __device__ inline SplitLayout split_layout(int N, int kch, int CK, int RS) {
     SplitLayout L;
     L.hslot = static_cast<uint32_t>(N) * 128u;
     L.h = static_cast<uint32_t>(kch) * kATileBytes;
     L.recv = L.h + static_cast<uint32_t>(kch) * L.hslot;
-    L.bars = L.recv + static_cast<uint32_t>(CK * RS * N) * 4u;
-    L.colbest = L.bars + 8u * (kch + 1);
+    L.bars = L.recv + static_cast<uint32_t>(CK * RS * split_row(N)) * 4u;
+    L.colbest = L.bars + 8u * (kch + 2);
     L.misc = L.colbest + 8u * N;
     L.total = L.misc + 16u + 1024u;  // + slack to align the dynamic base to 1024
     return L;
 }
 
-// Position of float n within a partial row i of recv: the row's 16-byte
-// chunks are rotated by i, so the 32 lanes of a warp storing 32 different rows
-// spread over all banks, and a warp reading one row's consecutive columns
-// still touches distinct banks.
-__device__ __forceinline__ int split_pos(int i, int n, int N) {
-    const int nc = N >> 2;
-    return ((((n >> 2) + i) % nc) << 2) | (n & 3);
+// Position of float n within partial row i of recv (rows of NR floats, NR a
+// power of two): the row's 16-byte chunks are permuted by the low bits of i,
+// so lanes storing the same chunk of different rows spread over the banks,
+// and a warp reading one row's consecutive columns still touches distinct
+// banks.
+template <int NR>
+__device__ __forceinline__ int split_pos(int i, int n) {
+    return ((((n >> 2) ^ i) & ((NR >> 2) - 1)) << 2) | (n & 3);
 }
 
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+// Asynchronous remote store of 16 bytes, completing on the destination
+// CTA's mbarrier.
+__device__ __forceinline__ void st_async_v4(uint32_t dst_cluster, float x, float y, float z, float w,
+                                            uint32_t bar_cluster) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     dst_cluster),
+                 "f"(x), "f"(y), "f"(z), "f"(w), "r"(bar_cluster)
                  : "memory");
 }
 
-template <bool kGumbel>
+template <bool kGumbel, int N>
 __global__ void __launch_bounds__(kSplitThreads, 1)
 head_split_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_h,
-                  const HeadArgs a, int N, int CK, int RS, int alloc_cols) {
+                  const HeadArgs a, int CK, int RS, int alloc_cols) {
+    constexpr int NR = split_row(N);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -847,6 +858,7 @@ head_split_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     const SplitLayout Lo = split_layout(N, kch, CK, RS);
     const uint32_t bar_full = base + Lo.bars;        // [kch]
     const uint32_t bar_acc = bar_full + 8u * kch;
+    const uint32_t bar_recv = bar_acc + 8u;
     unsigned long long *colbest = reinterpret_cast<unsigned long long *>(smem + Lo.colbest);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lo.misc);
     int *flag = reinterpret_cast<int *>(smem + Lo.misc + 4);
@@ -857,21 +869,25 @@ head_split_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     const int kbase = rank * kch * kTileK;
 
     if (threadIdx.x == 0) {
-        for (int c = 0; c <= kch; ++c) mbar_init(bar_full + 8u * c, 1);
+        for (int c = 0; c < kch + 2; ++c) mbar_init(bar_full + 8u * c, 1);
         fence_mbar_init();
-    }
-    pdl_allow_dependents();
-    for (int i = threadIdx.x; i < N; i += blockDim.x) colbest[i] = 0ull;
-    __syncthreads();
-    if (warp == 0 && lane == 0) {
-        // Every slice at once: W (independent of the previous kernel) first,
-        // h (its output) after the programmatic-launch wait.
+        // every source's rows of this CTA: CK x RS rows of N floats
+        mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>(CK * RS * N) * 4u);
+        // Every W slice at once (W never depends on the previous kernel); h,
+        // the previous kernel's output, after the programmatic-launch wait.
         prefetch_tensormap(&map_w);
-        prefetch_tensormap(&map_h);
         for (int c = 0; c < kch; ++c) {
             mbar_arrive_expect_tx(bar_full + 8u * c, kATileBytes + Lo.hslot);
             tma_load_2d(base + c * kATileBytes, &map_w, kbase + c * kTileK, v0, bar_full + 8u * c);
         }
+    }
+    // Peers store into this CTA's shared memory only after the matching wait
+    // below, i.e. after this CTA's barriers are initialised.
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    pdl_allow_dependents();
+    for (int i = threadIdx.x; i < N; i += blockDim.x) colbest[i] = 0ull;
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&map_h);
         pdl_wait_prerequisites();
         for (int c = 0; c < kch; ++c)
             tma_load_2d(base + Lo.h + c * Lo.hslot, &map_h, kbase + c * kTileK, 0, bar_full + 8u * c);
@@ -886,11 +902,12 @@ head_split_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 1 && lane == 0) {
         // D[128 x N] += W_slice[128 x 64] . h_slice[N x 64]^T per slice, in arrival order
-        const uint32_t idesc = mma_idesc(kTileM, N);
+        constexpr uint32_t idesc = mma_idesc(kTileM, N);
         bool ok = true;
         for (int c = 0; c < kch; ++c) {
             if (ok && !mbar_wait(bar_full + 8u * c, 0)) {
@@ -909,39 +926,35 @@ head_split_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     __syncwarp();
 
     // ---- accumulator row (vocab row 32 w + lane of the tile) -> its owner
+    bool sent = false;
     if (warp < 4) {
         const int vl = warp * 32 + lane;
-        const int owner = vl / RS;
-        bool ready = true;
-        if (!mbar_wait(bar_acc, 0)) {
-            flag_error(a.err, TTS_ERRBIT_TIMEOUT);
-            ready = false;
-        }
+        const int owner = vl / RS;  // < CK: RS = 128 / CK
+        const int i = vl - owner * RS;
+        const bool ready = mbar_wait(bar_acc, 0);
+        if (!ready) flag_error(a.err, TTS_ERRBIT_TIMEOUT);
         tc_fence_after();
         if (__all_sync(kFull, ready)) {
-            const int i = vl - owner * RS;
-            const uint32_t row = base + Lo.recv + static_cast<uint32_t>((rank * RS + i) * N) * 4u;
-            const uint32_t dst = map_cluster(row, static_cast<uint32_t>(owner < CK ? owner : 0));
+            const uint32_t row = base + Lo.recv + static_cast<uint32_t>((rank * RS + i) * NR) * 4u;
+            const uint32_t dst = map_cluster(row, static_cast<uint32_t>(owner));
+            const uint32_t dbar = map_cluster(bar_recv, static_cast<uint32_t>(owner));
+#pragma unroll
             for (int c0 = 0; c0 < N; c0 += 16) {
                 float v[16];
                 tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
-                if (owner < CK) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        st_cluster_v4(dst + 4u * split_pos(i, c0 + 4 * q, N), v[4 * q], v[4 * q + 1], v[4 * q + 2],
-                                      v[4 * q + 3]);
-                }
+                for (int q = 0; q < 4; ++q)
+                    st_async_v4(dst + 4u * split_pos<NR>(i, c0 + 4 * q), v[4 * q], v[4 * q + 1], v[4 * q + 2],
+                                v[4 * q + 3], dbar);
             }
+            sent = true;
         }
     }
     tc_fence_before();
-    // every partial row is in its owner's shared memory after this barrier
-    cluster_sync();
-    if (warp == 1) {
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(alloc_cols)
-                     : "memory");
-    }
+    // every partial row of this CTA's 32 rows has arrived (a failed peer
+    // leaves this wait to run out)
+    const bool got = mbar_wait(bar_recv, 0);
+    if (!got && threadIdx.x == 0) flag_error(a.err, TTS_ERRBIT_TIMEOUT);
 
     // ---- sum the CK partials of this CTA's rows and select per batch row.
     // Item = (8-row group, batch row); consecutive threads take consecutive
@@ -949,7 +962,7 @@ head_split_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     const float *recv = reinterpret_cast<const float *>(smem + Lo.recv);
     const int items = (RS / 8) * N;
     const int aR = a.R, aV = a.V;
-    for (int item = threadIdx.x; item < items; item += blockDim.x) {
+    for (int item = threadIdx.x; item < items && got; item += blockDim.x) {
         const int n = item % N, g = item / N;
         const int r = n;
         const int v = v0 + rank * RS + 8 * g;
@@ -958,8 +971,9 @@ head_split_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int i = 8 * g + e;
-            float x = 0.0f;
-            for (int src = 0; src < CK; ++src) x += recv[(src * RS + i) * N + split_pos(i, n, N)];
+            const float *src = recv + static_cast<size_t>(i) * NR + split_pos<NR>(i, n);
+            float x = src[0];
+            for (int s = 1; s < CK; ++s) x += src[static_cast<size_t>(s) * RS * NR];
             lg[e] = x;
         }
         if (a.bias) {
@@ -1018,10 +1032,16 @@ head_split_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
         if (best) atomicMax(colbest + n, best);
     }
     __syncthreads();
-    for (int n = threadIdx.x; n < N; n += blockDim.x) {
-        const unsigned long long k = colbest[n];
-        if (n < aR && k) atomicMax(a.ws.keys + n, k);
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(alloc_cols)
+                     : "memory");
     }
+    if (static_cast<int>(threadIdx.x) < N) {
+        const unsigned long long k = colbest[threadIdx.x];
+        if (static_cast<int>(threadIdx.x) < aR && k) atomicMax(a.ws.keys + threadIdx.x, k);
+    }
+    (void)sent;
     finish_selection(a.ws, a.R, a.ids, a.best, flag, gridDim.x, a.ids_host, a.count_host, a.V - 1);
 }
 
@@ -1112,14 +1132,24 @@ int max_active_clusters(const void *kernel, int ck, uint32_t smem) {
     return n;
 }
 
+// The instance for a padded batch width N (16, 32, 48 or 64).
+const void *split_kernel(bool gumbel, int N) {
+    using K = void (*)(CUtensorMap, CUtensorMap, HeadArgs, int, int, int);
+    static const K table[2][4] = {
+        {head_split_kernel<false, 16>, head_split_kernel<false, 32>, head_split_kernel<false, 48>,
+         head_split_kernel<false, 64>},
+        {head_split_kernel<true, 16>, head_split_kernel<true, 32>, head_split_kernel<true, 48>,
+         head_split_kernel<true, 64>}};
+    return reinterpret_cast<const void *>(table[gumbel ? 1 : 0][N / 16 - 1]);
+}
+
 bool plan_split(int R, int H, int V, bool gumbel, SplitPlan *p) {
     if (R > kSplitMaxN || H % kTileK != 0) return false;
     p->N = (R + 15) / 16 * 16;
     p->alloc_cols = 32;
     while (p->alloc_cols < p->N) p->alloc_cols <<= 1;
     p->ncl = (V + kTileM - 1) / kTileM;
-    const void *kernel = gumbel ? reinterpret_cast<const void *>(head_split_kernel<true>)
-                                : reinterpret_cast<const void *>(head_split_kernel<false>);
+    const void *kernel = split_kernel(gumbel, p->N);
     for (int ck : {4, 8, 2}) {
         if (H % (kTileK * ck) != 0) continue;
         const int kch = H / kTileK / ck;
@@ -1255,9 +1285,8 @@ int launch_head(const HeadLaunch &L, LaunchOpts o) {
                                static_cast<const float *>(st->W), st->a);
     } else if (st->split) {
         const SplitPlan &p = st->sp;
-        const auto kernel = st->a.mode == TTS_GUMBEL ? head_split_kernel<true> : head_split_kernel<false>;
-        if (!ensure_dynamic_smem(reinterpret_cast<const void *>(kernel), static_cast<int>(p.smem)))
-            return TTS_ERR_CUDA;
+        const void *kernel = split_kernel(st->a.mode == TTS_GUMBEL, p.N);
+        if (!ensure_dynamic_smem(kernel, static_cast<int>(p.smem))) return TTS_ERR_CUDA;
         cfg.gridDim = dim3(static_cast<unsigned>(p.ncl * p.CK), 1, 1);
         cfg.blockDim = dim3(kSplitThreads, 1, 1);
         cfg.dynamicSmemBytes = p.smem;
@@ -1268,7 +1297,10 @@ int launch_head(const HeadLaunch &L, LaunchOpts o) {
         ++na;
         cfg.attrs = attr;
         cfg.numAttrs = na;
-        e = cudaLaunchKernelEx(&cfg, kernel, st->mw, st->mh, st->a, p.N, p.CK, p.RS, p.alloc_cols);
+        void *args[] = {const_cast<CUtensorMap *>(&st->mw), const_cast<CUtensorMap *>(&st->mh),
+                        const_cast<HeadArgs *>(&st->a), const_cast<int *>(&p.CK), const_cast<int *>(&p.RS),
+                        const_cast<int *>(&p.alloc_cols)};
+        e = cudaLaunchKernelExC(&cfg, kernel, args);
     } else {
         const TcPlan &p = st->p;
         const bool features = st->a.mode == kModeExpand || st->a.mode == kModeLinear;
@@ -1309,7 +1341,7 @@ extern "C" int tts_codebook_head_select(const void *d_h, const void *d_W, int32_
     const int st = tts::prepare_head(d_h, d_W, dtype, R, H, V, mode, temperature, d_seed, d_step,
                                      d_eos_allowed, d_ids, d_best, d_logits_out, d_ws, ws_bytes, &L);
     if (st != TTS_OK) return st;
-    return tts::launch_head(L, {static_cast<cudaStream_t>(stream), false});
+    return tts::launch_head(L, {static_cast<cudaStream_t>(stream), tts::thread_pdl()});
 }
 
 // The two-layer audio head ("TontaubeV1", section 3): z = Mish(h W1^T + b1)

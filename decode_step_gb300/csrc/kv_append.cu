@@ -367,7 +367,7 @@ extern "C" int tts_kv_append(const tts_kv_cache *cache, const int32_t *d_block_t
     const int st = tts::prepare_append(cache, d_block_table, max_blocks_per_seq, d_ctx_before, B, q_len,
                                        d_k_new, d_v_new, d_err, &L);
     if (st != TTS_OK) return st;
-    return tts::launch_append(L, {static_cast<cudaStream_t>(stream), false});
+    return tts::launch_append(L, {static_cast<cudaStream_t>(stream), tts::thread_pdl()});
 }
 
 extern "C" int tts_kv_append_rope(const tts_kv_cache *cache, const int32_t *d_block_table,
@@ -379,5 +379,5 @@ extern "C" int tts_kv_append_rope(const tts_kv_cache *cache, const int32_t *d_bl
     const int st = tts::prepare_append_rope(cache, d_block_table, max_blocks_per_seq, d_ctx_before, B, q_len,
                                             num_q_heads, rope_base, d_q, d_k_new, d_v_new, d_err, &L);
     if (st != TTS_OK) return st;
-    return tts::launch_append(L, {static_cast<cudaStream_t>(stream), false});
+    return tts::launch_append(L, {static_cast<cudaStream_t>(stream), tts::thread_pdl()});
 }

@@ -92,14 +92,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete; false after about a
-// second without completion (the caller records TTS_ERRBIT_TIMEOUT).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Waits for the phase with the given parity to complete; false after `limit`
+// SM clock cycles (default about a second) without completion (the caller
+// records TTS_ERRBIT_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit = kWaitLimitCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 63u) == 0 && clock64() - t0 > kWaitLimitCycles) return false;
+        if ((n & 63u) == 0 && clock64() - t0 > limit) return false;
     }
 }
 

@@ -102,6 +102,29 @@ extern "C" const char *tts_status_string(int status) {
 extern "C" int tts_version(void) { return 100; }
 
 namespace tts {
+ThreadOpts &thread_opts() {
+    static thread_local ThreadOpts opts;
+    return opts;
+}
+}  // namespace tts
+
+extern "C" int32_t tts_set_launch_flags(int32_t flags) {
+    tts::ThreadOpts &o = tts::thread_opts();
+    const int32_t prev = o.launch_flags;
+    o.launch_flags = flags & TTS_LAUNCH_PROGRAMMATIC;
+    return prev;
+}
+
+extern "C" int tts_test_set_stall(int32_t what, int64_t wait_limit_cycles) {
+    if (what < TTS_TEST_STALL_NONE || what > TTS_TEST_STALL_PREDICTOR_GRID) return TTS_ERR_INVALID;
+    if (wait_limit_cycles < 1000 || wait_limit_cycles > 4000000000LL) return TTS_ERR_INVALID;
+    tts::ThreadOpts &o = tts::thread_opts();
+    o.stall = what;
+    o.wait_limit = wait_limit_cycles;
+    return TTS_OK;
+}
+
+namespace tts {
 
 int sm_count() {
     static std::atomic<int> cached[64];

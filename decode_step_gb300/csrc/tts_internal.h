@@ -13,6 +13,17 @@ namespace tts {
 // Number of SMs of the current device (cached per device ordinal).
 int sm_count();
 
+// Options of the calling thread (tts_set_launch_flags, tts_test_set_stall):
+// whether single-kernel calls launch as programmatic dependents, and the
+// test-only stall and wait limit handed to the kernels that support them.
+struct ThreadOpts {
+    int launch_flags = 0;
+    int stall = 0;                       // TTS_TEST_STALL_* (0: none)
+    long long wait_limit = 2000000000LL; // SM clock cycles per bounded wait
+};
+ThreadOpts &thread_opts();
+inline bool thread_pdl() { return (thread_opts().launch_flags & TTS_LAUNCH_PROGRAMMATIC) != 0; }
+
 // TMA descriptor of a 2-D tensor [rows][cols] (cols contiguous) of 1-byte
 // (uint8) or 2-byte (bf16) elements, read in boxes of box_rows x box_cols with
 // 128-byte swizzle (box_cols * elem_bytes <= 128); out-of-range box elements

@@ -538,6 +538,39 @@ int tts_code_predictor_graph_create(const tts_code_predictor_desc *desc, tts_cod
 int tts_code_predictor_graph_launch(tts_code_predictor_graph *graph, void *stream);
 void tts_code_predictor_graph_destroy(tts_code_predictor_graph *graph);
 
+/* ------------------------------------------------------ launch options */
+
+/* No counterpart on the pages: kernel-launch plumbing.  With
+ * TTS_LAUNCH_PROGRAMMATIC set, the single-kernel calls this thread makes
+ * afterwards (tts_kv_append, tts_kv_append_rope, tts_decode_attn,
+ * tts_codebook_head_select) launch their kernel as a
+ * programmatic dependent of the previous kernel in the stream: it may start
+ * while that kernel finishes (hiding the launch latency, as the kernels of
+ * tts_decode_step do) and waits for its completion before touching anything
+ * that kernel may write, except: tts_decode_attn reads d_ctx_lens and
+ * d_block_table, and tts_codebook_head_select reads d_W, before that wait,
+ * so the previous kernel must not write those.  The setting is per calling
+ * thread.  Returns the previous flags. */
+enum { TTS_LAUNCH_PROGRAMMATIC = 1 };
+int32_t tts_set_launch_flags(int32_t flags);
+
+/* Test support (no counterpart on the pages): makes a bounded on-device wait
+ * run out, to test the timeout path without faulting or hanging a GPU.  For
+ * the calls this thread makes afterwards, every wait of the kernels below
+ * gives up after wait_limit_cycles SM clock cycles (default 2e9, about one
+ * second) and, with
+ *   TTS_TEST_STALL_ATTN_RING: each warp of tts_decode_attn's bf16 / FP8
+ *     kernel expects 16 more bytes on its first ring stage than its copies
+ *     deliver, so its first wait runs out;
+ *   TTS_TEST_STALL_PREDICTOR_GRID: the persistent code-predictor kernel's
+ *     first grid barrier waits for one CTA more than the grid has.
+ * The kernel then ORs TTS_ERRBIT_TIMEOUT into *d_err, stops issuing work,
+ * waits (bounded) for the copies it issued, and returns; its outputs are
+ * undefined.  TTS_TEST_STALL_NONE restores normal operation.
+ * TTS_ERR_INVALID for an unknown mode or a limit outside [1e3, 4e9]. */
+enum { TTS_TEST_STALL_NONE = 0, TTS_TEST_STALL_ATTN_RING = 1, TTS_TEST_STALL_PREDICTOR_GRID = 2 };
+int tts_test_set_stall(int32_t what, int64_t wait_limit_cycles);
+
 /* ----------------------------------------------------------------- misc */
 
 /* Static description of a status code. */

@@ -241,3 +241,17 @@ def test_step_graph_set_rejects_bad_sizes(L):
     assert create([1, 64], offs=(64 * 1024,)) == -1    # starts past the buffers
     assert L.tts_step_graph_set_launch(None, 4, None, None) == -1
     L.tts_step_graph_set_destroy(None)
+
+
+def test_launch_flags_and_stall_arguments():
+    """The thread's launch flags round-trip; the test stall rejects unknown
+    modes and wait limits outside [1e3, 4e9] (host-side checks, no GPU)."""
+    from decode_step_gb300 import _lib
+    lib = _lib.lib()
+    prev = lib.tts_set_launch_flags(_lib.LAUNCH_PROGRAMMATIC)
+    assert lib.tts_set_launch_flags(prev) == _lib.LAUNCH_PROGRAMMATIC
+    assert lib.tts_set_launch_flags(0) == prev
+    assert lib.tts_test_set_stall(3, 10_000) == -1
+    assert lib.tts_test_set_stall(1, 10) == -1
+    assert lib.tts_test_set_stall(1, 5_000_000_000) == -1
+    assert lib.tts_test_set_stall(0, 2_000_000_000) == 0
