@@ -60,6 +60,9 @@ def parse_args(argv=None):
                          "'workloads' object (comma-separated ids, 'f' suffix: FP8 E4M3 KV cache; "
                          "empty: none)")
     ap.add_argument("--sweep-reps", type=int, default=30)
+    ap.add_argument("--chained", type=int, default=1,
+                    help="time the kernels back to back as programmatic dependents (needs a second copy of "
+                         "the cache and 15 more of W; 0 to skip, e.g. for profiling runs)")
     ap.add_argument("--code-predictor", type=int, default=1,
                     help="time the code predictor's frame loop (workloads.CODE_PREDICTOR; 0 to skip)")
     ap.add_argument("--audio-heads", default="acoustic-b64,semantic-cb0-b16",
@@ -759,12 +762,14 @@ def run_native(args):
     # of W.  One pair of events around each run; mean per launch.
     gpu_out = step.out.detach().cpu()
     gpu_ids = step.ids.detach().cpu().numpy()
-    cache2 = bd.KVCache(cache.k_pool.clone(), cache.v_pool.clone())
+    att_us_iso = 1e3 * statistics.fmean(t_att)
+    head_us_iso = 1e3 * statistics.fmean(t_head)
+    cache2 = bd.KVCache(cache.k_pool.clone(), cache.v_pool.clone()) if args.chained else None
     d2 = {k: d[k].clone() for k in ("block_table", "ctx_lens", "q")}
     attn_sets = [(cache, d["block_table"], d["ctx_lens"], d["q"], step.attn_ws),
                  (cache2, d2["block_table"], d2["ctx_lens"], d2["q"], torch.zeros_like(step.attn_ws))]
     out2 = torch.empty_like(step.out)
-    W_copies = [W] + [W.clone() for _ in range(15)]
+    W_copies = [W] + ([W.clone() for _ in range(15)] if args.chained else [])
     n_chain = min(K, 400)
 
     def chained(fn):
@@ -792,8 +797,11 @@ def run_native(args):
         bd.tts_codebook_head_select(step.out.view(step.R, -1), W_copies[i % len(W_copies)], step.ids, step.head_ws,
                                     mode=mode, temperature=w.T, seed=seed, step=stp)
 
-    att_chain_us = chained(attn_i)
-    head_chain_us = chained(head_i)
+    if args.chained:
+        att_chain_us = chained(attn_i)
+        head_chain_us = chained(head_i)
+    else:
+        att_chain_us, head_chain_us = att_us_iso, head_us_iso
     del cache2, d2, out2, W_copies, attn_sets
     torch.cuda.empty_cache()
 
@@ -869,8 +877,9 @@ def run_native(args):
         "roofline": {"bound": "hbm", "kernel": "decode_attn", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "traffic": traffic, "algorithmic_bytes": ab, "launch_us": att_chain_us,
-                     "timing": f"{n_chain} launches back to back as programmatic dependents, alternating two "
-                               "copies of the inputs (2 x 205 MB > L2); CUDA events around the run",
+                     "timing": (f"{n_chain} launches back to back as programmatic dependents, alternating two "
+                                "copies of the inputs (2 x cache > L2); CUDA events around the run")
+                     if args.chained else "single launches after an L2 flush (chained pass skipped)",
                      "achieved_isolated": ab / (att_us * 1e-6) / 1e9,
                      "frac_isolated": ab / (att_us * 1e-6) / 1e9 / peaks["hbm_gbs"],
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"

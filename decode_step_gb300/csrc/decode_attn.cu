@@ -81,11 +81,22 @@ struct AttnArgs {
     int stall;             // test support: first ring stage expects 16 bytes that never come
 };
 
-__device__ __forceinline__ int warp_of_tile(long long t, long long T, long long W) {
-    return static_cast<int>(((t + 1) * W - 1) / T);
+// The work partition: Wtot warps share the flat list of T tiles in order,
+// the first rem = T mod Wtot warps taking q + 1 tiles and the others q = T /
+// Wtot (32-bit arithmetic: the merges evaluate these at every split segment).
+struct Part {
+    int q, rem;
+};
+__device__ __forceinline__ Part make_part(long long T, long long W) {
+    Part p;
+    p.q = static_cast<int>(T / W);
+    p.rem = static_cast<int>(T - static_cast<long long>(p.q) * W);
+    return p;
 }
-__device__ __forceinline__ long long range_start(long long w, long long T, long long W) {
-    return w * T / W;
+__device__ __forceinline__ int range_start(const Part &p, int w) { return w * p.q + min(w, p.rem); }
+__device__ __forceinline__ int warp_of_tile(const Part &p, int t) {
+    const int big = p.rem * (p.q + 1);
+    return t < big ? t / (p.q + 1) : p.rem + (t - big) / p.q;
 }
 
 // Context lengths -> per-stream tile prefix (x Hkv, stream-major) in shared
@@ -168,65 +179,87 @@ __device__ __forceinline__ long long active_workers(int workers, long long Ttot,
 
 // The last contributor of a split segment merges the contributors' partials
 // (log-sum-exp combine).  Output unit = 4 dims of one query row; a lane takes
-// units u, u + 32, ... and, per batch of 8 contributors, issues every load
-// it needs (each contributor's row maximum, row sum and 4 output dims) before
-// using any, so a merge costs one dependent round trip per batch instead of
-// one per row for the maxima and another for the outputs.  Batches fold in
-// with a running maximum (one batch for up to 8 contributors).
+// two units (u and u + 32) per pass and, per batch of 4 contributors, issues
+// every load both need (each contributor's row maximum, row sum and 4 output
+// dims) before using any, so a merge of up to 4 contributors costs one
+// dependent round trip per 64 units (per 2 query rows at head_dim 128)
+// instead of one per row for the maxima and another for the outputs.
+// Batches fold in with a running maximum.
 template <typename T, int D>
 __device__ void merge_split_segment(const AttnArgs &a, int b, int g, int n_rows, int w_first,
                                     int w_last, bool first_shifted, int lane) {
     constexpr int UPR = D / 4;  // float4 units per row
+    constexpr int CB = 4;       // contributors per batch
     const int NRS = a.nr_slot;
     const size_t SF = static_cast<size_t>(NRS) * D + 2 * NRS;
     const size_t ML = static_cast<size_t>(NRS) * D;  // offset of the maxima; sums follow
     const int nc = w_last - w_first + 1;
+    const int units = n_rows * UPR;
     auto slot = [&](int i) -> const float * {
         return a.part + (static_cast<size_t>(w_first + i) * 2 + (i == 0 && first_shifted)) * SF;
     };
-    for (int u = lane; u < n_rows * UPR; u += 32) {
-        const int r = u / UPR, c = u - r * UPR;
-        float M = kNegBig, L = 0.0f;
-        float4 O = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        for (int c0 = 0; c0 < nc; c0 += 8) {
-            float mi[8], li[8];
-            float4 oi[8];
+    for (int u0 = lane; u0 < units; u0 += 64) {
+        int rr[2], cc[2];
+        bool has[2];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                if (c0 + k < nc) {
-                    const float *p = slot(c0 + k);
-                    mi[k] = __ldcg(p + ML + r);
-                    li[k] = __ldcg(p + ML + NRS + r);
-                    oi[k] = __ldcg(reinterpret_cast<const float4 *>(p + static_cast<size_t>(r) * D) + c);
-                } else {
-                    mi[k] = kNegBig;
-                    li[k] = 0.0f;
-                    oi[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int h = 0; h < 2; ++h) {
+            const int u = u0 + 32 * h;
+            has[h] = u < units;
+            rr[h] = has[h] ? u / UPR : 0;
+            cc[h] = has[h] ? u - rr[h] * UPR : 0;
+        }
+        float M[2] = {kNegBig, kNegBig}, L[2] = {0.0f, 0.0f};
+        float4 O[2] = {make_float4(0.0f, 0.0f, 0.0f, 0.0f), make_float4(0.0f, 0.0f, 0.0f, 0.0f)};
+        for (int c0 = 0; c0 < nc; c0 += CB) {
+            float mi[2][CB], li[2][CB];
+            float4 oi[2][CB];
+#pragma unroll
+            for (int k = 0; k < CB; ++k) {
+                const bool in = c0 + k < nc;
+                const float *pk = in ? slot(c0 + k) : nullptr;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (in && has[h]) {
+                        mi[h][k] = __ldcg(pk + ML + rr[h]);
+                        li[h][k] = __ldcg(pk + ML + NRS + rr[h]);
+                        oi[h][k] = __ldcg(reinterpret_cast<const float4 *>(pk + static_cast<size_t>(rr[h]) * D) + cc[h]);
+                    } else {
+                        mi[h][k] = kNegBig;
+                        li[h][k] = 0.0f;
+                        oi[h][k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    }
                 }
             }
-            float Mn = M;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) Mn = fmaxf(Mn, mi[k]);
-            const float sc = exp2f(M - Mn);
-            L *= sc;
-            O.x *= sc; O.y *= sc; O.z *= sc; O.w *= sc;
+            for (int h = 0; h < 2; ++h) {
+                float Mn = M[h];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float f = exp2f(mi[k] - Mn);
-                L = fmaf(li[k], f, L);
-                O.x = fmaf(oi[k].x, f, O.x);
-                O.y = fmaf(oi[k].y, f, O.y);
-                O.z = fmaf(oi[k].z, f, O.z);
-                O.w = fmaf(oi[k].w, f, O.w);
+                for (int k = 0; k < CB; ++k) Mn = fmaxf(Mn, mi[h][k]);
+                const float sc = exp2f(M[h] - Mn);
+                L[h] *= sc;
+                O[h].x *= sc; O[h].y *= sc; O[h].z *= sc; O[h].w *= sc;
+#pragma unroll
+                for (int k = 0; k < CB; ++k) {
+                    const float f = exp2f(mi[h][k] - Mn);
+                    L[h] = fmaf(li[h][k], f, L[h]);
+                    O[h].x = fmaf(oi[h][k].x, f, O[h].x);
+                    O[h].y = fmaf(oi[h][k].y, f, O[h].y);
+                    O[h].z = fmaf(oi[h][k].z, f, O[h].z);
+                    O[h].w = fmaf(oi[h][k].w, f, O[h].w);
+                }
+                M[h] = Mn;
             }
-            M = Mn;
         }
-        const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-        T *dst = out_row<T, D>(a, b, g, r) + 4 * c;
-        store_elem(dst + 0, O.x * inv);
-        store_elem(dst + 1, O.y * inv);
-        store_elem(dst + 2, O.z * inv);
-        store_elem(dst + 3, O.w * inv);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (!has[h]) continue;
+            const float inv = L[h] > 0.0f ? 1.0f / L[h] : 0.0f;
+            T *dst = out_row<T, D>(a, b, g, rr[h]) + 4 * cc[h];
+            store_elem(dst + 0, O[h].x * inv);
+            store_elem(dst + 1, O[h].y * inv);
+            store_elem(dst + 2, O[h].z * inv);
+            store_elem(dst + 3, O[h].w * inv);
+        }
     }
 }
 
@@ -237,11 +270,11 @@ __device__ void merge_split_segment(const AttnArgs &a, int b, int g, int n_rows,
 // for the last contributor, makes the others' partials visible before the
 // warp barrier that precedes the merge's loads).
 template <typename T, int D>
-__device__ void finish_split_segment(const AttnArgs &a, int seg, int s0, int s1, int n_rows,
-                                     long long Ttot, long long Wtot, int lane) {
+__device__ void finish_split_segment(const AttnArgs &a, int seg, int s0, int s1, int n_rows, const Part &pt,
+                                     int lane) {
     __syncwarp();
-    const int w_first = warp_of_tile(s0, Ttot, Wtot);
-    const int w_last = warp_of_tile(s1 - 1, Ttot, Wtot);
+    const int w_first = warp_of_tile(pt, s0);
+    const int w_last = warp_of_tile(pt, s1 - 1);
     int last = 0;
     if (lane == 0) {
         int old;
@@ -251,8 +284,8 @@ __device__ void finish_split_segment(const AttnArgs &a, int seg, int s0, int s1,
     last = __shfl_sync(kFull, last, 0);
     if (!last) return;
     __syncwarp();
-    merge_split_segment<T, D>(a, seg / a.Hkv, seg % a.Hkv, n_rows, w_first, w_last,
-                              range_start(w_first, Ttot, Wtot) != s0, lane);
+    merge_split_segment<T, D>(a, seg / a.Hkv, seg % a.Hkv, n_rows, w_first, w_last, range_start(pt, w_first) != s0,
+                              lane);
     if (lane == 0) a.counters[seg] = 0;
 }
 
@@ -290,8 +323,9 @@ decode_attn_simt_kernel(const AttnArgs a) {
     const long long Wtot = active_workers(a.workers, Ttot, static_cast<long long>(a.B) * a.Hkv);
     const int wid = blockIdx.x * kWarps + warp;
     if (Ttot == 0 || wid >= Wtot) return;
-    const int t0 = static_cast<int>(range_start(wid, Ttot, Wtot));
-    const int t1 = static_cast<int>(range_start(wid + 1, Ttot, Wtot));
+    const Part pt = make_part(Ttot, Wtot);
+    const int t0 = range_start(pt, wid);
+    const int t1 = range_start(pt, wid + 1);
     const int n = t1 - t0;
     if (n <= 0) return;
 
@@ -409,7 +443,7 @@ decode_attn_simt_kernel(const AttnArgs a) {
                 part[NR * D + NR + lane * HALF + k] = l_tot[k];
             }
         }
-        finish_split_segment<T, D>(a, seg_id, s0, s1, n_rows, Ttot, Wtot, lane);
+        finish_split_segment<T, D>(a, seg_id, s0, s1, n_rows, pt, lane);
     };
 
     bool timed_out = false;
@@ -596,11 +630,17 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Launch shape of the tensor-core kernel (measured best: 12 warps per SM with
-// two tiles in flight each; fewer warps with deeper rings were slower).
+// Launch shapes of the tensor-core kernel.  Up to 4 query rows per KV head
+// (single-token decode): 3 CTAs of 4 warps per SM, two tiles in flight per
+// warp (measured best; 2 CTAs with three tiles each were 2-4 % slower at
+// workloads 3 and 4).  8 rows and more (the 10 rows of a 5-token verify
+// block): 2 CTAs with three tiles in flight per warp, whose larger register
+// budget the wider query fragments and merges use (measured 7 % faster at
+// workload 5 than 3 CTAs with two).
 constexpr int kTcWarps = 4;
-constexpr int kTcMaxStages = 2;
-constexpr int kTcCtasPerSm = 3;
+constexpr int kTcWideRows = 8;
+__host__ __device__ constexpr int tc_ctas_per_sm(int rows) { return rows >= kTcWideRows ? 2 : 3; }
+__host__ __device__ constexpr int tc_max_stages(int ctas) { return ctas == 2 ? 3 : 2; }
 
 // One stage of a warp's ring: K and V of one (block, head) tile, each as two
 // 16-row x 64-column boxes (128-byte swizzle, 2 KB each), then the query rows
@@ -645,11 +685,12 @@ __host__ __device__ inline TcSmem tc_smem(int n_rows, int B, int stages, bool fp
     return s;
 }
 
-// Deepest ring (<= kTcMaxStages) that fits kTcCtasPerSm CTAs per SM; 0 if
-// not even one stage fits.
+// Deepest ring (up to the shape's maximum) that fits the shape's CTAs per
+// SM; 0 if not even one stage fits.
 __host__ inline int tc_stages(int n_rows, int B, bool fp8) {
-    const int budget = 227 * 1024 / kTcCtasPerSm - 1024;
-    for (int st = kTcMaxStages; st >= 1; --st)
+    const int ctas = tc_ctas_per_sm(n_rows);
+    const int budget = 227 * 1024 / ctas - 1024;
+    for (int st = tc_max_stages(ctas); st >= 1; --st)
         if (tc_smem(n_rows, B, st, fp8).total <= budget) return st;
     return 0;
 }
@@ -673,8 +714,8 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
     return r;
 }
 
-template <bool kFp8, int kRing>
-__global__ void __launch_bounds__(kTcWarps * 32, kTcCtasPerSm)
+template <bool kFp8, int kRing, int kCtas>
+__global__ void __launch_bounds__(kTcWarps * 32, kCtas)
 decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                       const AttnArgs a) {
     constexpr int D = 128;
@@ -699,8 +740,9 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
     const long long Wtot = active_workers(a.workers, Ttot, static_cast<long long>(a.B) * a.Hkv);
     const int wid = blockIdx.x * kTcWarps + warp;
     if (Ttot == 0 || wid >= Wtot) return;
-    const int t0 = static_cast<int>(range_start(wid, Ttot, Wtot));
-    const int t1 = static_cast<int>(range_start(wid + 1, Ttot, Wtot));
+    const Part pt = make_part(Ttot, Wtot);
+    const int t0 = range_start(pt, wid);
+    const int t1 = range_start(pt, wid + 1);
     const int n = t1 - t0;
     if (n <= 0) return;
 
@@ -825,7 +867,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
                 *reinterpret_cast<float2 *>(part + rB * D + nt * 8 + 2 * ft) = make_float2(o[nt][2], o[nt][3]);
             if (ft == 0) { part[NRS * D + rB] = mB; part[NRS * D + NRS + rB] = lb; }
         }
-        finish_split_segment<T, D>(a, seg_id, s0, s1, n_rows, Ttot, Wtot, lane);
+        finish_split_segment<T, D>(a, seg_id, s0, s1, n_rows, pt, lane);
     };
 
     bool timed_out = false;
@@ -1079,7 +1121,7 @@ int padded_rows(int rows) {
 }
 
 int ctas_per_sm(int dtype, int nr) {
-    if (dtype == TTS_BF16 || dtype == TTS_FP8_E4M3) return kTcCtasPerSm;
+    if (dtype == TTS_BF16 || dtype == TTS_FP8_E4M3) return tc_ctas_per_sm(nr);
     return nr <= 4 ? 3 : 1;
 }
 
@@ -1128,9 +1170,14 @@ int launch_simt(const AttnArgs &a, int nr, int ctas, LaunchOpts o) {
 
 template <bool kFp8>
 int launch_tc(const AttnArgs &a, const CUtensorMap &kmap, const CUtensorMap &vmap, int ctas, LaunchOpts o) {
-    static_assert(kTcMaxStages == 2, "ring depths instantiated: 1 and 2");
-    const size_t smem = tc_smem(a.group * a.q_len, a.B, a.stages, kFp8).total;
-    auto kern = a.stages == 2 ? decode_attn_tc_kernel<kFp8, 2> : decode_attn_tc_kernel<kFp8, 1>;
+    static_assert(tc_max_stages(3) == 2 && tc_max_stages(2) == 3, "instantiated: 3 CTAs x 1-2 stages, 2 x 1-3");
+    const int rows = a.group * a.q_len;
+    const size_t smem = tc_smem(rows, a.B, a.stages, kFp8).total;
+    const auto kern = tc_ctas_per_sm(rows) == 2
+                          ? (a.stages == 3   ? decode_attn_tc_kernel<kFp8, 3, 2>
+                             : a.stages == 2 ? decode_attn_tc_kernel<kFp8, 2, 2>
+                                             : decode_attn_tc_kernel<kFp8, 1, 2>)
+                          : (a.stages == 2 ? decode_attn_tc_kernel<kFp8, 2, 3> : decode_attn_tc_kernel<kFp8, 1, 3>);
     if (!ensure_dynamic_smem(reinterpret_cast<const void *>(kern), static_cast<int>(smem)))
         return TTS_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -1308,7 +1355,7 @@ extern "C" int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block
 namespace tts {
 namespace {
 
-constexpr size_t kStaticScratchBytes = size_t(24) << 20;  // 24 MiB
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_attn_scratch[kStaticScratchBytes];

@@ -65,13 +65,15 @@ HeadWs head_ws(void *ws, int R) {
 __device__ void finish_selection(const HeadWs &ws, int R, int32_t *ids, float *best, int *flag,
                                  unsigned int publishers, int32_t *ids_host = nullptr, int32_t *count_host = nullptr,
                                  int32_t boundary = -1) {
-    // The barrier orders every thread's key atomics before thread 0's fence
-    // (fences are cumulative), so one fence per CTA publishes them all.
+    // The barrier orders every thread's key atomics before thread 0's ticket,
+    // whose release (cumulative) publishes them all.
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
-        *flag = atomicAdd(ws.ticket, 1u) == publishers - 1u;
-        if (*flag) __threadfence();
+        // release: the CTA's key atomics (ordered before this by the barrier);
+        // acquire, for the last CTA: every other CTA's
+        unsigned int old;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(ws.ticket) : "memory");
+        *flag = old == publishers - 1u;
     }
     __syncthreads();
     if (!*flag) return;
@@ -267,6 +269,18 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+
+// Same, without waiting: the caller issues several and then tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 struct TcLayout {
     uint32_t stage_bytes;   // A tile + B tile
@@ -790,19 +804,19 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
 // W and h k-slice of the CTA is requested at once (no ring reuse: at 64 x
 // 2048 x 4097 the CTA's 128 KB of W and 64 KB of h are all in flight), so the
 // load time is the HBM burst itself.  The epilogue runs once per CTA with its
-// instructions fetched cold, so it is short and has one wait: each
-// accumulator row (one vocab row, read from TMEM by the thread of that lane)
-// goes by asynchronous remote stores into the shared memory of the CTA that
-// owns the row, completing on that CTA's mbarrier; each CTA waits for its own
-// 32 rows from all CK sources, sums them, selects per batch row and folds its
-// best keys into the global keys; the last CTA converts keys to ids.
+// instructions fetched cold, so it is short and has one wait: each warp reads
+// its 32 accumulator rows (one vocab row per lane) from TMEM, stages them in
+// the idle slice area and sends each owning CTA its rows with one bulk copy
+// completing on that CTA's mbarrier; each CTA waits for its own 32 rows from
+// all CK sources, sums them, selects per batch row and folds its best keys
+// into the global keys; the last CTA converts keys to ids.
 constexpr int kSplitThreads = 256;
 constexpr int kSplitMaxN = 64;
 
 struct SplitLayout {
     uint32_t hslot;    // bytes of one h k-slice (N rows x 128 B)
     uint32_t h;        // offset of the h slices (after the W slices)
-    uint32_t recv;     // offset of recv[CK][RS][NR] fp32 partials
+    uint32_t recv;     // offset of recv[CK][RS][NR] fp32 partials (after the slices, or the staging rows if larger)
     uint32_t bars;     // kch full barriers, the accumulator barrier, the receive barrier
     uint32_t colbest;  // [N] packed keys
     uint32_t misc;     // TMEM address, flag
@@ -817,7 +831,11 @@ __host__ __device__ inline SplitLayout split_layout(int N, int kch, int CK, int 
     SplitLayout L;
     L.hslot = static_cast<uint32_t>(N) * 128u;
     L.h = static_cast<uint32_t>(kch) * kATileBytes;
-    L.recv = L.h + static_cast<uint32_t>(kch) * L.hslot;
+    // after the MMAs the W and h slices hold the staged accumulator rows
+    // (128 rows of NR floats): at least that much room before recv
+    const uint32_t slices = L.h + static_cast<uint32_t>(kch) * L.hslot;
+    const uint32_t staging = static_cast<uint32_t>(kTileM * split_row(N)) * 4u;
+    L.recv = slices > staging ? slices : staging;
     L.bars = L.recv + static_cast<uint32_t>(CK * RS * split_row(N)) * 4u;
     L.colbest = L.bars + 8u * (kch + 2);
     L.misc = L.colbest + 8u * N;
@@ -833,16 +851,6 @@ __host__ __device__ inline SplitLayout split_layout(int N, int kch, int CK, int 
 template <int NR>
 __device__ __forceinline__ int split_pos(int i, int n) {
     return ((((n >> 2) ^ i) & ((NR >> 2) - 1)) << 2) | (n & 3);
-}
-
-// Asynchronous remote store of 16 bytes, completing on the destination
-// CTA's mbarrier.
-__device__ __forceinline__ void st_async_v4(uint32_t dst_cluster, float x, float y, float z, float w,
-                                            uint32_t bar_cluster) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-                     dst_cluster),
-                 "f"(x), "f"(y), "f"(z), "f"(w), "r"(bar_cluster)
-                 : "memory");
 }
 
 template <bool kGumbel, int N>
@@ -871,8 +879,8 @@ head_split_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     if (threadIdx.x == 0) {
         for (int c = 0; c < kch + 2; ++c) mbar_init(bar_full + 8u * c, 1);
         fence_mbar_init();
-        // every source's rows of this CTA: CK x RS rows of N floats
-        mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>(CK * RS * N) * 4u);
+        // every source's rows of this CTA: CK x RS rows of NR floats
+        mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>(CK * RS * NR) * 4u);
         // Every W slice at once (W never depends on the previous kernel); h,
         // the previous kernel's output, after the programmatic-launch wait.
         prefetch_tensormap(&map_w);
@@ -925,8 +933,11 @@ head_split_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     }
     __syncwarp();
 
-    // ---- accumulator row (vocab row 32 w + lane of the tile) -> its owner
-    bool sent = false;
+    // ---- accumulator rows -> their owners.  Warp w holds the tile's rows
+    // 32 w .. 32 w + 31 (one per lane, all N columns); it stages them in the
+    // now idle slice area in the owner's layout and sends each owner's run of
+    // rows with one bulk copy onto the owner's receive barrier (with CK = 4
+    // a warp's rows all belong to one owner).
     if (warp < 4) {
         const int vl = warp * 32 + lane;
         const int owner = vl / RS;  // < CK: RS = 128 / CK
@@ -935,101 +946,119 @@ head_split_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
         if (!ready) flag_error(a.err, TTS_ERRBIT_TIMEOUT);
         tc_fence_after();
         if (__all_sync(kFull, ready)) {
-            const uint32_t row = base + Lo.recv + static_cast<uint32_t>((rank * RS + i) * NR) * 4u;
-            const uint32_t dst = map_cluster(row, static_cast<uint32_t>(owner));
-            const uint32_t dbar = map_cluster(bar_recv, static_cast<uint32_t>(owner));
+            uint32_t r[N];
 #pragma unroll
-            for (int c0 = 0; c0 < N; c0 += 16) {
-                float v[16];
-                tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
+            for (int c0 = 0; c0 < N; c0 += 16)
+                tmem_ld16_nowait(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, r + c0);
+            tmem_wait_ld();
+            const uint32_t srow = base + static_cast<uint32_t>(vl * NR) * 4u;
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    st_async_v4(dst + 4u * split_pos<NR>(i, c0 + 4 * q), v[4 * q], v[4 * q + 1], v[4 * q + 2],
-                                v[4 * q + 3], dbar);
+            for (int q = 0; q < N / 4; ++q)
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(srow + 4u * split_pos<NR>(i, 4 * q)),
+                             "r"(r[4 * q]), "r"(r[4 * q + 1]), "r"(r[4 * q + 2]), "r"(r[4 * q + 3])
+                             : "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the copies read through the async proxy
+            __syncwarp();
+            if (lane == 0) {
+                for (int row = warp * 32; row < warp * 32 + 32;) {
+                    const int o = row / RS;
+                    const int end = min(warp * 32 + 32, (o + 1) * RS);
+                    const uint32_t dst = base + Lo.recv + static_cast<uint32_t>((rank * RS + row - o * RS) * NR) * 4u;
+                    bulk_copy_to_peer(map_cluster(dst, static_cast<uint32_t>(o)),
+                                      base + static_cast<uint32_t>(row * NR) * 4u,
+                                      static_cast<uint32_t>((end - row) * NR) * 4u,
+                                      map_cluster(bar_recv, static_cast<uint32_t>(o)));
+                    row = end;
+                }
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
             }
-            sent = true;
         }
     }
     tc_fence_before();
-    // every partial row of this CTA's 32 rows has arrived (a failed peer
-    // leaves this wait to run out)
-    const bool got = mbar_wait(bar_recv, 0);
-    if (!got && threadIdx.x == 0) flag_error(a.err, TTS_ERRBIT_TIMEOUT);
 
     // ---- sum the CK partials of this CTA's rows and select per batch row.
-    // Item = (8-row group, batch row); consecutive threads take consecutive
-    // batch rows, so each recv row is read with consecutive addresses.
+    // Item = (8-row group g, batch row n), G = RS / 8 groups; the G items of
+    // one batch row sit in G consecutive lanes and meet in a shuffle max.
+    // Warps 4-7 run the same loop once early without committing anything (its
+    // reads land on not yet written rows), so its instructions are cached by
+    // the time the rows arrive.
     const float *recv = reinterpret_cast<const float *>(smem + Lo.recv);
-    const int items = (RS / 8) * N;
+    const int G = RS / 8;
+    const int items = G * N;
     const int aR = a.R, aV = a.V;
-    for (int item = threadIdx.x; item < items && got; item += blockDim.x) {
-        const int n = item % N, g = item / N;
-        const int r = n;
-        const int v = v0 + rank * RS + 8 * g;
-        if (r >= aR || v >= aV) continue;
-        float lg[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int i = 8 * g + e;
-            const float *src = recv + static_cast<size_t>(i) * NR + split_pos<NR>(i, n);
-            float x = src[0];
-            for (int s = 1; s < CK; ++s) x += src[static_cast<size_t>(s) * RS * NR];
-            lg[e] = x;
+    bool got = true;
+    for (int pass = warp >= 4 ? 0 : 1; pass < 2; ++pass) {
+        const bool commit = pass == 1;
+        if (commit) {
+            got = mbar_wait(bar_recv, 0);
+            if (!got && threadIdx.x == 0) flag_error(a.err, TTS_ERRBIT_TIMEOUT);
         }
-        if (a.bias) {
+        for (int item = threadIdx.x; item < items && got; item += blockDim.x) {
+            const int g = item % G, n = item / G;
+            const int r = n;
+            const int v = v0 + rank * RS + 8 * g;
+            const bool live = r < aR && v < aV;
+            unsigned long long best = 0ull;
+            if (live) {
+                float lg[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                if (v + e < aV) lg[e] += a.bias[v + e];
-        }
-        // ids this row may choose: below the structural tail, or a tail id
-        // whose mask bit is set (the boundary token alone with eos_allowed)
-        int tail0 = aV;
-        uint32_t tm = 0u;
-        if (a.tail) {
-            tail0 = aV - a.n_tail;
-            tm = a.tail[r];
-        } else if (a.eos && !a.eos[r]) {
-            tail0 = aV - 1;
-        }
-        uint32_t allow = 0xFFu;
-        if (v + 8 > tail0) {
-            allow = 0u;
+                for (int e = 0; e < 8; ++e) {
+                    const int ii = 8 * g + e;
+                    const float *src = recv + static_cast<size_t>(ii) * NR + split_pos<NR>(ii, n);
+                    float x = src[0];
+                    for (int sidx = 1; sidx < CK; ++sidx) x += src[static_cast<size_t>(sidx) * RS * NR];
+                    lg[e] = x;
+                }
+                if (a.bias) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int id = v + e;
-                const bool ok = id < aV && (id < tail0 || ((tm >> (id - tail0)) & 1u));
-                allow |= ok ? 1u << e : 0u;
+                    for (int e = 0; e < 8; ++e)
+                        if (v + e < aV) lg[e] += a.bias[v + e];
+                }
+                // ids this row may choose: below the structural tail, or a tail
+                // id whose mask bit is set (the boundary token alone with eos_allowed)
+                int tail0 = aV;
+                uint32_t tm = 0u;
+                if (a.tail) {
+                    tail0 = aV - a.n_tail;
+                    tm = a.tail[r];
+                } else if (a.eos && !a.eos[r]) {
+                    tail0 = aV - 1;
+                }
+                uint32_t allow = 0xFFu;
+                if (v + 8 > tail0) {
+                    allow = 0u;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int id = v + e;
+                        const bool ok = id < aV && (id < tail0 || ((tm >> (id - tail0)) & 1u));
+                        allow |= ok ? 1u << e : 0u;
+                    }
+                }
+                if constexpr (kGumbel) {
+                    const Philox4x64 ph(static_cast<uint64_t>(v >> 3), 0, a.pos, 0, a.seed[r], a.step[r]);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        if (!((allow >> e) & 1u)) continue;
+                        const float u = bits_to_uniform(ph.half(e));
+                        const unsigned long long k =
+                            pack_argmax(lg[e] / a.temperature + gumbel_from_uniform(u), v + e);
+                        best = k > best ? k : best;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        if (!((allow >> e) & 1u)) continue;
+                        const unsigned long long k = pack_argmax(lg[e], v + e);
+                        best = k > best ? k : best;
+                    }
+                }
             }
-        }
-        unsigned long long best = 0ull;
-        if constexpr (kGumbel) {
-            // skip the logarithms of entries whose uniform cannot beat the
-            // batch row's current best (exact for the entries kept)
-            float lmax = -INFINITY;
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                if ((allow >> e) & 1u) lmax = fmaxf(lmax, lg[e]);
-            const unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(colbest + n);
-            float thr = 0.0f;
-            if (cur) thr = expf(-expf(-(unpack_value(cur) - lmax / a.temperature - kGumbelSlack)));
-            const Philox4x64 ph(static_cast<uint64_t>(v >> 3), 0, a.pos, 0, a.seed[r], a.step[r]);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                if (!((allow >> e) & 1u)) continue;
-                const float u = bits_to_uniform(ph.half(e));
-                if (!(u > thr)) continue;
-                const unsigned long long k = pack_argmax(lg[e] / a.temperature + gumbel_from_uniform(u), v + e);
-                best = k > best ? k : best;
+            for (int o = 1; o < G; o <<= 1) {
+                const unsigned long long other = __shfl_xor_sync(kFull, best, o);
+                best = other > best ? other : best;
             }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                if (!((allow >> e) & 1u)) continue;
-                const unsigned long long k = pack_argmax(lg[e], v + e);
-                best = k > best ? k : best;
-            }
+            if (commit && g == 0) colbest[n] = best;
         }
-        if (best) atomicMax(colbest + n, best);
     }
     __syncthreads();
     if (warp == 1) {
@@ -1041,7 +1070,8 @@ head_split_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
         const unsigned long long k = colbest[threadIdx.x];
         if (static_cast<int>(threadIdx.x) < aR && k) atomicMax(a.ws.keys + threadIdx.x, k);
     }
-    (void)sent;
+    // this CTA's outgoing copies have finished reading its staging rows
+    if (warp < 4 && lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
     finish_selection(a.ws, a.R, a.ids, a.best, flag, gridDim.x, a.ids_host, a.count_host, a.V - 1);
 }
 

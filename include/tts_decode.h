@@ -218,9 +218,9 @@ int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block_table,
  * allocate, plugin hosts that give a library no allocator, and real-time
  * loops that cannot absorb cudaMalloc's implicit synchronisation inside a
  * frame budget.  Same arguments and results as tts_decode_attn, without
- * d_ws / ws_bytes.  The split partials live in one 24 MiB file-scope device
+ * d_ws / ws_bytes.  The split partials live in one 16 MiB file-scope device
  * array that every GPU loading this library holds until the process exits; a
- * request whose tts_decode_attn_workspace_size exceeds 24 MiB returns
+ * request whose tts_decode_attn_workspace_size exceeds 16 MiB returns
  * TTS_ERR_SCRATCH_LIMIT and launches nothing.  The first call in a CUDA
  * context (per device, and again after that context is replaced, e.g. by
  * cudaDeviceReset) looks up the array's device address with
