@@ -770,23 +770,39 @@ def run_native(args):
                  (cache2, d2["block_table"], d2["ctx_lens"], d2["q"], torch.zeros_like(step.attn_ws))]
     out2 = torch.empty_like(step.out)
     W_copies = [W] + ([W.clone() for _ in range(15)] if args.chained else [])
-    n_chain = min(K, 400)
+    # launches per captured chain: a multiple of the two attention input sets
+    # and of the 16 copies of W; the chain is replayed n_rep times
+    n_graph = 32
+    n_rep = max(2, -(-min(K, 400) // n_graph))
 
     def chained(fn):
+        """Mean per-launch time of fn(0), fn(1), ... captured once as a CUDA
+        graph with each launch a programmatic dependent of the one before,
+        the graph replayed n_rep times between two events.  Capturing keeps
+        the binding's host cost per call (about 13 us for the attention, 20 us
+        for the head) out of the chain, which a host loop would make the
+        bottleneck for kernels shorter than that."""
         for i in range(4):
             fn(i)
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         prev = bd.tts_set_launch_flags(bd._lib.LAUNCH_PROGRAMMATIC)
         try:
-            e0.record(stream)
-            for i in range(n_chain):
-                fn(i)
-            e1.record(stream)
-            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, capture_error_mode="thread_local"):
+                for i in range(n_graph):
+                    fn(i)
         finally:
             bd.tts_set_launch_flags(prev)
-        return e0.elapsed_time(e1) * 1e3 / n_chain
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_rep):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        del g
+        return e0.elapsed_time(e1) * 1e3 / (n_rep * n_graph)
 
     def attn_i(i):
         c, tbl, lens, q, ws = attn_sets[i & 1]
@@ -877,8 +893,9 @@ def run_native(args):
         "roofline": {"bound": "hbm", "kernel": "decode_attn", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "traffic": traffic, "algorithmic_bytes": ab, "launch_us": att_chain_us,
-                     "timing": (f"{n_chain} launches back to back as programmatic dependents, alternating two "
-                                "copies of the inputs (2 x cache > L2); CUDA events around the run")
+                     "timing": (f"{n_graph} launches captured as one CUDA graph, each a programmatic dependent "
+                                f"of the one before, alternating two copies of the inputs (2 x cache > L2); the "
+                                f"graph replayed {n_rep} times between CUDA events")
                      if args.chained else "single launches after an L2 flush (chained pass skipped)",
                      "achieved_isolated": ab / (att_us * 1e-6) / 1e9,
                      "frac_isolated": ab / (att_us * 1e-6) / 1e9 / peaks["hbm_gbs"],
@@ -886,8 +903,9 @@ def run_native(args):
                      if peak_kind == "measured" else "fallback"},
         "kernels": {
             "decode_attn_us_chained": att_chain_us, "head_select_us_chained": head_chain_us,
-            "chained_note": "per-kernel time with the launch latency hidden (launches back to back as "
-                            "programmatic dependents, inputs rotated beyond L2); the *_us keys below are "
+            "chained_note": "per-kernel time with the launch latency hidden (a captured chain of launches, "
+                            "each a programmatic dependent of the one before, inputs rotated beyond L2); the "
+                            "*_us keys below are "
                             "single launches after an L2 flush, each bracketed by events (launch latency "
                             "included)",
             "kv_append_us": app_us, "decode_attn_us": att_us, "head_select_us": head_us,
