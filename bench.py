@@ -494,8 +494,34 @@ def kernel_sweep(ids, reps, flush_l2, peaks, device) -> dict:
             nxt = torch.empty(w.B, dtype=torch.int32, device=device)
             t_ver = timed(lambda: bd.tts_spec_verify(tl, dp, dt, w.T, vs, vt, n_acc, nxt))
             vb = verify_bytes(w)
+            # with the launch latency hidden: 32 launches over 16 copies of the
+            # rows (beyond L2) captured as one graph, each a programmatic
+            # dependent of the one before, replayed 8 times between events
+            vsets = [(tl, dp)] + [(tl.clone(), dp.clone()) for _ in range(15)]
+            for i in range(4):
+                bd.tts_spec_verify(*vsets[i % 16], dt, w.T, vs, vt, n_acc, nxt)
+            prev = bd.tts_set_launch_flags(bd._lib.LAUNCH_PROGRAMMATIC)
+            try:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, capture_error_mode="thread_local"):
+                    for i in range(32):
+                        bd.tts_spec_verify(*vsets[i % 16], dt, w.T, vs, vt, n_acc, nxt)
+            finally:
+                bd.tts_set_launch_flags(prev)
+            g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(8):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            t_ver_chain = e0.elapsed_time(e1) * 1e3 / (8 * 32)
+            del g, vsets
             entry.update({"spec_verify_us": t_ver, "spec_verify_gbs": vb / t_ver / 1e3,
-                          "spec_verify_frac": vb / t_ver / 1e3 / hbm, "spec_verify_bytes": vb})
+                          "spec_verify_frac": vb / t_ver / 1e3 / hbm, "spec_verify_bytes": vb,
+                          "spec_verify_us_chained": t_ver_chain,
+                          "spec_verify_frac_chained": vb / t_ver_chain / 1e3 / hbm})
             # the whole speculative step captured once (inputs from pinned
             # memory, append, causal attention over K + 1 rows, Gumbel head
             # keeping its logits, verify, results to pinned memory): wall

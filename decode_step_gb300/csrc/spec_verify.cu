@@ -7,13 +7,13 @@
 //
 // One CTA per stream.  Staged kernel (the stream's rows fit in shared
 // memory): bulk copies bring the K target rows (K + 1 with the bonus draw)
-// and the K draft rows into shared memory at once; warp groups reduce each
-// target row to its max and sum of exp((x - max) / T); lane i of one warp
-// tests draft i and a ballot finds the first rejection; the CTA draws the
-// replacement (or bonus) token with a block-wide argmax over packed
-// (key, index) pairs, each thread taking groups of 8 consecutive vocabulary
-// entries so one Philox block feeds 8 draws.  Streaming kernel (rows too
-// large for shared memory): the same steps reading global memory.
+// and the K draft rows into shared memory while the threads generate the
+// draw's Gumbel noise (one Philox block per 8 consecutive vocabulary entries)
+// and the accept uniforms; warp groups reduce each target row to its max and
+// sum of exp((x - max) / T); lane i of one warp tests draft i and a ballot
+// finds the first rejection; the CTA draws the replacement (or bonus) token
+// with a block-wide argmax over packed (key, index) pairs.  Streaming kernel
+// (rows too large for shared memory): the same steps reading global memory.
 #include "tts_common.cuh"
 #include "tts_internal.h"
 
@@ -125,7 +125,7 @@ spec_verify_kernel(const float *__restrict__ tl, const float *__restrict__ dp,
     }
     unsigned long long best = 0ull;
     for (int gi = threadIdx.x; gi < groups; gi += kThreads) {
-        const Philox4x64 ph(static_cast<uint64_t>(gi), 2u, static_cast<uint64_t>(row), 0u, key0, key1);
+        const Philox4x64 ph(static_cast<uint64_t>(gi), 2u, 0u, 0u, key0, key1);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int v = gi * 8 + e;
@@ -170,43 +170,188 @@ __device__ __forceinline__ uint32_t interior_bytes(const float *g, size_t n) {
     return a1 > a0 ? static_cast<uint32_t>(a1 - a0) : 0u;
 }
 
-// Shared-memory image of `n` floats at `g`: the 16-byte-aligned interior by
-// bulk copies (one thread, completing on `bar`, whose expected bytes are
-// already set), the ragged ends by plain loads of the calling threads.
-// `dst` is congruent to `g` modulo 16.
-__device__ void stage_floats(float *dst, const float *g, size_t n, uint32_t bar) {
+// The 16-byte-aligned interior of the shared-memory image of `n` floats at
+// `g` by bulk copies (one thread, completing on `bar`, whose expected bytes
+// the caller sets); `dst` is congruent to `g` modulo 16.  The ragged ends
+// are the caller's, by plain loads.
+__device__ void stage_bulk(float *dst, const float *g, size_t n, uint32_t bar) {
     const uintptr_t s0 = reinterpret_cast<uintptr_t>(g), s1 = s0 + n * 4;
     const uintptr_t a0 = (s0 + 15) & ~uintptr_t(15), a1 = s1 & ~uintptr_t(15);
-    if (a1 <= a0) {  // no aligned interior
-        for (size_t i = threadIdx.x; i < n; i += blockDim.x) dst[i] = __ldg(g + i);
-        return;
-    }
-    const size_t head = (a0 - s0) / 4, tail_from = (a1 - s0) / 4;
-    for (size_t i = threadIdx.x; i < head; i += blockDim.x) dst[i] = __ldg(g + i);
-    for (size_t i = tail_from + threadIdx.x; i < n; i += blockDim.x) dst[i] = __ldg(g + i);
+    if (a1 <= a0) return;
+    const size_t head = (a0 - s0) / 4;
     const uint32_t bytes = static_cast<uint32_t>(a1 - a0);
-    if (threadIdx.x == 0) {
-        const uint32_t d = smem_addr(dst + head);
-        const uint8_t *src = reinterpret_cast<const uint8_t *>(a0);
-        for (uint32_t off = 0; off < bytes; off += kBulkChunk) {
-            const uint32_t len = bytes - off < kBulkChunk ? bytes - off : kBulkChunk;
-            bulk_load_nohint(d + off, src + off, len, bar);
-        }
+    const uint32_t d = smem_addr(dst + head);
+    const uint8_t *src = reinterpret_cast<const uint8_t *>(a0);
+    for (uint32_t off = 0; off < bytes; off += kBulkChunk) {
+        const uint32_t len = bytes - off < kBulkChunk ? bytes - off : kBulkChunk;
+        bulk_load_nohint(d + off, src + off, len, bar);
     }
 }
-
-struct StagedLayout {
-    uint32_t target, draft, total;  // float offsets of the two images (mod-16 placed), bytes
-};
 __host__ __device__ inline uint32_t staged_target_rows(int K, int flags) {
     return static_cast<uint32_t>(K) + ((flags & TTS_VERIFY_BONUS) ? 1u : 0u);
 }
-// Byte offsets of the images are chosen per stream (their alignment follows
-// the global rows); this bounds the room they need.
-__host__ __device__ inline uint32_t staged_bytes(int K, int V, int flags) {
-    return (staged_target_rows(K, flags) + static_cast<uint32_t>(K)) * static_cast<uint32_t>(V) * 4u + 64u;
+// Float offsets of the staged kernel's shared-memory areas: the target rows'
+// image and the draft rows' image (each placed at the float offset that makes
+// it congruent to its global rows modulo 16 bytes, within 4 floats of slack),
+// then the draw's Gumbel noise, one float per vocabulary entry.
+struct StagedLayout {
+    uint32_t draft, noise, bytes;
+};
+__host__ __device__ inline StagedLayout staged_layout(int K, int V, int flags) {
+    const uint32_t nt = staged_target_rows(K, flags) * static_cast<uint32_t>(V);
+    const uint32_t nd = static_cast<uint32_t>(K) * static_cast<uint32_t>(V);
+    StagedLayout L;
+    L.draft = (nt + 4 + 3) & ~3u;
+    L.noise = L.draft + ((nd + 4 + 3) & ~3u);
+    L.bytes = (L.noise + ((static_cast<uint32_t>(V) + 3) & ~3u)) * 4u;
+    return L;
 }
 
+// Hardware base-2 exponential and logarithm (PTX ex2 / lg2, .approx): used
+// where their error (a few units of 2^-23 relative for ex2, about 2^-22
+// absolute for lg2) is far below the 1e-3 within which the walk's ratios and
+// the draw's keys count as near-ties.
+__device__ __forceinline__ float hw_ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float hw_lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Gumbel noise -ln(-ln u) of the verify draw, u = (2k + 1) 2^-24 in (0, 1):
+// the inner -ln u by the Taylor series of -ln(1 - w) = w + w^2/2 + ... in
+// w = 1 - u (exact in fp32) when w < 1/16 (truncated after w^5 / 5: relative
+// error below w^5 / 6), else by the hardware log2; the outer log by the
+// hardware log2.  Its distance to the exact value is tested over every u.
+__device__ __forceinline__ float verify_gumbel(float u) {
+    constexpr float kLn2 = 0.69314718055994531f;
+    const float w = 1.0f - u;
+    const float inner = w < 0.0625f ? w * (1.0f + w * (0.5f + w * (0.33333334f + w * (0.25f + w * 0.2f))))
+                                    : -kLn2 * hw_lg2(u);
+    return -kLn2 * hw_lg2(inner);
+}
+
+// Warp roles of the staged kernel while the rows land.
+constexpr int kRaggedWarp = kStagedWarps - 1;   // the rows' unaligned ends by plain loads
+constexpr int kAcceptWarp = kStagedWarps - 2;   // the accept test's inputs
+constexpr int kNoiseThreads = 32 * (kStagedWarps - 2);
+
+// The staged kernel's per-stream scalars in shared memory.
+struct VerifyScalars {
+    float red_m[kStagedWarps], red_s[kStagedWarps];  // per-warp parts of the row statistics
+    float row_max[kMaxK], row_sum[kMaxK];
+    float acc_u[kMaxK], acc_pd[kMaxK];  // accept test: uniform, draft probability of the token
+    int acc_d[kMaxK];                   // accept test: draft token
+    int reject, accepted, draw, ok;
+    unsigned long long best, best_p;
+    float warm_m, warm_s;  // the warm-up runs' outputs (scratch copy only)
+};
+
+// The three phases after the rows land are out-of-line functions: while the
+// rows are in flight, two idle warps run each of them once on scratch data so
+// that their instructions are already on the SM when the CTA needs them (each
+// runs once per CTA, so every instruction would otherwise be fetched cold).
+
+// One warp's part of a row's statistics: the max m of x[v] over
+// v = v0 + lane, v0 + lane + stride, ... and the sum of 2^((x[v] - m) k2)
+// against it (exp((x - m) / T) with k2 = log2(e) / T); lane 0 stores them.
+__device__ __noinline__ void warp_row_part(const float *x, int V, int v0, int stride, float k2, float *m_out,
+                                           float *s_out) {
+    const int lane = threadIdx.x & 31;
+    float m = -INFINITY, s = 0.0f;
+    for (int v = v0 + lane; v < V; v += stride) m = fmaxf(m, x[v]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+    if (m != -INFINITY)
+        for (int v = v0 + lane; v < V; v += stride) s += hw_ex2((x[v] - m) * k2);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+    if (lane == 0) {
+        *m_out = m;
+        *s_out = s;
+    }
+}
+
+// The accept walk, one warp: lane i < K merges row i's wpr parts into its max
+// M and sum Z and tests draft i, accepted iff p_d > 0 and u_i < p_t / p_d
+// (as u_i p_d Z < 2^((x_d - M) k2)); the first failure stops the walk.  An
+// out-of-range token stops it with no draw (checked only where the walk
+// reaches it).
+__device__ __noinline__ void accept_walk(VerifyScalars *S, const float *st, int K, int V, int wpr, float k2,
+                                         int flags, int32_t *err) {
+    const int lane = threadIdx.x & 31;
+    bool ok = true, bad_token = false;
+    if (lane < K) {
+        float M = -INFINITY, Z = 0.0f;
+        for (int w = 0; w < wpr; ++w) M = fmaxf(M, S->red_m[lane * wpr + w]);
+        for (int w = 0; w < wpr; ++w) {
+            const float mw = S->red_m[lane * wpr + w];
+            if (mw != -INFINITY) Z += S->red_s[lane * wpr + w] * hw_ex2((mw - M) * k2);
+        }
+        S->row_max[lane] = M;
+        S->row_sum[lane] = Z;
+        const int d = S->acc_d[lane];
+        if (d < 0 || d >= V) {
+            ok = false;
+            bad_token = true;
+        } else {
+            const float e = hw_ex2((st[static_cast<size_t>(lane) * V + d] - M) * k2);
+            const float pd = S->acc_pd[lane];
+            ok = pd > 0.0f && S->acc_u[lane] * pd * Z < e;
+        }
+    }
+    const unsigned fails = __ballot_sync(kFull, lane < K && !ok);
+    const unsigned bads = __ballot_sync(kFull, bad_token);
+    const int reject = fails ? __ffs(fails) - 1 : -1;
+    const bool bad_first = reject >= 0 && ((bads >> reject) & 1u);
+    if (lane == 0) {
+        if (bad_first) flag_error(err, TTS_ERRBIT_TOKEN);
+        S->reject = reject;
+        S->accepted = reject >= 0 ? reject : K;
+        S->draw = !bad_first && (reject >= 0 || (flags & TTS_VERIFY_BONUS)) ? 1 : 0;
+    }
+}
+
+struct DrawBest {
+    unsigned long long r, p;
+};
+// One thread's part of the draw over row x, entries v = v0, v0 + stride, ...:
+// the largest packed (key, index) of x / T + G (p) and, for a rejection (pdr:
+// the rejected row's draft probabilities), of log(residual) + G over entries
+// with a positive residual max(2^((x - m) k2) iz - p_d, 0) (r).
+__device__ __noinline__ DrawBest draw_part(const float *x, const float *pdr, const float *G, int V, int v0,
+                                           int stride, float m, float iz, float inv_t, float k2) {
+    constexpr float kLn2 = 0.69314718055994531f;
+    DrawBest best{0ull, 0ull};
+    for (int v = v0; v < V; v += stride) {
+        const float g = G[v], xv = x[v];
+        const unsigned long long kp = pack_argmax(xv * inv_t + g, v);
+        best.p = kp > best.p ? kp : best.p;
+        if (pdr) {
+            const float r = fmaxf(hw_ex2((xv - m) * k2) * iz - pdr[v], 0.0f);
+            if (r > 0.0f) {
+                const unsigned long long kr = pack_argmax(kLn2 * hw_lg2(r) + g, v);
+                best.r = kr > best.r ? kr : best.r;
+            }
+        }
+    }
+    return best;
+}
+
+// Staged kernel, one CTA per stream.  The stream's rows arrive by bulk copies
+// (target rows on one barrier, draft rows on another) while warps compute
+// what depends only on the stream's key: the draw's Gumbel noise for every
+// vocabulary entry (keyed by (stream, step, entry): a stream draws at most
+// once per call, from whichever row) and the accept test's inputs.  Then each
+// target row's max and sum of exp((x - max) / T) (per warp: the max of its
+// part, then the sum against it; merged across warps with rescaling), the
+// accept walk in one warp, and the draw over the chosen row from shared
+// memory, spread over every thread.  Every exit waits (bounded) for the
+// copies into shared memory.
 __global__ void __launch_bounds__(kStagedThreads)
 spec_verify_staged_kernel(const float *__restrict__ tl, const float *__restrict__ dp,
                           const int32_t *__restrict__ dt, int K, int V, float T,
@@ -214,116 +359,126 @@ spec_verify_staged_kernel(const float *__restrict__ tl, const float *__restrict_
                           int32_t *__restrict__ n_accepted, int32_t *__restrict__ next_token,
                           int32_t *err) {
     extern __shared__ __align__(16) float sm[];
-    __shared__ __align__(8) uint64_t bar_storage;
-    __shared__ float red_m[kStagedWarps], red_s[kStagedWarps];
-    __shared__ float row_max[kMaxK], row_sum[kMaxK];
-    __shared__ int s_reject, s_accepted, s_draw, s_ok;
-    __shared__ unsigned long long s_best, s_best_p;
+    __shared__ __align__(8) uint64_t bars[2];  // target rows, draft rows
+    __shared__ VerifyScalars S, scratch;       // scratch: the warm-up runs' outputs
     const int b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t bar = smem_addr(&bar_storage);
-    if (threadIdx.x == 0) {
-        mbar_init(bar, 1);
-        fence_mbar_init();
-        s_best = 0ull;
-        s_best_p = 0ull;
-        s_ok = 1;
-    }
-    __syncthreads();
-    pdl_wait_prerequisites();
-    pdl_allow_dependents();
-
-    // ---- stage the rows: each image starts at the float offset that makes it
-    // congruent to its global rows modulo 16 bytes
+    const uint32_t bar_t = smem_addr(&bars[0]), bar_d = smem_addr(&bars[1]);
     const float *tl_b = tl + static_cast<size_t>(b) * (K + 1) * V;
     const float *dp_b = dp + static_cast<size_t>(b) * K * V;
     const uint32_t nt = staged_target_rows(K, flags) * static_cast<uint32_t>(V);
     const uint32_t nd = static_cast<uint32_t>(K) * static_cast<uint32_t>(V);
+    const StagedLayout Lo = staged_layout(K, V, flags);
     float *st = sm + ((reinterpret_cast<uintptr_t>(tl_b) & 15) >> 2);
-    float *sdr = sm + ((nt + 4 + 3) & ~3u) + ((reinterpret_cast<uintptr_t>(dp_b) & 15) >> 2);
-    if (threadIdx.x == 0) mbar_arrive_expect_tx(bar, interior_bytes(tl_b, nt) + interior_bytes(dp_b, nd));
-    stage_floats(st, tl_b, nt, bar);
-    stage_floats(sdr, dp_b, nd, bar);
-    if (!mbar_wait(bar, 0)) {
-        if (threadIdx.x == 0) s_ok = 0;
+    float *sdr = sm + Lo.draft + ((reinterpret_cast<uintptr_t>(dp_b) & 15) >> 2);
+    float *G = sm + Lo.noise;
+    pdl_wait_prerequisites();  // the target rows may come from the kernel before
+    if (threadIdx.x == 0) {
+        mbar_init(bar_t, 1);
+        mbar_init(bar_d, 1);
+        fence_mbar_init();
+        S.best = 0ull;
+        S.best_p = 0ull;
+        S.ok = 1;
+        // target rows first (the statistics need them first)
+        mbar_arrive_expect_tx(bar_t, interior_bytes(tl_b, nt));
+        stage_bulk(st, tl_b, nt, bar_t);
+        mbar_arrive_expect_tx(bar_d, interior_bytes(dp_b, nd));
+        stage_bulk(sdr, dp_b, nd, bar_d);
     }
-    __syncthreads();  // also orders the ragged ends' plain stores
-    if (!s_ok) {
+    __syncthreads();  // the barriers are initialised before anyone waits
+    pdl_allow_dependents();
+    const uint64_t key0 = seed[b], key1 = step[b];
+    const int groups = (V + 7) / 8;
+    const float inv_t = 1.0f / T, k2 = 1.4426950408889634f / T;
+    const int wpr = K >= kStagedWarps ? 1 : kStagedWarps / K;
+
+    // ---- while the rows land (the warm-up runs read scratch or in-flight
+    // shared memory and write only `scratch`)
+    if (warp == kRaggedWarp) {
+        for (int part = 0; part < 2; ++part) {
+            float *dst = part ? sdr : st;
+            const float *g = part ? dp_b : tl_b;
+            const size_t n = part ? nd : nt;
+            const uintptr_t s0 = reinterpret_cast<uintptr_t>(g), s1 = s0 + n * 4;
+            const uintptr_t a0 = (s0 + 15) & ~uintptr_t(15), a1 = s1 & ~uintptr_t(15);
+            if (a1 <= a0) {
+                for (size_t i = lane; i < n; i += 32) dst[i] = __ldg(g + i);
+            } else {
+                const size_t head = (a0 - s0) / 4, tail_from = (a1 - s0) / 4;
+                if (static_cast<size_t>(lane) < head) dst[lane] = __ldg(g + lane);
+                if (tail_from + lane < n) dst[tail_from + lane] = __ldg(g + tail_from + lane);
+            }
+        }
+        const int vw = V < 64 ? V : 64;
+        warp_row_part(G, vw, 0, 32, k2, &scratch.warm_m, &scratch.warm_s);
+        const DrawBest w = draw_part(G, G, G, vw, lane, 32, 0.0f, 1.0f, inv_t, k2);
+        if (lane == 0) scratch.best = w.r ^ w.p;
+    } else if (warp == kAcceptWarp) {
+        if (lane < K) {
+            const int d = dt[static_cast<size_t>(b) * K + lane];
+            S.acc_d[lane] = d;
+            S.acc_pd[lane] = (d >= 0 && d < V) ? __ldg(dp_b + static_cast<size_t>(lane) * V + d) : 0.0f;
+            S.acc_u[lane] = philox_uniform(key0, key1, 1u, 0u, static_cast<uint32_t>(lane));
+        }
+        if (lane < kMaxK) scratch.acc_d[lane] = 0;
+        scratch.red_m[lane] = 0.0f;
+        scratch.red_s[lane] = 1.0f;
+        __syncwarp();
+        // a one-entry "row" per lane inside scratch (V = 1, every token 0)
+        accept_walk(&scratch, scratch.red_s, K, 1, wpr, k2, flags, nullptr);
+    } else {
+        for (int gi = threadIdx.x; gi < groups; gi += kNoiseThreads) {
+            const Philox4x64 ph(static_cast<uint64_t>(gi), 2u, 0u, 0u, key0, key1);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int v = gi * 8 + e;
+                if (v < V) G[v] = verify_gumbel(bits_to_uniform(ph.half(e)));
+            }
+        }
+    }
+    if (!mbar_wait(bar_t, 0)) S.ok = 0;
+    __syncthreads();  // also orders the ragged ends, the noise and the accept inputs
+    if (!S.ok) {
         if (threadIdx.x == 0) {
             flag_error(err, TTS_ERRBIT_TIMEOUT);
             n_accepted[b] = 0;
             next_token[b] = -1;
+            mbar_wait(bar_t, 0);  // bounded: let the copies land before the CTA exits
+            mbar_wait(bar_d, 0);
         }
-        mbar_wait(bar, 0);  // bounded: let the copies land before the CTA exits
         return;
     }
 
-    // ---- softmax statistics of the K target rows: wpr warps per row.
-    // exp((x - M) / T) as exp2((x - M) * log2(e) / T).
-    const float inv_t = 1.0f / T, k2 = 1.4426950408889634f / T;
-    const int wpr = K >= kStagedWarps ? 1 : kStagedWarps / K;
+    // ---- max and sum of exp((x - M) / T) of the K target rows, wpr warps per row
     const int my_row = warp / wpr, sub = warp - my_row * wpr;
-    const float *x_row = st + static_cast<size_t>(my_row) * V;
-    if (my_row < K) {
-        float m = -INFINITY;
-        for (int v = sub * 32 + lane; v < V; v += wpr * 32) m = fmaxf(m, x_row[v]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-        if (lane == 0) red_m[warp] = m;
-    }
+    if (my_row < K)
+        warp_row_part(st + static_cast<size_t>(my_row) * V, V, sub * 32, wpr * 32, k2, &S.red_m[warp],
+                      &S.red_s[warp]);
     __syncthreads();
-    if (my_row < K) {
-        float M = -INFINITY;
-        for (int w = 0; w < wpr; ++w) M = fmaxf(M, red_m[my_row * wpr + w]);
-        float s = 0.0f;
-        for (int v = sub * 32 + lane; v < V; v += wpr * 32) s += exp2f((x_row[v] - M) * k2);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
-        if (lane == 0) red_s[warp] = s;
-        if (sub == 0 && lane == 0) row_max[my_row] = M;
-    }
+    if (warp == 0) accept_walk(&S, st, K, V, wpr, k2, flags, err);
     __syncthreads();
-    if (threadIdx.x < K) {
-        float s = 0.0f;
-        for (int w = 0; w < wpr; ++w) s += red_s[threadIdx.x * wpr + w];
-        row_sum[threadIdx.x] = s;
-    }
-    __syncthreads();
-
-    // ---- accept / reject: lane i tests draft i; the first failure stops
-    if (warp == 0) {
-        bool ok = true, bad_token = false;
-        if (lane < K) {
-            const int d = dt[static_cast<size_t>(b) * K + lane];
-            if (d < 0 || d >= V) {
-                ok = false;
-                bad_token = true;
-            } else {
-                const float pt = exp2f((st[static_cast<size_t>(lane) * V + d] - row_max[lane]) * k2) / row_sum[lane];
-                const float pd = sdr[static_cast<size_t>(lane) * V + d];
-                ok = pd > 0.0f && philox_uniform(seed[b], step[b], 1u, 0u, static_cast<uint32_t>(lane)) < pt / pd;
-            }
-        }
-        const unsigned fails = __ballot_sync(kFull, lane < K && !ok);
-        const unsigned bads = __ballot_sync(kFull, bad_token);
-        const int reject = fails ? __ffs(fails) - 1 : -1;
-        // an out-of-range token stops the walk with no draw (checked only
-        // where the walk reaches it)
-        const bool bad_first = reject >= 0 && ((bads >> reject) & 1u);
-        if (lane == 0) {
-            if (bad_first) flag_error(err, TTS_ERRBIT_TOKEN);
-            s_reject = reject;
-            s_accepted = reject >= 0 ? reject : K;
-            s_draw = !bad_first && (reject >= 0 || (flags & TTS_VERIFY_BONUS)) ? 1 : 0;
-        }
-    }
-    __syncthreads();
-    if (!s_draw) {
+    if (!S.draw) {
         if (threadIdx.x == 0) {
-            n_accepted[b] = s_accepted;
+            n_accepted[b] = S.accepted;
             next_token[b] = -1;
+            if (!mbar_wait(bar_d, 0)) flag_error(err, TTS_ERRBIT_TIMEOUT);  // the copies land before the exit
         }
         return;
+    }
+    const int reject = S.reject;
+    if (reject >= 0) {  // the residual reads the rejected row's draft probabilities
+        if (!mbar_wait(bar_d, 0)) S.ok = 0;
+        __syncthreads();
+        if (!S.ok) {
+            if (threadIdx.x == 0) {
+                flag_error(err, TTS_ERRBIT_TIMEOUT);
+                n_accepted[b] = 0;
+                next_token[b] = -1;
+                mbar_wait(bar_d, 0);
+            }
+            return;
+        }
     }
 
     // ---- the replacement draw (rejection at row `reject`) or the bonus draw
@@ -332,50 +487,35 @@ spec_verify_staged_kernel(const float *__restrict__ tl, const float *__restrict_
     // log p_t + G, as p_t is exp(x / T) up to a common factor) for the case of
     // a residual that is zero everywhere, where the draw falls back to p_t.
     // Bonus: x / T + G.
-    const int reject = s_reject;
     const int row = reject >= 0 ? reject : K;
-    const float *x = st + static_cast<size_t>(row) * V;
-    const float *pdr = reject >= 0 ? sdr + static_cast<size_t>(row) * V : nullptr;
-    const float m = reject >= 0 ? row_max[row] : 0.0f;
-    const float iz = reject >= 0 ? 1.0f / row_sum[row] : 1.0f;
-    const uint64_t key0 = seed[b], key1 = step[b];
-    const int groups = (V + 7) / 8;
-    unsigned long long best_r = 0ull, best_p = 0ull;
-    for (int gi = threadIdx.x; gi < groups; gi += blockDim.x) {
-        const Philox4x64 ph(static_cast<uint64_t>(gi), 2u, static_cast<uint64_t>(row), 0u, key0, key1);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int v = gi * 8 + e;
-            if (v >= V) break;
-            const float g = gumbel_from_uniform(bits_to_uniform(ph.half(e)));
-            const unsigned long long kp = pack_argmax(x[v] * inv_t + g, v);
-            best_p = kp > best_p ? kp : best_p;
-            if (reject >= 0) {
-                const float r = fmaxf(exp2f((x[v] - m) * k2) * iz - pdr[v], 0.0f);
-                if (r > 0.0f) {
-                    const unsigned long long kr = pack_argmax(logf(r) + g, v);
-                    best_r = kr > best_r ? kr : best_r;
-                }
-            }
-        }
-    }
+    DrawBest best = draw_part(st + static_cast<size_t>(row) * V,
+                              reject >= 0 ? sdr + static_cast<size_t>(row) * V : nullptr, G, V, threadIdx.x,
+                              blockDim.x, reject >= 0 ? S.row_max[row] : 0.0f,
+                              reject >= 0 ? 1.0f / S.row_sum[row] : 1.0f, inv_t, k2);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long a = __shfl_xor_sync(kFull, best_r, o);
-        const unsigned long long c = __shfl_xor_sync(kFull, best_p, o);
-        best_r = a > best_r ? a : best_r;
-        best_p = c > best_p ? c : best_p;
+        const unsigned long long a = __shfl_xor_sync(kFull, best.r, o);
+        const unsigned long long c = __shfl_xor_sync(kFull, best.p, o);
+        best.r = a > best.r ? a : best.r;
+        best.p = c > best.p ? c : best.p;
     }
     if (lane == 0) {
-        if (best_r) atomicMax(&s_best, best_r);
-        if (best_p) atomicMax(&s_best_p, best_p);
+        if (best.r) atomicMax(&S.best, best.r);
+        if (best.p) atomicMax(&S.best_p, best.p);
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        const unsigned long long pick = reject >= 0 && s_best ? s_best : s_best_p;
-        n_accepted[b] = s_accepted;
+        const unsigned long long pick = reject >= 0 && S.best ? S.best : S.best_p;
+        n_accepted[b] = S.accepted;
         next_token[b] = pick ? unpack_index(pick) : -1;
+        if (reject < 0 && !mbar_wait(bar_d, 0)) flag_error(err, TTS_ERRBIT_TIMEOUT);  // before the exit
     }
+}
+
+// Test support: the verify draw's Gumbel noise of n 32-bit Philox words.
+__global__ void verify_noise_kernel(const uint32_t *bits, float *out, int n) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) out[i] = verify_gumbel(bits_to_uniform(bits[i]));
 }
 
 }  // namespace
@@ -394,7 +534,7 @@ extern "C" int tts_spec_verify(const float *d_target_logits, const float *d_draf
         temperature == INFINITY || (flags & ~TTS_VERIFY_BONUS) != 0)
         return TTS_ERR_INVALID;
     if (B == 0) return TTS_OK;
-    const size_t smem = staged_bytes(K, V, flags);
+    const size_t smem = staged_layout(K, V, flags).bytes;
     if (smem <= 200u * 1024u) {
         if (!ensure_dynamic_smem(reinterpret_cast<const void *>(spec_verify_staged_kernel), static_cast<int>(smem)))
             return TTS_ERR_CUDA;
@@ -406,5 +546,13 @@ extern "C" int tts_spec_verify(const float *d_target_logits, const float *d_draf
             d_target_logits, d_draft_probs, d_draft_tokens, K, V, temperature, d_seed, d_step, flags,
             d_n_accepted, d_next_token, d_err);
     }
+    return launch_status();
+}
+
+extern "C" int tts_test_verify_noise(const uint32_t *d_bits, float *d_out, int32_t n, void *stream) {
+    using namespace tts;
+    if (n < 0 || (n > 0 && (!d_bits || !d_out))) return TTS_ERR_INVALID;
+    if (n == 0) return TTS_OK;
+    verify_noise_kernel<<<(n + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(d_bits, d_out, n);
     return launch_status();
 }

@@ -276,10 +276,11 @@ int tts_codebook_head_select(const void *d_h, const void *d_W, int32_t dtype, in
  *   u_i < p_t[d] / p_d[d], u_i the Philox uniform (key (seed[b], step[b]),
  *   counter (i / 8, 1, 0, 0)).  At the first rejection the replacement token is
  *   drawn from max(p_t - p_d, 0), normalised (Gumbel-max, counter
- *   (v / 8, 2, i, 0); from p_t itself if that residual is zero everywhere) and
+ *   (v / 8, 2, 0, 0); from p_t itself if that residual is zero everywhere) and
  *   verification stops.  If all K are accepted, next_token = -1, or with
  *   TTS_VERIFY_BONUS a token drawn from softmax(target_logits[b][K] /
- *   temperature) (counter (v / 8, 2, K, 0)).
+ *   temperature) (counter (v / 8, 2, 0, 0): a stream draws at most once per
+ *   call, so the draw's noise does not depend on the row drawn from).
  *  d_target_logits float [B][K+1][V];  d_draft_probs float [B][K][V]
  *  d_draft_tokens int32 [B][K];  d_seed, d_step uint64 [B]
  *  d_n_accepted, d_next_token int32 [B]
@@ -570,6 +571,14 @@ int32_t tts_set_launch_flags(int32_t flags);
  * TTS_ERR_INVALID for an unknown mode or a limit outside [1e3, 4e9]. */
 enum { TTS_TEST_STALL_NONE = 0, TTS_TEST_STALL_ATTN_RING = 1, TTS_TEST_STALL_PREDICTOR_GRID = 2 };
 int tts_test_set_stall(int32_t what, int64_t wait_limit_cycles);
+
+/* Test support (no counterpart on the pages): the Gumbel noise the
+ * speculative verify's draw uses, -ln(-ln u), for n 32-bit Philox words:
+ * u = (2 (bits >> 9) + 1) / 2^24, so that a test can bound its distance to
+ * the exact value over every u.  d_bits uint32 [n], d_out float [n] (device);
+ * enqueued on `stream`.  TTS_ERR_INVALID for n < 0 or a null pointer with
+ * n > 0. */
+int tts_test_verify_noise(const uint32_t *d_bits, float *d_out, int32_t n, void *stream);
 
 /* ----------------------------------------------------------------- misc */
 

@@ -616,10 +616,12 @@ static void row_probs(const float *x, int V, float T, float *p) {
  * p_d == 0 rejects; otherwise the draft is accepted when u_i < p_t[d] / p_d
  * (u_i the Philox uniform tag 1, pos 0, idx i).  At the first rejection the
  * replacement token is drawn from the clamped residual max(p_t - p_d, 0),
- * normalised (Gumbel-max over log of the residual, tag 2, pos i, idx v; if the
+ * normalised (Gumbel-max over log of the residual, tag 2, pos 0, idx v; if the
  * residual is zero everywhere, from p_t itself) and verification stops.  If
  * every draft is accepted next_token = -1, or with flags & 1 a bonus token is
- * drawn from softmax(target_logits[b][K] / T) (tag 2, pos K).
+ * drawn from softmax(target_logits[b][K] / T) (tag 2, pos 0).  A stream draws
+ * at most once per call, so the draw's noise is keyed by (stream, step, v)
+ * whichever row it draws from.
  * gap_accept[b]: min |p_t/p_d - u| over the tests made (inf if none);
  * gap_resid[b]: gap between the two largest keys of the final draw (inf if
  * none).  Returns 0, or -1 on a draft token outside [0, V). */
@@ -657,7 +659,7 @@ int orc_spec_verify(const float *target_logits, const float *draft_probs,
             for (int v = 0; v < V; ++v) {
                 const float r = any ? fmaxf(pt[v] - dp[v], 0.0f) : pt[v];
                 if (!(r > 0.0f)) continue;
-                const float key = logf(r) + orc_gumbel(seed[b], step[b], 2u, (uint32_t)i, (uint32_t)v);
+                const float key = logf(r) + orc_gumbel(seed[b], step[b], 2u, 0u, (uint32_t)v);
                 if (next < 0 || key > top) { sec = top; top = key; next = v; }
                 else if (key > sec) sec = key;
             }
@@ -669,7 +671,7 @@ int orc_spec_verify(const float *target_logits, const float *draft_probs,
             const float *tl = target_logits + ((size_t)b * (K + 1) + K) * V;
             float top = -INFINITY, sec = -INFINITY;
             for (int v = 0; v < V; ++v) {
-                const float key = tl[v] / T + orc_gumbel(seed[b], step[b], 2u, (uint32_t)K, (uint32_t)v);
+                const float key = tl[v] / T + orc_gumbel(seed[b], step[b], 2u, 0u, (uint32_t)v);
                 if (next < 0 || key > top) { sec = top; top = key; next = v; }
                 else if (key > sec) sec = key;
             }

@@ -415,6 +415,43 @@ def check_verify_bonus_token(o):
     assert (r["next_token"] == -1).all(), "no bonus token unless asked for"
 
 
+def check_verify_draw_noise(o):
+    """The replacement and bonus draws are Gumbel-max with the noise at
+    counter position 0 of tag 2, whichever row they draw from: the token
+    maximises log(residual) + G (or target / T + G for the bonus), G the
+    pinned Philox-Gumbel of (seed, step, tag 2, position 0, entry).  Rows 1 and
+    K = 2 are drawn from, so noise keyed by the row would differ."""
+    T = 0.7
+    V = 40
+    rng = np.random.default_rng(19)
+    tl = rng.standard_normal((3, V)).astype(np.float32)
+    tl[1, 7] = -1e30                                   # p_t = 0 at draft 1's token: rejected
+    dp = np.stack([_softmax64(tl[0], T), _softmax64(rng.standard_normal(V), 1.0)]).astype(np.float32)
+    tokens = np.array([[3, 7]], dtype=np.int32)        # draft 0: p_d = p_t, accepted
+    tlb = rng.standard_normal((3, V)).astype(np.float32)
+    dpb = _softmax64(tlb[:2], T).astype(np.float32)    # every draft accepted: the bonus row 2 is drawn
+    tokens_b = np.array([[1, 2]], dtype=np.int32)
+    resid = np.maximum(_softmax64(tl[1], T) - dp[1].astype(np.float64), 0.0)
+    checked = [0, 0]
+    for seed in range(40):
+        g = np.array([o.gumbel(seed, 0, 2, 0, v) for v in range(V)])
+        for case, (x, d, tok, bonus) in enumerate(((tl, dp, tokens, False), (tlb, dpb, tokens_b, True))):
+            r = _verify_one(o, x, d, tok, [seed], T, bonus=bonus)
+            if case == 0:
+                assert r["n_accepted"][0] == 1
+                key = np.where(resid > 0, np.log(np.where(resid > 0, resid, 1.0)) + g, -np.inf)
+            else:
+                if r["n_accepted"][0] != 2:
+                    continue
+                key = x[2].astype(np.float64) / T + g
+            top = np.sort(key)[-2:]
+            if top[1] - top[0] < 1e-3:
+                continue
+            assert r["next_token"][0] == int(np.argmax(key)), f"seed {seed}: {'bonus' if bonus else 'residual'} draw"
+            checked[case] += 1
+    assert min(checked) >= 30, checked
+
+
 # ---------------------------------------------------------------- FP8 cache
 
 def _torch_e4m3_table():

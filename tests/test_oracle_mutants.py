@@ -90,6 +90,12 @@ MUTANTS = [
     ("masked head: mask bits reversed", "!((tail_allowed[r] >> j) & 1u)",
      "!((tail_allowed[r] >> (n_tail - 1 - j)) & 1u)"),
     ("verify: bonus always drawn", "if (!rejected && (flags & 1)) {", "if (!rejected) {"),
+    ("verify: draw noise keyed by the rejected row",
+     "logf(r) + orc_gumbel(seed[b], step[b], 2u, 0u, (uint32_t)v)",
+     "logf(r) + orc_gumbel(seed[b], step[b], 2u, (uint32_t)i, (uint32_t)v)"),
+    ("verify: bonus noise keyed by the bonus row",
+     "tl[v] / T + orc_gumbel(seed[b], step[b], 2u, 0u, (uint32_t)v)",
+     "tl[v] / T + orc_gumbel(seed[b], step[b], 2u, (uint32_t)K, (uint32_t)v)"),
     ("verify: bonus from the last draft row",
      "target_logits + ((size_t)b * (K + 1) + K) * V;", "target_logits + ((size_t)b * (K + 1) + K - 1) * V;"),
 ]
