@@ -95,7 +95,7 @@ _SIGNATURES = {
     "tts_code_predictor_graph_destroy": (None, [_vp]),
     "tts_set_launch_flags": (_i32, [_i32]),
     "tts_test_set_stall": (ctypes.c_int, [_i32, ctypes.c_int64]),
-    "tts_test_verify_noise": (ctypes.c_int, [_vp, _vp, _i32, _vp]),
+    "tts_test_gumbel_noise": (ctypes.c_int, [_vp, _vp, _i32, _vp]),
     "tts_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "tts_version": (ctypes.c_int, []),
 }

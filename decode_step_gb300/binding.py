@@ -507,11 +507,11 @@ def tts_test_set_stall(what: int, wait_limit_cycles: int = 2_000_000_000) -> Non
     check("tts_test_set_stall", lib().tts_test_set_stall(int(what), int(wait_limit_cycles)))
 
 
-def tts_test_verify_noise(bits, out, stream=None) -> None:
-    """Test support: the verify draw's Gumbel noise of the 32-bit Philox words
+def tts_test_gumbel_noise(bits, out, stream=None) -> None:
+    """Test support: the library's Gumbel noise of the 32-bit Philox words
     `bits` (int32 / uint32 view, device) into `out` (float32, same length)."""
     n = bits.numel()
     if out.numel() != n:
         raise ValueError("bits and out must have the same length")
-    check("tts_test_verify_noise", lib().tts_test_verify_noise(_dev(bits, "bits", torch.int32), _dev(out, "out", torch.float32),
+    check("tts_test_gumbel_noise", lib().tts_test_gumbel_noise(_dev(bits, "bits", torch.int32), _dev(out, "out", torch.float32),
                                                                n, _stream(stream)))

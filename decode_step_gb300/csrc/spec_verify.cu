@@ -207,34 +207,6 @@ __host__ __device__ inline StagedLayout staged_layout(int K, int V, int flags) {
     return L;
 }
 
-// Hardware base-2 exponential and logarithm (PTX ex2 / lg2, .approx): used
-// where their error (a few units of 2^-23 relative for ex2, about 2^-22
-// absolute for lg2) is far below the 1e-3 within which the walk's ratios and
-// the draw's keys count as near-ties.
-__device__ __forceinline__ float hw_ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ float hw_lg2(float x) {
-    float y;
-    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// Gumbel noise -ln(-ln u) of the verify draw, u = (2k + 1) 2^-24 in (0, 1):
-// the inner -ln u by the Taylor series of -ln(1 - w) = w + w^2/2 + ... in
-// w = 1 - u (exact in fp32) when w < 1/16 (truncated after w^5 / 5: relative
-// error below w^5 / 6), else by the hardware log2; the outer log by the
-// hardware log2.  Its distance to the exact value is tested over every u.
-__device__ __forceinline__ float verify_gumbel(float u) {
-    constexpr float kLn2 = 0.69314718055994531f;
-    const float w = 1.0f - u;
-    const float inner = w < 0.0625f ? w * (1.0f + w * (0.5f + w * (0.33333334f + w * (0.25f + w * 0.2f))))
-                                    : -kLn2 * hw_lg2(u);
-    return -kLn2 * hw_lg2(inner);
-}
-
 // Warp roles of the staged kernel while the rows land.
 constexpr int kRaggedWarp = kStagedWarps - 1;   // the rows' unaligned ends by plain loads
 constexpr int kAcceptWarp = kStagedWarps - 2;   // the accept test's inputs
@@ -433,7 +405,7 @@ spec_verify_staged_kernel(const float *__restrict__ tl, const float *__restrict_
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int v = gi * 8 + e;
-                if (v < V) G[v] = verify_gumbel(bits_to_uniform(ph.half(e)));
+                if (v < V) G[v] = gumbel_from_uniform(bits_to_uniform(ph.half(e)));
             }
         }
     }
@@ -512,10 +484,10 @@ spec_verify_staged_kernel(const float *__restrict__ tl, const float *__restrict_
     }
 }
 
-// Test support: the verify draw's Gumbel noise of n 32-bit Philox words.
-__global__ void verify_noise_kernel(const uint32_t *bits, float *out, int n) {
+// Test support: the Gumbel noise of n 32-bit Philox words.
+__global__ void gumbel_noise_kernel(const uint32_t *bits, float *out, int n) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < n) out[i] = verify_gumbel(bits_to_uniform(bits[i]));
+    if (i < n) out[i] = gumbel_from_uniform(bits_to_uniform(bits[i]));
 }
 
 }  // namespace
@@ -549,10 +521,10 @@ extern "C" int tts_spec_verify(const float *d_target_logits, const float *d_draf
     return launch_status();
 }
 
-extern "C" int tts_test_verify_noise(const uint32_t *d_bits, float *d_out, int32_t n, void *stream) {
+extern "C" int tts_test_gumbel_noise(const uint32_t *d_bits, float *d_out, int32_t n, void *stream) {
     using namespace tts;
     if (n < 0 || (n > 0 && (!d_bits || !d_out))) return TTS_ERR_INVALID;
     if (n == 0) return TTS_OK;
-    verify_noise_kernel<<<(n + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(d_bits, d_out, n);
+    gumbel_noise_kernel<<<(n + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(d_bits, d_out, n);
     return launch_status();
 }

@@ -182,7 +182,35 @@ __device__ __forceinline__ float philox_uniform(uint64_t seed, uint64_t step, ui
     return bits_to_uniform(p.half(idx & 7));
 }
 
-__device__ __forceinline__ float gumbel_from_uniform(float u) { return -logf(-logf(u)); }
+// Hardware base-2 exponential and logarithm (PTX ex2 / lg2, .approx), for
+// selection keys and softmax sums where their error (a few units of 2^-23
+// relative for ex2, about 2^-22 absolute for lg2) is far below the 1e-3
+// within which two keys or ratios count as near-ties.
+__device__ __forceinline__ float hw_ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float hw_lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Gumbel noise -ln(-ln u) for u = (2k + 1) 2^-24 in (0, 1) (bits_to_uniform):
+// the inner -ln u by the Taylor series of -ln(1 - w) = w + w^2/2 + ... in
+// w = 1 - u (exact in fp32) when w < 1/16 (truncated after w^5 / 5: relative
+// error below w^5 / 6), else by the hardware log2 (near u = 1 its absolute
+// error would swamp -ln u, and those u give the largest draws); the outer log
+// by the hardware log2.  Its distance to the exact value is tested over every
+// u (tts_test_gumbel_noise).
+__device__ __forceinline__ float gumbel_from_uniform(float u) {
+    constexpr float kLn2 = 0.69314718055994531f;
+    const float w = 1.0f - u;
+    const float inner = w < 0.0625f ? w * (1.0f + w * (0.5f + w * (0.33333334f + w * (0.25f + w * 0.2f))))
+                                    : -kLn2 * hw_lg2(u);
+    return -kLn2 * hw_lg2(inner);
+}
 
 // ------------------------------------------------------- argmax key packing
 

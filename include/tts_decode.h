@@ -572,13 +572,14 @@ int32_t tts_set_launch_flags(int32_t flags);
 enum { TTS_TEST_STALL_NONE = 0, TTS_TEST_STALL_ATTN_RING = 1, TTS_TEST_STALL_PREDICTOR_GRID = 2 };
 int tts_test_set_stall(int32_t what, int64_t wait_limit_cycles);
 
-/* Test support (no counterpart on the pages): the Gumbel noise the
- * speculative verify's draw uses, -ln(-ln u), for n 32-bit Philox words:
+/* Test support (no counterpart on the pages): the Gumbel noise every Gumbel
+ * draw of the library uses (head, verify, code predictor), -ln(-ln u), for n
+ * 32-bit Philox words:
  * u = (2 (bits >> 9) + 1) / 2^24, so that a test can bound its distance to
  * the exact value over every u.  d_bits uint32 [n], d_out float [n] (device);
  * enqueued on `stream`.  TTS_ERR_INVALID for n < 0 or a null pointer with
  * n > 0. */
-int tts_test_verify_noise(const uint32_t *d_bits, float *d_out, int32_t n, void *stream);
+int tts_test_gumbel_noise(const uint32_t *d_bits, float *d_out, int32_t n, void *stream);
 
 /* ----------------------------------------------------------------- misc */
 

@@ -257,11 +257,11 @@ def test_launch_flags_and_stall_arguments():
     assert lib.tts_test_set_stall(0, 2_000_000_000) == 0
 
 
-def test_verify_noise_arguments():
-    """The verify-noise test entry point rejects a negative count and null
+def test_gumbel_noise_arguments():
+    """The Gumbel-noise test entry point rejects a negative count and null
     pointers, and does nothing for n = 0 (host-side checks, no GPU)."""
     from decode_step_gb300 import _lib
     lib = _lib.lib()
-    assert lib.tts_test_verify_noise(None, None, 4, None) == -1
-    assert lib.tts_test_verify_noise(None, None, -1, None) == -1
-    assert lib.tts_test_verify_noise(None, None, 0, None) == 0
+    assert lib.tts_test_gumbel_noise(None, None, 4, None) == -1
+    assert lib.tts_test_gumbel_noise(None, None, -1, None) == -1
+    assert lib.tts_test_gumbel_noise(None, None, 0, None) == 0
