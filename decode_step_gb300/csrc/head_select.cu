@@ -843,14 +843,17 @@ __host__ __device__ inline SplitLayout split_layout(int N, int kch, int CK, int 
     return L;
 }
 
+constexpr int kSplitMaxCK = 8;  // widest cluster split of the split build
+
 // Position of float n within partial row i of recv (rows of NR floats, NR a
-// power of two): the row's 16-byte chunks are permuted by the low bits of i,
-// so lanes storing the same chunk of different rows spread over the banks,
-// and a warp reading one row's consecutive columns still touches distinct
-// banks.
+// power of two): the row's 16-byte chunks are permuted by i ^ 2 (i / 8), a
+// bijection per row.  Lanes storing the same chunk of 8 consecutive rows
+// land in distinct bank groups, and a warp reading 8-row groups g of
+// columns n (lane = g + G n) spreads over the banks too, the 2 (i / 8) term
+// separating the groups that the low bits of i alone would put on one bank.
 template <int NR>
 __device__ __forceinline__ int split_pos(int i, int n) {
-    return ((((n >> 2) ^ i) & ((NR >> 2) - 1)) << 2) | (n & 3);
+    return ((((n >> 2) ^ i ^ ((i >> 3) << 1)) & ((NR >> 2) - 1)) << 2) | (n & 3);
 }
 
 template <bool kGumbel, int N>
@@ -1000,13 +1003,25 @@ head_split_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
             const bool live = r < aR && v < aV;
             unsigned long long best = 0ull;
             if (live) {
+                // every source's partials first (independent loads, one
+                // latency), then the sums in source order
+                float part[kSplitMaxCK][8];
+#pragma unroll
+                for (int sidx = 0; sidx < kSplitMaxCK; ++sidx) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int ii = 8 * g + e;
+                        part[sidx][e] = sidx < CK ? recv[(static_cast<size_t>(sidx) * RS + ii) * NR + split_pos<NR>(ii, n)]
+                                                  : 0.0f;
+                    }
+                }
                 float lg[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const int ii = 8 * g + e;
-                    const float *src = recv + static_cast<size_t>(ii) * NR + split_pos<NR>(ii, n);
-                    float x = src[0];
-                    for (int sidx = 1; sidx < CK; ++sidx) x += src[static_cast<size_t>(sidx) * RS * NR];
+                    float x = part[0][e];
+#pragma unroll
+                    for (int sidx = 1; sidx < kSplitMaxCK; ++sidx)
+                        if (sidx < CK) x += part[sidx][e];
                     lg[e] = x;
                 }
                 if (a.bias) {
@@ -1180,7 +1195,7 @@ bool plan_split(int R, int H, int V, bool gumbel, SplitPlan *p) {
     while (p->alloc_cols < p->N) p->alloc_cols <<= 1;
     p->ncl = (V + kTileM - 1) / kTileM;
     const void *kernel = split_kernel(gumbel, p->N);
-    for (int ck : {4, 8, 2}) {
+    for (int ck : {4, 8, 2}) {  // each at most kSplitMaxCK
         if (H % (kTileK * ck) != 0) continue;
         const int kch = H / kTileK / ck;
         const int RS = kTileM / ck;
