@@ -33,8 +33,11 @@ __global__ void __launch_bounds__(128)
 kv_append_kernel(const int32_t *__restrict__ table, int max_blocks,
                  const int32_t *__restrict__ ctx_before, int q_len, int Hkv, int num_blocks,
                  int row_vecs, const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
-                 uint4 *__restrict__ k_pool, uint4 *__restrict__ v_pool, int32_t *err) {
-    pdl_wait_prerequisites();
+                 uint4 *__restrict__ k_pool, uint4 *__restrict__ v_pool, int32_t *err, int wait_last) {
+    // wait_last: the inputs are not written by the kernel before (they come
+    // from pinned host memory); the append runs at once and waits for that
+    // kernel only before it ends, so the kernels after it still find both done
+    if (!wait_last) pdl_wait_prerequisites();
     pdl_allow_dependents();
     const int per_tensor = Hkv * row_vecs;
     const size_t src0 = static_cast<size_t>(blockIdx.x) * per_tensor;
@@ -53,12 +56,14 @@ kv_append_kernel(const int32_t *__restrict__ table, int max_blocks,
     const int cap = max_blocks * TTS_BLOCK_TOKENS;
     if (before < 0 || before >= cap || j >= cap - before) {
         if (threadIdx.x == 0) flag_error(err, TTS_ERRBIT_CTX_LEN);
+        if (wait_last) pdl_wait_prerequisites();
         return;
     }
     const int s = before + j;
     const int blk = table[static_cast<size_t>(b) * max_blocks + s / TTS_BLOCK_TOKENS];
     if (blk < 0 || blk >= num_blocks) {
         if (threadIdx.x == 0) flag_error(err, TTS_ERRBIT_BLOCK_ID);
+        if (wait_last) pdl_wait_prerequisites();
         return;
     }
     const int slot = s % TTS_BLOCK_TOKENS;
@@ -76,6 +81,7 @@ kv_append_kernel(const int32_t *__restrict__ table, int max_blocks,
         if (i < 2 * per_tensor) store(i, ahead[u]);
     }
     for (int i = threadIdx.x + kVecsAhead * blockDim.x; i < 2 * per_tensor; i += blockDim.x) store(i, load(i));
+    if (wait_last) pdl_wait_prerequisites();
 }
 
 // Byte of token slot s within a dimension's 16 value codes (slot order
@@ -279,7 +285,7 @@ int prepare_append(const tts_kv_cache *cache, const int32_t *d_block_table, int3
         if (!aligned16(cache->k_pool) || !aligned16(d_k_new) || !aligned16(d_v_new)) return TTS_ERR_INVALID;
         if (static_cast<long>(B) * q_len > 0x7FFFFFFFL) return TTS_ERR_INVALID;
         *out = AppendLaunch{cache, d_block_table, max_blocks_per_seq, d_ctx_before, B, q_len, d_k_new, d_v_new,
-                            d_err, false, 0, nullptr, {}};
+                            d_err, false, 0, nullptr, {}, false};
         return TTS_OK;
     }
     if (cache->dtype != TTS_F32 && cache->dtype != TTS_BF16) return TTS_ERR_UNSUPPORTED;
@@ -291,7 +297,7 @@ int prepare_append(const tts_kv_cache *cache, const int32_t *d_block_table, int3
         return TTS_ERR_INVALID;
     if (static_cast<long>(B) * q_len > 0x7FFFFFFFL) return TTS_ERR_INVALID;
     *out = AppendLaunch{cache, d_block_table, max_blocks_per_seq, d_ctx_before, B, q_len, d_k_new, d_v_new, d_err,
-                        false, 0, nullptr, {}};
+                        false, 0, nullptr, {}, false};
     return TTS_OK;
 }
 
@@ -350,7 +356,7 @@ int launch_append(const AppendLaunch &L, LaunchOpts o) {
                            static_cast<int>(L.cache->num_kv_heads), static_cast<int>(L.cache->num_blocks),
                            row_vecs, static_cast<const uint4 *>(L.k_new), static_cast<const uint4 *>(L.v_new),
                            static_cast<uint4 *>(L.cache->k_pool), static_cast<uint4 *>(L.cache->v_pool),
-                           L.err) != cudaSuccess) {
+                           L.err, L.wait_last ? 1 : 0) != cudaSuccess) {
         cudaGetLastError();
         return TTS_ERR_CUDA;
     }

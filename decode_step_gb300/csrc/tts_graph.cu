@@ -171,6 +171,29 @@ int capture_step(const tts_step_graph_desc *d, const CopySegs *segs, cudaGraph_t
                       d->num_q_heads, d->scale, d->causal, d->d_q, d->d_attn_out, d->d_attn_ws, d->attn_ws_bytes,
                       d->d_err, &at);
     if (st != TTS_OK) return st;
+    // Inputs read straight from the pinned buffer, which nothing writes during
+    // a launch: the plain append's table, positions and rows (so it need not
+    // wait for the copy kernel, only finish after it), and the attention's
+    // table and lengths (read before its programmatic-launch wait).  The query
+    // rows, read after the wait, stay on the device copy.
+    const auto pinned_alias = [d](const void *p) -> const void * {
+        const uint8_t *base = static_cast<const uint8_t *>(d->d_inputs), *q = static_cast<const uint8_t *>(p);
+        if (!p || q < base || q >= base + d->input_bytes) return nullptr;
+        return static_cast<const uint8_t *>(d->h_inputs) + (q - base);
+    };
+    const auto *h_table = static_cast<const int32_t *>(pinned_alias(d->d_block_table));
+    const auto *h_before = static_cast<const int32_t *>(pinned_alias(d->d_ctx_before));
+    const auto *h_lens = static_cast<const int32_t *>(pinned_alias(d->d_ctx_lens));
+    const void *h_k = pinned_alias(d->d_k_new), *h_v = pinned_alias(d->d_v_new);
+    if ((c->dtype == TTS_BF16 || c->dtype == TTS_F32) && d->rope_base == 0.0f && h_table && h_before && h_lens &&
+        h_k && h_v) {
+        st = prepare_append(c, h_table, d->max_blocks_per_seq, h_before, d->B, d->q_len, h_k, h_v, d->d_err, &ap);
+        if (st != TTS_OK) return st;
+        ap.wait_last = true;
+        st = prepare_attn(c, h_table, d->max_blocks_per_seq, h_lens, d->max_ctx_len, d->B, d->q_len, d->num_q_heads,
+                          d->scale, d->causal, d->d_q, d->d_attn_out, d->d_attn_ws, d->attn_ws_bytes, d->d_err, &at);
+        if (st != TTS_OK) return st;
+    }
     const long long H = static_cast<long long>(d->num_q_heads) * c->head_dim;
     if (H > 0x7FFFFFFF) return TTS_ERR_INVALID;
     // The tensor-core head's last CTA writes the ids and the boundary count to

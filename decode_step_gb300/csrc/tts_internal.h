@@ -103,6 +103,10 @@ struct AppendLaunch {
     int Hq;
     void *q;
     RopeFreqs freqs;
+    // bf16 / fp32 rows without rotation only: the inputs do not come from the
+    // kernel before (they are read from pinned host memory), so the append
+    // runs at once and waits for that kernel just before it ends
+    bool wait_last;
 };
 int prepare_append(const tts_kv_cache *cache, const int32_t *d_block_table, int32_t max_blocks_per_seq,
                    const int32_t *d_ctx_before, int32_t B, int32_t q_len, const void *d_k_new,
