@@ -115,24 +115,28 @@ __device__ bool p_grid_sync(const PersistArgs &a, unsigned int k) {
     __syncthreads();
     if (threadIdx.x == 0) {
         ok = 1;
-        __threadfence();
-        atomicAdd(a.bar, 1u);
+        // arrival with release semantics: the CTA's writes (ordered before it
+        // by the barrier above) are visible to whoever acquires the count
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.bar) : "memory");
         const unsigned int target = k * gridDim.x + (a.stall && k == 1 ? 1u : 0u);
         const long long t0 = clock64();
+        // poll the count alone (acquire); the abort word and the clock every
+        // 16th poll
         for (uint32_t n = 0;; ++n) {
             if (ld_acquire_u32(a.bar) >= target) break;
-            if (ld_acquire_u32(a.bar + 1) != 0u) {
-                ok = 0;
-                break;
-            }
-            if ((n & 63u) == 0 && clock64() - t0 > a.wait_limit) {
-                flag_error(a.err, TTS_ERRBIT_TIMEOUT);
-                atomicExch(a.bar + 1, 1u);
-                ok = 0;
-                break;
+            if ((n & 15u) == 15u) {
+                if (ld_acquire_u32(a.bar + 1) != 0u) {
+                    ok = 0;
+                    break;
+                }
+                if (clock64() - t0 > a.wait_limit) {
+                    flag_error(a.err, TTS_ERRBIT_TIMEOUT);
+                    atomicExch(a.bar + 1, 1u);
+                    ok = 0;
+                    break;
+                }
             }
         }
-        __threadfence();
     }
     __syncthreads();
     return ok != 0;
