@@ -288,30 +288,41 @@ __device__ __noinline__ void accept_walk(VerifyScalars *S, const float *st, int 
     }
 }
 
-struct DrawBest {
-    unsigned long long r, p;
-};
 // One thread's part of the draw over row x, entries v = v0, v0 + stride, ...:
-// the largest packed (key, index) of x / T + G (p) and, for a rejection (pdr:
-// the rejected row's draft probabilities), of log(residual) + G over entries
-// with a positive residual max(2^((x - m) k2) iz - p_d, 0) (r).
-__device__ __noinline__ DrawBest draw_part(const float *x, const float *pdr, const float *G, int V, int v0,
-                                           int stride, float m, float iz, float inv_t, float k2) {
+// the largest packed (key, index) of log(residual) + G over entries with a
+// positive residual max(2^((x - m) k2) iz - p_d, 0) when pdr (the rejected
+// row's draft probabilities) is given, else of x / T + G (0 if none).
+__device__ __noinline__ unsigned long long draw_part(const float *x, const float *pdr, const float *G, int V, int v0,
+                                                     int stride, float m, float iz, float inv_t, float k2) {
     constexpr float kLn2 = 0.69314718055994531f;
-    DrawBest best{0ull, 0ull};
-    for (int v = v0; v < V; v += stride) {
-        const float g = G[v], xv = x[v];
-        const unsigned long long kp = pack_argmax(xv * inv_t + g, v);
-        best.p = kp > best.p ? kp : best.p;
-        if (pdr) {
-            const float r = fmaxf(hw_ex2((xv - m) * k2) * iz - pdr[v], 0.0f);
+    unsigned long long best = 0ull;
+    if (pdr) {
+        for (int v = v0; v < V; v += stride) {
+            const float r = fmaxf(hw_ex2((x[v] - m) * k2) * iz - pdr[v], 0.0f);
             if (r > 0.0f) {
-                const unsigned long long kr = pack_argmax(kLn2 * hw_lg2(r) + g, v);
-                best.r = kr > best.r ? kr : best.r;
+                const unsigned long long k = pack_argmax(kLn2 * hw_lg2(r) + G[v], v);
+                best = k > best ? k : best;
             }
+        }
+    } else {
+        for (int v = v0; v < V; v += stride) {
+            const unsigned long long k = pack_argmax(x[v] * inv_t + G[v], v);
+            best = k > best ? k : best;
         }
     }
     return best;
+}
+
+// The block's largest of each thread's `best` into *dst (a shared word that
+// starts at 0); every thread returns after the block barrier.
+__device__ __forceinline__ void block_max_key(unsigned long long best, unsigned long long *dst) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long other = __shfl_xor_sync(kFull, best, o);
+        best = other > best ? other : best;
+    }
+    if ((threadIdx.x & 31) == 0 && best) atomicMax(dst, best);
+    __syncthreads();
 }
 
 // Staged kernel, one CTA per stream.  The stream's rows arrive by bulk copies
@@ -384,8 +395,9 @@ spec_verify_staged_kernel(const float *__restrict__ tl, const float *__restrict_
         }
         const int vw = V < 64 ? V : 64;
         warp_row_part(G, vw, 0, 32, k2, &scratch.warm_m, &scratch.warm_s);
-        const DrawBest w = draw_part(G, G, G, vw, lane, 32, 0.0f, 1.0f, inv_t, k2);
-        if (lane == 0) scratch.best = w.r ^ w.p;
+        const unsigned long long wr = draw_part(G, G, G, vw, lane, 32, 0.0f, 1.0f, inv_t, k2);
+        const unsigned long long wp = draw_part(G, nullptr, G, vw, lane, 32, 0.0f, 1.0f, inv_t, k2);
+        if (lane == 0) scratch.best = wr ^ wp;
     } else if (warp == kAcceptWarp) {
         if (lane < K) {
             const int d = dt[static_cast<size_t>(b) * K + lane];
@@ -454,28 +466,22 @@ spec_verify_staged_kernel(const float *__restrict__ tl, const float *__restrict_
     }
 
     // ---- the replacement draw (rejection at row `reject`) or the bonus draw
-    // (row K), in one pass.  Rejection: key log(residual) + G over entries with
-    // a positive residual, and alongside it x / T + G (the argmax of
-    // log p_t + G, as p_t is exp(x / T) up to a common factor) for the case of
-    // a residual that is zero everywhere, where the draw falls back to p_t.
-    // Bonus: x / T + G.
+    // (row K).  Rejection: key log(residual) + G over entries with a positive
+    // residual; only if there is none (a residual that is zero everywhere) a
+    // second pass with x / T + G, the argmax of log p_t + G (p_t is exp(x / T)
+    // up to a common factor): the draw falls back to p_t.  Bonus: x / T + G.
     const int row = reject >= 0 ? reject : K;
-    DrawBest best = draw_part(st + static_cast<size_t>(row) * V,
-                              reject >= 0 ? sdr + static_cast<size_t>(row) * V : nullptr, G, V, threadIdx.x,
-                              blockDim.x, reject >= 0 ? S.row_max[row] : 0.0f,
-                              reject >= 0 ? 1.0f / S.row_sum[row] : 1.0f, inv_t, k2);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long a = __shfl_xor_sync(kFull, best.r, o);
-        const unsigned long long c = __shfl_xor_sync(kFull, best.p, o);
-        best.r = a > best.r ? a : best.r;
-        best.p = c > best.p ? c : best.p;
+    const float *x = st + static_cast<size_t>(row) * V;
+    if (reject >= 0) {
+        block_max_key(draw_part(x, sdr + static_cast<size_t>(row) * V, G, V, threadIdx.x, blockDim.x,
+                                S.row_max[row], 1.0f / S.row_sum[row], inv_t, k2),
+                      &S.best);
+        // a residual that is zero everywhere (p_t = p_d up to rounding): p_t
+        if (S.best == 0ull)
+            block_max_key(draw_part(x, nullptr, G, V, threadIdx.x, blockDim.x, 0.0f, 1.0f, inv_t, k2), &S.best_p);
+    } else {
+        block_max_key(draw_part(x, nullptr, G, V, threadIdx.x, blockDim.x, 0.0f, 1.0f, inv_t, k2), &S.best_p);
     }
-    if (lane == 0) {
-        if (best.r) atomicMax(&S.best, best.r);
-        if (best.p) atomicMax(&S.best_p, best.p);
-    }
-    __syncthreads();
     if (threadIdx.x == 0) {
         const unsigned long long pick = reject >= 0 && S.best ? S.best : S.best_p;
         n_accepted[b] = S.accepted;

@@ -171,6 +171,29 @@ def test_spec_verify_shapes(orc, B, K, V):
         assert int(err.item()) == 0
 
 
+@pytest.mark.parametrize("V", [4097, 16385])
+def test_spec_verify_zero_residual_draws_from_target(orc, V):
+    """A residual that is zero everywhere: draft "probabilities" of 1 for every
+    entry make max(p_t - p_d, 0) vanish, so a rejection draws from p_t itself
+    (the fallback of the residual draw), in the staged kernel (V = 4097) and
+    the streaming one (V = 16385); compared with the oracle."""
+    B, K = 16, 4
+    tl, _, dt, vseed, vstep = _verify_case(B, K, V, 4242 + V)
+    dp = np.ones((B, K, V), dtype=np.float32)
+    T = 0.7
+    n_acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bd.tts_spec_verify(dev(tl), dev(dp), dev(dt), T, dev(vseed), dev(vstep), n_acc, nxt, err=err)
+    torch.cuda.synchronize()
+    ref = orc.spec_verify(tl, dp, dt, T, vseed, vstep)
+    assert (ref["n_accepted"] < K).all(), "every stream should reject somewhere (p_d = 1)"
+    tie = (ref["gap_accept"] < NEAR_TIE) | (ref["gap_resid"] < NEAR_TIE)
+    bad = (host(n_acc) != ref["n_accepted"]) | (host(nxt) != ref["next_token"])
+    assert not (bad & ~tie).any(), f"differs at streams {np.nonzero(bad & ~tie)[0]}"
+    assert (host(nxt) >= 0).all() and int(err.item()) == 0
+
+
 def test_spec_verify_bad_token():
     """A draft token outside the vocabulary where the walk reaches it stops the
     walk there with no draw and sets the token error bit."""
