@@ -83,6 +83,7 @@ _SIGNATURES = {
                                        _vp, _vp]),
     "tts_step_graph_create": (ctypes.c_int, [ctypes.POINTER(StepGraphDesc), ctypes.POINTER(_vp)]),
     "tts_step_graph_launch": (ctypes.c_int, [_vp, _vp]),
+    "tts_step_graph_run": (ctypes.c_int, [_vp, _vp]),
     "tts_step_graph_destroy": (None, [_vp]),
     "tts_step_graph_set_create": (ctypes.c_int, [ctypes.POINTER(StepGraphDesc), _vp, _i32, _vp, _vp, _i32,
                                                  ctypes.POINTER(_vp)]),

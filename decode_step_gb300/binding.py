@@ -371,6 +371,12 @@ class StepGraph:
             raise ValueError("graph destroyed")
         check("tts_step_graph_launch", lib().tts_step_graph_launch(self._handle, _stream(stream)))
 
+    def run(self, stream=None) -> None:
+        """tts_step_graph_run: launch and return once the ids are in host memory."""
+        if self._handle is None:
+            raise ValueError("graph destroyed")
+        check("tts_step_graph_run", lib().tts_step_graph_run(self._handle, _stream(stream)))
+
     def close(self) -> None:
         if getattr(self, "_handle", None) is not None:
             lib().tts_step_graph_destroy(self._handle)

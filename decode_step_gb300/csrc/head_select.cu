@@ -61,10 +61,12 @@ HeadWs head_ws(void *ws, int R) {
 // after their atomics.  The last of them converts keys to ids and resets the
 // workspace.  No waiting.
 // ids_host / count_host (nullable, pinned host memory): the ids again and the
-// number of rows whose id is `boundary`, written by the last CTA.
+// number of rows whose id is `boundary`, written by the last CTA; then, with
+// seq_host, the launch's number (*seq_dev incremented) to seq_host, after a
+// system-scope fence, so a host that sees the number sees the ids.
 __device__ void finish_selection(const HeadWs &ws, int R, int32_t *ids, float *best, int *flag,
                                  unsigned int publishers, int32_t *ids_host = nullptr, int32_t *count_host = nullptr,
-                                 int32_t boundary = -1) {
+                                 int32_t boundary = -1, int32_t *seq_host = nullptr, uint32_t *seq_dev = nullptr) {
     // The barrier orders every thread's key atomics before thread 0's ticket,
     // whose release (cumulative) publishes them all.
     __syncthreads();
@@ -99,6 +101,14 @@ __device__ void finish_selection(const HeadWs &ws, int R, int32_t *ids, float *b
         __syncthreads();
         if (threadIdx.x == 0) *count_host = *flag;
     }
+    if (seq_host) {
+        __syncthreads();  // every id and the count written before the number
+        if (threadIdx.x == 0) {
+            const unsigned int seq = atomicAdd(seq_dev, 1u) + 1u;
+            __threadfence_system();
+            *reinterpret_cast<volatile int32_t *>(seq_host) = static_cast<int32_t>(seq);
+        }
+    }
 }
 
 // Head modes beyond the public TTS_ARGMAX / TTS_GUMBEL: the first layer of
@@ -128,6 +138,8 @@ struct HeadArgs {
     __nv_bfloat16 *seg_out[3];  //   written to seg_out[j] [R][seg_start[j + 1] - seg_start[j]]
     int32_t *ids_host;        // selection: the ids again, in pinned host memory (nullable)
     int32_t *count_host;      //   and the count of rows choosing id V - 1 (nullable)
+    int32_t *seq_host;        //   and then the launch's number (nullable; with seq_dev)
+    uint32_t *seq_dev;
 };
 
 // Mish(x) = x tanh(ln(1 + e^x)) in fp32 (past x = 20, ln(1 + e^x) rounds to x).
@@ -794,7 +806,7 @@ head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant_
         if (r0 + cn < a.R && k) atomicMax(a.ws.keys + r0 + cn, k);
     }
     finish_selection(a.ws, a.R, a.ids, a.best, flag, (gridDim.x / CK) * gridDim.y, a.ids_host, a.count_host,
-                     a.V - 1);
+                     a.V - 1, a.seq_host, a.seq_dev);
 }
 
 // ------------------------------------------- split build (narrow batches)
@@ -1087,7 +1099,8 @@ head_split_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     }
     // this CTA's outgoing copies have finished reading its staging rows
     if (warp < 4 && lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-    finish_selection(a.ws, a.R, a.ids, a.best, flag, gridDim.x, a.ids_host, a.count_host, a.V - 1);
+    finish_selection(a.ws, a.R, a.ids, a.best, flag, gridDim.x, a.ids_host, a.count_host, a.V - 1, a.seq_host,
+                     a.seq_dev);
 }
 
 // ------------------------------------------------------------- host side
@@ -1253,8 +1266,9 @@ int prepare_head_ex(const void *d_h, const void *d_W, int32_t dtype, int32_t R, 
         return TTS_ERR_INVALID;
     if (x.n_tail < 0 || x.n_tail > 32 || x.n_tail > V) return TTS_ERR_INVALID;
     if (dtype != TTS_F32 && dtype != TTS_BF16) return TTS_ERR_UNSUPPORTED;
-    if (dtype == TTS_F32 && (x.bias || x.tail || expand || x.pos || x.ids_host || x.count_host))
+    if (dtype == TTS_F32 && (x.bias || x.tail || expand || x.pos || x.ids_host || x.count_host || x.seq_host))
         return TTS_ERR_UNSUPPORTED;
+    if ((x.seq_host != nullptr) != (x.seq_dev != nullptr) || (x.seq_host && !x.ids_host)) return TTS_ERR_INVALID;
     if (linear) {
         // up to three outputs over consecutive feature ranges, 8 features per store
         if (x.seg_start[0] != 0 || x.seg_start[3] != V || V % 8 != 0) return TTS_ERR_INVALID;
@@ -1280,6 +1294,8 @@ int prepare_head_ex(const void *d_h, const void *d_W, int32_t dtype, int32_t R, 
     a.pos = x.pos;
     a.ids_host = x.ids_host;
     a.count_host = x.count_host;
+    a.seq_host = x.seq_host;
+    a.seq_dev = x.seq_dev;
     for (int j = 0; j < 4; ++j) a.seg_start[j] = x.seg_start[j];
     for (int j = 0; j < 3; ++j) a.seg_out[j] = static_cast<__nv_bfloat16 *>(x.seg_out[j]);
     st->dtype = dtype;

@@ -14,6 +14,9 @@
 // that to a small kernel).
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <chrono>
+
 #include <new>
 
 #include "tts_common.cuh"
@@ -136,6 +139,12 @@ bool pinned_host(const void *p) {
 struct tts_step_graph {
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
+    // launch numbering for tts_step_graph_run (single graphs whose head
+    // writes the ids to host memory): the head's last CTA increments d_seq
+    // and writes it to the pinned h_seq after the ids
+    int32_t *h_seq = nullptr;
+    uint32_t *d_seq = nullptr;
+    uint32_t launches = 0;
 };
 
 namespace tts {
@@ -145,7 +154,7 @@ namespace {
 // step and instantiates it.  With segs, the input copy moves those regions;
 // without, all of input_bytes.
 int capture_step(const tts_step_graph_desc *d, const CopySegs *segs, cudaGraph_t *graph_out,
-                 cudaGraphExec_t *exec_out) {
+                 cudaGraphExec_t *exec_out, int32_t *h_seq = nullptr, uint32_t *d_seq = nullptr) {
     *graph_out = nullptr;
     *exec_out = nullptr;
     if (!d->cache || d->B < 1) return TTS_ERR_INVALID;
@@ -203,6 +212,12 @@ int capture_step(const tts_step_graph_desc *d, const CopySegs *segs, cudaGraph_t
     if (host_ids) {
         hx.ids_host = d->h_ids;
         hx.count_host = d->h_boundary_count;
+        // the launch number marks the ids as complete only when the head is
+        // the step's last kernel (no verify stage after it)
+        if (!d->d_n_accepted) {
+            hx.seq_host = h_seq;
+            hx.seq_dev = d_seq;
+        }
     }
     st = prepare_head_ex(d->d_attn_out, d->d_W, c->dtype == TTS_FP8_E4M3 ? TTS_BF16 : c->dtype,
                          static_cast<int32_t>(R), static_cast<int32_t>(H), d->V, d->mode, d->temperature, d->d_seed,
@@ -291,9 +306,25 @@ extern "C" int tts_step_graph_create(const tts_step_graph_desc *d, tts_step_grap
     *out = nullptr;
     tts_step_graph *g = new (std::nothrow) tts_step_graph();
     if (!g) return TTS_ERR_CUDA;
-    const int st = capture_step(d, nullptr, &g->graph, &g->exec);
+    // the launch counter (device, zeroed here) and its host copy (pinned);
+    // without them (allocation failed) tts_step_graph_run synchronises the
+    // stream instead, and the descriptor's checks below decide the status
+    const uint32_t zero = 0;
+    if (cudaMalloc(reinterpret_cast<void **>(&g->d_seq), sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemcpy(g->d_seq, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaHostAlloc(reinterpret_cast<void **>(&g->h_seq), sizeof(int32_t), cudaHostAllocDefault) != cudaSuccess) {
+        cudaGetLastError();
+        if (g->d_seq) cudaFree(g->d_seq);
+        if (g->h_seq) cudaFreeHost(g->h_seq);
+        cudaGetLastError();
+        g->d_seq = nullptr;
+        g->h_seq = nullptr;
+    } else {
+        *g->h_seq = 0;
+    }
+    const int st = capture_step(d, nullptr, &g->graph, &g->exec, g->h_seq, g->d_seq);
     if (st != TTS_OK) {
-        delete g;
+        tts_step_graph_destroy(g);
         return st;
     }
     *out = g;
@@ -306,6 +337,39 @@ extern "C" int tts_step_graph_launch(tts_step_graph *g, void *stream) {
         cudaGetLastError();
         return TTS_ERR_CUDA;
     }
+    ++g->launches;
+    return TTS_OK;
+}
+
+extern "C" int tts_step_graph_run(tts_step_graph *g, void *stream) {
+    const int st = tts_step_graph_launch(g, stream);
+    if (st != TTS_OK) return st;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // A graph with a verify stage or an fp32 head has no launch number: wait
+    // for the stream.  Otherwise spin on the pinned number (a plain host
+    // read; the device's system-scope fence orders the ids before it), for
+    // at most a second before falling back to the stream (a failed launch
+    // never writes the number; the stream then reports the error).
+    bool seen = false;
+    if (g->h_seq && g->launches != 0) {
+        const volatile int32_t *w = g->h_seq;
+        const auto t0 = std::chrono::steady_clock::now();
+        for (uint32_t n = 0;; ++n) {
+            if (static_cast<int32_t>(static_cast<uint32_t>(*w) - g->launches) >= 0) {
+                seen = true;
+                break;
+            }
+            if ((n & 1023u) == 0 && std::chrono::steady_clock::now() - t0 > std::chrono::seconds(1)) break;
+        }
+    }
+    if (seen) {
+        std::atomic_thread_fence(std::memory_order_acquire);
+        return TTS_OK;
+    }
+    if (cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return TTS_ERR_CUDA;
+    }
     return TTS_OK;
 }
 
@@ -313,6 +377,8 @@ extern "C" void tts_step_graph_destroy(tts_step_graph *g) {
     if (!g) return;
     if (g->exec) cudaGraphExecDestroy(g->exec);
     if (g->graph) cudaGraphDestroy(g->graph);
+    if (g->d_seq) cudaFree(g->d_seq);
+    if (g->h_seq) cudaFreeHost(g->h_seq);
     delete g;
 }
 

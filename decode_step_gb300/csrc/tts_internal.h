@@ -152,6 +152,10 @@ struct HeadExtras {
     void *seg_out[3] = {nullptr, nullptr, nullptr};
     int32_t *ids_host = nullptr;    // the ids again, in pinned host memory
     int32_t *count_host = nullptr;  // rows whose id is the boundary V - 1
+    // then the launch's number (*seq_dev incremented) in pinned host memory,
+    // written after the ids are visible to the host (both or neither)
+    int32_t *seq_host = nullptr;
+    uint32_t *seq_dev = nullptr;
 };
 int prepare_head_ex(const void *d_h, const void *d_W, int32_t dtype, int32_t R, int32_t H, int32_t V,
                     int32_t mode, float temperature, const uint64_t *d_seed, const uint64_t *d_step,

@@ -134,9 +134,10 @@ class GraphedStep:
         return int(self.boundary_host.item())
 
     def __call__(self) -> torch.Tensor:
-        """Runs the captured step and returns the (pinned, host) ids once they are there."""
-        self.graph.launch(self.stream)
-        self.stream.synchronize()
+        """Runs the captured step and returns the (pinned, host) ids once they
+        are there (tts_step_graph_run: a spin on the launch number the head
+        writes after them, or a stream synchronisation)."""
+        self.graph.run(self.stream)
         return self.ids_host
 
 

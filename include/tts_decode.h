@@ -435,6 +435,18 @@ int tts_step_graph_create(const tts_step_graph_desc *desc, tts_step_graph **out)
 /* Launches the captured step on `stream` (asynchronous). */
 int tts_step_graph_launch(tts_step_graph *graph, void *stream);
 
+/* Launches the captured step on `stream` and returns once its ids (and the
+ * boundary count) are in the pinned host buffers: a serving loop's call.  For
+ * a bf16 / FP8 step without a verify stage, the head's last CTA writes a
+ * launch number to pinned host memory after the ids (system-scope fence
+ * between), and this call spins on that number instead of synchronising the
+ * stream (at most a second, then it synchronises the stream, which also
+ * reports a failed launch); the launch's last CTAs may still be exiting when
+ * it returns (later work on the stream is ordered after them as usual).
+ * Other steps: launch, then cudaStreamSynchronize.  TTS_ERR_CUDA on a launch
+ * or stream error. */
+int tts_step_graph_run(tts_step_graph *graph, void *stream);
+
 /* Frees the graph (no GPU work of it may still be pending).  NULL is a no-op. */
 void tts_step_graph_destroy(tts_step_graph *graph);
 

@@ -491,6 +491,31 @@ def test_graphed_step_matches_direct_step(orc, parity):
     assert int(step.err.item()) == 0
 
 
+def test_graphed_step_run_returns_each_launchs_ids():
+    """tts_step_graph_run returns once that launch's ids are in host memory:
+    the query rows alternate between two sets, the ids are copied the moment
+    the call returns, and the launch numbering starts past two asynchronous
+    launches."""
+    inp = wl.make_inputs(wl.custom(3, B=24), with_verify=False)
+    w = inp["workload"]
+    u = Uploaded(inp)
+    cache = bd.KVCache(u.k_pool, u.v_pool)
+    step = DecodeStep(cache, u.W, w.Hq, w.B, w.ctx_hi)
+    qs = [u.q, torch.randn(u.q.shape, device="cuda").to(u.q.dtype)]
+    want = [step(u.table, u.ctx_before, u.ctx_lens, q, u.k_new, u.v_new).cpu().clone() for q in qs]
+    assert not torch.equal(want[0], want[1])
+    g = GraphedStep(step, {"block_table": u.table, "ctx_before": u.ctx_before, "ctx_lens": u.ctx_lens,
+                           "q": u.q, "k_new": u.k_new, "v_new": u.v_new})
+    g.graph.launch(g.stream)
+    g.graph.launch(g.stream)
+    g.stream.synchronize()
+    for i in range(20):
+        g.host["q"].copy_(qs[i & 1].cpu())
+        g.ids_host.fill_(-7)
+        assert torch.equal(g().clone(), want[i & 1]), f"run {i} returned before its ids"
+    assert int(step.err.item()) == 0
+
+
 def test_graphed_step_boundary_count():
     """The captured step counts the rows whose id is the boundary token V - 1
     on the device: a boundary row of W aligned with half the streams'
