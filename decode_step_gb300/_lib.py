@@ -88,6 +88,7 @@ _SIGNATURES = {
     "tts_step_graph_set_create": (ctypes.c_int, [ctypes.POINTER(StepGraphDesc), _vp, _i32, _vp, _vp, _i32,
                                                  ctypes.POINTER(_vp)]),
     "tts_step_graph_set_launch": (ctypes.c_int, [_vp, _i32, _vp, _vp]),
+    "tts_step_graph_set_run": (ctypes.c_int, [_vp, _i32, _vp, _vp]),
     "tts_step_graph_set_destroy": (None, [_vp]),
     "tts_code_predictor_workspace_size": (_sz, [_i32] * 7),
     "tts_code_predictor_run": (ctypes.c_int, [ctypes.POINTER(CodePredictorDesc), _vp]),

@@ -426,6 +426,16 @@ class StepGraphSet:
               lib().tts_step_graph_set_launch(self._handle, int(n_streams), ctypes.byref(chosen), _stream(stream)))
         return chosen.value
 
+    def run(self, n_streams: int, stream=None) -> int:
+        """tts_step_graph_set_run: launch and return once the ids are in host
+        memory; returns the size whose graph ran."""
+        if self._handle is None:
+            raise ValueError("graph set destroyed")
+        chosen = ctypes.c_int32(0)
+        check("tts_step_graph_set_run",
+              lib().tts_step_graph_set_run(self._handle, int(n_streams), ctypes.byref(chosen), _stream(stream)))
+        return chosen.value
+
     def close(self) -> None:
         if getattr(self, "_handle", None) is not None:
             lib().tts_step_graph_set_destroy(self._handle)

@@ -145,6 +145,7 @@ struct tts_step_graph {
     int32_t *h_seq = nullptr;
     uint32_t *d_seq = nullptr;
     uint32_t launches = 0;
+    bool numbered = false;  // the head writes the number (see capture_step)
 };
 
 namespace tts {
@@ -154,7 +155,9 @@ namespace {
 // step and instantiates it.  With segs, the input copy moves those regions;
 // without, all of input_bytes.
 int capture_step(const tts_step_graph_desc *d, const CopySegs *segs, cudaGraph_t *graph_out,
-                 cudaGraphExec_t *exec_out, int32_t *h_seq = nullptr, uint32_t *d_seq = nullptr) {
+                 cudaGraphExec_t *exec_out, int32_t *h_seq = nullptr, uint32_t *d_seq = nullptr,
+                 bool *numbered = nullptr) {
+    if (numbered) *numbered = false;
     *graph_out = nullptr;
     *exec_out = nullptr;
     if (!d->cache || d->B < 1) return TTS_ERR_INVALID;
@@ -214,9 +217,10 @@ int capture_step(const tts_step_graph_desc *d, const CopySegs *segs, cudaGraph_t
         hx.count_host = d->h_boundary_count;
         // the launch number marks the ids as complete only when the head is
         // the step's last kernel (no verify stage after it)
-        if (!d->d_n_accepted) {
+        if (!d->d_n_accepted && h_seq && d_seq) {
             hx.seq_host = h_seq;
             hx.seq_dev = d_seq;
+            if (numbered) *numbered = true;
         }
     }
     st = prepare_head_ex(d->d_attn_out, d->d_W, c->dtype == TTS_FP8_E4M3 ? TTS_BF16 : c->dtype,
@@ -300,29 +304,71 @@ int capture_step(const tts_step_graph_desc *d, const CopySegs *segs, cudaGraph_t
 }  // namespace
 }  // namespace tts
 
+namespace tts {
+namespace {
+
+// Launch-number pair of a graph or a graph set: a device counter (zeroed) and
+// its pinned host copy, both or neither (an allocation failure leaves the
+// caller to synchronise the stream).
+void alloc_seq(int32_t **h_seq, uint32_t **d_seq) {
+    const uint32_t zero = 0;
+    *h_seq = nullptr;
+    *d_seq = nullptr;
+    if (cudaMalloc(reinterpret_cast<void **>(d_seq), sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemcpy(*d_seq, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaHostAlloc(reinterpret_cast<void **>(h_seq), sizeof(int32_t), cudaHostAllocDefault) != cudaSuccess) {
+        cudaGetLastError();
+        if (*d_seq) cudaFree(*d_seq);
+        if (*h_seq) cudaFreeHost(*h_seq);
+        cudaGetLastError();
+        *h_seq = nullptr;
+        *d_seq = nullptr;
+        return;
+    }
+    **h_seq = 0;
+}
+
+void free_seq(int32_t *h_seq, uint32_t *d_seq) {
+    if (d_seq) cudaFree(d_seq);
+    if (h_seq) cudaFreeHost(h_seq);
+}
+
+// Waits until launch number `launches` has written its ids: a spin on the
+// pinned number (a plain host read; the device's system-scope fence orders
+// the ids before it), for at most a second before synchronising the stream
+// (a failed launch never writes the number; the stream then reports the
+// error).  Without a number (h_seq null, or a step whose head is not its last
+// kernel: the number never moves) the stream is synchronised.
+int wait_for_launch(const int32_t *h_seq, bool numbered, uint32_t launches, cudaStream_t s) {
+    if (h_seq && numbered) {
+        const volatile int32_t *w = h_seq;
+        const auto t0 = std::chrono::steady_clock::now();
+        for (uint32_t n = 0;; ++n) {
+            if (static_cast<int32_t>(static_cast<uint32_t>(*w) - launches) >= 0) {
+                std::atomic_thread_fence(std::memory_order_acquire);
+                return TTS_OK;
+            }
+            if ((n & 1023u) == 0 && std::chrono::steady_clock::now() - t0 > std::chrono::seconds(1)) break;
+        }
+    }
+    if (cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return TTS_ERR_CUDA;
+    }
+    return TTS_OK;
+}
+
+}  // namespace
+}  // namespace tts
+
 extern "C" int tts_step_graph_create(const tts_step_graph_desc *d, tts_step_graph **out) {
     using namespace tts;
     if (!d || !out) return TTS_ERR_INVALID;
     *out = nullptr;
     tts_step_graph *g = new (std::nothrow) tts_step_graph();
     if (!g) return TTS_ERR_CUDA;
-    // the launch counter (device, zeroed here) and its host copy (pinned);
-    // without them (allocation failed) tts_step_graph_run synchronises the
-    // stream instead, and the descriptor's checks below decide the status
-    const uint32_t zero = 0;
-    if (cudaMalloc(reinterpret_cast<void **>(&g->d_seq), sizeof(uint32_t)) != cudaSuccess ||
-        cudaMemcpy(g->d_seq, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess ||
-        cudaHostAlloc(reinterpret_cast<void **>(&g->h_seq), sizeof(int32_t), cudaHostAllocDefault) != cudaSuccess) {
-        cudaGetLastError();
-        if (g->d_seq) cudaFree(g->d_seq);
-        if (g->h_seq) cudaFreeHost(g->h_seq);
-        cudaGetLastError();
-        g->d_seq = nullptr;
-        g->h_seq = nullptr;
-    } else {
-        *g->h_seq = 0;
-    }
-    const int st = capture_step(d, nullptr, &g->graph, &g->exec, g->h_seq, g->d_seq);
+    tts::alloc_seq(&g->h_seq, &g->d_seq);
+    const int st = capture_step(d, nullptr, &g->graph, &g->exec, g->h_seq, g->d_seq, &g->numbered);
     if (st != TTS_OK) {
         tts_step_graph_destroy(g);
         return st;
@@ -344,41 +390,14 @@ extern "C" int tts_step_graph_launch(tts_step_graph *g, void *stream) {
 extern "C" int tts_step_graph_run(tts_step_graph *g, void *stream) {
     const int st = tts_step_graph_launch(g, stream);
     if (st != TTS_OK) return st;
-    const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // A graph with a verify stage or an fp32 head has no launch number: wait
-    // for the stream.  Otherwise spin on the pinned number (a plain host
-    // read; the device's system-scope fence orders the ids before it), for
-    // at most a second before falling back to the stream (a failed launch
-    // never writes the number; the stream then reports the error).
-    bool seen = false;
-    if (g->h_seq && g->launches != 0) {
-        const volatile int32_t *w = g->h_seq;
-        const auto t0 = std::chrono::steady_clock::now();
-        for (uint32_t n = 0;; ++n) {
-            if (static_cast<int32_t>(static_cast<uint32_t>(*w) - g->launches) >= 0) {
-                seen = true;
-                break;
-            }
-            if ((n & 1023u) == 0 && std::chrono::steady_clock::now() - t0 > std::chrono::seconds(1)) break;
-        }
-    }
-    if (seen) {
-        std::atomic_thread_fence(std::memory_order_acquire);
-        return TTS_OK;
-    }
-    if (cudaStreamSynchronize(s) != cudaSuccess) {
-        cudaGetLastError();
-        return TTS_ERR_CUDA;
-    }
-    return TTS_OK;
+    return tts::wait_for_launch(g->h_seq, g->numbered, g->launches, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" void tts_step_graph_destroy(tts_step_graph *g) {
     if (!g) return;
     if (g->exec) cudaGraphExecDestroy(g->exec);
     if (g->graph) cudaGraphDestroy(g->graph);
-    if (g->d_seq) cudaFree(g->d_seq);
-    if (g->h_seq) cudaFreeHost(g->h_seq);
+    tts::free_seq(g->h_seq, g->d_seq);
     delete g;
 }
 
@@ -388,6 +407,11 @@ struct tts_step_graph_set {
     int n = 0;
     int32_t sizes[TTS_GRAPH_SET_MAX];
     tts_step_graph graphs[TTS_GRAPH_SET_MAX];
+    // one launch-number pair shared by every size (launches on one stream)
+    int32_t *h_seq = nullptr;
+    uint32_t *d_seq = nullptr;
+    uint32_t launches = 0;
+    bool numbered = false;
 };
 
 extern "C" int tts_step_graph_set_create(const tts_step_graph_desc *d, const int32_t *sizes, int32_t n_sizes,
@@ -409,6 +433,7 @@ extern "C" int tts_step_graph_set_create(const tts_step_graph_desc *d, const int
     }
     tts_step_graph_set *set = new (std::nothrow) tts_step_graph_set();
     if (!set) return TTS_ERR_CUDA;
+    alloc_seq(&set->h_seq, &set->d_seq);
     for (int k = 0; k < n_sizes; ++k) {
         tts_step_graph_desc dk = *d;
         dk.B = sizes[k];
@@ -418,7 +443,8 @@ extern "C" int tts_step_graph_set_create(const tts_step_graph_desc *d, const int
             segs.off[i] = seg_offset[i];
             segs.bytes[i] = seg_row_bytes[i] * static_cast<size_t>(sizes[k]);
         }
-        const int st = capture_step(&dk, &segs, &set->graphs[k].graph, &set->graphs[k].exec);
+        const int st = capture_step(&dk, &segs, &set->graphs[k].graph, &set->graphs[k].exec, set->h_seq, set->d_seq,
+                                    &set->numbered);
         if (st != TTS_OK) {
             tts_step_graph_set_destroy(set);
             return st;
@@ -437,7 +463,15 @@ extern "C" int tts_step_graph_set_launch(tts_step_graph_set *set, int32_t n_stre
     while (k < set->n && set->sizes[k] < n_streams) ++k;
     if (k == set->n) return TTS_ERR_INVALID;  // more streams than the largest size: split the cohort
     if (chosen_B) *chosen_B = set->sizes[k];
-    return tts_step_graph_launch(&set->graphs[k], stream);
+    const int st = tts_step_graph_launch(&set->graphs[k], stream);
+    if (st == TTS_OK) ++set->launches;
+    return st;
+}
+
+extern "C" int tts_step_graph_set_run(tts_step_graph_set *set, int32_t n_streams, int32_t *chosen_B, void *stream) {
+    const int st = tts_step_graph_set_launch(set, n_streams, chosen_B, stream);
+    if (st != TTS_OK) return st;
+    return tts::wait_for_launch(set->h_seq, set->numbered, set->launches, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" void tts_step_graph_set_destroy(tts_step_graph_set *set) {
@@ -446,5 +480,6 @@ extern "C" void tts_step_graph_set_destroy(tts_step_graph_set *set) {
         if (set->graphs[k].exec) cudaGraphExecDestroy(set->graphs[k].exec);
         if (set->graphs[k].graph) cudaGraphDestroy(set->graphs[k].graph);
     }
+    tts::free_seq(set->h_seq, set->d_seq);
     delete set;
 }

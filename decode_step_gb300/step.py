@@ -226,9 +226,8 @@ class GraphedStepSet:
         if b is None:
             raise ValueError(f"{n} streams exceed the largest captured size {self.sizes[-1]}")
         self._pad(n, b)
-        chosen = self.graphs.launch(n, self.stream)
+        chosen = self.graphs.run(n, self.stream)
         assert chosen == b
-        self.stream.synchronize()
         return self.ids_host[:n * self.step.q_len]
 
     def step_streams(self, arrays: dict) -> torch.Tensor:

@@ -478,6 +478,11 @@ int tts_step_graph_set_create(const tts_step_graph_desc *desc, const int32_t *si
  * TTS_ERR_INVALID if n_streams exceeds the largest size (split the cohort). */
 int tts_step_graph_set_launch(tts_step_graph_set *set, int32_t n_streams, int32_t *chosen_B, void *stream);
 
+/* tts_step_graph_set_launch, then the wait of tts_step_graph_run: returns
+ * once the launch's ids are in the pinned host buffers (one launch number is
+ * shared by every size of the set, so launch a set on one stream at a time). */
+int tts_step_graph_set_run(tts_step_graph_set *set, int32_t n_streams, int32_t *chosen_B, void *stream);
+
 /* Frees every graph of the set (no GPU work of it may still be pending). */
 void tts_step_graph_set_destroy(tts_step_graph_set *set);
 
