@@ -197,8 +197,9 @@ int capture_step(const tts_step_graph_desc *d, const CopySegs *segs, cudaGraph_t
     const auto *h_before = static_cast<const int32_t *>(pinned_alias(d->d_ctx_before));
     const auto *h_lens = static_cast<const int32_t *>(pinned_alias(d->d_ctx_lens));
     const void *h_k = pinned_alias(d->d_k_new), *h_v = pinned_alias(d->d_v_new);
-    if ((c->dtype == TTS_BF16 || c->dtype == TTS_F32) && d->rope_base == 0.0f && h_table && h_before && h_lens &&
-        h_k && h_v) {
+    const bool aliased = (c->dtype == TTS_BF16 || c->dtype == TTS_F32) && d->rope_base == 0.0f && h_table &&
+                         h_before && h_lens && h_k && h_v;
+    if (aliased) {
         st = prepare_append(c, h_table, d->max_blocks_per_seq, h_before, d->B, d->q_len, h_k, h_v, d->d_err, &ap);
         if (st != TTS_OK) return st;
         ap.wait_last = true;
@@ -246,11 +247,62 @@ int capture_step(const tts_step_graph_desc *d, const CopySegs *segs, cudaGraph_t
         cudaGetLastError();
         return TTS_ERR_CUDA;
     }
+    // With the append's and the attention's inputs read from the pinned
+    // buffer, the copy kernel moves only what later kernels read from the
+    // device buffer: the query rows, the head's keys and mask, the verify
+    // stage's inputs (whichever lie in the buffer).  Regions it cannot move
+    // (unaligned, too many) keep the whole copy.
+    CopySegs trimmed{};
+    const CopySegs *copy_segs = segs;
+    if (aliased) {
+        const uint8_t *base = static_cast<const uint8_t *>(d->d_inputs);
+        const auto off_of = [base](const void *p) { return static_cast<size_t>(static_cast<const uint8_t *>(p) - base); };
+        const size_t drop[5] = {off_of(d->d_block_table), off_of(d->d_ctx_before), off_of(d->d_ctx_lens),
+                                off_of(d->d_k_new), off_of(d->d_v_new)};
+        const auto dropped = [&drop](size_t off) {
+            for (size_t x : drop)
+                if (x == off) return true;
+            return false;
+        };
+        if (segs) {
+            for (int i = 0; i < segs->n; ++i) {
+                if (dropped(segs->off[i])) continue;
+                trimmed.off[trimmed.n] = segs->off[i];
+                trimmed.bytes[trimmed.n] = segs->bytes[i];
+                ++trimmed.n;
+            }
+            copy_segs = &trimmed;
+        } else {
+            const size_t elem = c->dtype == TTS_F32 ? 4u : 2u;
+            const size_t K = d->q_len > 1 ? static_cast<size_t>(d->q_len - 1) : 0u;
+            const size_t B = static_cast<size_t>(d->B), Rs = static_cast<size_t>(R);
+            const struct { const void *p; size_t bytes; } need[] = {
+                {d->d_q, Rs * static_cast<size_t>(d->num_q_heads) * c->head_dim * elem},
+                {d->d_seed, Rs * 8}, {d->d_step, Rs * 8}, {d->d_eos_allowed, Rs},
+                {d->d_draft_probs, B * K * static_cast<size_t>(d->V) * 4}, {d->d_draft_tokens, B * K * 4},
+                {d->d_vseed, B * 8}, {d->d_vstep, B * 8}};
+            bool fits = true;
+            for (const auto &r : need) {
+                if (!r.p) continue;
+                const uint8_t *q = static_cast<const uint8_t *>(r.p);
+                if (q < base || q >= base + d->input_bytes) continue;  // a device buffer of its own
+                const size_t off = static_cast<size_t>(q - base), bytes = (r.bytes + 3) & ~size_t(3);
+                if ((off & 15u) != 0 || bytes > d->input_bytes - off || trimmed.n == kMaxSegs) {
+                    fits = false;
+                    break;
+                }
+                trimmed.off[trimmed.n] = off;
+                trimmed.bytes[trimmed.n] = bytes;
+                ++trimmed.n;
+            }
+            if (fits && trimmed.n > 0) copy_segs = &trimmed;
+        }
+    }
     const int sms = sm_count() > 0 ? sm_count() : 148;
     size_t words = d->input_bytes / 16;
-    if (segs) {
+    if (copy_segs) {
         words = 0;
-        for (int i = 0; i < segs->n; ++i) words += segs->bytes[i] / 16;
+        for (int i = 0; i < copy_segs->n; ++i) words += (copy_segs->bytes[i] + 15) / 16;
     }
     const size_t want = (words + kCopyThreads - 1) / kCopyThreads;
     const unsigned copy_ctas = static_cast<unsigned>(want < static_cast<size_t>(sms) * 4 ? (want > 0 ? want : 1)
@@ -260,9 +312,9 @@ int capture_step(const tts_step_graph_desc *d, const CopySegs *segs, cudaGraph_t
     cudaGraph_t graph = nullptr;
     bool ok = cudaStreamBeginCapture(s, cudaStreamCaptureModeRelaxed) == cudaSuccess;
     if (ok) {
-        if (segs)
+        if (copy_segs)
             copy_segments_from_host_kernel<<<copy_ctas, kCopyThreads, 0, s>>>(
-                static_cast<uint8_t *>(d->d_inputs), static_cast<const uint8_t *>(d->h_inputs), *segs);
+                static_cast<uint8_t *>(d->d_inputs), static_cast<const uint8_t *>(d->h_inputs), *copy_segs);
         else
             copy_from_host_kernel<<<copy_ctas, kCopyThreads, 0, s>>>(static_cast<uint4 *>(d->d_inputs),
                                                                      static_cast<const uint4 *>(d->h_inputs), words);
