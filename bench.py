@@ -960,10 +960,12 @@ def run_native(args):
         "e2e_by_active_streams": e2e_sizes,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": n_e2e, "note": "wall clock; tts_step_graph (one CUDA graph captured by the "
-                                        "library): a copy kernel reads the step's packed inputs from "
-                                        "pinned host memory, the step runs, the ids and a boundary-token "
-                                        "count are written to pinned host memory; the host launches and "
-                                        "synchronises every step"},
+                                        "library): every input of the step crosses from pinned host "
+                                        "memory each step (the append and the attention's tile map read "
+                                        "theirs there directly, a copy kernel moves the query rows to the "
+                                        "device), the step runs, the ids and a boundary-token count are "
+                                        "written to pinned host memory; the host calls tts_step_graph_run "
+                                        "(launch, then wait for the ids) every step"},
     }
     if world == 1:
         g_out = wl.to_f32(gpu_out.view(torch.int16).numpy().view(np.uint16), w.dtype) if w.dtype == "bf16" \
