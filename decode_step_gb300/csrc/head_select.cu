@@ -35,10 +35,19 @@ constexpr int kTileM = 128;           // vocab rows per MMA tile
 constexpr int kTileK = 64;            // hidden elements per stage (one 128-byte swizzle span)
 constexpr int kStagesTC = 4;
 // Warps 0-3 read the accumulator, 4 is the TMA producer, 5 the MMA issuer;
-// all twelve share the token-selection loop, whose Gumbel path (one
+// all of them share the token-selection loop, whose Gumbel path (one
 // Philox4x64-10 block per 8 vocabulary entries) is bound by the latency of its
-// 64-bit multiply chains and wants many warps.
+// 64-bit multiply chains and wants many warps: the Gumbel build runs 768
+// threads (1024 for 256-column chunks, whose items then split evenly over
+// the passes), at one CTA per SM (measured at 256 x 2048 x 16385: 41.0 us
+// with 384 threads, 35.8 with 768, 34.0 with 1024; at 320 x 2048 x 4097 in
+// 160-column chunks: 20.1, 17.7, 19.0).
 constexpr int kThreadsTC = 384;
+constexpr int kThreadsGumbel = 768;
+constexpr int kThreadsGumbelWide = 1024;
+__host__ __device__ constexpr int tc_threads(bool gumbel, int N) {
+    return !gumbel ? kThreadsTC : (N >= 256 ? kThreadsGumbelWide : kThreadsGumbel);
+}
 constexpr int kMaxN = 256;            // widest MMA N
 constexpr int kATileBytes = kTileM * kTileK * 2;  // 16 KB
 
@@ -354,8 +363,8 @@ __device__ __forceinline__ void st_async_u64(uint32_t dst_cluster, unsigned long
 // runs long enough to pay for its larger code; the narrow build's epilogue
 // runs once per CTA, where every instruction line is fetched cold.  Kept
 // apart so each epilogue is compiled without the others' code.
-template <bool kFeatures, bool kWide>
-__global__ void __launch_bounds__(kThreadsTC, 2)
+template <bool kFeatures, bool kWide, int kThreads>
+__global__ void __launch_bounds__(kThreads, kThreads > kThreadsTC ? 1 : 2)
 head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_h,
                const HeadArgs a, int N, int CK, int alloc_cols) {
     extern __shared__ uint8_t smem_raw[];
@@ -1110,7 +1119,7 @@ struct TcPlan {
     uint32_t smem;
 };
 
-TcPlan plan_tc(int R, int H, int V) {
+TcPlan plan_tc(int R, int H, int V, bool gumbel) {
     TcPlan p;
     p.chunks = (R + kMaxN - 1) / kMaxN;
     const int per = (R + p.chunks - 1) / p.chunks;
@@ -1134,7 +1143,9 @@ TcPlan plan_tc(int R, int H, int V) {
         const uint32_t smem = tc_layout(p.N, ck).total;
         int per_sm = static_cast<int>((227u * 1024u) / (smem + 1024u));
         per_sm = per_sm < tmem_fit ? per_sm : tmem_fit;
-        per_sm = per_sm < 2 ? per_sm : 2;  // registers: the kernel is built for two CTAs per SM
+        // registers: the kernel is built for two CTAs per SM, one with more threads
+        const int reg_fit = tc_threads(gumbel, p.N) > kThreadsTC ? 1 : 2;
+        per_sm = per_sm < reg_fit ? per_sm : reg_fit;
         if (per_sm < 1 || static_cast<long>(vtiles) * p.chunks * ck > static_cast<long>(sms) * per_sm) break;
         p.CK = ck;
         p.smem = smem;
@@ -1317,7 +1328,7 @@ int prepare_head_ex(const void *d_h, const void *d_W, int32_t dtype, int32_t R, 
             return TTS_ERR_CUDA;
         return TTS_OK;
     }
-    st->p = plan_tc(R, H, V);
+    st->p = plan_tc(R, H, V, mode == TTS_GUMBEL);
     if (!cached_tma_2d_bf16(&st->mw, d_W, static_cast<uint64_t>(V), static_cast<uint64_t>(H), kTileM, kTileK) ||
         !cached_tma_2d_bf16(&st->mh, d_h, static_cast<uint64_t>(R), static_cast<uint64_t>(H),
                             static_cast<uint32_t>(st->p.N), kTileK))
@@ -1366,13 +1377,17 @@ int launch_head(const HeadLaunch &L, LaunchOpts o) {
         const TcPlan &p = st->p;
         const bool features = st->a.mode == kModeExpand || st->a.mode == kModeLinear;
         const bool wide = !features && st->a.mode == TTS_ARGMAX && p.N >= 128;
-        const auto kernel = features ? head_tc_kernel<true, false>
-                                     : (wide ? head_tc_kernel<false, true> : head_tc_kernel<false, false>);
+        const int threads = tc_threads(!features && st->a.mode == TTS_GUMBEL, p.N);
+        const auto kernel = features                          ? head_tc_kernel<true, false, kThreadsTC>
+                            : wide                            ? head_tc_kernel<false, true, kThreadsTC>
+                            : threads == kThreadsGumbelWide   ? head_tc_kernel<false, false, kThreadsGumbelWide>
+                            : threads == kThreadsGumbel       ? head_tc_kernel<false, false, kThreadsGumbel>
+                                                              : head_tc_kernel<false, false, kThreadsTC>;
         if (!ensure_dynamic_smem(reinterpret_cast<const void *>(kernel), static_cast<int>(p.smem)))
             return TTS_ERR_CUDA;
         cfg.gridDim = dim3(static_cast<unsigned>(((st->a.V + kTileM - 1) / kTileM) * p.CK),
                            static_cast<unsigned>(p.chunks), 1);
-        cfg.blockDim = dim3(kThreadsTC, 1, 1);
+        cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
         cfg.dynamicSmemBytes = p.smem;
         attr[na].id = cudaLaunchAttributeClusterDimension;
         attr[na].val.clusterDim.x = static_cast<unsigned>(p.CK);
