@@ -157,6 +157,10 @@ def test_step_graph_rejects_bad_descriptors(L):
     desc = _lib.StepGraphDesc()  # all null
     assert L.tts_step_graph_create(ctypes.byref(desc), ctypes.byref(handle)) == -1
     assert L.tts_step_graph_launch(None, None) == -1
+    assert L.tts_step_graph_run(None, None) == -1
+    chosen = ctypes.c_int32(-7)
+    assert L.tts_step_graph_set_run(None, 4, ctypes.byref(chosen), None) == -1
+    assert chosen.value == -7                         # nothing chosen for a missing set
     L.tts_step_graph_destroy(None)
 
 
