@@ -208,9 +208,10 @@ __host__ __device__ inline StagedLayout staged_layout(int K, int V, int flags) {
 }
 
 // Warp roles of the staged kernel while the rows land.
-constexpr int kRaggedWarp = kStagedWarps - 1;   // the rows' unaligned ends by plain loads
-constexpr int kAcceptWarp = kStagedWarps - 2;   // the accept test's inputs
-constexpr int kNoiseThreads = 32 * (kStagedWarps - 2);
+constexpr int kRaggedWarp = kStagedWarps - 1;    // the rows' unaligned ends by plain loads
+constexpr int kAcceptWarp = kStagedWarps - 2;    // the accept test's inputs
+constexpr int kDrawWarmWarp = kStagedWarps - 3;  // the draw's warm-up
+constexpr int kNoiseThreads = 32 * (kStagedWarps - 3);
 
 // The staged kernel's per-stream scalars in shared memory.
 struct VerifyScalars {
@@ -224,9 +225,16 @@ struct VerifyScalars {
 };
 
 // The three phases after the rows land are out-of-line functions: while the
-// rows are in flight, two idle warps run each of them once on scratch data so
-// that their instructions are already on the SM when the CTA needs them (each
-// runs once per CTA, so every instruction would otherwise be fetched cold).
+// rows are in flight, three warps each run one of them once on scratch data,
+// first thing, so that their instructions are already on the SM when the CTA
+// needs them (each runs once per CTA, so every instruction would otherwise be
+// fetched cold).
+
+// Elements a thread loads before it uses the first of them in the row
+// statistics and the draw: independent shared-memory loads and exponentials
+// in flight instead of one load's latency per element.
+constexpr int kRowUnroll = 8;
+constexpr int kDrawUnroll = 4;
 
 // One warp's part of a row's statistics: the max m of x[v] over
 // v = v0 + lane, v0 + lane + stride, ... and the sum of 2^((x[v] - m) k2)
@@ -234,12 +242,33 @@ struct VerifyScalars {
 __device__ __noinline__ void warp_row_part(const float *x, int V, int v0, int stride, float k2, float *m_out,
                                            float *s_out) {
     const int lane = threadIdx.x & 31;
+    const int first = v0 + lane, span = kRowUnroll * stride;
     float m = -INFINITY, s = 0.0f;
-    for (int v = v0 + lane; v < V; v += stride) m = fmaxf(m, x[v]);
+    int v = first;
+    for (; v + (kRowUnroll - 1) * stride < V; v += span) {
+        float xv[kRowUnroll];
+#pragma unroll
+        for (int j = 0; j < kRowUnroll; ++j) xv[j] = x[v + j * stride];
+#pragma unroll
+        for (int j = 0; j < kRowUnroll; ++j) m = fmaxf(m, xv[j]);
+    }
+    for (; v < V; v += stride) m = fmaxf(m, x[v]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-    if (m != -INFINITY)
-        for (int v = v0 + lane; v < V; v += stride) s += hw_ex2((x[v] - m) * k2);
+    if (m != -INFINITY) {
+        v = first;
+        for (; v + (kRowUnroll - 1) * stride < V; v += span) {
+            float e[kRowUnroll];
+#pragma unroll
+            for (int j = 0; j < kRowUnroll; ++j) e[j] = hw_ex2((x[v + j * stride] - m) * k2);
+#pragma unroll
+            for (int w = kRowUnroll / 2; w > 0; w >>= 1)
+#pragma unroll
+                for (int j = 0; j < w; ++j) e[j] += e[j + w];
+            s += e[0];
+        }
+        for (; v < V; v += stride) s += hw_ex2((x[v] - m) * k2);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
     if (lane == 0) {
@@ -288,24 +317,54 @@ __device__ __noinline__ void accept_walk(VerifyScalars *S, const float *st, int 
     }
 }
 
+// One entry of the residual draw: folds its key log(residual) + g into
+// `best` when the residual max(2^((x - m) k2) iz - p_d, 0) is positive.
+__device__ __forceinline__ void draw_residual(float xv, float pv, float g, int v, float m, float iz, float k2,
+                                              unsigned long long &best) {
+    constexpr float kLn2 = 0.69314718055994531f;
+    const float r = fmaxf(hw_ex2((xv - m) * k2) * iz - pv, 0.0f);
+    if (r > 0.0f) {
+        const unsigned long long k = pack_argmax(kLn2 * hw_lg2(r) + g, v);
+        best = k > best ? k : best;
+    }
+}
 // One thread's part of the draw over row x, entries v = v0, v0 + stride, ...:
 // the largest packed (key, index) of log(residual) + G over entries with a
-// positive residual max(2^((x - m) k2) iz - p_d, 0) when pdr (the rejected
-// row's draft probabilities) is given, else of x / T + G (0 if none).
+// positive residual when pdr (the rejected row's draft probabilities) is
+// given, else of x / T + G (0 if none).
 __device__ __noinline__ unsigned long long draw_part(const float *x, const float *pdr, const float *G, int V, int v0,
                                                      int stride, float m, float iz, float inv_t, float k2) {
-    constexpr float kLn2 = 0.69314718055994531f;
     unsigned long long best = 0ull;
+    const int span = kDrawUnroll * stride;
+    int v = v0;
     if (pdr) {
-        for (int v = v0; v < V; v += stride) {
-            const float r = fmaxf(hw_ex2((x[v] - m) * k2) * iz - pdr[v], 0.0f);
-            if (r > 0.0f) {
-                const unsigned long long k = pack_argmax(kLn2 * hw_lg2(r) + G[v], v);
+        for (; v + (kDrawUnroll - 1) * stride < V; v += span) {
+            float xv[kDrawUnroll], pv[kDrawUnroll], gv[kDrawUnroll];
+#pragma unroll
+            for (int j = 0; j < kDrawUnroll; ++j) {
+                xv[j] = x[v + j * stride];
+                pv[j] = pdr[v + j * stride];
+                gv[j] = G[v + j * stride];
+            }
+#pragma unroll
+            for (int j = 0; j < kDrawUnroll; ++j) draw_residual(xv[j], pv[j], gv[j], v + j * stride, m, iz, k2, best);
+        }
+        for (; v < V; v += stride) draw_residual(x[v], pdr[v], G[v], v, m, iz, k2, best);
+    } else {
+        for (; v + (kDrawUnroll - 1) * stride < V; v += span) {
+            float xv[kDrawUnroll], gv[kDrawUnroll];
+#pragma unroll
+            for (int j = 0; j < kDrawUnroll; ++j) {
+                xv[j] = x[v + j * stride];
+                gv[j] = G[v + j * stride];
+            }
+#pragma unroll
+            for (int j = 0; j < kDrawUnroll; ++j) {
+                const unsigned long long k = pack_argmax(xv[j] * inv_t + gv[j], v + j * stride);
                 best = k > best ? k : best;
             }
         }
-    } else {
-        for (int v = v0; v < V; v += stride) {
+        for (; v < V; v += stride) {
             const unsigned long long k = pack_argmax(x[v] * inv_t + G[v], v);
             best = k > best ? k : best;
         }
@@ -376,41 +435,63 @@ spec_verify_staged_kernel(const float *__restrict__ tl, const float *__restrict_
     const float inv_t = 1.0f / T, k2 = 1.4426950408889634f / T;
     const int wpr = K >= kStagedWarps ? 1 : kStagedWarps / K;
 
-    // ---- while the rows land (the warm-up runs read scratch or in-flight
-    // shared memory and write only `scratch`)
+    // ---- while the rows land.  Three warps each run one of the later
+    // phases once on scratch data first (reading scratch or in-flight shared
+    // memory, writing only `scratch`), so that the three fetch their
+    // instructions in parallel and early; their own global loads are issued
+    // before the warm-up and used after it.
     if (warp == kRaggedWarp) {
+        // the rows' unaligned ends: at most one head and one tail float per
+        // lane and image (all of a row image below 16 bytes: plain copies)
+        float *dst_h[2], *dst_t[2];
+        float val_h[2], val_t[2];
+#pragma unroll
         for (int part = 0; part < 2; ++part) {
             float *dst = part ? sdr : st;
             const float *g = part ? dp_b : tl_b;
             const size_t n = part ? nd : nt;
             const uintptr_t s0 = reinterpret_cast<uintptr_t>(g), s1 = s0 + n * 4;
             const uintptr_t a0 = (s0 + 15) & ~uintptr_t(15), a1 = s1 & ~uintptr_t(15);
+            dst_h[part] = dst_t[part] = nullptr;
+            val_h[part] = val_t[part] = 0.0f;
             if (a1 <= a0) {
                 for (size_t i = lane; i < n; i += 32) dst[i] = __ldg(g + i);
             } else {
                 const size_t head = (a0 - s0) / 4, tail_from = (a1 - s0) / 4;
-                if (static_cast<size_t>(lane) < head) dst[lane] = __ldg(g + lane);
-                if (tail_from + lane < n) dst[tail_from + lane] = __ldg(g + tail_from + lane);
+                if (static_cast<size_t>(lane) < head) {
+                    dst_h[part] = dst + lane;
+                    val_h[part] = __ldg(g + lane);
+                }
+                if (tail_from + lane < n) {
+                    dst_t[part] = dst + tail_from + lane;
+                    val_t[part] = __ldg(g + tail_from + lane);
+                }
             }
         }
-        const int vw = V < 64 ? V : 64;
-        warp_row_part(G, vw, 0, 32, k2, &scratch.warm_m, &scratch.warm_s);
-        const unsigned long long wr = draw_part(G, G, G, vw, lane, 32, 0.0f, 1.0f, inv_t, k2);
-        const unsigned long long wp = draw_part(G, nullptr, G, vw, lane, 32, 0.0f, 1.0f, inv_t, k2);
-        if (lane == 0) scratch.best = wr ^ wp;
-    } else if (warp == kAcceptWarp) {
-        if (lane < K) {
-            const int d = dt[static_cast<size_t>(b) * K + lane];
-            S.acc_d[lane] = d;
-            S.acc_pd[lane] = (d >= 0 && d < V) ? __ldg(dp_b + static_cast<size_t>(lane) * V + d) : 0.0f;
-            S.acc_u[lane] = philox_uniform(key0, key1, 1u, 0u, static_cast<uint32_t>(lane));
+        warp_row_part(G, V < 256 ? V : 256, 0, 32, k2, &scratch.warm_m, &scratch.warm_s);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+            if (dst_h[part]) *dst_h[part] = val_h[part];
+            if (dst_t[part]) *dst_t[part] = val_t[part];
         }
+    } else if (warp == kAcceptWarp) {
+        const int d = lane < K ? dt[static_cast<size_t>(b) * K + lane] : 0;
         if (lane < kMaxK) scratch.acc_d[lane] = 0;
         scratch.red_m[lane] = 0.0f;
         scratch.red_s[lane] = 1.0f;
         __syncwarp();
         // a one-entry "row" per lane inside scratch (V = 1, every token 0)
         accept_walk(&scratch, scratch.red_s, K, 1, wpr, k2, flags, nullptr);
+        if (lane < K) {
+            S.acc_d[lane] = d;
+            S.acc_pd[lane] = (d >= 0 && d < V) ? __ldg(dp_b + static_cast<size_t>(lane) * V + d) : 0.0f;
+            S.acc_u[lane] = philox_uniform(key0, key1, 1u, 0u, static_cast<uint32_t>(lane));
+        }
+    } else if (warp == kDrawWarmWarp) {
+        const int vw = V < 256 ? V : 256;  // long enough to run the unrolled loops
+        const unsigned long long wr = draw_part(G, G, G, vw, lane, 32, 0.0f, 1.0f, inv_t, k2);
+        const unsigned long long wp = draw_part(G, nullptr, G, vw, lane, 32, 0.0f, 1.0f, inv_t, k2);
+        if (lane == 0) scratch.best = wr ^ wp;
     } else {
         for (int gi = threadIdx.x; gi < groups; gi += kNoiseThreads) {
             const Philox4x64 ph(static_cast<uint64_t>(gi), 2u, 0u, 0u, key0, key1);
