@@ -182,9 +182,11 @@ def tts_decode_attn(cache: KVCache, block_table, ctx_lens, max_ctx_len, q, out, 
 
 def tts_decode_attn_noalloc(cache: KVCache, block_table, ctx_lens, max_ctx_len, q, out, scale,
                             causal=False, err=None, stream=None):
-    """tts_decode_attn without a workspace: for callers that cannot allocate
-    device memory (graph capture, fully reserved memory); uses the library's
-    24 MiB static scratch, shared by all calls."""
+    """tts_decode_attn without a workspace, for callers that cannot allocate
+    device memory where they run a step (all free memory given to the KV
+    pool, a host without an allocator, a frame budget that cannot absorb
+    cudaMalloc's synchronisation); uses the library's 16 MiB static scratch,
+    shared by all calls."""
     B, max_blocks = block_table.shape
     _, q_len, Hq, D = q.shape
     args = (ctypes.byref(cache.desc), _dev(block_table, "block_table", torch.int32), max_blocks,

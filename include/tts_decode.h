@@ -224,7 +224,7 @@ int tts_decode_attn(const tts_kv_cache *cache, const int32_t *d_block_table,
  * TTS_ERR_SCRATCH_LIMIT and launches nothing.  The first call in a CUDA
  * context (per device, and again after that context is replaced, e.g. by
  * cudaDeviceReset) looks up the array's device address with
- * cudaGetSymbolAddress; make that first call before any stream capture.
+ * cudaGetSymbolAddress; later calls in that context reuse the address.
  * Arguments are validated before anything is queued, so a rejected call
  * leaves the array untouched.  Every call shares the one array and it keeps
  * the previous call's contents: each call clears the part that must start at
